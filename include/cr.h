@@ -1,0 +1,199 @@
+/*
+ * cr.h -- C ABI of the GB300 conditional-simulation library (libcr.so).
+ *
+ * The library computes the hot path of "Mixed-Precision GPU Acceleration for Confidence
+ * Regions of Spatial Excursion Sets" (Zhang, Abdulah, Cao, French, Alomairy, Genton,
+ * Keyes): a dense covariance over n locations, a tile Cholesky factor with per-tile
+ * FP64/FP32/FP16 precision chosen from a tolerance, the mixed-precision triangular
+ * multiply that turns standard-normal draws into correlated fields, the universal-kriging
+ * correction, per-location exceedance counts and the calibration of the inner and outer
+ * confidence regions.  One process drives one GPU; nothing here is distributed.
+ *
+ * Conventions (all entry points):
+ *  - Every call returns a cr_status; CR_OK = 0.  No exception or abort crosses the ABI.
+ *    cr_status_str() names a code, cr_last_error_detail() gives the calling thread's last
+ *    message.
+ *  - Pointers named d_* are device pointers (allocated and owned by the caller, e.g. by
+ *    PyTorch); h_* are host pointers owned by the caller.  The library owns only the
+ *    storage behind an opaque cr_tilemat handle (cr_tilemat_create / cr_tilemat_destroy).
+ *  - Matrices passed as pointers are column-major with an explicit leading dimension
+ *    (LAPACK style) unless stated otherwise.  Sizes are element counts.
+ *  - Device work is enqueued on the given stream and is asynchronous, except where a
+ *    call returns host values; those calls synchronise the stream and say so.
+ *  - Sizes out of range, NULL where a pointer is required, or calls in the wrong order
+ *    return CR_ERR_ARG or CR_ERR_STATE without touching the GPU.
+ */
+#ifndef CR_H
+#define CR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* cr_stream;
+
+typedef int cr_status;
+enum {
+  CR_OK = 0,
+  CR_ERR_ARG = 1,             /* invalid argument */
+  CR_ERR_CUDA = 2,            /* a CUDA runtime/driver call failed */
+  CR_ERR_NOMEM = 3,           /* device allocation inside a tile matrix failed */
+  CR_ERR_NOT_SPD = 4,         /* a Cholesky pivot was not positive (see info) */
+  CR_ERR_EMPTY_SAMPLE = 5,    /* every simulation left the psi or phi set empty */
+  CR_ERR_NONPOS_MSPE = 6,     /* a pointwise MSPE v_i <= 0 */
+  CR_ERR_TIMEOUT = 7,         /* a bounded device-side wait gave up */
+  CR_ERR_STATE = 8,           /* call made in the wrong order */
+  CR_ERR_NOT_IMPLEMENTED = 9,
+  CR_ERR_RANGE = 10           /* scaled factor not representable in FP16 */
+};
+
+/* Tile precision classes. */
+enum { CR_PREC_FP64 = 0, CR_PREC_FP32 = 1, CR_PREC_FP16 = 2 };
+
+/* Covariance families.
+ *  CR_COV_MATERN: C(h) = sigma2 2^(1-nu)/Gamma(nu) (h/range)^nu K_nu(h/range), C(0) = sigma2
+ *                 (the page's Matern model, Section VI-C; parameterisation as stated here).
+ *  CR_COV_POWEXP: C(h) = sigma2 exp(-(h/range)^nu) (Section VI-B.2). */
+enum { CR_COV_MATERN = 0, CR_COV_POWEXP = 1 };
+
+typedef struct {
+  int family;       /* CR_COV_MATERN or CR_COV_POWEXP */
+  double sigma2;    /* marginal variance (theta0) */
+  double range;     /* beta > 0 */
+  double nu;        /* smoothness > 0 */
+  double nugget;    /* added to every diagonal entry (>= 0) */
+  int n_pred;       /* rows [0, n_pred) are prediction sites, [n_pred, n) observations */
+  double tau2;      /* measurement-error variance, observation diagonal only (Eq.4) */
+} cr_cov_params;
+
+/* Result of the precision policy (Section V-D, V-E). */
+typedef struct {
+  double fixedacc;  /* tolerance used for the final map */
+  int iters;        /* maps computed (automatic refinement, Section V-D) */
+  int n_fp64, n_fp32, n_fp16;   /* lower tiles per class */
+  double R_hp;      /* Eq.10 ratio v_max^HP / v_min^HP (NaN without FP16 tiles) */
+  double rho1, rho2;/* Eq.11 ratios */
+  int check1, check2;           /* Eq.10 / Eq.11 passed */
+  double ell, u_s;  /* Eq.12 bounds */
+  double s;         /* applied integer scale (1 = unscaled) */
+  int range_ok;     /* ell <= u_s */
+} cr_pmap_info;
+
+typedef struct {
+  double q_in, q_out;   /* critical values (Section V-C) */
+  int n_psi, n_phi;     /* sample sizes after dropping empty-set sentinels */
+} cr_calib_info;
+
+typedef struct cr_tilemat_s* cr_tilemat;
+
+/* ---------------------------------------------------------------- housekeeping */
+const char* cr_status_str(cr_status code);
+const char* cr_last_error_detail(void);
+cr_status cr_version(int* major, int* minor);
+
+/* A symmetric n x n matrix stored as its lower tiles (i >= j) of nb x nb entries.
+ * NT = ceil(n / nb) tile rows; rows and columns past n are padding and behave like the
+ * identity.  nb must be a multiple of 128 with 128 <= nb <= 1024.  The handle owns its
+ * device storage (allocated on the current device); destroy frees it. */
+cr_status cr_tilemat_create(int n, int nb, cr_tilemat* out);
+cr_status cr_tilemat_destroy(cr_tilemat V);
+cr_status cr_tilemat_info(cr_tilemat V, int* n, int* nb, int* nt);
+
+/* Joint covariance (Section V Eq.4) of the n locations d_xy (n x 2, row-major pairs
+ * (x_i, y_i), device, FP64), prediction sites first.  Fills the FP64 lower tiles and the
+ * per-tile statistics (Frobenius norm, min and max entry over valid entries, Section
+ * V-D).  Asynchronous. */
+cr_status cr_cov_build(cr_tilemat V, const double* d_xy, const cr_cov_params* p, cr_stream stream);
+
+/* Per-tile statistics as NT x NT row-major host arrays (lower part filled).
+ * Synchronises the stream used by cr_cov_build. */
+cr_status cr_tile_stats(cr_tilemat V, double* h_frob, double* h_vmin, double* h_vmax);
+
+/* Tile precision map, FP16 screening checks and covariance scale (Section V-D/E, Alg.2
+ * steps 7-10).  amp = 0 keeps every tile FP64 with s = 1.  With auto_mode != 0 the
+ * tolerance starts at 1e-4 and shrinks by 0.9 until both checks pass or no FP16 tile is
+ * left; otherwise fixedacc is used as given and failed checks are only reported.
+ * h_map (NT x NT int8 row-major, lower part written, may be NULL) receives CR_PREC_*.
+ * Allocates the per-precision tile storage.  Synchronises. */
+cr_status cr_precision_map(cr_tilemat V, int amp, double fixedacc, int auto_mode,
+                           int8_t* h_map, cr_pmap_info* info);
+
+/* Adaptive mixed-precision Cholesky (Section IV-B, Alg.2 step 12): scales the tiles by
+ * s^2, rounds each to its class, and factors in place, V <- L_s = chol(s^2 V).  FP64
+ * tiles run on the FP64 units; FP32/FP16 products on the tensor cores with FP32
+ * accumulation.  *info = 0 on success, else the 1-based global column of the first
+ * non-positive pivot (LAPACK convention) and CR_ERR_NOT_SPD.  Synchronises. */
+cr_status cr_potrf_adaptive(cr_tilemat V, cr_stream stream, int* info);
+
+/* Copies the tile matrix into a dense n x n column-major FP64 matrix (lower triangle;
+ * the strict upper triangle is set to zero).  what = 0: the covariance V built by
+ * cr_cov_build; what = 1: the current working tiles as stored in their precision
+ * (after cr_potrf_adaptive: the factor L_s).  Asynchronous. */
+cr_status cr_tilemat_to_dense(cr_tilemat V, int what, double* d_out, int ld, cr_stream stream);
+
+/* n x M standard normals (column-major, ldz >= n) from the library's counter-based
+ * stream: SplitMix64 on seed + (c+1)*0x9E3779B97F4A7C15, 53-bit uniforms, Box-Muller in
+ * FP64; element (i, j) uses pair floor((offset + j n + i) / 2) (Section V-B, Desc_rnorm).
+ * Asynchronous. */
+cr_status cr_rnorm(double* d_Z, int ldz, int n, int M, uint64_t seed, uint64_t offset,
+                   cr_stream stream);
+
+/* Flags of cr_trmm_sim. */
+enum {
+  CR_TRMM_FP16_DEST = 1,   /* round each output to FP16 before widening (Alg.1 FP16 destination) */
+  CR_TRMM_GENERATE = 2     /* ignore d_Z; draw M_rand from (seed, offset) in FP32 and round */
+};
+
+/* Mixed-precision TRMM (Section IV-C Eq.3, Alg.1): Y = L_s B with B = fp16(M_rand / s)
+ * when the factor was built with amp != 0, else Y = L M_rand in FP64.  d_Z is the n x M
+ * column-major FP64 M_rand (ldz >= n), d_Y the n x M column-major FP64 output
+ * (ldy >= n).  With CR_TRMM_GENERATE, M_rand is drawn in FP32 from the stream of
+ * cr_rnorm(seed, offset) and d_Z may be NULL.  h_bnorm (may be NULL) receives ||B||_F of
+ * the rescaled right-hand side before rounding (Alg.1 step 6); a non-NULL h_bnorm
+ * synchronises.  Requires a factored matrix. */
+cr_status cr_trmm_sim(cr_tilemat L, const double* d_Z, int ldz, int M, uint64_t seed,
+                      uint64_t offset, double* d_Y, int ldy, int flags, double* h_bnorm,
+                      cr_stream stream);
+
+/* Universal kriging (Section V-A Eq.5-6, Alg.2 steps 2-6) from the FP64 covariance held
+ * by V (built with n_pred prediction sites first, n_pred a multiple of nb): Sigma_y is
+ * the observation block, V_op the n_o x n_p observation/prediction block.  d_Xo (n_o x 3)
+ * and d_Xp (n_p x 3) are column-major trend designs, d_yo the n_o observations.
+ * Outputs: d_W (n_o x n_p column-major, ldw >= n_o) weights, d_zhat (n_p) prediction,
+ * d_v (n_p) pointwise MSPE with theta0 = sigma2.  Must be called before
+ * cr_potrf_adaptive overwrites nothing it needs (it reads only cr_cov_build's FP64
+ * tiles, which the factorisation keeps).  *info as in cr_potrf_adaptive for Sigma_y.
+ * Synchronises. */
+cr_status cr_krige(cr_tilemat V, const double* d_Xo, const double* d_Xp, const double* d_yo,
+                   double* d_W, int ldw, double* d_zhat, double* d_v, cr_stream stream,
+                   int* info);
+
+/* Conditioning correction (Section V-B Eq.7): S = M_p + W^T (y_o 1^T - M_o), where the
+ * simulations d_Y (n x M column-major, ldy) hold the prediction rows first (M_p = rows
+ * [0, n_p), M_o = rows [n_p, n_p + n_o)).  d_S is n_p x M column-major (lds >= n_p).
+ * FP64.  Asynchronous. */
+cr_status cr_krige_correct(const double* d_W, int ldw, const double* d_yo, const double* d_Y,
+                           int ldy, int n_p, int n_o, int M, double* d_S, int lds,
+                           cr_stream stream);
+
+/* Calibration (Section V-C Eq.8-9, Alg.2 steps 18-22): t = (zhat - u)/sqrt(v);
+ * psi_j = min{t_i : S_ij >= u}, phi_j = max{t_i : S_ij <= u} in one pass over d_S
+ * (n_p x M column-major, lds >= n_p); per-location exceedance counts
+ * count_i = #{j : S_ij >= u}; empirical quantiles q_out = Q_{1-level}(psi),
+ * q_in = Q_level(phi) on the samples without empty-set sentinels; regions
+ * d_cin[i] = t_i > q_in, d_cout[i] = t_i >= q_out (uint8).  d_count, d_psi, d_phi may
+ * be NULL.  Returns CR_ERR_NONPOS_MSPE if some v_i <= 0 and CR_ERR_EMPTY_SAMPLE if a
+ * sample is empty.  Synchronises. */
+cr_status cr_calibrate(const double* d_S, int lds, int n_p, int M, const double* d_zhat,
+                       const double* d_v, double u, double level, uint8_t* d_cin,
+                       uint8_t* d_cout, int32_t* d_count, double* d_psi, double* d_phi,
+                       cr_calib_info* out, cr_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CR_H */

@@ -1,0 +1,159 @@
+// Status codes, error reporting, tile-matrix lifetime and TMA descriptor creation.
+#include <stdio.h>
+
+#include <mutex>
+
+#include "common.cuh"
+
+namespace cr {
+
+static thread_local std::string g_detail;
+
+void set_error(const std::string& msg) { g_detail = msg; }
+
+cr_status fail(cr_status code, const std::string& msg) {
+  g_detail = msg;
+  return code;
+}
+
+cr_status cuda_fail(cudaError_t e, const char* what) {
+  g_detail = std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
+  return e == cudaErrorMemoryAllocation ? CR_ERR_NOMEM : CR_ERR_CUDA;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point, so the library does not
+// link libcuda directly and loads on machines without a driver.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+cr_status make_tensor_map_3d_f16(CUtensorMap* tm, void* base, int inner, int rows, int slots, int box_inner,
+                                 int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(CR_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)rows, (cuuint64_t)slots};
+  cuuint64_t strides[2] = {(cuuint64_t)inner * 2, (cuuint64_t)inner * rows * 2};
+  cuuint32_t box[3] = {(cuuint32_t)box_inner, (cuuint32_t)box_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(CR_ERR_CUDA, "cuTensorMapEncodeTiled (3d) failed: " + std::to_string((int)r));
+  return CR_OK;
+}
+
+cr_status make_tensor_map_2d_f16(CUtensorMap* tm, void* base, int inner, int outer, int ld, int box_inner,
+                                 int box_outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(CR_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(CR_ERR_CUDA, "cuTensorMapEncodeTiled (2d) failed: " + std::to_string((int)r));
+  return CR_OK;
+}
+
+template <class T>
+static void dfree(T*& p) {
+  if (p) cudaFree((void*)p);
+  p = nullptr;
+}
+
+cr_status free_class_storage(cr_tilemat V) {
+  dfree(V->d_cls); dfree(V->d_i64); dfree(V->d_i32); dfree(V->d_hi16); dfree(V->d_lo16);
+  dfree(V->pool64); dfree(V->pool32); dfree(V->pool16); dfree(V->ws64);
+  V->mapped = false;
+  V->factored = false;
+  return CR_OK;
+}
+
+}  // namespace cr
+
+using namespace cr;
+
+extern "C" const char* cr_status_str(cr_status code) {
+  switch (code) {
+    case CR_OK: return "CR_OK";
+    case CR_ERR_ARG: return "CR_ERR_ARG";
+    case CR_ERR_CUDA: return "CR_ERR_CUDA";
+    case CR_ERR_NOMEM: return "CR_ERR_NOMEM";
+    case CR_ERR_NOT_SPD: return "CR_ERR_NOT_SPD";
+    case CR_ERR_EMPTY_SAMPLE: return "CR_ERR_EMPTY_SAMPLE";
+    case CR_ERR_NONPOS_MSPE: return "CR_ERR_NONPOS_MSPE";
+    case CR_ERR_TIMEOUT: return "CR_ERR_TIMEOUT";
+    case CR_ERR_STATE: return "CR_ERR_STATE";
+    case CR_ERR_NOT_IMPLEMENTED: return "CR_ERR_NOT_IMPLEMENTED";
+    case CR_ERR_RANGE: return "CR_ERR_RANGE";
+    default: return "CR_ERR_UNKNOWN";
+  }
+}
+
+extern "C" const char* cr_last_error_detail(void) { return g_detail.c_str(); }
+
+extern "C" cr_status cr_version(int* major, int* minor) {
+  if (major) *major = 0;
+  if (minor) *minor = 1;
+  return CR_OK;
+}
+
+extern "C" cr_status cr_tilemat_create(int n, int nb, cr_tilemat* out) {
+  if (!out) return fail(CR_ERR_ARG, "cr_tilemat_create: NULL out");
+  *out = nullptr;
+  if (n <= 0 || nb < 128 || nb > 1024 || nb % 128 != 0) return fail(CR_ERR_ARG, "cr_tilemat_create: n > 0, nb in {128..1024} step 128");
+  cr_tilemat V = new cr_tilemat_s();
+  V->n = n;
+  V->nb = nb;
+  V->nt = (n + nb - 1) / nb;
+  V->npad = V->nt * nb;
+  V->ntiles = V->nt * (V->nt + 1) / 2;
+  cudaGetDevice(&V->device);
+  const size_t tile = (size_t)nb * nb;
+  cudaError_t e;
+  if ((e = cudaMalloc(&V->master, (size_t)V->ntiles * tile * sizeof(double))) != cudaSuccess ||
+      (e = cudaMalloc(&V->stat_part, (size_t)V->ntiles * (nb / 64) * 3 * sizeof(double))) != cudaSuccess ||
+      (e = cudaMalloc(&V->stats, (size_t)V->ntiles * 3 * sizeof(double))) != cudaSuccess ||
+      (e = cudaMalloc(&V->minv, tile * sizeof(double))) != cudaSuccess ||
+      (e = cudaMalloc(&V->scratch64, tile * sizeof(double))) != cudaSuccess ||
+      (e = cudaMalloc(&V->d_status, 4 * sizeof(int))) != cudaSuccess) {
+    cr_status st = cuda_fail(e, "cr_tilemat_create: cudaMalloc");
+    cr_tilemat_destroy(V);
+    return st;
+  }
+  cudaMemset(V->d_status, 0, 4 * sizeof(int));
+  *out = V;
+  return CR_OK;
+}
+
+extern "C" cr_status cr_tilemat_destroy(cr_tilemat V) {
+  if (!V) return CR_OK;
+  cudaSetDevice(V->device);
+  cudaDeviceSynchronize();
+  free_class_storage(V);
+  dfree(V->b16); dfree(V->bnorm_part);
+  dfree(V->master); dfree(V->stat_part); dfree(V->stats); dfree(V->minv); dfree(V->scratch64); dfree(V->d_status);
+  delete V;
+  return CR_OK;
+}
+
+extern "C" cr_status cr_tilemat_info(cr_tilemat V, int* n, int* nb, int* nt) {
+  if (!V) return fail(CR_ERR_ARG, "cr_tilemat_info: NULL handle");
+  if (n) *n = V->n;
+  if (nb) *nb = V->nb;
+  if (nt) *nt = V->nt;
+  return CR_OK;
+}

@@ -1,0 +1,205 @@
+// Calibration of the inner and outer confidence regions.
+//
+// "Mixed-Precision GPU Acceleration for Confidence Regions of Spatial Excursion Sets":
+//  - Alg.2 step 18 / Eq.1: t = (zhat - u) / sqrt(v), positive MSPEs required.
+//  - Section V-C Eq.8 / Alg.2 step 19 (Desc_col_summary_index_both): psi_j = min{t_i : S_ij >= u},
+//    phi_j = max{t_i : S_ij <= u}, both in one pass over S; sentinels +inf / -inf for empty sets.
+//  - Per-location exceedance counts count_i = #{j : S_ij >= u}, fused into the same pass.
+//  - Section V-C Eq.9: Q_p(a) = a_(max{1, min{N, ceil(p N)}}) on each sorted sample without
+//    sentinels (ceil taken of p N - 1e-9 so a product that is an integer up to rounding stays);
+//    q_out = Q_alpha(psi), q_in = Q_{1-alpha}(phi), alpha = 1 - level.
+//  - Alg.2 step 22: C_in = {t_i > q_in}, C_out = {t_i >= q_out}.
+// The scan streams S once from HBM: each CTA owns a 2048-row x 32-column block, keeps its
+// rows' t and counts in registers, reduces each column with warp shuffles and writes one
+// partial per column; a second kernel combines the partials in a fixed order (deterministic).
+#include <math.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "calib.cuh"
+#include "common.cuh"
+
+namespace cr {
+
+__global__ void k_tstat(const double* __restrict__ zhat, const double* __restrict__ v, double u, int n_p, double* __restrict__ t,
+                        int* __restrict__ bad) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_p; i += gridDim.x * blockDim.x) {
+    const double vi = v[i];
+    if (!(vi > 0.0)) atomicOr(bad, 1);
+    t[i] = (zhat[i] - u) / sqrt(vi);
+  }
+}
+
+__global__ void __launch_bounds__(SCAN_THREADS) k_scan(const double* __restrict__ S, int lds, int n_p, int M,
+                                                       const double* __restrict__ t, double u, double* __restrict__ psi_part,
+                                                       double* __restrict__ phi_part, int32_t* __restrict__ count) {
+  constexpr int RPT = SCAN_ROWS / SCAN_THREADS;   // rows per thread
+  const int rb = blockIdx.x, cbk = blockIdx.y;
+  const int row0 = rb * SCAN_ROWS + threadIdx.x;
+  double tq[RPT];
+  int cnt[RPT];
+#pragma unroll
+  for (int q = 0; q < RPT; ++q) {
+    const int r = row0 + q * SCAN_THREADS;
+    tq[q] = r < n_p ? t[r] : 0.0;
+    cnt[q] = 0;
+  }
+  __shared__ double s_mn[SCAN_THREADS / 32][SCAN_COLS];
+  __shared__ double s_mx[SCAN_THREADS / 32][SCAN_COLS];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c_end = min(SCAN_COLS, M - cbk * SCAN_COLS);
+  for (int c = 0; c < c_end; ++c) {
+    const double* col = S + (size_t)(cbk * SCAN_COLS + c) * lds;
+    double val[RPT];
+#pragma unroll
+    for (int q = 0; q < RPT; ++q) {
+      const int r = row0 + q * SCAN_THREADS;
+      val[q] = r < n_p ? __ldcs(col + r) : NAN;
+    }
+    double mn = INFINITY, mx = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < RPT; ++q) {
+      if (val[q] >= u) { mn = fmin(mn, tq[q]); ++cnt[q]; }
+      if (val[q] <= u) mx = fmax(mx, tq[q]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      mn = fmin(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+      mx = fmax(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    if (lane == 0) { s_mn[warp][c] = mn; s_mx[warp][c] = mx; }
+  }
+  __syncthreads();
+  if (threadIdx.x < c_end) {
+    double mn = INFINITY, mx = -INFINITY;
+    for (int w = 0; w < SCAN_THREADS / 32; ++w) { mn = fmin(mn, s_mn[w][threadIdx.x]); mx = fmax(mx, s_mx[w][threadIdx.x]); }
+    const size_t o = (size_t)rb * M + cbk * SCAN_COLS + threadIdx.x;
+    psi_part[o] = mn;
+    phi_part[o] = mx;
+  }
+  if (count) {
+#pragma unroll
+    for (int q = 0; q < RPT; ++q) {
+      const int r = row0 + q * SCAN_THREADS;
+      if (r < n_p && cnt[q]) atomicAdd(&count[r], cnt[q]);
+    }
+  }
+}
+
+__global__ void k_scan_reduce(const double* __restrict__ psi_part, const double* __restrict__ phi_part, int nrb, int M,
+                              double* __restrict__ psi, double* __restrict__ phi) {
+  for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < M; j += gridDim.x * blockDim.x) {
+    double mn = INFINITY, mx = -INFINITY;
+    for (int r = 0; r < nrb; ++r) { mn = fmin(mn, psi_part[(size_t)r * M + j]); mx = fmax(mx, phi_part[(size_t)r * M + j]); }
+    psi[j] = mn;
+    phi[j] = mx;
+  }
+}
+
+__global__ void k_regions(const double* __restrict__ t, int n_p, double q_in, double q_out, uint8_t* __restrict__ cin,
+                          uint8_t* __restrict__ cout) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_p; i += gridDim.x * blockDim.x) {
+    cin[i] = t[i] > q_in ? 1 : 0;
+    cout[i] = t[i] >= q_out ? 1 : 0;
+  }
+}
+
+double empirical_quantile(std::vector<double>& a, double p) {
+  std::sort(a.begin(), a.end());
+  const long N = (long)a.size();
+  long k = (long)ceil(p * (double)N - 1e-9);
+  k = std::max(1L, std::min(N, k));
+  return a[k - 1];
+}
+
+cr_status calibrate_core(const double* d_S, int lds, int n_p, int M, const double* d_zhat, const double* d_v, double u,
+                         double level, uint8_t* d_cin, uint8_t* d_cout, int32_t* d_count, double* d_psi, double* d_phi,
+                         cr_calib_info* out, cudaStream_t stream, const CalibScratch& sc) {
+  const int nrb = (n_p + SCAN_ROWS - 1) / SCAN_ROWS;
+  CR_CUDA(cudaMemsetAsync(sc.bad, 0, sizeof(int), stream));
+  k_tstat<<<std::min(1024, (n_p + 255) / 256), 256, 0, stream>>>(d_zhat, d_v, u, n_p, sc.t, sc.bad);
+  CR_CHECK_LAUNCH("k_tstat");
+  if (d_count) CR_CUDA(cudaMemsetAsync(d_count, 0, (size_t)n_p * sizeof(int32_t), stream));
+  dim3 grid(nrb, (M + SCAN_COLS - 1) / SCAN_COLS);
+  k_scan<<<grid, SCAN_THREADS, 0, stream>>>(d_S, lds, n_p, M, sc.t, u, sc.psi_part, sc.phi_part, d_count);
+  CR_CHECK_LAUNCH("k_scan");
+  k_scan_reduce<<<std::min(1024, (M + 255) / 256), 256, 0, stream>>>(sc.psi_part, sc.phi_part, nrb, M, sc.psi, sc.phi);
+  CR_CHECK_LAUNCH("k_scan_reduce");
+  std::vector<double> psi(M), phi(M);
+  int bad = 0;
+  CR_CUDA(cudaMemcpyAsync(psi.data(), sc.psi, M * sizeof(double), cudaMemcpyDeviceToHost, stream));
+  CR_CUDA(cudaMemcpyAsync(phi.data(), sc.phi, M * sizeof(double), cudaMemcpyDeviceToHost, stream));
+  CR_CUDA(cudaMemcpyAsync(&bad, sc.bad, sizeof(int), cudaMemcpyDeviceToHost, stream));
+  if (d_psi) CR_CUDA(cudaMemcpyAsync(d_psi, sc.psi, M * sizeof(double), cudaMemcpyDeviceToDevice, stream));
+  if (d_phi) CR_CUDA(cudaMemcpyAsync(d_phi, sc.phi, M * sizeof(double), cudaMemcpyDeviceToDevice, stream));
+  CR_CUDA(cudaStreamSynchronize(stream));
+  if (bad) return fail(CR_ERR_NONPOS_MSPE, "cr_calibrate: some v_i <= 0");
+  std::vector<double> a_psi, a_phi;
+  a_psi.reserve(M);
+  a_phi.reserve(M);
+  for (int j = 0; j < M; ++j) {
+    if (psi[j] != INFINITY) a_psi.push_back(psi[j]);
+    if (phi[j] != -INFINITY) a_phi.push_back(phi[j]);
+  }
+  cr_calib_info info{};
+  info.n_psi = (int)a_psi.size();
+  info.n_phi = (int)a_phi.size();
+  if (out) *out = info;
+  if (a_psi.empty() || a_phi.empty())
+    return fail(CR_ERR_EMPTY_SAMPLE, "cr_calibrate: n_psi=" + std::to_string(info.n_psi) + " n_phi=" + std::to_string(info.n_phi));
+  const double alpha = 1.0 - level;
+  info.q_out = empirical_quantile(a_psi, alpha);
+  info.q_in = empirical_quantile(a_phi, 1.0 - alpha);
+  if (out) *out = info;
+  k_regions<<<std::min(1024, (n_p + 255) / 256), 256, 0, stream>>>(sc.t, n_p, info.q_in, info.q_out, d_cin, d_cout);
+  CR_CHECK_LAUNCH("k_regions");
+  return CR_OK;
+}
+
+// Library-managed scratch for cr_calibrate, grown on demand (one per process).
+static std::mutex g_mu;
+static CalibScratch g_sc;
+static size_t g_np = 0, g_M = 0, g_nrbM = 0;
+
+static cr_status ensure_scratch(int n_p, int M) {
+  const int nrb = (n_p + SCAN_ROWS - 1) / SCAN_ROWS;
+  if ((size_t)n_p > g_np) {
+    if (g_sc.t) cudaFree(g_sc.t);
+    g_sc.t = nullptr;
+    CR_CUDA(cudaMalloc(&g_sc.t, (size_t)n_p * sizeof(double)));
+    g_np = n_p;
+  }
+  if ((size_t)M > g_M) {
+    if (g_sc.psi) cudaFree(g_sc.psi);
+    if (g_sc.phi) cudaFree(g_sc.phi);
+    g_sc.psi = g_sc.phi = nullptr;
+    CR_CUDA(cudaMalloc(&g_sc.psi, (size_t)M * sizeof(double)));
+    CR_CUDA(cudaMalloc(&g_sc.phi, (size_t)M * sizeof(double)));
+    g_M = M;
+  }
+  if ((size_t)nrb * M > g_nrbM) {
+    if (g_sc.psi_part) cudaFree(g_sc.psi_part);
+    if (g_sc.phi_part) cudaFree(g_sc.phi_part);
+    g_sc.psi_part = g_sc.phi_part = nullptr;
+    CR_CUDA(cudaMalloc(&g_sc.psi_part, (size_t)nrb * M * sizeof(double)));
+    CR_CUDA(cudaMalloc(&g_sc.phi_part, (size_t)nrb * M * sizeof(double)));
+    g_nrbM = (size_t)nrb * M;
+  }
+  if (!g_sc.bad) CR_CUDA(cudaMalloc(&g_sc.bad, sizeof(int)));
+  return CR_OK;
+}
+
+}  // namespace cr
+
+using namespace cr;
+
+extern "C" cr_status cr_calibrate(const double* d_S, int lds, int n_p, int M, const double* d_zhat, const double* d_v, double u,
+                                  double level, uint8_t* d_cin, uint8_t* d_cout, int32_t* d_count, double* d_psi,
+                                  double* d_phi, cr_calib_info* out, cr_stream stream) {
+  if (!d_S || !d_zhat || !d_v || !d_cin || !d_cout || n_p <= 0 || M <= 0 || lds < n_p || !(level > 0.0 && level < 1.0))
+    return fail(CR_ERR_ARG, "cr_calibrate: argument");
+  std::lock_guard<std::mutex> lk(g_mu);
+  CR_TRY(ensure_scratch(n_p, M));
+  return calibrate_core(d_S, lds, n_p, M, d_zhat, d_v, u, level, d_cin, d_cout, d_count, d_psi, d_phi, out, stream, g_sc);
+}

@@ -1,0 +1,26 @@
+// Calibration scan interfaces (calib.cu).
+#pragma once
+#include "common.cuh"
+
+namespace cr {
+
+constexpr int SCAN_THREADS = 256;
+constexpr int SCAN_ROWS = 2048;   // rows per CTA (8 per thread)
+constexpr int SCAN_COLS = 32;     // simulation columns per CTA
+
+// Device scratch of one calibration: t (n_p), psi/phi (M), per-row-block partials
+// (ceil(n_p / SCAN_ROWS) x M each) and an MSPE flag.
+struct CalibScratch {
+  double* t = nullptr;
+  double* psi = nullptr;
+  double* phi = nullptr;
+  double* psi_part = nullptr;
+  double* phi_part = nullptr;
+  int* bad = nullptr;
+};
+
+cr_status calibrate_core(const double* d_S, int lds, int n_p, int M, const double* d_zhat, const double* d_v, double u,
+                         double level, uint8_t* d_cin, uint8_t* d_cout, int32_t* d_count, double* d_psi, double* d_phi,
+                         cr_calib_info* out, cudaStream_t stream, const CalibScratch& sc);
+
+}  // namespace cr

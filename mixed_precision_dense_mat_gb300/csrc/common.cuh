@@ -1,0 +1,116 @@
+// Internal definitions shared by the translation units of libcr.so.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+#include "../../include/cr.h"
+
+namespace cr {
+
+// ----------------------------------------------------------------- errors
+void set_error(const std::string& msg);
+cr_status fail(cr_status code, const std::string& msg);
+cr_status cuda_fail(cudaError_t e, const char* what);
+
+#define CR_CUDA(call)                                               \
+  do {                                                              \
+    cudaError_t e__ = (call);                                       \
+    if (e__ != cudaSuccess) return ::cr::cuda_fail(e__, #call);     \
+  } while (0)
+
+#define CR_CHECK_LAUNCH(what)                                       \
+  do {                                                              \
+    cudaError_t e__ = cudaGetLastError();                           \
+    if (e__ != cudaSuccess) return ::cr::cuda_fail(e__, what);      \
+  } while (0)
+
+#define CR_TRY(expr)                                                \
+  do {                                                              \
+    cr_status s__ = (expr);                                         \
+    if (s__ != CR_OK) return s__;                                   \
+  } while (0)
+
+// Device status word bits (written by kernels, read by the host after a sync).
+enum : int { DEV_ERR_TIMEOUT = 1, DEV_ERR_BOUNDS = 2 };
+
+// ----------------------------------------------------------------- tile indexing
+__host__ __device__ inline int tidx(int i, int j) { return i * (i + 1) / 2 + j; }  // i >= j
+
+// Kernel-side view of the tile storage.
+struct TileView {
+  int n, nb, nt;
+  int8_t* cls;     // [ntiles] CR_PREC_*
+  int* i64;        // [ntiles] slot in pool64 or -1
+  int* i32;        // [ntiles] slot in pool32 or -1
+  int* hi16;       // [ntiles] FP16 slot of the value (FP16 class) or of its high part
+  int* lo16;       // [ntiles] FP16 slot of the low part (FP32/FP64 classes) or -1
+  double* pool64;
+  float* pool32;
+  __half* pool16;
+};
+
+}  // namespace cr
+
+struct cr_tilemat_s {
+  int n = 0, nb = 0, nt = 0, npad = 0, ntiles = 0;
+  int device = 0;
+  // covariance (FP64 lower tiles) and statistics
+  double* master = nullptr;      // ntiles * nb * nb
+  double* stat_part = nullptr;   // ntiles * (nb/64) * 3 partials
+  double* stats = nullptr;       // ntiles * 3 : sum of squares, min, max
+  cr_cov_params params{};
+  bool built = false;
+  std::vector<double> h_frob, h_vmin, h_vmax;   // ntiles each, after cr_tile_stats
+  bool stats_on_host = false;
+  // precision map and class storage
+  bool mapped = false;
+  int amp = 1;
+  double s = 1.0;
+  int eA = 0;                     // power-of-two scale of FP32-class TRSM inputs
+  cr_pmap_info pinfo{};
+  std::vector<int8_t> h_cls;
+  std::vector<int> h_i64, h_i32, h_hi16, h_lo16;
+  int n64 = 0, n32 = 0, n16 = 0;  // slots per pool
+  int ws_hi0 = 0, ws_lo0 = 0, minv_hi = 0, minv_lo = 0;
+  int8_t* d_cls = nullptr;
+  int *d_i64 = nullptr, *d_i32 = nullptr, *d_hi16 = nullptr, *d_lo16 = nullptr;
+  double* pool64 = nullptr;
+  float* pool32 = nullptr;
+  __half* pool16 = nullptr;
+  double* ws64 = nullptr;         // nt * nb * nb: FP64-class TRSM inputs
+  double* minv = nullptr;         // nb * nb: inverse of the current diagonal factor
+  double* scratch64 = nullptr;    // nb * nb: temporaries of the diagonal factorisation
+  int* d_status = nullptr;        // [0] device error bits, [1] first failing column (1-based) or 0, [2] Minv exponent
+  CUtensorMap tm_pool16;          // 3-D map over pool16 (slot, row, col)
+  // simulation right-hand side B = fp16(M_rand / s), npad x M column-major
+  __half* b16 = nullptr;
+  size_t b16_elems = 0;
+  int b16_M = -1;
+  CUtensorMap tm_b16;
+  double* bnorm_part = nullptr;   // per-block partial sums of ||B||_F^2
+  bool factored = false;
+  int info = 0;
+
+  cr::TileView view() const {
+    cr::TileView v;
+    v.n = n; v.nb = nb; v.nt = nt;
+    v.cls = d_cls; v.i64 = d_i64; v.i32 = d_i32; v.hi16 = d_hi16; v.lo16 = d_lo16;
+    v.pool64 = pool64; v.pool32 = pool32; v.pool16 = pool16;
+    return v;
+  }
+};
+
+namespace cr {
+// Implemented in the translation units.
+cr_status free_class_storage(cr_tilemat V);
+cr_status make_tensor_map_3d_f16(CUtensorMap* tm, void* base, int inner, int rows, int slots,
+                                 int box_inner, int box_rows);
+cr_status make_tensor_map_2d_f16(CUtensorMap* tm, void* base, int inner, int outer, int ld,
+                                 int box_inner, int box_outer);
+}  // namespace cr

@@ -1,0 +1,208 @@
+// FP64 kernels: batched strided tile GEMM (C = beta C + alpha sum_p A_p B_p^T), the 64 x 64
+// Cholesky-plus-inverse base block, and conversions of FP64 tiles to FP16 high/low parts.
+//
+// On GB300 the FP64 units deliver about 1.2 TFLOP/s (two FMA lanes per SM per clock), so
+// these kernels are bound by the FP64 pipe and need no elaborate data staging; what matters
+// is spreading the work over many SMs (small output blocks) on the critical path.
+#include <math.h>
+
+#include "common.cuh"
+#include "fp64.cuh"
+
+namespace cr {
+
+template <int BM, int BN>
+__global__ void __launch_bounds__(256) k_dgemm(const DJob* __restrict__ jobs, const DPair* __restrict__ pairs) {
+  constexpr int KB = 16;
+  constexpr int TM = BM / 16, TN = BN / 16;
+  __shared__ double As[KB][BM + 1];
+  __shared__ double Bs[KB][BN + 1];
+  const DJob jb = jobs[blockIdx.x];
+  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+  double acc[TM][TN];
+#pragma unroll
+  for (int a = 0; a < TM; ++a)
+#pragma unroll
+    for (int b = 0; b < TN; ++b) acc[a][b] = 0.0;
+  for (int pi = 0; pi < jb.pcnt; ++pi) {
+    const DPair pr = pairs[jb.pbeg + pi];
+    const int K = min(pr.K, jb.kmax);
+    const double* Ab = pr.A + (size_t)jb.arow * pr.sAm;
+    const double* Bb = pr.B + (size_t)jb.brow * pr.sBn;
+    for (int k0 = 0; k0 < K; k0 += KB) {
+      for (int idx = threadIdx.x; idx < BM * KB; idx += 256) {
+        const int m = idx / KB, k = idx % KB;
+        As[k][m] = (m < jb.m && k0 + k < K) ? Ab[(size_t)m * pr.sAm + (size_t)(k0 + k) * pr.sAk] : 0.0;
+      }
+      for (int idx = threadIdx.x; idx < BN * KB; idx += 256) {
+        const int nn = idx / KB, k = idx % KB;
+        Bs[k][nn] = (nn < jb.n && k0 + k < K) ? Bb[(size_t)nn * pr.sBn + (size_t)(k0 + k) * pr.sBk] : 0.0;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int k = 0; k < KB; ++k) {
+        double a[TM], b[TN];
+#pragma unroll
+        for (int q = 0; q < TM; ++q) a[q] = As[k][ty + 16 * q];
+#pragma unroll
+        for (int q = 0; q < TN; ++q) b[q] = Bs[k][tx + 16 * q];
+#pragma unroll
+        for (int x = 0; x < TM; ++x)
+#pragma unroll
+          for (int y = 0; y < TN; ++y) acc[x][y] = fma(a[x], b[y], acc[x][y]);
+      }
+      __syncthreads();
+    }
+  }
+#pragma unroll
+  for (int x = 0; x < TM; ++x)
+#pragma unroll
+    for (int y = 0; y < TN; ++y) {
+      const int m = ty + 16 * x, nn = tx + 16 * y;
+      if (m < jb.m && nn < jb.n) {
+        double* c = jb.C + (size_t)m * jb.sCm + (size_t)nn * jb.sCn;
+        const double prev = jb.beta != 0.0 ? jb.beta * *c : 0.0;
+        *c = prev + jb.alpha * acc[x][y];
+      }
+    }
+}
+
+cr_status dgemm_launch(int bm, const DJob* d_jobs, const DPair* d_pairs, int njobs, cudaStream_t stream) {
+  if (njobs <= 0) return CR_OK;
+  switch (bm) {
+    case 16: k_dgemm<16, 16><<<njobs, 256, 0, stream>>>(d_jobs, d_pairs); break;
+    case 32: k_dgemm<32, 32><<<njobs, 256, 0, stream>>>(d_jobs, d_pairs); break;
+    case 64: k_dgemm<64, 64><<<njobs, 256, 0, stream>>>(d_jobs, d_pairs); break;
+    default: return fail(CR_ERR_ARG, "dgemm_launch: block size");
+  }
+  CR_CHECK_LAUNCH("k_dgemm");
+  return CR_OK;
+}
+
+// Cholesky of the 64 x 64 block at A (row-major, leading dimension lda; lower part read,
+// lower part overwritten with L) and its inverse M = L^-1 written (lower, upper zeroed) at
+// Minv.  A non-positive pivot records its 1-based global column (gcol0 + c + 1) in
+// status[1] with atomicMin.
+__global__ void __launch_bounds__(256) k_potrf64_base(double* A, int lda, double* Minv, int ldm, int gcol0, int* status) {
+  // L holds the factor in its lower triangle; the inverse M is kept transposed in the strict
+  // upper triangle (M[r][c] at L[c][r], r > c) with its diagonal in dg.
+  __shared__ double L[64][65];
+  __shared__ double dg[64];
+  for (int idx = threadIdx.x; idx < 64 * 64; idx += 256) {
+    const int r = idx / 64, c = idx % 64;
+    L[r][c] = r >= c ? A[(size_t)r * lda + c] : 0.0;
+  }
+  __syncthreads();
+  for (int c = 0; c < 64; ++c) {
+    if (threadIdx.x == 0) {
+      const double d = L[c][c];
+      if (!(d > 0.0)) atomicMin(&status[1], gcol0 + c + 1);
+      L[c][c] = sqrt(d);
+    }
+    __syncthreads();
+    const double dc = L[c][c];
+    for (int r = c + 1 + threadIdx.x; r < 64; r += 256) L[r][c] /= dc;
+    __syncthreads();
+    // trailing update of the lower part: rows r > c, columns q in (c, r]
+    const int m = 63 - c;
+    for (int idx = threadIdx.x; idx < m * m; idx += 256) {
+      const int r = c + 1 + idx / m, q = c + 1 + idx % m;
+      if (q <= r) L[r][q] -= L[r][c] * L[q][c];
+    }
+    __syncthreads();
+  }
+  // inverse by forward substitution, one column of M per thread
+  if (threadIdx.x < 64) {
+    const int c = threadIdx.x;
+    dg[c] = 1.0 / L[c][c];
+    for (int r = c + 1; r < 64; ++r) {
+      double sum = L[r][c] * dg[c];
+      for (int q = c + 1; q < r; ++q) sum = fma(L[r][q], L[c][q], sum);
+      L[c][r] = -sum / L[r][r];
+    }
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < 64 * 64; idx += 256) {
+    const int r = idx / 64, c = idx % 64;
+    if (r >= c) A[(size_t)r * lda + c] = L[r][c];
+    Minv[(size_t)r * ldm + c] = r > c ? L[c][r] : (r == c ? dg[c] : 0.0);
+  }
+}
+
+// FP64 tile -> FP16 high and low parts (x = hi + lo to ~2^-22), optionally zeroing the
+// strict upper triangle (diagonal factor tiles).
+__global__ void __launch_bounds__(256) k_split_tile(const double* __restrict__ src, int nb, __half* __restrict__ hi,
+                                                    __half* __restrict__ lo, int lower_only) {
+  const size_t count = (size_t)nb * nb;
+  for (size_t idx = blockIdx.x * 256 + threadIdx.x; idx < count; idx += (size_t)gridDim.x * 256) {
+    const int r = (int)(idx / nb), c = (int)(idx % nb);
+    const double x = (lower_only && c > r) ? 0.0 : src[idx];
+    const __half h = __double2half(x);
+    hi[idx] = h;
+    lo[idx] = __double2half(x - (double)__half2float(h));
+  }
+}
+
+// Splits the inverse factor: chooses eM with max|M| 2^eM <= 2^14 (status[2] = eM) and writes
+// the FP16 high/low parts of M 2^eM.  One CTA.
+__global__ void __launch_bounds__(1024) k_split_minv(const double* __restrict__ Minv, int nb, __half* __restrict__ hi,
+                                                     __half* __restrict__ lo, int* status) {
+  __shared__ double red[32];
+  __shared__ int s_e;
+  const size_t count = (size_t)nb * nb;
+  double mx = 0.0;
+  for (size_t idx = threadIdx.x; idx < count; idx += blockDim.x) mx = fmax(mx, fabs(Minv[idx]));
+  for (int o = 16; o > 0; o >>= 1) mx = fmax(mx, __shfl_down_sync(0xffffffffu, mx, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double m = 0.0;
+    for (int q = 0; q < (int)(blockDim.x >> 5); ++q) m = fmax(m, red[q]);
+    int e = 0;
+    if (m > 0.0 && isfinite(m)) {
+      int ex;
+      frexp(m, &ex);          // m < 2^ex
+      e = 14 - ex;            // m 2^e < 2^14
+    }
+    s_e = e;
+    status[2] = e;
+  }
+  __syncthreads();
+  const double sc = ldexp(1.0, s_e);
+  for (size_t idx = threadIdx.x; idx < count; idx += blockDim.x) {
+    const double x = Minv[idx] * sc;
+    const __half h = __double2half(x);
+    hi[idx] = h;
+    lo[idx] = __double2half(x - (double)__half2float(h));
+  }
+}
+
+__global__ void k_status_init(int* status) {
+  status[0] = 0;
+  status[1] = 0x7fffffff;
+  status[2] = 0;
+  status[3] = 0;
+}
+
+cr_status potrf64_base_launch(double* A, int lda, double* Minv, int ldm, int gcol0, int* status, cudaStream_t s) {
+  k_potrf64_base<<<1, 256, 0, s>>>(A, lda, Minv, ldm, gcol0, status);
+  CR_CHECK_LAUNCH("k_potrf64_base");
+  return CR_OK;
+}
+cr_status split_tile_launch(const double* src, int nb, __half* hi, __half* lo, int lower_only, cudaStream_t s) {
+  k_split_tile<<<128, 256, 0, s>>>(src, nb, hi, lo, lower_only);
+  CR_CHECK_LAUNCH("k_split_tile");
+  return CR_OK;
+}
+cr_status split_minv_launch(const double* Minv, int nb, __half* hi, __half* lo, int* status, cudaStream_t s) {
+  k_split_minv<<<1, 1024, 0, s>>>(Minv, nb, hi, lo, status);
+  CR_CHECK_LAUNCH("k_split_minv");
+  return CR_OK;
+}
+cr_status status_init_launch(int* status, cudaStream_t s) {
+  k_status_init<<<1, 1, 0, s>>>(status);
+  CR_CHECK_LAUNCH("k_status_init");
+  return CR_OK;
+}
+
+}  // namespace cr

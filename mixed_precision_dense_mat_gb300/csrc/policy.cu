@@ -1,0 +1,217 @@
+// Host-side precision policy and allocation of the per-precision tile storage.
+//
+// "Mixed-Precision GPU Acceleration for Confidence Regions of Spatial Excursion Sets":
+//  - Section IV-B / VI-D: per-tile FP64/FP32/FP16 chosen by comparing each tile's norm with
+//    the global norm; diagonal tiles stay FP64.  Rule used: off-diagonal tile (i, j) takes
+//    the lowest p in {FP16, FP32} with ||V_ij||_F * NT <= (fixedacc / eps_p) ||V||_F, else
+//    FP64 (eps_FP16 = 2^-10 as in Eq.11, eps_FP32 = 2^-23); ||V||_F over the full symmetric
+//    matrix.
+//  - Section V-D: automatic mode (start 1e-4, times 0.9 while a check fails, stop when both
+//    pass or no FP16 tile is left); Eq.10 and Eq.11 checks over the FP16 tiles.
+//  - Section V-E Eq.12: s = floor(min(65504, min_f u_f)) - 1 when above 1, else 1.
+#include <float.h>
+#include <math.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace cr {
+cr_status fetch_stats(cr_tilemat V);
+
+namespace {
+
+struct Checks {
+  int n16 = 0;
+  double R = NAN, rho1 = NAN, rho2 = NAN;
+  bool c1 = true, c2 = true;
+};
+
+void make_map(const cr_tilemat V, double fixedacc, std::vector<int8_t>& cls) {
+  const int nt = V->nt;
+  double g2 = 0.0;
+  for (int i = 0; i < nt; ++i) {
+    g2 += V->h_frob[tidx(i, i)] * V->h_frob[tidx(i, i)];
+    for (int j = 0; j < i; ++j) g2 += 2.0 * V->h_frob[tidx(i, j)] * V->h_frob[tidx(i, j)];
+  }
+  const double g = sqrt(g2);
+  const double lim16 = (fixedacc / ldexp(1.0, -10)) * g;
+  const double lim32 = (fixedacc / ldexp(1.0, -23)) * g;
+  cls.assign(V->ntiles, CR_PREC_FP64);
+  for (int i = 0; i < nt; ++i)
+    for (int j = 0; j < i; ++j) {
+      const double lhs = V->h_frob[tidx(i, j)] * nt;
+      cls[tidx(i, j)] = lhs <= lim16 ? CR_PREC_FP16 : (lhs <= lim32 ? CR_PREC_FP32 : CR_PREC_FP64);
+    }
+}
+
+Checks checks(const cr_tilemat V, const std::vector<int8_t>& cls) {
+  Checks c;
+  double vmax_hp = -INFINITY, vmin_hp = INFINITY, fmax_hp = -INFINITY, vmax_all = -INFINITY, fmax_all = -INFINITY;
+  for (int t = 0; t < V->ntiles; ++t) {
+    vmax_all = std::max(vmax_all, V->h_vmax[t]);
+    fmax_all = std::max(fmax_all, V->h_frob[t]);
+    if (cls[t] == CR_PREC_FP16) {
+      ++c.n16;
+      vmax_hp = std::max(vmax_hp, V->h_vmax[t]);
+      vmin_hp = std::min(vmin_hp, V->h_vmin[t]);
+      fmax_hp = std::max(fmax_hp, V->h_frob[t]);
+    }
+  }
+  if (c.n16 == 0) return c;
+  c.R = vmax_hp / vmin_hp;
+  c.rho1 = vmax_hp / vmax_all;
+  c.rho2 = fmax_hp / fmax_all;
+  c.c1 = c.R < 65504.0 / ldexp(1.0, -24);
+  c.c2 = std::max(c.rho1, c.rho2) < 1e-4 / ldexp(1.0, -10);
+  return c;
+}
+
+void scale(const cr_tilemat V, const std::vector<int8_t>& cls, cr_pmap_info* info) {
+  const double xmin[2] = {ldexp(1.0, -126), ldexp(1.0, -14)};   // FP32, FP16
+  const double xmax[2] = {(double)FLT_MAX, 65504.0};
+  const int fmt[2] = {CR_PREC_FP32, CR_PREC_FP16};
+  double ell = -INFINITY, us = 65504.0;
+  bool present = false;
+  for (int q = 0; q < 2; ++q) {
+    double vmn = INFINITY, vmx = -INFINITY;
+    bool any = false;
+    for (int i = 0; i < V->nt; ++i)
+      for (int j = 0; j < i; ++j)
+        if (cls[tidx(i, j)] == fmt[q]) {
+          any = true;
+          vmn = std::min(vmn, V->h_vmin[tidx(i, j)]);
+          vmx = std::max(vmx, V->h_vmax[tidx(i, j)]);
+        }
+    if (!any) continue;
+    present = true;
+    const double lf = vmn > 0 ? sqrt(xmin[q] / vmn) : INFINITY;
+    const double uf = vmx > 0 ? sqrt(xmax[q] / vmx) : INFINITY;
+    ell = std::max(ell, lf);
+    us = std::min(us, uf);
+  }
+  if (!present) {
+    info->s = 1.0; info->ell = NAN; info->u_s = NAN; info->range_ok = 1;
+    return;
+  }
+  const double cand = floor(us) - 1.0;
+  info->s = cand > 1.0 ? cand : 1.0;
+  info->ell = ell;
+  info->u_s = us;
+  info->range_ok = ell <= us;
+}
+
+template <class T>
+cr_status upload(T** d, const std::vector<T>& h) {
+  if (*d) cudaFree(*d);
+  *d = nullptr;
+  CR_CUDA(cudaMalloc(d, std::max<size_t>(1, h.size()) * sizeof(T)));
+  CR_CUDA(cudaMemcpy(*d, h.data(), h.size() * sizeof(T), cudaMemcpyHostToDevice));
+  return CR_OK;
+}
+
+}  // namespace
+
+cr_status allocate_class_storage(cr_tilemat V) {
+  free_class_storage(V);
+  const int nt = V->nt, T = V->ntiles;
+  const size_t tile = (size_t)V->nb * V->nb;
+  V->h_i64.assign(T, -1); V->h_i32.assign(T, -1); V->h_hi16.assign(T, -1); V->h_lo16.assign(T, -1);
+  V->n64 = V->n32 = 0;
+  int off64 = 0;   // off-diagonal FP64 tiles
+  for (int t = 0; t < T; ++t) {
+    if (V->h_cls[t] == CR_PREC_FP64) V->h_i64[t] = V->n64++;
+    else if (V->h_cls[t] == CR_PREC_FP32) V->h_i32[t] = V->n32++;
+  }
+  for (int i = 0; i < nt; ++i)
+    for (int j = 0; j < i; ++j) off64 += V->h_cls[tidx(i, j)] == CR_PREC_FP64;
+  V->n16 = 0;
+  if (V->amp) {
+    for (int t = 0; t < T; ++t) V->h_hi16[t] = V->n16++;
+    for (int t = 0; t < T; ++t)
+      if (V->h_cls[t] != CR_PREC_FP16) V->h_lo16[t] = V->n16++;
+    V->ws_hi0 = V->n16; V->n16 += nt;
+    V->ws_lo0 = V->n16; V->n16 += nt;
+    V->minv_hi = V->n16++;
+    V->minv_lo = V->n16++;
+  }
+  CR_TRY(upload(&V->d_cls, V->h_cls));
+  CR_TRY(upload(&V->d_i64, V->h_i64));
+  CR_TRY(upload(&V->d_i32, V->h_i32));
+  CR_TRY(upload(&V->d_hi16, V->h_hi16));
+  CR_TRY(upload(&V->d_lo16, V->h_lo16));
+  CR_CUDA(cudaMalloc(&V->pool64, std::max<size_t>(1, (size_t)V->n64) * tile * sizeof(double)));
+  if (V->n32) CR_CUDA(cudaMalloc(&V->pool32, (size_t)V->n32 * tile * sizeof(float)));
+  if (V->n16) {
+    CR_CUDA(cudaMalloc(&V->pool16, (size_t)V->n16 * tile * sizeof(__half)));
+    CR_TRY(make_tensor_map_3d_f16(&V->tm_pool16, V->pool16, V->nb, V->nb, V->n16, 64, 128));
+  }
+  if (off64 > 0) CR_CUDA(cudaMalloc(&V->ws64, (size_t)nt * tile * sizeof(double)));
+  V->mapped = true;
+  return CR_OK;
+}
+
+}  // namespace cr
+
+using namespace cr;
+
+extern "C" cr_status cr_precision_map(cr_tilemat V, int amp, double fixedacc, int auto_mode, int8_t* h_map,
+                                      cr_pmap_info* info) {
+  if (!V) return fail(CR_ERR_ARG, "cr_precision_map: NULL handle");
+  if (amp && !auto_mode && !(fixedacc > 0)) return fail(CR_ERR_ARG, "cr_precision_map: fixedacc must be > 0");
+  CR_CUDA(cudaSetDevice(V->device));
+  CR_TRY(fetch_stats(V));
+  cr_pmap_info pi{};
+  std::vector<int8_t> cls;
+  Checks c;
+  if (!amp) {
+    cls.assign(V->ntiles, CR_PREC_FP64);
+    pi.fixedacc = fixedacc;
+    pi.iters = 0;
+    c = checks(V, cls);
+    pi.s = 1.0; pi.ell = NAN; pi.u_s = NAN; pi.range_ok = 1;
+  } else {
+    double fa = auto_mode ? 1e-4 : fixedacc;
+    int it = 0;
+    for (;;) {
+      make_map(V, fa, cls);
+      c = checks(V, cls);
+      ++it;
+      if (!auto_mode || c.n16 == 0 || (c.c1 && c.c2) || it >= 100000) break;
+      fa = fa * 0.9;
+    }
+    pi.fixedacc = fa;
+    pi.iters = it;
+    scale(V, cls, &pi);
+  }
+  pi.R_hp = c.R; pi.rho1 = c.rho1; pi.rho2 = c.rho2; pi.check1 = c.c1; pi.check2 = c.c2;
+  pi.n_fp64 = pi.n_fp32 = pi.n_fp16 = 0;
+  double vmax_all = -INFINITY;
+  for (int t = 0; t < V->ntiles; ++t) {
+    pi.n_fp64 += cls[t] == CR_PREC_FP64;
+    pi.n_fp32 += cls[t] == CR_PREC_FP32;
+    pi.n_fp16 += cls[t] == CR_PREC_FP16;
+    vmax_all = std::max(vmax_all, V->h_vmax[t]);
+  }
+  if (h_map) {
+    for (int i = 0; i < V->nt; ++i)
+      for (int j = 0; j < V->nt; ++j) h_map[i * V->nt + j] = j <= i ? cls[tidx(i, j)] : (int8_t)-1;
+  }
+  if (info) *info = pi;
+  V->h_cls = cls;
+  V->amp = amp ? 1 : 0;
+  V->s = pi.s;
+  V->pinfo = pi;
+  // Power-of-two scale for FP32-class triangular-solve inputs, which live on the s^2 V scale:
+  // W 2^-eA stays below 2^14 so its FP16 high/low split cannot overflow.
+  V->eA = 0;
+  if (V->amp) {
+    const double top = V->s * V->s * vmax_all;
+    while (ldexp(top, -V->eA) > 16384.0) ++V->eA;
+    // The factor L_s (magnitude up to s sqrt(max V_ii)) is read in FP16 by the simulation
+    // multiply (Alg.1 casts every off-diagonal factor tile to FP16).
+    if (V->s * sqrt(vmax_all) >= 65520.0)
+      return fail(CR_ERR_RANGE, "cr_precision_map: s * sqrt(max V_ii) exceeds the FP16 range");
+  }
+  return allocate_class_storage(V);
+}

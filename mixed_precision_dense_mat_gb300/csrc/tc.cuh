@@ -1,0 +1,31 @@
+// Parameters of the tensor-core tile kernel (tc.cu).
+#pragma once
+#include "common.cuh"
+
+namespace cr {
+
+constexpr int TC_BM = 128, TC_BN = 128, TC_BK = 64;
+constexpr int TC_STAGES = 6;
+constexpr int TC_STAGE_BYTES = (TC_BM + TC_BN) * TC_BK * 2;   // A and B, FP16, 32 KB
+constexpr int TC_THREADS = 192;
+constexpr size_t TC_SMEM = (size_t)TC_STAGES * TC_STAGE_BYTES + 1024 + 256;
+
+enum { TC_UPDATE = 0, TC_TRSM = 1, TC_TRMM = 2 };
+
+struct TcParams {
+  TileView v;
+  int mode;
+  int j;              // tile column (update / triangular solve)
+  const int* rows;    // tile rows of this launch (triangular solve); NULL: rows j, j+1, ...
+  int ws_hi0, ws_lo0, minv_hi, minv_lo;
+  int eA;             // FP32-class inputs were scaled by 2^-eA
+  const int* status;  // status[2]: exponent eM of the scaled inverse factor
+  int* err;           // device error bits
+  double* ws64;       // FP64-class triangular-solve inputs
+  double* Y;          // simulation output (n x M column-major)
+  int ldy, M, ncb, flags;
+};
+
+cr_status tc_launch(const TcParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid, cudaStream_t stream);
+
+}  // namespace cr

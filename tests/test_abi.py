@@ -1,0 +1,55 @@
+"""The C-ABI library loads and exports every entry point declared in include/cr.h (CPU only:
+no call here touches a GPU; argument checks return before any device work)."""
+import ctypes
+import os
+
+import pytest
+
+import mixed_precision_dense_mat_gb300 as cr
+from mixed_precision_dense_mat_gb300 import build_lib
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(build_lib.LIB):
+        build_lib.build()
+    return ctypes.CDLL(build_lib.LIB)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = cr.header_functions()
+    assert len(names) >= 16
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+    assert set(cr._SIGNATURES) == set(names)
+
+
+def test_status_strings_and_version(lib):
+    cr.load()
+    assert cr._lib.cr_status_str(0) == b"CR_OK"
+    assert cr._lib.cr_status_str(4) == b"CR_ERR_NOT_SPD"
+    for code, name in cr.STATUS.items():
+        assert cr._lib.cr_status_str(code).decode() == name
+    a, b = ctypes.c_int(), ctypes.c_int()
+    assert cr._lib.cr_version(ctypes.byref(a), ctypes.byref(b)) == 0
+
+
+def test_argument_errors_without_gpu(lib):
+    cr.load()
+    h = ctypes.c_void_p()
+    assert cr._lib.cr_tilemat_create(100, 100, ctypes.byref(h)) == 1      # nb must be a multiple of 128
+    assert b"nb" in cr._lib.cr_last_error_detail()
+    assert cr._lib.cr_tilemat_create(-5, 128, ctypes.byref(h)) == 1
+    assert cr._lib.cr_tilemat_create(10, 128, None) == 1
+    assert cr._lib.cr_cov_build(None, None, None, None) == 1
+    assert cr._lib.cr_potrf_adaptive(None, None, None) == 1
+    assert cr._lib.cr_rnorm(None, 1, 1, 1, 0, 0, None) == 1
+    assert cr._lib.cr_calibrate(None, 1, 1, 1, None, None, 0.0, 0.9, None, None, None, None, None, None, None) == 1
+    assert cr._lib.cr_krige_correct(None, 1, None, None, 1, 1, 1, 1, None, 1, None) == 1
+    assert cr._lib.cr_tilemat_destroy(None) == 0
+
+
+def test_header_declares_documented_path():
+    names = cr.header_functions()
+    for n in ("cr_cov_build", "cr_precision_map", "cr_potrf_adaptive", "cr_trmm_sim", "cr_krige", "cr_calibrate"):
+        assert n in names

@@ -1,0 +1,196 @@
+"""Parity of the CUDA path with the oracle (GPU).  Inputs come from inputgen only; expected
+values come from oracle/ only.  Tolerances: FP64 paths 1e-11 relative Frobenius (tighter
+where the arithmetic allows), adaptive simulation 1e-2 relative Frobenius on Y, integer and
+index outputs bit-exact."""
+import numpy as np
+import pytest
+import torch
+
+import inputgen
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def colmajor(a):
+    """numpy (n, m) -> CUDA column-major tensor"""
+    return torch.from_numpy(np.asfortranarray(a).T.copy()).cuda().T
+
+
+def relf(a, b):
+    return np.linalg.norm(a - b) / np.linalg.norm(b)
+
+
+COV_CASES = {
+    "a_exp": dict(n=1024, nb=128, family="matern", beta=0.1, nu=0.5, nugget=1e-6, n_pred=None, tau2=0.0),
+    "ragged_nu15": dict(n=1000, nb=128, family="matern", beta=0.3, nu=1.5, nugget=1e-4, n_pred=None, tau2=0.0),
+    "nu1_krige": dict(n=600, nb=128, family="matern", beta=0.1, nu=1.0, nugget=0.0, n_pred=300, tau2=0.01),
+    "nu07": dict(n=500, nb=128, family="matern", beta=0.2, nu=0.7, nugget=1e-5, n_pred=None, tau2=0.0),
+    "nu25": dict(n=384, nb=128, family="matern", beta=0.2, nu=2.5, nugget=1e-3, n_pred=None, tau2=0.0),
+    "powexp": dict(n=512, nb=128, family="powexp", beta=0.033, nu=0.5, nugget=1e-6, n_pred=None, tau2=0.0),
+}
+
+
+def _build(lib, c, seed=1):
+    xy = inputgen.morton_sorted(inputgen.uniform_locations(c["n"], seed))
+    V = lib.TileMat(c["n"], c["nb"])
+    lib.cov_build(V, dev(xy), c["family"], 1.0, c["beta"], c["nu"], nugget=c["nugget"], n_pred=c["n_pred"],
+                  tau2=c["tau2"])
+    Vo = oracle.covariance_matrix(xy, c["family"], 1.0, c["beta"], c["nu"], c["nugget"], c["n_pred"], c["tau2"])
+    return xy, V, Vo
+
+
+@pytest.mark.parametrize("case", list(COV_CASES))
+def test_covariance_and_stats(lib, case):
+    c = COV_CASES[case]
+    xy, V, Vo = _build(lib, c)
+    G = lib.tilemat_to_dense(V, 0).cpu().numpy()
+    Lo = np.tril(Vo)
+    err = np.max(np.abs(G - Lo))
+    assert err <= 2e-14, f"max abs covariance error {err:.3e}"
+    f, mn, mx = lib.tile_stats(V)
+    fo, mno, mxo = oracle.tile_stats(Vo, c["nb"])
+    low = np.tril(np.ones_like(f, dtype=bool))
+    np.testing.assert_allclose(f[low], fo[low], rtol=1e-13)
+    np.testing.assert_allclose(mn[low], mno[low], rtol=1e-13, atol=1e-300)
+    np.testing.assert_allclose(mx[low], mxo[low], rtol=1e-13)
+    V.close()
+
+
+@pytest.mark.parametrize("fixedacc,auto", [(1e-6, False), (1e-3, False), (1e-4, True)])
+def test_precision_map_matches_oracle(lib, fixedacc, auto):
+    c = COV_CASES["a_exp"]
+    xy, V, Vo = _build(lib, c)
+    m, info = lib.precision_map(V, amp=True, fixedacc=fixedacc, auto=auto)
+    fo, mno, mxo = oracle.tile_stats(Vo, c["nb"])
+    ref = oracle.select_precision(fo, mno, mxo, fixedacc, auto)
+    low = np.tril(np.ones(m.shape, dtype=bool))
+    np.testing.assert_array_equal(m[low], ref["map"][low])
+    assert info["s"] == ref["s"]
+    assert info["iters"] == ref["iters"] and info["fixedacc"] == ref["fixedacc"]
+    assert bool(info["check1"]) == ref["check1"] and bool(info["check2"]) == ref["check2"]
+    assert info["n_fp16"] == ref["n_fp16"]
+    V.close()
+
+
+@pytest.mark.parametrize("case", ["a_exp", "ragged_nu15"])
+def test_fp64_cholesky_and_simulation(lib, case):
+    c = COV_CASES[case]
+    xy, V, Vo = _build(lib, c)
+    lib.precision_map(V, amp=False)
+    assert lib.potrf_adaptive(V) == 0
+    L = lib.tilemat_to_dense(V, 1).cpu().numpy()
+    Lo = oracle.cholesky_lower(Vo)
+    # FP64 rounding differences between two Cholesky orderings, measured against LAPACK
+    scale = max(1.0, relf(np.linalg.cholesky(Vo), Lo) / 1e-14)
+    eL = relf(L, Lo)
+    assert eL <= 1e-11 * scale, f"L error {eL:.3e} (ordering noise x{scale:.1f})"
+    M = 64
+    Z = inputgen.standard_normals(c["n"], M, 3)
+    Y = lib.trmm_sim(V, colmajor(Z), M).cpu().numpy()
+    eY = relf(Y, oracle.simulate(Lo, Z))
+    assert eY <= 1e-11 * scale, f"Y error {eY:.3e}"
+    V.close()
+
+
+@pytest.mark.parametrize("case,fixedacc", [("a_exp", 1e-6), ("a_exp", 1e-3), ("ragged_nu15", 1e-6), ("nu07", 1e-2)])
+def test_adaptive_cholesky_and_simulation(lib, case, fixedacc):
+    c = COV_CASES[case]
+    xy, V, Vo = _build(lib, c)
+    m, info = lib.precision_map(V, amp=True, fixedacc=fixedacc)
+    assert lib.potrf_adaptive(V) == 0
+    s = info["s"]
+    L = lib.tilemat_to_dense(V, 1).cpu().numpy() / s
+    Lo = oracle.cholesky_lower(Vo)
+    eL = relf(L, Lo)
+    M = 200
+    Z = inputgen.standard_normals(c["n"], M, 4)
+    Y = lib.trmm_sim(V, colmajor(Z), M).cpu().numpy()
+    Yo = oracle.simulate(Lo, Z)
+    eY = relf(Y, Yo)
+    Y16 = lib.trmm_sim(V, colmajor(Z), M, flags=lib.CR_TRMM_FP16_DEST).cpu().numpy()
+    eY16 = relf(Y16, Yo)
+    msg = (f"fp64/32/16 tiles {info['n_fp64']}/{info['n_fp32']}/{info['n_fp16']} s={s} "
+           f"eL={eL:.2e} eY={eY:.2e} eY16={eY16:.2e}")
+    assert eY <= 1e-2 and eY16 <= 1e-2, msg
+    assert eL <= 1e-2, msg
+    V.close()
+
+
+def test_rnorm_stream_matches_oracle(lib):
+    n, M, seed, off = 777, 33, 42, 5
+    Z = lib.rnorm(n, M, seed, off).cpu().numpy()
+    Zo = oracle.rnorm(n, M, seed, off)
+    assert np.max(np.abs(Z - Zo)) <= 1e-13
+
+
+def test_generated_simulation_matches_oracle_stream(lib):
+    c = COV_CASES["a_exp"]
+    xy, V, Vo = _build(lib, c)
+    lib.precision_map(V, amp=True, fixedacc=1e-6)
+    assert lib.potrf_adaptive(V) == 0
+    M, seed = 100, 9
+    Y, bn = lib.trmm_sim(V, None, M, seed=seed, flags=lib.CR_TRMM_GENERATE, want_bnorm=True)
+    Zo = oracle.rnorm(c["n"], M, seed)
+    Yo = oracle.simulate(oracle.cholesky_lower(Vo), Zo)
+    assert relf(Y.cpu().numpy(), Yo) <= 1e-2
+    s = lib.precision_map.__self__ if False else None
+    V.close()
+
+
+def test_calibration_bit_exact(lib):
+    rng = np.random.default_rng(17)
+    n_p, M, u = 3000, 257, 0.25
+    S = rng.standard_normal((n_p, M))
+    z = rng.standard_normal(n_p) * 0.5
+    v = rng.uniform(0.3, 2.0, n_p)
+    out = lib.calibrate(colmajor(S), dev(z), dev(v), u, 0.9, counts=True, extrema=True)
+    ref = oracle.calibrate(S, z, v, u, 0.9)
+    np.testing.assert_array_equal(out["psi"].cpu().numpy(), ref["psi"])
+    np.testing.assert_array_equal(out["phi"].cpu().numpy(), ref["phi"])
+    np.testing.assert_array_equal(out["count"].cpu().numpy(), ref["count"])
+    assert out["q_in"] == ref["q_in"] and out["q_out"] == ref["q_out"]
+    assert out["n_psi"] == ref["n_psi"] and out["n_phi"] == ref["n_phi"]
+    np.testing.assert_array_equal(out["c_in"].cpu().numpy(), ref["c_in"])
+    np.testing.assert_array_equal(out["c_out"].cpu().numpy(), ref["c_out"])
+
+
+def test_calibration_errors(lib):
+    n_p, M = 100, 10
+    S = np.full((n_p, M), 5.0)
+    with pytest.raises(lib.CrError) as ei:
+        lib.calibrate(colmajor(S), dev(np.zeros(n_p)), dev(np.ones(n_p)), 1.0, 0.9)
+    assert ei.value.name == "CR_ERR_EMPTY_SAMPLE"
+    v = np.ones(n_p)
+    v[7] = 0.0
+    with pytest.raises(lib.CrError) as ei:
+        lib.calibrate(colmajor(np.zeros((n_p, M))), dev(np.zeros(n_p)), dev(v), 1.0, 0.9)
+    assert ei.value.name == "CR_ERR_NONPOS_MSPE"
+
+
+def test_krige_correct_matches_oracle(lib):
+    rng = np.random.default_rng(2)
+    n_p, n_o, M = 300, 200, 70
+    W = rng.standard_normal((n_o, n_p))
+    y = rng.standard_normal(n_o)
+    Y = rng.standard_normal((n_p + n_o, M))
+    S = lib.krige_correct(colmajor(W), dev(y), colmajor(Y), n_p, n_o).cpu().numpy()
+    So = oracle.conditional_correction(W, y, Y[:n_p], Y[n_p:])
+    assert relf(S, So) <= 1e-14
+
+
+def test_not_spd_reports_column(lib):
+    # points 0 and 1 coincide and there is no nugget: V_00 = V_01 = V_11 = 1 exactly, so the
+    # second pivot is 1 - 1 * 1 = 0 exactly and column 2 (1-based) is reported
+    xy = inputgen.morton_sorted(inputgen.uniform_locations(256, 3))
+    xy[1] = xy[0]
+    V = lib.TileMat(256, 128)
+    lib.cov_build(V, dev(xy), "matern", 1.0, 0.1, 0.5, nugget=0.0)
+    lib.precision_map(V, amp=False)
+    info = lib.potrf_adaptive(V)
+    assert info == 2
+    V.close()
