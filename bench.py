@@ -1,0 +1,356 @@
+#!/usr/bin/env python
+"""Benchmark of the conditional-simulation hot path on GB300.
+
+One step = one pass of the whole path over the headline workload (n = 32768 uniform sites,
+exponential Matern range 0.03, nugget 1e-4, tile 512, M = 2048 simulations, fixedacc 1e-4):
+covariance tiles + statistics, precision map + scale, adaptive Cholesky, normal draws fused
+with the mixed-precision TRMM, calibration scan + quantiles + regions.  Inputs (locations,
+zhat, v) are resident in HBM before the timed region; the tile matrix (>1 GB) is far larger
+than L2, so no flush is needed between steps.
+
+Metric (per the paper's own TRMM measure extended to the factorisation): Cholesky+TRMM
+TFLOP/s = (n^3/3 + n^2/2 + n/6 + n^2 M) / time; `value` divides by the whole step time.
+The JSON line also reports the Cholesky+TRMM-only rate, its multiple of the measured FP64
+peak, the fraction of the precision-weighted peak, and simulations per second.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+With N > 1 (torchrun) each rank runs an independent replica (the path is single-GPU).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import inputgen  # noqa: E402
+
+FP64_PEAK_TFLOPS = 1.19       # measured DFMA rate on this GB300 pool (profiles/fp64_peak_microbench.md)
+WORKLOAD = inputgen.WORKLOADS["c"]
+SEED_Z = 12345
+
+
+def flops(n, M):
+    return n ** 3 / 3.0 + n ** 2 / 2.0 + n / 6.0, float(n) ** 2 * M
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        return {"hbm": p["hbm_gbs"], "bf16": p["bf16_tflops"], "bf16_sus": p.get("bf16_tflops_sustained", p["bf16_tflops"]),
+                "src": "measured"}
+    return {"hbm": 6800.0, "bf16": 1900.0, "bf16_sus": 1700.0, "src": "fallback"}
+
+
+def attributed_flops(pmap: np.ndarray, nb: int, n: int, M: int):
+    """Algorithmic flops by the arithmetic that executes them (FP64 units, FP16 tensor
+    MMAs, FP32-class 3-MMA FP16 splits) for the left-looking schedule of the library."""
+    nt = pmap.shape[0]
+    f = {"fp64": 0.0, "fp32": 0.0, "fp16": 0.0}
+    name = {0: "fp64", 1: "fp32", 2: "fp16"}
+    b3 = float(nb) ** 3
+    for j in range(nt):
+        f["fp64"] += b3 / 3.0                       # diagonal factor
+        for i in range(j, nt):
+            for k in range(j):
+                pc = max(pmap[i, j], pmap[i, k], pmap[j, k])
+                f[name[pc]] += b3 if i == j else 2.0 * b3   # SYRK / GEMM
+            if i > j:
+                f[name[pmap[i, j]]] += b3           # triangular solve at the tile's class
+    trmm = {"fp16": float(n) ** 2 * M - n * nb * M, "fp32": float(n) * nb * M}   # off-diagonal / diagonal
+    return f, trmm
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.rows = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", gpu_id, f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([x.strip() for x in line.split(",")])
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in self.rows:
+            try:
+                sm.append(float(r[0]))
+                mx.append(float(r[1]))
+            except (ValueError, IndexError):
+                continue
+            for k, nm in enumerate(names):
+                if len(r) > 4 + k and r[4 + k].lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def oracle_sample(n_s: int, M_s: int):
+    """The oracle as it stands on the leading n_s sites of the workload: covariance,
+    unblocked Cholesky, simulation, calibration.  Returns (seconds, flops)."""
+    import oracle
+    w = WORKLOAD
+    xy = inputgen.workload_locations(w)[:n_s]
+    Z = inputgen.standard_normals(n_s, M_s, SEED_Z)
+    t0 = time.perf_counter()
+    V = oracle.covariance_matrix(xy, w.family, w.sigma2, w.beta, w.nu, w.nugget)
+    L = oracle.cholesky_lower(V)
+    Y = oracle.simulate(L, Z)
+    oracle.calibrate(Y, np.zeros(n_s), np.diag(V).copy(), w.u, w.level)
+    dt = time.perf_counter() - t0
+    fc, ft = flops(n_s, M_s)
+    return dt, fc + ft
+
+
+def cpu_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        nums = [d.get("num_threads", 1) for d in threadpool_info()]
+        if nums:
+            return int(max(nums))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    n_s, M_s = 2048, 2048
+    for _ in range(args.warmup):
+        oracle_sample(n_s, M_s)
+    times, fl = [], 0.0
+    for _ in range(args.steps):
+        dt, fl = oracle_sample(n_s, M_s)
+        times.append(dt)
+    ms = 1e3 * float(np.mean(times))
+    val = fl / (ms / 1e3) / 1e12
+    unit = "TFLOP/s"
+    line = {"metric": "Cholesky+TRMM TFLOP/s", "value": val, "unit": unit, "impl": "reference", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"oracle on the leading {n_s} sites of {WORKLOAD.name}", "n": n_s, "M": M_s},
+            "cpu_baseline": {"value": val, "unit": unit, "cores": cpu_threads(), "kind": "oracle",
+                             "sample": f"leading {n_s} of {WORKLOAD.n} sites, M={M_s}, one full oracle pass per step"},
+            "e2e": {"value": val, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- GPU path
+def run_ours(args, world, rank, local):
+    import torch
+    import mixed_precision_dense_mat_gb300 as cr
+    torch.cuda.set_device(local)
+    cr.load()
+    w = WORKLOAD
+    n, nb, M = w.n, w.nb, w.M
+    dev = torch.device("cuda", local)
+    xy_h = inputgen.workload_locations(w)
+    xy = torch.from_numpy(xy_h).to(dev)
+    V = cr.TileMat(n, nb)
+    Y = cr.colmajor_empty(n, M, torch.float64)
+    zhat = torch.zeros(n, dtype=torch.float64, device=dev)              # no observations: zhat = 0
+    vvec = torch.full((n,), w.sigma2 + w.nugget, dtype=torch.float64, device=dev)   # v_i = V_ii
+    stream = torch.cuda.current_stream()
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    info_box = {}
+
+    def step(seed, e):
+        e[0].record(stream)
+        cr.cov_build(V, xy, w.family, w.sigma2, w.beta, w.nu, nugget=w.nugget)
+        e[1].record(stream)
+        pmap, info = cr.precision_map(V, amp=True, fixedacc=w.fixedacc)
+        e[2].record(stream)
+        info_box["map"], info_box["info"] = pmap, info
+        assert cr.potrf_adaptive(V) == 0
+        e[3].record(stream)
+        cr.trmm_sim(V, None, M, seed=seed, out=Y, flags=cr.CR_TRMM_GENERATE)
+        e[4].record(stream)
+        out = cr.calibrate(Y, zhat, vvec, w.u, w.level)
+        e[5].record(stream)
+        return out
+
+    for q in range(args.warmup):
+        step(SEED_Z + q, [ev() for _ in range(6)])
+    torch.cuda.synchronize()
+
+    gpu_id = os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local] if "CUDA_VISIBLE_DEVICES" in os.environ else str(local)
+    clocks = ClockSampler(gpu_id)
+    barrier(world)
+    torch.cuda.synchronize()
+    l0 = cr.kernel_launches()
+    evs = [[ev() for _ in range(6)] for _ in range(args.steps)]
+    t_start, t_end = ev(), ev()
+    wall0 = time.perf_counter()
+    t_start.record(stream)
+    for q in range(args.steps):
+        step(SEED_Z + 100 + q, evs[q])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - wall0
+    launches = cr.kernel_launches() - l0
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    total_ms = max_over_ranks(total_ms, world)
+    stages = ["cov_build", "precision_map", "potrf", "rng_trmm", "calibrate"]
+    st = {s: float(np.mean([evs[q][k].elapsed_time(evs[q][k + 1]) for q in range(args.steps)])) for k, s in enumerate(stages)}
+    ms = total_ms / args.steps
+    fc, ft = flops(n, M)
+    value = world * (fc + ft) / (ms / 1e3) / 1e12
+    ct_ms = st["potrf"] + st["rng_trmm"]
+    ct_tflops = (fc + ft) / (ct_ms / 1e3) / 1e12
+
+    pk = peaks()
+    pmap, info = info_box["map"], info_box["info"]
+    fch, ftr = attributed_flops(pmap.copy(), nb, n, M)
+    p16 = pk["bf16_sus"] * 1e12
+    peak_of = {"fp64": FP64_PEAK_TFLOPS * 1e12, "fp16": p16, "fp32": p16 / 3.0}
+    t_star = sum(fch[k] / peak_of[k] for k in fch) + sum(ftr[k] / peak_of[k] for k in ftr)
+    frac_weighted = t_star / (ct_ms / 1e3)
+
+    # roofline of the simulation multiply (TRMM), timed live: one launch per step
+    trmm_flops = 2.0 * (ftr["fp16"] + 2.0 * ftr["fp32"]) / 2.0   # algorithmic n^2 M (diagonal counted once)
+    trmm_flops = float(n) ** 2 * M
+    trmm_ms = st["rng_trmm"]
+    roof = {"kernel": "k_tc (TRMM mode) + fused normal draws", "bound": "tensor",
+            "achieved": trmm_flops / (trmm_ms / 1e3) / 1e12, "peak": pk["bf16"], "unit": "TFLOP/s",
+            "frac": None, "traffic": None, "peak_source": f"{pk['src']} bf16 burst (FP16 runs at the bf16 rate)"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+
+    # end to end through the public API with host buffers: H2D of the locations, D2H of
+    # the regions and counts, every step
+    xy_pin = torch.from_numpy(xy_h).pin_memory()
+    cin_h = torch.empty(n, dtype=torch.uint8).pin_memory()
+    cout_h = torch.empty(n, dtype=torch.uint8).pin_memory()
+    cnt_h = torch.empty(n, dtype=torch.int32).pin_memory()
+    e2e_steps = max(1, min(args.steps, 3))
+    barrier(world)
+    torch.cuda.synchronize()
+    a, b = ev(), ev()
+    a.record(stream)
+    for q in range(e2e_steps):
+        xy.copy_(xy_pin, non_blocking=True)
+        out = step(SEED_Z + 200 + q, [ev() for _ in range(6)])
+        cin_h.copy_(out["c_in"], non_blocking=True)
+        cout_h.copy_(out["c_out"], non_blocking=True)
+        cnt_h.copy_(out["count"], non_blocking=True)
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(a.elapsed_time(b) / e2e_steps, world)
+    e2e_val = world * (fc + ft) / (e2e_ms / 1e3) / 1e12
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n_s, M_s = 3072, 2048
+        dt, fl = oracle_sample(n_s, M_s)
+        cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
+               "sample": f"one oracle pass (covariance, unblocked Cholesky, simulation, calibration) on the leading "
+                         f"{n_s} of {n} sites with M={M_s}: {dt:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": "Cholesky+TRMM TFLOP/s", "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f16/f32/f64 adaptive", "data": "synthetic",
+            "config": {"workload": w.name, "n": n, "nb": nb, "M": M, "fixedacc": w.fixedacc, "range": w.beta,
+                       "nu": w.nu, "nugget": w.nugget, "l2": "working set (tiles > 1 GB) larger than L2; no flush",
+                       "parallelism": f"replicas x{world}"},
+            "chol_trmm": {"tflops": ct_tflops, "ms": ct_ms, "x_fp64_peak": ct_tflops / FP64_PEAK_TFLOPS,
+                          "frac_weighted_peak": frac_weighted, "weighted_peak_ms": t_star * 1e3,
+                          "flops_by_precision": {k: fch[k] + ftr.get(k, 0.0) for k in fch}},
+            "sims_per_s": world * M / (st["rng_trmm"] / 1e3),
+            "stages_ms": st,
+            "precision_map": {"n_fp64": info["n_fp64"], "n_fp32": info["n_fp32"], "n_fp16": info["n_fp16"],
+                              "s": info["s"], "check1": info["check1"], "check2": info["check2"]},
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": int(xy_h.nbytes),
+                    "d2h_bytes_per_step": int(n * (1 + 1 + 4))},
+            "gpu_launches": launches,
+            "clocks": clk,
+            "wall_s_timed": wall,
+        }
+        print(json.dumps(line), flush=True)
+    V.close()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = dist_setup()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank)
+        else:
+            run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

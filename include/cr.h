@@ -95,6 +95,10 @@ const char* cr_status_str(cr_status code);
 const char* cr_last_error_detail(void);
 cr_status cr_version(int* major, int* minor);
 
+/* Number of CUDA kernels this library has launched in the process so far (all devices);
+ * *count receives the running total.  Host-side counter, no device work. */
+cr_status cr_kernel_launches(uint64_t* count);
+
 /* A symmetric n x n matrix stored as its lower tiles (i >= j) of nb x nb entries.
  * NT = ceil(n / nb) tile rows; rows and columns past n are padding and behave like the
  * identity.  nb must be a multiple of 128 with 128 <= nb <= 1024.  The handle owns its

@@ -77,6 +77,7 @@ _SIGNATURES = {
     "cr_status_str": (ctypes.c_char_p, [_I]),
     "cr_last_error_detail": (ctypes.c_char_p, []),
     "cr_version": (_I, [ctypes.POINTER(_I), ctypes.POINTER(_I)]),
+    "cr_kernel_launches": (_I, [ctypes.POINTER(_U64)]),
     "cr_tilemat_create": (_I, [_I, _I, ctypes.POINTER(_P)]),
     "cr_tilemat_destroy": (_I, [_P]),
     "cr_tilemat_info": (_I, [_P, ctypes.POINTER(_I), ctypes.POINTER(_I), ctypes.POINTER(_I)]),
@@ -147,6 +148,14 @@ def as_colmajor(t):
     if t.stride(0) != 1:
         t = t.T.contiguous().T
     return t, max(1, t.stride(1))
+
+
+def kernel_launches() -> int:
+    """cr_kernel_launches: kernels launched by the library in this process so far."""
+    load()
+    c = _U64(0)
+    _check(_lib.cr_kernel_launches(ctypes.byref(c)))
+    return c.value
 
 
 class TileMat:

@@ -1,6 +1,7 @@
 // Status codes, error reporting, tile-matrix lifetime and TMA descriptor creation.
 #include <stdio.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -8,6 +9,9 @@
 namespace cr {
 
 static thread_local std::string g_detail;
+static std::atomic<uint64_t> g_launches{0};
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 void set_error(const std::string& msg) { g_detail = msg; }
 
@@ -108,6 +112,12 @@ extern "C" const char* cr_last_error_detail(void) { return g_detail.c_str(); }
 extern "C" cr_status cr_version(int* major, int* minor) {
   if (major) *major = 0;
   if (minor) *minor = 1;
+  return CR_OK;
+}
+
+extern "C" cr_status cr_kernel_launches(uint64_t* count) {
+  if (!count) return fail(CR_ERR_ARG, "cr_kernel_launches: NULL");
+  *count = g_launches.load(std::memory_order_relaxed);
   return CR_OK;
 }
 

@@ -24,8 +24,12 @@ cr_status cuda_fail(cudaError_t e, const char* what);
     if (e__ != cudaSuccess) return ::cr::cuda_fail(e__, #call);     \
   } while (0)
 
+void count_launch();
+
+// Every kernel launch is followed by this check, which also counts the launch.
 #define CR_CHECK_LAUNCH(what)                                       \
   do {                                                              \
+    ::cr::count_launch();                                           \
     cudaError_t e__ = cudaGetLastError();                           \
     if (e__ != cudaSuccess) return ::cr::cuda_fail(e__, what);      \
   } while (0)
