@@ -197,6 +197,29 @@ cr_status cr_calibrate(const double* d_S, int lds, int n_p, int M, const double*
                        uint8_t* d_cout, int32_t* d_count, double* d_psi, double* d_phi,
                        cr_calib_info* out, cr_stream stream);
 
+/* Calibration without any allocation.  The paper has no counterpart to this entry point:
+ * it exists for callers that cannot allocate device memory themselves, for example code
+ * running under a memory pool or a graph-capture regime that forbids cudaMalloc/cudaFree,
+ * or embedders that must keep the device footprint fixed after start-up.  It computes
+ * exactly what cr_calibrate computes, with the same arguments and outputs, but its device
+ * scratch (t, psi, phi and the per-block partials of the scan) lives in a fixed array
+ * inside the library (CR_NOALLOC_SCRATCH_BYTES, held by every device that loads the
+ * library until the process exits) and the host-side quantile samples in a fixed host
+ * array; it never calls cudaMalloc, cudaFree or any allocating routine.
+ * Limits: M <= CR_NOALLOC_MAX_M and 8 n_p + 16 M + 16 ceil(n_p / 2048) M + 1536 bytes
+ * <= CR_NOALLOC_SCRATCH_BYTES; larger problems return CR_ERR_ARG (use cr_calibrate).
+ * The first call on a device looks up the array's device address (once per device, with
+ * that device current), so make the first call before any stream capture.  All calls
+ * share the one array and the one host buffer: calls that overlap (two streams, two host
+ * threads, or two devices at once) race and must be serialised by the caller.
+ * Synchronises the stream. */
+#define CR_NOALLOC_SCRATCH_BYTES (8u << 20)
+#define CR_NOALLOC_MAX_M 65536
+cr_status cr_calibrate_noalloc(const double* d_S, int lds, int n_p, int M, const double* d_zhat,
+                               const double* d_v, double u, double level, uint8_t* d_cin,
+                               uint8_t* d_cout, int32_t* d_count, double* d_psi, double* d_phi,
+                               cr_calib_info* out, cr_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

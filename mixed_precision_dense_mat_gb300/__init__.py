@@ -91,6 +91,8 @@ _SIGNATURES = {
     "cr_krige": (_I, [_P, _P, _P, _P, _P, _I, _P, _P, _P, ctypes.POINTER(_I)]),
     "cr_krige_correct": (_I, [_P, _I, _P, _P, _I, _I, _I, _I, _P, _I, _P]),
     "cr_calibrate": (_I, [_P, _I, _I, _I, _P, _P, _D, _D, _P, _P, _P, _P, _P, ctypes.POINTER(CalibInfo), _P]),
+    "cr_calibrate_noalloc": (_I, [_P, _I, _I, _I, _P, _P, _D, _D, _P, _P, _P, _P, _P, ctypes.POINTER(CalibInfo),
+                                  _P]),
 }
 
 

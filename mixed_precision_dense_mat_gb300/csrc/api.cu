@@ -9,18 +9,31 @@
 namespace cr {
 
 static thread_local std::string g_detail;
+// Message set without allocating (a string with static storage), used by the allocation-free
+// entry point; any other error clears it.
+static thread_local const char* g_literal = nullptr;
 static std::atomic<uint64_t> g_launches{0};
 
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
-void set_error(const std::string& msg) { g_detail = msg; }
+void set_error(const std::string& msg) {
+  g_literal = nullptr;
+  g_detail = msg;
+}
+
+cr_status fail_literal(cr_status code, const char* msg) {
+  g_literal = msg;
+  return code;
+}
 
 cr_status fail(cr_status code, const std::string& msg) {
+  g_literal = nullptr;
   g_detail = msg;
   return code;
 }
 
 cr_status cuda_fail(cudaError_t e, const char* what) {
+  g_literal = nullptr;
   g_detail = std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
   return e == cudaErrorMemoryAllocation ? CR_ERR_NOMEM : CR_ERR_CUDA;
 }
@@ -107,7 +120,7 @@ extern "C" const char* cr_status_str(cr_status code) {
   }
 }
 
-extern "C" const char* cr_last_error_detail(void) { return g_detail.c_str(); }
+extern "C" const char* cr_last_error_detail(void) { return g_literal ? g_literal : g_detail.c_str(); }
 
 extern "C" cr_status cr_version(int* major, int* minor) {
   if (major) *major = 0;

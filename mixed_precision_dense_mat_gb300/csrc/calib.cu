@@ -203,3 +203,126 @@ extern "C" cr_status cr_calibrate(const double* d_S, int lds, int n_p, int M, co
   CR_TRY(ensure_scratch(n_p, M));
   return calibrate_core(d_S, lds, n_p, M, d_zhat, d_v, u, level, d_cin, d_cout, d_count, d_psi, d_phi, out, stream, g_sc);
 }
+
+// ---------------------------------------------------------------------------------------
+// Allocation-free calibration, for callers that cannot allocate device memory (a memory
+// pool or capture regime that forbids cudaMalloc/cudaFree, or an embedder whose device
+// footprint must stay fixed after start-up).  Same kernels and results as cr_calibrate;
+// the scratch is a fixed array of this file instead of library-managed allocations.
+namespace cr {
+
+cr_status fail_literal(cr_status code, const char* msg);
+
+namespace {
+
+// Device scratch shared by every call on a device (held until the process exits).  In host
+// code this name only identifies the symbol: its device address is looked up once per
+// device with cudaGetSymbolAddress and passed to the kernels as a plain pointer.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[CR_NOALLOC_SCRATCH_BYTES];
+
+// Host copies of psi and phi for the quantiles (fixed, so the host side allocates nothing).
+static double g_noalloc_psi[CR_NOALLOC_MAX_M];
+static double g_noalloc_phi[CR_NOALLOC_MAX_M];
+
+constexpr int kNoallocMaxDevices = 64;
+static unsigned char* g_noalloc_dev[kNoallocMaxDevices];   // device address per device
+static std::mutex g_noalloc_mu;
+
+size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Q_p of the sorted prefix a[0, N) (N >= 1), same rule as empirical_quantile.
+double quantile_sorted(const double* a, long N, double p) {
+  long k = (long)ceil(p * (double)N - 1e-9);
+  k = std::max(1L, std::min(N, k));
+  return a[k - 1];
+}
+
+}  // namespace
+}  // namespace cr
+
+extern "C" cr_status cr_calibrate_noalloc(const double* d_S, int lds, int n_p, int M, const double* d_zhat,
+                                          const double* d_v, double u, double level, uint8_t* d_cin, uint8_t* d_cout,
+                                          int32_t* d_count, double* d_psi, double* d_phi, cr_calib_info* out,
+                                          cr_stream stream) {
+  if (!d_S || !d_zhat || !d_v || !d_cin || !d_cout || n_p <= 0 || M <= 0 || lds < n_p || !(level > 0.0 && level < 1.0))
+    return fail_literal(CR_ERR_ARG, "cr_calibrate_noalloc: argument");
+  if (M > CR_NOALLOC_MAX_M) return fail_literal(CR_ERR_ARG, "cr_calibrate_noalloc: M exceeds CR_NOALLOC_MAX_M");
+  const size_t nrb = ((size_t)n_p + SCAN_ROWS - 1) / SCAN_ROWS;
+  const size_t need = 8 * (size_t)n_p + 16 * (size_t)M + 16 * nrb * (size_t)M + 1536;
+  if (need > CR_NOALLOC_SCRATCH_BYTES)
+    return fail_literal(CR_ERR_ARG, "cr_calibrate_noalloc: problem needs more than CR_NOALLOC_SCRATCH_BYTES of scratch");
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_literal(CR_ERR_CUDA, cudaGetErrorName(e));
+  if (dev < 0 || dev >= kNoallocMaxDevices) return fail_literal(CR_ERR_ARG, "cr_calibrate_noalloc: device index too large");
+  if (!g_noalloc_dev[dev]) {   // once per device, with that device current
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return fail_literal(CR_ERR_CUDA, cudaGetErrorName(e));
+    g_noalloc_dev[dev] = static_cast<unsigned char*>(p);
+  }
+  // carve the array: t | psi | phi | psi_part | phi_part | flag
+  unsigned char* base = g_noalloc_dev[dev];
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    unsigned char* q = base + off;
+    off += round256(bytes);
+    return q;
+  };
+  double* t = reinterpret_cast<double*>(take(8 * (size_t)n_p));
+  double* psi = reinterpret_cast<double*>(take(8 * (size_t)M));
+  double* phi = reinterpret_cast<double*>(take(8 * (size_t)M));
+  double* psi_part = reinterpret_cast<double*>(take(8 * nrb * M));
+  double* phi_part = reinterpret_cast<double*>(take(8 * nrb * M));
+  int* bad = reinterpret_cast<int*>(take(sizeof(int)));
+
+  // The array keeps the previous call's contents: clear what is accumulated (the MSPE flag
+  // and the caller's counts); t, psi, phi and the partials are fully overwritten.
+#define NA_CUDA(call)                                                 \
+  do {                                                                \
+    cudaError_t e__ = (call);                                         \
+    if (e__ != cudaSuccess) return fail_literal(CR_ERR_CUDA, cudaGetErrorName(e__)); \
+  } while (0)
+  NA_CUDA(cudaMemsetAsync(bad, 0, sizeof(int), stream));
+  if (d_count) NA_CUDA(cudaMemsetAsync(d_count, 0, (size_t)n_p * sizeof(int32_t), stream));
+  k_tstat<<<std::min(1024, (n_p + 255) / 256), 256, 0, stream>>>(d_zhat, d_v, u, n_p, t, bad);
+  count_launch();
+  NA_CUDA(cudaGetLastError());
+  dim3 grid((unsigned)nrb, (M + SCAN_COLS - 1) / SCAN_COLS);
+  k_scan<<<grid, SCAN_THREADS, 0, stream>>>(d_S, lds, n_p, M, t, u, psi_part, phi_part, d_count);
+  count_launch();
+  NA_CUDA(cudaGetLastError());
+  k_scan_reduce<<<std::min(1024, (M + 255) / 256), 256, 0, stream>>>(psi_part, phi_part, (int)nrb, M, psi, phi);
+  count_launch();
+  NA_CUDA(cudaGetLastError());
+  int h_bad = 0;
+  NA_CUDA(cudaMemcpyAsync(g_noalloc_psi, psi, (size_t)M * sizeof(double), cudaMemcpyDeviceToHost, stream));
+  NA_CUDA(cudaMemcpyAsync(g_noalloc_phi, phi, (size_t)M * sizeof(double), cudaMemcpyDeviceToHost, stream));
+  NA_CUDA(cudaMemcpyAsync(&h_bad, bad, sizeof(int), cudaMemcpyDeviceToHost, stream));
+  if (d_psi) NA_CUDA(cudaMemcpyAsync(d_psi, psi, (size_t)M * sizeof(double), cudaMemcpyDeviceToDevice, stream));
+  if (d_phi) NA_CUDA(cudaMemcpyAsync(d_phi, phi, (size_t)M * sizeof(double), cudaMemcpyDeviceToDevice, stream));
+  NA_CUDA(cudaStreamSynchronize(stream));
+  if (h_bad) return fail_literal(CR_ERR_NONPOS_MSPE, "cr_calibrate_noalloc: some v_i <= 0");
+  long n_psi = 0, n_phi = 0;   // drop the empty-set sentinels in place
+  for (int j = 0; j < M; ++j) {
+    if (g_noalloc_psi[j] != INFINITY) g_noalloc_psi[n_psi++] = g_noalloc_psi[j];
+    if (g_noalloc_phi[j] != -INFINITY) g_noalloc_phi[n_phi++] = g_noalloc_phi[j];
+  }
+  cr_calib_info info{};
+  info.n_psi = (int)n_psi;
+  info.n_phi = (int)n_phi;
+  if (out) *out = info;
+  if (n_psi == 0 || n_phi == 0) return fail_literal(CR_ERR_EMPTY_SAMPLE, "cr_calibrate_noalloc: empty psi or phi sample");
+  std::sort(g_noalloc_psi, g_noalloc_psi + n_psi);
+  std::sort(g_noalloc_phi, g_noalloc_phi + n_phi);
+  const double alpha = 1.0 - level;
+  info.q_out = quantile_sorted(g_noalloc_psi, n_psi, alpha);
+  info.q_in = quantile_sorted(g_noalloc_phi, n_phi, 1.0 - alpha);
+  if (out) *out = info;
+  k_regions<<<std::min(1024, (n_p + 255) / 256), 256, 0, stream>>>(t, n_p, info.q_in, info.q_out, d_cin, d_cout);
+  count_launch();
+  NA_CUDA(cudaGetLastError());
+#undef NA_CUDA
+  return CR_OK;
+}
