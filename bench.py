@@ -336,7 +336,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--n", type=int, default=0, help="profiling only: smaller n of the same workload family")
     args = ap.parse_args()
+    global WORKLOAD
+    if args.n:
+        import dataclasses
+        WORKLOAD = dataclasses.replace(WORKLOAD, n_pred=args.n, name=WORKLOAD.name.replace("n=32768", f"n={args.n}"))
     world, rank, local = dist_setup()
     if world > 1:
         import torch.distributed as dist

@@ -93,7 +93,7 @@ static void dfree(T*& p) {
 
 cr_status free_class_storage(cr_tilemat V) {
   dfree(V->d_cls); dfree(V->d_i64); dfree(V->d_i32); dfree(V->d_hi16); dfree(V->d_lo16);
-  dfree(V->pool64); dfree(V->pool32); dfree(V->pool16); dfree(V->ws64);
+  dfree(V->pool64); dfree(V->pool32); dfree(V->pool16); dfree(V->ws64); dfree(V->w32);
   V->mapped = false;
   V->factored = false;
   return CR_OK;
@@ -167,8 +167,10 @@ extern "C" cr_status cr_tilemat_destroy(cr_tilemat V) {
   cudaSetDevice(V->device);
   cudaDeviceSynchronize();
   free_class_storage(V);
-  dfree(V->b16); dfree(V->bnorm_part);
+  dfree(V->b16); dfree(V->bnorm_part); dfree(V->diag_tasks); dfree(V->diag_flags); dfree(V->minv_part);
   dfree(V->master); dfree(V->stat_part); dfree(V->stats); dfree(V->minv); dfree(V->scratch64); dfree(V->d_status);
+  if (V->s_hi) cudaStreamDestroy(V->s_hi);
+  if (V->s_lo) cudaStreamDestroy(V->s_lo);
   delete V;
   return CR_OK;
 }

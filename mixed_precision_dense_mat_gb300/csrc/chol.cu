@@ -1,20 +1,26 @@
-// Adaptive mixed-precision tile Cholesky driver (left-looking, one tile column at a time).
+// Adaptive mixed-precision tile Cholesky driver (left-looking by tile column, with lookahead).
 //
 // "Mixed-Precision GPU Acceleration for Confidence Regions of Spatial Excursion Sets",
 // Section IV-B and Alg.2 step 12: L_s = chol(s^2 V) with the tile precisions of the map;
-// diagonal tiles FP64.  For tile column j:
-//   1. FP64 products (destination and both operands FP64) on the FP64 units;
-//   2. every other product on the tensor cores (FP16, or FP16 high/low parts for FP32-class
-//      accuracy), accumulated in FP32 and applied to the destination in its own precision;
-//   3. the FP64 diagonal tile is factored together with its inverse (recursive 2 x 2 blocks
-//      down to 64 x 64, the GEMMs spread over many SMs);
-//   4. the off-diagonal tiles of the column are solved, L_ij = A_ij L_jj^-T, as a product with
-//      the inverse factor, in the tile's precision.
-// The schedule depends only on the map, so it is built once on the host (all job lists are
-// uploaded in one copy) and then replayed in stream order.
+// diagonal tiles FP64.  For tile column j the update A_ij -= sum_{k<j} L_ik L_jk^T is split:
+//   OLD(j)  terms k < j-1, on a low-priority stream: FP64 products on the FP64 units, all
+//           others on the tensor cores (FP16 MMAs, or FP16 high/low parts for FP32-class
+//           accuracy) accumulated in FP32 into an intermediate;
+//   NEW(j)  term k = j-1, on a high-priority stream, finishing the solve inputs;
+// then, on the high-priority stream, the FP64 diagonal tile is factored together with its
+// inverse by the on-device dataflow executor (diag.cu), and the off-diagonal tiles are
+// solved, L_ij = A_ij L_jj^-T, as a product with that inverse in the tile's precision.
+// OLD(j+1) needs only columns < j, so it runs on the tensor cores while column j's FP64
+// diagonal factorisation (the critical path) runs on the FP64 units.  Work buffers are
+// double-buffered by column parity.  The schedule depends only on the map: all job lists
+// are built on the host and uploaded in one copy, then replayed with events between the
+// two streams.  This replaces the paper's PaRSEC task runtime on one GPU.
+#include <stdlib.h>
+
 #include <functional>
 
 #include "common.cuh"
+#include "diag.cuh"
 #include "fp64.cuh"
 #include "tc.cuh"
 
@@ -31,7 +37,15 @@ __global__ void k_zero_upper(double* A, int nb) {
 
 namespace {
 
-using Op = std::function<cr_status(cudaStream_t, const DJob*, const DPair*)>;
+struct Exec {
+  cudaStream_t hi, lo;
+  const DJob* dj;
+  const DPair* dp;
+  std::vector<cudaEvent_t> ev;   // per column: [2j] solves done (hi), [2j+1] older updates done (lo)
+  cudaEvent_t start;
+};
+
+using Op = std::function<cr_status(Exec&)>;
 
 struct Plan {
   std::vector<DJob> jobs;
@@ -42,11 +56,11 @@ struct Plan {
     pairs.push_back(DPair{A, B, sAm, sAk, sBn, sBk, K});
     return (int)pairs.size() - 1;
   }
-  void dgemm(int block, const std::vector<DJob>& js) {
+  void dgemm(int block, const std::vector<DJob>& js, bool on_lo) {
     if (js.empty()) return;
     const int off = (int)jobs.size(), cnt = (int)js.size();
     jobs.insert(jobs.end(), js.begin(), js.end());
-    ops.push_back([=](cudaStream_t s, const DJob* dj, const DPair* dp) -> cr_status { return dgemm_launch(block, dj + off, dp, cnt, s); });
+    ops.push_back([=](Exec& x) -> cr_status { return dgemm_launch(block, x.dj + off, x.dp, cnt, on_lo ? x.lo : x.hi); });
   }
 };
 
@@ -58,77 +72,23 @@ DJob job(double* C, int sCm, int sCn, int m, int n, int pbeg, int pcnt, double a
   return j;
 }
 
-// Cholesky and inverse of the n x n diagonal block at offset `off` of the FP64 tile A
-// (row-major, ld nb); inverse into M (same layout), temporaries in T.
-void plan_chol_inv(Plan& P, cr_tilemat V, double* A, double* M, double* T, int off, int n, int gcol0) {
-  const int nb = V->nb;
-  int* status = V->d_status;
-  if (n == 64) {
-    double* a = A + (size_t)off * nb + off;
-    double* m = M + (size_t)off * nb + off;
-    const int g = gcol0 + off;
-    P.ops.push_back([=](cudaStream_t s, const DJob*, const DPair*) -> cr_status { return potrf64_base_launch(a, nb, m, nb, g, status, s); });
-    return;
-  }
-  const int h = n / 2;
-  const int bs = 16;
-  const int nbk = h / bs;
-  plan_chol_inv(P, V, A, M, T, off, h, gcol0);
-  double* A21 = A + (size_t)(off + h) * nb + off;
-  double* A22 = A + (size_t)(off + h) * nb + off + h;
-  double* M11 = M + (size_t)off * nb + off;
-  double* M21 = M + (size_t)(off + h) * nb + off;
-  double* M22 = M + (size_t)(off + h) * nb + off + h;
-  double* U = T + h;   // second h x h scratch block
-  std::vector<DJob> js;
-  // T = A21 M11^T
-  int p = P.add_pair(A21, M11, nb, 1, nb, 1, h);
-  for (int bi = 0; bi < nbk; ++bi)
-    for (int bj = 0; bj < nbk; ++bj)
-      js.push_back(job(T + (size_t)bi * bs * nb + bj * bs, nb, 1, bs, bs, p, 1, 1.0, 0.0, bi * bs, bj * bs, h));
-  P.dgemm(bs, js);
-  js.clear();
-  // A22 -= T T^T (lower blocks)
-  p = P.add_pair(T, T, nb, 1, nb, 1, h);
-  for (int bi = 0; bi < nbk; ++bi)
-    for (int bj = 0; bj <= bi; ++bj)
-      js.push_back(job(A22 + (size_t)bi * bs * nb + bj * bs, nb, 1, bs, bs, p, 1, -1.0, 1.0, bi * bs, bj * bs, h));
-  P.dgemm(bs, js);
-  js.clear();
-  // A21 = T
-  P.ops.push_back([=](cudaStream_t s, const DJob*, const DPair*) -> cr_status {
-    CR_CUDA(cudaMemcpy2DAsync(A21, nb * sizeof(double), T, nb * sizeof(double), h * sizeof(double), h,
-                              cudaMemcpyDeviceToDevice, s));
-    return CR_OK;
-  });
-  plan_chol_inv(P, V, A, M, T, off + h, h, gcol0);
-  // U = L21 M11 (B(n, k) = M11[k][n])
-  p = P.add_pair(A21, M11, nb, 1, 1, nb, h);
-  for (int bi = 0; bi < nbk; ++bi)
-    for (int bj = 0; bj < nbk; ++bj)
-      js.push_back(job(U + (size_t)bi * bs * nb + bj * bs, nb, 1, bs, bs, p, 1, 1.0, 0.0, bi * bs, bj * bs, h));
-  P.dgemm(bs, js);
-  js.clear();
-  // M21 = -M22 U (B(n, k) = U[k][n])
-  p = P.add_pair(M22, U, nb, 1, 1, nb, h);
-  for (int bi = 0; bi < nbk; ++bi)
-    for (int bj = 0; bj < nbk; ++bj)
-      js.push_back(job(M21 + (size_t)bi * bs * nb + bj * bs, nb, 1, bs, bs, p, 1, -1.0, 0.0, bi * bs, bj * bs, h));
-  P.dgemm(bs, js);
-}
-
 }  // namespace
 
-cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t stream) {
+cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
   const int nt = V->nt, nb = V->nb;
   const size_t nb2 = (size_t)nb * nb;
   const int nsb = nb / TC_BM;
   const auto& cls = V->h_cls;
   auto t64 = [&](int i, int j) { return V->pool64 + (size_t)V->h_i64[tidx(i, j)] * nb2; };
+  auto ws64 = [&](int par, int i) { return V->ws64 + ((size_t)par * nt + i) * nb2; };
   Plan P;
   int* status = V->d_status;
-  P.ops.push_back([=](cudaStream_t s, const DJob*, const DPair*) -> cr_status { return status_init_launch(status, s); });
-  P.ops.push_back([=](cudaStream_t s, const DJob*, const DPair*) -> cr_status { return convert_tiles(V, s); });
+  P.ops.push_back([=](Exec& x) -> cr_status {
+    CR_TRY(status_init_launch(status, x.hi));
+    CR_TRY(convert_tiles(V, x.hi));
+    CR_CUDA(cudaEventRecord(x.start, x.hi));   // the first two OLD steps wait for the converted tiles
+    return CR_OK;
+  });
 
   // rows solved on the tensor cores, per column
   std::vector<int> rows_flat;
@@ -147,23 +107,35 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t stream) {
 
   TcParams base{};
   base.v = V->view();
-  base.ws_hi0 = V->ws_hi0;
-  base.ws_lo0 = V->ws_lo0;
   base.minv_hi = V->minv_hi;
   base.minv_lo = V->minv_lo;
   base.eA = V->eA;
   base.status = V->d_status;
   base.err = V->d_status;
-  base.ws64 = V->ws64;
+  const CUtensorMap* tm = &V->tm_pool16;
 
   for (int j = 0; j < nt; ++j) {
-    // 1. FP64 products
+    const int par = j & 1;
+    const int knew = j - 1;                  // newest term (none for j = 0)
+    const int kold_end = j > 0 ? j - 1 : 0;  // older terms [0, kold_end)
+    TcParams tp = base;
+    tp.j = j;
+    tp.ws_hi0 = V->ws_hi0 + par * nt;
+    tp.ws_lo0 = V->ws_lo0 + par * nt;
+    tp.ws64 = V->ws64 ? ws64(par, 0) : nullptr;
+    tp.w32 = V->w32 ? V->w32 + (size_t)par * nt * nb2 : nullptr;
+
+    // ---------------- OLD(j) on the low-priority stream
+    P.ops.push_back([=](Exec& x) -> cr_status {
+      CR_CUDA(cudaStreamWaitEvent(x.lo, j >= 2 ? x.ev[2 * (j - 2)] : x.start, 0));
+      return CR_OK;
+    });
     {
       std::vector<DJob> js;
       for (int i = j; i < nt; ++i) {
         if (cls[tidx(i, j)] != CR_PREC_FP64) continue;
         const int pbeg = (int)P.pairs.size();
-        for (int k = 0; k < j; ++k)
+        for (int k = 0; k < kold_end; ++k)
           if (cls[tidx(i, k)] == CR_PREC_FP64 && cls[tidx(j, k)] == CR_PREC_FP64)
             P.add_pair(t64(i, k), t64(j, k), nb, 1, nb, 1, nb);
         const int pcnt = (int)P.pairs.size() - pbeg;
@@ -175,61 +147,96 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t stream) {
             js.push_back(job(C + (size_t)bi * 64 * nb + bj * 64, nb, 1, 64, 64, pbeg, pcnt, -1.0, 1.0, bi * 64, bj * 64, nb));
           }
       }
-      P.dgemm(64, js);
+      P.dgemm(64, js, true);
     }
-    // 2. tensor-core products (also stages the solve inputs), or plain copies without AMP
     if (V->amp) {
-      TcParams tp = base;
-      tp.mode = TC_UPDATE;
-      tp.j = j;
-      tp.rows = nullptr;
+      TcParams t = tp;
+      t.mode = TC_UPD_OLD;
+      t.rows = nullptr;
+      t.kbeg = 0;
+      t.kend = kold_end;
       const int grid = (nt - j) * nsb * nsb;
-      const CUtensorMap* tm = &V->tm_pool16;
-      P.ops.push_back([=](cudaStream_t s, const DJob*, const DPair*) -> cr_status { return tc_launch(tp, *tm, *tm, grid, s); });
+      P.ops.push_back([=](Exec& x) -> cr_status { return tc_launch(t, *tm, *tm, grid, x.lo); });
     } else {
       for (int i = j + 1; i < nt; ++i) {
-        double* dst = V->ws64 + (size_t)i * nb2;
+        double* dst = ws64(par, i);
         const double* src = t64(i, j);
-        P.ops.push_back([=](cudaStream_t s, const DJob*, const DPair*) -> cr_status {
-          CR_CUDA(cudaMemcpyAsync(dst, src, nb2 * sizeof(double), cudaMemcpyDeviceToDevice, s));
+        P.ops.push_back([=](Exec& x) -> cr_status {
+          CR_CUDA(cudaMemcpyAsync(dst, src, nb2 * sizeof(double), cudaMemcpyDeviceToDevice, x.lo));
           return CR_OK;
         });
       }
     }
-    // 3. diagonal factor and its inverse
+    P.ops.push_back([=](Exec& x) -> cr_status {
+      CR_CUDA(cudaEventRecord(x.ev[2 * j + 1], x.lo));
+      CR_CUDA(cudaStreamWaitEvent(x.hi, x.ev[2 * j + 1], 0));
+      return CR_OK;
+    });
+
+    // ---------------- NEW(j) on the high-priority stream
+    if (knew >= 0) {
+      std::vector<DJob> js;
+      for (int i = j; i < nt; ++i) {
+        if (cls[tidx(i, j)] != CR_PREC_FP64) continue;
+        if (!(cls[tidx(i, knew)] == CR_PREC_FP64 && cls[tidx(j, knew)] == CR_PREC_FP64)) continue;
+        const int p = P.add_pair(t64(i, knew), t64(j, knew), nb, 1, nb, 1, nb);
+        double* C = i == j ? t64(i, j) : ws64(par, i);
+        for (int bi = 0; bi < nb / 64; ++bi)
+          for (int bj = 0; bj < nb / 64; ++bj) {
+            if (i == j && bj > bi) continue;
+            js.push_back(job(C + (size_t)bi * 64 * nb + bj * 64, nb, 1, 64, 64, p, 1, -1.0, 1.0, bi * 64, bj * 64, nb));
+          }
+      }
+      P.dgemm(64, js, false);
+    }
+    if (V->amp) {
+      TcParams t = tp;
+      t.mode = TC_UPD_NEW;
+      t.rows = nullptr;
+      t.kbeg = knew >= 0 ? knew : 0;
+      t.kend = knew >= 0 ? j : 0;
+      const int grid = (nt - j) * nsb * nsb;
+      P.ops.push_back([=](Exec& x) -> cr_status { return tc_launch(t, *tm, *tm, grid, x.hi); });
+    }
+
+    // ---------------- diagonal factor and its inverse (FP64 dataflow executor)
     double* Ajj = t64(j, j);
     double* Minv = V->minv;
     double* T = V->scratch64;
-    P.ops.push_back([=](cudaStream_t s, const DJob*, const DPair*) -> cr_status {
-      CR_CUDA(cudaMemsetAsync(Minv, 0, nb2 * sizeof(double), s));
-      return CR_OK;
-    });
-    plan_chol_inv(P, V, Ajj, Minv, T, 0, nb, j * nb);
-    P.ops.push_back([=](cudaStream_t s, const DJob*, const DPair*) -> cr_status {
-      k_zero_upper<<<64, 256, 0, s>>>(Ajj, nb);
-      CR_CHECK_LAUNCH("k_zero_upper");
-      return CR_OK;
-    });
+    {
+      const int db = V->diag_db, ntask = V->diag_ntasks, g = j * nb;
+      int dgrid = 152;
+      if (const char* e = getenv("CR_DIAG_GRID")) dgrid = atoi(e);
+      int* flags = V->diag_flags;
+      const int4* tasks = V->diag_tasks;
+      P.ops.push_back([=](Exec& x) -> cr_status {
+        CR_CUDA(cudaMemsetAsync(Minv, 0, nb2 * sizeof(double), x.hi));
+        CR_TRY(diag_chol_launch(db, Ajj, Minv, T, nb, g, status, flags, tasks, ntask, dgrid, x.hi));
+        k_zero_upper<<<64, 256, 0, x.hi>>>(Ajj, nb);
+        CR_CHECK_LAUNCH("k_zero_upper");
+        return CR_OK;
+      });
+    }
     if (V->amp) {
       __half* mh = V->pool16 + (size_t)V->minv_hi * nb2;
       __half* ml = V->pool16 + (size_t)V->minv_lo * nb2;
       __half* dh = V->pool16 + (size_t)V->h_hi16[tidx(j, j)] * nb2;
       __half* dl = V->pool16 + (size_t)V->h_lo16[tidx(j, j)] * nb2;
-      P.ops.push_back([=](cudaStream_t s, const DJob*, const DPair*) -> cr_status {
-        CR_TRY(split_minv_launch(Minv, nb, mh, ml, status, s));
-        return split_tile_launch(Ajj, nb, dh, dl, 1, s);
+      double* part = V->minv_part;
+      P.ops.push_back([=](Exec& x) -> cr_status {
+        CR_TRY(split_minv_launch(Minv, nb, mh, ml, status, part, x.hi));
+        return split_tile_launch(Ajj, nb, dh, dl, 1, x.hi);
       });
     }
-    // 4. off-diagonal solves
+
+    // ---------------- off-diagonal solves
     const int ntc = rows_off[j + 1] - rows_off[j];
     if (ntc > 0) {
-      TcParams tp = base;
-      tp.mode = TC_TRSM;
-      tp.j = j;
-      tp.rows = d_rows + rows_off[j];
+      TcParams t = tp;
+      t.mode = TC_TRSM;
+      t.rows = d_rows + rows_off[j];
       const int grid = ntc * nsb * nsb;
-      const CUtensorMap* tm = &V->tm_pool16;
-      P.ops.push_back([=](cudaStream_t s, const DJob*, const DPair*) -> cr_status { return tc_launch(tp, *tm, *tm, grid, s); });
+      P.ops.push_back([=](Exec& x) -> cr_status { return tc_launch(t, *tm, *tm, grid, x.hi); });
     }
     {
       std::vector<DJob> js;
@@ -237,41 +244,68 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t stream) {
       for (int i = j + 1; i < nt; ++i) {
         if (cls[tidx(i, j)] != CR_PREC_FP64) continue;
         fp64_rows.push_back(i);
-        const int p = P.add_pair(V->ws64 + (size_t)i * nb2, Minv, nb, 1, nb, 1, nb);
+        const int p = P.add_pair(ws64(par, i), Minv, nb, 1, nb, 1, nb);
         double* C = t64(i, j);
         for (int bi = 0; bi < nb / 64; ++bi)
           for (int bj = 0; bj < nb / 64; ++bj)
             js.push_back(job(C + (size_t)bi * 64 * nb + bj * 64, nb, 1, 64, 64, p, 1, 1.0, 0.0, bi * 64, bj * 64, (bj + 1) * 64));
       }
-      P.dgemm(64, js);
+      P.dgemm(64, js, false);
       if (V->amp) {
         for (int i : fp64_rows) {
           const double* src = t64(i, j);
           __half* h = V->pool16 + (size_t)V->h_hi16[tidx(i, j)] * nb2;
           __half* l = V->pool16 + (size_t)V->h_lo16[tidx(i, j)] * nb2;
-          P.ops.push_back([=](cudaStream_t s, const DJob*, const DPair*) -> cr_status { return split_tile_launch(src, nb, h, l, 0, s); });
+          P.ops.push_back([=](Exec& x) -> cr_status { return split_tile_launch(src, nb, h, l, 0, x.hi); });
         }
       }
     }
+    P.ops.push_back([=](Exec& x) -> cr_status {
+      CR_CUDA(cudaEventRecord(x.ev[2 * j], x.hi));
+      return CR_OK;
+    });
   }
 
-  // upload job lists and replay
+  // streams, events, job upload, replay
+  if (!V->s_hi) {
+    int lo_prio = 0, hi_prio = 0;
+    CR_CUDA(cudaDeviceGetStreamPriorityRange(&lo_prio, &hi_prio));
+    CR_CUDA(cudaStreamCreateWithPriority(&V->s_hi, cudaStreamNonBlocking, hi_prio));
+    CR_CUDA(cudaStreamCreateWithPriority(&V->s_lo, cudaStreamNonBlocking, lo_prio));
+  }
+  Exec x;
+  x.hi = V->s_hi;
+  x.lo = getenv("CR_SERIAL") ? V->s_hi : V->s_lo;
+  x.ev.resize(2 * nt);
+  cr_status st = CR_OK;
+  for (auto& e : x.ev) cudaEventCreateWithFlags(&e, cudaEventDisableTiming);
+  cudaEventCreateWithFlags(&x.start, cudaEventDisableTiming);
   DJob* d_jobs = nullptr;
   DPair* d_pairs = nullptr;
-  cr_status st = CR_OK;
   if (!P.jobs.empty() && cudaMalloc(&d_jobs, P.jobs.size() * sizeof(DJob)) != cudaSuccess) st = fail(CR_ERR_NOMEM, "job list");
   if (st == CR_OK && !P.pairs.empty() && cudaMalloc(&d_pairs, P.pairs.size() * sizeof(DPair)) != cudaSuccess)
     st = fail(CR_ERR_NOMEM, "pair list");
   if (st == CR_OK && d_jobs)
-    if (cudaMemcpyAsync(d_jobs, P.jobs.data(), P.jobs.size() * sizeof(DJob), cudaMemcpyHostToDevice, stream) != cudaSuccess)
+    if (cudaMemcpyAsync(d_jobs, P.jobs.data(), P.jobs.size() * sizeof(DJob), cudaMemcpyHostToDevice, caller) != cudaSuccess)
       st = fail(CR_ERR_CUDA, "job upload");
   if (st == CR_OK && d_pairs)
-    if (cudaMemcpyAsync(d_pairs, P.pairs.data(), P.pairs.size() * sizeof(DPair), cudaMemcpyHostToDevice, stream) !=
-        cudaSuccess)
+    if (cudaMemcpyAsync(d_pairs, P.pairs.data(), P.pairs.size() * sizeof(DPair), cudaMemcpyHostToDevice, caller) != cudaSuccess)
       st = fail(CR_ERR_CUDA, "pair upload");
-  for (size_t q = 0; st == CR_OK && q < P.ops.size(); ++q) st = P.ops[q](stream, d_jobs, d_pairs);
-  cudaError_t e = cudaStreamSynchronize(stream);
-  if (st == CR_OK && e != cudaSuccess) st = cuda_fail(e, "cholesky");
+  x.dj = d_jobs;
+  x.dp = d_pairs;
+  if (st == CR_OK) {
+    // both library streams start after the caller's prior work (and the uploads)
+    cudaEventRecord(x.start, caller);
+    cudaStreamWaitEvent(x.hi, x.start, 0);
+    cudaStreamWaitEvent(x.lo, x.start, 0);
+  }
+  for (size_t q = 0; st == CR_OK && q < P.ops.size(); ++q) st = P.ops[q](x);
+  cudaError_t e1 = cudaStreamSynchronize(x.hi);
+  cudaError_t e2 = cudaStreamSynchronize(x.lo);
+  if (st == CR_OK && e1 != cudaSuccess) st = cuda_fail(e1, "cholesky (critical stream)");
+  if (st == CR_OK && e2 != cudaSuccess) st = cuda_fail(e2, "cholesky (bulk stream)");
+  for (auto& e : x.ev) cudaEventDestroy(e);
+  cudaEventDestroy(x.start);
   if (d_jobs) cudaFree(d_jobs);
   if (d_pairs) cudaFree(d_pairs);
   if (d_rows) cudaFree(d_rows);
@@ -287,6 +321,24 @@ extern "C" cr_status cr_potrf_adaptive(cr_tilemat V, cr_stream stream, int* info
   if (info) *info = 0;
   if (!V->mapped) return fail(CR_ERR_STATE, "cr_potrf_adaptive: call cr_precision_map first");
   CR_CUDA(cudaSetDevice(V->device));
+  // block size of the diagonal-tile dataflow factorisation
+  int db = 16;
+  if (const char* e = getenv("CR_DIAG_DB")) db = atoi(e);
+  if (db != 16 && db != 32) db = 16;
+  if (db != V->diag_db) {
+    if (V->diag_tasks) cudaFree(V->diag_tasks);
+    if (V->diag_flags) cudaFree(V->diag_flags);
+    V->diag_tasks = nullptr;
+    V->diag_flags = nullptr;
+    std::vector<int4> tasks;
+    diag_task_list(V->nb / db, tasks);
+    CR_CUDA(cudaMalloc(&V->diag_tasks, tasks.size() * sizeof(int4)));
+    CR_CUDA(cudaMemcpy(V->diag_tasks, tasks.data(), tasks.size() * sizeof(int4), cudaMemcpyHostToDevice));
+    CR_CUDA(cudaMalloc(&V->diag_flags, diag_flag_words(V->nb, db) * sizeof(int)));
+    V->diag_ntasks = (int)tasks.size();
+    V->diag_db = db;
+  }
+  if (!V->minv_part) CR_CUDA(cudaMalloc(&V->minv_part, 64 * sizeof(double)));
   CR_TRY(build_and_run_cholesky(V, stream));
   int h[4];
   CR_CUDA(cudaMemcpy(h, V->d_status, sizeof(h), cudaMemcpyDeviceToHost));

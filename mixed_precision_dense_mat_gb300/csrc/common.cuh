@@ -87,7 +87,9 @@ struct cr_tilemat_s {
   double* pool64 = nullptr;
   float* pool32 = nullptr;
   __half* pool16 = nullptr;
-  double* ws64 = nullptr;         // nt * nb * nb: FP64-class TRSM inputs
+  double* ws64 = nullptr;         // 2 * nt * nb * nb: FP64-class solve inputs (double-buffered by column parity)
+  float* w32 = nullptr;           // 2 * nt * nb * nb: FP32 intermediate of FP16/FP32-class tiles (same)
+  cudaStream_t s_hi = nullptr, s_lo = nullptr;   // critical chain / bulk updates
   double* minv = nullptr;         // nb * nb: inverse of the current diagonal factor
   double* scratch64 = nullptr;    // nb * nb: temporaries of the diagonal factorisation
   int* d_status = nullptr;        // [0] device error bits, [1] first failing column (1-based) or 0, [2] Minv exponent
@@ -98,6 +100,11 @@ struct cr_tilemat_s {
   int b16_M = -1;
   CUtensorMap tm_b16;
   double* bnorm_part = nullptr;   // per-block partial sums of ||B||_F^2
+  // diagonal-tile dataflow factorisation: task list and flag scratch
+  int4* diag_tasks = nullptr;
+  int diag_ntasks = 0, diag_db = 0;
+  int* diag_flags = nullptr;
+  double* minv_part = nullptr;    // per-block partial maxima of |L_jj^-1|
   bool factored = false;
   int info = 0;
 

@@ -136,28 +136,39 @@ __global__ void __launch_bounds__(256) k_split_tile(const double* __restrict__ s
   const size_t count = (size_t)nb * nb;
   for (size_t idx = blockIdx.x * 256 + threadIdx.x; idx < count; idx += (size_t)gridDim.x * 256) {
     const int r = (int)(idx / nb), c = (int)(idx % nb);
-    const double x = (lower_only && c > r) ? 0.0 : src[idx];
-    const __half h = __double2half(x);
+    // via FP32: the pair keeps the leading 22 bits, which is all an FP16 pair can hold
+    const float x = (lower_only && c > r) ? 0.0f : (float)src[idx];
+    const __half h = __float2half_rn(x);
     hi[idx] = h;
-    lo[idx] = __double2half(x - (double)__half2float(h));
+    lo[idx] = __float2half_rn(x - __half2float(h));
   }
 }
 
-// Splits the inverse factor: chooses eM with max|M| 2^eM <= 2^14 (status[2] = eM) and writes
-// the FP16 high/low parts of M 2^eM.  One CTA.
-__global__ void __launch_bounds__(1024) k_split_minv(const double* __restrict__ Minv, int nb, __half* __restrict__ hi,
-                                                     __half* __restrict__ lo, int* status) {
-  __shared__ double red[32];
-  __shared__ int s_e;
-  const size_t count = (size_t)nb * nb;
+constexpr int SPLIT_PARTS = 64;
+
+// Partial maxima of |M| over SPLIT_PARTS CTAs.
+__global__ void __launch_bounds__(256) k_absmax_part(const double* __restrict__ M, size_t count, double* __restrict__ part) {
+  __shared__ double red[8];
   double mx = 0.0;
-  for (size_t idx = threadIdx.x; idx < count; idx += blockDim.x) mx = fmax(mx, fabs(Minv[idx]));
+  for (size_t idx = blockIdx.x * 256 + threadIdx.x; idx < count; idx += (size_t)gridDim.x * 256) mx = fmax(mx, fabs(M[idx]));
   for (int o = 16; o > 0; o >>= 1) mx = fmax(mx, __shfl_down_sync(0xffffffffu, mx, o));
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
   __syncthreads();
   if (threadIdx.x == 0) {
     double m = 0.0;
-    for (int q = 0; q < (int)(blockDim.x >> 5); ++q) m = fmax(m, red[q]);
+    for (int q = 0; q < 8; ++q) m = fmax(m, red[q]);
+    part[blockIdx.x] = m;
+  }
+}
+
+// Splits the inverse factor: eM with max|M| 2^eM < 2^14 (status[2] = eM) and the FP16 high/low
+// parts of M 2^eM.  Every CTA combines the partial maxima itself.
+__global__ void __launch_bounds__(256) k_split_minv(const double* __restrict__ Minv, size_t count, const double* __restrict__ part,
+                                                    __half* __restrict__ hi, __half* __restrict__ lo, int* status) {
+  __shared__ int s_e;
+  if (threadIdx.x == 0) {
+    double m = 0.0;
+    for (int q = 0; q < SPLIT_PARTS; ++q) m = fmax(m, part[q]);
     int e = 0;
     if (m > 0.0 && isfinite(m)) {
       int ex;
@@ -165,15 +176,15 @@ __global__ void __launch_bounds__(1024) k_split_minv(const double* __restrict__ 
       e = 14 - ex;            // m 2^e < 2^14
     }
     s_e = e;
-    status[2] = e;
+    if (blockIdx.x == 0) status[2] = e;
   }
   __syncthreads();
-  const double sc = ldexp(1.0, s_e);
-  for (size_t idx = threadIdx.x; idx < count; idx += blockDim.x) {
-    const double x = Minv[idx] * sc;
-    const __half h = __double2half(x);
+  const float sc = ldexpf(1.0f, s_e);
+  for (size_t idx = blockIdx.x * 256 + threadIdx.x; idx < count; idx += (size_t)gridDim.x * 256) {
+    const float x = (float)Minv[idx] * sc;
+    const __half h = __float2half_rn(x);
     hi[idx] = h;
-    lo[idx] = __double2half(x - (double)__half2float(h));
+    lo[idx] = __float2half_rn(x - __half2float(h));
   }
 }
 
@@ -194,8 +205,11 @@ cr_status split_tile_launch(const double* src, int nb, __half* hi, __half* lo, i
   CR_CHECK_LAUNCH("k_split_tile");
   return CR_OK;
 }
-cr_status split_minv_launch(const double* Minv, int nb, __half* hi, __half* lo, int* status, cudaStream_t s) {
-  k_split_minv<<<1, 1024, 0, s>>>(Minv, nb, hi, lo, status);
+cr_status split_minv_launch(const double* Minv, int nb, __half* hi, __half* lo, int* status, double* part, cudaStream_t s) {
+  const size_t count = (size_t)nb * nb;
+  k_absmax_part<<<SPLIT_PARTS, 256, 0, s>>>(Minv, count, part);
+  CR_CHECK_LAUNCH("k_absmax_part");
+  k_split_minv<<<128, 256, 0, s>>>(Minv, count, part, hi, lo, status);
   CR_CHECK_LAUNCH("k_split_minv");
   return CR_OK;
 }

@@ -25,7 +25,8 @@ struct DJob {
 cr_status dgemm_launch(int block, const DJob* d_jobs, const DPair* d_pairs, int njobs, cudaStream_t stream);
 cr_status potrf64_base_launch(double* A, int lda, double* Minv, int ldm, int gcol0, int* status, cudaStream_t s);
 cr_status split_tile_launch(const double* src, int nb, __half* hi, __half* lo, int lower_only, cudaStream_t s);
-cr_status split_minv_launch(const double* Minv, int nb, __half* hi, __half* lo, int* status, cudaStream_t s);
+// part: 64 doubles of device scratch
+cr_status split_minv_launch(const double* Minv, int nb, __half* hi, __half* lo, int* status, double* part, cudaStream_t s);
 cr_status status_init_launch(int* status, cudaStream_t s);
 
 }  // namespace cr

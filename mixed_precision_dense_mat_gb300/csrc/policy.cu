@@ -130,8 +130,8 @@ cr_status allocate_class_storage(cr_tilemat V) {
     for (int t = 0; t < T; ++t) V->h_hi16[t] = V->n16++;
     for (int t = 0; t < T; ++t)
       if (V->h_cls[t] != CR_PREC_FP16) V->h_lo16[t] = V->n16++;
-    V->ws_hi0 = V->n16; V->n16 += nt;
-    V->ws_lo0 = V->n16; V->n16 += nt;
+    V->ws_hi0 = V->n16; V->n16 += 2 * nt;   // two sets, by column parity
+    V->ws_lo0 = V->n16; V->n16 += 2 * nt;
     V->minv_hi = V->n16++;
     V->minv_lo = V->n16++;
   }
@@ -146,7 +146,8 @@ cr_status allocate_class_storage(cr_tilemat V) {
     CR_CUDA(cudaMalloc(&V->pool16, (size_t)V->n16 * tile * sizeof(__half)));
     CR_TRY(make_tensor_map_3d_f16(&V->tm_pool16, V->pool16, V->nb, V->nb, V->n16, 64, 128));
   }
-  if (off64 > 0) CR_CUDA(cudaMalloc(&V->ws64, (size_t)nt * tile * sizeof(double)));
+  if (off64 > 0) CR_CUDA(cudaMalloc(&V->ws64, 2 * (size_t)nt * tile * sizeof(double)));
+  if (V->amp) CR_CUDA(cudaMalloc(&V->w32, 2 * (size_t)nt * tile * sizeof(float)));
   V->mapped = true;
   return CR_OK;
 }

@@ -57,10 +57,10 @@ __device__ __forceinline__ int for_each_step(const TcParams& p, const Job& jb, F
   const TileView& v = p.v;
   const int nq = v.nb / TC_BK;
   int s = 0;
-  if (p.mode == TC_UPDATE) {
+  if (p.mode == TC_UPD_OLD || p.mode == TC_UPD_NEW) {
     const int i = jb.i, j = p.j;
     const int cd = v.cls[tidx(i, j)];
-    for (int k = 0; k < j; ++k) {
+    for (int k = p.kbeg; k < p.kend; ++k) {
       const int ti = tidx(i, k), tj = tidx(j, k);
       const int pc = max(cd, max((int)v.cls[ti], (int)v.cls[tj]));
       if (pc == CR_PREC_FP64) continue;
@@ -128,7 +128,8 @@ __device__ __forceinline__ void epilogue_store(const TcParams& p, const Job& jb,
   const int t = tidx(i, j);
   const int cd = v.cls[t];
   const size_t off = (size_t)(jb.rb * TC_BM + r_local) * nb + jb.cb * TC_BN + c0;
-  if (p.mode == TC_UPDATE) {
+  if (p.mode == TC_UPD_OLD) {
+    // older terms: class storage -> intermediate (FP64 in place / FP64 workspace / FP32 workspace)
     if (i == j || cd == CR_PREC_FP64) {
       const double* src = v.pool64 + (size_t)v.i64[t] * nb2 + off;
       double* dst = (i == j) ? const_cast<double*>(src) : p.ws64 + (size_t)i * nb2 + off;
@@ -137,8 +138,34 @@ __device__ __forceinline__ void epilogue_store(const TcParams& p, const Job& jb,
         const double2 a = *reinterpret_cast<const double2*>(src + q);
         *reinterpret_cast<double2*>(dst + q) = make_double2(a.x - (double)acc[q], a.y - (double)acc[q + 1]);
       }
+    } else {
+      float* dst = p.w32 + (size_t)i * nb2 + off;
+      if (cd == CR_PREC_FP32) {
+        const float* src = v.pool32 + (size_t)v.i32[t] * nb2 + off;
+#pragma unroll
+        for (int q = 0; q < 16; q += 4)
+          *reinterpret_cast<float4*>(dst + q) =
+              make_float4(src[q] - acc[q], src[q + 1] - acc[q + 1], src[q + 2] - acc[q + 2], src[q + 3] - acc[q + 3]);
+      } else {
+        const __half* src = v.pool16 + (size_t)v.hi16[t] * nb2 + off;
+#pragma unroll
+        for (int q = 0; q < 16; q += 4)
+          *reinterpret_cast<float4*>(dst + q) =
+              make_float4(__half2float(src[q]) - acc[q], __half2float(src[q + 1]) - acc[q + 1],
+                          __half2float(src[q + 2]) - acc[q + 2], __half2float(src[q + 3]) - acc[q + 3]);
+      }
+    }
+  } else if (p.mode == TC_UPD_NEW) {
+    // newest term: intermediate -> solve inputs in the tile's precision
+    if (i == j || cd == CR_PREC_FP64) {
+      double* dst = (i == j) ? v.pool64 + (size_t)v.i64[t] * nb2 + off : p.ws64 + (size_t)i * nb2 + off;
+#pragma unroll
+      for (int q = 0; q < 16; q += 2) {
+        const double2 a = *reinterpret_cast<const double2*>(dst + q);
+        *reinterpret_cast<double2*>(dst + q) = make_double2(a.x - (double)acc[q], a.y - (double)acc[q + 1]);
+      }
     } else if (cd == CR_PREC_FP32) {
-      const float* src = v.pool32 + (size_t)v.i32[t] * nb2 + off;
+      const float* src = p.w32 + (size_t)i * nb2 + off;
       __half* hi = v.pool16 + (size_t)(p.ws_hi0 + i) * nb2 + off;
       __half* lo = v.pool16 + (size_t)(p.ws_lo0 + i) * nb2 + off;
       const float sc = ldexpf(1.0f, -p.eA);
@@ -150,10 +177,10 @@ __device__ __forceinline__ void epilogue_store(const TcParams& p, const Job& jb,
         lo[q] = __float2half_rn(w - __half2float(h));
       }
     } else {
-      const __half* src = v.pool16 + (size_t)v.hi16[t] * nb2 + off;
+      const float* src = p.w32 + (size_t)i * nb2 + off;
       __half* dst = v.pool16 + (size_t)(p.ws_hi0 + i) * nb2 + off;
 #pragma unroll
-      for (int q = 0; q < 16; ++q) dst[q] = __float2half_rn(__half2float(src[q]) - acc[q]);
+      for (int q = 0; q < 16; ++q) dst[q] = __float2half_rn(src[q] - acc[q]);
     }
   } else {   // TC_TRSM
     const int eM = p.status[2];
@@ -290,6 +317,7 @@ cr_status tc_launch(const TcParams& p, const CUtensorMap& tmA, const CUtensorMap
   static bool configured = false;
   if (!configured) {
     CR_CUDA(cudaFuncSetAttribute(k_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC_SMEM));
+    CR_CUDA(cudaFuncSetAttribute(k_tc, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared));
     configured = true;
   }
   if (grid <= 0) return CR_OK;

@@ -10,12 +10,18 @@ constexpr int TC_STAGE_BYTES = (TC_BM + TC_BN) * TC_BK * 2;   // A and B, FP16, 
 constexpr int TC_THREADS = 192;
 constexpr size_t TC_SMEM = (size_t)TC_STAGES * TC_STAGE_BYTES + 1024 + 256;
 
-enum { TC_UPDATE = 0, TC_TRSM = 1, TC_TRMM = 2 };
+// TC_UPD_OLD: products k in [kbeg, kend) from the class storage into the intermediate
+//             (FP32 workspace w32, FP64 workspace ws64, diagonal FP64 in place);
+// TC_UPD_NEW: products k in [kbeg, kend) from the intermediate into the solve inputs
+//             (FP16 / FP16 high-low workspace slots, ws64, diagonal in place).
+enum { TC_UPD_OLD = 0, TC_TRSM = 1, TC_TRMM = 2, TC_UPD_NEW = 3 };
 
 struct TcParams {
   TileView v;
   int mode;
   int j;              // tile column (update / triangular solve)
+  int kbeg, kend;     // update terms
+  float* w32;         // FP32 intermediate of FP16/FP32-class tiles (tile row i at i nb^2)
   const int* rows;    // tile rows of this launch (triangular solve); NULL: rows j, j+1, ...
   int ws_hi0, ws_lo0, minv_hi, minv_lo;
   int eA;             // FP32-class inputs were scaled by 2^-eA
