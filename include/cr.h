@@ -108,9 +108,12 @@ cr_status cr_tilemat_destroy(cr_tilemat V);
 cr_status cr_tilemat_info(cr_tilemat V, int* n, int* nb, int* nt);
 
 /* Joint covariance (Section V Eq.4) of the n locations d_xy (n x 2, row-major pairs
- * (x_i, y_i), device, FP64), prediction sites first.  Fills the FP64 lower tiles and the
- * per-tile statistics (Frobenius norm, min and max entry over valid entries, Section
- * V-D).  Asynchronous. */
+ * (x_i, y_i), device, FP64; copied, so the caller may free it afterwards), prediction sites
+ * first.  Computes the per-tile statistics (Frobenius norm, min and max entry over valid
+ * entries, Section V-D) in one pass without storing the matrix: the tiles are generated
+ * in their precision classes by cr_potrf_adaptive, and cr_tilemat_to_dense / cr_krige
+ * evaluate V in FP64 on demand.  For Matern nu in {1/2, 3/2, 5/2} the statistics are
+ * evaluated in double-float arithmetic (about 1e-14 relative).  Asynchronous. */
 cr_status cr_cov_build(cr_tilemat V, const double* d_xy, const cr_cov_params* p, cr_stream stream);
 
 /* Per-tile statistics as NT x NT row-major host arrays (lower part filled).

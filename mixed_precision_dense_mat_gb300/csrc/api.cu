@@ -147,7 +147,7 @@ extern "C" cr_status cr_tilemat_create(int n, int nb, cr_tilemat* out) {
   cudaGetDevice(&V->device);
   const size_t tile = (size_t)nb * nb;
   cudaError_t e;
-  if ((e = cudaMalloc(&V->master, (size_t)V->ntiles * tile * sizeof(double))) != cudaSuccess ||
+  if ((e = cudaMalloc(&V->xy, (size_t)n * 2 * sizeof(double))) != cudaSuccess ||
       (e = cudaMalloc(&V->stat_part, (size_t)V->ntiles * (nb / 64) * 3 * sizeof(double))) != cudaSuccess ||
       (e = cudaMalloc(&V->stats, (size_t)V->ntiles * 3 * sizeof(double))) != cudaSuccess ||
       (e = cudaMalloc(&V->minv, tile * sizeof(double))) != cudaSuccess ||
@@ -168,7 +168,7 @@ extern "C" cr_status cr_tilemat_destroy(cr_tilemat V) {
   cudaDeviceSynchronize();
   free_class_storage(V);
   dfree(V->b16); dfree(V->bnorm_part); dfree(V->diag_tasks); dfree(V->diag_flags); dfree(V->minv_part);
-  dfree(V->master); dfree(V->stat_part); dfree(V->stats); dfree(V->minv); dfree(V->scratch64); dfree(V->d_status);
+  dfree(V->xy); dfree(V->stat_part); dfree(V->stats); dfree(V->minv); dfree(V->scratch64); dfree(V->d_status);
   if (V->s_hi) cudaStreamDestroy(V->s_hi);
   if (V->s_lo) cudaStreamDestroy(V->s_lo);
   delete V;

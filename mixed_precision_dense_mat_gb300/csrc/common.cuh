@@ -46,6 +46,16 @@ enum : int { DEV_ERR_TIMEOUT = 1, DEV_ERR_BOUNDS = 2 };
 // ----------------------------------------------------------------- tile indexing
 __host__ __device__ inline int tidx(int i, int j) { return i * (i + 1) / 2 + j; }  // i >= j
 
+// Covariance model as the kernels see it.
+struct CovK {
+  int family;        // CR_COV_*
+  int kind;          // Matern: 0 nu=1/2, 1 nu=3/2, 2 nu=5/2, 3 general (quadrature)
+  double sigma2, inv_range, nu, nugget, tau2, norm;   // norm = 2^(1-nu) / Gamma(nu)
+  int n_pred;
+  int use_df;        // closed-form Matern orders: statistics and reduced-precision tiles in double-float
+  float sig_hi, sig_lo, invr_hi, invr_lo;   // sigma2 and 1/range as double-float pairs
+};
+
 // Kernel-side view of the tile storage.
 struct TileView {
   int n, nb, nt;
@@ -64,8 +74,9 @@ struct TileView {
 struct cr_tilemat_s {
   int n = 0, nb = 0, nt = 0, npad = 0, ntiles = 0;
   int device = 0;
-  // covariance (FP64 lower tiles) and statistics
-  double* master = nullptr;      // ntiles * nb * nb
+  // covariance model, locations and tile statistics (tiles are generated on demand)
+  double* xy = nullptr;          // n x 2 locations (copy of the caller's)
+  cr::CovK covk{};
   double* stat_part = nullptr;   // ntiles * (nb/64) * 3 partials
   double* stats = nullptr;       // ntiles * 3 : sum of squares, min, max
   cr_cov_params params{};

@@ -1,23 +1,29 @@
-// Covariance tile generation, tile statistics, conversion to the precision classes and
-// dense extraction.
+// Covariance evaluation: tile statistics, generation of each tile in its precision class,
+// dense extraction and dense blocks for kriging.
 //
 // "Mixed-Precision GPU Acceleration for Confidence Regions of Spatial Excursion Sets":
 // Section V Eq.4 (joint covariance, tau^2 on the observation block only), Section VI-B.2
 // (power-exponential model), Section VI-C (Matern model), Section V-D (tile Frobenius
-// norms and entry extrema used by the precision checks), Alg.2 step 12 (scaling by s^2
-// and rounding each tile to its class).
+// norms and entry extrema used by the precision checks), Alg.2 step 12 (the tiles of s^2 V
+// in their selected precisions).
+//
+// The FP64 matrix is never stored.  cr_cov_build makes one pass that only reduces the
+// per-tile statistics; the factorisation generates each tile directly in its class (FP64
+// tiles in FP64, FP32/FP16 tiles rounded from a double-float evaluation).  For the
+// closed-form Matern orders (nu = 1/2, 3/2, 5/2) both passes evaluate in double-float
+// arithmetic on the FP32 units (about 1e-14 relative; GB300's FP64 units run at 1/60 of the
+// FP32 rate); FP64 tiles and the other models use FP64.
 #include <math.h>
 
+#include <mutex>
+
 #include "common.cuh"
+#include "cov.cuh"
+#include "df.cuh"
 
 namespace cr {
 
-struct CovK {
-  int family;        // CR_COV_*
-  int kind;          // Matern: 0 nu=1/2, 1 nu=3/2, 2 nu=5/2, 3 general (quadrature)
-  double sigma2, inv_range, nu, nugget, tau2, norm;   // norm = 2^(1-nu) / Gamma(nu)
-  int n_pred;
-};
+__constant__ DfExpTables c_dfexp;
 
 // K_nu(x) e^x by the trapezoidal rule on K_nu(x) = int_0^inf exp(-x cosh t) cosh(nu t) dt
 // (the integrand is even and analytic in the strip |Im t| < pi/2, so the rule converges
@@ -42,7 +48,7 @@ __device__ double bessel_k_scaled(double nu, double x) {
   return h * sum;
 }
 
-// Correlation part of the covariance at scaled distance x = h / range > 0.
+// FP64 covariance at scaled distance x = h / range > 0.
 __device__ __forceinline__ double cov_of_x(const CovK& p, double x) {
   if (p.family == CR_COV_POWEXP) return p.sigma2 * exp(-pow(x, p.nu));
   switch (p.kind) {
@@ -56,67 +62,136 @@ __device__ __forceinline__ double cov_of_x(const CovK& p, double x) {
   }
 }
 
-__device__ __forceinline__ double cov_entry(const CovK& p, const double* __restrict__ xy, int n,
-                                            int gi, int gj, double xi, double yi) {
-  if (gi == gj) return p.sigma2 + p.nugget + (gi >= p.n_pred ? p.tau2 : 0.0);
-  const double dx = xi - xy[2 * gj], dy = yi - xy[2 * gj + 1];
+__device__ __forceinline__ double diag_value(const CovK& p, int gi) {
+  return p.sigma2 + p.nugget + (gi >= p.n_pred ? p.tau2 : 0.0);
+}
+
+// FP64 entry V[gi, gj] (valid indices).
+__device__ __forceinline__ double cov_entry64(const CovK& p, const double* __restrict__ xy, int gi, int gj) {
+  if (gi == gj) return diag_value(p, gi);
+  const double dx = xy[2 * gi] - xy[2 * gj], dy = xy[2 * gi + 1] - xy[2 * gj + 1];
   const double h = sqrt(dx * dx + dy * dy);
   if (h == 0.0) return p.sigma2;
   return cov_of_x(p, h * p.inv_range);
 }
 
-// One CTA per (lower tile, 64-row block).  Writes the FP64 tile rows and partial
-// statistics (sum of squares, min, max over valid entries) of its rows.
-__global__ void __launch_bounds__(256) k_cov_tiles(const double* __restrict__ xy, int n, int nb,
-                                                   CovK p, double* __restrict__ master,
-                                                   double* __restrict__ stat_part) {
-  const int t = blockIdx.x;
-  const int rbk = blockIdx.y;
-  const int nrb = gridDim.y;
-  int i = (int)floor((sqrt(8.0 * t + 1.0) - 1.0) * 0.5);
+// Double-float entry for an off-diagonal pair with coordinate differences (dx, dy); sets
+// *fallback when the scaled distance leaves the double-float exponential's range.
+__device__ __forceinline__ df cov_entry_df(const CovK& p, df dx, df dy, df sig, df inv_range, const DfExpTables& T,
+                                           bool* fallback) {
+  const df d2 = df_add(df_mul(dx, dx), df_mul(dy, dy));
+  if (d2.hi == 0.0f) return sig;
+  const df x = df_mul(df_sqrt(d2), inv_range);
+  if (x.hi > 80.0f) {
+    *fallback = true;
+    return {0.0f, 0.0f};
+  }
+  df v = df_exp(df_neg(x), T);
+  if (p.kind == 1) {
+    v = df_mul(df_add_f(x, 1.0f), v);
+  } else if (p.kind == 2) {
+    const df third = {0.3333333432674408f, -9.934107e-09f};   // 1/3 = hi + lo
+    v = df_mul(df_add_f(df_add(x, df_mul(df_mul(x, x), third)), 1.0f), v);
+  }
+  return df_mul(v, sig);
+}
+
+struct Pt {
+  df x, y;
+};
+
+__device__ __forceinline__ Pt load_pt(const double* xy, int g) {
+  return {df_from_double(xy[2 * g]), df_from_double(xy[2 * g + 1])};
+}
+
+__device__ __forceinline__ void tile_of(int t, int& i, int& j) {
+  i = (int)floor((sqrt(8.0 * t + 1.0) - 1.0) * 0.5);
   while (i * (i + 1) / 2 > t) --i;
   while ((i + 1) * (i + 2) / 2 <= t) ++i;
-  const int j = t - i * (i + 1) / 2;
+  j = t - i * (i + 1) / 2;
+}
 
-  __shared__ double s_x[64], s_y[64];
+// Statistics pass: one CTA per (lower tile, 64-row block); partial sum of squares, min and
+// max over valid entries.  Nothing is stored.
+template <bool DF>
+__global__ void __launch_bounds__(256) k_cov_stats(const double* __restrict__ xy, int n, int nb, CovK p,
+                                                   double* __restrict__ stat_part) {
+  int i, j;
+  tile_of(blockIdx.x, i, j);
+  const int rbk = blockIdx.y, nrb = gridDim.y;
   const int r0 = rbk * 64;
-  if (threadIdx.x < 64) {
-    const int gi = i * nb + r0 + threadIdx.x;
-    s_x[threadIdx.x] = gi < n ? xy[2 * gi] : 0.0;
-    s_y[threadIdx.x] = gi < n ? xy[2 * gi + 1] : 0.0;
+  extern __shared__ float4 s_pts[];   // nb column points then 64 row points, as (x.hi, x.lo, y.hi, y.lo)
+  float4* s_col = s_pts;
+  float4* s_row = s_pts + nb;
+  for (int q = threadIdx.x; q < nb + 64; q += blockDim.x) {
+    const int g = q < nb ? j * nb + q : i * nb + r0 + (q - nb);
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (g < n) {
+      const Pt pt = load_pt(xy, g);
+      v = make_float4(pt.x.hi, pt.x.lo, pt.y.hi, pt.y.lo);
+    }
+    s_pts[q] = v;
   }
+  // exponential tables in shared memory: their per-thread indices diverge
+  __shared__ DfExpTables s_T;
+  for (int q = threadIdx.x; q < 64; q += blockDim.x) {
+    s_T.t_hi[q] = c_dfexp.t_hi[q];
+    s_T.t_lo[q] = c_dfexp.t_lo[q];
+  }
+  if (threadIdx.x == 0) { s_T.c1 = c_dfexp.c1; s_T.c2 = c_dfexp.c2; s_T.c3 = c_dfexp.c3; }
   __syncthreads();
-
-  double ssq = 0.0, vmn = INFINITY, vmx = -INFINITY;
-  double* out = master + (size_t)t * nb * nb;
+  const df sig = {p.sig_hi, p.sig_lo}, invr = {p.invr_hi, p.invr_lo};
+  df ssq = {0.0f, 0.0f};
+  df dmn = {INFINITY, 0.0f}, dmx = {-INFINITY, 0.0f};   // double-float extrema (no FP64 work per entry)
+  double ssq64 = 0.0, vmn = INFINITY, vmx = -INFINITY;
   for (int idx = threadIdx.x; idx < 64 * nb; idx += blockDim.x) {
     const int r = r0 + idx / nb, c = idx % nb;
     const int gi = i * nb + r, gj = j * nb + c;
-    double v;
-    if (gi >= n || gj >= n) {
-      v = (gi == gj) ? 1.0 : 0.0;
+    if (gi >= n || gj >= n) continue;
+    if (DF) {
+      df v;
+      bool fb = gi == gj;
+      if (!fb) {
+        const float4 a = s_row[r - r0], b = s_col[c];
+        const df dx = df_add({a.x, a.y}, df_neg({b.x, b.y}));
+        const df dy = df_add({a.z, a.w}, df_neg({b.z, b.w}));
+        v = cov_entry_df(p, dx, dy, sig, invr, s_T, &fb);
+      }
+      if (fb) {   // diagonal entries and distances outside the double-float exponential: FP64
+        const double v64 = cov_entry64(p, xy, gi, gj);
+        ssq = df_add(ssq, df_from_double(v64 * v64));
+        vmn = fmin(vmn, v64);
+        vmx = fmax(vmx, v64);
+      } else {
+        ssq = df_add(ssq, df_mul(v, v));
+        if (df_lt(v, dmn)) dmn = v;
+        if (df_lt(dmx, v)) dmx = v;
+      }
     } else {
-      v = cov_entry(p, xy, n, gi, gj, s_x[r - r0], s_y[r - r0]);
-      ssq += v * v;
-      vmn = fmin(vmn, v);
-      vmx = fmax(vmx, v);
+      const double v64 = cov_entry64(p, xy, gi, gj);
+      ssq64 += v64 * v64;
+      vmn = fmin(vmn, v64);
+      vmx = fmax(vmx, v64);
     }
-    out[(size_t)r * nb + c] = v;
   }
-  // block reduction
+  if (DF) {
+    vmn = fmin(vmn, df_to_double(dmn));
+    vmx = fmax(vmx, df_to_double(dmx));
+  }
+  double s = DF ? df_to_double(ssq) : ssq64;
   __shared__ double red[3][8];
   for (int o = 16; o > 0; o >>= 1) {
-    ssq += __shfl_down_sync(0xffffffffu, ssq, o);
+    s += __shfl_down_sync(0xffffffffu, s, o);
     vmn = fmin(vmn, __shfl_down_sync(0xffffffffu, vmn, o));
     vmx = fmax(vmx, __shfl_down_sync(0xffffffffu, vmx, o));
   }
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  if (l == 0) { red[0][w] = ssq; red[1][w] = vmn; red[2][w] = vmx; }
+  if (l == 0) { red[0][w] = s; red[1][w] = vmn; red[2][w] = vmx; }
   __syncthreads();
   if (threadIdx.x == 0) {
     double a = 0.0, b = INFINITY, c = -INFINITY;
     for (int q = 0; q < (int)(blockDim.x >> 5); ++q) { a += red[0][q]; b = fmin(b, red[1][q]); c = fmax(c, red[2][q]); }
-    double* sp = stat_part + ((size_t)t * nrb + rbk) * 3;
+    double* sp = stat_part + ((size_t)blockIdx.x * nrb + rbk) * 3;
     sp[0] = a; sp[1] = b; sp[2] = c;
   }
 }
@@ -132,52 +207,85 @@ __global__ void k_stats_reduce(const double* __restrict__ part, int ntiles, int 
   stats[3 * t] = a; stats[3 * t + 1] = b; stats[3 * t + 2] = c;
 }
 
-// Scale by s^2 and round each tile to its class (Alg.2 step 12).
-__global__ void __launch_bounds__(256) k_convert(const double* __restrict__ master, int nb, double s2,
-                                                 TileView v) {
+// Generation of s^2 V in each tile's class (Alg.2 step 12).  One CTA per (tile, 64-row
+// block).  Padding rows/columns are the identity (scaled by s^2).
+__global__ void __launch_bounds__(256) k_generate(const double* __restrict__ xy, int n, int nb, CovK p, double s2,
+                                                  float s2_hi, float s2_lo, TileView v) {
   const int t = blockIdx.x;
-  const size_t base = (size_t)t * nb * nb;
-  const size_t count = (size_t)nb * nb;
+  int i, j;
+  tile_of(t, i, j);
+  const int r0 = blockIdx.y * 64;
   const int cls = v.cls[t];
-  const size_t chunk = count / gridDim.y;
-  const size_t beg = chunk * blockIdx.y;
-  const double2* src = reinterpret_cast<const double2*>(master + base + beg);
-  if (cls == CR_PREC_FP64) {
-    double2* dst = reinterpret_cast<double2*>(v.pool64 + (size_t)v.i64[t] * count + beg);
-    for (size_t q = threadIdx.x; q < chunk / 2; q += blockDim.x) {
-      double2 a = src[q];
-      dst[q] = make_double2(a.x * s2, a.y * s2);
+  const bool use_df = p.use_df && cls != CR_PREC_FP64;
+  extern __shared__ float4 s_pts[];
+  float4* s_col = s_pts;
+  float4* s_row = s_pts + nb;
+  if (use_df) {
+    for (int q = threadIdx.x; q < nb + 64; q += blockDim.x) {
+      const int g = q < nb ? j * nb + q : i * nb + r0 + (q - nb);
+      float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (g < n) {
+        const Pt pt = load_pt(xy, g);
+        w = make_float4(pt.x.hi, pt.x.lo, pt.y.hi, pt.y.lo);
+      }
+      s_pts[q] = w;
     }
-  } else if (cls == CR_PREC_FP32) {
-    float2* dst = reinterpret_cast<float2*>(v.pool32 + (size_t)v.i32[t] * count + beg);
-    for (size_t q = threadIdx.x; q < chunk / 2; q += blockDim.x) {
-      double2 a = src[q];
-      dst[q] = make_float2((float)(a.x * s2), (float)(a.y * s2));
+  }
+  __shared__ DfExpTables s_T;
+  for (int q = threadIdx.x; q < 64; q += blockDim.x) {
+    s_T.t_hi[q] = c_dfexp.t_hi[q];
+    s_T.t_lo[q] = c_dfexp.t_lo[q];
+  }
+  if (threadIdx.x == 0) { s_T.c1 = c_dfexp.c1; s_T.c2 = c_dfexp.c2; s_T.c3 = c_dfexp.c3; }
+  __syncthreads();
+  const size_t count = (size_t)nb * nb;
+  const df sig = {p.sig_hi, p.sig_lo}, invr = {p.invr_hi, p.invr_lo}, s2d = {s2_hi, s2_lo};
+  for (int idx = threadIdx.x; idx < 64 * nb; idx += blockDim.x) {
+    const int r = r0 + idx / nb, c = idx % nb;
+    const int gi = i * nb + r, gj = j * nb + c;
+    const size_t off = (size_t)r * nb + c;
+    double v64 = 0.0;
+    df vd = {0.0f, 0.0f};
+    bool have_df = false;
+    if (gi >= n || gj >= n) {
+      v64 = (gi == gj) ? s2 : 0.0;
+    } else if (use_df && gi != gj) {
+      const float4 a = s_row[r - r0], b = s_col[c];
+      const df dx = df_add({a.x, a.y}, df_neg({b.x, b.y}));
+      const df dy = df_add({a.z, a.w}, df_neg({b.z, b.w}));
+      bool fb = false;
+      vd = cov_entry_df(p, dx, dy, sig, invr, s_T, &fb);
+      if (fb) v64 = cov_entry64(p, xy, gi, gj) * s2;
+      else { vd = df_mul(vd, s2d); have_df = true; }
+    } else {
+      v64 = cov_entry64(p, xy, gi, gj) * s2;
     }
-  } else {
-    __half2* dst = reinterpret_cast<__half2*>(v.pool16 + (size_t)v.hi16[t] * count + beg);
-    for (size_t q = threadIdx.x; q < chunk / 2; q += blockDim.x) {
-      double2 a = src[q];
-      dst[q] = __halves2half2(__double2half(a.x * s2), __double2half(a.y * s2));
+    if (cls == CR_PREC_FP64) {
+      v.pool64[(size_t)v.i64[t] * count + off] = v64;
+    } else {
+      const float f = have_df ? __fadd_rn(vd.hi, vd.lo) : (float)v64;
+      if (cls == CR_PREC_FP32) v.pool32[(size_t)v.i32[t] * count + off] = f;
+      else v.pool16[(size_t)v.hi16[t] * count + off] = __float2half_rn(f);
     }
   }
 }
 
-// Dense column-major copy of the lower triangle (what = 0: covariance, 1: working tiles).
-__global__ void k_to_dense(const double* __restrict__ master, TileView v, int what, double* __restrict__ out, int ld) {
+// Dense column-major lower triangle of V (what = 0, FP64 evaluation) or of the working
+// tiles as stored (what = 1).
+__global__ void k_to_dense(const double* __restrict__ xy, CovK p, TileView v, int what, double* __restrict__ out, int ld) {
   const int n = v.n, nb = v.nb;
   const int gj = blockIdx.x * 32 + (threadIdx.x & 31);
   for (int gi = blockIdx.y * 8 + (threadIdx.x >> 5); gi < n; gi += gridDim.y * 8) {
     if (gj >= n) continue;
     double val = 0.0;
     if (gi >= gj) {
-      const int i = gi / nb, j = gj / nb, r = gi % nb, c = gj % nb;
-      const int t = tidx(i, j);
-      const size_t off = (size_t)r * nb + c;
-      const size_t count = (size_t)nb * nb;
       if (what == 0) {
-        val = master[(size_t)t * count + off];
+        val = cov_entry64(p, xy, gi, gj);
       } else {
+        const int i = gi / nb, j = gj / nb, r = gi % nb, c = gj % nb;
+        const int t = tidx(i, j);
+        const size_t off = (size_t)r * nb + c;
+        const size_t count = (size_t)nb * nb;
         const int cls = v.cls[t];
         if (cls == CR_PREC_FP64) val = v.pool64[(size_t)v.i64[t] * count + off];
         else if (cls == CR_PREC_FP32) val = (double)v.pool32[(size_t)v.i32[t] * count + off];
@@ -187,6 +295,49 @@ __global__ void k_to_dense(const double* __restrict__ master, TileView v, int wh
     out[(size_t)gj * ld + gi] = val;
   }
 }
+
+__global__ void k_cov_block(CovK p, const double* __restrict__ xy, int r0, int c0, int m, int k, double* __restrict__ out,
+                            int ld) {
+  const size_t total = (size_t)m * k;
+  for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < total; e += (size_t)gridDim.x * blockDim.x) {
+    const int jj = (int)(e / m), ii = (int)(e % m);
+    out[(size_t)jj * ld + ii] = cov_entry64(p, xy, r0 + ii, c0 + jj);
+  }
+}
+
+cr_status cov_block_launch(const CovK& p, const double* xy, int n, int r0, int c0, int m, int k, double* out, int ld,
+                           cudaStream_t s) {
+  (void)n;
+  k_cov_block<<<2048, 256, 0, s>>>(p, xy, r0, c0, m, k, out, ld);
+  CR_CHECK_LAUNCH("k_cov_block");
+  return CR_OK;
+}
+
+// Per-device upload of the double-float exponential's constants.
+static cr_status ensure_df_tables() {
+  static std::mutex mu;
+  static bool done[64] = {false};
+  int dev = 0;
+  CR_CUDA(cudaGetDevice(&dev));
+  std::lock_guard<std::mutex> lk(mu);
+  if (dev < 64 && done[dev]) return CR_OK;
+  DfExpTables T;
+  for (int q = 0; q < 64; ++q) {
+    const df d = df_from_double(exp2((double)q / 64.0));
+    T.t_hi[q] = d.hi;
+    T.t_lo[q] = d.lo;
+  }
+  const double c = log(2.0) / 64.0;                 // in [2^-7, 2^-6): 11 significant bits -> step 2^-17
+  const double c1 = nearbyint(c * 131072.0) / 131072.0;
+  T.c1 = (float)c1;
+  T.c2 = (float)(c - c1);
+  T.c3 = (float)(c - c1 - (double)T.c2);
+  CR_CUDA(cudaMemcpyToSymbol(c_dfexp, &T, sizeof(T)));
+  if (dev < 64) done[dev] = true;
+  return CR_OK;
+}
+
+cr_status fetch_stats(cr_tilemat V);
 
 }  // namespace cr
 
@@ -200,6 +351,7 @@ extern "C" cr_status cr_cov_build(cr_tilemat V, const double* d_xy, const cr_cov
     return fail(CR_ERR_ARG, "cr_cov_build: parameter out of range");
   if (p->family == CR_COV_POWEXP && p->nu > 2.0) return fail(CR_ERR_ARG, "cr_cov_build: power-exponential needs nu <= 2");
   CR_CUDA(cudaSetDevice(V->device));
+  CR_TRY(ensure_df_tables());
   CovK k{};
   k.family = p->family;
   k.sigma2 = p->sigma2;
@@ -215,13 +367,22 @@ extern "C" cr_status cr_cov_build(cr_tilemat V, const double* d_xy, const cr_cov
     else if (p->nu == 2.5) k.kind = 2;
     k.norm = exp((1.0 - p->nu) * log(2.0) - lgamma(p->nu));
   }
+  k.use_df = (p->family == CR_COV_MATERN && k.kind <= 2) ? 1 : 0;
+  {
+    const df a = df_from_double(k.sigma2), b = df_from_double(k.inv_range);
+    k.sig_hi = a.hi; k.sig_lo = a.lo; k.invr_hi = b.hi; k.invr_lo = b.lo;
+  }
+  CR_CUDA(cudaMemcpyAsync(V->xy, d_xy, (size_t)V->n * 2 * sizeof(double), cudaMemcpyDeviceToDevice, stream));
   const int nrb = V->nb / 64;
   dim3 grid(V->ntiles, nrb);
-  k_cov_tiles<<<grid, 256, 0, stream>>>(d_xy, V->n, V->nb, k, V->master, V->stat_part);
-  CR_CHECK_LAUNCH("k_cov_tiles");
+  const size_t smem = (size_t)(V->nb + 64) * sizeof(float4);
+  if (k.use_df) k_cov_stats<true><<<grid, 256, smem, stream>>>(V->xy, V->n, V->nb, k, V->stat_part);
+  else k_cov_stats<false><<<grid, 256, smem, stream>>>(V->xy, V->n, V->nb, k, V->stat_part);
+  CR_CHECK_LAUNCH("k_cov_stats");
   k_stats_reduce<<<(V->ntiles + 127) / 128, 128, 0, stream>>>(V->stat_part, V->ntiles, nrb, V->stats);
   CR_CHECK_LAUNCH("k_stats_reduce");
   V->params = *p;
+  V->covk = k;
   V->built = true;
   V->stats_on_host = false;
   V->mapped = false;
@@ -250,9 +411,12 @@ cr_status fetch_stats(cr_tilemat V) {
 }
 
 cr_status convert_tiles(cr_tilemat V, cudaStream_t stream) {
-  dim3 grid(V->ntiles, 8);
-  k_convert<<<grid, 256, 0, stream>>>(V->master, V->nb, V->s * V->s, V->view());
-  CR_CHECK_LAUNCH("k_convert");
+  dim3 grid(V->ntiles, V->nb / 64);
+  const size_t smem = (size_t)(V->nb + 64) * sizeof(float4);
+  const double s2 = V->s * V->s;
+  const df s2d = df_from_double(s2);
+  k_generate<<<grid, 256, smem, stream>>>(V->xy, V->n, V->nb, V->covk, s2, s2d.hi, s2d.lo, V->view());
+  CR_CHECK_LAUNCH("k_generate");
   return CR_OK;
 }
 }  // namespace cr
@@ -278,7 +442,7 @@ extern "C" cr_status cr_tilemat_to_dense(cr_tilemat V, int what, double* d_out, 
   if (what == 1 && !V->mapped) return fail(CR_ERR_STATE, "cr_tilemat_to_dense: no working tiles yet");
   CR_CUDA(cudaSetDevice(V->device));
   dim3 grid((V->n + 31) / 32, 64);
-  k_to_dense<<<grid, 256, 0, stream>>>(V->master, V->view(), what, d_out, ld);
+  k_to_dense<<<grid, 256, 0, stream>>>(V->xy, V->covk, V->view(), what, d_out, ld);
   CR_CHECK_LAUNCH("k_to_dense");
   return CR_OK;
 }

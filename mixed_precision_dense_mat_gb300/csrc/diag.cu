@@ -88,10 +88,11 @@ __device__ __forceinline__ void load_block_t(double (*S)[DB + 1], const double* 
   }
 }
 
+// Cholesky of the DB x DB block k held (lower part) in L, in place, with its inverse in X;
+// then both are written to the tile (factor, lower part) and to Minv (inverse, upper zero).
 template <int DB>
-__device__ void task_potrf(const Ctx& c, int k, double (*L)[DB + 1], double (*X)[DB + 1], double* s_r) {
+__device__ void potrf_block(const Ctx& c, int k, double (*L)[DB + 1], double (*X)[DB + 1], double* s_r) {
   double* a = c.A + (size_t)(k * DB) * c.nb + k * DB;
-  load_block<DB>(L, a, c.nb, true);
   for (int idx = threadIdx.x; idx < DB * DB; idx += blockDim.x) {
     const int r = idx / DB, q = idx % DB;
     X[r][q] = (r == q) ? 1.0 : 0.0;
@@ -151,6 +152,25 @@ struct Frag {
       for (int x = 0; x < PER; ++x) acc[x] = fma(a, Q[c0 + x * (DB / PER)][q], acc[x]);
     }
   }
+  // S(r, col) += alpha acc (lower part only when asked)
+  __device__ void add_to(double (*S)[DB + 1], double alpha, bool lower_only) {
+    const int r = threadIdx.x / (DB / PER), c0 = threadIdx.x % (DB / PER);
+#pragma unroll
+    for (int x = 0; x < PER; ++x) {
+      const int col = c0 + x * (DB / PER);
+      if (!(lower_only && col > r)) S[r][col] += alpha * acc[x];
+    }
+  }
+  // S(r, col) = acc and dst(r, col) = acc
+  __device__ void put(double (*S)[DB + 1], double* dst, int ld) {
+    const int r = threadIdx.x / (DB / PER), c0 = threadIdx.x % (DB / PER);
+#pragma unroll
+    for (int x = 0; x < PER; ++x) {
+      const int col = c0 + x * (DB / PER);
+      S[r][col] = acc[x];
+      dst[(size_t)r * ld + col] = acc[x];
+    }
+  }
   // dst(r, col) = alpha acc (+ dst when accumulate)
   __device__ void store(double* dst, int ld, double alpha, bool accumulate, bool lower_only) {
     const int r = threadIdx.x / (DB / PER), c0 = threadIdx.x % (DB / PER);
@@ -181,15 +201,67 @@ __device__ void chain_product(const Ctx& c, const double* Prow, const double* Qc
   f.store(dst, c.nb, alpha, false, false);
 }
 
+// The critical chain, run by one CTA with the blocks kept in shared memory:
+// POTRF(0); then for k = 0 .. NB-2: TRSM(k+1,k), SYRK(k+1,k+1,k), POTRF(k+1).
 template <int DB>
-__global__ void __launch_bounds__(256) k_diag_chol(Ctx c, const int4* __restrict__ tasks, int ntasks, int* counter) {
+__device__ void run_chain(const Ctx& c, double (*S0)[DB + 1], double (*S1)[DB + 1], double (*S2)[DB + 1],
+                          double (*S3)[DB + 1], double* s_r, int* s_ok) {
+  const int NB = c.NB;
+  const size_t rowstride = (size_t)DB * c.nb;
+  load_block<DB>(S0, c.A, c.nb, true);
+  potrf_block<DB>(c, 0, S0, S1, s_r);   // S1 = M_00
+  __syncthreads();
+  if (threadIdx.x == 0) st_release(&c.fac[0], 1);
+  for (int k = 0; k + 1 < NB; ++k) {
+    const int i = k + 1;
+    // TRSM(i, k): L_ik = A_ik M_kk^T, M_kk in S1
+    if (threadIdx.x == 0) *s_ok = wait_ge(c, &c.ver[i * NB + k], k) ? 1 : 0;
+    __syncthreads();
+    if (!*s_ok) return;
+    load_block<DB>(S2, c.A + i * rowstride + k * DB, c.nb);
+    __syncthreads();
+    Frag<DB> f;
+    f.zero();
+    f.mac(S2, S1);
+    f.put(S3, c.A + i * rowstride + k * DB, c.nb);   // S3 = L_ik
+    __syncthreads();
+    if (threadIdx.x == 0) st_release(&c.fac[i * NB + k], 1);
+    // SYRK(i, i, k) into the diagonal block, then POTRF(i)
+    if (threadIdx.x == 0) *s_ok = wait_ge(c, &c.ver[i * NB + i], k) ? 1 : 0;
+    __syncthreads();
+    if (!*s_ok) return;
+    load_block<DB>(S0, c.A + i * rowstride + i * DB, c.nb, true);
+    __syncthreads();
+    Frag<DB> g;
+    g.zero();
+    g.mac(S3, S3);
+    g.add_to(S0, -1.0, true);
+    __syncthreads();
+    potrf_block<DB>(c, i, S0, S1, s_r);   // S1 = M_ii
+    __syncthreads();
+    if (threadIdx.x == 0) st_release(&c.fac[i * NB + i], 1);
+  }
+}
+
+template <int DB>
+__global__ void __launch_bounds__(256) k_diag_chol(Ctx c, const int4* __restrict__ tasks, int ntasks, int* counter,
+                                                   int* role) {
   __shared__ double S0[DB][DB + 1];
   __shared__ double S1[DB][DB + 1];
+  __shared__ double S2[DB][DB + 1];
+  __shared__ double S3[DB][DB + 1];
   __shared__ double s_r;
   __shared__ int s_task;
   __shared__ int s_ok;
   const int NB = c.NB;
   const size_t rowstride = (size_t)DB * c.nb;
+  // the first CTA to start takes the critical chain: it is resident, so the chain progresses
+  if (threadIdx.x == 0) s_task = atomicAdd(role, 1);
+  __syncthreads();
+  if (s_task == 0) {
+    run_chain<DB>(c, S0, S1, S2, S3, &s_r, &s_ok);
+    return;
+  }
   while (true) {
     if (threadIdx.x == 0) s_task = atomicAdd(counter, 1);
     __syncthreads();
@@ -223,9 +295,7 @@ __global__ void __launch_bounds__(256) k_diag_chol(Ctx c, const int4* __restrict
     }
     __syncthreads();
     if (!s_ok) break;
-    if (type == T_POTRF) {
-      task_potrf<DB>(c, tk.w, S0, S1, &s_r);
-    } else if (type == T_TRSM) {
+    if (type == T_TRSM) {
       const int i = tk.y, k = tk.w;
       double* a = c.A + i * rowstride + k * DB;
       load_block<DB>(S0, a, c.nb);
@@ -256,9 +326,9 @@ __global__ void __launch_bounds__(256) k_diag_chol(Ctx c, const int4* __restrict
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-      __threadfence();
-      if (type == T_POTRF) st_release(&c.fac[tk.w * NB + tk.w], 1);
-      else if (type == T_TRSM) st_release(&c.fac[tk.y * NB + tk.w], 1);
+      // the barrier orders the CTA's stores before this thread's release store, which makes
+      // them visible at GPU scope to an acquiring reader of the flag
+      if (type == T_TRSM) st_release(&c.fac[tk.y * NB + tk.w], 1);
       else if (type == T_UPDATE) st_release(&c.ver[tk.y * NB + tk.z], tk.w + 1);
       else if (type == T_TMUL) st_release(&c.tfl[tk.y * NB + tk.z], 1);
       else st_release(&c.inv[tk.y * NB + tk.z], 1);
@@ -270,11 +340,12 @@ __global__ void __launch_bounds__(256) k_diag_chol(Ctx c, const int4* __restrict
 
 void diag_task_list(int NB, std::vector<int4>& tasks) {
   tasks.clear();
+  // POTRF(k), TRSM(k+1,k) and UPDATE(k+1,k+1,k) belong to the chain CTA and are not queued
   for (int k = 0; k < NB; ++k) {
-    tasks.push_back(make_int4(T_POTRF, k, k, k));
-    for (int i = k + 1; i < NB; ++i) tasks.push_back(make_int4(T_TRSM, i, k, k));
+    for (int i = k + 2; i < NB; ++i) tasks.push_back(make_int4(T_TRSM, i, k, k));
     for (int j = k + 1; j < NB; ++j)
-      for (int i = j; i < NB; ++i) tasks.push_back(make_int4(T_UPDATE, i, j, k));
+      for (int i = j; i < NB; ++i)
+        if (!(i == k + 1 && j == k + 1)) tasks.push_back(make_int4(T_UPDATE, i, j, k));
     // doubling steps whose pair ends with diagonal block k, smallest pairs first
     for (int s = 1; 2 * s <= NB; s *= 2) {
       const int base = k + 1 - 2 * s;
@@ -295,6 +366,7 @@ cr_status diag_chol_launch(int db, double* A, double* Minv, double* T, int nb, i
   c.ver = flags; c.fac = flags + NB * NB; c.inv = flags + 2 * NB * NB; c.tfl = flags + 3 * NB * NB;
   c.abort_flag = flags + 4 * NB * NB;
   int* counter = flags + 4 * NB * NB + 1;
+  int* role = flags + 4 * NB * NB + 2;
   c.status = status; c.gcol0 = gcol0;
   CR_CUDA(cudaMemsetAsync(flags, 0, diag_flag_words(nb, db) * sizeof(int), s));
   static bool configured = false;
@@ -305,8 +377,8 @@ cr_status diag_chol_launch(int db, double* A, double* Minv, double* T, int nb, i
     CR_CUDA(cudaFuncSetAttribute(k_diag_chol<32>, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared));
     configured = true;
   }
-  if (db == 16) k_diag_chol<16><<<grid, 256, 0, s>>>(c, d_tasks, ntasks, counter);
-  else if (db == 32) k_diag_chol<32><<<grid, 256, 0, s>>>(c, d_tasks, ntasks, counter);
+  if (db == 16) k_diag_chol<16><<<grid, 256, 0, s>>>(c, d_tasks, ntasks, counter, role);
+  else if (db == 32) k_diag_chol<32><<<grid, 256, 0, s>>>(c, d_tasks, ntasks, counter, role);
   else return fail(CR_ERR_ARG, "diag_chol_launch: block size");
   CR_CHECK_LAUNCH("k_diag_chol");
   return CR_OK;

@@ -7,10 +7,10 @@
 namespace cr {
 
 // Flag words needed by diag_chol_launch for a tile of size nb and block size db (16 or 32):
-// ver, fac, inv, tfl (NB^2 each), the abort flag and the task counter.
+// ver, fac, inv, tfl (NB^2 each), the abort flag, the task counter and the role counter.
 inline int diag_flag_words(int nb, int db) {
   const int NB = nb / db;
-  return 4 * NB * NB + 2;
+  return 4 * NB * NB + 3;
 }
 
 // Fixed topological task order for NB x NB blocks (type, i, j, k / s).
