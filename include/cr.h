@@ -166,15 +166,15 @@ cr_status cr_trmm_sim(cr_tilemat L, const double* d_Z, int ldz, int M, uint64_t 
                       uint64_t offset, double* d_Y, int ldy, int flags, double* h_bnorm,
                       cr_stream stream);
 
-/* Universal kriging (Section V-A Eq.5-6, Alg.2 steps 2-6) from the FP64 covariance held
- * by V (built with n_pred prediction sites first, n_pred a multiple of nb): Sigma_y is
- * the observation block, V_op the n_o x n_p observation/prediction block.  d_Xo (n_o x 3)
- * and d_Xp (n_p x 3) are column-major trend designs, d_yo the n_o observations.
- * Outputs: d_W (n_o x n_p column-major, ldw >= n_o) weights, d_zhat (n_p) prediction,
- * d_v (n_p) pointwise MSPE with theta0 = sigma2.  Must be called before
- * cr_potrf_adaptive overwrites nothing it needs (it reads only cr_cov_build's FP64
- * tiles, which the factorisation keeps).  *info as in cr_potrf_adaptive for Sigma_y.
- * Synchronises. */
+/* Universal kriging (Section V-A Eq.5-6, Alg.2 steps 2-6), all in FP64, for the
+ * covariance model and locations of V (built by cr_cov_build with n_pred prediction sites
+ * first and n_o = n - n_pred observation sites): Sigma_y = V_o + tau2 I is factored as its
+ * own FP64 tile matrix, V_op (the n_o x n_p observation/prediction block) is evaluated in
+ * FP64.  d_Xo (n_o x 3) and d_Xp (n_p x 3) are column-major trend designs, d_yo the n_o
+ * observations.  Outputs: d_W (n_o x n_p column-major, ldw >= n_o) weights, d_zhat (n_p)
+ * prediction W^T y_o, d_v (n_p) pointwise MSPE with theta0 = sigma2.  Independent of V's
+ * precision map and factor (callable before or after cr_potrf_adaptive).  *info as in
+ * cr_potrf_adaptive, for Sigma_y.  Allocates its workspace internally.  Synchronises. */
 cr_status cr_krige(cr_tilemat V, const double* d_Xo, const double* d_Xp, const double* d_yo,
                    double* d_W, int ldw, double* d_zhat, double* d_v, cr_stream stream,
                    int* info);

@@ -216,6 +216,13 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
         CR_CHECK_LAUNCH("k_zero_upper");
         return CR_OK;
       });
+      if (V->minv_all) {
+        double* keep = V->minv_all + (size_t)j * nb2;
+        P.ops.push_back([=](Exec& x) -> cr_status {
+          CR_CUDA(cudaMemcpyAsync(keep, Minv, nb2 * sizeof(double), cudaMemcpyDeviceToDevice, x.hi));
+          return CR_OK;
+        });
+      }
     }
     if (V->amp) {
       __half* mh = V->pool16 + (size_t)V->minv_hi * nb2;

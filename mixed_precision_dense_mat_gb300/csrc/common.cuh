@@ -102,6 +102,7 @@ struct cr_tilemat_s {
   float* w32 = nullptr;           // 2 * nt * nb * nb: FP32 intermediate of FP16/FP32-class tiles (same)
   cudaStream_t s_hi = nullptr, s_lo = nullptr;   // critical chain / bulk updates
   double* minv = nullptr;         // nb * nb: inverse of the current diagonal factor
+  double* minv_all = nullptr;     // nt * nb * nb: every diagonal factor's inverse (kept on request)
   double* scratch64 = nullptr;    // nb * nb: temporaries of the diagonal factorisation
   int* d_status = nullptr;        // [0] device error bits, [1] first failing column (1-based) or 0, [2] Minv exponent
   CUtensorMap tm_pool16;          // 3-D map over pool16 (slot, row, col)
