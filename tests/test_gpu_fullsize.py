@@ -1,0 +1,143 @@
+"""Parity at the benchmark sizes, in the configuration bench.py runs, on outputs the oracle
+can compute piece by piece and on properties that hold at any size:
+  * tile statistics of sampled tiles against the oracle's;
+  * the precision map, checks and scale recomputed by the oracle's policy from the GPU's
+    statistics (host logic, bit-exact);
+  * the leading principal block of the factor and of the simulations: the Cholesky factor
+    of a leading block of V is the leading block of the full factor, and Y = L Z is lower
+    triangular, so the oracle computes both exactly on that block;
+  * sampled rows of Y against the GPU's own factor (the simulation multiply at full K);
+  * the calibration of the GPU's simulations, bit-exact against the oracle;
+  * kriging at 16384 + 16384 sites: unbiasedness X_o^T W = X_p^T and positive MSPEs.
+"""
+import numpy as np
+import pytest
+import torch
+
+import inputgen
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def colmajor(a):
+    return torch.from_numpy(np.asfortranarray(a).T.copy()).cuda().T
+
+
+def relf(a, b):
+    return np.linalg.norm(a - b) / np.linalg.norm(b)
+
+
+def _sampled_stats_check(w, xy, f, mn, mx, rng, count=24):
+    nt = f.shape[0]
+    picks = {(0, 0), (nt - 1, nt - 1), (nt - 1, 0)}
+    while len(picks) < count:
+        i = int(rng.integers(0, nt))
+        picks.add((i, int(rng.integers(0, i + 1))))
+    n, nb = w.n, w.nb
+    for (i, j) in picks:
+        T = oracle.covariance_matrix(xy, w.family, w.sigma2, w.beta, w.nu, w.nugget, w.n_pred, w.tau2,
+                                     rows=slice(i * nb, min(n, (i + 1) * nb)), cols=slice(j * nb, min(n, (j + 1) * nb)))
+        assert f[i, j] == pytest.approx(np.linalg.norm(T), rel=1e-12)
+        assert mn[i, j] == pytest.approx(T.min(), rel=1e-12, abs=1e-300)
+        assert mx[i, j] == pytest.approx(T.max(), rel=1e-12)
+
+
+def _policy_check(f, mn, mx, pmap, info, fixedacc):
+    ref = oracle.select_precision(f, mn, mx, fixedacc, auto=False)
+    low = np.tril(np.ones(pmap.shape, dtype=bool))
+    np.testing.assert_array_equal(pmap[low], ref["map"][low])
+    assert info["s"] == ref["s"]
+    assert bool(info["check1"]) == ref["check1"] and bool(info["check2"]) == ref["check2"]
+
+
+def _leading_block(lib, V, w, xy, Z, Y, s, n_s, tol_L, tol_Y):
+    Vo = oracle.covariance_matrix(xy[:n_s], w.family, w.sigma2, w.beta, w.nu, w.nugget)
+    Lo = oracle.cholesky_lower(Vo)
+    Ld = lib.tilemat_to_dense(V, 1)
+    Lg = Ld[:n_s, :n_s].cpu().numpy() / s
+    eL = relf(Lg, Lo)
+    eY = relf(Y[:n_s], oracle.simulate(Lo, Z[:n_s]))
+    assert eL <= tol_L and eY <= tol_Y, (eL, eY)
+    return Ld
+
+
+def test_headline_workload_full_size(lib):
+    w = inputgen.WORKLOADS["c"]
+    rng = np.random.default_rng(0)
+    xy = inputgen.workload_locations(w)
+    V = lib.TileMat(w.n, w.nb)
+    lib.cov_build(V, dev(xy), w.family, w.sigma2, w.beta, w.nu, nugget=w.nugget)
+    f, mn, mx = lib.tile_stats(V)
+    _sampled_stats_check(w, xy, f, mn, mx, rng)
+    pmap, info = lib.precision_map(V, amp=True, fixedacc=w.fixedacc)
+    _policy_check(f, mn, mx, pmap, info, w.fixedacc)
+    assert info["n_fp16"] > info["n_fp32"] > 0           # majority FP16 tiles at this tolerance
+    assert lib.potrf_adaptive(V) == 0
+    Z = inputgen.standard_normals(w.n, w.M, 12345)
+    Yt = lib.trmm_sim(V, colmajor(Z), w.M)
+    Y = Yt.cpu().numpy()
+    s = info["s"]
+    Ld = _leading_block(lib, V, w, xy, Z, Y, s, 2048, 1e-2, 1e-2)
+    # sampled rows at full K-chain length against the GPU's own factor
+    rows = np.sort(rng.choice(w.n, 12, replace=False))
+    Lr = Ld[torch.from_numpy(rows).cuda()].cpu().numpy() / s
+    del Ld
+    torch.cuda.empty_cache()
+    assert relf(Y[rows], Lr @ Z) <= 2e-3
+    # calibration of these simulations (no observations: zhat = 0, v = V_ii), bit-exact
+    v = np.full(w.n, w.sigma2 + w.nugget)
+    out = lib.calibrate(Yt, dev(np.zeros(w.n)), dev(v), w.u, w.level, counts=True)
+    ref = oracle.calibrate(Y, np.zeros(w.n), v, w.u, w.level)
+    assert out["q_in"] == ref["q_in"] and out["q_out"] == ref["q_out"]
+    np.testing.assert_array_equal(out["count"].cpu().numpy(), ref["count"])
+    np.testing.assert_array_equal(out["c_in"].cpu().numpy(), ref["c_in"])
+    np.testing.assert_array_equal(out["c_out"].cpu().numpy(), ref["c_out"])
+    V.close()
+
+
+def test_strong_correlation_workload_full_size(lib):
+    w = inputgen.WORKLOADS["b"]
+    rng = np.random.default_rng(1)
+    xy = inputgen.workload_locations(w)
+    V = lib.TileMat(w.n, w.nb)
+    lib.cov_build(V, dev(xy), w.family, w.sigma2, w.beta, w.nu, nugget=w.nugget)
+    f, mn, mx = lib.tile_stats(V)
+    _sampled_stats_check(w, xy, f, mn, mx, rng)
+    pmap, info = lib.precision_map(V, amp=True, fixedacc=w.fixedacc)
+    _policy_check(f, mn, mx, pmap, info, w.fixedacc)
+    assert lib.potrf_adaptive(V) == 0
+    Z = inputgen.standard_normals(w.n, w.M, 7)
+    Y = lib.trmm_sim(V, colmajor(Z), w.M).cpu().numpy()
+    lead = 2048 // w.nb
+    all64 = bool(np.all(pmap[:lead, :lead][np.tril(np.ones((lead, lead), dtype=bool))] == 0))
+    # leading tiles in FP64 keep FP64 accuracy of the factor; the simulation multiply runs
+    # on FP16 operands in the adaptive mode (Alg.1)
+    _leading_block(lib, V, w, xy, Z, Y, info["s"], 2048, 1e-9 if all64 else 1e-2, 1e-2)
+    V.close()
+
+
+def test_kriging_workload_full_size(lib):
+    w = inputgen.WORKLOADS["k"]
+    xy = inputgen.workload_locations(w)
+    n_p, n_o = w.n_pred, w.n_obs
+    X = np.column_stack([np.ones(w.n), xy[:, 0], xy[:, 1]])
+    y = inputgen.observation_values(xy[n_p:], (1.0, 0.5, -0.3), 0.1, 3)
+    V = lib.TileMat(w.n, w.nb)
+    lib.cov_build(V, dev(xy), w.family, w.sigma2, w.beta, w.nu, nugget=w.nugget, n_pred=n_p, tau2=w.tau2)
+    W, z, v = lib.krige(V, colmajor(X[n_p:]), colmajor(X[:n_p]), dev(y))
+    Wt = W
+    # unbiasedness, evaluated on the device in FP64
+    XoT_W = (torch.from_numpy(X[n_p:]).cuda().T @ Wt).cpu().numpy()
+    assert np.max(np.abs(XoT_W - X[:n_p].T)) <= 1e-6 * np.max(np.abs(X[:n_p]))
+    vv = v.cpu().numpy()
+    assert np.all(vv > 0) and np.all(vv < 2 * w.sigma2)
+    zz = z.cpu().numpy()
+    assert np.all(np.isfinite(zz))
+    # prediction at a grid site next to an observation is close to the trend plus noise scale
+    assert abs(np.mean(zz) - np.mean(1.0 + 0.5 * xy[:n_p, 0] - 0.3 * xy[:n_p, 1])) < 0.1
+    V.close()
