@@ -77,7 +77,6 @@ DJob job(double* C, int sCm, int sCn, int m, int n, int pbeg, int pcnt, double a
 cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
   const int nt = V->nt, nb = V->nb;
   const size_t nb2 = (size_t)nb * nb;
-  const int nsb = nb / TC_BM;
   const auto& cls = V->h_cls;
   auto t64 = [&](int i, int j) { return V->pool64 + (size_t)V->h_i64[tidx(i, j)] * nb2; };
   auto ws64 = [&](int par, int i) { return V->ws64 + ((size_t)par * nt + i) * nb2; };
@@ -155,8 +154,8 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
       t.rows = nullptr;
       t.kbeg = 0;
       t.kend = kold_end;
-      const int grid = (nt - j) * nsb * nsb;
-      P.ops.push_back([=](Exec& x) -> cr_status { return tc_launch(t, *tm, *tm, grid, x.lo); });
+      t.nrows = nt - j;
+      P.ops.push_back([=](Exec& x) -> cr_status { return tc_launch(t, *tm, *tm, x.lo); });
     } else {
       for (int i = j + 1; i < nt; ++i) {
         double* dst = ws64(par, i);
@@ -195,8 +194,8 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
       t.rows = nullptr;
       t.kbeg = knew >= 0 ? knew : 0;
       t.kend = knew >= 0 ? j : 0;
-      const int grid = (nt - j) * nsb * nsb;
-      P.ops.push_back([=](Exec& x) -> cr_status { return tc_launch(t, *tm, *tm, grid, x.hi); });
+      t.nrows = nt - j;
+      P.ops.push_back([=](Exec& x) -> cr_status { return tc_launch(t, *tm, *tm, x.hi); });
     }
 
     // ---------------- diagonal factor and its inverse (FP64 dataflow executor)
@@ -205,8 +204,9 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
     double* T = V->scratch64;
     {
       const int db = V->diag_db, ntask = V->diag_ntasks, g = j * nb;
-      int dgrid = 152;
-      if (const char* e = getenv("CR_DIAG_GRID")) dgrid = atoi(e);
+      // one executor CTA per SM: the chain CTA plus one worker per remaining SM
+      int dgrid = 0;
+      CR_CUDA(cudaDeviceGetAttribute(&dgrid, cudaDevAttrMultiProcessorCount, V->device));
       int* flags = V->diag_flags;
       const int4* tasks = V->diag_tasks;
       P.ops.push_back([=](Exec& x) -> cr_status {
@@ -242,8 +242,8 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
       TcParams t = tp;
       t.mode = TC_TRSM;
       t.rows = d_rows + rows_off[j];
-      const int grid = ntc * nsb * nsb;
-      P.ops.push_back([=](Exec& x) -> cr_status { return tc_launch(t, *tm, *tm, grid, x.hi); });
+      t.nrows = ntc;
+      P.ops.push_back([=](Exec& x) -> cr_status { return tc_launch(t, *tm, *tm, x.hi); });
     }
     {
       std::vector<DJob> js;
@@ -282,7 +282,7 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
   }
   Exec x;
   x.hi = V->s_hi;
-  x.lo = getenv("CR_SERIAL") ? V->s_hi : V->s_lo;
+  x.lo = V->s_lo;
   x.ev.resize(2 * nt);
   cr_status st = CR_OK;
   for (auto& e : x.ev) cudaEventCreateWithFlags(&e, cudaEventDisableTiming);
@@ -329,16 +329,14 @@ extern "C" cr_status cr_potrf_adaptive(cr_tilemat V, cr_stream stream, int* info
   if (!V->mapped) return fail(CR_ERR_STATE, "cr_potrf_adaptive: call cr_precision_map first");
   CR_CUDA(cudaSetDevice(V->device));
   // block size of the diagonal-tile dataflow factorisation
-  int db = 16;
-  if (const char* e = getenv("CR_DIAG_DB")) db = atoi(e);
-  if (db != 16 && db != 32) db = 16;
+  const int db = 16;
   if (db != V->diag_db) {
     if (V->diag_tasks) cudaFree(V->diag_tasks);
     if (V->diag_flags) cudaFree(V->diag_flags);
     V->diag_tasks = nullptr;
     V->diag_flags = nullptr;
     std::vector<int4> tasks;
-    diag_task_list(V->nb / db, tasks);
+    if (!diag_task_list(V->nb / db, tasks)) return fail(CR_ERR_STATE, "cr_potrf_adaptive: diagonal task list failed its progress check");
     CR_CUDA(cudaMalloc(&V->diag_tasks, tasks.size() * sizeof(int4)));
     CR_CUDA(cudaMemcpy(V->diag_tasks, tasks.data(), tasks.size() * sizeof(int4), cudaMemcpyHostToDevice));
     CR_CUDA(cudaMalloc(&V->diag_flags, diag_flag_words(V->nb, db) * sizeof(int)));

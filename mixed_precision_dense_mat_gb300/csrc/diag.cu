@@ -1,28 +1,36 @@
 // FP64 factorisation of one diagonal tile, L_jj = chol(A_jj), together with its inverse
 // M = L_jj^-1, as an on-device dataflow executor.
 //
-// The nb x nb tile is cut into DB x DB blocks.  The blocked Cholesky DAG (the tile-DAG
+// The nb x nb tile is cut into 16 x 16 blocks.  The blocked Cholesky DAG (the tile-DAG
 // formulation of Section IV-A of "Mixed-Precision GPU Acceleration for Confidence Regions
-// of Spatial Excursion Sets", here inside one tile and on one GPU) is listed in a fixed
-// topological order:
-//   POTRF(k)      factor block (k,k) and invert it                   needs ver(k,k) = k
-//   TRSM(i,k)     L_ik = A_ik M_kk^T                                 needs POTRF(k), ver(i,k) = k
-//   UPDATE(i,j,k) A_ij -= L_ik L_jk^T  (k < j <= i)                   needs TRSM(i,k), TRSM(j,k), ver(i,j) = k
-// The inverse is assembled by recursive doubling: for every aligned pair of diagonal
-// super-blocks of s blocks each, [[L11, 0], [L21, L22]]^-1 has lower-left part
-// M21 = -M22 (L21 M11), computed block by block as
-//   TMUL(R,C,s)   T_RC = sum_m L_Rm M_mC      (m over the M11 half)
-//   MMUL(R,C,s)   M_RC = -sum_m M_Rm T_mC     (m over the M22 half)
-// so the inverse's dependent chain is about 2 NB block products instead of NB^2.  The
-// inverse tasks of a pair are listed right after the factorisation step that finishes the
-// pair's last diagonal block.
-// A fixed grid of CTAs takes tasks from a global counter in that order and waits (bounded,
-// wall-clock limited) on per-block flags released by the producers.  A task only waits on
-// tasks earlier in the order, which were taken by CTAs that are already running, so the
-// scheme needs no co-residency guarantee.  On GB300 the FP64 units give about two FMA lanes
-// per SM per clock, so small blocks and many SMs keep the dependent chain short; the CTAs
-// use little shared memory and can share SMs with tensor-core kernels.
+// of Spatial Excursion Sets", here inside one tile and on one GPU) and the blocked forward
+// substitution L M = I that gives the inverse are listed in a fixed order:
+//   POTRF(k)       factor block (k,k), invert it                     needs ver(k,k) = k
+//   TRSM(i,k)      L_ik = A_ik M_kk^T                                needs POTRF(k), ver(i,k) = k
+//   UPDATE(i,j,k)  A_ij -= L_ik L_jk^T  (k < j <= i)                  needs TRSM(i,k), TRSM(j,k), ver(i,j) = k
+//   IUPD(R,C,m)    W_RC += L_Rm M_mC    (C <= m < R)                  needs TRSM(R,m), M_mC, iver(R,C) = m - C
+//   ISOLVE(R,C)    M_RC = -M_RR W_RC    (C < R)                       needs POTRF(R), iver(R,C) = R - C
+// Every task is one 16 x 16 x 16 product.  The inverse tasks are listed shortly after their
+// inputs can exist, so the substitution runs behind the factorisation and only a few
+// products remain once the last diagonal block is factored.
+//
+// One CTA, the first to start, runs the critical chain POTRF(0), then per k TRSM(k+1,k),
+// UPDATE(k+1,k+1,k) and POTRF(k+1) with its blocks in shared memory.  The other CTAs take
+// the listed tasks from a global counter and wait (bounded, wall-clock limited) on per-block
+// flags released by the producers.  The list is ordered so that a task only waits on
+// earlier tasks, or on chain steps whose own inputs are earlier tasks; every waited-on task
+// is therefore held by a running CTA, and the scheme needs no co-residency guarantee
+// (checked on the host when the list is built).
+//
+// On GB300 an FP64 FMA has a dependent latency of about 64 cycles, each SM sub-partition
+// issues one warp-wide FP64 instruction per ~64 cycles, and a double reciprocal square root
+// or division costs over 400 cycles.  The kernels therefore keep FP64 instructions off
+// control flow (exponent tests in integer arithmetic), spread FP64 work evenly over the four
+// sub-partitions, and factor diagonal blocks without divisions (fraction-free elimination).
 #include <math.h>
+
+#include <algorithm>
+#include <vector>
 
 #include "common.cuh"
 #include "diag.cuh"
@@ -32,7 +40,7 @@ namespace cr {
 
 namespace {
 
-enum { T_POTRF = 0, T_TRSM = 1, T_UPDATE = 2, T_TMUL = 3, T_MMUL = 4 };
+enum { T_TRSM = 1, T_UPDATE = 2, T_IUPD = 3, T_ISOLVE = 4 };
 
 __device__ __forceinline__ int ld_acquire(const int* p) {
   int v;
@@ -46,12 +54,12 @@ __device__ __forceinline__ void st_release(int* p, int v) {
 struct Ctx {
   double* A;
   double* Minv;
-  double* T;   // products L21 M11 of the doubling steps (same block positions as M21)
+  double* W;   // accumulators W_RC of the substitution (same block positions as M_RC)
   int nb, NB;
   int* ver;    // NB x NB: updates applied to block (i, j)
   int* fac;    // NB x NB: L block (i, j) final (for i == j also the inverse block M_ii)
-  int* inv;    // NB x NB: inverse block (i, j), i > j, final
-  int* tfl;    // NB x NB: T block (i, j) final
+  int* inv;    // NB x NB: inverse block (R, C), R > C, final
+  int* iver;   // NB x NB: products accumulated into W_RC
   int* abort_flag;
   int* status;
   int gcol0;
@@ -72,185 +80,241 @@ __device__ bool wait_ge(const Ctx& c, const int* p, int v) {
   }
 }
 
-template <int DB>
-__device__ __forceinline__ void load_block(double (*S)[DB + 1], const double* src, int ld, bool lower_only = false) {
+constexpr int DB = 16;                        // block size: 256 threads, one element of a block each
+constexpr int NT_LOWER = DB * (DB + 1) / 2;   // 136 lower-triangle elements
+typedef double Blk[DB + 1];                   // padded shared-memory row
+
+__device__ __forceinline__ void load_block(Blk* S, const double* src, int ld) {
   for (int idx = threadIdx.x; idx < DB * DB; idx += blockDim.x) {
     const int r = idx / DB, q = idx % DB;
-    S[r][q] = (lower_only && q > r) ? 0.0 : __ldcg(src + (size_t)r * ld + q);
+    S[r][q] = __ldcg(src + (size_t)r * ld + q);
   }
 }
 // S[col][q] = src[q][col]
-template <int DB>
-__device__ __forceinline__ void load_block_t(double (*S)[DB + 1], const double* src, int ld) {
+__device__ __forceinline__ void load_block_t(Blk* S, const double* src, int ld) {
   for (int idx = threadIdx.x; idx < DB * DB; idx += blockDim.x) {
     const int r = idx / DB, q = idx % DB;
     S[q][r] = __ldcg(src + (size_t)r * ld + q);
   }
 }
 
-// Cholesky of the DB x DB block k held (lower part) in L, in place, with its inverse in X;
-// then both are written to the tile (factor, lower part) and to Minv (inverse, upper zero).
-template <int DB>
-__device__ void potrf_block(const Ctx& c, int k, double (*L)[DB + 1], double (*X)[DB + 1], double* s_r) {
+// x 2^e by integer exponent adjustment, exact for normal x and results; zero, subnormal
+// and non-finite x are returned unchanged (the callers keep magnitudes in the normal range,
+// and a non-finite pivot is reported as a failed factorisation).  Branch-free, with no FP64
+// instruction.
+__device__ __forceinline__ double scale2(double x, int e) {
+  const int hi = __double2hiint(x), lo = __double2loint(x);
+  const int ex = (hi >> 20) & 0x7ff;
+  const double y = __hiloint2double(hi + (e << 20), lo);
+  return (ex == 0 || ex == 0x7ff) ? x : y;
+}
+// unbiased binary exponent of a positive normal number, 0 for anything else (integer tests)
+__device__ __forceinline__ int expo_pos(double x) {
+  const int hi = __double2hiint(x);
+  const int ex = (hi >> 20) & 0x7ff;
+  return (hi > 0 && ex != 0 && ex != 0x7ff) ? ex - 1023 : 0;
+}
+// x > 0 without an FP64 comparison (NaN and zero give false)
+__device__ __forceinline__ bool positive(double x) {
+  const int hi = __double2hiint(x), lo = __double2loint(x);
+  const int ex = (hi >> 20) & 0x7ff;
+  const bool nan = ex == 0x7ff && (((hi & 0xfffff) | lo) != 0);
+  return hi >= 0 && ((hi | lo) != 0) && !nan;
+}
+
+// Element owned by each thread in the fraction-free factorisation, packed as
+// (isT << 8) | (i << 4) | j: threads 0..135 the lower triangle (i >= j, row by row) of the
+// working matrix T, threads 136..255 the strict lower triangle of the transformed identity.
+// (Measured on GB300: this plain order beats orderings that group elements by the step in
+// which they fall idle.)
+struct FFMap {
+  unsigned short e[256];
+};
+constexpr FFMap make_ff_map() {
+  FFMap m{};
+  int n = 0;
+  for (int i = 0; i < DB; ++i)
+    for (int j = 0; j <= i; ++j) m.e[n++] = (unsigned short)((1 << 8) | (i << 4) | j);
+  for (int i = 1; i < DB; ++i)
+    for (int j = 0; j < i; ++j) m.e[n++] = (unsigned short)((i << 4) | j);
+  return m;
+}
+__constant__ FFMap c_ffmap = make_ff_map();
+
+struct FFShared {
+  double col[2][DB];        // column c of the working matrix, double-buffered by step parity
+  int ex[2];                // -k_c: minus the binary exponent of the pivot t_cc
+  double row[2][DB];        // row c of the transformed identity
+  double alpha[DB + 1];     // alpha_c
+  double piv[DB];           // t_cc
+  double r[DB];             // 1 / sqrt(alpha_c t_cc)
+  double part[2][NT_LOWER]; // halves of the fused symmetric update
+};
+
+// Cholesky factor and inverse of diagonal block k, after subtracting P P^T when P is given
+// (the last symmetric update of the block, fused).  Division-free (fraction-free)
+// elimination: the Schur complement is carried as T = alpha_c S, and step c performs
+//   T <- 2^-k_c (t_cc T - t_c t_c^T)      with 2^-k_c t_cc in [1, 2),
+// so alpha_{c+1} = alpha_c t_cc 2^-k_c; the same row operations turn the identity into
+// Y = diag(alpha) U^-1 (A = U D U^T, U unit lower).  With r_c = 1 / sqrt(alpha_c t_cc):
+//   L_ic = t_ic r_c   and   L^-1 = diag(r) Y   (diagonal r_c alpha_c).
+// A step costs one multiply and one FMA per element and no division or square root; the
+// exact power-of-two scaling is applied by each thread to its own result, with the exponent
+// published by the pivot's owner, so a step's dependent path is a barrier, a shared load,
+// the multiply, the FMA and a few integer instructions.  The 16 reciprocal square roots
+// are taken together at the end.  The factor (lower part) is written to the tile, the
+// inverse (upper part zero) to Minv and to X.
+__device__ void potrf_ff(const Ctx& c, int k, const Blk* P, Blk* X, FFShared& sh) {
+  const int t = threadIdx.x;
+  const int code = c_ffmap.e[t];
+  const bool isT = (code >> 8) != 0;
+  const int i = (code >> 4) & 15, j = code & 15;
   double* a = c.A + (size_t)(k * DB) * c.nb + k * DB;
-  for (int idx = threadIdx.x; idx < DB * DB; idx += blockDim.x) {
-    const int r = idx / DB, q = idx % DB;
-    X[r][q] = (r == q) ? 1.0 : 0.0;
+  if (P) {
+    // lower element e = ii (ii + 1) / 2 + jj of P P^T, inner dimension in halves: thread t
+    // sums half (t & 1) of element t >> 1 (elements 0..127); lanes 0..15 of warp 0 also sum
+    // the halves of elements 128..135
+    auto half_sum = [&](int item) {
+      const int e = item >> 1, q0 = (item & 1) * (DB / 2);
+      int ii = 0;
+      while ((ii + 1) * (ii + 2) / 2 <= e) ++ii;
+      const int jj = e - ii * (ii + 1) / 2;
+      double s0 = 0.0, s1 = 0.0;
+#pragma unroll
+      for (int q = 0; q < DB / 2; q += 2) {
+        s0 = fma(P[ii][q0 + q], P[jj][q0 + q], s0);
+        s1 = fma(P[ii][q0 + q + 1], P[jj][q0 + q + 1], s1);
+      }
+      sh.part[item & 1][e] = s0 + s1;
+    };
+    half_sum(t);
+    if (t < 2 * (NT_LOWER - 128)) half_sum(256 + t);
+    __syncthreads();
+  }
+  double v = 0.0;
+  if (isT) {
+    v = __ldcg(a + (size_t)i * c.nb + j);
+    if (P) {
+      const int e = i * (i + 1) / 2 + j;
+      v -= sh.part[0][e] + sh.part[1][e];
+    }
+  }
+  if (t == 0) sh.alpha[0] = 1.0;
+  for (int col = 0; col < DB; ++col) {
+    const int par = col & 1;
+    if (isT && j == col) {
+      sh.col[par][i] = v;
+      if (i == col) sh.ex[par] = -expo_pos(v);
+    }
+    if (!isT && i == col) sh.row[par][j] = v;
+    __syncthreads();
+    const double d = sh.col[par][col];
+    if (isT) {
+      if (j > col) v = scale2(fma(-sh.col[par][i], sh.col[par][j], d * v), sh.ex[par]);
+    } else if (i > col && j <= col) {
+      const double yc = (j == col) ? sh.alpha[col] : sh.row[par][j];
+      v = scale2(fma(-sh.col[par][i], yc, d * v), sh.ex[par]);
+    }
+    if (t == 0) {
+      if (!positive(d)) atomicMin(&c.status[1], c.gcol0 + k * DB + col + 1);
+      sh.piv[col] = d;
+      sh.alpha[col + 1] = scale2(sh.alpha[col] * d, sh.ex[par]);
+    }
   }
   __syncthreads();
-  for (int col = 0; col < DB; ++col) {
-    if (threadIdx.x == 0) {
-      const double d = L[col][col];
-      if (!(d > 0.0)) atomicMin(&c.status[1], c.gcol0 + k * DB + col + 1);
-      const double r = rsqrt(d);
-      L[col][col] = d * r;
-      *s_r = r;
-    }
-    __syncthreads();
-    const double rc = *s_r;
-    for (int i = threadIdx.x; i < DB; i += blockDim.x) {
-      if (i > col) L[i][col] *= rc;
-      if (i <= col) X[col][i] *= rc;
-    }
-    __syncthreads();
-    // L[r][q] -= L[r][col] L[q][col] (col < q <= r);  X[r][q] -= L[r][col] X[col][q] (q <= col < r)
-    const int rows = DB - col - 1;
-    for (int idx = threadIdx.x; idx < rows * DB; idx += blockDim.x) {
-      const int r = col + 1 + idx / DB, q = idx % DB;
-      const double lrc = L[r][col];
-      if (q > col) {
-        if (q <= r) L[r][q] -= lrc * L[q][col];
-      } else {
-        X[r][q] -= lrc * X[col][q];
-      }
-    }
-    __syncthreads();
-  }
+  if (t < DB) sh.r[t] = rsqrt(sh.alpha[t] * sh.piv[t]);
+  __syncthreads();
   double* m = c.Minv + (size_t)(k * DB) * c.nb + k * DB;
-  for (int idx = threadIdx.x; idx < DB * DB; idx += blockDim.x) {
-    const int r = idx / DB, q = idx % DB;
-    if (q <= r) a[(size_t)r * c.nb + q] = L[r][q];
-    m[(size_t)r * c.nb + q] = (q <= r) ? X[r][q] : 0.0;
+  if (isT) {
+    a[(size_t)i * c.nb + j] = v * sh.r[j];
+    if (i != j) {
+      X[j][i] = 0.0;
+      m[(size_t)j * c.nb + i] = 0.0;
+    } else {
+      const double xd = sh.r[i] * sh.alpha[i];
+      X[i][i] = xd;
+      m[(size_t)i * c.nb + i] = xd;
+    }
+  } else {
+    const double x = sh.r[i] * v;
+    X[i][j] = x;
+    m[(size_t)i * c.nb + j] = x;
   }
 }
 
-template <int DB>
-struct Frag {
-  static constexpr int PER = (DB * DB) / 256;   // outputs per thread (1 for DB = 16, 4 for DB = 32)
-  double acc[PER];
-  __device__ void zero() {
-#pragma unroll
-    for (int x = 0; x < PER; ++x) acc[x] = 0.0;
+// Output element (r, cc) of the triangular product P M^T (M lower) owned by this thread.
+// Warp w takes the column pair p(w) = w (w < 4) or 11 - w (w >= 4), so the two warps of
+// each sub-partition hold pairs whose inner lengths add up to the same total.
+__device__ __forceinline__ void trsm_owner(int& r, int& cc) {
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int pair = w < 4 ? w : 11 - w;
+  r = lane & 15;
+  cc = 2 * pair + (lane >> 4);
+}
+// sum over q <= cc of P[r][q] M[cc][q]; the extra term at q = cc + 1 (cc even) multiplies
+// a zero of M's upper part
+__device__ __forceinline__ double trsm_elem(const Blk* P, const Blk* M, int r, int cc) {
+  double s0 = 0.0, s1 = 0.0;
+  for (int q = 0; q <= (cc | 1); q += 2) {
+    s0 = fma(P[r][q], M[cc][q], s0);
+    s1 = fma(P[r][q + 1], M[cc][q + 1], s1);
   }
-  // acc(r, col) += sum_q P[r][q] Q[col][q]
-  __device__ void mac(double (*P)[DB + 1], double (*Q)[DB + 1]) {
-    const int r = threadIdx.x / (DB / PER), c0 = threadIdx.x % (DB / PER);
-#pragma unroll 8
-    for (int q = 0; q < DB; ++q) {
-      const double a = P[r][q];
-#pragma unroll
-      for (int x = 0; x < PER; ++x) acc[x] = fma(a, Q[c0 + x * (DB / PER)][q], acc[x]);
-    }
-  }
-  // S(r, col) += alpha acc (lower part only when asked)
-  __device__ void add_to(double (*S)[DB + 1], double alpha, bool lower_only) {
-    const int r = threadIdx.x / (DB / PER), c0 = threadIdx.x % (DB / PER);
-#pragma unroll
-    for (int x = 0; x < PER; ++x) {
-      const int col = c0 + x * (DB / PER);
-      if (!(lower_only && col > r)) S[r][col] += alpha * acc[x];
-    }
-  }
-  // S(r, col) = acc and dst(r, col) = acc
-  __device__ void put(double (*S)[DB + 1], double* dst, int ld) {
-    const int r = threadIdx.x / (DB / PER), c0 = threadIdx.x % (DB / PER);
-#pragma unroll
-    for (int x = 0; x < PER; ++x) {
-      const int col = c0 + x * (DB / PER);
-      S[r][col] = acc[x];
-      dst[(size_t)r * ld + col] = acc[x];
-    }
-  }
-  // dst(r, col) = alpha acc (+ dst when accumulate)
-  __device__ void store(double* dst, int ld, double alpha, bool accumulate, bool lower_only) {
-    const int r = threadIdx.x / (DB / PER), c0 = threadIdx.x % (DB / PER);
-#pragma unroll
-    for (int x = 0; x < PER; ++x) {
-      const int col = c0 + x * (DB / PER);
-      if (lower_only && col > r) continue;
-      double* o = dst + (size_t)r * ld + col;
-      *o = accumulate ? __ldcg(o) + alpha * acc[x] : alpha * acc[x];
-    }
-  }
-};
+  return s0 + s1;
+}
 
-// dst = alpha sum_{m = m0}^{m1 - 1} P_m Q_m with P_m the block at Prow + m DB (ld nb) and Q_m
-// the block at Qcol + m DB nb (ld nb).
-template <int DB>
-__device__ void chain_product(const Ctx& c, const double* Prow, const double* Qcol, int m0, int m1, double* dst, double alpha,
-                              double (*S0)[DB + 1], double (*S1)[DB + 1]) {
-  Frag<DB> f;
-  f.zero();
-  for (int m = m0; m < m1; ++m) {
-    load_block<DB>(S0, Prow + (size_t)m * DB, c.nb);
-    load_block_t<DB>(S1, Qcol + (size_t)m * DB * c.nb, c.nb);
-    __syncthreads();
-    f.mac(S0, S1);
-    __syncthreads();
+// sum_q P[r][q] Q[col][q] for (r, col) = (tid / 16, tid % 16), two accumulation chains to
+// halve the FP64 latency of the sum
+__device__ __forceinline__ double gemm_elem(const Blk* P, const Blk* Q) {
+  const int r = threadIdx.x / DB, col = threadIdx.x % DB;
+  double s0 = 0.0, s1 = 0.0;
+#pragma unroll
+  for (int q = 0; q < DB; q += 2) {
+    s0 = fma(P[r][q], Q[col][q], s0);
+    s1 = fma(P[r][q + 1], Q[col][q + 1], s1);
   }
-  f.store(dst, c.nb, alpha, false, false);
+  return s0 + s1;
 }
 
 // The critical chain, run by one CTA with the blocks kept in shared memory:
-// POTRF(0); then for k = 0 .. NB-2: TRSM(k+1,k), SYRK(k+1,k+1,k), POTRF(k+1).
-template <int DB>
-__device__ void run_chain(const Ctx& c, double (*S0)[DB + 1], double (*S1)[DB + 1], double (*S2)[DB + 1],
-                          double (*S3)[DB + 1], double* s_r, int* s_ok) {
+// POTRF(0); then for k = 0 .. NB-2: TRSM(k+1,k), then UPDATE(k+1,k+1,k) fused into POTRF(k+1).
+__device__ void run_chain(const Ctx& c, Blk* S1, Blk* S2, Blk* S3, FFShared& sh, int* s_ok) {
   const int NB = c.NB;
   const size_t rowstride = (size_t)DB * c.nb;
-  load_block<DB>(S0, c.A, c.nb, true);
-  potrf_block<DB>(c, 0, S0, S1, s_r);   // S1 = M_00
+  potrf_ff(c, 0, nullptr, S1, sh);   // S1 = M_00
   __syncthreads();
   if (threadIdx.x == 0) st_release(&c.fac[0], 1);
+  int r, cc;
+  trsm_owner(r, cc);
   for (int k = 0; k + 1 < NB; ++k) {
     const int i = k + 1;
     // TRSM(i, k): L_ik = A_ik M_kk^T, M_kk in S1
     if (threadIdx.x == 0) *s_ok = wait_ge(c, &c.ver[i * NB + k], k) ? 1 : 0;
     __syncthreads();
     if (!*s_ok) return;
-    load_block<DB>(S2, c.A + i * rowstride + k * DB, c.nb);
+    double* aik = c.A + i * rowstride + k * DB;
+    load_block(S2, aik, c.nb);
     __syncthreads();
-    Frag<DB> f;
-    f.zero();
-    f.mac(S2, S1);
-    f.put(S3, c.A + i * rowstride + k * DB, c.nb);   // S3 = L_ik
+    const double l = trsm_elem(S2, S1, r, cc);
+    S3[r][cc] = l;                     // S3 = L_ik
+    aik[(size_t)r * c.nb + cc] = l;
     __syncthreads();
     if (threadIdx.x == 0) st_release(&c.fac[i * NB + k], 1);
-    // SYRK(i, i, k) into the diagonal block, then POTRF(i)
+    // UPDATE(i, i, k) fused into POTRF(i)
     if (threadIdx.x == 0) *s_ok = wait_ge(c, &c.ver[i * NB + i], k) ? 1 : 0;
     __syncthreads();
     if (!*s_ok) return;
-    load_block<DB>(S0, c.A + i * rowstride + i * DB, c.nb, true);
-    __syncthreads();
-    Frag<DB> g;
-    g.zero();
-    g.mac(S3, S3);
-    g.add_to(S0, -1.0, true);
-    __syncthreads();
-    potrf_block<DB>(c, i, S0, S1, s_r);   // S1 = M_ii
+    potrf_ff(c, i, S3, S1, sh);        // S1 = M_ii
     __syncthreads();
     if (threadIdx.x == 0) st_release(&c.fac[i * NB + i], 1);
   }
 }
 
-template <int DB>
-__global__ void __launch_bounds__(256) k_diag_chol(Ctx c, const int4* __restrict__ tasks, int ntasks, int* counter,
-                                                   int* role) {
-  __shared__ double S0[DB][DB + 1];
-  __shared__ double S1[DB][DB + 1];
-  __shared__ double S2[DB][DB + 1];
-  __shared__ double S3[DB][DB + 1];
-  __shared__ double s_r;
+__global__ void __launch_bounds__(256) k_diag_chol(Ctx c, const int4* __restrict__ tasks, int ntasks, int* counter, int* role) {
+  __shared__ Blk S0[DB];
+  __shared__ Blk S1[DB];
+  __shared__ Blk S2[DB];
+  __shared__ Blk S3[DB];
+  __shared__ FFShared sh;
   __shared__ int s_task;
   __shared__ int s_ok;
   const int NB = c.NB;
@@ -259,7 +323,7 @@ __global__ void __launch_bounds__(256) k_diag_chol(Ctx c, const int4* __restrict
   if (threadIdx.x == 0) s_task = atomicAdd(role, 1);
   __syncthreads();
   if (s_task == 0) {
-    run_chain<DB>(c, S0, S1, S2, S3, &s_r, &s_ok);
+    run_chain(c, S1, S2, S3, sh, &s_ok);
     return;
   }
   while (true) {
@@ -271,25 +335,20 @@ __global__ void __launch_bounds__(256) k_diag_chol(Ctx c, const int4* __restrict
     const int type = tk.x;
     if (threadIdx.x == 0) {
       bool ok = true;
-      if (type == T_POTRF) {
-        const int k = tk.w;
-        ok = wait_ge(c, &c.ver[k * NB + k], k);
-      } else if (type == T_TRSM) {
+      if (type == T_TRSM) {
         const int i = tk.y, k = tk.w;
         ok = wait_ge(c, &c.fac[k * NB + k], 1) && wait_ge(c, &c.ver[i * NB + k], k);
       } else if (type == T_UPDATE) {
         const int i = tk.y, j = tk.z, k = tk.w;
         ok = wait_ge(c, &c.fac[i * NB + k], 1) && wait_ge(c, &c.fac[j * NB + k], 1) && wait_ge(c, &c.ver[i * NB + j], k);
+      } else if (type == T_IUPD) {
+        const int R = tk.y, C = tk.z, m = tk.w;
+        ok = wait_ge(c, &c.fac[R * NB + m], 1) &&
+             (m == C ? wait_ge(c, &c.fac[C * NB + C], 1) : wait_ge(c, &c.inv[m * NB + C], 1)) &&
+             wait_ge(c, &c.iver[R * NB + C], m - C);
       } else {
-        const int R = tk.y, C = tk.z, s = tk.w;
-        const int base = C - C % (2 * s);
-        if (type == T_TMUL) {
-          for (int m = C; ok && m < base + s; ++m)
-            ok = wait_ge(c, &c.fac[R * NB + m], 1) && (m == C ? wait_ge(c, &c.fac[C * NB + C], 1) : wait_ge(c, &c.inv[m * NB + C], 1));
-        } else {
-          for (int m = base + s; ok && m <= R; ++m)
-            ok = (m == R ? wait_ge(c, &c.fac[R * NB + R], 1) : wait_ge(c, &c.inv[R * NB + m], 1)) && wait_ge(c, &c.tfl[m * NB + C], 1);
-        }
+        const int R = tk.y, C = tk.z;
+        ok = wait_ge(c, &c.fac[R * NB + R], 1) && wait_ge(c, &c.iver[R * NB + C], R - C);
       }
       s_ok = ok ? 1 : 0;
     }
@@ -298,31 +357,41 @@ __global__ void __launch_bounds__(256) k_diag_chol(Ctx c, const int4* __restrict
     if (type == T_TRSM) {
       const int i = tk.y, k = tk.w;
       double* a = c.A + i * rowstride + k * DB;
-      load_block<DB>(S0, a, c.nb);
-      load_block<DB>(S1, c.Minv + k * rowstride + k * DB, c.nb);
+      load_block(S0, a, c.nb);
+      load_block(S1, c.Minv + k * rowstride + k * DB, c.nb);
       __syncthreads();
-      Frag<DB> f;
-      f.zero();
-      f.mac(S0, S1);
-      f.store(a, c.nb, 1.0, false, false);
-    } else if (type == T_UPDATE) {
-      const int i = tk.y, j = tk.z, k = tk.w;
-      load_block<DB>(S0, c.A + i * rowstride + k * DB, c.nb);
-      load_block<DB>(S1, c.A + j * rowstride + k * DB, c.nb);
-      __syncthreads();
-      Frag<DB> f;
-      f.zero();
-      f.mac(S0, S1);
-      f.store(c.A + i * rowstride + j * DB, c.nb, -1.0, true, i == j);
-    } else if (type == T_TMUL) {
-      const int R = tk.y, C = tk.z, s = tk.w;
-      const int base = C - C % (2 * s);
-      chain_product<DB>(c, c.A + R * rowstride, c.Minv + C * DB, C, base + s, c.T + R * rowstride + C * DB, 1.0, S0, S1);
+      int r, cc;
+      trsm_owner(r, cc);
+      a[(size_t)r * c.nb + cc] = trsm_elem(S0, S1, r, cc);
     } else {
-      const int R = tk.y, C = tk.z, s = tk.w;
-      const int base = C - C % (2 * s);
-      chain_product<DB>(c, c.Minv + R * rowstride, c.T + C * DB, base + s, R + 1, c.Minv + R * rowstride + C * DB, -1.0, S0,
-                        S1);
+      const int r = threadIdx.x / DB, col = threadIdx.x % DB;
+      if (type == T_UPDATE) {
+        const int i = tk.y, j = tk.z, k = tk.w;
+        load_block(S0, c.A + i * rowstride + k * DB, c.nb);
+        load_block(S1, c.A + j * rowstride + k * DB, c.nb);
+        __syncthreads();
+        const double p = gemm_elem(S0, S1);
+        if (!(i == j && col > r)) {
+          double* o = c.A + i * rowstride + j * DB + (size_t)r * c.nb + col;
+          *o = __ldcg(o) - p;
+        }
+      } else if (type == T_IUPD) {
+        // W_RC (+)= L_Rm M_mC
+        const int R = tk.y, C = tk.z, m = tk.w;
+        load_block(S0, c.A + R * rowstride + m * DB, c.nb);
+        load_block_t(S1, c.Minv + m * rowstride + C * DB, c.nb);
+        __syncthreads();
+        const double p = gemm_elem(S0, S1);
+        double* o = c.W + R * rowstride + C * DB + (size_t)r * c.nb + col;
+        *o = (m == C) ? p : __ldcg(o) + p;
+      } else {
+        // M_RC = -M_RR W_RC
+        const int R = tk.y, C = tk.z;
+        load_block(S0, c.Minv + R * rowstride + R * DB, c.nb);
+        load_block_t(S1, c.W + R * rowstride + C * DB, c.nb);
+        __syncthreads();
+        c.Minv[R * rowstride + C * DB + (size_t)r * c.nb + col] = -gemm_elem(S0, S1);
+      }
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -330,7 +399,7 @@ __global__ void __launch_bounds__(256) k_diag_chol(Ctx c, const int4* __restrict
       // them visible at GPU scope to an acquiring reader of the flag
       if (type == T_TRSM) st_release(&c.fac[tk.y * NB + tk.w], 1);
       else if (type == T_UPDATE) st_release(&c.ver[tk.y * NB + tk.z], tk.w + 1);
-      else if (type == T_TMUL) st_release(&c.tfl[tk.y * NB + tk.z], 1);
+      else if (type == T_IUPD) st_release(&c.iver[tk.y * NB + tk.z], tk.w - tk.z + 1);
       else st_release(&c.inv[tk.y * NB + tk.z], 1);
     }
   }
@@ -338,32 +407,90 @@ __global__ void __launch_bounds__(256) k_diag_chol(Ctx c, const int4* __restrict
 
 }  // namespace
 
-void diag_task_list(int NB, std::vector<int4>& tasks) {
+bool diag_task_list(int NB, std::vector<int4>& tasks) {
+  // Step k lists what POTRF(k) and the k-th block column of the factor enable; POTRF(k),
+  // TRSM(k+1,k) and UPDATE(k+1,k+1,k) belong to the chain CTA and are not listed.
+  // The inverse tasks of step k are listed after the factorisation tasks of step k + 2, so
+  // that they fill idle CTAs instead of delaying the updates the chain waits for.
   tasks.clear();
-  // POTRF(k), TRSM(k+1,k) and UPDATE(k+1,k+1,k) belong to the chain CTA and are not queued
+  const int lag = 2;
+  auto inverse_step = [&](int k) {
+    for (int C = 0; C < k; ++C) tasks.push_back(make_int4(T_ISOLVE, k, C, 0));
+    for (int C = 0; C <= k; ++C)
+      for (int R = k + 1; R < NB; ++R) tasks.push_back(make_int4(T_IUPD, R, C, k));
+  };
   for (int k = 0; k < NB; ++k) {
     for (int i = k + 2; i < NB; ++i) tasks.push_back(make_int4(T_TRSM, i, k, k));
     for (int j = k + 1; j < NB; ++j)
       for (int i = j; i < NB; ++i)
         if (!(i == k + 1 && j == k + 1)) tasks.push_back(make_int4(T_UPDATE, i, j, k));
-    // doubling steps whose pair ends with diagonal block k, smallest pairs first
-    for (int s = 1; 2 * s <= NB; s *= 2) {
-      const int base = k + 1 - 2 * s;
-      if (base < 0 || base % (2 * s) != 0) continue;
-      for (int a = 0; a < s; ++a)
-        for (int b = 0; b < s; ++b) tasks.push_back(make_int4(T_TMUL, base + s + a, base + b, s));
-      for (int a = 0; a < s; ++a)
-        for (int b = 0; b < s; ++b) tasks.push_back(make_int4(T_MMUL, base + s + a, base + b, s));
-    }
+    if (k >= lag) inverse_step(k - lag);
   }
+  for (int k = std::max(0, NB - lag); k < NB; ++k) inverse_step(k);
+  // Progress check.  Chain node times: POTRF(k) = 3k, TRSM(k+1,k) = 3k+1,
+  // UPDATE(k+1,k+1,k) = 3k+2.  A listed task waits on earlier listed tasks and on chain
+  // nodes; chain nodes wait on listed tasks.  Every wait ends if each chain node a task
+  // waits on needs, through the chain up to it, only tasks listed before that task.
+  const int Q = (int)tasks.size();
+  std::vector<int> pos_trsm(NB * NB, -1), pos_isolve(NB * NB, -1);
+  std::vector<int> pos_upd((size_t)NB * NB * NB, -1), pos_iupd((size_t)NB * NB * NB, -1);
+  for (int t = 0; t < Q; ++t) {
+    const int4 tk = tasks[t];
+    if (tk.x == T_TRSM) pos_trsm[tk.y * NB + tk.w] = t;
+    else if (tk.x == T_UPDATE) pos_upd[((size_t)tk.y * NB + tk.z) * NB + tk.w] = t;
+    else if (tk.x == T_IUPD) pos_iupd[((size_t)tk.y * NB + tk.z) * NB + tk.w] = t;
+    else pos_isolve[tk.y * NB + tk.z] = t;
+  }
+  auto upd = [&](int i, int j, int k) { return pos_upd[((size_t)i * NB + j) * NB + k]; };
+  auto iupd = [&](int R, int C, int m) { return pos_iupd[((size_t)R * NB + C) * NB + m]; };
+  auto before = [](int p, int t) { return p >= 0 && p < t; };
+  const int nchain = 3 * NB;
+  std::vector<int> need(nchain, -1);   // last listed position the chain needs up to time tau
+  for (int tau = 0; tau < nchain; ++tau) {
+    int p = tau > 0 ? need[tau - 1] : -1;
+    const int k = tau / 3, kind = tau % 3;
+    if (kind != 0 && k >= 1 && k + 1 < NB) {
+      const int q = kind == 1 ? upd(k + 1, k, k - 1) : upd(k + 1, k + 1, k - 1);
+      if (q < 0) return false;
+      p = std::max(p, q);
+    }
+    need[tau] = p;
+  }
+  auto chain_ok = [&](int tau, int t) { return tau < nchain && need[tau] < t; };
+  auto fac_ok = [&](int i, int k, int t) {
+    if (i == k) return chain_ok(3 * k, t);
+    if (i == k + 1) return chain_ok(3 * k + 1, t);
+    return before(pos_trsm[i * NB + k], t);
+  };
+  for (int t = 0; t < Q; ++t) {
+    const int4 tk = tasks[t];
+    bool ok;
+    if (tk.x == T_TRSM) {
+      const int i = tk.y, k = tk.w;
+      ok = chain_ok(3 * k, t) && (k == 0 || before(upd(i, k, k - 1), t));
+    } else if (tk.x == T_UPDATE) {
+      const int i = tk.y, j = tk.z, k = tk.w;
+      ok = fac_ok(i, k, t) && fac_ok(j, k, t) && (k == 0 || before(upd(i, j, k - 1), t));
+    } else if (tk.x == T_IUPD) {
+      const int R = tk.y, C = tk.z, m = tk.w;
+      ok = fac_ok(R, m, t) && (m == C ? chain_ok(3 * C, t) : before(pos_isolve[m * NB + C], t)) &&
+           (m == C || before(iupd(R, C, m - 1), t));
+    } else {
+      const int R = tk.y, C = tk.z;
+      ok = chain_ok(3 * R, t) && before(iupd(R, C, R - 1), t);
+    }
+    if (!ok) return false;
+  }
+  return true;
 }
 
-cr_status diag_chol_launch(int db, double* A, double* Minv, double* T, int nb, int gcol0, int* status, int* flags,
+cr_status diag_chol_launch(int db, double* A, double* Minv, double* W, int nb, int gcol0, int* status, int* flags,
                            const int4* d_tasks, int ntasks, int grid, cudaStream_t s) {
+  if (db != DB || nb % DB != 0 || grid < 2) return fail(CR_ERR_ARG, "diag_chol_launch: block size 16 dividing nb and at least 2 CTAs");
   const int NB = nb / db;
   Ctx c;
-  c.A = A; c.Minv = Minv; c.T = T; c.nb = nb; c.NB = NB;
-  c.ver = flags; c.fac = flags + NB * NB; c.inv = flags + 2 * NB * NB; c.tfl = flags + 3 * NB * NB;
+  c.A = A; c.Minv = Minv; c.W = W; c.nb = nb; c.NB = NB;
+  c.ver = flags; c.fac = flags + NB * NB; c.inv = flags + 2 * NB * NB; c.iver = flags + 3 * NB * NB;
   c.abort_flag = flags + 4 * NB * NB;
   int* counter = flags + 4 * NB * NB + 1;
   int* role = flags + 4 * NB * NB + 2;
@@ -373,13 +500,10 @@ cr_status diag_chol_launch(int db, double* A, double* Minv, double* T, int nb, i
   if (!configured) {
     // same shared-memory carveout as the tensor-core kernel, so these small CTAs can share
     // SMs with it instead of waiting for SMs to be reconfigured
-    CR_CUDA(cudaFuncSetAttribute(k_diag_chol<16>, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared));
-    CR_CUDA(cudaFuncSetAttribute(k_diag_chol<32>, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared));
+    CR_CUDA(cudaFuncSetAttribute(k_diag_chol, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared));
     configured = true;
   }
-  if (db == 16) k_diag_chol<16><<<grid, 256, 0, s>>>(c, d_tasks, ntasks, counter, role);
-  else if (db == 32) k_diag_chol<32><<<grid, 256, 0, s>>>(c, d_tasks, ntasks, counter, role);
-  else return fail(CR_ERR_ARG, "diag_chol_launch: block size");
+  k_diag_chol<<<grid, 256, 0, s>>>(c, d_tasks, ntasks, counter, role);
   CR_CHECK_LAUNCH("k_diag_chol");
   return CR_OK;
 }

@@ -177,8 +177,7 @@ extern "C" cr_status cr_trmm_sim(cr_tilemat L, const double* d_Z, int ldz, int M
   tp.M = M;
   tp.ncb = (M + TC_BN - 1) / TC_BN;
   tp.flags = flags;
-  const int grid = L->nt * (L->nb / TC_BM) * tp.ncb;
-  CR_TRY(tc_launch(tp, L->tm_pool16, L->tm_b16, grid, stream));
+  CR_TRY(tc_launch(tp, L->tm_pool16, L->tm_b16, stream));
   if (h_bnorm) {
     std::vector<double> part(COMP_BLOCKS);
     CR_CUDA(cudaMemcpyAsync(part.data(), L->bnorm_part, COMP_BLOCKS * sizeof(double), cudaMemcpyDeviceToHost, stream));

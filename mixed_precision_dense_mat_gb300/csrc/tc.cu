@@ -1,10 +1,12 @@
-// Tensor-core tile kernel (tcgen05.mma kind::f16, FP32 accumulation in TMEM, TMA-fed
-// 6-stage shared-memory ring, warp-specialised: warp 0 TMA producer, warp 1 MMA issuer and
-// TMEM owner, warps 2-5 epilogue).  One CTA computes one 128 x 128 output block.
+// Tensor-core tile kernel: tcgen05.mma kind::f16 with FP32 accumulation in TMEM, fed by TMA
+// through a 4-stage shared-memory ring; persistent (one CTA per SM at most, output blocks
+// taken round-robin), warp-specialised (warp 0 TMA producer and k-term table, warp 1 MMA
+// issuer and TMEM owner, warps 2-5 epilogue), with two TMEM accumulators so that the
+// epilogue of one 128 x 256 output block overlaps the main loop of the next.
 //
 // Three uses, all from "Mixed-Precision GPU Acceleration for Confidence Regions of Spatial
 // Excursion Sets":
-//  TC_UPDATE  Cholesky column update A_ij -= sum_k L_ik L_jk^T (Section IV-B) for the
+//  TC_UPD_*   Cholesky column update A_ij -= sum_k L_ik L_jk^T (Section IV-B) for the
 //             products whose lowest operand precision is FP16 (one FP16 MMA) or FP32 (three
 //             MMAs on FP16 high/low parts: hi*hi + hi*lo + lo*hi).  Products between FP64
 //             tiles are left to the FP64 kernel.
@@ -23,305 +25,553 @@ namespace {
 
 struct Job {
   int i, rb, cb;
-  bool skip;
 };
 
-__device__ __forceinline__ Job decode(const TcParams& p) {
-  const int nsb = p.v.nb / TC_BM;
+__host__ __device__ inline int tc_nsbm(int nb) { return nb / TC_BM; }
+__host__ __device__ inline int tc_nsbn(int nb) { return (nb + TC_BN - 1) / TC_BN; }
+// output blocks (rb, cb) of a diagonal tile that hold part of its lower triangle
+__host__ __device__ inline int tc_diag_blocks(int nb) {
+  int d = 0;
+  for (int rb = 0; rb < tc_nsbm(nb); ++rb) d += ((rb + 1) * TC_BM + TC_BN - 1) / TC_BN;
+  return d;
+}
+
+__host__ __device__ inline int tc_num_blocks(const TcParams& p) {
+  const int nb = p.v.nb, per = tc_nsbm(nb) * tc_nsbn(nb);
+  if (p.mode == TC_TRMM) return p.v.nt * tc_nsbm(nb) * p.ncb;
+  if (p.mode == TC_TRSM) return p.nrows * per;
+  return p.nrows > 0 ? tc_diag_blocks(nb) + (p.nrows - 1) * per : 0;
+}
+
+__device__ __forceinline__ Job decode(const TcParams& p, int t) {
+  const int nb = p.v.nb, nsbm = tc_nsbm(nb), nsbn = tc_nsbn(nb);
   Job jb;
-  jb.skip = false;
   if (p.mode == TC_TRMM) {
-    const int per_row = nsb * p.ncb;
-    jb.i = p.v.nt - 1 - (int)blockIdx.x / per_row;   // longest K-chains first
-    const int rem = blockIdx.x % per_row;
+    const int per_row = nsbm * p.ncb;
+    jb.i = p.v.nt - 1 - t / per_row;   // longest K-chains first
+    const int rem = t % per_row;
     jb.rb = rem / p.ncb;
     jb.cb = rem % p.ncb;
+  } else if (p.mode == TC_TRSM) {
+    const int per = nsbm * nsbn;
+    jb.i = p.rows[t / per];
+    jb.rb = (t % per) / nsbn;
+    jb.cb = (t % per) % nsbn;
   } else {
-    const int per = nsb * nsb;
-    const int ri = blockIdx.x / per;
-    jb.i = p.rows ? p.rows[ri] : p.j + ri;
-    const int rem = blockIdx.x % per;
-    jb.rb = rem / nsb;
-    jb.cb = rem % nsb;
-    jb.skip = (jb.i == p.j && jb.cb > jb.rb);
+    const int d = tc_diag_blocks(nb);
+    if (t < d) {
+      // diagonal tile: the blocks of row rb that reach the lower triangle
+      jb.i = p.j;
+      int rb = 0, left = t;
+      while (true) {
+        const int in_row = ((rb + 1) * TC_BM + TC_BN - 1) / TC_BN;
+        if (left < in_row) break;
+        left -= in_row;
+        ++rb;
+      }
+      jb.rb = rb;
+      jb.cb = left;
+    } else {
+      const int per = nsbm * nsbn, u = t - d;
+      jb.i = p.j + 1 + u / per;
+      jb.rb = (u % per) / nsbn;
+      jb.cb = (u % per) % nsbn;
+    }
   }
   return jb;
 }
 
-// Enumerates the pipeline steps of one CTA.  Each step is one 64-wide K chunk of an
-// (A, B) pair of FP16 operand tiles; f(step, a_slot, a_k, b_slot, b_c0, b_c1).  A is read
-// from the FP16 tile pool at rows [rb*128, rb*128+128); B from the pool (b_slot >= 0, rows
-// [cb*128, +128), K offset b_c0) or from the 2-D right-hand-side map (b_slot < 0).
-template <class F>
-__device__ __forceinline__ int for_each_step(const TcParams& p, const Job& jb, F&& f) {
+// Per-k metadata of one output block, gathered by the 32 lanes of warp 0 into shared memory
+// so that the step enumeration below does no global loads: for the update modes entry
+// k - kbeg holds (product class, A hi slot, B hi slot, A lo slot, B lo slot); for the
+// simulation multiply entry k holds the slot of the factor tile (i, k) in field 1 and, for
+// k = i, the low part of the diagonal factor in field 3.
+__device__ __forceinline__ void fill_ktable(const TcParams& p, const Job& jb, int* kt) {
   const TileView& v = p.v;
-  const int nq = v.nb / TC_BK;
-  int s = 0;
+  const int lane = threadIdx.x & 31;
   if (p.mode == TC_UPD_OLD || p.mode == TC_UPD_NEW) {
     const int i = jb.i, j = p.j;
     const int cd = v.cls[tidx(i, j)];
-    for (int k = p.kbeg; k < p.kend; ++k) {
+    for (int k = p.kbeg + lane; k < p.kend; k += 32) {
       const int ti = tidx(i, k), tj = tidx(j, k);
       const int pc = max(cd, max((int)v.cls[ti], (int)v.cls[tj]));
+      int* e = kt + TC_KT_INTS * (k - p.kbeg);
+      e[0] = pc;
+      e[1] = v.hi16[ti];
+      e[2] = v.hi16[tj];
+      e[3] = pc == CR_PREC_FP32 ? v.lo16[ti] : 0;
+      e[4] = pc == CR_PREC_FP32 ? v.lo16[tj] : 0;
+    }
+  } else if (p.mode == TC_TRMM) {
+    const int i = jb.i;
+    for (int k = lane; k <= i; k += 32) {
+      int* e = kt + TC_KT_INTS * k;
+      e[1] = v.hi16[tidx(i, k)];
+      if (k == i) e[3] = v.lo16[tidx(i, i)];
+    }
+  }
+}
+
+// Enumerates the pipeline steps of one output block.  Each step is one 64-wide K chunk of an
+// (A, B) pair of FP16 operands; f(a_slot, a_k, b_slot, b_k, b_row).  A is read from the FP16
+// tile pool at rows [rb*128, +128); B (256 rows from b_row) from the pool (b_slot >= 0) or
+// from the 2-D right-hand-side map (b_slot < 0, b_k the global row of the simulation
+// matrix).  kt is the table of fill_ktable.  Returns the number of steps.
+template <class F>
+__device__ __forceinline__ int for_each_step(const TcParams& p, const Job& jb, const int* kt, F&& f) {
+  const TileView& v = p.v;
+  const int nq = v.nb / TC_BK;
+  const int brow = jb.cb * TC_BN;
+  int s = 0;
+  if (p.mode == TC_UPD_OLD || p.mode == TC_UPD_NEW) {
+    for (int k = p.kbeg; k < p.kend; ++k) {
+      const int* e = kt + TC_KT_INTS * (k - p.kbeg);
+      const int pc = e[0];
       if (pc == CR_PREC_FP64) continue;
-      const int ahi = v.hi16[ti], bhi = v.hi16[tj];
+      const int ahi = e[1], bhi = e[2];
       if (pc == CR_PREC_FP16) {
-        for (int q = 0; q < nq; ++q) f(s++, ahi, q * TC_BK, bhi, q * TC_BK, jb.cb * TC_BN);
+        for (int q = 0; q < nq; ++q, ++s) f(ahi, q * TC_BK, bhi, q * TC_BK, brow);
       } else {
-        const int alo = v.lo16[ti], blo = v.lo16[tj];
+        const int alo = e[3], blo = e[4];
         for (int q = 0; q < nq; ++q) {
-          f(s++, ahi, q * TC_BK, bhi, q * TC_BK, jb.cb * TC_BN);
-          f(s++, ahi, q * TC_BK, blo, q * TC_BK, jb.cb * TC_BN);
-          f(s++, alo, q * TC_BK, bhi, q * TC_BK, jb.cb * TC_BN);
+          f(ahi, q * TC_BK, bhi, q * TC_BK, brow);
+          f(ahi, q * TC_BK, blo, q * TC_BK, brow);
+          f(alo, q * TC_BK, bhi, q * TC_BK, brow);
+          s += 3;
         }
       }
     }
   } else if (p.mode == TC_TRSM) {
     const int i = jb.i;
     const int cd = v.cls[tidx(i, p.j)];
-    const int nqk = (jb.cb + 1) * (TC_BN / TC_BK);   // inverse factor is lower triangular
+    const int nqk = min(nq, (jb.cb + 1) * (TC_BN / TC_BK));   // the inverse factor is lower triangular
     const int wh = p.ws_hi0 + i, wl = p.ws_lo0 + i;
     for (int q = 0; q < nqk; ++q) {
-      f(s++, wh, q * TC_BK, p.minv_hi, q * TC_BK, jb.cb * TC_BN);
-      f(s++, wh, q * TC_BK, p.minv_lo, q * TC_BK, jb.cb * TC_BN);
-      if (cd == CR_PREC_FP32) f(s++, wl, q * TC_BK, p.minv_hi, q * TC_BK, jb.cb * TC_BN);
+      f(wh, q * TC_BK, p.minv_hi, q * TC_BK, brow);
+      f(wh, q * TC_BK, p.minv_lo, q * TC_BK, brow);
+      s += 2;
+      if (cd == CR_PREC_FP32) {
+        f(wl, q * TC_BK, p.minv_hi, q * TC_BK, brow);
+        ++s;
+      }
     }
   } else {
     const int i = jb.i;
     for (int k = 0; k < i; ++k) {
-      const int a = v.hi16[tidx(i, k)];
-      for (int q = 0; q < nq; ++q) f(s++, a, q * TC_BK, -1, k * v.nb + q * TC_BK, jb.cb * TC_BN);
+      const int a = kt[TC_KT_INTS * k + 1];
+      for (int q = 0; q < nq; ++q, ++s) f(a, q * TC_BK, -1, k * v.nb + q * TC_BK, brow);
     }
     const int nqd = (jb.rb + 1) * (TC_BM / TC_BK);    // the diagonal factor is lower triangular
-    const int dh = v.hi16[tidx(i, i)], dl = v.lo16[tidx(i, i)];
+    const int dh = kt[TC_KT_INTS * i + 1], dl = kt[TC_KT_INTS * i + 3];
     for (int q = 0; q < nqd; ++q) {
-      f(s++, dh, q * TC_BK, -1, i * v.nb + q * TC_BK, jb.cb * TC_BN);
-      f(s++, dl, q * TC_BK, -1, i * v.nb + q * TC_BK, jb.cb * TC_BN);
+      f(dh, q * TC_BK, -1, i * v.nb + q * TC_BK, brow);
+      f(dl, q * TC_BK, -1, i * v.nb + q * TC_BK, brow);
+      s += 2;
     }
   }
   return s;
 }
 
 struct NoOp {
-  __device__ void operator()(int, int, int, int, int, int) const {}
+  __device__ void operator()(int, int, int, int, int) const {}
 };
 
-__device__ __forceinline__ void epilogue_store(const TcParams& p, const Job& jb, int r_local, int c0, const float* acc) {
+// Output of the simulation multiply for the thread's row r_local and 16 columns from c0:
+// Y is column-major, so the 32 lanes of a warp (32 consecutive rows) write contiguously.
+__device__ __forceinline__ void trmm_store(const TcParams& p, const Job& jb, int r_local, int c0, const float* acc) {
   const TileView& v = p.v;
-  const int nb = v.nb;
-  const size_t nb2 = (size_t)nb * nb;
-  if (p.mode == TC_TRMM) {
-    const int row = jb.i * nb + jb.rb * TC_BM + r_local;
-    if (row >= v.n) return;
-    const bool f16 = (p.flags & CR_TRMM_FP16_DEST) != 0;
+  const int row = jb.i * v.nb + jb.rb * TC_BM + r_local;
+  if (row >= v.n) return;
+  const bool f16 = (p.flags & CR_TRMM_FP16_DEST) != 0;
 #pragma unroll
-    for (int q = 0; q < 16; ++q) {
-      const int col = jb.cb * TC_BN + c0 + q;
-      if (col < p.M) {
-        const float a = f16 ? __half2float(__float2half_rn(acc[q])) : acc[q];
-        p.Y[(size_t)col * p.ldy + row] = (double)a;
-      }
+  for (int q = 0; q < 16; ++q) {
+    const int col = jb.cb * TC_BN + c0 + q;
+    if (col < p.M) {
+      const float a = f16 ? __half2float(__float2half_rn(acc[q])) : acc[q];
+      p.Y[(size_t)col * p.ldy + row] = (double)a;
     }
-    return;
   }
+}
+
+// Where the epilogue of a tile-update or triangular-solve block reads and writes; resolved
+// once per block.  All tiles are row-major nb x nb; off is the element offset in the tile.
+enum {
+  EK_OLD64,   // dst64 = src64 - acc          (diagonal in place, or FP64 class into ws64)
+  EK_OLD32,   // f32 = src32 - acc            (FP32 class into w32)
+  EK_OLD16,   // f32 = src16 - acc            (FP16 class into w32)
+  EK_NEW64,   // dst64 -= acc
+  EK_NEW32,   // w = (w32 - acc) 2^-eA, split into FP16 high/low solve inputs
+  EK_NEW16,   // FP16 solve input = w32 - acc
+  EK_TRSM16,  // FP16 factor tile = acc 2^-eM
+  EK_TRSM32   // x = acc 2^(eA - eM): FP32 tile, FP16 high/low shadows
+};
+struct Epi {
+  int kind;
+  double* d64;
+  const double* s64;
+  float* f32;
+  const float* s32;
+  const __half* s16;
+  __half* h;
+  __half* l;
+  float sc;
+};
+
+__device__ __forceinline__ Epi make_epi(const TcParams& p, const Job& jb) {
+  const TileView& v = p.v;
+  const size_t nb2 = (size_t)v.nb * v.nb;
   const int i = jb.i, j = p.j;
   const int t = tidx(i, j);
   const int cd = v.cls[t];
-  const size_t off = (size_t)(jb.rb * TC_BM + r_local) * nb + jb.cb * TC_BN + c0;
+  Epi e{};
   if (p.mode == TC_UPD_OLD) {
-    // older terms: class storage -> intermediate (FP64 in place / FP64 workspace / FP32 workspace)
     if (i == j || cd == CR_PREC_FP64) {
-      const double* src = v.pool64 + (size_t)v.i64[t] * nb2 + off;
-      double* dst = (i == j) ? const_cast<double*>(src) : p.ws64 + (size_t)i * nb2 + off;
-#pragma unroll
-      for (int q = 0; q < 16; q += 2) {
-        const double2 a = *reinterpret_cast<const double2*>(src + q);
-        *reinterpret_cast<double2*>(dst + q) = make_double2(a.x - (double)acc[q], a.y - (double)acc[q + 1]);
-      }
+      e.kind = EK_OLD64;
+      e.s64 = v.pool64 + (size_t)v.i64[t] * nb2;
+      e.d64 = (i == j) ? const_cast<double*>(e.s64) : p.ws64 + (size_t)i * nb2;
+    } else if (cd == CR_PREC_FP32) {
+      e.kind = EK_OLD32;
+      e.f32 = p.w32 + (size_t)i * nb2;
+      e.s32 = v.pool32 + (size_t)v.i32[t] * nb2;
     } else {
-      float* dst = p.w32 + (size_t)i * nb2 + off;
-      if (cd == CR_PREC_FP32) {
-        const float* src = v.pool32 + (size_t)v.i32[t] * nb2 + off;
-#pragma unroll
-        for (int q = 0; q < 16; q += 4)
-          *reinterpret_cast<float4*>(dst + q) =
-              make_float4(src[q] - acc[q], src[q + 1] - acc[q + 1], src[q + 2] - acc[q + 2], src[q + 3] - acc[q + 3]);
-      } else {
-        const __half* src = v.pool16 + (size_t)v.hi16[t] * nb2 + off;
-#pragma unroll
-        for (int q = 0; q < 16; q += 4)
-          *reinterpret_cast<float4*>(dst + q) =
-              make_float4(__half2float(src[q]) - acc[q], __half2float(src[q + 1]) - acc[q + 1],
-                          __half2float(src[q + 2]) - acc[q + 2], __half2float(src[q + 3]) - acc[q + 3]);
-      }
+      e.kind = EK_OLD16;
+      e.f32 = p.w32 + (size_t)i * nb2;
+      e.s16 = v.pool16 + (size_t)v.hi16[t] * nb2;
     }
   } else if (p.mode == TC_UPD_NEW) {
-    // newest term: intermediate -> solve inputs in the tile's precision
     if (i == j || cd == CR_PREC_FP64) {
-      double* dst = (i == j) ? v.pool64 + (size_t)v.i64[t] * nb2 + off : p.ws64 + (size_t)i * nb2 + off;
-#pragma unroll
-      for (int q = 0; q < 16; q += 2) {
-        const double2 a = *reinterpret_cast<const double2*>(dst + q);
-        *reinterpret_cast<double2*>(dst + q) = make_double2(a.x - (double)acc[q], a.y - (double)acc[q + 1]);
-      }
+      e.kind = EK_NEW64;
+      e.d64 = (i == j) ? v.pool64 + (size_t)v.i64[t] * nb2 : p.ws64 + (size_t)i * nb2;
     } else if (cd == CR_PREC_FP32) {
-      const float* src = p.w32 + (size_t)i * nb2 + off;
-      __half* hi = v.pool16 + (size_t)(p.ws_hi0 + i) * nb2 + off;
-      __half* lo = v.pool16 + (size_t)(p.ws_lo0 + i) * nb2 + off;
-      const float sc = ldexpf(1.0f, -p.eA);
-#pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        const float w = (src[q] - acc[q]) * sc;
-        const __half h = __float2half_rn(w);
-        hi[q] = h;
-        lo[q] = __float2half_rn(w - __half2float(h));
-      }
+      e.kind = EK_NEW32;
+      e.s32 = p.w32 + (size_t)i * nb2;
+      e.h = v.pool16 + (size_t)(p.ws_hi0 + i) * nb2;
+      e.l = v.pool16 + (size_t)(p.ws_lo0 + i) * nb2;
+      e.sc = ldexpf(1.0f, -p.eA);
     } else {
-      const float* src = p.w32 + (size_t)i * nb2 + off;
-      __half* dst = v.pool16 + (size_t)(p.ws_hi0 + i) * nb2 + off;
-#pragma unroll
-      for (int q = 0; q < 16; ++q) dst[q] = __float2half_rn(src[q] - acc[q]);
+      e.kind = EK_NEW16;
+      e.s32 = p.w32 + (size_t)i * nb2;
+      e.h = v.pool16 + (size_t)(p.ws_hi0 + i) * nb2;
     }
   } else {   // TC_TRSM
     const int eM = p.status[2];
     if (cd == CR_PREC_FP16) {
-      const float sc = ldexpf(1.0f, -eM);
-      __half* dst = v.pool16 + (size_t)v.hi16[t] * nb2 + off;
-#pragma unroll
-      for (int q = 0; q < 16; ++q) dst[q] = __float2half_rn(acc[q] * sc);
+      e.kind = EK_TRSM16;
+      e.h = v.pool16 + (size_t)v.hi16[t] * nb2;
+      e.sc = ldexpf(1.0f, -eM);
     } else {
-      const float sc = ldexpf(1.0f, p.eA - eM);
-      float* d32 = v.pool32 + (size_t)v.i32[t] * nb2 + off;
-      __half* hi = v.pool16 + (size_t)v.hi16[t] * nb2 + off;
-      __half* lo = v.pool16 + (size_t)v.lo16[t] * nb2 + off;
+      e.kind = EK_TRSM32;
+      e.f32 = v.pool32 + (size_t)v.i32[t] * nb2;
+      e.h = v.pool16 + (size_t)v.hi16[t] * nb2;
+      e.l = v.pool16 + (size_t)v.lo16[t] * nb2;
+      e.sc = ldexpf(1.0f, p.eA - eM);
+    }
+  }
+  return e;
+}
+
+// One 32 x 32 chunk of a row-major tile: lane `lane` handles column col0 + lane of the 32
+// rows from row offset base (element offsets off(r) = base + r nb + lane); st holds the
+// accumulator chunk (st[r][lane]).  The reads of all 32 rows are issued before any store,
+// so that each lane keeps 32 loads in flight.
+__device__ __forceinline__ void epi_chunk(const Epi& e, size_t base, int nb, int lane, const float (*st)[33]) {
+  const size_t o = base + lane;
+  switch (e.kind) {
+    case EK_OLD64: {
+      double x[32];
 #pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        const float x = acc[q] * sc;
-        d32[q] = x;
+      for (int r = 0; r < 32; ++r) x[r] = e.s64[o + (size_t)r * nb];
+#pragma unroll
+      for (int r = 0; r < 32; ++r) e.d64[o + (size_t)r * nb] = x[r] - (double)st[r][lane];
+      break;
+    }
+    case EK_NEW64: {
+      double x[32];
+#pragma unroll
+      for (int r = 0; r < 32; ++r) x[r] = e.d64[o + (size_t)r * nb];
+#pragma unroll
+      for (int r = 0; r < 32; ++r) e.d64[o + (size_t)r * nb] = x[r] - (double)st[r][lane];
+      break;
+    }
+    case EK_OLD32: {
+      float x[32];
+#pragma unroll
+      for (int r = 0; r < 32; ++r) x[r] = e.s32[o + (size_t)r * nb];
+#pragma unroll
+      for (int r = 0; r < 32; ++r) e.f32[o + (size_t)r * nb] = x[r] - st[r][lane];
+      break;
+    }
+    case EK_OLD16: {
+      __half x[32];
+#pragma unroll
+      for (int r = 0; r < 32; ++r) x[r] = e.s16[o + (size_t)r * nb];
+#pragma unroll
+      for (int r = 0; r < 32; ++r) e.f32[o + (size_t)r * nb] = __half2float(x[r]) - st[r][lane];
+      break;
+    }
+    case EK_NEW32: {
+      float x[32];
+#pragma unroll
+      for (int r = 0; r < 32; ++r) x[r] = e.s32[o + (size_t)r * nb];
+#pragma unroll
+      for (int r = 0; r < 32; ++r) {
+        const float w = (x[r] - st[r][lane]) * e.sc;
+        const __half h = __float2half_rn(w);
+        e.h[o + (size_t)r * nb] = h;
+        e.l[o + (size_t)r * nb] = __float2half_rn(w - __half2float(h));
+      }
+      break;
+    }
+    case EK_NEW16: {
+      float x[32];
+#pragma unroll
+      for (int r = 0; r < 32; ++r) x[r] = e.s32[o + (size_t)r * nb];
+#pragma unroll
+      for (int r = 0; r < 32; ++r) e.h[o + (size_t)r * nb] = __float2half_rn(x[r] - st[r][lane]);
+      break;
+    }
+    case EK_TRSM16: {
+#pragma unroll
+      for (int r = 0; r < 32; ++r) e.h[o + (size_t)r * nb] = __float2half_rn(st[r][lane] * e.sc);
+      break;
+    }
+    default: {
+#pragma unroll
+      for (int r = 0; r < 32; ++r) {
+        const float x = st[r][lane] * e.sc;
         const __half h = __float2half_rn(x);
-        hi[q] = h;
-        lo[q] = __float2half_rn(x - __half2float(h));
+        e.f32[o + (size_t)r * nb] = x;
+        e.h[o + (size_t)r * nb] = h;
+        e.l[o + (size_t)r * nb] = __float2half_rn(x - __half2float(h));
       }
     }
   }
 }
 
+// Shared-memory layout after the stage ring (offsets from the 1 KB aligned base).
+struct TcBars {
+  uint64_t full[TC_STAGES], empty[TC_STAGES];   // stage ring
+  uint64_t tfull[2], tempty[2];                 // TMEM accumulators
+  uint64_t kfull[2], kempty[2];                 // k-term tables
+  int steps[2];                                 // step count of the block in each accumulator
+  uint32_t tmem;
+  int abort;
+};
+static_assert(sizeof(TcBars) <= 256, "barrier area");
+
 }  // namespace
 
 __global__ void __launch_bounds__(TC_THREADS, 1)
-    k_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const TcParams p) {
-  const Job jb = decode(p);
-  if (jb.skip) return;
+    k_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const TcParams p, int nblocks) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + TC_STAGES * TC_STAGE_BYTES);
-  uint64_t* empty = full + TC_STAGES;
-  uint64_t* accb = empty + TC_STAGES;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accb + 1);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  TcBars* bars = reinterpret_cast<TcBars*>(smem + TC_STAGES * TC_STAGE_BYTES);
+  float* estage = reinterpret_cast<float*>(smem + TC_STAGES * TC_STAGE_BYTES + 256);   // 4 warps x 32 x 33
+  int* ktab = reinterpret_cast<int*>(smem + TC_STAGES * TC_STAGE_BYTES + 256 + TC_EPI_BYTES);
+  const int kt_ints = TC_KT_INTS * p.v.nt;
+  volatile int* abort_flag = &bars->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < TC_STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], 1);
     }
-    mbar_init(accb, 1);
-    *abort_flag = 0;
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->tfull[b], 2);       // the MMA thread's arrival and the MMA completion
+      mbar_init(&bars->tempty[b], 128);    // every epilogue thread
+      mbar_init(&bars->kfull[b], 1);
+      mbar_init(&bars->kempty[b], 1);
+    }
+    bars->abort = 0;
     fence_mbar_init();
   }
-  if (warp == 1) tmem_alloc(tmem_slot, TC_BN);
+  if (warp == 1) tmem_alloc(&bars->tmem, TC_TMEM_COLS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  const int S = for_each_step(p, jb, NoOp());
+  const uint32_t tmem = bars->tmem;
 
   if (warp == 0) {
-    if (lane == 0 && S > 0) {
+    // k-term tables and TMA producer
+    if (lane == 0) {
       prefetch_tmap(&tmA);
       prefetch_tmap(&tmB);
-      for_each_step(p, jb, [&](int s, int aslot, int ak, int bslot, int bc0, int bc1) {
-        if (*abort_flag) return;
-        const int st = s % TC_STAGES;
-        const uint32_t ph = (uint32_t)(s / TC_STAGES) & 1u;
-        if (!mbar_wait(&empty[st], ph ^ 1u)) {
+    }
+    uint32_t gs = 0;   // global step count of this CTA
+    int u = 0;
+    for (int t = blockIdx.x; t < nblocks; t += gridDim.x, ++u) {
+      const int b = u & 1;
+      const uint32_t ph = (uint32_t)(u >> 1) & 1u;
+      int* kt = ktab + b * kt_ints;
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(&bars->kempty[b], ph ^ 1u);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok || *abort_flag) {
+        if (lane == 0 && !ok) {
           *abort_flag = 1;
           atomicOr(p.err, DEV_ERR_TIMEOUT);
-          return;
         }
-        mbar_arrive_expect_tx(&full[st], TC_STAGE_BYTES);
-        uint8_t* sa = smem + st * TC_STAGE_BYTES;
-        uint8_t* sb = sa + TC_BM * TC_BK * 2;
-        tma_load_3d(sa, &tmA, &full[st], ak, jb.rb * TC_BM, aslot);
-        if (bslot >= 0) tma_load_3d(sb, &tmA, &full[st], bc0, bc1, bslot);
-        else tma_load_2d(sb, &tmB, &full[st], bc0, bc1);
-      });
+        break;
+      }
+      const Job jb = decode(p, t);
+      fill_ktable(p, jb, kt);
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bars->kfull[b]);
+        for_each_step(p, jb, kt, [&](int aslot, int ak, int bslot, int bk, int brow) {
+          if (*abort_flag) return;
+          const int st = gs % TC_STAGES;
+          const uint32_t sph = (gs / TC_STAGES) & 1u;
+          ++gs;
+          if (!mbar_wait(&bars->empty[st], sph ^ 1u)) {
+            *abort_flag = 1;
+            atomicOr(p.err, DEV_ERR_TIMEOUT);
+            return;
+          }
+          mbar_arrive_expect_tx(&bars->full[st], TC_STAGE_BYTES);
+          uint8_t* sa = smem + st * TC_STAGE_BYTES;
+          uint8_t* sb = sa + TC_BM * TC_BK * 2;
+          tma_load_3d(sa, &tmA, &bars->full[st], ak, jb.rb * TC_BM, aslot);
+          if (bslot >= 0) {
+            tma_load_3d(sb, &tmA, &bars->full[st], bk, brow, bslot);
+            tma_load_3d(sb + 128 * TC_BK * 2, &tmA, &bars->full[st], bk, brow + 128, bslot);
+          } else {
+            tma_load_2d(sb, &tmB, &bars->full[st], bk, brow);
+            tma_load_2d(sb + 128 * TC_BK * 2, &tmB, &bars->full[st], bk, brow + 128);
+          }
+        });
+      }
+      __syncwarp();
     }
   } else if (warp == 1) {
     if (lane == 0) {
       const uint32_t idesc = idesc_f16_f32(TC_BM, TC_BN);
-      for (int s = 0; s < S; ++s) {
-        const int st = s % TC_STAGES;
-        const uint32_t ph = (uint32_t)(s / TC_STAGES) & 1u;
+      uint32_t gs = 0;
+      int u = 0;
+      for (int t = blockIdx.x; t < nblocks; t += gridDim.x, ++u) {
+        const int b = u & 1;
+        const uint32_t ph = (uint32_t)(u >> 1) & 1u;
         if (*abort_flag) break;
-        if (!mbar_wait(&full[st], ph)) {
+        if (!mbar_wait(&bars->kfull[b], ph) || !mbar_wait(&bars->tempty[b], ph ^ 1u)) {
           *abort_flag = 1;
           atomicOr(p.err, DEV_ERR_TIMEOUT);
           break;
         }
+        const Job jb = decode(p, t);
+        const int S = for_each_step(p, jb, ktab + b * kt_ints, NoOp());
+        mbar_arrive(&bars->kempty[b]);
         tc_fence_after();
-        const uint32_t sa = smem_u32(smem + st * TC_STAGE_BYTES);
-        const uint32_t sb = sa + TC_BM * TC_BK * 2;
-        const uint64_t da = desc_sw128(sa), db = desc_sw128(sb);
+        const uint32_t acc = tmem + (uint32_t)(b * TC_BN);
+        bool ok = true;
+        for (int s = 0; s < S; ++s, ++gs) {
+          const int st = gs % TC_STAGES;
+          const uint32_t sph = (gs / TC_STAGES) & 1u;
+          if (*abort_flag || !mbar_wait(&bars->full[st], sph)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + st * TC_STAGE_BYTES);
+          const uint32_t sb = sa + TC_BM * TC_BK * 2;
+          const uint64_t da = desc_sw128(sa), db = desc_sw128(sb);
 #pragma unroll
-        for (int kk = 0; kk < TC_BK / 16; ++kk)
-          mma_f16(tmem, da + (uint64_t)((kk * 32) >> 4), db + (uint64_t)((kk * 32) >> 4), idesc, (s | kk) != 0);
-        mma_commit(&empty[st]);
+          for (int kk = 0; kk < TC_BK / 16; ++kk)
+            mma_f16(acc, da + (uint64_t)((kk * 32) >> 4), db + (uint64_t)((kk * 32) >> 4), idesc, (s | kk) != 0);
+          mma_commit(&bars->empty[st]);
+        }
+        if (!ok) {
+          *abort_flag = 1;
+          atomicOr(p.err, DEV_ERR_TIMEOUT);
+          break;
+        }
+        bars->steps[b] = S;
+        mbar_arrive(&bars->tfull[b]);
+        if (S > 0) mma_commit(&bars->tfull[b]);
+        else mbar_arrive(&bars->tfull[b]);
       }
-      if (S > 0) mma_commit(accb);
-      else mbar_arrive(accb);
     }
   } else {
     // epilogue: warp w reads TMEM lanes of quadrant (w % 4)
     const int quad = warp & 3;
     const int r_local = quad * 32 + lane;
-    bool ok = true;
-    if (S > 0) {
-      ok = mbar_wait(accb, 0);
-      if (!ok && lane == 0) atomicOr(p.err, DEV_ERR_TIMEOUT);
-      tc_fence_after();
-    }
-    for (int c0 = 0; c0 < TC_BN; c0 += 16) {
-      float acc[16];
-      if (S > 0) {
-        tmem_ld16(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)c0, acc);
-      } else {
-#pragma unroll
-        for (int q = 0; q < 16; ++q) acc[q] = 0.0f;
+    int u = 0;
+    for (int t = blockIdx.x; t < nblocks; t += gridDim.x, ++u) {
+      const int b = u & 1;
+      const uint32_t ph = (uint32_t)(u >> 1) & 1u;
+      if (*abort_flag) break;
+      if (!mbar_wait(&bars->tfull[b], ph)) {
+        if (lane == 0) atomicOr(p.err, DEV_ERR_TIMEOUT);
+        *abort_flag = 1;
+        break;
       }
-      if (ok) epilogue_store(p, jb, r_local, c0, acc);
+      tc_fence_after();
+      const Job jb = decode(p, t);
+      const int S = bars->steps[b];
+      const uint32_t tq = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(b * TC_BN);
+      if (p.mode == TC_TRMM) {
+        for (int c0 = 0; c0 < TC_BN; c0 += 16) {
+          float acc[16];
+          if (S > 0) {
+            tmem_ld16(tq + (uint32_t)c0, acc);
+          } else {
+#pragma unroll
+            for (int q = 0; q < 16; ++q) acc[q] = 0.0f;
+          }
+          trmm_store(p, jb, r_local, c0, acc);
+        }
+      } else {
+        // row-major tiles: each 32 x 32 chunk of the warp's quadrant goes through shared
+        // memory so that consecutive lanes handle consecutive columns of one row
+        const Epi e = make_epi(p, jb);
+        const int ncols = min(TC_BN, p.v.nb - jb.cb * TC_BN);
+        float(*st)[33] = reinterpret_cast<float(*)[33]>(estage + (warp - 2) * 32 * 33);
+        const size_t base = (size_t)(jb.rb * TC_BM + quad * 32) * p.v.nb + jb.cb * TC_BN;
+        for (int g = 0; g < ncols; g += 32) {
+          float acc[32];
+          if (S > 0) {
+            tmem_ld16(tq + (uint32_t)g, acc);
+            tmem_ld16(tq + (uint32_t)(g + 16), acc + 16);
+          } else {
+#pragma unroll
+            for (int q = 0; q < 32; ++q) acc[q] = 0.0f;
+          }
+#pragma unroll
+          for (int q = 0; q < 32; ++q) st[lane][q] = acc[q];
+          __syncwarp();
+          epi_chunk(e, base + g, p.v.nb, lane, st);
+          __syncwarp();
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bars->tempty[b]);
     }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
-    // all MMAs issued by this CTA are complete once accb has fired
-    if (S > 0) mbar_wait(accb, 0);
     tc_fence_after();
-    tmem_dealloc(tmem, TC_BN);
+    tmem_dealloc(tmem, TC_TMEM_COLS);
   }
 }
 
-cr_status tc_launch(const TcParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid, cudaStream_t stream) {
+cr_status tc_launch(const TcParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, cudaStream_t stream) {
+  constexpr int kMaxSmem = 227 * 1024;
   static bool configured = false;
   if (!configured) {
-    CR_CUDA(cudaFuncSetAttribute(k_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC_SMEM));
+    CR_CUDA(cudaFuncSetAttribute(k_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem));
     CR_CUDA(cudaFuncSetAttribute(k_tc, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared));
     configured = true;
   }
-  if (grid <= 0) return CR_OK;
-  k_tc<<<grid, TC_THREADS, TC_SMEM, stream>>>(tmA, tmB, p);
+  const int nblocks = tc_num_blocks(p);
+  if (nblocks <= 0) return CR_OK;
+  int dev = 0, sms = 0;
+  CR_CUDA(cudaGetDevice(&dev));
+  CR_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  const size_t smem = TC_SMEM + 2 * (((size_t)TC_KT_INTS * sizeof(int) * p.v.nt + 15) & ~(size_t)15);
+  if (smem > (size_t)kMaxSmem) return fail(CR_ERR_ARG, "tensor-core kernel: too many tiles per column for the k-term tables");
+  const int grid = nblocks < sms ? nblocks : sms;
+  k_tc<<<grid, TC_THREADS, smem, stream>>>(tmA, tmB, p, nblocks);
   CR_CHECK_LAUNCH("k_tc");
   return CR_OK;
 }

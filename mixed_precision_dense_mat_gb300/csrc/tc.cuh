@@ -4,11 +4,15 @@
 
 namespace cr {
 
-constexpr int TC_BM = 128, TC_BN = 128, TC_BK = 64;
-constexpr int TC_STAGES = 6;
-constexpr int TC_STAGE_BYTES = (TC_BM + TC_BN) * TC_BK * 2;   // A and B, FP16, 32 KB
+constexpr int TC_BM = 128, TC_BN = 256, TC_BK = 64;            // output block 128 x 256, K chunk 64
+constexpr int TC_STAGES = 4;
+constexpr int TC_STAGE_BYTES = (TC_BM + TC_BN) * TC_BK * 2;     // A and B, FP16, 48 KB
 constexpr int TC_THREADS = 192;
-constexpr size_t TC_SMEM = (size_t)TC_STAGES * TC_STAGE_BYTES + 1024 + 256;
+constexpr int TC_KT_INTS = 5;                                   // ints per k-term table entry
+constexpr int TC_TMEM_COLS = 2 * TC_BN;                         // two accumulators
+constexpr int TC_EPI_BYTES = 4 * 32 * 33 * 4;                   // epilogue staging, one 32 x 32 chunk per warp
+// stages, 1 KB alignment slack, barriers, epilogue staging; the two k-term tables come on top
+constexpr size_t TC_SMEM = (size_t)TC_STAGES * TC_STAGE_BYTES + 1024 + 256 + TC_EPI_BYTES;
 
 // TC_UPD_OLD: products k in [kbeg, kend) from the class storage into the intermediate
 //             (FP32 workspace w32, FP64 workspace ws64, diagonal FP64 in place);
@@ -22,7 +26,8 @@ struct TcParams {
   int j;              // tile column (update / triangular solve)
   int kbeg, kend;     // update terms
   float* w32;         // FP32 intermediate of FP16/FP32-class tiles (tile row i at i nb^2)
-  const int* rows;    // tile rows of this launch (triangular solve); NULL: rows j, j+1, ...
+  const int* rows;    // tile rows of this launch (triangular solve; updates: NULL = j, j+1, ...)
+  int nrows;          // number of tile rows (triangular solve; updates: rows j .. j+nrows-1)
   int ws_hi0, ws_lo0, minv_hi, minv_lo;
   int eA;             // FP32-class inputs were scaled by 2^-eA
   const int* status;  // status[2]: exponent eM of the scaled inverse factor
@@ -32,6 +37,8 @@ struct TcParams {
   int ldy, M, ncb, flags;
 };
 
-cr_status tc_launch(const TcParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid, cudaStream_t stream);
+// Launches the persistent kernel over every output block of the launch described by p (one
+// CTA per SM at most).
+cr_status tc_launch(const TcParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, cudaStream_t stream);
 
 }  // namespace cr
