@@ -94,6 +94,7 @@ static void dfree(T*& p) {
 cr_status free_class_storage(cr_tilemat V) {
   dfree(V->d_cls); dfree(V->d_i64); dfree(V->d_i32); dfree(V->d_hi16); dfree(V->d_lo16);
   dfree(V->pool64); dfree(V->pool32); dfree(V->pool16); dfree(V->ws64); dfree(V->w32);
+  V->cap64 = V->cap32 = V->cap16 = V->cap_ws64 = V->cap_w32 = 0;
   V->mapped = false;
   V->factored = false;
   return CR_OK;

@@ -92,6 +92,7 @@ struct cr_tilemat_s {
   std::vector<int8_t> h_cls;
   std::vector<int> h_i64, h_i32, h_hi16, h_lo16;
   int n64 = 0, n32 = 0, n16 = 0;  // slots per pool
+  size_t cap64 = 0, cap32 = 0, cap16 = 0, cap_ws64 = 0, cap_w32 = 0;   // allocated elements, kept across maps
   int ws_hi0 = 0, ws_lo0 = 0, minv_hi = 0, minv_lo = 0;
   int8_t* d_cls = nullptr;
   int *d_i64 = nullptr, *d_i32 = nullptr, *d_hi16 = nullptr, *d_lo16 = nullptr;

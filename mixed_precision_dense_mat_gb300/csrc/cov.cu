@@ -9,10 +9,12 @@
 //
 // The FP64 matrix is never stored.  cr_cov_build makes one pass that only reduces the
 // per-tile statistics; the factorisation generates each tile directly in its class (FP64
-// tiles in FP64, FP32/FP16 tiles rounded from a double-float evaluation).  For the
-// closed-form Matern orders (nu = 1/2, 3/2, 5/2) both passes evaluate in double-float
-// arithmetic on the FP32 units (about 1e-14 relative; GB300's FP64 units run at 1/60 of the
-// FP32 rate); FP64 tiles and the other models use FP64.
+// tiles in FP64, FP32 tiles rounded from a double-float evaluation, FP16 tiles from a
+// single-precision one).  For the closed-form Matern orders (nu = 1/2, 3/2, 5/2) the
+// statistics and the FP32 tiles are evaluated in double-float arithmetic on the FP32 units
+// (about 1e-14 relative; GB300's FP64 units run at 1/60 of the FP32 rate), the FP16 tiles in
+// FP32 (a few ulp, against the 2^-11 rounding of FP16); FP64 tiles and the other models use
+// FP64.
 #include <math.h>
 
 #include <mutex>
@@ -239,6 +241,28 @@ __global__ void __launch_bounds__(256) k_generate(const double* __restrict__ xy,
   if (threadIdx.x == 0) { s_T.c1 = c_dfexp.c1; s_T.c2 = c_dfexp.c2; s_T.c3 = c_dfexp.c3; }
   __syncthreads();
   const size_t count = (size_t)nb * nb;
+  if (use_df && cls == CR_PREC_FP16) {
+    // FP16 tiles (off-diagonal): a single-precision evaluation, a few ulp of FP32, is far
+    // inside the 2^-11 rounding of the stored value; distances from the double-float
+    // coordinates, so that near points do not lose digits to cancellation
+    __half* dst = v.pool16 + (size_t)v.hi16[t] * count;
+    const float sig = p.sig_hi, invr = p.invr_hi, s2f = (float)s2;
+    for (int idx = threadIdx.x; idx < 64 * nb; idx += blockDim.x) {
+      const int r = r0 + idx / nb, c = idx % nb;
+      const int gi = i * nb + r, gj = j * nb + c;
+      float f = 0.0f;
+      if (gi < n && gj < n) {
+        const float4 a = s_row[r - r0], b = s_col[c];
+        const float dx = (a.x - b.x) + (a.y - b.y), dy = (a.z - b.z) + (a.w - b.w);
+        const float x = sqrtf(fmaf(dx, dx, dy * dy)) * invr;
+        const float e = expf(-x);
+        const float poly = p.kind == 0 ? 1.0f : (p.kind == 1 ? 1.0f + x : fmaf(x * x, 1.0f / 3.0f, 1.0f + x));
+        f = sig * poly * e * s2f;
+      }
+      dst[(size_t)r * nb + c] = __float2half_rn(f);
+    }
+    return;
+  }
   const df sig = {p.sig_hi, p.sig_lo}, invr = {p.invr_hi, p.invr_lo}, s2d = {s2_hi, s2_lo};
   for (int idx = threadIdx.x; idx < 64 * nb; idx += blockDim.x) {
     const int r = r0 + idx / nb, c = idx % nb;

@@ -101,19 +101,32 @@ void scale(const cr_tilemat V, const std::vector<int8_t>& cls, cr_pmap_info* inf
   info->range_ok = ell <= us;
 }
 
+// per-tile tables have ntiles entries for the life of the tile matrix: allocated once
 template <class T>
 cr_status upload(T** d, const std::vector<T>& h) {
+  if (!*d) CR_CUDA(cudaMalloc(d, std::max<size_t>(1, h.size()) * sizeof(T)));
+  CR_CUDA(cudaMemcpy(*d, h.data(), h.size() * sizeof(T), cudaMemcpyHostToDevice));
+  return CR_OK;
+}
+
+// (re)allocates *d only when the new size exceeds its capacity, so that repeated maps of the
+// same matrix neither free nor allocate (cudaFree synchronises the device)
+template <class T>
+cr_status ensure(T** d, size_t* cap, size_t need) {
+  if (need <= *cap && *d) return CR_OK;
   if (*d) cudaFree(*d);
   *d = nullptr;
-  CR_CUDA(cudaMalloc(d, std::max<size_t>(1, h.size()) * sizeof(T)));
-  CR_CUDA(cudaMemcpy(*d, h.data(), h.size() * sizeof(T), cudaMemcpyHostToDevice));
+  *cap = 0;
+  CR_CUDA(cudaMalloc(d, std::max<size_t>(1, need) * sizeof(T)));
+  *cap = need;
   return CR_OK;
 }
 
 }  // namespace
 
 cr_status allocate_class_storage(cr_tilemat V) {
-  free_class_storage(V);
+  V->mapped = false;
+  V->factored = false;
   const int nt = V->nt, T = V->ntiles;
   const size_t tile = (size_t)V->nb * V->nb;
   V->h_i64.assign(T, -1); V->h_i32.assign(T, -1); V->h_hi16.assign(T, -1); V->h_lo16.assign(T, -1);
@@ -140,14 +153,14 @@ cr_status allocate_class_storage(cr_tilemat V) {
   CR_TRY(upload(&V->d_i32, V->h_i32));
   CR_TRY(upload(&V->d_hi16, V->h_hi16));
   CR_TRY(upload(&V->d_lo16, V->h_lo16));
-  CR_CUDA(cudaMalloc(&V->pool64, std::max<size_t>(1, (size_t)V->n64) * tile * sizeof(double)));
-  if (V->n32) CR_CUDA(cudaMalloc(&V->pool32, (size_t)V->n32 * tile * sizeof(float)));
+  CR_TRY(ensure(&V->pool64, &V->cap64, std::max<size_t>(1, (size_t)V->n64) * tile));
+  if (V->n32) CR_TRY(ensure(&V->pool32, &V->cap32, (size_t)V->n32 * tile));
   if (V->n16) {
-    CR_CUDA(cudaMalloc(&V->pool16, (size_t)V->n16 * tile * sizeof(__half)));
+    CR_TRY(ensure(&V->pool16, &V->cap16, (size_t)V->n16 * tile));
     CR_TRY(make_tensor_map_3d_f16(&V->tm_pool16, V->pool16, V->nb, V->nb, V->n16, 64, 128));
   }
-  if (off64 > 0) CR_CUDA(cudaMalloc(&V->ws64, 2 * (size_t)nt * tile * sizeof(double)));
-  if (V->amp) CR_CUDA(cudaMalloc(&V->w32, 2 * (size_t)nt * tile * sizeof(float)));
+  if (off64 > 0) CR_TRY(ensure(&V->ws64, &V->cap_ws64, 2 * (size_t)nt * tile));
+  if (V->amp) CR_TRY(ensure(&V->w32, &V->cap_w32, 2 * (size_t)nt * tile));
   V->mapped = true;
   return CR_OK;
 }
