@@ -114,6 +114,14 @@ __device__ __forceinline__ int expo_pos(double x) {
   const int ex = (hi >> 20) & 0x7ff;
   return (hi > 0 && ex != 0 && ex != 0x7ff) ? ex - 1023 : 0;
 }
+// Row of element e of a row-by-row lower triangle (e = i (i + 1) / 2 + j, j <= i), in closed
+// form: a data-dependent loop would diverge across the lanes of a warp.
+__device__ __forceinline__ int tri_row(int e) {
+  int i = (int)((sqrtf(8.0f * (float)e + 1.0f) - 1.0f) * 0.5f);
+  if ((i + 1) * (i + 2) / 2 <= e) ++i;
+  if (i * (i + 1) / 2 > e) --i;
+  return i;
+}
 // x > 0 without an FP64 comparison (NaN and zero give false)
 __device__ __forceinline__ bool positive(double x) {
   const int hi = __double2hiint(x), lo = __double2loint(x);
@@ -122,53 +130,118 @@ __device__ __forceinline__ bool positive(double x) {
   return hi >= 0 && ((hi | lo) != 0) && !nan;
 }
 
-// Element owned by each thread in the fraction-free factorisation, packed as
-// (isT << 8) | (i << 4) | j: threads 0..135 the lower triangle (i >= j, row by row) of the
-// working matrix T, threads 136..255 the strict lower triangle of the transformed identity.
-// (Measured on GB300: this plain order beats orderings that group elements by the step in
-// which they fall idle.)
-struct FFMap {
-  unsigned short e[256];
+
+// Fraction-free factorisation of one N x N diagonal block by N^2 threads: threads
+// 0 .. N(N+1)/2-1 own the lower triangle of the working matrix (row by row), the others the
+// strict lower triangle of the transformed identity.  N = 16 uses the whole CTA and
+// __syncthreads; N = 8 would use warps 0-1 and named barrier 1 (measured on GB300: splitting
+// a 16 x 16 block into 8 x 8 halves is slower than eliminating it whole).
+constexpr int H = DB / 2;
+template <int N>
+struct FFS {
+  double col[2][N];   // column c of the working matrix, double-buffered by step parity
+  double row[2][N];   // row c of the transformed identity (unit-diagonal form)
+  double piv[N];      // t_cc
+  double alpha[N];    // alpha_c
+  double r[N];        // 1 / sqrt(alpha_c t_cc)
 };
-constexpr FFMap make_ff_map() {
-  FFMap m{};
-  int n = 0;
-  for (int i = 0; i < DB; ++i)
-    for (int j = 0; j <= i; ++j) m.e[n++] = (unsigned short)((1 << 8) | (i << 4) | j);
-  for (int i = 1; i < DB; ++i)
-    for (int j = 0; j < i; ++j) m.e[n++] = (unsigned short)((i << 4) | j);
-  return m;
+
+template <int N>
+__device__ __forceinline__ void ffbar() {
+  if (N == DB) __syncthreads();
+  else asm volatile("bar.sync 1, 64;" ::: "memory");
 }
-__constant__ FFMap c_ffmap = make_ff_map();
+
+// Division-free (fraction-free) elimination of the SPD block src (lower part, row stride
+// DB + 1): the Schur complement is carried as T = alpha_c S, and step c performs
+//   T <- 2^-k_c (t_cc T - t_c t_c^T)      with 2^-k_c t_cc in [1, 2),
+// so alpha_{c+1} = alpha_c t_cc 2^-k_c.  The same row operations applied to the identity,
+// carried with unit diagonal (Z = U^-1, A = U D U^T with U unit lower), give
+//   L_ic = t_ic r_c   and   L^-1 = diag(r) Z diag(alpha),   r_c = 1 / sqrt(alpha_c t_cc).
+// Every element's step is the same predicated multiply, FMA and exponent adjustment (no
+// divergent paths, no division or square root); the power of two comes from the pivot's
+// owner.  The alpha_c are a prefix product of the normalised pivots, taken by a shuffle scan
+// after the last step, followed by the N reciprocal square roots.  Lout receives L (lower
+// part), Xout L^-1 (upper part zero).  gcol: global column of the block's first column, for
+// the failure report.
+template <int N>
+__device__ void ffN(const Ctx& c, int gcol, const double* src, double* Lout, double* Xout, FFS<N>& f) {
+  const int t = threadIdx.x;   // 0 .. N*N-1
+  const bool isT = t < N * (N + 1) / 2;
+  int i, j;
+  if (isT) {
+    i = tri_row(t);
+    j = t - i * (i + 1) / 2;
+  } else {
+    const int u = t - N * (N + 1) / 2;   // strict lower: row i holds i elements
+    i = tri_row(u) + 1;
+    j = u - i * (i - 1) / 2;
+  }
+  double v = isT ? src[i * (DB + 1) + j] : 0.0;
+  for (int col = 0; col < N; ++col) {
+    const int par = col & 1;
+    // the owners of column col publish it (the pivot owner also into piv); nothing else
+    // stands between the last step's result and the barrier
+    if (isT && j == col) {
+      f.col[par][i] = v;
+      if (i == col) f.piv[col] = v;
+    }
+    if (!isT && i == col) f.row[par][j] = v;
+    ffbar<N>();
+    const double d = f.col[par][col];
+    const double a = f.col[par][i];
+    const double b = isT ? f.col[par][j] : (j == col ? 1.0 : f.row[par][j]);
+    const bool act = isT ? (j > col) : (i > col && j <= col);
+    const int e = -expo_pos(d);   // integer work that overlaps the FP64 latency below
+    if (__any_sync(0xffffffffu, act)) {   // warp-uniform: idle warps issue no FP64 work
+      const double nv = scale2(fma(-a, b, d * v), e);
+      v = act ? nv : v;                     // a select: divergent branches cost ~100 cycles a step
+    }
+  }
+  ffbar<N>();
+  if (t < 32) {
+    // alpha_t = prod_{c < t} 2^-k_c t_cc, inclusive shuffle scan over lanes 0 .. N-1
+    double x = 1.0;
+    if (t >= 1 && t < N) {
+      const double p = f.piv[t - 1];
+      if (!positive(p)) atomicMin(&c.status[1], gcol + t);
+      x = scale2(p, -expo_pos(p));
+    }
+    if (t == 0 && !positive(f.piv[0])) atomicMin(&c.status[1], gcol + 1);
+#pragma unroll
+    for (int o = 1; o < N; o <<= 1) {
+      const double y = __shfl_up_sync(0xffffffffu, x, o);
+      if (t >= o) x *= y;
+    }
+    if (t < N) {
+      f.alpha[t] = x;
+      f.r[t] = rsqrt(x * f.piv[t]);
+    }
+  }
+  ffbar<N>();
+  if (isT) {
+    Lout[i * (DB + 1) + j] = v * f.r[j];
+    if (i != j) Xout[j * (DB + 1) + i] = 0.0;
+    else Xout[i * (DB + 1) + i] = f.r[i] * f.alpha[i];
+  } else {
+    Xout[i * (DB + 1) + j] = f.r[i] * v * f.alpha[j];
+  }
+  ffbar<N>();
+}
 
 struct FFShared {
-  double col[2][DB];        // column c of the working matrix, double-buffered by step parity
-  int ex[2];                // -k_c: minus the binary exponent of the pivot t_cc
-  double row[2][DB];        // row c of the transformed identity
-  double alpha[DB + 1];     // alpha_c
-  double piv[DB];           // t_cc
-  double r[DB];             // 1 / sqrt(alpha_c t_cc)
-  double part[2][NT_LOWER]; // halves of the fused symmetric update
+  union {
+    double part[2][NT_LOWER];   // halves of the fused symmetric update (before the factorisation)
+    Blk l16[DB];                // the factor of the diagonal block
+  };
+  FFS<DB> f;
 };
 
 // Cholesky factor and inverse of diagonal block k, after subtracting P P^T when P is given
-// (the last symmetric update of the block, fused).  Division-free (fraction-free)
-// elimination: the Schur complement is carried as T = alpha_c S, and step c performs
-//   T <- 2^-k_c (t_cc T - t_c t_c^T)      with 2^-k_c t_cc in [1, 2),
-// so alpha_{c+1} = alpha_c t_cc 2^-k_c; the same row operations turn the identity into
-// Y = diag(alpha) U^-1 (A = U D U^T, U unit lower).  With r_c = 1 / sqrt(alpha_c t_cc):
-//   L_ic = t_ic r_c   and   L^-1 = diag(r) Y   (diagonal r_c alpha_c).
-// A step costs one multiply and one FMA per element and no division or square root; the
-// exact power-of-two scaling is applied by each thread to its own result, with the exponent
-// published by the pivot's owner, so a step's dependent path is a barrier, a shared load,
-// the multiply, the FMA and a few integer instructions.  The 16 reciprocal square roots
-// are taken together at the end.  The factor (lower part) is written to the tile, the
-// inverse (upper part zero) to Minv and to X.
-__device__ void potrf_ff(const Ctx& c, int k, const Blk* P, Blk* X, FFShared& sh) {
+// (the last symmetric update of the block, fused).  A16 is shared-memory scratch; the factor
+// (lower part) is written to the tile, the inverse (upper part zero) to Minv and to X.
+__device__ void potrf16(const Ctx& c, int k, const Blk* P, Blk* A16, Blk* X, FFShared& sh) {
   const int t = threadIdx.x;
-  const int code = c_ffmap.e[t];
-  const bool isT = (code >> 8) != 0;
-  const int i = (code >> 4) & 15, j = code & 15;
   double* a = c.A + (size_t)(k * DB) * c.nb + k * DB;
   if (P) {
     // lower element e = ii (ii + 1) / 2 + jj of P P^T, inner dimension in halves: thread t
@@ -176,8 +249,7 @@ __device__ void potrf_ff(const Ctx& c, int k, const Blk* P, Blk* X, FFShared& sh
     // the halves of elements 128..135
     auto half_sum = [&](int item) {
       const int e = item >> 1, q0 = (item & 1) * (DB / 2);
-      int ii = 0;
-      while ((ii + 1) * (ii + 2) / 2 <= e) ++ii;
+      const int ii = tri_row(e);
       const int jj = e - ii * (ii + 1) / 2;
       double s0 = 0.0, s1 = 0.0;
 #pragma unroll
@@ -191,54 +263,20 @@ __device__ void potrf_ff(const Ctx& c, int k, const Blk* P, Blk* X, FFShared& sh
     if (t < 2 * (NT_LOWER - 128)) half_sum(256 + t);
     __syncthreads();
   }
-  double v = 0.0;
-  if (isT) {
-    v = __ldcg(a + (size_t)i * c.nb + j);
-    if (P) {
-      const int e = i * (i + 1) / 2 + j;
-      v -= sh.part[0][e] + sh.part[1][e];
-    }
-  }
-  if (t == 0) sh.alpha[0] = 1.0;
-  for (int col = 0; col < DB; ++col) {
-    const int par = col & 1;
-    if (isT && j == col) {
-      sh.col[par][i] = v;
-      if (i == col) sh.ex[par] = -expo_pos(v);
-    }
-    if (!isT && i == col) sh.row[par][j] = v;
-    __syncthreads();
-    const double d = sh.col[par][col];
-    if (isT) {
-      if (j > col) v = scale2(fma(-sh.col[par][i], sh.col[par][j], d * v), sh.ex[par]);
-    } else if (i > col && j <= col) {
-      const double yc = (j == col) ? sh.alpha[col] : sh.row[par][j];
-      v = scale2(fma(-sh.col[par][i], yc, d * v), sh.ex[par]);
-    }
-    if (t == 0) {
-      if (!positive(d)) atomicMin(&c.status[1], c.gcol0 + k * DB + col + 1);
-      sh.piv[col] = d;
-      sh.alpha[col + 1] = scale2(sh.alpha[col] * d, sh.ex[par]);
-    }
+  if (t < NT_LOWER) {
+    const int i = tri_row(t);
+    const int j = t - i * (i + 1) / 2;
+    double v = __ldcg(a + (size_t)i * c.nb + j);
+    if (P) v -= sh.part[0][t] + sh.part[1][t];
+    A16[i][j] = v;
   }
   __syncthreads();
-  if (t < DB) sh.r[t] = rsqrt(sh.alpha[t] * sh.piv[t]);
-  __syncthreads();
+  ffN<DB>(c, c.gcol0 + k * DB, &A16[0][0], &sh.l16[0][0], &X[0][0], sh.f);
   double* m = c.Minv + (size_t)(k * DB) * c.nb + k * DB;
-  if (isT) {
-    a[(size_t)i * c.nb + j] = v * sh.r[j];
-    if (i != j) {
-      X[j][i] = 0.0;
-      m[(size_t)j * c.nb + i] = 0.0;
-    } else {
-      const double xd = sh.r[i] * sh.alpha[i];
-      X[i][i] = xd;
-      m[(size_t)i * c.nb + i] = xd;
-    }
-  } else {
-    const double x = sh.r[i] * v;
-    X[i][j] = x;
-    m[(size_t)i * c.nb + j] = x;
+  {
+    const int i = t / DB, j = t % DB;
+    m[(size_t)i * c.nb + j] = X[i][j];
+    if (j <= i) a[(size_t)i * c.nb + j] = sh.l16[i][j];
   }
 }
 
@@ -277,10 +315,10 @@ __device__ __forceinline__ double gemm_elem(const Blk* P, const Blk* Q) {
 
 // The critical chain, run by one CTA with the blocks kept in shared memory:
 // POTRF(0); then for k = 0 .. NB-2: TRSM(k+1,k), then UPDATE(k+1,k+1,k) fused into POTRF(k+1).
-__device__ void run_chain(const Ctx& c, Blk* S1, Blk* S2, Blk* S3, FFShared& sh, int* s_ok) {
+__device__ void run_chain(const Ctx& c, Blk* S0, Blk* S1, Blk* S2, Blk* S3, FFShared& sh, int* s_ok) {
   const int NB = c.NB;
   const size_t rowstride = (size_t)DB * c.nb;
-  potrf_ff(c, 0, nullptr, S1, sh);   // S1 = M_00
+  potrf16(c, 0, nullptr, S0, S1, sh);   // S1 = M_00
   __syncthreads();
   if (threadIdx.x == 0) st_release(&c.fac[0], 1);
   int r, cc;
@@ -303,7 +341,7 @@ __device__ void run_chain(const Ctx& c, Blk* S1, Blk* S2, Blk* S3, FFShared& sh,
     if (threadIdx.x == 0) *s_ok = wait_ge(c, &c.ver[i * NB + i], k) ? 1 : 0;
     __syncthreads();
     if (!*s_ok) return;
-    potrf_ff(c, i, S3, S1, sh);        // S1 = M_ii
+    potrf16(c, i, S3, S0, S1, sh);        // S1 = M_ii
     __syncthreads();
     if (threadIdx.x == 0) st_release(&c.fac[i * NB + i], 1);
   }
@@ -323,7 +361,7 @@ __global__ void __launch_bounds__(256) k_diag_chol(Ctx c, const int4* __restrict
   if (threadIdx.x == 0) s_task = atomicAdd(role, 1);
   __syncthreads();
   if (s_task == 0) {
-    run_chain(c, S1, S2, S3, sh, &s_ok);
+    run_chain(c, S0, S1, S2, S3, sh, &s_ok);
     return;
   }
   while (true) {
@@ -420,10 +458,12 @@ bool diag_task_list(int NB, std::vector<int4>& tasks) {
       for (int R = k + 1; R < NB; ++R) tasks.push_back(make_int4(T_IUPD, R, C, k));
   };
   for (int k = 0; k < NB; ++k) {
+    // all solves of the step first (they run side by side), then the updates row by row,
+    // nearest the diagonal first: UPDATE(k+2,k+1,k) and UPDATE(k+2,k+2,k) feed the chain's
+    // next step
     for (int i = k + 2; i < NB; ++i) tasks.push_back(make_int4(T_TRSM, i, k, k));
-    for (int j = k + 1; j < NB; ++j)
-      for (int i = j; i < NB; ++i)
-        if (!(i == k + 1 && j == k + 1)) tasks.push_back(make_int4(T_UPDATE, i, j, k));
+    for (int i = k + 2; i < NB; ++i)
+      for (int j = k + 1; j <= i; ++j) tasks.push_back(make_int4(T_UPDATE, i, j, k));
     if (k >= lag) inverse_step(k - lag);
   }
   for (int k = std::max(0, NB - lag); k < NB; ++k) inverse_step(k);
