@@ -34,7 +34,11 @@ sys.path.insert(0, ROOT)
 
 import inputgen  # noqa: E402
 
-FP64_PEAK_TFLOPS = 1.19       # measured DFMA rate on this GB300 pool (profiles/fp64_peak_microbench.md)
+FP64_PEAK_TFLOPS = 1.19       # measured DFMA rate on GB300 (profiles/fp64_peak_microbench.md)
+# DRAM bytes per launch from one ncu capture of the kernel as it stands (profiles/); None once
+# the kernel has changed since the capture
+NCU_TRAFFIC_PER_LAUNCH = {"k_diag_chol": None, "k_tc_old": None, "k_tc_trmm": None}
+TIMED_KERNELS = ["k_diag_chol", "k_tc_old", "k_tc_new", "k_tc_trsm", "k_tc_trmm", "k_cov_stats", "k_generate", "k_scan"]
 WORKLOAD = inputgen.WORKLOADS["c"]
 SEED_Z = 12345
 
@@ -233,6 +237,8 @@ def run_ours(args, world, rank, local):
     barrier(world)
     torch.cuda.synchronize()
     l0 = cr.kernel_launches()
+    cr.timing_reset()
+    cr.timing_enable(not args.no_kernel_timing)
     evs = [[ev() for _ in range(6)] for _ in range(args.steps)]
     t_start, t_end = ev(), ev()
     wall0 = time.perf_counter()
@@ -243,7 +249,9 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     barrier(world)
     wall = time.perf_counter() - wall0
+    cr.timing_enable(False)
     launches = cr.kernel_launches() - l0
+    ktime = {k: cr.timing_read(k) for k in TIMED_KERNELS}
     clk = clocks.stop()
     total_ms = t_start.elapsed_time(t_end)
     total_ms = max_over_ranks(total_ms, world)
@@ -263,14 +271,46 @@ def run_ours(args, world, rank, local):
     t_star = sum(fch[k] / peak_of[k] for k in fch) + sum(ftr[k] / peak_of[k] for k in ftr)
     frac_weighted = t_star / (ct_ms / 1e3)
 
-    # roofline of the simulation multiply (TRMM), timed live: one launch per step
-    trmm_flops = 2.0 * (ftr["fp16"] + 2.0 * ftr["fp32"]) / 2.0   # algorithmic n^2 M (diagonal counted once)
-    trmm_flops = float(n) ** 2 * M
-    trmm_ms = st["rng_trmm"]
-    roof = {"kernel": "k_tc (TRMM mode) + fused normal draws", "bound": "tensor",
-            "achieved": trmm_flops / (trmm_ms / 1e3) / 1e12, "peak": pk["bf16"], "unit": "TFLOP/s",
-            "frac": None, "traffic": None, "peak_source": f"{pk['src']} bf16 burst (FP16 runs at the bf16 rate)"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
+    # per-kernel device time inside the timed region (library events on each kernel's own
+    # stream) and the roofline of each against its algorithmic work per launch
+    kern = {}
+    def entry(name, bound, work_per_launch, unit, peak, peak_note):
+        k_ms, cnt = ktime[name]
+        if cnt == 0:
+            return None
+        per = k_ms / cnt
+        ach = work_per_launch / (per / 1e3) / (1e12 if unit == "TFLOP/s" else 1e9)
+        return {"kernel": name, "bound": bound, "launches_per_step": cnt / args.steps, "ms_per_launch": per,
+                "ms_per_step": k_ms / args.steps, "achieved": ach, "peak": peak, "unit": unit, "frac": ach / peak,
+                "traffic": NCU_TRAFFIC_PER_LAUNCH.get(name), "peak_source": peak_note}
+    meas = "measured" if pk["src"] == "measured" else "fallback"
+    kern["k_diag_chol"] = entry("k_diag_chol", "alu", 2.0 * nb ** 3 / 3.0, "TFLOP/s", FP64_PEAK_TFLOPS,
+                                "FP64 DFMA rate, own microbenchmark (profiles/fp64_peak_microbench.md); work: "
+                                "nb^3/3 factor + nb^3/3 triangular inverse per launch")
+    kern["k_tc_trmm"] = entry("k_tc_trmm", "tensor", float(n) ** 2 * M, "TFLOP/s", pk["bf16"],
+                              f"{meas} bf16 burst (FP16 MMA runs at the bf16 rate); work: n^2 M per launch")
+    kern["k_scan"] = entry("k_scan", "hbm", 8.0 * n * M + 16.0 * n, "GB/s", pk["hbm"],
+                           f"{meas} HBM copy bandwidth; work: 8 n M + 16 n bytes per launch")
+    # the Cholesky's tensor-core kernels together: algorithmic products / their summed time
+    tc_ms = sum(ktime[k][0] for k in ("k_tc_old", "k_tc_new", "k_tc_trsm")) / args.steps
+    if tc_ms > 0:
+        ach = (fch["fp16"] + fch["fp32"]) / (tc_ms / 1e3) / 1e12
+        kern["k_tc_cholesky"] = {"kernel": "k_tc_old + k_tc_new + k_tc_trsm", "bound": "tensor", "ms_per_step": tc_ms,
+                                 "achieved": ach, "peak": pk["bf16_sus"], "unit": "TFLOP/s",
+                                 "frac": ach / pk["bf16_sus"], "traffic": None,
+                                 "peak_source": f"{meas} bf16 sustained; work: FP16- and FP32-class Cholesky products "
+                                                "(one per product, however many MMAs it takes)"}
+    for k in ("k_tc_new", "k_tc_trsm", "k_cov_stats", "k_generate"):
+        k_ms, cnt = ktime[k]
+        if cnt:
+            kern[k] = {"kernel": k, "ms_per_step": k_ms / args.steps, "launches_per_step": cnt / args.steps}
+    timed = {k: v for k, v in kern.items() if v and "achieved" in v}
+    roof = None
+    if timed:
+        dominant = max(timed.values(), key=lambda e: e["ms_per_step"])
+        roof = {key: dominant[key] for key in ("bound", "achieved", "peak", "unit", "frac", "traffic")}
+        roof["kernel"] = dominant["kernel"]
+        roof["peak_source"] = dominant["peak_source"]
 
     # end to end through the public API with host buffers: H2D of the locations, D2H of
     # the regions and counts, every step
@@ -296,7 +336,7 @@ def run_ours(args, world, rank, local):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        n_s, M_s = 3072, 2048
+        n_s, M_s = 8192, 2048     # about 10-20 s of host work
         dt, fl = oracle_sample(n_s, M_s)
         cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
                "sample": f"one oracle pass (covariance, unblocked Cholesky, simulation, calibration) on the leading "
@@ -318,6 +358,7 @@ def run_ours(args, world, rank, local):
             "precision_map": {"n_fp64": info["n_fp64"], "n_fp32": info["n_fp32"], "n_fp16": info["n_fp16"],
                               "s": info["s"], "check1": info["check1"], "check2": info["check2"]},
             "roofline": roof,
+            "kernels": kern,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": int(xy_h.nbytes),
                     "d2h_bytes_per_step": int(n * (1 + 1 + 4))},
@@ -332,10 +373,11 @@ def run_ours(args, world, rank, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-kernel-timing", action="store_true", help="skip the per-kernel device timing (no roofline)")
     ap.add_argument("--n", type=int, default=0, help="profiling only: smaller n of the same workload family")
     args = ap.parse_args()
     global WORKLOAD

@@ -99,6 +99,22 @@ cr_status cr_version(int* major, int* minor);
  * *count receives the running total.  Host-side counter, no device work. */
 cr_status cr_kernel_launches(uint64_t* count);
 
+/* Device timing of the library's main kernels, for measurement (the paper has no counterpart).
+ * While enabled, every launch of a timed kernel is bracketed by two CUDA events recorded on
+ * the stream the kernel is launched on, and the durations are accumulated per kernel name:
+ *   "k_diag_chol"   FP64 factor and inverse of one diagonal tile
+ *   "k_tc_old", "k_tc_new", "k_tc_trsm", "k_tc_trmm"   tensor-core kernel by mode
+ *   "k_cov_stats", "k_generate"   covariance statistics and tile generation
+ *   "k_scan"        calibration scan
+ * cr_timing_enable(on) switches recording on (1) or off (0); it does not clear the totals.
+ * cr_timing_read(name, &ms, &n) synchronises the device, folds every recorded launch into the
+ * totals and returns the total milliseconds and launch count of `name` (0 if never timed).
+ * cr_timing_reset() clears all totals.  cr_timing_enable(1) creates a pool of 16384 events
+ * (8192 timed launches between two reads); launches beyond the pool are not timed. */
+cr_status cr_timing_enable(int on);
+cr_status cr_timing_read(const char* kernel, double* total_ms, uint64_t* launches);
+cr_status cr_timing_reset(void);
+
 /* A symmetric n x n matrix stored as its lower tiles (i >= j) of nb x nb entries.
  * NT = ceil(n / nb) tile rows; rows and columns past n are padding and behave like the
  * identity.  nb must be a multiple of 128 with 128 <= nb <= 1024.  The handle owns its

@@ -78,6 +78,9 @@ _SIGNATURES = {
     "cr_last_error_detail": (ctypes.c_char_p, []),
     "cr_version": (_I, [ctypes.POINTER(_I), ctypes.POINTER(_I)]),
     "cr_kernel_launches": (_I, [ctypes.POINTER(_U64)]),
+    "cr_timing_enable": (_I, [_I]),
+    "cr_timing_read": (_I, [ctypes.c_char_p, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_U64)]),
+    "cr_timing_reset": (_I, []),
     "cr_tilemat_create": (_I, [_I, _I, ctypes.POINTER(_P)]),
     "cr_tilemat_destroy": (_I, [_P]),
     "cr_tilemat_info": (_I, [_P, ctypes.POINTER(_I), ctypes.POINTER(_I), ctypes.POINTER(_I)]),
@@ -158,6 +161,27 @@ def kernel_launches() -> int:
     c = _U64(0)
     _check(_lib.cr_kernel_launches(ctypes.byref(c)))
     return c.value
+
+
+def timing_enable(on: bool) -> None:
+    """cr_timing_enable: bracket launches of the timed kernels with CUDA events."""
+    load()
+    _check(_lib.cr_timing_enable(1 if on else 0))
+
+
+def timing_read(kernel: str) -> tuple[float, int]:
+    """cr_timing_read: (total milliseconds, launches) of a timed kernel; synchronises."""
+    load()
+    ms = ctypes.c_double(0.0)
+    n = _U64(0)
+    _check(_lib.cr_timing_read(kernel.encode(), ctypes.byref(ms), ctypes.byref(n)))
+    return ms.value, n.value
+
+
+def timing_reset() -> None:
+    """cr_timing_reset: clear the accumulated kernel times."""
+    load()
+    _check(_lib.cr_timing_reset())
 
 
 class TileMat:

@@ -2,6 +2,10 @@
 #include <stdio.h>
 
 #include <atomic>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
 #include <mutex>
 
 #include "common.cuh"
@@ -15,6 +19,59 @@ static thread_local const char* g_literal = nullptr;
 static std::atomic<uint64_t> g_launches{0};
 
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+namespace {
+struct TimingState {
+  std::mutex mu;
+  bool on = false;
+  std::vector<cudaEvent_t> free_events;
+  struct Pending { std::string name; cudaEvent_t a, b; };
+  std::vector<Pending> pending;
+  std::map<std::string, std::pair<double, uint64_t>> totals;
+  // an event from the pool made by cr_timing_enable; when the pool runs dry the launch is
+  // simply not timed (no event is created between launches)
+  cudaEvent_t get() {
+    if (free_events.empty()) return nullptr;
+    cudaEvent_t e = free_events.back();
+    free_events.pop_back();
+    return e;
+  }
+  void fold() {
+    for (auto& p : pending) {
+      float ms = 0.0f;
+      if (cudaEventSynchronize(p.b) == cudaSuccess && cudaEventElapsedTime(&ms, p.a, p.b) == cudaSuccess) {
+        auto& t = totals[p.name];
+        t.first += ms;
+        t.second += 1;
+      }
+      free_events.push_back(p.a);
+      free_events.push_back(p.b);
+    }
+    pending.clear();
+  }
+};
+TimingState& timing() {
+  static TimingState t;
+  return t;
+}
+}  // namespace
+
+TimedScope::TimedScope(const char* n, cudaStream_t s) : name(n), stream(s) {
+  auto& T = timing();
+  std::lock_guard<std::mutex> lk(T.mu);
+  if (!T.on) return;
+  start = T.get();
+  if (start && cudaEventRecord(start, stream) != cudaSuccess) start = nullptr;
+}
+
+TimedScope::~TimedScope() {
+  if (!start) return;
+  auto& T = timing();
+  std::lock_guard<std::mutex> lk(T.mu);
+  cudaEvent_t stop = T.get();
+  if (stop && cudaEventRecord(stop, stream) == cudaSuccess) T.pending.push_back({name, start, stop});
+  else T.free_events.push_back(start);
+}
 
 void set_error(const std::string& msg) {
   g_literal = nullptr;
@@ -129,6 +186,42 @@ extern "C" cr_status cr_version(int* major, int* minor) {
   return CR_OK;
 }
 
+extern "C" cr_status cr_timing_enable(int on) {
+  auto& T = timing();
+  std::lock_guard<std::mutex> lk(T.mu);
+  if (on) {
+    // events are created here, not between launches: creating them while the library
+    // enqueues its schedule would hold back the launches it is timing
+    T.fold();
+    while (T.free_events.size() < 16384) {
+      cudaEvent_t e = nullptr;
+      if (cudaEventCreate(&e) != cudaSuccess) return fail(CR_ERR_CUDA, "cr_timing_enable: cudaEventCreate");
+      T.free_events.push_back(e);
+    }
+  }
+  T.on = on != 0;
+  return CR_OK;
+}
+
+extern "C" cr_status cr_timing_read(const char* kernel, double* total_ms, uint64_t* launches) {
+  if (!kernel || !total_ms || !launches) return fail(CR_ERR_ARG, "cr_timing_read: NULL argument");
+  auto& T = timing();
+  std::lock_guard<std::mutex> lk(T.mu);
+  T.fold();
+  auto it = T.totals.find(kernel);
+  *total_ms = it == T.totals.end() ? 0.0 : it->second.first;
+  *launches = it == T.totals.end() ? 0 : it->second.second;
+  return CR_OK;
+}
+
+extern "C" cr_status cr_timing_reset(void) {
+  auto& T = timing();
+  std::lock_guard<std::mutex> lk(T.mu);
+  T.fold();
+  T.totals.clear();
+  return CR_OK;
+}
+
 extern "C" cr_status cr_kernel_launches(uint64_t* count) {
   if (!count) return fail(CR_ERR_ARG, "cr_kernel_launches: NULL");
   *count = g_launches.load(std::memory_order_relaxed);
@@ -151,7 +244,7 @@ extern "C" cr_status cr_tilemat_create(int n, int nb, cr_tilemat* out) {
   if ((e = cudaMalloc(&V->xy, (size_t)n * 2 * sizeof(double))) != cudaSuccess ||
       (e = cudaMalloc(&V->stat_part, (size_t)V->ntiles * (nb / 64) * 3 * sizeof(double))) != cudaSuccess ||
       (e = cudaMalloc(&V->stats, (size_t)V->ntiles * 3 * sizeof(double))) != cudaSuccess ||
-      (e = cudaMalloc(&V->minv, tile * sizeof(double))) != cudaSuccess ||
+      (e = cudaMalloc(&V->minv, 2 * tile * sizeof(double))) != cudaSuccess ||
       (e = cudaMalloc(&V->scratch64, tile * sizeof(double))) != cudaSuccess ||
       (e = cudaMalloc(&V->d_status, 4 * sizeof(int))) != cudaSuccess) {
     cr_status st = cuda_fail(e, "cr_tilemat_create: cudaMalloc");
@@ -172,6 +265,7 @@ extern "C" cr_status cr_tilemat_destroy(cr_tilemat V) {
   dfree(V->xy); dfree(V->stat_part); dfree(V->stats); dfree(V->minv); dfree(V->scratch64); dfree(V->d_status);
   if (V->s_hi) cudaStreamDestroy(V->s_hi);
   if (V->s_lo) cudaStreamDestroy(V->s_lo);
+  if (V->s_mid) cudaStreamDestroy(V->s_mid);
   delete V;
   return CR_OK;
 }

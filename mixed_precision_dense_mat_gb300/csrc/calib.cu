@@ -31,52 +31,87 @@ __global__ void k_tstat(const double* __restrict__ zhat, const double* __restric
   }
 }
 
+// Order-preserving 64-bit keys of doubles: for x, y not NaN and with -0 taken as +0,
+// x < y exactly when key(x) < key(y) as unsigned integers.  The scan compares and reduces
+// keys in integer arithmetic: GB300's FP64 units issue a warp instruction only every ~64
+// cycles, which would bound a double-precision scan far below HBM bandwidth.
+__device__ __forceinline__ unsigned long long dkey(double x) {
+  unsigned long long b = (unsigned long long)__double_as_longlong(x);
+  if (b == 0x8000000000000000ull) b = 0;   // -0 -> +0
+  return (b >> 63) ? ~b : (b | 0x8000000000000000ull);
+}
+__device__ __forceinline__ double dkey_inv(unsigned long long k) {
+  const unsigned long long b = (k >> 63) ? (k & 0x7fffffffffffffffull) : ~k;
+  return __longlong_as_double((long long)b);
+}
+__device__ __forceinline__ bool dnan(double x) {
+  return ((unsigned long long)__double_as_longlong(x) & 0x7fffffffffffffffull) > 0x7ff0000000000000ull;
+}
+
 __global__ void __launch_bounds__(SCAN_THREADS) k_scan(const double* __restrict__ S, int lds, int n_p, int M,
                                                        const double* __restrict__ t, double u, double* __restrict__ psi_part,
                                                        double* __restrict__ phi_part, int32_t* __restrict__ count) {
   constexpr int RPT = SCAN_ROWS / SCAN_THREADS;   // rows per thread
+  constexpr unsigned long long KEY_PINF = 0xfff0000000000000ull, KEY_MINF = 0x000fffffffffffffull;
   const int rb = blockIdx.x, cbk = blockIdx.y;
   const int row0 = rb * SCAN_ROWS + threadIdx.x;
-  double tq[RPT];
+  const unsigned long long ku = dkey(u);
+  unsigned long long tk[RPT];
   int cnt[RPT];
 #pragma unroll
   for (int q = 0; q < RPT; ++q) {
     const int r = row0 + q * SCAN_THREADS;
-    tq[q] = r < n_p ? t[r] : 0.0;
+    tk[q] = r < n_p ? dkey(t[r]) : 0ull;
     cnt[q] = 0;
   }
-  __shared__ double s_mn[SCAN_THREADS / 32][SCAN_COLS];
-  __shared__ double s_mx[SCAN_THREADS / 32][SCAN_COLS];
+  __shared__ unsigned long long s_mn[SCAN_THREADS / 32][SCAN_COLS];
+  __shared__ unsigned long long s_mx[SCAN_THREADS / 32][SCAN_COLS];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c_end = min(SCAN_COLS, M - cbk * SCAN_COLS);
-  for (int c = 0; c < c_end; ++c) {
+  double nxt[RPT];
+  auto load_col = [&](int c, double* dst) {
     const double* col = S + (size_t)(cbk * SCAN_COLS + c) * lds;
-    double val[RPT];
 #pragma unroll
     for (int q = 0; q < RPT; ++q) {
       const int r = row0 + q * SCAN_THREADS;
-      val[q] = r < n_p ? __ldcs(col + r) : NAN;
+      dst[q] = r < n_p ? __ldcs(col + r) : __longlong_as_double(0x7ff8000000000000ll);   // NaN: no row
     }
-    double mn = INFINITY, mx = -INFINITY;
+  };
+  if (c_end > 0) load_col(0, nxt);
+  for (int c = 0; c < c_end; ++c) {
+    double val[RPT];
+#pragma unroll
+    for (int q = 0; q < RPT; ++q) val[q] = nxt[q];
+    if (c + 1 < c_end) load_col(c + 1, nxt);   // next column in flight during this one's work
+    unsigned long long mn = KEY_PINF, mx = KEY_MINF;
 #pragma unroll
     for (int q = 0; q < RPT; ++q) {
-      if (val[q] >= u) { mn = fmin(mn, tq[q]); ++cnt[q]; }
-      if (val[q] <= u) mx = fmax(mx, tq[q]);
+      const bool ok = !dnan(val[q]);
+      const unsigned long long kv = dkey(val[q]);
+      const bool ge = ok && kv >= ku, le = ok && kv <= ku;
+      if (ge && tk[q] < mn) mn = tk[q];
+      if (le && tk[q] > mx) mx = tk[q];
+      cnt[q] += ge ? 1 : 0;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-      mn = fmin(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-      mx = fmax(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      const unsigned long long a = __shfl_xor_sync(0xffffffffu, mn, o);
+      const unsigned long long b = __shfl_xor_sync(0xffffffffu, mx, o);
+      mn = a < mn ? a : mn;
+      mx = b > mx ? b : mx;
     }
     if (lane == 0) { s_mn[warp][c] = mn; s_mx[warp][c] = mx; }
   }
   __syncthreads();
   if (threadIdx.x < c_end) {
-    double mn = INFINITY, mx = -INFINITY;
-    for (int w = 0; w < SCAN_THREADS / 32; ++w) { mn = fmin(mn, s_mn[w][threadIdx.x]); mx = fmax(mx, s_mx[w][threadIdx.x]); }
+    unsigned long long mn = KEY_PINF, mx = KEY_MINF;
+    for (int w = 0; w < SCAN_THREADS / 32; ++w) {
+      mn = s_mn[w][threadIdx.x] < mn ? s_mn[w][threadIdx.x] : mn;
+      mx = s_mx[w][threadIdx.x] > mx ? s_mx[w][threadIdx.x] : mx;
+    }
     const size_t o = (size_t)rb * M + cbk * SCAN_COLS + threadIdx.x;
-    psi_part[o] = mn;
-    phi_part[o] = mx;
+    psi_part[o] = dkey_inv(mn);   // +inf / -inf when the block's column has no qualifying row
+    phi_part[o] = dkey_inv(mx);
   }
   if (count) {
 #pragma unroll
@@ -122,7 +157,10 @@ cr_status calibrate_core(const double* d_S, int lds, int n_p, int M, const doubl
   CR_CHECK_LAUNCH("k_tstat");
   if (d_count) CR_CUDA(cudaMemsetAsync(d_count, 0, (size_t)n_p * sizeof(int32_t), stream));
   dim3 grid(nrb, (M + SCAN_COLS - 1) / SCAN_COLS);
-  k_scan<<<grid, SCAN_THREADS, 0, stream>>>(d_S, lds, n_p, M, sc.t, u, sc.psi_part, sc.phi_part, d_count);
+  {
+    TimedScope ts("k_scan", stream);
+    k_scan<<<grid, SCAN_THREADS, 0, stream>>>(d_S, lds, n_p, M, sc.t, u, sc.psi_part, sc.phi_part, d_count);
+  }
   CR_CHECK_LAUNCH("k_scan");
   k_scan_reduce<<<std::min(1024, (M + 255) / 256), 256, 0, stream>>>(sc.psi_part, sc.phi_part, nrb, M, sc.psi, sc.phi);
   CR_CHECK_LAUNCH("k_scan_reduce");

@@ -17,6 +17,7 @@
 // two streams.  This replaces the paper's PaRSEC task runtime on one GPU.
 #include <stdlib.h>
 
+#include <algorithm>
 #include <functional>
 
 #include "common.cuh"
@@ -38,10 +39,12 @@ __global__ void k_zero_upper(double* A, int nb) {
 namespace {
 
 struct Exec {
-  cudaStream_t hi, lo;
+  cudaStream_t hi, lo, mid;
   const DJob* dj;
   const DPair* dp;
-  std::vector<cudaEvent_t> ev;   // per column: [2j] solves done (hi), [2j+1] older updates done (lo)
+  // per column j: OLD(j) done (lo); diagonal factor and inverse split (hi); NEW(j) rows j+1..
+  // done (mid); solve of row j+1 done (hi); solves of rows j+2.. done (mid)
+  std::vector<cudaEvent_t> ev_old, ev_split, ev_newr, ev_crit, ev_rest;
   cudaEvent_t start;
 };
 
@@ -56,11 +59,13 @@ struct Plan {
     pairs.push_back(DPair{A, B, sAm, sAk, sBn, sBk, K});
     return (int)pairs.size() - 1;
   }
-  void dgemm(int block, const std::vector<DJob>& js, bool on_lo) {
+  void dgemm(int block, const std::vector<DJob>& js, bool on_lo, bool on_mid = false) {
     if (js.empty()) return;
     const int off = (int)jobs.size(), cnt = (int)js.size();
     jobs.insert(jobs.end(), js.begin(), js.end());
-    ops.push_back([=](Exec& x) -> cr_status { return dgemm_launch(block, x.dj + off, x.dp, cnt, on_lo ? x.lo : x.hi); });
+    ops.push_back([=](Exec& x) -> cr_status {
+      return dgemm_launch(block, x.dj + off, x.dp, cnt, on_lo ? x.lo : (on_mid ? x.mid : x.hi));
+    });
   }
 };
 
@@ -112,6 +117,67 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
   base.status = V->d_status;
   base.err = V->d_status;
   const CUtensorMap* tm = &V->tm_pool16;
+  // grid caps: the persistent tensor-core CTAs hold their SMs for a whole launch, and a
+  // higher stream priority does not preempt them, so the bulk and lookahead launches leave
+  // SMs free for the few blocks the critical stream launches (at most 8 per launch)
+  int sms = 0;
+  CR_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, V->device));
+  // lookahead launches of column j have about 8 (nt - j) output blocks of short inner length
+  // that must finish within one diagonal factorisation: about 16 blocks per CTA
+  auto cap_mid_of = [&](int j) { return std::min(48, std::max(8, (8 * (nt - j) + 15) / 16)); };
+
+  // FP64 products of the newest term k = j - 1 into rows [r0, r1) of column j
+  auto new_dgemm = [&](int j, int r0, int r1, bool on_mid) {
+    const int knew = j - 1, par = j & 1;
+    if (knew < 0) return;
+    std::vector<DJob> js;
+    for (int i = r0; i < r1; ++i) {
+      if (cls[tidx(i, j)] != CR_PREC_FP64) continue;
+      if (!(cls[tidx(i, knew)] == CR_PREC_FP64 && cls[tidx(j, knew)] == CR_PREC_FP64)) continue;
+      const int p = P.add_pair(t64(i, knew), t64(j, knew), nb, 1, nb, 1, nb);
+      double* C = i == j ? t64(i, j) : ws64(par, i);
+      for (int bi = 0; bi < nb / 64; ++bi)
+        for (int bj = 0; bj < nb / 64; ++bj) {
+          if (i == j && bj > bi) continue;
+          js.push_back(job(C + (size_t)bi * 64 * nb + bj * 64, nb, 1, 64, 64, p, 1, -1.0, 1.0, bi * 64, bj * 64, nb));
+        }
+    }
+    P.dgemm(64, js, false, on_mid);
+  };
+  // solves of rows [r0, r1) of column j: tensor cores for FP16/FP32-class tiles (rows list at
+  // d_rows + off, cnt entries), FP64 products with the inverse for FP64-class tiles
+  auto solves = [&](int j, int r0, int r1, const TcParams& tp, int off, int cnt, bool on_mid, int cap_mid) {
+    const int par = j & 1;
+    if (cnt > 0) {
+      TcParams t = tp;
+      t.mode = TC_TRSM;
+      t.rows = d_rows + off;
+      t.nrows = cnt;
+      t.max_ctas = on_mid ? cap_mid : 0;
+      P.ops.push_back([=](Exec& x) -> cr_status { return tc_launch(t, *tm, *tm, on_mid ? x.mid : x.hi); });
+    }
+    std::vector<DJob> js;
+    std::vector<int> fp64_rows;
+    double* Minv = V->minv + (size_t)par * nb2;
+    for (int i = r0; i < r1; ++i) {
+      if (cls[tidx(i, j)] != CR_PREC_FP64) continue;
+      fp64_rows.push_back(i);
+      const int p = P.add_pair(ws64(par, i), Minv, nb, 1, nb, 1, nb);
+      double* C = t64(i, j);
+      for (int bi = 0; bi < nb / 64; ++bi)
+        for (int bj = 0; bj < nb / 64; ++bj)
+          js.push_back(job(C + (size_t)bi * 64 * nb + bj * 64, nb, 1, 64, 64, p, 1, 1.0, 0.0, bi * 64, bj * 64, (bj + 1) * 64));
+    }
+    P.dgemm(64, js, false, on_mid);
+    if (V->amp) {
+      for (int i : fp64_rows) {
+        const double* src = t64(i, j);
+        __half* h = V->pool16 + (size_t)V->h_hi16[tidx(i, j)] * nb2;
+        __half* l = V->pool16 + (size_t)V->h_lo16[tidx(i, j)] * nb2;
+        P.ops.push_back([=](Exec& x) -> cr_status { return split_tile_launch(src, nb, h, l, 0, on_mid ? x.mid : x.hi); });
+      }
+    }
+  };
 
   for (int j = 0; j < nt; ++j) {
     const int par = j & 1;
@@ -121,12 +187,21 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
     tp.j = j;
     tp.ws_hi0 = V->ws_hi0 + par * nt;
     tp.ws_lo0 = V->ws_lo0 + par * nt;
+    tp.minv_hi = V->minv_hi + par;
+    tp.minv_lo = V->minv_lo + par;
+    tp.status = V->d_status + par;           // status[2 + par]: exponent of this column's scaled inverse
     tp.ws64 = V->ws64 ? ws64(par, 0) : nullptr;
     tp.w32 = V->w32 ? V->w32 + (size_t)par * nt * nb2 : nullptr;
+    const int cap_mid = cap_mid_of(j), cap_lo = std::max(1, sms - cap_mid - 8);
 
-    // ---------------- OLD(j) on the low-priority stream
+    // ---------------- OLD(j) on the low-priority stream: needs columns <= j-2 complete
     P.ops.push_back([=](Exec& x) -> cr_status {
-      CR_CUDA(cudaStreamWaitEvent(x.lo, j >= 2 ? x.ev[2 * (j - 2)] : x.start, 0));
+      if (j >= 2) {
+        CR_CUDA(cudaStreamWaitEvent(x.lo, x.ev_crit[j - 2], 0));
+        CR_CUDA(cudaStreamWaitEvent(x.lo, x.ev_rest[j - 2], 0));
+      } else {
+        CR_CUDA(cudaStreamWaitEvent(x.lo, x.start, 0));
+      }
       return CR_OK;
     });
     {
@@ -151,10 +226,11 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
     if (V->amp) {
       TcParams t = tp;
       t.mode = TC_UPD_OLD;
-      t.rows = nullptr;
       t.kbeg = 0;
       t.kend = kold_end;
+      t.row0 = j;
       t.nrows = nt - j;
+      t.max_ctas = cap_lo;
       P.ops.push_back([=](Exec& x) -> cr_status { return tc_launch(t, *tm, *tm, x.lo); });
     } else {
       for (int i = j + 1; i < nt; ++i) {
@@ -166,42 +242,43 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
         });
       }
     }
+    P.ops.push_back([=](Exec& x) -> cr_status { CR_CUDA(cudaEventRecord(x.ev_old[j], x.lo)); return CR_OK; });
+
+    // ---------------- lookahead stream, part 1: NEW(j) for rows j+1.. (needs OLD(j) and the
+    // solve of row j of column j-1, which is on the critical stream)
     P.ops.push_back([=](Exec& x) -> cr_status {
-      CR_CUDA(cudaEventRecord(x.ev[2 * j + 1], x.lo));
-      CR_CUDA(cudaStreamWaitEvent(x.hi, x.ev[2 * j + 1], 0));
+      CR_CUDA(cudaStreamWaitEvent(x.mid, x.ev_old[j], 0));
+      if (j >= 1) CR_CUDA(cudaStreamWaitEvent(x.mid, x.ev_crit[j - 1], 0));
       return CR_OK;
     });
-
-    // ---------------- NEW(j) on the high-priority stream
-    if (knew >= 0) {
-      std::vector<DJob> js;
-      for (int i = j; i < nt; ++i) {
-        if (cls[tidx(i, j)] != CR_PREC_FP64) continue;
-        if (!(cls[tidx(i, knew)] == CR_PREC_FP64 && cls[tidx(j, knew)] == CR_PREC_FP64)) continue;
-        const int p = P.add_pair(t64(i, knew), t64(j, knew), nb, 1, nb, 1, nb);
-        double* C = i == j ? t64(i, j) : ws64(par, i);
-        for (int bi = 0; bi < nb / 64; ++bi)
-          for (int bj = 0; bj < nb / 64; ++bj) {
-            if (i == j && bj > bi) continue;
-            js.push_back(job(C + (size_t)bi * 64 * nb + bj * 64, nb, 1, 64, 64, p, 1, -1.0, 1.0, bi * 64, bj * 64, nb));
-          }
-      }
-      P.dgemm(64, js, false);
+    new_dgemm(j, j + 1, nt, true);
+    if (V->amp && j + 1 < nt) {
+      TcParams t = tp;
+      t.mode = TC_UPD_NEW;
+      t.kbeg = knew >= 0 ? knew : 0;
+      t.kend = knew >= 0 ? j : 0;
+      t.row0 = j + 1;
+      t.nrows = nt - j - 1;
+      t.max_ctas = cap_mid;
+      P.ops.push_back([=](Exec& x) -> cr_status { return tc_launch(t, *tm, *tm, x.mid); });
     }
+    P.ops.push_back([=](Exec& x) -> cr_status { CR_CUDA(cudaEventRecord(x.ev_newr[j], x.mid)); return CR_OK; });
+
+    // ---------------- critical stream: NEW(j) for the diagonal tile, its factor and inverse
+    P.ops.push_back([=](Exec& x) -> cr_status { CR_CUDA(cudaStreamWaitEvent(x.hi, x.ev_old[j], 0)); return CR_OK; });
+    new_dgemm(j, j, j + 1, false);
     if (V->amp) {
       TcParams t = tp;
       t.mode = TC_UPD_NEW;
-      t.rows = nullptr;
       t.kbeg = knew >= 0 ? knew : 0;
       t.kend = knew >= 0 ? j : 0;
-      t.nrows = nt - j;
+      t.row0 = j;
+      t.nrows = 1;
       P.ops.push_back([=](Exec& x) -> cr_status { return tc_launch(t, *tm, *tm, x.hi); });
     }
-
-    // ---------------- diagonal factor and its inverse (FP64 dataflow executor)
     double* Ajj = t64(j, j);
-    double* Minv = V->minv;
-    double* T = V->scratch64;
+    double* Minv = V->minv + (size_t)par * nb2;
+    double* W = V->scratch64;
     {
       const int db = V->diag_db, ntask = V->diag_ntasks, g = j * nb;
       // one executor CTA per SM: the chain CTA plus one worker per remaining SM
@@ -211,7 +288,7 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
       const int4* tasks = V->diag_tasks;
       P.ops.push_back([=](Exec& x) -> cr_status {
         CR_CUDA(cudaMemsetAsync(Minv, 0, nb2 * sizeof(double), x.hi));
-        CR_TRY(diag_chol_launch(db, Ajj, Minv, T, nb, g, status, flags, tasks, ntask, dgrid, x.hi));
+        CR_TRY(diag_chol_launch(db, Ajj, Minv, W, nb, g, status, flags, tasks, ntask, dgrid, x.hi));
         k_zero_upper<<<64, 256, 0, x.hi>>>(Ajj, nb);
         CR_CHECK_LAUNCH("k_zero_upper");
         return CR_OK;
@@ -225,52 +302,35 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
       }
     }
     if (V->amp) {
-      __half* mh = V->pool16 + (size_t)V->minv_hi * nb2;
-      __half* ml = V->pool16 + (size_t)V->minv_lo * nb2;
+      __half* mh = V->pool16 + (size_t)(V->minv_hi + par) * nb2;
+      __half* ml = V->pool16 + (size_t)(V->minv_lo + par) * nb2;
       __half* dh = V->pool16 + (size_t)V->h_hi16[tidx(j, j)] * nb2;
       __half* dl = V->pool16 + (size_t)V->h_lo16[tidx(j, j)] * nb2;
       double* part = V->minv_part;
+      int* st_par = status + par;
       P.ops.push_back([=](Exec& x) -> cr_status {
-        CR_TRY(split_minv_launch(Minv, nb, mh, ml, status, part, x.hi));
+        CR_TRY(split_minv_launch(Minv, nb, mh, ml, st_par, part, x.hi));
         return split_tile_launch(Ajj, nb, dh, dl, 1, x.hi);
       });
     }
-
-    // ---------------- off-diagonal solves
-    const int ntc = rows_off[j + 1] - rows_off[j];
-    if (ntc > 0) {
-      TcParams t = tp;
-      t.mode = TC_TRSM;
-      t.rows = d_rows + rows_off[j];
-      t.nrows = ntc;
-      P.ops.push_back([=](Exec& x) -> cr_status { return tc_launch(t, *tm, *tm, x.hi); });
-    }
+    P.ops.push_back([=](Exec& x) -> cr_status { CR_CUDA(cudaEventRecord(x.ev_split[j], x.hi)); return CR_OK; });
+    // the solve of row j+1 (its update is on the lookahead stream) feeds the next column
+    P.ops.push_back([=](Exec& x) -> cr_status { CR_CUDA(cudaStreamWaitEvent(x.hi, x.ev_newr[j], 0)); return CR_OK; });
     {
-      std::vector<DJob> js;
-      std::vector<int> fp64_rows;
-      for (int i = j + 1; i < nt; ++i) {
-        if (cls[tidx(i, j)] != CR_PREC_FP64) continue;
-        fp64_rows.push_back(i);
-        const int p = P.add_pair(ws64(par, i), Minv, nb, 1, nb, 1, nb);
-        double* C = t64(i, j);
-        for (int bi = 0; bi < nb / 64; ++bi)
-          for (int bj = 0; bj < nb / 64; ++bj)
-            js.push_back(job(C + (size_t)bi * 64 * nb + bj * 64, nb, 1, 64, 64, p, 1, 1.0, 0.0, bi * 64, bj * 64, (bj + 1) * 64));
-      }
-      P.dgemm(64, js, false);
-      if (V->amp) {
-        for (int i : fp64_rows) {
-          const double* src = t64(i, j);
-          __half* h = V->pool16 + (size_t)V->h_hi16[tidx(i, j)] * nb2;
-          __half* l = V->pool16 + (size_t)V->h_lo16[tidx(i, j)] * nb2;
-          P.ops.push_back([=](Exec& x) -> cr_status { return split_tile_launch(src, nb, h, l, 0, x.hi); });
-        }
-      }
+      const int off = rows_off[j];
+      const int cnt = (rows_off[j + 1] > off && j + 1 < nt && rows_flat[off] == j + 1) ? 1 : 0;
+      solves(j, j + 1, std::min(nt, j + 2), tp, off, cnt, false, 0);
     }
-    P.ops.push_back([=](Exec& x) -> cr_status {
-      CR_CUDA(cudaEventRecord(x.ev[2 * j], x.hi));
-      return CR_OK;
-    });
+    P.ops.push_back([=](Exec& x) -> cr_status { CR_CUDA(cudaEventRecord(x.ev_crit[j], x.hi)); return CR_OK; });
+
+    // ---------------- lookahead stream, part 2: solves of rows j+2.. once the inverse is split
+    P.ops.push_back([=](Exec& x) -> cr_status { CR_CUDA(cudaStreamWaitEvent(x.mid, x.ev_split[j], 0)); return CR_OK; });
+    {
+      int off = rows_off[j];
+      if (rows_off[j + 1] > off && rows_flat[off] == j + 1) ++off;
+      solves(j, j + 2, nt, tp, off, rows_off[j + 1] - off, true, cap_mid);
+    }
+    P.ops.push_back([=](Exec& x) -> cr_status { CR_CUDA(cudaEventRecord(x.ev_rest[j], x.mid)); return CR_OK; });
   }
 
   // streams, events, job upload, replay
@@ -278,14 +338,18 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
     int lo_prio = 0, hi_prio = 0;
     CR_CUDA(cudaDeviceGetStreamPriorityRange(&lo_prio, &hi_prio));
     CR_CUDA(cudaStreamCreateWithPriority(&V->s_hi, cudaStreamNonBlocking, hi_prio));
+    CR_CUDA(cudaStreamCreateWithPriority(&V->s_mid, cudaStreamNonBlocking, hi_prio));
     CR_CUDA(cudaStreamCreateWithPriority(&V->s_lo, cudaStreamNonBlocking, lo_prio));
   }
   Exec x;
   x.hi = V->s_hi;
   x.lo = V->s_lo;
-  x.ev.resize(2 * nt);
+  x.mid = V->s_mid;
   cr_status st = CR_OK;
-  for (auto& e : x.ev) cudaEventCreateWithFlags(&e, cudaEventDisableTiming);
+  for (auto* evs : {&x.ev_old, &x.ev_split, &x.ev_newr, &x.ev_crit, &x.ev_rest}) {
+    evs->resize(nt);
+    for (auto& e : *evs) cudaEventCreateWithFlags(&e, cudaEventDisableTiming);
+  }
   cudaEventCreateWithFlags(&x.start, cudaEventDisableTiming);
   DJob* d_jobs = nullptr;
   DPair* d_pairs = nullptr;
@@ -305,13 +369,17 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
     cudaEventRecord(x.start, caller);
     cudaStreamWaitEvent(x.hi, x.start, 0);
     cudaStreamWaitEvent(x.lo, x.start, 0);
+    cudaStreamWaitEvent(x.mid, x.start, 0);
   }
   for (size_t q = 0; st == CR_OK && q < P.ops.size(); ++q) st = P.ops[q](x);
   cudaError_t e1 = cudaStreamSynchronize(x.hi);
   cudaError_t e2 = cudaStreamSynchronize(x.lo);
+  cudaError_t e3 = cudaStreamSynchronize(x.mid);
   if (st == CR_OK && e1 != cudaSuccess) st = cuda_fail(e1, "cholesky (critical stream)");
   if (st == CR_OK && e2 != cudaSuccess) st = cuda_fail(e2, "cholesky (bulk stream)");
-  for (auto& e : x.ev) cudaEventDestroy(e);
+  if (st == CR_OK && e3 != cudaSuccess) st = cuda_fail(e3, "cholesky (lookahead stream)");
+  for (auto* evs : {&x.ev_old, &x.ev_split, &x.ev_newr, &x.ev_crit, &x.ev_rest})
+    for (auto& e : *evs) cudaEventDestroy(e);
   cudaEventDestroy(x.start);
   if (d_jobs) cudaFree(d_jobs);
   if (d_pairs) cudaFree(d_pairs);

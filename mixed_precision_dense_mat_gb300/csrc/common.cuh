@@ -26,6 +26,16 @@ cr_status cuda_fail(cudaError_t e, const char* what);
 
 void count_launch();
 
+// Opt-in device timing of named kernels (cr_timing_enable): a scope object records an event
+// on the launch stream before and after the launch it brackets.
+struct TimedScope {
+  TimedScope(const char* name, cudaStream_t s);
+  ~TimedScope();
+  const char* name;
+  cudaStream_t stream;
+  cudaEvent_t start = nullptr;
+};
+
 // Every kernel launch is followed by this check, which also counts the launch.
 #define CR_CHECK_LAUNCH(what)                                       \
   do {                                                              \
@@ -101,8 +111,8 @@ struct cr_tilemat_s {
   __half* pool16 = nullptr;
   double* ws64 = nullptr;         // 2 * nt * nb * nb: FP64-class solve inputs (double-buffered by column parity)
   float* w32 = nullptr;           // 2 * nt * nb * nb: FP32 intermediate of FP16/FP32-class tiles (same)
-  cudaStream_t s_hi = nullptr, s_lo = nullptr;   // critical chain / bulk updates
-  double* minv = nullptr;         // nb * nb: inverse of the current diagonal factor
+  cudaStream_t s_hi = nullptr, s_lo = nullptr, s_mid = nullptr;   // critical chain / bulk updates / lookahead rows
+  double* minv = nullptr;         // 2 * nb * nb: inverse of the diagonal factor, by column parity
   double* minv_all = nullptr;     // nt * nb * nb: every diagonal factor's inverse (kept on request)
   double* scratch64 = nullptr;    // nb * nb: temporaries of the diagonal factorisation
   int* d_status = nullptr;        // [0] device error bits, [1] first failing column (1-based) or 0, [2] Minv exponent

@@ -77,6 +77,10 @@ __device__ __forceinline__ double cov_entry64(const CovK& p, const double* __res
   return cov_of_x(p, h * p.inv_range);
 }
 
+__device__ __noinline__ double cov_entry64_ool(const CovK& p, const double* __restrict__ xy, int gi, int gj) {
+  return cov_entry64(p, xy, gi, gj);
+}
+
 // Double-float entry for an off-diagonal pair with coordinate differences (dx, dy); sets
 // *fallback when the scaled distance leaves the double-float exponential's range.
 __device__ __forceinline__ df cov_entry_df(const CovK& p, df dx, df dy, df sig, df inv_range, const DfExpTables& T,
@@ -151,24 +155,27 @@ __global__ void __launch_bounds__(256) k_cov_stats(const double* __restrict__ xy
     const int gi = i * nb + r, gj = j * nb + c;
     if (gi >= n || gj >= n) continue;
     if (DF) {
-      df v;
       bool fb = gi == gj;
+      df v = {0.0f, 0.0f};
       if (!fb) {
         const float4 a = s_row[r - r0], b = s_col[c];
         const df dx = df_add({a.x, a.y}, df_neg({b.x, b.y}));
         const df dy = df_add({a.z, a.w}, df_neg({b.z, b.w}));
         v = cov_entry_df(p, dx, dy, sig, invr, s_T, &fb);
       }
-      if (fb) {   // diagonal entries and distances outside the double-float exponential: FP64
-        const double v64 = cov_entry64(p, xy, gi, gj);
+      if (__builtin_expect(fb, 0)) {
+        // diagonal entries and distances outside the double-float exponential: FP64, out of
+        // line, so that no FP64 instruction is predicated into the common path (GB300's FP64
+        // units run at 1/64 of the FP32 rate)
+        const double v64 = cov_entry64_ool(p, xy, gi, gj);
         ssq = df_add(ssq, df_from_double(v64 * v64));
         vmn = fmin(vmn, v64);
         vmx = fmax(vmx, v64);
-      } else {
-        ssq = df_add(ssq, df_mul(v, v));
-        if (df_lt(v, dmn)) dmn = v;
-        if (df_lt(dmx, v)) dmx = v;
+        continue;
       }
+      ssq = df_add(ssq, df_mul(v, v));
+      if (df_lt(v, dmn)) dmn = v;
+      if (df_lt(dmx, v)) dmx = v;
     } else {
       const double v64 = cov_entry64(p, xy, gi, gj);
       ssq64 += v64 * v64;
@@ -242,8 +249,8 @@ __global__ void __launch_bounds__(256) k_generate(const double* __restrict__ xy,
   __syncthreads();
   const size_t count = (size_t)nb * nb;
   if (use_df && cls == CR_PREC_FP16) {
-    // FP16 tiles (off-diagonal): a single-precision evaluation, a few ulp of FP32, is far
-    // inside the 2^-11 rounding of the stored value; distances from the double-float
+    // FP16 tiles (off-diagonal): a single-precision evaluation, accurate to a few 1e-6, is
+    // far inside the 2^-11 rounding of the stored value; distances from the double-float
     // coordinates, so that near points do not lose digits to cancellation
     __half* dst = v.pool16 + (size_t)v.hi16[t] * count;
     const float sig = p.sig_hi, invr = p.invr_hi, s2f = (float)s2;
@@ -255,7 +262,7 @@ __global__ void __launch_bounds__(256) k_generate(const double* __restrict__ xy,
         const float4 a = s_row[r - r0], b = s_col[c];
         const float dx = (a.x - b.x) + (a.y - b.y), dy = (a.z - b.z) + (a.w - b.w);
         const float x = sqrtf(fmaf(dx, dx, dy * dy)) * invr;
-        const float e = expf(-x);
+        const float e = __expf(-x);   // ex2-based: ~3e-6 relative at x < 50, against FP16's 4.9e-4
         const float poly = p.kind == 0 ? 1.0f : (p.kind == 1 ? 1.0f + x : fmaf(x * x, 1.0f / 3.0f, 1.0f + x));
         f = sig * poly * e * s2f;
       }
@@ -279,7 +286,7 @@ __global__ void __launch_bounds__(256) k_generate(const double* __restrict__ xy,
       const df dy = df_add({a.z, a.w}, df_neg({b.z, b.w}));
       bool fb = false;
       vd = cov_entry_df(p, dx, dy, sig, invr, s_T, &fb);
-      if (fb) v64 = cov_entry64(p, xy, gi, gj) * s2;
+      if (__builtin_expect(fb, 0)) v64 = cov_entry64_ool(p, xy, gi, gj) * s2;
       else { vd = df_mul(vd, s2d); have_df = true; }
     } else {
       v64 = cov_entry64(p, xy, gi, gj) * s2;
@@ -400,8 +407,11 @@ extern "C" cr_status cr_cov_build(cr_tilemat V, const double* d_xy, const cr_cov
   const int nrb = V->nb / 64;
   dim3 grid(V->ntiles, nrb);
   const size_t smem = (size_t)(V->nb + 64) * sizeof(float4);
-  if (k.use_df) k_cov_stats<true><<<grid, 256, smem, stream>>>(V->xy, V->n, V->nb, k, V->stat_part);
-  else k_cov_stats<false><<<grid, 256, smem, stream>>>(V->xy, V->n, V->nb, k, V->stat_part);
+  {
+    TimedScope ts("k_cov_stats", stream);
+    if (k.use_df) k_cov_stats<true><<<grid, 256, smem, stream>>>(V->xy, V->n, V->nb, k, V->stat_part);
+    else k_cov_stats<false><<<grid, 256, smem, stream>>>(V->xy, V->n, V->nb, k, V->stat_part);
+  }
   CR_CHECK_LAUNCH("k_cov_stats");
   k_stats_reduce<<<(V->ntiles + 127) / 128, 128, 0, stream>>>(V->stat_part, V->ntiles, nrb, V->stats);
   CR_CHECK_LAUNCH("k_stats_reduce");
@@ -439,7 +449,10 @@ cr_status convert_tiles(cr_tilemat V, cudaStream_t stream) {
   const size_t smem = (size_t)(V->nb + 64) * sizeof(float4);
   const double s2 = V->s * V->s;
   const df s2d = df_from_double(s2);
-  k_generate<<<grid, 256, smem, stream>>>(V->xy, V->n, V->nb, V->covk, s2, s2d.hi, s2d.lo, V->view());
+  {
+    TimedScope ts("k_generate", stream);
+    k_generate<<<grid, 256, smem, stream>>>(V->xy, V->n, V->nb, V->covk, s2, s2d.hi, s2d.lo, V->view());
+  }
   CR_CHECK_LAUNCH("k_generate");
   return CR_OK;
 }

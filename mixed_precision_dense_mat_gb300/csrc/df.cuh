@@ -82,8 +82,12 @@ struct DfExpTables {
 // exp(r) = 1 + r + r^2/2 + (r^3/6 + r^4/24 + r^5/120) with the bracket in FP32 (its
 // magnitude is below 3e-8, so its FP32 rounding stays near 1e-15 of the result).
 __device__ __forceinline__ df df_exp(df y, const DfExpTables& T) {
-  const float kf = rintf(__fmul_rn(y.hi, 92.33248261689366f));   // 64 / ln 2
-  const int k = (int)kf;
+  // k = round(y 64 / ln 2) by adding 1.5 2^23 (exact rounding to nearest for |v| < 2^22):
+  // FADD and integer work only, no conversion instruction
+  const float big = 12582912.0f;
+  const float kb = __fadd_rn(__fmul_rn(y.hi, 92.33248261689366f), big);   // 64 / ln 2
+  const float kf = __fsub_rn(kb, big);
+  const int k = __float_as_int(kb) - __float_as_int(big);
   const float t = __fmaf_rn(-kf, T.c1, y.hi);                     // exact (see above)
   df r = df_two_sum(t, y.lo);
   r = df_add(r, df_neg(df_two_prod(kf, T.c2)));

@@ -543,7 +543,10 @@ cr_status diag_chol_launch(int db, double* A, double* Minv, double* W, int nb, i
     CR_CUDA(cudaFuncSetAttribute(k_diag_chol, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared));
     configured = true;
   }
-  k_diag_chol<<<grid, 256, 0, s>>>(c, d_tasks, ntasks, counter, role);
+  {
+    TimedScope ts("k_diag_chol", s);
+    k_diag_chol<<<grid, 256, 0, s>>>(c, d_tasks, ntasks, counter, role);
+  }
   CR_CHECK_LAUNCH("k_diag_chol");
   return CR_OK;
 }

@@ -145,8 +145,8 @@ cr_status allocate_class_storage(cr_tilemat V) {
       if (V->h_cls[t] != CR_PREC_FP16) V->h_lo16[t] = V->n16++;
     V->ws_hi0 = V->n16; V->n16 += 2 * nt;   // two sets, by column parity
     V->ws_lo0 = V->n16; V->n16 += 2 * nt;
-    V->minv_hi = V->n16++;
-    V->minv_lo = V->n16++;
+    V->minv_hi = V->n16; V->n16 += 2;   // by column parity
+    V->minv_lo = V->n16; V->n16 += 2;
   }
   CR_TRY(upload(&V->d_cls, V->h_cls));
   CR_TRY(upload(&V->d_i64, V->h_i64));

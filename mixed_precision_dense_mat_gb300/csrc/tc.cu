@@ -40,7 +40,8 @@ __host__ __device__ inline int tc_num_blocks(const TcParams& p) {
   const int nb = p.v.nb, per = tc_nsbm(nb) * tc_nsbn(nb);
   if (p.mode == TC_TRMM) return p.v.nt * tc_nsbm(nb) * p.ncb;
   if (p.mode == TC_TRSM) return p.nrows * per;
-  return p.nrows > 0 ? tc_diag_blocks(nb) + (p.nrows - 1) * per : 0;
+  if (p.nrows <= 0) return 0;
+  return p.row0 == p.j ? tc_diag_blocks(nb) + (p.nrows - 1) * per : p.nrows * per;
 }
 
 __device__ __forceinline__ Job decode(const TcParams& p, int t) {
@@ -58,7 +59,7 @@ __device__ __forceinline__ Job decode(const TcParams& p, int t) {
     jb.rb = (t % per) / nsbn;
     jb.cb = (t % per) % nsbn;
   } else {
-    const int d = tc_diag_blocks(nb);
+    const int d = p.row0 == p.j ? tc_diag_blocks(nb) : 0;
     if (t < d) {
       // diagonal tile: the blocks of row rb that reach the lower triangle
       jb.i = p.j;
@@ -73,7 +74,7 @@ __device__ __forceinline__ Job decode(const TcParams& p, int t) {
       jb.cb = left;
     } else {
       const int per = nsbm * nsbn, u = t - d;
-      jb.i = p.j + 1 + u / per;
+      jb.i = p.row0 + (d > 0 ? 1 : 0) + u / per;
       jb.rb = (u % per) / nsbn;
       jb.cb = (u % per) % nsbn;
     }
@@ -570,8 +571,13 @@ cr_status tc_launch(const TcParams& p, const CUtensorMap& tmA, const CUtensorMap
   CR_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
   const size_t smem = TC_SMEM + 2 * (((size_t)TC_KT_INTS * sizeof(int) * p.v.nt + 15) & ~(size_t)15);
   if (smem > (size_t)kMaxSmem) return fail(CR_ERR_ARG, "tensor-core kernel: too many tiles per column for the k-term tables");
-  const int grid = nblocks < sms ? nblocks : sms;
-  k_tc<<<grid, TC_THREADS, smem, stream>>>(tmA, tmB, p, nblocks);
+  const int cap = (p.max_ctas > 0 && p.max_ctas < sms) ? p.max_ctas : sms;
+  const int grid = nblocks < cap ? nblocks : cap;
+  {
+    static const char* names[4] = {"k_tc_old", "k_tc_trsm", "k_tc_trmm", "k_tc_new"};
+    TimedScope ts(names[p.mode & 3], stream);
+    k_tc<<<grid, TC_THREADS, smem, stream>>>(tmA, tmB, p, nblocks);
+  }
   CR_CHECK_LAUNCH("k_tc");
   return CR_OK;
 }

@@ -26,8 +26,9 @@ struct TcParams {
   int j;              // tile column (update / triangular solve)
   int kbeg, kend;     // update terms
   float* w32;         // FP32 intermediate of FP16/FP32-class tiles (tile row i at i nb^2)
-  const int* rows;    // tile rows of this launch (triangular solve; updates: NULL = j, j+1, ...)
-  int nrows;          // number of tile rows (triangular solve; updates: rows j .. j+nrows-1)
+  const int* rows;    // tile rows of this launch (triangular solve)
+  int row0, nrows;    // updates: tile rows row0 .. row0+nrows-1 (row0 = j includes the diagonal tile);
+                      // triangular solve: nrows entries of rows
   int ws_hi0, ws_lo0, minv_hi, minv_lo;
   int eA;             // FP32-class inputs were scaled by 2^-eA
   const int* status;  // status[2]: exponent eM of the scaled inverse factor
@@ -35,6 +36,8 @@ struct TcParams {
   double* ws64;       // FP64-class triangular-solve inputs
   double* Y;          // simulation output (n x M column-major)
   int ldy, M, ncb, flags;
+  int max_ctas;       // grid cap (0: one CTA per SM); background launches leave SMs free for
+                      // the critical stream, whose CTAs cannot preempt persistent ones
 };
 
 // Launches the persistent kernel over every output block of the launch described by p (one
