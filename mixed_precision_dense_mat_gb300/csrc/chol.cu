@@ -278,6 +278,7 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
     }
     double* Ajj = t64(j, j);
     double* Minv = V->minv + (size_t)par * nb2;
+    unsigned long long* amax = reinterpret_cast<unsigned long long*>(V->minv_part);
     double* W = V->scratch64;
     {
       const int db = V->diag_db, ntask = V->diag_ntasks, g = j * nb;
@@ -288,7 +289,7 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
       const int4* tasks = V->diag_tasks;
       P.ops.push_back([=](Exec& x) -> cr_status {
         CR_CUDA(cudaMemsetAsync(Minv, 0, nb2 * sizeof(double), x.hi));
-        CR_TRY(diag_chol_launch(db, Ajj, Minv, W, nb, g, status, flags, tasks, ntask, dgrid, x.hi));
+        CR_TRY(diag_chol_launch(db, Ajj, Minv, W, nb, g, status, flags, tasks, ntask, dgrid, amax, x.hi));
         k_zero_upper<<<64, 256, 0, x.hi>>>(Ajj, nb);
         CR_CHECK_LAUNCH("k_zero_upper");
         return CR_OK;
@@ -306,12 +307,8 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
       __half* ml = V->pool16 + (size_t)(V->minv_lo + par) * nb2;
       __half* dh = V->pool16 + (size_t)V->h_hi16[tidx(j, j)] * nb2;
       __half* dl = V->pool16 + (size_t)V->h_lo16[tidx(j, j)] * nb2;
-      double* part = V->minv_part;
       int* st_par = status + par;
-      P.ops.push_back([=](Exec& x) -> cr_status {
-        CR_TRY(split_minv_launch(Minv, nb, mh, ml, st_par, part, x.hi));
-        return split_tile_launch(Ajj, nb, dh, dl, 1, x.hi);
-      });
+      P.ops.push_back([=](Exec& x) -> cr_status { return split_diag_launch(Minv, Ajj, nb, amax, mh, ml, dh, dl, st_par, x.hi); });
     }
     P.ops.push_back([=](Exec& x) -> cr_status { CR_CUDA(cudaEventRecord(x.ev_split[j], x.hi)); return CR_OK; });
     // the solve of row j+1 (its update is on the lookahead stream) feeds the next column

@@ -63,7 +63,19 @@ struct Ctx {
   int* abort_flag;
   int* status;
   int gcol0;
+  unsigned long long* amax;   // IEEE bits of max |M| over the inverse (non-negative doubles order as unsigned)
 };
+
+// Folds the calling warp's |x| into the inverse's running maximum (one atomic per warp).
+__device__ __forceinline__ void fold_amax(const Ctx& c, double x) {
+  unsigned long long b = (unsigned long long)__double_as_longlong(x) & 0x7fffffffffffffffull;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long y = __shfl_xor_sync(0xffffffffu, b, o);
+    b = y > b ? y : b;
+  }
+  if ((threadIdx.x & 31) == 0) atomicMax(c.amax, b);
+}
 
 // Thread 0 waits until *p >= v; false on timeout (sets the abort flag and the error bit).
 __device__ bool wait_ge(const Ctx& c, const int* p, int v) {
@@ -277,6 +289,7 @@ __device__ void potrf16(const Ctx& c, int k, const Blk* P, Blk* A16, Blk* X, FFS
     const int i = t / DB, j = t % DB;
     m[(size_t)i * c.nb + j] = X[i][j];
     if (j <= i) a[(size_t)i * c.nb + j] = sh.l16[i][j];
+    fold_amax(c, X[i][j]);
   }
 }
 
@@ -428,7 +441,9 @@ __global__ void __launch_bounds__(256) k_diag_chol(Ctx c, const int4* __restrict
         load_block(S0, c.Minv + R * rowstride + R * DB, c.nb);
         load_block_t(S1, c.W + R * rowstride + C * DB, c.nb);
         __syncthreads();
-        c.Minv[R * rowstride + C * DB + (size_t)r * c.nb + col] = -gemm_elem(S0, S1);
+        const double mv = -gemm_elem(S0, S1);
+        c.Minv[R * rowstride + C * DB + (size_t)r * c.nb + col] = mv;
+        fold_amax(c, mv);
       }
     }
     __syncthreads();
@@ -525,7 +540,7 @@ bool diag_task_list(int NB, std::vector<int4>& tasks) {
 }
 
 cr_status diag_chol_launch(int db, double* A, double* Minv, double* W, int nb, int gcol0, int* status, int* flags,
-                           const int4* d_tasks, int ntasks, int grid, cudaStream_t s) {
+                           const int4* d_tasks, int ntasks, int grid, unsigned long long* amax, cudaStream_t s) {
   if (db != DB || nb % DB != 0 || grid < 2) return fail(CR_ERR_ARG, "diag_chol_launch: block size 16 dividing nb and at least 2 CTAs");
   const int NB = nb / db;
   Ctx c;
@@ -534,8 +549,9 @@ cr_status diag_chol_launch(int db, double* A, double* Minv, double* W, int nb, i
   c.abort_flag = flags + 4 * NB * NB;
   int* counter = flags + 4 * NB * NB + 1;
   int* role = flags + 4 * NB * NB + 2;
-  c.status = status; c.gcol0 = gcol0;
+  c.status = status; c.gcol0 = gcol0; c.amax = amax;
   CR_CUDA(cudaMemsetAsync(flags, 0, diag_flag_words(nb, db) * sizeof(int), s));
+  CR_CUDA(cudaMemsetAsync(amax, 0, sizeof(unsigned long long), s));
   static bool configured = false;
   if (!configured) {
     // same shared-memory carveout as the tensor-core kernel, so these small CTAs can share

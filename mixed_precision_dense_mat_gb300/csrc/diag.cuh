@@ -20,7 +20,8 @@ bool diag_task_list(int NB, std::vector<int4>& tasks);
 // A (nb x nb row-major, ld nb): lower part overwritten by L; Minv (same layout) receives
 // L^-1 (lower; the caller zeroes it beforehand); W: nb x nb FP64 scratch.  flags:
 // diag_flag_words(nb, db) ints of device scratch, cleared by this call.
+// amax: device word that receives the IEEE bits of max |L^-1| (cleared by this call).
 cr_status diag_chol_launch(int db, double* A, double* Minv, double* W, int nb, int gcol0, int* status, int* flags,
-                           const int4* d_tasks, int ntasks, int grid, cudaStream_t s);
+                           const int4* d_tasks, int ntasks, int grid, unsigned long long* amax, cudaStream_t s);
 
 }  // namespace cr

@@ -144,47 +144,41 @@ __global__ void __launch_bounds__(256) k_split_tile(const double* __restrict__ s
   }
 }
 
-constexpr int SPLIT_PARTS = 64;
-
-// Partial maxima of |M| over SPLIT_PARTS CTAs.
-__global__ void __launch_bounds__(256) k_absmax_part(const double* __restrict__ M, size_t count, double* __restrict__ part) {
-  __shared__ double red[8];
-  double mx = 0.0;
-  for (size_t idx = blockIdx.x * 256 + threadIdx.x; idx < count; idx += (size_t)gridDim.x * 256) mx = fmax(mx, fabs(M[idx]));
-  for (int o = 16; o > 0; o >>= 1) mx = fmax(mx, __shfl_down_sync(0xffffffffu, mx, o));
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    double m = 0.0;
-    for (int q = 0; q < 8; ++q) m = fmax(m, red[q]);
-    part[blockIdx.x] = m;
-  }
-}
-
-// Splits the inverse factor: eM with max|M| 2^eM < 2^14 (status[2] = eM) and the FP16 high/low
-// parts of M 2^eM.  Every CTA combines the partial maxima itself.
-__global__ void __launch_bounds__(256) k_split_minv(const double* __restrict__ Minv, size_t count, const double* __restrict__ part,
-                                                    __half* __restrict__ hi, __half* __restrict__ lo, int* status) {
-  __shared__ int s_e;
-  if (threadIdx.x == 0) {
-    double m = 0.0;
-    for (int q = 0; q < SPLIT_PARTS; ++q) m = fmax(m, part[q]);
-    int e = 0;
-    if (m > 0.0 && isfinite(m)) {
-      int ex;
-      frexp(m, &ex);          // m < 2^ex
-      e = 14 - ex;            // m 2^e < 2^14
+// Splits the inverse factor and the diagonal factor of one column in one launch:
+//  - eM with max|M| 2^eM < 2^14 (status[2] = eM), from the running maximum the diagonal
+//    executor accumulated (IEEE bits of max |M|), and the FP16 high/low parts of M 2^eM;
+//  - the FP16 high/low parts of the diagonal factor L (lower part; zero above).
+// Elements [0, nb^2) are M, [nb^2, 2 nb^2) are L; both through FP32, whose 24 bits cover
+// everything an FP16 pair can hold.
+__global__ void __launch_bounds__(256) k_split_diag(const double* __restrict__ Minv, const double* __restrict__ L, int nb,
+                                                    const unsigned long long* __restrict__ amax, __half* __restrict__ mh,
+                                                    __half* __restrict__ ml, __half* __restrict__ lh, __half* __restrict__ ll,
+                                                    int* status) {
+  const unsigned long long bits = *amax;
+  const int ef = (int)((bits >> 52) & 0x7ff);   // max |M| in [2^(ef-1023), 2^(ef-1022))
+  const int e = (bits == 0 || ef == 0 || ef == 0x7ff) ? 0 : 14 - (ef - 1022);
+  if (blockIdx.x == 0 && threadIdx.x == 0) status[2] = e;
+  const float sc = ldexpf(1.0f, e);
+  const size_t count = (size_t)nb * nb;
+  for (size_t idx = blockIdx.x * 256 + threadIdx.x; idx < 2 * count; idx += (size_t)gridDim.x * 256) {
+    float x;
+    __half *h, *l;
+    size_t o;
+    if (idx < count) {
+      o = idx;
+      x = (float)Minv[o] * sc;
+      h = mh;
+      l = ml;
+    } else {
+      o = idx - count;
+      const int r = (int)(o / nb), c = (int)(o % nb);
+      x = c > r ? 0.0f : (float)L[o];
+      h = lh;
+      l = ll;
     }
-    s_e = e;
-    if (blockIdx.x == 0) status[2] = e;
-  }
-  __syncthreads();
-  const float sc = ldexpf(1.0f, s_e);
-  for (size_t idx = blockIdx.x * 256 + threadIdx.x; idx < count; idx += (size_t)gridDim.x * 256) {
-    const float x = (float)Minv[idx] * sc;
-    const __half h = __float2half_rn(x);
-    hi[idx] = h;
-    lo[idx] = __float2half_rn(x - __half2float(h));
+    const __half hv = __float2half_rn(x);
+    h[o] = hv;
+    l[o] = __float2half_rn(x - __half2float(hv));
   }
 }
 
@@ -205,12 +199,10 @@ cr_status split_tile_launch(const double* src, int nb, __half* hi, __half* lo, i
   CR_CHECK_LAUNCH("k_split_tile");
   return CR_OK;
 }
-cr_status split_minv_launch(const double* Minv, int nb, __half* hi, __half* lo, int* status, double* part, cudaStream_t s) {
-  const size_t count = (size_t)nb * nb;
-  k_absmax_part<<<SPLIT_PARTS, 256, 0, s>>>(Minv, count, part);
-  CR_CHECK_LAUNCH("k_absmax_part");
-  k_split_minv<<<128, 256, 0, s>>>(Minv, count, part, hi, lo, status);
-  CR_CHECK_LAUNCH("k_split_minv");
+cr_status split_diag_launch(const double* Minv, const double* L, int nb, const unsigned long long* amax, __half* mh, __half* ml,
+                            __half* lh, __half* ll, int* status, cudaStream_t s) {
+  k_split_diag<<<256, 256, 0, s>>>(Minv, L, nb, amax, mh, ml, lh, ll, status);
+  CR_CHECK_LAUNCH("k_split_diag");
   return CR_OK;
 }
 cr_status status_init_launch(int* status, cudaStream_t s) {

@@ -26,7 +26,10 @@ cr_status dgemm_launch(int block, const DJob* d_jobs, const DPair* d_pairs, int 
 cr_status potrf64_base_launch(double* A, int lda, double* Minv, int ldm, int gcol0, int* status, cudaStream_t s);
 cr_status split_tile_launch(const double* src, int nb, __half* hi, __half* lo, int lower_only, cudaStream_t s);
 // part: 64 doubles of device scratch
-cr_status split_minv_launch(const double* Minv, int nb, __half* hi, __half* lo, int* status, double* part, cudaStream_t s);
+// FP16 high/low splits of the inverse factor (scaled by 2^eM, status[2] = eM, from the maximum
+// in *amax) and of the diagonal factor's lower part, in one launch.
+cr_status split_diag_launch(const double* Minv, const double* L, int nb, const unsigned long long* amax, __half* mh, __half* ml,
+                            __half* lh, __half* ll, int* status, cudaStream_t s);
 cr_status status_init_launch(int* status, cudaStream_t s);
 
 }  // namespace cr
