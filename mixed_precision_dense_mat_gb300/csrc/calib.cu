@@ -44,9 +44,6 @@ __device__ __forceinline__ double dkey_inv(unsigned long long k) {
   const unsigned long long b = (k >> 63) ? (k & 0x7fffffffffffffffull) : ~k;
   return __longlong_as_double((long long)b);
 }
-__device__ __forceinline__ bool dnan(double x) {
-  return ((unsigned long long)__double_as_longlong(x) & 0x7fffffffffffffffull) > 0x7ff0000000000000ull;
-}
 
 __global__ void __launch_bounds__(SCAN_THREADS) k_scan(const double* __restrict__ S, int lds, int n_p, int M,
                                                        const double* __restrict__ t, double u, double* __restrict__ psi_part,
@@ -86,8 +83,10 @@ __global__ void __launch_bounds__(SCAN_THREADS) k_scan(const double* __restrict_
     unsigned long long mn = KEY_PINF, mx = KEY_MINF;
 #pragma unroll
     for (int q = 0; q < RPT; ++q) {
-      const bool ok = !dnan(val[q]);
       const unsigned long long kv = dkey(val[q]);
+      // NaN keys lie outside [key(-inf), key(+inf)]; a test on the double itself is compiled
+      // to an FP64 instruction, which on GB300 would bound the scan
+      const bool ok = kv >= KEY_MINF && kv <= KEY_PINF;
       const bool ge = ok && kv >= ku, le = ok && kv <= ku;
       if (ge && tk[q] < mn) mn = tk[q];
       if (le && tk[q] > mx) mx = tk[q];
