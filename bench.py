@@ -37,7 +37,11 @@ import inputgen  # noqa: E402
 FP64_PEAK_TFLOPS = 1.19       # measured DFMA rate on GB300 (profiles/fp64_peak_microbench.md)
 # DRAM bytes per launch from one ncu capture of the kernel as it stands (profiles/); None once
 # the kernel has changed since the capture
-NCU_TRAFFIC_PER_LAUNCH = {"k_diag_chol": None, "k_tc_old": None, "k_tc_trmm": None}
+NCU_TRAFFIC_PER_LAUNCH = {
+    "k_diag_chol": 1372672 + 9472,   # profiles/k_diag_chol_n8192.md (one 512 tile per launch at any n)
+    "k_tc_trmm": None,               # profiles/k_tc_trmm_n8192.md covers n = 8192 only (not proportional in n)
+    "k_scan": None,
+}
 TIMED_KERNELS = ["k_diag_chol", "k_tc_old", "k_tc_new", "k_tc_trsm", "k_tc_trmm", "k_cov_stats", "k_generate", "k_scan"]
 WORKLOAD = inputgen.WORKLOADS["c"]
 SEED_Z = 12345
