@@ -77,18 +77,53 @@ __device__ __forceinline__ void fold_amax(const Ctx& c, double x) {
   if ((threadIdx.x & 31) == 0) atomicMax(c.amax, b);
 }
 
-// Thread 0 waits until *p >= v; false on timeout (sets the abort flag and the error bit).
-__device__ bool wait_ge(const Ctx& c, const int* p, int v) {
-  if (ld_acquire(p) >= v) return true;
+// Lane `lane` of the polling warp gets the flag (p, v) it waits on for task tk (p = nullptr:
+// nothing); lanes 0-2 cover every task type.
+__device__ __forceinline__ void task_flag(const Ctx& c, int4 tk, int lane, const int*& p, int& v) {
+  const int NB = c.NB;
+  p = nullptr;
+  v = 1;
+  if (tk.x == T_TRSM) {
+    const int i = tk.y, k = tk.w;
+    if (lane == 0) p = &c.fac[k * NB + k];
+    else if (lane == 1) { p = &c.ver[i * NB + k]; v = k; }
+  } else if (tk.x == T_UPDATE) {
+    const int i = tk.y, j = tk.z, k = tk.w;
+    if (lane == 0) p = &c.fac[i * NB + k];
+    else if (lane == 1) p = &c.fac[j * NB + k];
+    else if (lane == 2) { p = &c.ver[i * NB + j]; v = k; }
+  } else if (tk.x == T_IUPD) {
+    const int R = tk.y, C = tk.z, m = tk.w;
+    if (lane == 0) p = &c.fac[R * NB + m];
+    else if (lane == 1) p = m == C ? &c.fac[C * NB + C] : &c.inv[m * NB + C];
+    else if (lane == 2) { p = &c.iver[R * NB + C]; v = m - C; }
+  } else {
+    const int R = tk.y, C = tk.z;
+    if (lane == 0) p = &c.fac[R * NB + R];
+    else if (lane == 1) { p = &c.iver[R * NB + C]; v = R - C; }
+  }
+}
+
+// All 32 lanes of a warp: waits until *p >= v for every lane with p != nullptr (the lanes
+// poll side by side).  False when the kernel's abort flag is set, or after 2 s, which sets
+// the abort flag and the timeout error bit.
+__device__ bool warp_wait_ge(const Ctx& c, const int* p, int v) {
+  bool done = p == nullptr || ld_acquire(p) >= v;
+  if (__all_sync(0xffffffffu, done)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
-    if (ld_acquire(p) >= v) return true;
-    if (ld_acquire(c.abort_flag)) return false;
-    if (global_timer_ns() - t0 > 2000000000ull) {
-      atomicOr(&c.status[0], DEV_ERR_TIMEOUT);
-      atomicExch(c.abort_flag, 1);
-      return false;
+    if (!done) done = ld_acquire(p) >= v;
+    if (__all_sync(0xffffffffu, done)) return true;
+    int stop = 0;
+    if ((threadIdx.x & 31) == 0) {
+      stop = ld_acquire(c.abort_flag);
+      if (!stop && global_timer_ns() - t0 > 2000000000ull) {
+        atomicOr(&c.status[0], DEV_ERR_TIMEOUT);
+        atomicExch(c.abort_flag, 1);
+        stop = 1;
+      }
     }
+    if (__shfl_sync(0xffffffffu, stop, 0)) return false;
   }
 }
 
@@ -148,7 +183,6 @@ __device__ __forceinline__ bool positive(double x) {
 // strict lower triangle of the transformed identity.  N = 16 uses the whole CTA and
 // __syncthreads; N = 8 would use warps 0-1 and named barrier 1 (measured on GB300: splitting
 // a 16 x 16 block into 8 x 8 halves is slower than eliminating it whole).
-constexpr int H = DB / 2;
 template <int N>
 struct FFS {
   double col[2][N];   // column c of the working matrix, double-buffered by step parity
@@ -249,10 +283,20 @@ struct FFShared {
   FFS<DB> f;
 };
 
+// Lower element t (row by row, t < 136) of diagonal block k, 0 for the other threads.
+__device__ __forceinline__ double diag_elem(const Ctx& c, int k) {
+  const int t = threadIdx.x;
+  if (t >= NT_LOWER) return 0.0;
+  const int i = tri_row(t);
+  const int j = t - i * (i + 1) / 2;
+  return __ldcg(c.A + (size_t)(k * DB + i) * c.nb + k * DB + j);
+}
+
 // Cholesky factor and inverse of diagonal block k, after subtracting P P^T when P is given
-// (the last symmetric update of the block, fused).  A16 is shared-memory scratch; the factor
-// (lower part) is written to the tile, the inverse (upper part zero) to Minv and to X.
-__device__ void potrf16(const Ctx& c, int k, const Blk* P, Blk* A16, Blk* X, FFShared& sh) {
+// (the last symmetric update of the block, fused).  v: the block's element from diag_elem,
+// read by the caller ahead of time.  A16 is shared-memory scratch; the factor (lower part)
+// is written to the tile, the inverse (upper part zero) to Minv and to X.
+__device__ void potrf16(const Ctx& c, int k, double v, const Blk* P, Blk* A16, Blk* X, FFShared& sh) {
   const int t = threadIdx.x;
   double* a = c.A + (size_t)(k * DB) * c.nb + k * DB;
   if (P) {
@@ -278,7 +322,6 @@ __device__ void potrf16(const Ctx& c, int k, const Blk* P, Blk* A16, Blk* X, FFS
   if (t < NT_LOWER) {
     const int i = tri_row(t);
     const int j = t - i * (i + 1) / 2;
-    double v = __ldcg(a + (size_t)i * c.nb + j);
     if (P) v -= sh.part[0][t] + sh.part[1][t];
     A16[i][j] = v;
   }
@@ -331,30 +374,34 @@ __device__ __forceinline__ double gemm_elem(const Blk* P, const Blk* Q) {
 __device__ void run_chain(const Ctx& c, Blk* S0, Blk* S1, Blk* S2, Blk* S3, FFShared& sh, int* s_ok) {
   const int NB = c.NB;
   const size_t rowstride = (size_t)DB * c.nb;
-  potrf16(c, 0, nullptr, S0, S1, sh);   // S1 = M_00
+  potrf16(c, 0, diag_elem(c, 0), nullptr, S0, S1, sh);   // S1 = M_00
   __syncthreads();
   if (threadIdx.x == 0) st_release(&c.fac[0], 1);
   int r, cc;
   trsm_owner(r, cc);
   for (int k = 0; k + 1 < NB; ++k) {
     const int i = k + 1;
-    // TRSM(i, k): L_ik = A_ik M_kk^T, M_kk in S1
-    if (threadIdx.x == 0) *s_ok = wait_ge(c, &c.ver[i * NB + k], k) ? 1 : 0;
+    // the inputs of TRSM(i, k) and of the fused UPDATE(i, i, k) are waited for and read
+    // together: the updates of step k - 1 that complete them are adjacent in the list
+    if (threadIdx.x < 32) {
+      const int lane = threadIdx.x;
+      const bool ok = warp_wait_ge(c, lane < 2 ? &c.ver[i * NB + (lane ? i : k)] : nullptr, k);
+      if (lane == 0) *s_ok = ok ? 1 : 0;
+    }
     __syncthreads();
     if (!*s_ok) return;
     double* aik = c.A + i * rowstride + k * DB;
+    const double vii = diag_elem(c, i);
     load_block(S2, aik, c.nb);
     __syncthreads();
+    // TRSM(i, k): L_ik = A_ik M_kk^T, M_kk in S1
     const double l = trsm_elem(S2, S1, r, cc);
     S3[r][cc] = l;                     // S3 = L_ik
     aik[(size_t)r * c.nb + cc] = l;
     __syncthreads();
     if (threadIdx.x == 0) st_release(&c.fac[i * NB + k], 1);
     // UPDATE(i, i, k) fused into POTRF(i)
-    if (threadIdx.x == 0) *s_ok = wait_ge(c, &c.ver[i * NB + i], k) ? 1 : 0;
-    __syncthreads();
-    if (!*s_ok) return;
-    potrf16(c, i, S3, S0, S1, sh);        // S1 = M_ii
+    potrf16(c, i, vii, S3, S0, S1, sh);   // S1 = M_ii
     __syncthreads();
     if (threadIdx.x == 0) st_release(&c.fac[i * NB + i], 1);
   }
@@ -368,6 +415,7 @@ __global__ void __launch_bounds__(256) k_diag_chol(Ctx c, const int4* __restrict
   __shared__ FFShared sh;
   __shared__ int s_task;
   __shared__ int s_ok;
+  __shared__ int4 s_tk;
   const int NB = c.NB;
   const size_t rowstride = (size_t)DB * c.nb;
   // the first CTA to start takes the critical chain: it is resident, so the chain progresses
@@ -377,34 +425,41 @@ __global__ void __launch_bounds__(256) k_diag_chol(Ctx c, const int4* __restrict
     run_chain(c, S0, S1, S2, S3, sh, &s_ok);
     return;
   }
+  // Warp 1 runs the queue: lane 0 claims task indices one ahead (the claim's round trip
+  // overlaps the current task) and lanes 0-2 poll the current task's flags side by side
+  // while warp 0 releases the previous task's flag.  A claimed task waits only behind the
+  // task its CTA is running, which is earlier in the list, so the progress argument above
+  // still holds.
+  const int lane = threadIdx.x & 31;
+  int claim = 0;
+  if (threadIdx.x == 32) claim = atomicAdd(counter, 1);
   while (true) {
-    if (threadIdx.x == 0) s_task = atomicAdd(counter, 1);
-    __syncthreads();
-    const int t = s_task;
-    if (t >= ntasks) break;
-    const int4 tk = tasks[t];
-    const int type = tk.x;
-    if (threadIdx.x == 0) {
-      bool ok = true;
-      if (type == T_TRSM) {
-        const int i = tk.y, k = tk.w;
-        ok = wait_ge(c, &c.fac[k * NB + k], 1) && wait_ge(c, &c.ver[i * NB + k], k);
-      } else if (type == T_UPDATE) {
-        const int i = tk.y, j = tk.z, k = tk.w;
-        ok = wait_ge(c, &c.fac[i * NB + k], 1) && wait_ge(c, &c.fac[j * NB + k], 1) && wait_ge(c, &c.ver[i * NB + j], k);
-      } else if (type == T_IUPD) {
-        const int R = tk.y, C = tk.z, m = tk.w;
-        ok = wait_ge(c, &c.fac[R * NB + m], 1) &&
-             (m == C ? wait_ge(c, &c.fac[C * NB + C], 1) : wait_ge(c, &c.inv[m * NB + C], 1)) &&
-             wait_ge(c, &c.iver[R * NB + C], m - C);
-      } else {
-        const int R = tk.y, C = tk.z;
-        ok = wait_ge(c, &c.fac[R * NB + R], 1) && wait_ge(c, &c.iver[R * NB + C], R - C);
+    if (threadIdx.x >= 32 && threadIdx.x < 64) {
+      int t = 0;
+      if (lane == 0) {
+        t = claim;
+        if (t < ntasks) claim = atomicAdd(counter, 1);
       }
-      s_ok = ok ? 1 : 0;
+      t = __shfl_sync(0xffffffffu, t, 0);
+      bool ok = true;
+      if (t < ntasks) {
+        const int4 tk = tasks[t];
+        const int* fp = nullptr;
+        int fv = 0;
+        task_flag(c, tk, lane, fp, fv);
+        ok = warp_wait_ge(c, fp, fv);
+        if (lane == 0) s_tk = tk;
+      }
+      if (lane == 0) {
+        s_task = t;
+        s_ok = ok ? 1 : 0;
+      }
     }
     __syncthreads();
-    if (!s_ok) break;
+    const int t = s_task;
+    if (t >= ntasks || !s_ok) break;
+    const int4 tk = s_tk;
+    const int type = tk.x;
     if (type == T_TRSM) {
       const int i = tk.y, k = tk.w;
       double* a = c.A + i * rowstride + k * DB;
@@ -418,23 +473,25 @@ __global__ void __launch_bounds__(256) k_diag_chol(Ctx c, const int4* __restrict
       const int r = threadIdx.x / DB, col = threadIdx.x % DB;
       if (type == T_UPDATE) {
         const int i = tk.y, j = tk.z, k = tk.w;
+        double* o = c.A + i * rowstride + j * DB + (size_t)r * c.nb + col;
+        const bool live = !(i == j && col > r);
+        // the destination is read with the operands: only this task writes it until its flag
+        const double d = live ? __ldcg(o) : 0.0;
         load_block(S0, c.A + i * rowstride + k * DB, c.nb);
         load_block(S1, c.A + j * rowstride + k * DB, c.nb);
         __syncthreads();
         const double p = gemm_elem(S0, S1);
-        if (!(i == j && col > r)) {
-          double* o = c.A + i * rowstride + j * DB + (size_t)r * c.nb + col;
-          *o = __ldcg(o) - p;
-        }
+        if (live) *o = d - p;
       } else if (type == T_IUPD) {
         // W_RC (+)= L_Rm M_mC
         const int R = tk.y, C = tk.z, m = tk.w;
+        double* o = c.W + R * rowstride + C * DB + (size_t)r * c.nb + col;
+        const double d = (m == C) ? 0.0 : __ldcg(o);
         load_block(S0, c.A + R * rowstride + m * DB, c.nb);
         load_block_t(S1, c.Minv + m * rowstride + C * DB, c.nb);
         __syncthreads();
         const double p = gemm_elem(S0, S1);
-        double* o = c.W + R * rowstride + C * DB + (size_t)r * c.nb + col;
-        *o = (m == C) ? p : __ldcg(o) + p;
+        *o = (m == C) ? p : d + p;
       } else {
         // M_RC = -M_RR W_RC
         const int R = tk.y, C = tk.z;
