@@ -10,11 +10,13 @@
 //    q_out = Q_alpha(psi), q_in = Q_{1-alpha}(phi), alpha = 1 - level.
 //  - Alg.2 step 22: C_in = {t_i > q_in}, C_out = {t_i >= q_out}.
 // The scan streams S once from HBM: each CTA owns a 2048-row x 32-column block, keeps its
-// rows' t and counts in registers, reduces each column with warp shuffles and writes one
-// partial per column; a second kernel combines the partials in a fixed order (deterministic).
+// rows' counts in registers and their t keys ranked per thread in shared memory, reduces each
+// column with warp shuffles and writes one partial per column; a second kernel combines the
+// partials in a fixed order (deterministic).
 #include <math.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "calib.cuh"
@@ -45,53 +47,99 @@ __device__ __forceinline__ double dkey_inv(unsigned long long k) {
   return __longlong_as_double((long long)b);
 }
 
+// High 32 bits of dkey(x), except that -0 keeps its own key (0x7fffffff): monotone in x, and
+// strictly ordered whenever the high words of two keys differ.
+__device__ __forceinline__ unsigned dkey_hi(double x) {
+  const unsigned hi = (unsigned)__double2hiint(x);
+  return hi ^ ((unsigned)((int)hi >> 31) | 0x80000000u);
+}
+
 __global__ void __launch_bounds__(SCAN_THREADS) k_scan(const double* __restrict__ S, int lds, int n_p, int M,
                                                        const double* __restrict__ t, double u, double* __restrict__ psi_part,
                                                        double* __restrict__ phi_part, int32_t* __restrict__ count) {
   constexpr int RPT = SCAN_ROWS / SCAN_THREADS;   // rows per thread
   constexpr unsigned long long KEY_PINF = 0xfff0000000000000ull, KEY_MINF = 0x000fffffffffffffull;
+  constexpr unsigned KH_PINF = 0xfff00000u, KH_MINF = 0x000fffffu;   // high words of +-inf (and of some NaNs)
   const int rb = blockIdx.x, cbk = blockIdx.y;
   const int row0 = rb * SCAN_ROWS + threadIdx.x;
   const unsigned long long ku = dkey(u);
-  unsigned long long tk[RPT];
+  const unsigned khu = dkey_hi(u);
+  // The thread's t keys, ranked among its own RPT rows (ties by row): a column's minimum over
+  // the qualifying rows is the lowest set bit of a mask in rank order, read back from shared
+  // memory once per column instead of a 64-bit compare-select per element.
+  __shared__ unsigned long long s_key[RPT][SCAN_THREADS];
+  unsigned bit[RPT];
   int cnt[RPT];
+  {
+    unsigned long long tk[RPT];
 #pragma unroll
-  for (int q = 0; q < RPT; ++q) {
-    const int r = row0 + q * SCAN_THREADS;
-    tk[q] = r < n_p ? dkey(t[r]) : 0ull;
-    cnt[q] = 0;
+    for (int q = 0; q < RPT; ++q) {
+      const int r = row0 + q * SCAN_THREADS;
+      tk[q] = r < n_p ? dkey(t[r]) : 0ull;
+      cnt[q] = 0;
+    }
+#pragma unroll
+    for (int q = 0; q < RPT; ++q) {
+      int rank = 0;
+#pragma unroll
+      for (int p = 0; p < RPT; ++p) rank += (tk[p] < tk[q] || (tk[p] == tk[q] && p < q)) ? 1 : 0;
+      bit[q] = 1u << rank;
+      s_key[rank][threadIdx.x] = tk[q];
+    }
   }
   __shared__ unsigned long long s_mn[SCAN_THREADS / 32][SCAN_COLS];
   __shared__ unsigned long long s_mx[SCAN_THREADS / 32][SCAN_COLS];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int c_end = min(SCAN_COLS, M - cbk * SCAN_COLS);
+  // this CTA's columns: a balanced share of the M columns (the grid is sized to the resident
+  // CTAs, so no partial last wave), flushed in chunks of SCAN_COLS
+  const int c_beg = (int)((long long)M * cbk / gridDim.y);
+  const int c_end = (int)((long long)M * (cbk + 1) / gridDim.y);
   double nxt[RPT];
   auto load_col = [&](int c, double* dst) {
-    const double* col = S + (size_t)(cbk * SCAN_COLS + c) * lds;
+    const double* col = S + (size_t)c * lds;
 #pragma unroll
     for (int q = 0; q < RPT; ++q) {
       const int r = row0 + q * SCAN_THREADS;
       dst[q] = r < n_p ? __ldcs(col + r) : __longlong_as_double(0x7ff8000000000000ll);   // NaN: no row
     }
   };
-  if (c_end > 0) load_col(0, nxt);
-  for (int c = 0; c < c_end; ++c) {
+  if (c_beg < c_end) load_col(c_beg, nxt);
+  for (int c = c_beg; c < c_end; ++c) {
     double val[RPT];
 #pragma unroll
     for (int q = 0; q < RPT; ++q) val[q] = nxt[q];
     if (c + 1 < c_end) load_col(c + 1, nxt);   // next column in flight during this one's work
-    unsigned long long mn = KEY_PINF, mx = KEY_MINF;
+    // S >= u and S <= u, NaN excluded, decided on the keys' high words.  An element whose high
+    // word equals u's or an infinity's, or that is +-0 or a tiny subnormal (-0 must equal +0),
+    // is left to the exact 64-bit test below, which the warp takes only when one of its lanes
+    // holds such an element.
+    unsigned gmask = 0, lmask = 0, smask = 0;
 #pragma unroll
     for (int q = 0; q < RPT; ++q) {
-      const unsigned long long kv = dkey(val[q]);
-      // NaN keys lie outside [key(-inf), key(+inf)]; a test on the double itself is compiled
-      // to an FP64 instruction, which on GB300 would bound the scan
-      const bool ok = kv >= KEY_MINF && kv <= KEY_PINF;
-      const bool ge = ok && kv >= ku, le = ok && kv <= ku;
-      if (ge && tk[q] < mn) mn = tk[q];
-      if (le && tk[q] > mx) mx = tk[q];
+      const unsigned kh = dkey_hi(val[q]);
+      const bool slow = kh == khu || kh == KH_PINF || kh == KH_MINF || (((unsigned)__double2hiint(val[q]) << 1) == 0u);
+      const bool ge = !slow && kh > khu && kh < KH_PINF;
+      const bool le = !slow && kh < khu && kh > KH_MINF;
+      gmask |= ge ? bit[q] : 0u;
+      lmask |= le ? bit[q] : 0u;
       cnt[q] += ge ? 1 : 0;
+      smask |= slow ? (1u << q) : 0u;
     }
+    if (__any_sync(0xffffffffu, smask != 0u)) {
+#pragma unroll
+      for (int q = 0; q < RPT; ++q) {
+        if (smask & (1u << q)) {
+          const unsigned long long kv = dkey(val[q]);
+          const bool ok = kv >= KEY_MINF && kv <= KEY_PINF;
+          const bool ge = ok && kv >= ku, le = ok && kv <= ku;
+          gmask |= ge ? bit[q] : 0u;
+          lmask |= le ? bit[q] : 0u;
+          cnt[q] += ge ? 1 : 0;
+        }
+      }
+    }
+    unsigned long long mn = gmask ? s_key[__ffs(gmask) - 1][threadIdx.x] : KEY_PINF;
+    unsigned long long mx = lmask ? s_key[31 - __clz(lmask)][threadIdx.x] : KEY_MINF;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const unsigned long long a = __shfl_xor_sync(0xffffffffu, mn, o);
@@ -99,18 +147,22 @@ __global__ void __launch_bounds__(SCAN_THREADS) k_scan(const double* __restrict_
       mn = a < mn ? a : mn;
       mx = b > mx ? b : mx;
     }
-    if (lane == 0) { s_mn[warp][c] = mn; s_mx[warp][c] = mx; }
-  }
-  __syncthreads();
-  if (threadIdx.x < c_end) {
-    unsigned long long mn = KEY_PINF, mx = KEY_MINF;
-    for (int w = 0; w < SCAN_THREADS / 32; ++w) {
-      mn = s_mn[w][threadIdx.x] < mn ? s_mn[w][threadIdx.x] : mn;
-      mx = s_mx[w][threadIdx.x] > mx ? s_mx[w][threadIdx.x] : mx;
+    const int slot = (c - c_beg) % SCAN_COLS;
+    if (lane == 0) { s_mn[warp][slot] = mn; s_mx[warp][slot] = mx; }
+    if (slot == SCAN_COLS - 1 || c == c_end - 1) {   // the same columns in every thread
+      __syncthreads();
+      if (threadIdx.x <= slot) {
+        unsigned long long m1 = KEY_PINF, m2 = KEY_MINF;
+        for (int w = 0; w < SCAN_THREADS / 32; ++w) {
+          m1 = s_mn[w][threadIdx.x] < m1 ? s_mn[w][threadIdx.x] : m1;
+          m2 = s_mx[w][threadIdx.x] > m2 ? s_mx[w][threadIdx.x] : m2;
+        }
+        const size_t o = (size_t)rb * M + (c - slot) + threadIdx.x;
+        psi_part[o] = dkey_inv(m1);   // +inf / -inf when the block's column has no qualifying row
+        phi_part[o] = dkey_inv(m2);
+      }
+      __syncthreads();
     }
-    const size_t o = (size_t)rb * M + cbk * SCAN_COLS + threadIdx.x;
-    psi_part[o] = dkey_inv(mn);   // +inf / -inf when the block's column has no qualifying row
-    phi_part[o] = dkey_inv(mx);
   }
   if (count) {
 #pragma unroll
@@ -139,6 +191,26 @@ __global__ void k_regions(const double* __restrict__ t, int n_p, double q_in, do
   }
 }
 
+// The scan's grid: one row of CTAs per SCAN_ROWS rows, and as many column groups as fill the
+// GPU's resident CTAs twice (at least one group, at most one per column).  No allocation, so
+// the allocation-free entry point uses it too.
+static std::atomic<int> g_scan_resident{0};
+static cudaError_t scan_grid(int n_p, int M, dim3* grid) {
+  int resident = g_scan_resident.load(std::memory_order_relaxed);
+  if (resident == 0) {
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_scan, SCAN_THREADS, 0);
+    if (e != cudaSuccess) return e;
+    resident = std::max(1, sms * per_sm);
+    g_scan_resident.store(resident, std::memory_order_relaxed);
+  }
+  const int nrb = (n_p + SCAN_ROWS - 1) / SCAN_ROWS;
+  *grid = dim3((unsigned)nrb, (unsigned)std::max(1, std::min(M, 2 * resident / nrb)));
+  return cudaSuccess;
+}
+
 double empirical_quantile(std::vector<double>& a, double p) {
   std::sort(a.begin(), a.end());
   const long N = (long)a.size();
@@ -155,7 +227,8 @@ cr_status calibrate_core(const double* d_S, int lds, int n_p, int M, const doubl
   k_tstat<<<std::min(1024, (n_p + 255) / 256), 256, 0, stream>>>(d_zhat, d_v, u, n_p, sc.t, sc.bad);
   CR_CHECK_LAUNCH("k_tstat");
   if (d_count) CR_CUDA(cudaMemsetAsync(d_count, 0, (size_t)n_p * sizeof(int32_t), stream));
-  dim3 grid(nrb, (M + SCAN_COLS - 1) / SCAN_COLS);
+  dim3 grid;
+  CR_CUDA(scan_grid(n_p, M, &grid));
   {
     TimedScope ts("k_scan", stream);
     k_scan<<<grid, SCAN_THREADS, 0, stream>>>(d_S, lds, n_p, M, sc.t, u, sc.psi_part, sc.phi_part, d_count);
@@ -326,7 +399,8 @@ extern "C" cr_status cr_calibrate_noalloc(const double* d_S, int lds, int n_p, i
   k_tstat<<<std::min(1024, (n_p + 255) / 256), 256, 0, stream>>>(d_zhat, d_v, u, n_p, t, bad);
   count_launch();
   NA_CUDA(cudaGetLastError());
-  dim3 grid((unsigned)nrb, (M + SCAN_COLS - 1) / SCAN_COLS);
+  dim3 grid;
+  NA_CUDA(scan_grid(n_p, M, &grid));
   k_scan<<<grid, SCAN_THREADS, 0, stream>>>(d_S, lds, n_p, M, t, u, psi_part, phi_part, d_count);
   count_launch();
   NA_CUDA(cudaGetLastError());

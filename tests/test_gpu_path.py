@@ -159,6 +159,34 @@ def test_calibration_bit_exact(lib):
     np.testing.assert_array_equal(out["c_out"].cpu().numpy(), ref["c_out"])
 
 
+@pytest.mark.parametrize("u", [0.25, 0.0, -1.5])
+def test_calibration_bit_exact_edge_values(lib, u):
+    # elements equal to u, one ulp either side, sharing u's high 32 bits, +-0, subnormals,
+    # +-inf and NaN, and rows with equal t: the scan decides most elements on 32-bit words
+    # and must agree exactly with the oracle's double comparisons on all of these
+    rng = np.random.default_rng(23)
+    n_p, M = 2500, 70
+    S = rng.standard_normal((n_p, M))
+    ub = np.float64(u).view(np.uint64)
+    special = np.array([u, np.nextafter(u, np.inf), np.nextafter(u, -np.inf), 0.0, -0.0, 5e-324, -5e-324,
+                        np.inf, -np.inf, np.nan, 2.2250738585072014e-308,
+                        (ub ^ np.uint64(0x5A5A5A5A)).view(np.float64), (ub ^ np.uint64(0xFFFFFFFF)).view(np.float64)])
+    mask = rng.random((n_p, M)) < 0.3
+    S[mask] = rng.choice(special, size=int(mask.sum()))
+    z = rng.standard_normal(n_p) * 0.5
+    v = rng.uniform(0.3, 2.0, n_p)
+    z[100:140] = z[99]      # equal t values on several rows
+    v[100:140] = v[99]
+    out = lib.calibrate(colmajor(S), dev(z), dev(v), u, 0.9, counts=True, extrema=True)
+    ref = oracle.calibrate(S, z, v, u, 0.9)
+    np.testing.assert_array_equal(out["psi"].cpu().numpy(), ref["psi"])
+    np.testing.assert_array_equal(out["phi"].cpu().numpy(), ref["phi"])
+    np.testing.assert_array_equal(out["count"].cpu().numpy(), ref["count"])
+    assert out["q_in"] == ref["q_in"] and out["q_out"] == ref["q_out"]
+    np.testing.assert_array_equal(out["c_in"].cpu().numpy(), ref["c_in"])
+    np.testing.assert_array_equal(out["c_out"].cpu().numpy(), ref["c_out"])
+
+
 def test_calibration_errors(lib):
     n_p, M = 100, 10
     S = np.full((n_p, M), 5.0)
