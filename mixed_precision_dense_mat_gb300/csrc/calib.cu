@@ -63,7 +63,14 @@ __global__ void __launch_bounds__(SCAN_THREADS) k_scan(const double* __restrict_
   const int rb = blockIdx.x, cbk = blockIdx.y;
   const int row0 = rb * SCAN_ROWS + threadIdx.x;
   const unsigned long long ku = dkey(u);
+  // The high-word "tie band" of u: elements whose key's high word falls in it are compared
+  // exactly.  For u = +-0 (or a tiny subnormal) it holds both zeros' words, which must compare
+  // equal; for an infinite or NaN u it holds every word, and the whole scan is exact.
   const unsigned khu = dkey_hi(u);
+  unsigned tie_lo = khu, tie_w = 0u;
+  if (khu >= KH_PINF || khu <= KH_MINF) { tie_lo = 0u; tie_w = 0xffffffffu; }
+  else if (khu == 0x7fffffffu || khu == 0x80000000u) { tie_lo = 0x7fffffffu; tie_w = 1u; }
+  const unsigned tie_hi = tie_lo + tie_w;
   // The thread's t keys, ranked among its own RPT rows (ties by row): a column's minimum over
   // the qualifying rows is the lowest set bit of a mask in rank order, read back from shared
   // memory once per column instead of a 64-bit compare-select per element.
@@ -109,17 +116,18 @@ __global__ void __launch_bounds__(SCAN_THREADS) k_scan(const double* __restrict_
 #pragma unroll
     for (int q = 0; q < RPT; ++q) val[q] = nxt[q];
     if (c + 1 < c_end) load_col(c + 1, nxt);   // next column in flight during this one's work
-    // S >= u and S <= u, NaN excluded, decided on the keys' high words.  An element whose high
-    // word equals u's or an infinity's, or that is +-0 or a tiny subnormal (-0 must equal +0),
-    // is left to the exact 64-bit test below, which the warp takes only when one of its lanes
-    // holds such an element.
+    // S >= u and S <= u, NaN excluded, decided on the keys' high words: a finite element whose
+    // word lies outside u's tie band is above or below u.  Elements in the band, and words of
+    // infinities or NaNs, are left to the exact 64-bit test below, which the warp takes only
+    // when one of its lanes holds such an element.
     unsigned gmask = 0, lmask = 0, smask = 0;
 #pragma unroll
     for (int q = 0; q < RPT; ++q) {
       const unsigned kh = dkey_hi(val[q]);
-      const bool slow = kh == khu || kh == KH_PINF || kh == KH_MINF || (((unsigned)__double2hiint(val[q]) << 1) == 0u);
-      const bool ge = !slow && kh > khu && kh < KH_PINF;
-      const bool le = !slow && kh < khu && kh > KH_MINF;
+      const bool finite = (kh - (KH_MINF + 1u)) < (KH_PINF - KH_MINF - 1u);   // strictly between the infinities' words
+      const bool slow = (kh - tie_lo) <= tie_w || !finite;
+      const bool ge = !slow && kh > tie_hi;
+      const bool le = !slow && !ge;
       gmask |= ge ? bit[q] : 0u;
       lmask |= le ? bit[q] : 0u;
       cnt[q] += ge ? 1 : 0;
@@ -140,12 +148,17 @@ __global__ void __launch_bounds__(SCAN_THREADS) k_scan(const double* __restrict_
     }
     unsigned long long mn = gmask ? s_key[__ffs(gmask) - 1][threadIdx.x] : KEY_PINF;
     unsigned long long mx = lmask ? s_key[31 - __clz(lmask)][threadIdx.x] : KEY_MINF;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const unsigned long long a = __shfl_xor_sync(0xffffffffu, mn, o);
-      const unsigned long long b = __shfl_xor_sync(0xffffffffu, mx, o);
-      mn = a < mn ? a : mn;
-      mx = b > mx ? b : mx;
+    // warp minimum / maximum of the 64-bit keys: the high words first, then the low words of
+    // the lanes that hold the extreme high word (two warp reductions each)
+    {
+      const unsigned h = (unsigned)(mn >> 32), hm = __reduce_min_sync(0xffffffffu, h);
+      const unsigned lm = __reduce_min_sync(0xffffffffu, h == hm ? (unsigned)mn : 0xffffffffu);
+      mn = ((unsigned long long)hm << 32) | lm;
+    }
+    {
+      const unsigned h = (unsigned)(mx >> 32), hm = __reduce_max_sync(0xffffffffu, h);
+      const unsigned lm = __reduce_max_sync(0xffffffffu, h == hm ? (unsigned)mx : 0u);
+      mx = ((unsigned long long)hm << 32) | lm;
     }
     const int slot = (c - c_beg) % SCAN_COLS;
     if (lane == 0) { s_mn[warp][slot] = mn; s_mx[warp][slot] = mx; }
