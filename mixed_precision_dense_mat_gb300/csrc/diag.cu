@@ -210,19 +210,44 @@ __device__ __forceinline__ void ffbar() {
 // after the last step, followed by the N reciprocal square roots.  Lout receives L (lower
 // part), Xout L^-1 (upper part zero).  gcol: global column of the block's first column, for
 // the failure report.
+// Which element each of the 256 threads carries through the elimination of a 16 x 16 block:
+// code = isT << 8 | i << 4 | j.  Working-matrix element (i, j), i >= j, is updated at steps
+// col < j; transformed-identity element (i, j), i > j, at steps j <= col < i.  Threads are
+// ordered by the last step that updates their element (then the first), so the elements
+// still live at a step sit in few warps, spread over the four sub-partitions, and the other
+// warps skip the step's FP64 instructions.
+struct ElemMap {
+  unsigned short code[DB * DB];
+};
+constexpr ElemMap make_elem_map() {
+  ElemMap m{};
+  int key[DB * DB] = {};
+  int n = 0;
+  for (int i = 0; i < DB; ++i)
+    for (int j = 0; j <= i; ++j) {   // working matrix: steps 0 .. j-1
+      m.code[n] = (unsigned short)(1 << 8 | i << 4 | j);
+      key[n++] = (j - 1) * 64 + 0;
+    }
+  for (int i = 1; i < DB; ++i)
+    for (int j = 0; j < i; ++j) {    // transformed identity: steps j .. i-1
+      m.code[n] = (unsigned short)(i << 4 | j);
+      key[n++] = (i - 1) * 64 + j;
+    }
+  for (int a = 1; a < n; ++a)        // stable insertion sort by key
+    for (int b = a; b > 0 && key[b - 1] > key[b]; --b) {
+      const int tk = key[b]; key[b] = key[b - 1]; key[b - 1] = tk;
+      const unsigned short tc = m.code[b]; m.code[b] = m.code[b - 1]; m.code[b - 1] = tc;
+    }
+  return m;
+}
+__constant__ ElemMap c_elem_map = make_elem_map();
+
 template <int N>
 __device__ void ffN(const Ctx& c, int gcol, const double* src, double* Lout, double* Xout, FFS<N>& f) {
   const int t = threadIdx.x;   // 0 .. N*N-1
-  const bool isT = t < N * (N + 1) / 2;
-  int i, j;
-  if (isT) {
-    i = tri_row(t);
-    j = t - i * (i + 1) / 2;
-  } else {
-    const int u = t - N * (N + 1) / 2;   // strict lower: row i holds i elements
-    i = tri_row(u) + 1;
-    j = u - i * (i - 1) / 2;
-  }
+  const int code = c_elem_map.code[t];
+  const bool isT = (code >> 8) != 0;
+  const int i = (code >> 4) & 15, j = code & 15;
   double v = isT ? src[i * (DB + 1) + j] : 0.0;
   for (int col = 0; col < N; ++col) {
     const int par = col & 1;
