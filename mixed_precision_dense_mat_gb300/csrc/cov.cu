@@ -252,21 +252,25 @@ __global__ void __launch_bounds__(256) k_generate(const double* __restrict__ xy,
     // FP16 tiles (off-diagonal): a single-precision evaluation, accurate to a few 1e-6, is
     // far inside the 2^-11 rounding of the stored value; distances from the double-float
     // coordinates, so that near points do not lose digits to cancellation
-    __half* dst = v.pool16 + (size_t)v.hi16[t] * count;
+    // Two adjacent columns per thread, converted to FP16 together (one packed conversion
+    // instead of two single ones, which issue on GB300's slow conversion pipe) and stored
+    // as one 4-byte pair.
+    __half2* dst = reinterpret_cast<__half2*>(v.pool16 + (size_t)v.hi16[t] * count);
     const float sig = p.sig_hi, invr = p.invr_hi, s2f = (float)s2;
-    for (int idx = threadIdx.x; idx < 64 * nb; idx += blockDim.x) {
-      const int r = r0 + idx / nb, c = idx % nb;
+    const int half_nb = nb / 2;
+    auto entry = [&](int r, int c) {
       const int gi = i * nb + r, gj = j * nb + c;
-      float f = 0.0f;
-      if (gi < n && gj < n) {
-        const float4 a = s_row[r - r0], b = s_col[c];
-        const float dx = (a.x - b.x) + (a.y - b.y), dy = (a.z - b.z) + (a.w - b.w);
-        const float x = sqrtf(fmaf(dx, dx, dy * dy)) * invr;
-        const float e = __expf(-x);   // ex2-based: ~3e-6 relative at x < 50, against FP16's 4.9e-4
-        const float poly = p.kind == 0 ? 1.0f : (p.kind == 1 ? 1.0f + x : fmaf(x * x, 1.0f / 3.0f, 1.0f + x));
-        f = sig * poly * e * s2f;
-      }
-      dst[(size_t)r * nb + c] = __float2half_rn(f);
+      if (gi >= n || gj >= n) return 0.0f;
+      const float4 a = s_row[r - r0], b = s_col[c];
+      const float dx = (a.x - b.x) + (a.y - b.y), dy = (a.z - b.z) + (a.w - b.w);
+      const float x = sqrtf(fmaf(dx, dx, dy * dy)) * invr;
+      const float e = __expf(-x);   // ex2-based: ~3e-6 relative at x < 50, against FP16's 4.9e-4
+      const float poly = p.kind == 0 ? 1.0f : (p.kind == 1 ? 1.0f + x : fmaf(x * x, 1.0f / 3.0f, 1.0f + x));
+      return sig * poly * e * s2f;
+    };
+    for (int idx = threadIdx.x; idx < 64 * half_nb; idx += blockDim.x) {
+      const int r = r0 + idx / half_nb, c = 2 * (idx % half_nb);
+      dst[((size_t)r * nb + c) / 2] = __floats2half2_rn(entry(r, c), entry(r, c + 1));
     }
     return;
   }
@@ -280,6 +284,8 @@ __global__ void __launch_bounds__(256) k_generate(const double* __restrict__ xy,
     bool have_df = false;
     if (gi >= n || gj >= n) {
       v64 = (gi == gj) ? s2 : 0.0;
+    } else if (cls == CR_PREC_FP64 && i == j && c > r) {
+      v64 = 0.0;   // upper part of a diagonal tile: never read (the factorisation uses the lower part)
     } else if (use_df && gi != gj) {
       const float4 a = s_row[r - r0], b = s_col[c];
       const df dx = df_add({a.x, a.y}, df_neg({b.x, b.y}));
