@@ -72,6 +72,11 @@ void scale(const cr_tilemat V, const std::vector<int8_t>& cls, cr_pmap_info* inf
   const double xmax[2] = {(double)FLT_MAX, 65504.0};
   const int fmt[2] = {CR_PREC_FP32, CR_PREC_FP16};
   double ell = -INFINITY, us = 65504.0;
+  // every factor tile of L_s = s L enters the TRMM as an FP16 cast (Alg.1 step 15) and the
+  // largest factor entry is sqrt(max V_ii): u_s also keeps s sqrt(max V_ii) inside FP16
+  double vmax_all = -INFINITY;
+  for (int t = 0; t < V->ntiles; ++t) vmax_all = std::max(vmax_all, V->h_vmax[t]);
+  if (vmax_all > 0) us = std::min(us, 65504.0 / sqrt(vmax_all));
   bool present = false;
   for (int q = 0; q < 2; ++q) {
     double vmn = INFINITY, vmx = -INFINITY;

@@ -24,6 +24,7 @@ from .krige import universal_kriging, conditional_correction
 from .calibrate import (standardized_statistic, extrema_scan, exceedance_counts,
                         empirical_quantile, sample_without_sentinels, confidence_regions,
                         EmptySample, calibrate)
+from .coverage import truth_field, excursion_set, coverage_event
 
 __all__ = [
     "matern", "powexp", "covariance_fn", "covariance_matrix", "covariance_entries",
@@ -33,4 +34,5 @@ __all__ = [
     "simulate", "splitmix64", "rnorm", "universal_kriging", "conditional_correction",
     "standardized_statistic", "extrema_scan", "exceedance_counts", "empirical_quantile",
     "sample_without_sentinels", "confidence_regions", "EmptySample", "calibrate",
+    "truth_field", "excursion_set", "coverage_event",
 ]

@@ -1,0 +1,35 @@
+"""Coverage of the confidence regions (oracle; test infrastructure).
+
+"Mixed-Precision GPU Acceleration for Confidence Regions of Spatial Excursion Sets":
+  * §VI-B.1: the true field of a replicate is Z = X b + L eta, with L L^T the joint
+    covariance V of all sites (prediction and observation) and eta i.i.d. N(0, 1).  The
+    observations are the true field at the observation sites; their measurement noise is
+    the tau^2 already on V's observation block (the reading taken for the noise).
+  * §VI-B.2 / Fig. 3: the excursion set of the truth over the prediction sites is
+    A = {i in D_p : Z_i >= u}; a replicate succeeds when C_in is inside A and A is inside
+    C_out.  The empirical coverage is the fraction of successful replicates.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def truth_field(L: np.ndarray, X: np.ndarray, b, eta: np.ndarray) -> np.ndarray:
+    """Z = X b + L eta for a lower-triangular L with L L^T = V (§VI-B.1); eta may hold one
+    draw per column."""
+    mean = np.asarray(X, dtype=np.float64) @ np.asarray(b, dtype=np.float64)
+    eta = np.asarray(eta, dtype=np.float64)
+    return (mean[:, None] if eta.ndim == 2 else mean) + np.asarray(L) @ eta
+
+
+def excursion_set(z_p: np.ndarray, u: float) -> np.ndarray:
+    """A = {i : z_i >= u} as a boolean mask (§VI-B.2)."""
+    return np.asarray(z_p) >= u
+
+
+def coverage_event(truth_p: np.ndarray, c_in, c_out, u: float) -> bool:
+    """True when C_in is a subset of A and A is a subset of C_out (§VI-B.2)."""
+    A = excursion_set(truth_p, u)
+    inner = np.asarray(c_in).astype(bool)
+    outer = np.asarray(c_out).astype(bool)
+    return bool(np.all(A[inner]) and np.all(outer[A]))

@@ -132,10 +132,18 @@ def fp16_checks(pmap, frob, vmin, vmax) -> dict:
 
 
 def covariance_scale(pmap, vmin, vmax) -> dict:
-    """Applied scale s of §V-E Eq.12."""
+    """Applied scale s of §V-E Eq.12.
+
+    Alg.1 (step 15) casts every off-diagonal factor tile of L_s = s L to FP16, and the
+    largest factor entry is sqrt(max V_ii) (|L_ij| <= sqrt(V_ii)), so the upper bound u_s
+    also keeps s sqrt(max V_ii) inside FP16; it binds only when no FP16-class tile bounds s
+    more tightly (for instance when none is left)."""
     NT = pmap.shape[0]
     consts = {PREC_FP32: (FP32_MIN_NORMAL, FP32_MAX), PREC_FP16: (FP16_MIN_NORMAL, FP16_MAX)}
+    vmax_all = max(vmax[i, j] for (i, j) in _lower(NT))
     ell, us = -math.inf, FP16_MAX
+    if vmax_all > 0:
+        us = min(us, FP16_MAX / math.sqrt(vmax_all))
     present = False
     for f, (xmin, xmax) in consts.items():
         tiles = [(i, j) for (i, j) in _lower(NT) if i != j and pmap[i, j] == f]

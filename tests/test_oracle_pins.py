@@ -282,6 +282,12 @@ def test_checks_and_scale_hand_example():
     assert not oracle.fp16_checks(pm, frob, vmin2, vmax)["check1"]
     # no reduced-precision tile: no scaling
     assert oracle.covariance_scale(np.zeros((3, 3), dtype=np.int8), vmin, vmax)["s"] == 1.0
+    # FP32 tiles only: the FP32 bound sqrt(FLT_MAX / 0.1) is far above the FP16 range, so the
+    # FP16 cast of the factor (largest entry sqrt(max V_ii) = 2) bounds s: u_s = 65504 / 2
+    pm32 = np.array([[0, -1, -1], [1, 0, -1], [1, 1, 0]], dtype=np.int8)
+    vmax4 = vmax.copy(); vmax4[1, 1] = 4.0
+    sc32 = oracle.covariance_scale(pm32, vmin, vmax4)
+    assert sc32["u_s"] == 32752.0 and sc32["s"] == 32751.0 and sc32["s"] * 2.0 < 65504.0
 
 
 def test_auto_refinement_steps():
@@ -345,3 +351,37 @@ def test_inputgen_morton_and_grid():
     p = inputgen.morton_permutation(g)
     # Z-order of the 4x4 grid: (0,0),(1,0),(0,1),(1,1),(2,0),...
     assert p[:4].tolist() == [0, 1, 4, 5] and p[4:8].tolist() == [2, 3, 6, 7]
+
+
+def test_coverage_event_hand_cases_and_set_semantics():
+    # truth over four prediction sites, u = 1.6: A = {0, 2}
+    truth = np.array([2.0, 0.5, 1.6, 1.59])
+    assert oracle.excursion_set(truth, 1.6).tolist() == [True, False, True, False]
+    assert oracle.coverage_event(truth, [1, 0, 0, 0], [1, 0, 1, 1], 1.6)        # {0} in A in {0,2,3}
+    assert not oracle.coverage_event(truth, [1, 1, 0, 0], [1, 1, 1, 1], 1.6)    # site 1 in C_in, not in A
+    assert not oracle.coverage_event(truth, [0, 0, 0, 0], [1, 1, 0, 1], 1.6)    # site 2 in A, not in C_out
+    assert oracle.coverage_event(truth, [0, 0, 0, 0], [1, 0, 1, 0], 1.6)        # C_out = A exactly
+    # against plain set inclusion on random masks
+    rng = np.random.default_rng(4)
+    for _ in range(300):
+        t = rng.standard_normal(9)
+        ci, co = rng.random(9) < 0.2, rng.random(9) < 0.7
+        A = {i for i in range(9) if t[i] >= 0.3}
+        want = {i for i in range(9) if ci[i]} <= A <= {i for i in range(9) if co[i]}
+        assert oracle.coverage_event(t, ci, co, 0.3) == want
+
+
+def test_truth_field_mean_and_covariance():
+    # Z = X b + L eta has mean X b and covariance L L^T = V: Monte Carlo on three sites
+    V = np.array([[2.0, 0.6, 0.2], [0.6, 1.0, 0.3], [0.2, 0.3, 1.5]])
+    L = oracle.cholesky_lower(V)
+    X = np.array([[1.0, 0.2], [1.0, 0.5], [1.0, 0.9]])
+    b = np.array([1.0, -2.0])
+    eta = np.random.default_rng(8).standard_normal((3, 200000))
+    Z = oracle.truth_field(L, X, b, eta)
+    R = eta.shape[1]
+    np.testing.assert_allclose(Z.mean(axis=1), X @ b, atol=5 * np.sqrt(np.diag(V).max() / R))
+    C = np.cov(Z)
+    assert np.max(np.abs(C - V)) < 5 * np.sqrt(2.0 * 2.0 / R) * 2
+    # one draw as a vector gives the same column
+    np.testing.assert_array_equal(oracle.truth_field(L, X, b, eta[:, 0]), Z[:, 0])
