@@ -29,13 +29,6 @@ namespace cr {
 
 cr_status convert_tiles(cr_tilemat V, cudaStream_t stream);
 
-__global__ void k_zero_upper(double* A, int nb) {
-  for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < nb * nb; idx += gridDim.x * blockDim.x) {
-    const int r = idx / nb, c = idx % nb;
-    if (c > r) A[idx] = 0.0;
-  }
-}
-
 namespace {
 
 struct Exec {
@@ -87,8 +80,14 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
   auto ws64 = [&](int par, int i) { return V->ws64 + ((size_t)par * nt + i) * nb2; };
   Plan P;
   int* status = V->d_status;
+  int* dflags = V->diag_flags;
+  unsigned long long* damax = reinterpret_cast<unsigned long long*>(V->minv_part);
+  const size_t dwords = 2 * (size_t)diag_flag_words(nb, V->diag_db);
   P.ops.push_back([=](Exec& x) -> cr_status {
     CR_TRY(status_init_launch(status, x.hi));
+    // both parities of the executor's flags and abs-max start cleared
+    CR_CUDA(cudaMemsetAsync(dflags, 0, dwords * sizeof(int), x.hi));
+    CR_CUDA(cudaMemsetAsync(damax, 0, 2 * sizeof(unsigned long long), x.hi));
     CR_TRY(convert_tiles(V, x.hi));
     CR_CUDA(cudaEventRecord(x.start, x.hi));   // the first two OLD steps wait for the converted tiles
     return CR_OK;
@@ -288,11 +287,9 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
       int* flags = V->diag_flags;
       const int4* tasks = V->diag_tasks;
       P.ops.push_back([=](Exec& x) -> cr_status {
-        CR_CUDA(cudaMemsetAsync(Minv, 0, nb2 * sizeof(double), x.hi));
-        CR_TRY(diag_chol_launch(db, Ajj, Minv, W, nb, g, status, flags, tasks, ntask, dgrid, amax, x.hi));
-        k_zero_upper<<<64, 256, 0, x.hi>>>(Ajj, nb);
-        CR_CHECK_LAUNCH("k_zero_upper");
-        return CR_OK;
+        // the executor zeroes the upper parts of Ajj and Minv and clears the other parity's
+        // flags and abs-max for the next column
+        return diag_chol_launch(db, Ajj, Minv, W, nb, g, status, flags, par, tasks, ntask, dgrid, amax, x.hi);
       });
       if (V->minv_all) {
         double* keep = V->minv_all + (size_t)j * nb2;
@@ -308,7 +305,7 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
       __half* dh = V->pool16 + (size_t)V->h_hi16[tidx(j, j)] * nb2;
       __half* dl = V->pool16 + (size_t)V->h_lo16[tidx(j, j)] * nb2;
       int* st_par = status + par;
-      P.ops.push_back([=](Exec& x) -> cr_status { return split_diag_launch(Minv, Ajj, nb, amax, mh, ml, dh, dl, st_par, x.hi); });
+      P.ops.push_back([=](Exec& x) -> cr_status { return split_diag_launch(Minv, Ajj, nb, amax + par, mh, ml, dh, dl, st_par, x.hi); });
     }
     P.ops.push_back([=](Exec& x) -> cr_status { CR_CUDA(cudaEventRecord(x.ev_split[j], x.hi)); return CR_OK; });
     // the solve of row j+1 (its update is on the lookahead stream) feeds the next column
@@ -404,7 +401,7 @@ extern "C" cr_status cr_potrf_adaptive(cr_tilemat V, cr_stream stream, int* info
     if (!diag_task_list(V->nb / db, tasks)) return fail(CR_ERR_STATE, "cr_potrf_adaptive: diagonal task list failed its progress check");
     CR_CUDA(cudaMalloc(&V->diag_tasks, tasks.size() * sizeof(int4)));
     CR_CUDA(cudaMemcpy(V->diag_tasks, tasks.data(), tasks.size() * sizeof(int4), cudaMemcpyHostToDevice));
-    CR_CUDA(cudaMalloc(&V->diag_flags, diag_flag_words(V->nb, db) * sizeof(int)));
+    CR_CUDA(cudaMalloc(&V->diag_flags, 2 * (size_t)diag_flag_words(V->nb, db) * sizeof(int)));
     V->diag_ntasks = (int)tasks.size();
     V->diag_db = db;
   }

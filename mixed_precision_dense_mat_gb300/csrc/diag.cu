@@ -64,6 +64,9 @@ struct Ctx {
   int* status;
   int gcol0;
   unsigned long long* amax;   // IEEE bits of max |M| over the inverse (non-negative doubles order as unsigned)
+  int* clear_flags;           // the next call's flag set, cleared here
+  int clear_words;
+  unsigned long long* clear_amax;
 };
 
 // Folds the calling warp's |x| into the inverse's running maximum (one atomic per warp).
@@ -356,7 +359,7 @@ __device__ void potrf16(const Ctx& c, int k, double v, const Blk* P, Blk* A16, B
   {
     const int i = t / DB, j = t % DB;
     m[(size_t)i * c.nb + j] = X[i][j];
-    if (j <= i) a[(size_t)i * c.nb + j] = sh.l16[i][j];
+    a[(size_t)i * c.nb + j] = j <= i ? sh.l16[i][j] : 0.0;
     fold_amax(c, X[i][j]);
   }
 }
@@ -449,6 +452,22 @@ __global__ void __launch_bounds__(256) k_diag_chol(Ctx c, const int4* __restrict
   if (s_task == 0) {
     run_chain(c, S0, S1, S2, S3, sh, &s_ok);
     return;
+  }
+  {
+    // Housekeeping the queue CTAs do while the chain factors the first block: clear the next
+    // call's flags and abs-max, and zero the strictly upper 16 x 16 blocks of the factor
+    // tile and of the inverse (no task reads them).
+    const int q = s_task - 1, nq = gridDim.x - 1;
+    for (int w = q * 256 + threadIdx.x; w < c.clear_words; w += nq * 256) c.clear_flags[w] = 0;
+    if (q == 0 && threadIdx.x == 0) *c.clear_amax = 0ull;
+    const int r = threadIdx.x / DB, col = threadIdx.x % DB;
+    for (int blk = q; blk < NB * NB; blk += nq) {
+      const int bi = blk / NB, bj = blk % NB;
+      if (bj <= bi) continue;
+      const size_t o = (size_t)(bi * DB + r) * c.nb + bj * DB + col;
+      c.A[o] = 0.0;
+      c.Minv[o] = 0.0;
+    }
   }
   // Warp 1 runs the queue: lane 0 claims task indices one ahead (the claim's round trip
   // overlaps the current task) and lanes 0-2 poll the current task's flags side by side
@@ -622,18 +641,23 @@ bool diag_task_list(int NB, std::vector<int4>& tasks) {
 }
 
 cr_status diag_chol_launch(int db, double* A, double* Minv, double* W, int nb, int gcol0, int* status, int* flags,
-                           const int4* d_tasks, int ntasks, int grid, unsigned long long* amax, cudaStream_t s) {
+                           int par, const int4* d_tasks, int ntasks, int grid, unsigned long long* amax, cudaStream_t s) {
   if (db != DB || nb % DB != 0 || grid < 2) return fail(CR_ERR_ARG, "diag_chol_launch: block size 16 dividing nb and at least 2 CTAs");
   const int NB = nb / db;
+  const int words = diag_flag_words(nb, db);
+  int* cur = flags + (size_t)(par & 1) * words;
   Ctx c;
   c.A = A; c.Minv = Minv; c.W = W; c.nb = nb; c.NB = NB;
+  c.clear_flags = flags + (size_t)((par & 1) ^ 1) * words;
+  c.clear_words = words;
+  c.clear_amax = amax + ((par & 1) ^ 1);
+  amax += par & 1;
+  flags = cur;
   c.ver = flags; c.fac = flags + NB * NB; c.inv = flags + 2 * NB * NB; c.iver = flags + 3 * NB * NB;
   c.abort_flag = flags + 4 * NB * NB;
   int* counter = flags + 4 * NB * NB + 1;
   int* role = flags + 4 * NB * NB + 2;
   c.status = status; c.gcol0 = gcol0; c.amax = amax;
-  CR_CUDA(cudaMemsetAsync(flags, 0, diag_flag_words(nb, db) * sizeof(int), s));
-  CR_CUDA(cudaMemsetAsync(amax, 0, sizeof(unsigned long long), s));
   static bool configured = false;
   if (!configured) {
     // same shared-memory carveout as the tensor-core kernel, so these small CTAs can share

@@ -17,11 +17,13 @@ inline int diag_flag_words(int nb, int db) {
 // order under which every wait of the executor ends; false if that check fails.
 bool diag_task_list(int NB, std::vector<int4>& tasks);
 
-// A (nb x nb row-major, ld nb): lower part overwritten by L; Minv (same layout) receives
-// L^-1 (lower; the caller zeroes it beforehand); W: nb x nb FP64 scratch.  flags:
-// diag_flag_words(nb, db) ints of device scratch, cleared by this call.
-// amax: device word that receives the IEEE bits of max |L^-1| (cleared by this call).
+// A (nb x nb row-major, ld nb): lower part overwritten by L, upper part zeroed; Minv (same
+// layout) receives L^-1 with its upper part zeroed; W: nb x nb FP64 scratch.
+// flags: two sets of diag_flag_words(nb, db) ints; set `par` must be zero on entry and is
+// used, set 1 - par is cleared for the next call.  amax: two words; amax[par] (zero on entry)
+// receives the IEEE bits of max |L^-1|, amax[1 - par] is cleared.  Calls alternate par, and
+// both sets are zero before the first call.
 cr_status diag_chol_launch(int db, double* A, double* Minv, double* W, int nb, int gcol0, int* status, int* flags,
-                           const int4* d_tasks, int ntasks, int grid, unsigned long long* amax, cudaStream_t s);
+                           int par, const int4* d_tasks, int ntasks, int grid, unsigned long long* amax, cudaStream_t s);
 
 }  // namespace cr
