@@ -177,6 +177,18 @@ struct NoOp {
   __device__ void operator()(int, int, int, int, int) const {}
 };
 
+// FP32 -> FP64 widening from the IEEE 754 fields (exponent rebiased by 1023 - 127, fraction
+// shifted up by 29 bits) on the integer units: on GB300 the conversion instruction issues on
+// the slow FP64/conversion pipe, which bounds the epilogues that widen every accumulator.
+// Zeros, subnormals and non-finite values (rare here) use the conversion instruction.
+__device__ __forceinline__ double widen(float f) {
+  const unsigned u = __float_as_uint(f);
+  const unsigned ex = (u >> 23) & 0xffu;
+  if (__builtin_expect(ex == 0u || ex == 0xffu, 0)) return (double)f;
+  const unsigned hi = (u & 0x80000000u) | ((ex + (1023u - 127u)) << 20) | ((u & 0x7fffffu) >> 3);
+  return __hiloint2double((int)hi, (int)(u << 29));
+}
+
 // Output of the simulation multiply for the thread's row r_local and 16 columns from c0:
 // Y is column-major, so the 32 lanes of a warp (32 consecutive rows) write contiguously.
 __device__ __forceinline__ void trmm_store(const TcParams& p, const Job& jb, int r_local, int c0, const float* acc) {
@@ -189,7 +201,7 @@ __device__ __forceinline__ void trmm_store(const TcParams& p, const Job& jb, int
     const int col = jb.cb * TC_BN + c0 + q;
     if (col < p.M) {
       const float a = f16 ? __half2float(__float2half_rn(acc[q])) : acc[q];
-      p.Y[(size_t)col * p.ldy + row] = (double)a;
+      p.Y[(size_t)col * p.ldy + row] = widen(a);
     }
   }
 }
@@ -271,6 +283,23 @@ __device__ __forceinline__ Epi make_epi(const TcParams& p, const Job& jb) {
   return e;
 }
 
+// FP16 high/low split of the values of rows r and r + 1 at element offset o (and o + nb),
+// two at a time: one packed conversion serves both rows (conversions issue on GB300's slow
+// conversion pipe).  with32 also stores the FP32 values.
+__device__ __forceinline__ void split_pair(const Epi& e, size_t o, int nb, float a, float b, bool with32) {
+  const __half2 h = __floats2half2_rn(a, b);
+  const float2 hf = __half22float2(h);
+  const __half2 l = __floats2half2_rn(a - hf.x, b - hf.y);
+  if (with32) {
+    e.f32[o] = a;
+    e.f32[o + nb] = b;
+  }
+  e.h[o] = __low2half(h);
+  e.h[o + nb] = __high2half(h);
+  e.l[o] = __low2half(l);
+  e.l[o + nb] = __high2half(l);
+}
+
 // One 32 x 32 chunk of a row-major tile: lane `lane` handles column col0 + lane of the 32
 // rows from row offset base (element offsets off(r) = base + r nb + lane); st holds the
 // accumulator chunk (st[r][lane]).  The reads of all 32 rows are issued before any store,
@@ -283,7 +312,7 @@ __device__ __forceinline__ void epi_chunk(const Epi& e, size_t base, int nb, int
 #pragma unroll
       for (int r = 0; r < 32; ++r) x[r] = e.s64[o + (size_t)r * nb];
 #pragma unroll
-      for (int r = 0; r < 32; ++r) e.d64[o + (size_t)r * nb] = x[r] - (double)st[r][lane];
+      for (int r = 0; r < 32; ++r) e.d64[o + (size_t)r * nb] = x[r] - widen(st[r][lane]);
       break;
     }
     case EK_NEW64: {
@@ -291,7 +320,7 @@ __device__ __forceinline__ void epi_chunk(const Epi& e, size_t base, int nb, int
 #pragma unroll
       for (int r = 0; r < 32; ++r) x[r] = e.d64[o + (size_t)r * nb];
 #pragma unroll
-      for (int r = 0; r < 32; ++r) e.d64[o + (size_t)r * nb] = x[r] - (double)st[r][lane];
+      for (int r = 0; r < 32; ++r) e.d64[o + (size_t)r * nb] = x[r] - widen(st[r][lane]);
       break;
     }
     case EK_OLD32: {
@@ -307,7 +336,11 @@ __device__ __forceinline__ void epi_chunk(const Epi& e, size_t base, int nb, int
 #pragma unroll
       for (int r = 0; r < 32; ++r) x[r] = e.s16[o + (size_t)r * nb];
 #pragma unroll
-      for (int r = 0; r < 32; ++r) e.f32[o + (size_t)r * nb] = __half2float(x[r]) - st[r][lane];
+      for (int r = 0; r < 32; r += 2) {
+        const float2 f = __half22float2(__halves2half2(x[r], x[r + 1]));
+        e.f32[o + (size_t)r * nb] = f.x - st[r][lane];
+        e.f32[o + (size_t)(r + 1) * nb] = f.y - st[r + 1][lane];
+      }
       break;
     }
     case EK_NEW32: {
@@ -315,12 +348,8 @@ __device__ __forceinline__ void epi_chunk(const Epi& e, size_t base, int nb, int
 #pragma unroll
       for (int r = 0; r < 32; ++r) x[r] = e.s32[o + (size_t)r * nb];
 #pragma unroll
-      for (int r = 0; r < 32; ++r) {
-        const float w = (x[r] - st[r][lane]) * e.sc;
-        const __half h = __float2half_rn(w);
-        e.h[o + (size_t)r * nb] = h;
-        e.l[o + (size_t)r * nb] = __float2half_rn(w - __half2float(h));
-      }
+      for (int r = 0; r < 32; r += 2)
+        split_pair(e, o + (size_t)r * nb, nb, (x[r] - st[r][lane]) * e.sc, (x[r + 1] - st[r + 1][lane]) * e.sc, false);
       break;
     }
     case EK_NEW16: {
@@ -328,23 +357,26 @@ __device__ __forceinline__ void epi_chunk(const Epi& e, size_t base, int nb, int
 #pragma unroll
       for (int r = 0; r < 32; ++r) x[r] = e.s32[o + (size_t)r * nb];
 #pragma unroll
-      for (int r = 0; r < 32; ++r) e.h[o + (size_t)r * nb] = __float2half_rn(x[r] - st[r][lane]);
+      for (int r = 0; r < 32; r += 2) {
+        const __half2 h = __floats2half2_rn(x[r] - st[r][lane], x[r + 1] - st[r + 1][lane]);
+        e.h[o + (size_t)r * nb] = __low2half(h);
+        e.h[o + (size_t)(r + 1) * nb] = __high2half(h);
+      }
       break;
     }
     case EK_TRSM16: {
 #pragma unroll
-      for (int r = 0; r < 32; ++r) e.h[o + (size_t)r * nb] = __float2half_rn(st[r][lane] * e.sc);
+      for (int r = 0; r < 32; r += 2) {
+        const __half2 h = __floats2half2_rn(st[r][lane] * e.sc, st[r + 1][lane] * e.sc);
+        e.h[o + (size_t)r * nb] = __low2half(h);
+        e.h[o + (size_t)(r + 1) * nb] = __high2half(h);
+      }
       break;
     }
     default: {
 #pragma unroll
-      for (int r = 0; r < 32; ++r) {
-        const float x = st[r][lane] * e.sc;
-        const __half h = __float2half_rn(x);
-        e.f32[o + (size_t)r * nb] = x;
-        e.h[o + (size_t)r * nb] = h;
-        e.l[o + (size_t)r * nb] = __float2half_rn(x - __half2float(h));
-      }
+      for (int r = 0; r < 32; r += 2)
+        split_pair(e, o + (size_t)r * nb, nb, st[r][lane] * e.sc, st[r + 1][lane] * e.sc, true);
     }
   }
 }
