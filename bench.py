@@ -38,13 +38,13 @@ FP64_PEAK_TFLOPS = 1.19       # measured DFMA rate on GB300 (profiles/fp64_peak_
 # DRAM bytes per launch from one ncu capture of the kernel as it stands (profiles/); None once
 # the kernel has changed since the capture
 NCU_TRAFFIC_PER_LAUNCH = {
-    "k_diag_chol": 1352448 + 7680,   # profiles/k_diag_chol_n8192.md (one 512 tile per launch at any n)
+    "k_diag_chol": 1353728 + 5888,   # profiles/k_diag_chol_n8192.md (one 512 tile per launch at any n)
     "k_tc_trmm": None,               # profiles/k_tc_trmm_n8192.md covers n = 8192 only (not proportional in n)
     "k_scan": None,                  # set per workload below: proportional to the rows scanned
 }
-# profiles/k_scan_n8192.md: DRAM bytes of one scan launch at n = 8192, M = 2048; the scan reads
+# profiles/k_scan_n32768.md: DRAM bytes of one scan launch at n = 32768, M = 2048; the scan reads
 # S once, so its traffic scales with n M
-SCAN_NCU_BYTES_N8192_M2048 = 134331904 + 3332864
+SCAN_NCU_BYTES_N32768_M2048 = 537289728 + 3527936
 TIMED_KERNELS = ["k_diag_chol", "k_tc_old", "k_tc_new", "k_tc_trsm", "k_tc_trmm", "k_cov_stats", "k_generate", "k_scan"]
 WORKLOAD = inputgen.WORKLOADS["c"]
 SEED_Z = 12345
@@ -299,8 +299,8 @@ def run_ours(args, world, rank, local):
     kern["k_scan"] = entry("k_scan", "hbm", 8.0 * n * M + 16.0 * n, "GB/s", pk["hbm"],
                            f"{meas} HBM copy bandwidth; work: 8 n M + 16 n bytes per launch")
     if kern["k_scan"]:
-        kern["k_scan"]["traffic"] = round(SCAN_NCU_BYTES_N8192_M2048 * (n * M) / (8192.0 * 2048.0))
-        kern["k_scan"]["traffic_note"] = "ncu DRAM bytes at n = 8192, M = 2048, scaled by n M"
+        kern["k_scan"]["traffic"] = round(SCAN_NCU_BYTES_N32768_M2048 * (n * M) / (32768.0 * 2048.0))
+        kern["k_scan"]["traffic_note"] = "ncu DRAM bytes at n = 32768, M = 2048 (scaled by n M at other sizes)"
     # the Cholesky's tensor-core kernels together: algorithmic products / their summed time
     tc_ms = sum(ktime[k][0] for k in ("k_tc_old", "k_tc_new", "k_tc_trsm")) / args.steps
     if tc_ms > 0:
