@@ -123,6 +123,10 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
   CR_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, V->device));
   // lookahead launches of column j have about 8 (nt - j) output blocks of short inner length
   // that must finish within one diagonal factorisation: about 16 blocks per CTA
+  // The critical stream's single-tile tensor-core launches (the last update of the diagonal
+  // tile, the solve of the tile below it) spread each output block's epilogue over HI_ESPLIT
+  // CTAs, and the bulk stream leaves HI_SMS SMs free for them.
+  constexpr int HI_ESPLIT = 4, HI_SMS = 32;
   auto cap_mid_of = [&](int j) { return std::min(48, std::max(8, (8 * (nt - j) + 15) / 16)); };
 
   // FP64 products of the newest term k = j - 1 into rows [r0, r1) of column j
@@ -153,6 +157,7 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
       t.rows = d_rows + off;
       t.nrows = cnt;
       t.max_ctas = on_mid ? cap_mid : 0;
+      t.esplit = on_mid ? 1 : HI_ESPLIT;
       P.ops.push_back([=](Exec& x) -> cr_status { return tc_launch(t, *tm, *tm, on_mid ? x.mid : x.hi); });
     }
     std::vector<DJob> js;
@@ -191,7 +196,7 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
     tp.status = V->d_status + par;           // status[2 + par]: exponent of this column's scaled inverse
     tp.ws64 = V->ws64 ? ws64(par, 0) : nullptr;
     tp.w32 = V->w32 ? V->w32 + (size_t)par * nt * nb2 : nullptr;
-    const int cap_mid = cap_mid_of(j), cap_lo = std::max(1, sms - cap_mid - 8);
+    const int cap_mid = cap_mid_of(j), cap_lo = std::max(1, sms - cap_mid - HI_SMS);
 
     // ---------------- OLD(j) on the low-priority stream: needs columns <= j-2 complete
     P.ops.push_back([=](Exec& x) -> cr_status {
@@ -273,6 +278,7 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
       t.kend = knew >= 0 ? j : 0;
       t.row0 = j;
       t.nrows = 1;
+      t.esplit = HI_ESPLIT;
       P.ops.push_back([=](Exec& x) -> cr_status { return tc_launch(t, *tm, *tm, x.hi); });
     }
     double* Ajj = t64(j, j);

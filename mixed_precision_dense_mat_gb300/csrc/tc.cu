@@ -17,6 +17,8 @@
 //             steps 11-13), every off-diagonal factor tile as its FP16 cast (step 15).
 #include "common.cuh"
 #include "ptx.cuh"
+#include <algorithm>
+
 #include "tc.cuh"
 
 namespace cr {
@@ -404,6 +406,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   const int kt_ints = TC_KT_INTS * p.v.nt;
   volatile int* abort_flag = &bars->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int es = p.mode == TC_TRMM ? 1 : max(1, p.esplit);   // nblocks counts es CTAs per output block
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < TC_STAGES; ++s) {
@@ -447,7 +450,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         break;
       }
-      const Job jb = decode(p, t);
+      const Job jb = decode(p, t / es);
       fill_ktable(p, jb, kt);
       __syncwarp();
       if (lane == 0) {
@@ -491,7 +494,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           atomicOr(p.err, DEV_ERR_TIMEOUT);
           break;
         }
-        const Job jb = decode(p, t);
+        const Job jb = decode(p, t / es);
         const int S = for_each_step(p, jb, ktab + b * kt_ints, NoOp());
         mbar_arrive(&bars->kempty[b]);
         tc_fence_after();
@@ -539,7 +542,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         break;
       }
       tc_fence_after();
-      const Job jb = decode(p, t);
+      const Job jb = decode(p, t / es);
+      const int part = t % es;
       const int S = bars->steps[b];
       const uint32_t tq = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(b * TC_BN);
       if (p.mode == TC_TRMM) {
@@ -558,9 +562,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // memory so that consecutive lanes handle consecutive columns of one row
         const Epi e = make_epi(p, jb);
         const int ncols = min(TC_BN, p.v.nb - jb.cb * TC_BN);
+        const int per = ((ncols / 32 + es - 1) / es) * 32;   // this CTA's share of the columns
+        const int g_end = min(ncols, (part + 1) * per);
         float(*st)[33] = reinterpret_cast<float(*)[33]>(estage + (warp - 2) * 32 * 33);
         const size_t base = (size_t)(jb.rb * TC_BM + quad * 32) * p.v.nb + jb.cb * TC_BN;
-        for (int g = 0; g < ncols; g += 32) {
+        for (int g = part * per; g < g_end; g += 32) {
           float acc[32];
           if (S > 0) {
             tmem_ld16(tq + (uint32_t)g, acc);
@@ -596,7 +602,8 @@ cr_status tc_launch(const TcParams& p, const CUtensorMap& tmA, const CUtensorMap
     CR_CUDA(cudaFuncSetAttribute(k_tc, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared));
     configured = true;
   }
-  const int nblocks = tc_num_blocks(p);
+  const int es = p.mode == TC_TRMM ? 1 : std::max(1, p.esplit);
+  const int nblocks = tc_num_blocks(p) * es;
   if (nblocks <= 0) return CR_OK;
   int dev = 0, sms = 0;
   CR_CUDA(cudaGetDevice(&dev));

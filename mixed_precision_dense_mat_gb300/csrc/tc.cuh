@@ -38,6 +38,9 @@ struct TcParams {
   int ldy, M, ncb, flags;
   int max_ctas;       // grid cap (0: one CTA per SM); background launches leave SMs free for
                       // the critical stream, whose CTAs cannot preempt persistent ones
+  int esplit;         // update and solve modes: 1, or CTAs per output block (each repeats the
+                      // block's products and writes 1/esplit of its columns), which spreads
+                      // the epilogue of a launch with few blocks over more SMs
 };
 
 // Launches the persistent kernel over every output block of the launch described by p (one
