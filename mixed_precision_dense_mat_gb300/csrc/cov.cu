@@ -150,15 +150,19 @@ __global__ void __launch_bounds__(256) k_cov_stats(const double* __restrict__ xy
   df ssq = {0.0f, 0.0f};
   df dmn = {INFINITY, 0.0f}, dmx = {-INFINITY, 0.0f};   // double-float extrema (no FP64 work per entry)
   double ssq64 = 0.0, vmn = INFINITY, vmx = -INFINITY;
-  for (int idx = threadIdx.x; idx < 64 * nb; idx += blockDim.x) {
-    const int r = r0 + idx / nb, c = idx % nb;
+  // each thread keeps one column point in registers and walks the 64 rows (the row point is
+  // a broadcast read): no per-entry index division
+  for (int c = threadIdx.x; c < nb; c += blockDim.x)
+#pragma unroll 1
+  for (int rr = 0; rr < 64; ++rr) {
+    const int r = r0 + rr;
     const int gi = i * nb + r, gj = j * nb + c;
     if (gi >= n || gj >= n) continue;
     if (DF) {
       bool fb = gi == gj;
       df v = {0.0f, 0.0f};
       if (!fb) {
-        const float4 a = s_row[r - r0], b = s_col[c];
+        const float4 a = s_row[rr], b = s_col[c];
         const df dx = df_add({a.x, a.y}, df_neg({b.x, b.y}));
         const df dy = df_add({a.z, a.w}, df_neg({b.z, b.w}));
         v = cov_entry_df(p, dx, dy, sig, invr, s_T, &fb);
@@ -268,15 +272,17 @@ __global__ void __launch_bounds__(256) k_generate(const double* __restrict__ xy,
       const float poly = p.kind == 0 ? 1.0f : (p.kind == 1 ? 1.0f + x : fmaf(x * x, 1.0f / 3.0f, 1.0f + x));
       return sig * poly * e * s2f;
     };
-    for (int idx = threadIdx.x; idx < 64 * half_nb; idx += blockDim.x) {
-      const int r = r0 + idx / half_nb, c = 2 * (idx % half_nb);
-      dst[((size_t)r * nb + c) / 2] = __floats2half2_rn(entry(r, c), entry(r, c + 1));
-    }
+    // each thread keeps its column pair and walks the 64 rows: no per-entry index division
+    for (int cp = threadIdx.x; cp < half_nb; cp += blockDim.x)
+#pragma unroll 1
+      for (int r = r0; r < r0 + 64; ++r)
+        dst[((size_t)r * nb + 2 * cp) / 2] = __floats2half2_rn(entry(r, 2 * cp), entry(r, 2 * cp + 1));
     return;
   }
   const df sig = {p.sig_hi, p.sig_lo}, invr = {p.invr_hi, p.invr_lo}, s2d = {s2_hi, s2_lo};
-  for (int idx = threadIdx.x; idx < 64 * nb; idx += blockDim.x) {
-    const int r = r0 + idx / nb, c = idx % nb;
+  for (int c = threadIdx.x; c < nb; c += blockDim.x)
+#pragma unroll 1
+  for (int r = r0; r < r0 + 64; ++r) {
     const int gi = i * nb + r, gj = j * nb + c;
     const size_t off = (size_t)r * nb + c;
     double v64 = 0.0;

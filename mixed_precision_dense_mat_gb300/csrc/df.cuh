@@ -61,13 +61,16 @@ __device__ __forceinline__ double df_to_double(df x) { return (double)x.hi + (do
 __device__ __forceinline__ bool df_lt(df a, df b) { return a.hi < b.hi || (a.hi == b.hi && a.lo < b.lo); }
 
 // sqrt of a non-negative double-float: FP32 square root refined by one Newton step whose
-// residual d - s^2 is formed exactly.
+// residual d - s^2 is formed exactly.  The step's coefficient 1/(2s) scales a correction of
+// relative size ~2^-24, so the approximate reciprocal (relative error ~2^-22) is ample.
 __device__ __forceinline__ df df_sqrt(df d) {
   if (d.hi <= 0.0f) return {0.0f, 0.0f};
   const float s = __fsqrt_rn(d.hi);
   const df p = df_two_prod(s, s);
   const float r = __fadd_rn(__fsub_rn(__fsub_rn(d.hi, p.hi), p.lo), d.lo);
-  return df_quick_two_sum(s, __fmul_rn(r, __fdiv_rn(0.5f, s)));
+  float inv_s;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv_s) : "f"(s));
+  return df_quick_two_sum(s, __fmul_rn(r, 0.5f * inv_s));
 }
 
 // Constants of df_exp: 2^(j/64) as double-float pairs and ln2/64 in three pieces, the first
