@@ -230,10 +230,13 @@ __global__ void __launch_bounds__(256) k_generate(const double* __restrict__ xy,
   const int r0 = blockIdx.y * 64;
   const int cls = v.cls[t];
   const bool use_df = p.use_df && cls != CR_PREC_FP64;
+  // FP16 tiles take the single-precision evaluation for the closed-form Matern orders and for
+  // the power-exponential family
+  const bool fast16 = cls == CR_PREC_FP16 && (p.use_df || p.family == CR_COV_POWEXP);
   extern __shared__ float4 s_pts[];
   float4* s_col = s_pts;
   float4* s_row = s_pts + nb;
-  if (use_df) {
+  if (use_df || fast16) {
     for (int q = threadIdx.x; q < nb + 64; q += blockDim.x) {
       const int g = q < nb ? j * nb + q : i * nb + r0 + (q - nb);
       float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -252,7 +255,7 @@ __global__ void __launch_bounds__(256) k_generate(const double* __restrict__ xy,
   if (threadIdx.x == 0) { s_T.c1 = c_dfexp.c1; s_T.c2 = c_dfexp.c2; s_T.c3 = c_dfexp.c3; }
   __syncthreads();
   const size_t count = (size_t)nb * nb;
-  if (use_df && cls == CR_PREC_FP16) {
+  if (fast16) {
     // FP16 tiles (off-diagonal): a single-precision evaluation, accurate to a few 1e-6, is
     // far inside the 2^-11 rounding of the stored value; distances from the double-float
     // coordinates, so that near points do not lose digits to cancellation
@@ -260,7 +263,8 @@ __global__ void __launch_bounds__(256) k_generate(const double* __restrict__ xy,
     // instead of two single ones, which issue on GB300's slow conversion pipe) and stored
     // as one 4-byte pair.
     __half2* dst = reinterpret_cast<__half2*>(v.pool16 + (size_t)v.hi16[t] * count);
-    const float sig = p.sig_hi, invr = p.invr_hi, s2f = (float)s2;
+    const float sig = p.sig_hi, invr = p.invr_hi, s2f = (float)s2, nuf = (float)p.nu;
+    const bool powexp = p.family == CR_COV_POWEXP;
     const int half_nb = nb / 2;
     auto entry = [&](int r, int c) {
       const int gi = i * nb + r, gj = j * nb + c;
@@ -268,6 +272,11 @@ __global__ void __launch_bounds__(256) k_generate(const double* __restrict__ xy,
       const float4 a = s_row[r - r0], b = s_col[c];
       const float dx = (a.x - b.x) + (a.y - b.y), dy = (a.z - b.z) + (a.w - b.w);
       const float x = sqrtf(fmaf(dx, dx, dy * dy)) * invr;
+      if (powexp) {
+        // exp(-x^nu), x^nu = 2^(nu log2 x) (x = 0 gives 2^-inf = 0): a few 1e-6 relative
+        const float y = x > 0.0f ? exp2f(nuf * __log2f(x)) : 0.0f;
+        return sig * __expf(-y) * s2f;
+      }
       const float e = __expf(-x);   // ex2-based: ~3e-6 relative at x < 50, against FP16's 4.9e-4
       const float poly = p.kind == 0 ? 1.0f : (p.kind == 1 ? 1.0f + x : fmaf(x * x, 1.0f / 3.0f, 1.0f + x));
       return sig * poly * e * s2f;

@@ -97,7 +97,8 @@ def test_fp64_cholesky_and_simulation(lib, case):
     V.close()
 
 
-@pytest.mark.parametrize("case,fixedacc", [("a_exp", 1e-6), ("a_exp", 1e-3), ("ragged_nu15", 1e-6), ("nu07", 1e-2)])
+@pytest.mark.parametrize("case,fixedacc", [("a_exp", 1e-6), ("a_exp", 1e-3), ("ragged_nu15", 1e-6), ("nu07", 1e-2),
+                                           ("powexp", 1e-3)])
 def test_adaptive_cholesky_and_simulation(lib, case, fixedacc):
     c = COV_CASES[case]
     xy, V, Vo = _build(lib, c)
@@ -116,6 +117,8 @@ def test_adaptive_cholesky_and_simulation(lib, case, fixedacc):
     eY16 = relf(Y16, Yo)
     msg = (f"fp64/32/16 tiles {info['n_fp64']}/{info['n_fp32']}/{info['n_fp16']} s={s} "
            f"eL={eL:.2e} eY={eY:.2e} eY16={eY16:.2e}")
+    if case == "powexp":
+        assert info["n_fp16"] > 0, msg   # the single-precision power-exponential tiles are exercised
     assert eY <= 1e-2 and eY16 <= 1e-2, msg
     assert eL <= 1e-2, msg
     V.close()
