@@ -83,11 +83,14 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
   int* dflags = V->diag_flags;
   unsigned long long* damax = reinterpret_cast<unsigned long long*>(V->minv_part);
   const size_t dwords = 2 * (size_t)diag_flag_words(nb, V->diag_db);
+  double* dpub = V->diag_pub;
+  const size_t dpub_bytes = diag_pub_doubles(nb, V->diag_db) * sizeof(double);
   P.ops.push_back([=](Exec& x) -> cr_status {
     CR_TRY(status_init_launch(status, x.hi));
     // both parities of the executor's flags and abs-max start cleared
     CR_CUDA(cudaMemsetAsync(dflags, 0, dwords * sizeof(int), x.hi));
     CR_CUDA(cudaMemsetAsync(damax, 0, 2 * sizeof(unsigned long long), x.hi));
+    CR_CUDA(cudaMemsetAsync(dpub, 0xff, dpub_bytes, x.hi));   // every element unpublished
     CR_TRY(convert_tiles(V, x.hi));
     CR_CUDA(cudaEventRecord(x.start, x.hi));   // the first two OLD steps wait for the converted tiles
     return CR_OK;
@@ -295,7 +298,7 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
       P.ops.push_back([=](Exec& x) -> cr_status {
         // the executor zeroes the upper parts of Ajj and Minv and clears the other parity's
         // flags and abs-max for the next column
-        return diag_chol_launch(db, Ajj, Minv, W, nb, g, status, flags, par, tasks, ntask, dgrid, amax, x.hi);
+        return diag_chol_launch(db, Ajj, Minv, W, nb, g, status, flags, par, dpub, tasks, ntask, dgrid, amax, x.hi);
       });
       if (V->minv_all) {
         double* keep = V->minv_all + (size_t)j * nb2;
@@ -401,6 +404,8 @@ extern "C" cr_status cr_potrf_adaptive(cr_tilemat V, cr_stream stream, int* info
   if (db != V->diag_db) {
     if (V->diag_tasks) cudaFree(V->diag_tasks);
     if (V->diag_flags) cudaFree(V->diag_flags);
+    if (V->diag_pub) cudaFree(V->diag_pub);
+    V->diag_pub = nullptr;
     V->diag_tasks = nullptr;
     V->diag_flags = nullptr;
     std::vector<int4> tasks;
@@ -408,6 +413,7 @@ extern "C" cr_status cr_potrf_adaptive(cr_tilemat V, cr_stream stream, int* info
     CR_CUDA(cudaMalloc(&V->diag_tasks, tasks.size() * sizeof(int4)));
     CR_CUDA(cudaMemcpy(V->diag_tasks, tasks.data(), tasks.size() * sizeof(int4), cudaMemcpyHostToDevice));
     CR_CUDA(cudaMalloc(&V->diag_flags, 2 * (size_t)diag_flag_words(V->nb, db) * sizeof(int)));
+    CR_CUDA(cudaMalloc(&V->diag_pub, diag_pub_doubles(V->nb, db) * sizeof(double)));
     V->diag_ntasks = (int)tasks.size();
     V->diag_db = db;
   }

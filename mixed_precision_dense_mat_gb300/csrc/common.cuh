@@ -127,6 +127,7 @@ struct cr_tilemat_s {
   int4* diag_tasks = nullptr;
   int diag_ntasks = 0, diag_db = 0;
   int* diag_flags = nullptr;
+  double* diag_pub = nullptr;     // the diagonal executor's publication buffers (diag_pub_doubles)
   double* minv_part = nullptr;    // per-block partial maxima of |L_jj^-1|
   bool factored = false;
   int info = 0;

@@ -67,7 +67,28 @@ struct Ctx {
   int* clear_flags;           // the next call's flag set, cleared here
   int clear_words;
   unsigned long long* clear_amax;
+  // Blocks the chain CTA produces, published without a release fence: pub_m[k] = M_kk and
+  // pub_l[k] = L_{k+1,k} (16 x 16 row-major each), pre-filled with PUB_EMPTY; readers poll
+  // the data itself until no element is PUB_EMPTY.  clear_pub: the next call's set.
+  double* pub_m;
+  double* pub_l;
+  double* clear_pub;
 };
+
+// NaN bit pattern marking an unpublished element; a produced value with this pattern is
+// stored as the quiet NaN 0x7ff8... instead, so that readers never wait on it.
+constexpr unsigned long long PUB_EMPTY = 0xffffffffffffffffull;
+
+__device__ __forceinline__ void st_pub(double* p, double x) {
+  unsigned long long b = (unsigned long long)__double_as_longlong(x);
+  if (b == PUB_EMPTY) b = 0x7ff8000000000000ull;
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(b) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_pub(const double* p) {
+  unsigned long long b;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(b) : "l"(p) : "memory");
+  return b;
+}
 
 // Folds the calling warp's |x| into the inverse's running maximum (one atomic per warp).
 __device__ __forceinline__ void fold_amax(const Ctx& c, double x) {
@@ -86,24 +107,24 @@ __device__ __forceinline__ void task_flag(const Ctx& c, int4 tk, int lane, const
   const int NB = c.NB;
   p = nullptr;
   v = 1;
+  // the chain's blocks (M_kk, L_{k+1,k}) have no flag: they are read from the publication
+  // buffers, which the operand loads poll
   if (tk.x == T_TRSM) {
     const int i = tk.y, k = tk.w;
-    if (lane == 0) p = &c.fac[k * NB + k];
-    else if (lane == 1) { p = &c.ver[i * NB + k]; v = k; }
+    if (lane == 1) { p = &c.ver[i * NB + k]; v = k; }
   } else if (tk.x == T_UPDATE) {
     const int i = tk.y, j = tk.z, k = tk.w;
     if (lane == 0) p = &c.fac[i * NB + k];
-    else if (lane == 1) p = &c.fac[j * NB + k];
+    else if (lane == 1 && j != k + 1) p = &c.fac[j * NB + k];
     else if (lane == 2) { p = &c.ver[i * NB + j]; v = k; }
   } else if (tk.x == T_IUPD) {
     const int R = tk.y, C = tk.z, m = tk.w;
-    if (lane == 0) p = &c.fac[R * NB + m];
-    else if (lane == 1) p = m == C ? &c.fac[C * NB + C] : &c.inv[m * NB + C];
+    if (lane == 0 && R != m + 1) p = &c.fac[R * NB + m];
+    else if (lane == 1 && m != C) p = &c.inv[m * NB + C];
     else if (lane == 2) { p = &c.iver[R * NB + C]; v = m - C; }
   } else {
     const int R = tk.y, C = tk.z;
-    if (lane == 0) p = &c.fac[R * NB + R];
-    else if (lane == 1) { p = &c.iver[R * NB + C]; v = R - C; }
+    if (lane == 1) { p = &c.iver[R * NB + C]; v = R - C; }
   }
 }
 
@@ -145,6 +166,34 @@ __device__ __forceinline__ void load_block_t(Blk* S, const double* src, int ld) 
   for (int idx = threadIdx.x; idx < DB * DB; idx += blockDim.x) {
     const int r = idx / DB, q = idx % DB;
     S[q][r] = __ldcg(src + (size_t)r * ld + q);
+  }
+}
+
+// All 256 threads: S (or its transpose) receives the published block at pub once none of its
+// elements is PUB_EMPTY.  False when the kernel's abort flag is set, or after 2 s, which sets
+// the abort flag and the timeout error bit.
+__device__ bool load_pub(const Ctx& c, Blk* S, const double* pub, bool transpose) {
+  const int r = threadIdx.x / DB, q = threadIdx.x % DB;
+  uint64_t t0 = 0;
+  for (int it = 0;; ++it) {
+    const unsigned long long b = ld_pub(pub + threadIdx.x);
+    if (!__syncthreads_or(b == PUB_EMPTY)) {
+      const double x = __longlong_as_double((long long)b);
+      if (transpose) S[q][r] = x;
+      else S[r][q] = x;
+      return true;
+    }
+    int stop = 0;
+    if (threadIdx.x == 0) {
+      if (it == 0) t0 = global_timer_ns();
+      stop = ld_acquire(c.abort_flag);
+      if (!stop && global_timer_ns() - t0 > 2000000000ull) {
+        atomicOr(&c.status[0], DEV_ERR_TIMEOUT);
+        atomicExch(c.abort_flag, 1);
+        stop = 1;
+      }
+    }
+    if (__syncthreads_or(stop)) return false;
   }
 }
 
@@ -359,6 +408,7 @@ __device__ void potrf16(const Ctx& c, int k, double v, const Blk* P, Blk* A16, B
   {
     const int i = t / DB, j = t % DB;
     m[(size_t)i * c.nb + j] = X[i][j];
+    st_pub(c.pub_m + k * DB * DB + t, X[i][j]);
     a[(size_t)i * c.nb + j] = j <= i ? sh.l16[i][j] : 0.0;
     fold_amax(c, X[i][j]);
   }
@@ -402,9 +452,8 @@ __device__ __forceinline__ double gemm_elem(const Blk* P, const Blk* Q) {
 __device__ void run_chain(const Ctx& c, Blk* S0, Blk* S1, Blk* S2, Blk* S3, FFShared& sh, int* s_ok) {
   const int NB = c.NB;
   const size_t rowstride = (size_t)DB * c.nb;
-  potrf16(c, 0, diag_elem(c, 0), nullptr, S0, S1, sh);   // S1 = M_00
+  potrf16(c, 0, diag_elem(c, 0), nullptr, S0, S1, sh);   // S1 = M_00, published
   __syncthreads();
-  if (threadIdx.x == 0) st_release(&c.fac[0], 1);
   int r, cc;
   trsm_owner(r, cc);
   for (int k = 0; k + 1 < NB; ++k) {
@@ -426,12 +475,11 @@ __device__ void run_chain(const Ctx& c, Blk* S0, Blk* S1, Blk* S2, Blk* S3, FFSh
     const double l = trsm_elem(S2, S1, r, cc);
     S3[r][cc] = l;                     // S3 = L_ik
     aik[(size_t)r * c.nb + cc] = l;
+    st_pub(c.pub_l + k * DB * DB + r * DB + cc, l);
     __syncthreads();
-    if (threadIdx.x == 0) st_release(&c.fac[i * NB + k], 1);
     // UPDATE(i, i, k) fused into POTRF(i)
-    potrf16(c, i, vii, S3, S0, S1, sh);   // S1 = M_ii
+    potrf16(c, i, vii, S3, S0, S1, sh);   // S1 = M_ii, published
     __syncthreads();
-    if (threadIdx.x == 0) st_release(&c.fac[i * NB + i], 1);
   }
 }
 
@@ -460,6 +508,8 @@ __global__ void __launch_bounds__(256) k_diag_chol(Ctx c, const int4* __restrict
     const int q = s_task - 1, nq = gridDim.x - 1;
     for (int w = q * 256 + threadIdx.x; w < c.clear_words; w += nq * 256) c.clear_flags[w] = 0;
     if (q == 0 && threadIdx.x == 0) *c.clear_amax = 0ull;
+    for (int w = q * 256 + threadIdx.x; w < 2 * NB * DB * DB; w += nq * 256)
+      c.clear_pub[w] = __longlong_as_double((long long)PUB_EMPTY);
     const int r = threadIdx.x / DB, col = threadIdx.x % DB;
     for (int blk = q; blk < NB * NB; blk += nq) {
       const int bi = blk / NB, bj = blk % NB;
@@ -508,7 +558,7 @@ __global__ void __launch_bounds__(256) k_diag_chol(Ctx c, const int4* __restrict
       const int i = tk.y, k = tk.w;
       double* a = c.A + i * rowstride + k * DB;
       load_block(S0, a, c.nb);
-      load_block(S1, c.Minv + k * rowstride + k * DB, c.nb);
+      if (!load_pub(c, S1, c.pub_m + k * DB * DB, false)) break;
       __syncthreads();
       int r, cc;
       trsm_owner(r, cc);
@@ -522,7 +572,11 @@ __global__ void __launch_bounds__(256) k_diag_chol(Ctx c, const int4* __restrict
         // the destination is read with the operands: only this task writes it until its flag
         const double d = live ? __ldcg(o) : 0.0;
         load_block(S0, c.A + i * rowstride + k * DB, c.nb);
-        load_block(S1, c.A + j * rowstride + k * DB, c.nb);
+        if (j == k + 1) {
+          if (!load_pub(c, S1, c.pub_l + k * DB * DB, false)) break;
+        } else {
+          load_block(S1, c.A + j * rowstride + k * DB, c.nb);
+        }
         __syncthreads();
         const double p = gemm_elem(S0, S1);
         if (live) *o = d - p;
@@ -531,15 +585,23 @@ __global__ void __launch_bounds__(256) k_diag_chol(Ctx c, const int4* __restrict
         const int R = tk.y, C = tk.z, m = tk.w;
         double* o = c.W + R * rowstride + C * DB + (size_t)r * c.nb + col;
         const double d = (m == C) ? 0.0 : __ldcg(o);
-        load_block(S0, c.A + R * rowstride + m * DB, c.nb);
-        load_block_t(S1, c.Minv + m * rowstride + C * DB, c.nb);
+        if (R == m + 1) {
+          if (!load_pub(c, S0, c.pub_l + m * DB * DB, false)) break;
+        } else {
+          load_block(S0, c.A + R * rowstride + m * DB, c.nb);
+        }
+        if (m == C) {
+          if (!load_pub(c, S1, c.pub_m + C * DB * DB, true)) break;
+        } else {
+          load_block_t(S1, c.Minv + m * rowstride + C * DB, c.nb);
+        }
         __syncthreads();
         const double p = gemm_elem(S0, S1);
         *o = (m == C) ? p : d + p;
       } else {
         // M_RC = -M_RR W_RC
         const int R = tk.y, C = tk.z;
-        load_block(S0, c.Minv + R * rowstride + R * DB, c.nb);
+        if (!load_pub(c, S0, c.pub_m + R * DB * DB, false)) break;
         load_block_t(S1, c.W + R * rowstride + C * DB, c.nb);
         __syncthreads();
         const double mv = -gemm_elem(S0, S1);
@@ -641,7 +703,8 @@ bool diag_task_list(int NB, std::vector<int4>& tasks) {
 }
 
 cr_status diag_chol_launch(int db, double* A, double* Minv, double* W, int nb, int gcol0, int* status, int* flags,
-                           int par, const int4* d_tasks, int ntasks, int grid, unsigned long long* amax, cudaStream_t s) {
+                           int par, double* pub, const int4* d_tasks, int ntasks, int grid, unsigned long long* amax,
+                           cudaStream_t s) {
   if (db != DB || nb % DB != 0 || grid < 2) return fail(CR_ERR_ARG, "diag_chol_launch: block size 16 dividing nb and at least 2 CTAs");
   const int NB = nb / db;
   const int words = diag_flag_words(nb, db);
@@ -651,6 +714,9 @@ cr_status diag_chol_launch(int db, double* A, double* Minv, double* W, int nb, i
   c.clear_flags = flags + (size_t)((par & 1) ^ 1) * words;
   c.clear_words = words;
   c.clear_amax = amax + ((par & 1) ^ 1);
+  c.pub_m = pub + (size_t)(par & 1) * diag_pub_doubles(nb, db) / 2;
+  c.pub_l = c.pub_m + (size_t)NB * DB * DB;
+  c.clear_pub = pub + (size_t)((par & 1) ^ 1) * diag_pub_doubles(nb, db) / 2;
   amax += par & 1;
   flags = cur;
   c.ver = flags; c.fac = flags + NB * NB; c.inv = flags + 2 * NB * NB; c.iver = flags + 3 * NB * NB;
