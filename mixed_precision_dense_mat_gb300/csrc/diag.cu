@@ -40,7 +40,8 @@ namespace cr {
 
 namespace {
 
-enum { T_TRSM = 1, T_UPDATE = 2, T_IUPD = 3, T_ISOLVE = 4 };
+// T_UPDATE2(i, j, k): UPDATE(i, j, k) and UPDATE(i, j+1, k) in one task (they share L_ik)
+enum { T_TRSM = 1, T_UPDATE = 2, T_IUPD = 3, T_ISOLVE = 4, T_UPDATE2 = 5 };
 
 __device__ __forceinline__ int ld_acquire(const int* p) {
   int v;
@@ -112,11 +113,13 @@ __device__ __forceinline__ void task_flag(const Ctx& c, int4 tk, int lane, const
   if (tk.x == T_TRSM) {
     const int i = tk.y, k = tk.w;
     if (lane == 1) { p = &c.ver[i * NB + k]; v = k; }
-  } else if (tk.x == T_UPDATE) {
+  } else if (tk.x == T_UPDATE || tk.x == T_UPDATE2) {
     const int i = tk.y, j = tk.z, k = tk.w;
     if (lane == 0) p = &c.fac[i * NB + k];
     else if (lane == 1 && j != k + 1) p = &c.fac[j * NB + k];
     else if (lane == 2) { p = &c.ver[i * NB + j]; v = k; }
+    else if (tk.x == T_UPDATE2 && lane == 3) p = &c.fac[(j + 1) * NB + k];
+    else if (tk.x == T_UPDATE2 && lane == 4) { p = &c.ver[i * NB + j + 1]; v = k; }
   } else if (tk.x == T_IUPD) {
     const int R = tk.y, C = tk.z, m = tk.w;
     if (lane == 0 && R != m + 1) p = &c.fac[R * NB + m];
@@ -580,6 +583,33 @@ __global__ void __launch_bounds__(256) k_diag_chol(Ctx c, const int4* __restrict
         __syncthreads();
         const double p = gemm_elem(S0, S1);
         if (live) *o = d - p;
+      } else if (type == T_UPDATE2) {
+        // A_ij -= L_ik L_jk^T and A_i,j+1 -= L_ik L_j+1,k^T (block j + 1 <= i is the diagonal one
+        // at most, lower part only)
+        const int i = tk.y, j = tk.z, k = tk.w;
+        double* o = c.A + i * rowstride + j * DB + (size_t)r * c.nb + col;
+        const bool live2 = !(i == j + 1 && col > r);
+        const double d1 = __ldcg(o);
+        const double d2 = live2 ? __ldcg(o + DB) : 0.0;
+        load_block(S0, c.A + i * rowstride + k * DB, c.nb);
+        if (j == k + 1) {
+          if (!load_pub(c, S1, c.pub_l + k * DB * DB, false)) break;
+        } else {
+          load_block(S1, c.A + j * rowstride + k * DB, c.nb);
+        }
+        load_block(S2, c.A + (j + 1) * rowstride + k * DB, c.nb);
+        __syncthreads();
+        double a0 = 0.0, a1 = 0.0, b0 = 0.0, b1 = 0.0;
+#pragma unroll
+        for (int q = 0; q < DB; q += 2) {
+          const double x0 = S0[r][q], x1 = S0[r][q + 1];
+          a0 = fma(x0, S1[col][q], a0);
+          a1 = fma(x1, S1[col][q + 1], a1);
+          b0 = fma(x0, S2[col][q], b0);
+          b1 = fma(x1, S2[col][q + 1], b1);
+        }
+        *o = d1 - (a0 + a1);
+        if (live2) o[DB] = d2 - (b0 + b1);
       } else if (type == T_IUPD) {
         // W_RC (+)= L_Rm M_mC
         const int R = tk.y, C = tk.z, m = tk.w;
@@ -615,6 +645,10 @@ __global__ void __launch_bounds__(256) k_diag_chol(Ctx c, const int4* __restrict
       // them visible at GPU scope to an acquiring reader of the flag
       if (type == T_TRSM) st_release(&c.fac[tk.y * NB + tk.w], 1);
       else if (type == T_UPDATE) st_release(&c.ver[tk.y * NB + tk.z], tk.w + 1);
+      else if (type == T_UPDATE2) {
+        st_release(&c.ver[tk.y * NB + tk.z], tk.w + 1);
+        st_release(&c.ver[tk.y * NB + tk.z + 1], tk.w + 1);
+      }
       else if (type == T_IUPD) st_release(&c.iver[tk.y * NB + tk.z], tk.w - tk.z + 1);
       else st_release(&c.inv[tk.y * NB + tk.z], 1);
     }
@@ -627,7 +661,10 @@ bool diag_task_list(int NB, std::vector<int4>& tasks) {
   // Step k lists what POTRF(k) and the k-th block column of the factor enable; POTRF(k),
   // TRSM(k+1,k) and UPDATE(k+1,k+1,k) belong to the chain CTA and are not listed.
   // The inverse tasks of step k are listed after the factorisation tasks of step k + 2, so
-  // that they fill idle CTAs instead of delaying the updates the chain waits for.
+  // that they fill idle CTAs instead of delaying the updates the chain waits for.  (Measured
+  // on GB300: ordering the list by an estimate of each task's latest start, so that rows
+  // near the diagonal of later steps overtake far rows of earlier steps, is slower: the
+  // overtaking tasks park CTAs until the chain reaches them.)
   tasks.clear();
   const int lag = 2;
   auto inverse_step = [&](int k) {
@@ -637,11 +674,11 @@ bool diag_task_list(int NB, std::vector<int4>& tasks) {
   };
   for (int k = 0; k < NB; ++k) {
     // all solves of the step first (they run side by side), then the updates row by row,
-    // nearest the diagonal first: UPDATE(k+2,k+1,k) and UPDATE(k+2,k+2,k) feed the chain's
-    // next step
+    // nearest the diagonal first, in pairs of adjacent blocks: UPDATE(k+2,k+1,k) and
+    // UPDATE(k+2,k+2,k) (one task) feed the chain's next step
     for (int i = k + 2; i < NB; ++i) tasks.push_back(make_int4(T_TRSM, i, k, k));
     for (int i = k + 2; i < NB; ++i)
-      for (int j = k + 1; j <= i; ++j) tasks.push_back(make_int4(T_UPDATE, i, j, k));
+      for (int j = k + 1; j <= i; j += 2) tasks.push_back(make_int4(j + 1 <= i ? T_UPDATE2 : T_UPDATE, i, j, k));
     if (k >= lag) inverse_step(k - lag);
   }
   for (int k = std::max(0, NB - lag); k < NB; ++k) inverse_step(k);
@@ -656,6 +693,10 @@ bool diag_task_list(int NB, std::vector<int4>& tasks) {
     const int4 tk = tasks[t];
     if (tk.x == T_TRSM) pos_trsm[tk.y * NB + tk.w] = t;
     else if (tk.x == T_UPDATE) pos_upd[((size_t)tk.y * NB + tk.z) * NB + tk.w] = t;
+    else if (tk.x == T_UPDATE2) {
+      pos_upd[((size_t)tk.y * NB + tk.z) * NB + tk.w] = t;
+      pos_upd[((size_t)tk.y * NB + tk.z + 1) * NB + tk.w] = t;
+    }
     else if (tk.x == T_IUPD) pos_iupd[((size_t)tk.y * NB + tk.z) * NB + tk.w] = t;
     else pos_isolve[tk.y * NB + tk.z] = t;
   }
@@ -686,9 +727,11 @@ bool diag_task_list(int NB, std::vector<int4>& tasks) {
     if (tk.x == T_TRSM) {
       const int i = tk.y, k = tk.w;
       ok = chain_ok(3 * k, t) && (k == 0 || before(upd(i, k, k - 1), t));
-    } else if (tk.x == T_UPDATE) {
+    } else if (tk.x == T_UPDATE || tk.x == T_UPDATE2) {
       const int i = tk.y, j = tk.z, k = tk.w;
       ok = fac_ok(i, k, t) && fac_ok(j, k, t) && (k == 0 || before(upd(i, j, k - 1), t));
+      if (tk.x == T_UPDATE2)
+        ok = ok && fac_ok(j + 1, k, t) && (k == 0 || before(upd(i, j + 1, k - 1), t));
     } else if (tk.x == T_IUPD) {
       const int R = tk.y, C = tk.z, m = tk.w;
       ok = fac_ok(R, m, t) && (m == C ? chain_ok(3 * C, t) : before(pos_isolve[m * NB + C], t)) &&
