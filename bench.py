@@ -38,7 +38,7 @@ FP64_PEAK_TFLOPS = 1.19       # measured DFMA rate on GB300 (profiles/fp64_peak_
 # DRAM bytes per launch from one ncu capture of the kernel as it stands (profiles/); None once
 # the kernel has changed since the capture
 NCU_TRAFFIC_PER_LAUNCH = {
-    "k_diag_chol": 1353728 + 5888,   # profiles/k_diag_chol_n8192.md (one 512 tile per launch at any n)
+    "k_diag_chol": 1324032 + 8704,   # profiles/k_diag_chol_n8192.md (one 512 tile per launch at any n)
     "k_tc_trmm": None,               # profiles/k_tc_trmm_n8192.md covers n = 8192 only (not proportional in n)
     "k_scan": None,                  # set per workload below: proportional to the rows scanned
 }
