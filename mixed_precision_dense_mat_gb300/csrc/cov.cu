@@ -224,10 +224,24 @@ __global__ void k_stats_reduce(const double* __restrict__ part, int ntiles, int 
 // block).  Padding rows/columns are the identity (scaled by s^2).
 __global__ void __launch_bounds__(256) k_generate(const double* __restrict__ xy, int n, int nb, CovK p, double s2,
                                                   float s2_hi, float s2_lo, TileView v) {
-  const int t = blockIdx.x;
-  int i, j;
-  tile_of(t, i, j);
-  const int r0 = blockIdx.y * 64;
+  // one-dimensional grid: the (diagonal tile, row block) CTAs first, so that the FP64
+  // evaluations of the diagonal tiles start at once and run beside the other tiles' work
+  const int nrb = nb / 64, ndiag = v.nt * nrb;
+  const int b = blockIdx.x;
+  int i, j, rb;
+  if (b < ndiag) {
+    i = j = b / nrb;
+    rb = b % nrb;
+  } else {
+    const int o = (b - ndiag) / nrb;   // off-diagonal tile o in row order: row i holds i of them
+    rb = (b - ndiag) % nrb;
+    i = (int)((1.0f + sqrtf(8.0f * (float)o + 1.0f)) * 0.5f);
+    while (i * (i - 1) / 2 > o) --i;
+    while ((i + 1) * i / 2 <= o) ++i;
+    j = o - i * (i - 1) / 2;
+  }
+  const int t = tidx(i, j);
+  const int r0 = rb * 64;
   const int cls = v.cls[t];
   const bool use_df = p.use_df && cls != CR_PREC_FP64;
   // FP16 tiles take the single-precision evaluation for the closed-form Matern orders and for
@@ -466,7 +480,7 @@ cr_status fetch_stats(cr_tilemat V) {
 }
 
 cr_status convert_tiles(cr_tilemat V, cudaStream_t stream) {
-  dim3 grid(V->ntiles, V->nb / 64);
+  const unsigned grid = (unsigned)V->ntiles * (V->nb / 64);
   const size_t smem = (size_t)(V->nb + 64) * sizeof(float4);
   const double s2 = V->s * V->s;
   const df s2d = df_from_double(s2);
