@@ -128,13 +128,25 @@ cr_status cr_tilemat_info(cr_tilemat V, int* n, int* nb, int* nt);
  * first.  Computes the per-tile statistics (Frobenius norm, min and max entry over valid
  * entries, Section V-D) in one pass without storing the matrix: the tiles are generated
  * in their precision classes by cr_potrf_adaptive, and cr_tilemat_to_dense / cr_krige
- * evaluate V in FP64 on demand.  For Matern nu in {1/2, 3/2, 5/2} the statistics are
- * evaluated in double-float arithmetic (about 1e-14 relative).  Asynchronous. */
+ * evaluate V in FP64 on demand.  For Matern nu in {1/2, 3/2, 5/2} the diagonal tiles'
+ * statistics are evaluated in double-float arithmetic (about 1e-14 relative) and the
+ * off-diagonal tiles' in FP32 with a rigorous relative error bound (cr_tile_stats_records);
+ * cr_precision_map and cr_tile_stats recompute exactly the records they need.  Other
+ * covariances: every tile exact.  Asynchronous. */
 cr_status cr_cov_build(cr_tilemat V, const double* d_xy, const cr_cov_params* p, cr_stream stream);
 
-/* Per-tile statistics as NT x NT row-major host arrays (lower part filled).
- * Synchronises the stream used by cr_cov_build. */
+/* Per-tile statistics as NT x NT row-major host arrays (lower part filled), each exact
+ * (about 1e-14 relative): tiles that still hold fast-pass records (below) are recomputed
+ * first.  Synchronises the stream used by cr_cov_build.  Any output pointer may be NULL. */
 cr_status cr_tile_stats(cr_tilemat V, double* h_frob, double* h_vmin, double* h_vmax);
+
+/* The statistics records as they stand, without recomputing any (same layout as
+ * cr_tile_stats), with h_err the relative bound of each record: 0 for an exact one, E > 0
+ * for a record of the fast FP32 pass (|record - exact| <= E |exact| for the Frobenius norm,
+ * the min and the max; the pass covers the off-diagonal tiles of the closed-form Matern
+ * orders, and cr_precision_map recomputes exactly the ones its decisions depend on), or
+ * +infinity where no bound holds.  Synchronises like cr_tile_stats. */
+cr_status cr_tile_stats_records(cr_tilemat V, double* h_frob, double* h_vmin, double* h_vmax, double* h_err);
 
 /* Tile precision map, FP16 screening checks and covariance scale (Section V-D/E, Alg.2
  * steps 7-10).  amp = 0 keeps every tile FP64 with s = 1.  With auto_mode != 0 the

@@ -9,6 +9,7 @@ The functions mirror include/cr.h:
   TileMat(n, nb)                         cr_tilemat_create / destroy
   cov_build(V, xy, ...)                  cr_cov_build
   tile_stats(V)                          cr_tile_stats
+  tile_stats_records(V)                  cr_tile_stats_records
   precision_map(V, amp, fixedacc, auto)  cr_precision_map
   potrf_adaptive(V)                      cr_potrf_adaptive
   tilemat_to_dense(V, what)              cr_tilemat_to_dense
@@ -86,6 +87,7 @@ _SIGNATURES = {
     "cr_tilemat_info": (_I, [_P, ctypes.POINTER(_I), ctypes.POINTER(_I), ctypes.POINTER(_I)]),
     "cr_cov_build": (_I, [_P, _P, ctypes.POINTER(CovParams), _P]),
     "cr_tile_stats": (_I, [_P, _P, _P, _P]),
+    "cr_tile_stats_records": (_I, [_P, _P, _P, _P, _P]),
     "cr_precision_map": (_I, [_P, _I, _D, _I, _P, ctypes.POINTER(PmapInfo)]),
     "cr_potrf_adaptive": (_I, [_P, _P, ctypes.POINTER(_I)]),
     "cr_tilemat_to_dense": (_I, [_P, _I, _P, _I, _P]),
@@ -225,6 +227,14 @@ def tile_stats(V: TileMat):
     f, a, b = (np.zeros((nt, nt)) for _ in range(3))
     _check(_lib.cr_tile_stats(V.handle, f.ctypes.data, a.ctypes.data, b.ctypes.data))
     return f, a, b
+
+
+def tile_stats_records(V: TileMat):
+    """cr_tile_stats_records: (frob, vmin, vmax, err) as NT x NT arrays, nothing recomputed."""
+    nt = V.nt
+    f, a, b, e = (np.zeros((nt, nt)) for _ in range(4))
+    _check(_lib.cr_tile_stats_records(V.handle, f.ctypes.data, a.ctypes.data, b.ctypes.data, e.ctypes.data))
+    return f, a, b, e
 
 
 def precision_map(V: TileMat, amp: bool = True, fixedacc: float = 1e-4, auto: bool = False):

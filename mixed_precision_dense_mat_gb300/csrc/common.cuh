@@ -57,6 +57,10 @@ enum : int { DEV_ERR_TIMEOUT = 1, DEV_ERR_BOUNDS = 2 };
 __host__ __device__ inline int tidx(int i, int j) { return i * (i + 1) / 2 + j; }  // i >= j
 
 // Covariance model as the kernels see it.
+// Doubles per tile statistics record: sum of squares, min, max, and the relative error bound
+// of an FP32-evaluated record (0 for an exact record, infinity where no bound holds).
+constexpr int STAT_W = 4;
+
 struct CovK {
   int family;        // CR_COV_*
   int kind;          // Matern: 0 nu=1/2, 1 nu=3/2, 2 nu=5/2, 3 general (quadrature)
@@ -87,11 +91,14 @@ struct cr_tilemat_s {
   // covariance model, locations and tile statistics (tiles are generated on demand)
   double* xy = nullptr;          // n x 2 locations (copy of the caller's)
   cr::CovK covk{};
-  double* stat_part = nullptr;   // ntiles * (nb/64) * 3 partials
-  double* stats = nullptr;       // ntiles * 3 : sum of squares, min, max
+  double* stat_part = nullptr;   // ntiles * (nb/64) * STAT_W partials
+  double* stats = nullptr;       // ntiles * STAT_W : sum of squares, min, max, error parameter
   cr_cov_params params{};
   bool built = false;
   std::vector<double> h_frob, h_vmin, h_vmax;   // ntiles each, after cr_tile_stats
+  std::vector<double> h_stat_err;  // per tile: relative error bound of its statistics (0: exact)
+  std::vector<char> h_stat_exact;  // per tile: statistics from the exact (double-float / FP64) pass
+  int* d_refine = nullptr;         // tile list of the exact pass (ntiles ints)
   bool stats_on_host = false;
   // precision map and class storage
   bool mapped = false;

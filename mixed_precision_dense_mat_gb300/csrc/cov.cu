@@ -117,27 +117,35 @@ __device__ __forceinline__ void tile_of(int t, int& i, int& j) {
   j = t - i * (i + 1) / 2;
 }
 
-// Statistics pass: one CTA per (lower tile, 64-row block); partial sum of squares, min and
-// max over valid entries.  Nothing is stored.
-template <bool DF>
-__global__ void __launch_bounds__(256) k_cov_stats(const double* __restrict__ xy, int n, int nb, CovK p,
-                                                   double* __restrict__ stat_part) {
-  int i, j;
-  tile_of(blockIdx.x, i, j);
-  const int rbk = blockIdx.y, nrb = gridDim.y;
-  const int r0 = rbk * 64;
-  extern __shared__ float4 s_pts[];   // nb column points then 64 row points, as (x.hi, x.lo, y.hi, y.lo)
-  float4* s_col = s_pts;
-  float4* s_row = s_pts + nb;
+// Column points (nb) then the 64 row points of row block r0 of tile (i, j) into shared
+// memory as (x.hi, x.lo, y.hi, y.lo); returns the thread's largest |coordinate| (high words).
+__device__ __forceinline__ float load_tile_points(const double* __restrict__ xy, int n, int nb, int i, int j, int r0,
+                                                  float4* s_pts) {
+  float cmax = 0.0f;
   for (int q = threadIdx.x; q < nb + 64; q += blockDim.x) {
     const int g = q < nb ? j * nb + q : i * nb + r0 + (q - nb);
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
     if (g < n) {
       const Pt pt = load_pt(xy, g);
       v = make_float4(pt.x.hi, pt.x.lo, pt.y.hi, pt.y.lo);
+      cmax = fmaxf(cmax, fmaxf(fabsf(v.x), fabsf(v.z)));
     }
     s_pts[q] = v;
   }
+  return cmax;
+}
+
+// Exact statistics of row block rbk of tile (i, j): partial sum of squares, min, max and 0
+// (an exact partial has no error bound) over valid entries, STAT_W doubles at sp.  Nothing
+// is stored.
+template <bool DF>
+__device__ __forceinline__ void stats_exact(const double* __restrict__ xy, int n, int nb, const CovK& p, int i, int j,
+                                            int rbk, double* __restrict__ sp) {
+  const int r0 = rbk * 64;
+  extern __shared__ float4 s_pts[];
+  float4* s_col = s_pts;
+  float4* s_row = s_pts + nb;
+  load_tile_points(xy, n, nb, i, j, r0, s_pts);
   // exponential tables in shared memory: their per-thread indices diverge
   __shared__ DfExpTables s_T;
   for (int q = threadIdx.x; q < 64; q += blockDim.x) {
@@ -204,20 +212,134 @@ __global__ void __launch_bounds__(256) k_cov_stats(const double* __restrict__ xy
   if (threadIdx.x == 0) {
     double a = 0.0, b = INFINITY, c = -INFINITY;
     for (int q = 0; q < (int)(blockDim.x >> 5); ++q) { a += red[0][q]; b = fmin(b, red[1][q]); c = fmax(c, red[2][q]); }
-    double* sp = stat_part + ((size_t)blockIdx.x * nrb + rbk) * 3;
-    sp[0] = a; sp[1] = b; sp[2] = c;
+    sp[0] = a; sp[1] = b; sp[2] = c; sp[3] = 0.0;
   }
 }
 
-__global__ void k_stats_reduce(const double* __restrict__ part, int ntiles, int nrb, double* __restrict__ stats) {
-  const int t = blockIdx.x * blockDim.x + threadIdx.x;
-  if (t >= ntiles) return;
-  double a = 0.0, b = INFINITY, c = -INFINITY;
-  for (int q = 0; q < nrb; ++q) {
-    const double* sp = part + ((size_t)t * nrb + q) * 3;
-    a += sp[0]; b = fmin(b, sp[1]); c = fmax(c, sp[2]);
+// Exact statistics pass over a tile list (every lower tile in order without one): one CTA
+// per (listed tile, 64-row block).
+template <bool DF>
+__global__ void __launch_bounds__(256) k_cov_stats(const double* __restrict__ xy, int n, int nb, CovK p,
+                                                   double* __restrict__ stat_part, const int* __restrict__ tiles) {
+  const int tile = tiles ? tiles[blockIdx.x] : blockIdx.x;
+  int i, j;
+  tile_of(tile, i, j);
+  stats_exact<DF>(xy, n, nb, p, i, j, blockIdx.y, stat_part + ((size_t)tile * gridDim.y + blockIdx.y) * STAT_W);
+}
+
+// Fast statistics of row block rbk of the off-diagonal tile (i, j), closed-form Matern
+// orders: every entry in FP32 (correctly rounded square root, expf within 2 ulp), distances
+// from the double-float coordinates.  Per entry, with u = 2^-24 and scaled distance x:
+//  - the computed x is off by at most 14 u x + (1/range) C 2^-42, C the largest |coordinate|
+//    (coordinate differences, squares, sum, root, scaling; the pairs' low words are rounded
+//    once more);
+//  - |d log v / dx| <= 1 for these orders, so that error passes to v unchanged;
+//  - the exponential (4 u), the polynomial (4 u) and the products with sigma^2 (3 u) add 11 u.
+// The sum of squares runs in FP32 per thread over K = 64 ceil(nb / 256) entries, in two
+// ranges (v^2 and (v 2^60)^2 for v < 2^-60, so that nothing underflows), so it adds K u to
+// the relative error of the sum (K u / 2 to its square root).  The partial's record holds
+// one relative bound E for its sum of squares' square root, min and max:
+//   E = 1.01 ((16 x_max + 16 + K) u + (1/range) C 2^-41) + 2^-40,
+// or infinity where the bound does not hold (x > 80, where expf leaves the normal range;
+// entries below 2^-100 or above 2^60, where products leave it).
+__device__ __forceinline__ void stats_fast(const double* __restrict__ xy, int n, int nb, const CovK& p, int i, int j,
+                                           int rbk, double* __restrict__ sp) {
+  const int r0 = rbk * 64;
+  extern __shared__ float4 s_pts[];
+  float4* s_col = s_pts;
+  float4* s_row = s_pts + nb;
+  float cmax = load_tile_points(xy, n, nb, i, j, r0, s_pts);
+  __syncthreads();
+  const float sig = p.sig_hi, invr = p.invr_hi;
+  const int kind = p.kind;
+  const float small_lim = 0x1.0p-60f, small_up = 0x1.0p60f;
+  float big = 0.0f, small = 0.0f, vmn = INFINITY, vmx = -INFINITY, xmx = 0.0f;
+  const int rows = min(64, n - (i * nb + r0));
+  for (int c = threadIdx.x; c < nb; c += blockDim.x) {
+    if (j * nb + c >= n) break;
+    const float4 b = s_col[c];
+#pragma unroll 4
+    for (int rr = 0; rr < rows; ++rr) {
+      const float4 a = s_row[rr];
+      const float dx = (a.x - b.x) + (a.y - b.y), dy = (a.z - b.z) + (a.w - b.w);
+      const float x = sqrtf(fmaf(dx, dx, dy * dy)) * invr;
+      const float e = expf(-x);
+      const float poly = kind == 0 ? 1.0f : (kind == 1 ? 1.0f + x : fmaf(x * x, 1.0f / 3.0f, 1.0f + x));
+      const float v = sig * poly * e;
+      if (v >= small_lim) {
+        big = fmaf(v, v, big);
+      } else {
+        const float w = v * small_up;
+        small = fmaf(w, w, small);
+      }
+      vmn = fminf(vmn, v);
+      vmx = fmaxf(vmx, v);
+      xmx = fmaxf(xmx, x);
+    }
   }
-  stats[3 * t] = a; stats[3 * t + 1] = b; stats[3 * t + 2] = c;
+  double sq = (double)big + (double)small * 0x1.0p-120;
+  double dmn = vmn, dmx = vmx, dxm = xmx, dcm = cmax;
+  for (int o = 16; o > 0; o >>= 1) {
+    sq += __shfl_down_sync(0xffffffffu, sq, o);
+    dmn = fmin(dmn, __shfl_down_sync(0xffffffffu, dmn, o));
+    dmx = fmax(dmx, __shfl_down_sync(0xffffffffu, dmx, o));
+    dxm = fmax(dxm, __shfl_down_sync(0xffffffffu, dxm, o));
+    dcm = fmax(dcm, __shfl_down_sync(0xffffffffu, dcm, o));
+  }
+  __shared__ double red[5][8];
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) { red[0][w] = sq; red[1][w] = dmn; red[2][w] = dmx; red[3][w] = dxm; red[4][w] = dcm; }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double a = 0.0, b = INFINITY, cc = -INFINITY, xm = 0.0, cm = 0.0;
+    for (int q = 0; q < (int)(blockDim.x >> 5); ++q) {
+      a += red[0][q]; b = fmin(b, red[1][q]); cc = fmax(cc, red[2][q]); xm = fmax(xm, red[3][q]);
+      cm = fmax(cm, red[4][q]);
+    }
+    const double u = 0x1.0p-24, K = 64.0 * ((nb + 255) / 256);
+    double E = 1.01 * ((16.0 * xm + 16.0 + K) * u + (double)p.invr_hi * cm * 0x1.0p-41) + 0x1.0p-40;
+    const bool empty = !(b <= cc);   // no valid entry in this row block
+    if (!empty && (!(xm <= 80.0) || !(b >= 0x1.0p-100) || !(cc <= 0x1.0p60))) E = INFINITY;
+    sp[0] = a; sp[1] = b; sp[2] = cc; sp[3] = E;
+  }
+}
+
+// Statistics pass of a new covariance for the closed-form Matern orders: CTAs 0 .. nt nrb - 1
+// take the diagonal tiles exactly (double-float, FP64 for the diagonal entries); the others
+// take the off-diagonal tiles, in row order, through the FP32 pass with its error bound.
+__global__ void __launch_bounds__(256) k_cov_stats_split(const double* __restrict__ xy, int n, int nb, int nt, CovK p,
+                                                         double* __restrict__ stat_part) {
+  const int nrb = nb / 64, ndiag = nt * nrb;
+  const int b = blockIdx.x;
+  int i, j, rbk;
+  if (b < ndiag) {
+    i = j = b / nrb;
+    rbk = b % nrb;
+  } else {
+    const int o = (b - ndiag) / nrb;   // off-diagonal tile o in row order: row i holds i of them
+    rbk = (b - ndiag) % nrb;
+    i = (int)((1.0f + sqrtf(8.0f * (float)o + 1.0f)) * 0.5f);
+    while (i * (i - 1) / 2 > o) --i;
+    while ((i + 1) * i / 2 <= o) ++i;
+    j = o - i * (i - 1) / 2;
+  }
+  double* sp = stat_part + ((size_t)tidx(i, j) * nrb + rbk) * STAT_W;
+  if (i == j) stats_exact<true>(xy, n, nb, p, i, j, rbk, sp);
+  else stats_fast(xy, n, nb, p, i, j, rbk, sp);
+}
+
+// Per-tile reduction of the partials of the tiles in the list (all tiles without one).
+__global__ void k_stats_reduce(const double* __restrict__ part, int ntiles, int nrb, double* __restrict__ stats,
+                               const int* __restrict__ tiles) {
+  const int q0 = blockIdx.x * blockDim.x + threadIdx.x;
+  if (q0 >= ntiles) return;
+  const int t = tiles ? tiles[q0] : q0;
+  double a = 0.0, b = INFINITY, c = -INFINITY, e = 0.0;
+  for (int q = 0; q < nrb; ++q) {
+    const double* sp = part + ((size_t)t * nrb + q) * STAT_W;
+    a += sp[0]; b = fmin(b, sp[1]); c = fmax(c, sp[2]); e = fmax(e, sp[3]);
+  }
+  stats[STAT_W * t] = a; stats[STAT_W * t + 1] = b; stats[STAT_W * t + 2] = c; stats[STAT_W * t + 3] = e;
 }
 
 // Generation of s^2 V in each tile's class (Alg.2 step 12).  One CTA per (tile, 64-row
@@ -443,12 +565,17 @@ extern "C" cr_status cr_cov_build(cr_tilemat V, const double* d_xy, const cr_cov
   dim3 grid(V->ntiles, nrb);
   const size_t smem = (size_t)(V->nb + 64) * sizeof(float4);
   {
+    // closed-form Matern orders: diagonal tiles exact, off-diagonal tiles through the
+    // error-bounded FP32 pass (the policy refines the tiles its decisions depend on);
+    // the other covariances: every tile exact
     TimedScope ts("k_cov_stats", stream);
-    if (k.use_df) k_cov_stats<true><<<grid, 256, smem, stream>>>(V->xy, V->n, V->nb, k, V->stat_part);
-    else k_cov_stats<false><<<grid, 256, smem, stream>>>(V->xy, V->n, V->nb, k, V->stat_part);
+    if (k.use_df)
+      k_cov_stats_split<<<(unsigned)V->ntiles * nrb, 256, smem, stream>>>(V->xy, V->n, V->nb, V->nt, k, V->stat_part);
+    else
+      k_cov_stats<false><<<grid, 256, smem, stream>>>(V->xy, V->n, V->nb, k, V->stat_part, nullptr);
   }
   CR_CHECK_LAUNCH("k_cov_stats");
-  k_stats_reduce<<<(V->ntiles + 127) / 128, 128, 0, stream>>>(V->stat_part, V->ntiles, nrb, V->stats);
+  k_stats_reduce<<<(V->ntiles + 127) / 128, 128, 0, stream>>>(V->stat_part, V->ntiles, nrb, V->stats, nullptr);
   CR_CHECK_LAUNCH("k_stats_reduce");
   V->params = *p;
   V->covk = k;
@@ -463,20 +590,49 @@ namespace cr {
 cr_status fetch_stats(cr_tilemat V) {
   if (!V->built) return fail(CR_ERR_STATE, "covariance not built");
   if (V->stats_on_host) return CR_OK;
-  std::vector<double> st(3 * (size_t)V->ntiles);
+  std::vector<double> st(STAT_W * (size_t)V->ntiles);
   CR_CUDA(cudaSetDevice(V->device));
   CR_CUDA(cudaDeviceSynchronize());
   CR_CUDA(cudaMemcpy(st.data(), V->stats, st.size() * sizeof(double), cudaMemcpyDeviceToHost));
   V->h_frob.resize(V->ntiles);
   V->h_vmin.resize(V->ntiles);
   V->h_vmax.resize(V->ntiles);
+  V->h_stat_err.resize(V->ntiles);
+  V->h_stat_exact.resize(V->ntiles);
   for (int t = 0; t < V->ntiles; ++t) {
-    V->h_frob[t] = sqrt(st[3 * t]);
-    V->h_vmin[t] = st[3 * t + 1];
-    V->h_vmax[t] = st[3 * t + 2];
+    V->h_frob[t] = sqrt(st[STAT_W * t]);
+    V->h_vmin[t] = st[STAT_W * t + 1];
+    V->h_vmax[t] = st[STAT_W * t + 2];
+    V->h_stat_err[t] = st[STAT_W * t + 3];
+    V->h_stat_exact[t] = st[STAT_W * t + 3] == 0.0;
   }
   V->stats_on_host = true;
   return CR_OK;
+}
+
+// Exact statistics of the listed tiles (replacing their FP32 records), then a fresh copy of
+// every record on the host.
+cr_status refine_stats(cr_tilemat V, const std::vector<int>& list) {
+  if (list.empty()) return CR_OK;
+  CR_CUDA(cudaSetDevice(V->device));
+  if (!V->d_refine) CR_CUDA(cudaMalloc(&V->d_refine, (size_t)V->ntiles * sizeof(int)));
+  CR_CUDA(cudaMemcpy(V->d_refine, list.data(), list.size() * sizeof(int), cudaMemcpyHostToDevice));
+  const int nrb = V->nb / 64;
+  const size_t smem = (size_t)(V->nb + 64) * sizeof(float4);
+  const dim3 grid((unsigned)list.size(), nrb);
+  {
+    TimedScope ts("k_cov_stats_refine", 0);
+    if (V->covk.use_df)
+      k_cov_stats<true><<<grid, 256, smem, 0>>>(V->xy, V->n, V->nb, V->covk, V->stat_part, V->d_refine);
+    else
+      k_cov_stats<false><<<grid, 256, smem, 0>>>(V->xy, V->n, V->nb, V->covk, V->stat_part, V->d_refine);
+  }
+  CR_CHECK_LAUNCH("k_cov_stats");
+  k_stats_reduce<<<((unsigned)list.size() + 127) / 128, 128, 0, 0>>>(V->stat_part, (int)list.size(), nrb, V->stats,
+                                                                      V->d_refine);
+  CR_CHECK_LAUNCH("k_stats_reduce");
+  V->stats_on_host = false;
+  return fetch_stats(V);
 }
 
 cr_status convert_tiles(cr_tilemat V, cudaStream_t stream) {
@@ -496,6 +652,12 @@ cr_status convert_tiles(cr_tilemat V, cudaStream_t stream) {
 extern "C" cr_status cr_tile_stats(cr_tilemat V, double* h_frob, double* h_vmin, double* h_vmax) {
   if (!V) return fail(CR_ERR_ARG, "cr_tile_stats: NULL handle");
   CR_TRY(fetch_stats(V));
+  {
+    std::vector<int> rest;
+    for (int t = 0; t < V->ntiles; ++t)
+      if (!V->h_stat_exact[t]) rest.push_back(t);
+    CR_TRY(refine_stats(V, rest));
+  }
   const int nt = V->nt;
   for (int i = 0; i < nt; ++i)
     for (int j = 0; j < nt; ++j) {
@@ -504,6 +666,23 @@ extern "C" cr_status cr_tile_stats(cr_tilemat V, double* h_frob, double* h_vmin,
       if (h_frob) h_frob[i * nt + j] = low ? V->h_frob[t] : 0.0;
       if (h_vmin) h_vmin[i * nt + j] = low ? V->h_vmin[t] : 0.0;
       if (h_vmax) h_vmax[i * nt + j] = low ? V->h_vmax[t] : 0.0;
+    }
+  return CR_OK;
+}
+
+extern "C" cr_status cr_tile_stats_records(cr_tilemat V, double* h_frob, double* h_vmin, double* h_vmax,
+                                          double* h_err) {
+  if (!V) return fail(CR_ERR_ARG, "cr_tile_stats_records: NULL handle");
+  CR_TRY(fetch_stats(V));
+  const int nt = V->nt;
+  for (int i = 0; i < nt; ++i)
+    for (int j = 0; j < nt; ++j) {
+      const bool low = j <= i;
+      const int t = low ? tidx(i, j) : 0;
+      if (h_frob) h_frob[i * nt + j] = low ? V->h_frob[t] : 0.0;
+      if (h_vmin) h_vmin[i * nt + j] = low ? V->h_vmin[t] : 0.0;
+      if (h_vmax) h_vmax[i * nt + j] = low ? V->h_vmax[t] : 0.0;
+      if (h_err) h_err[i * nt + j] = low ? V->h_stat_err[t] : 0.0;
     }
   return CR_OK;
 }

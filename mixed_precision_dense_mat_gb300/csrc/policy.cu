@@ -18,6 +18,7 @@
 
 namespace cr {
 cr_status fetch_stats(cr_tilemat V);
+cr_status refine_stats(cr_tilemat V, const std::vector<int>& list);
 
 namespace {
 
@@ -106,6 +107,78 @@ void scale(const cr_tilemat V, const std::vector<int8_t>& cls, cr_pmap_info* inf
   info->range_ok = ell <= us;
 }
 
+// ---- decisions on error-bounded statistics --------------------------------------------------
+// A tile's statistics are either exact (double-float / FP64 pass) or from the FP32 pass with a
+// relative bound E on each of them.  The policy runs on the point values; then every
+// comparison it made is re-examined over the intervals the bounds allow, and the FP32 tiles a
+// comparison or an extreme could depend on are recomputed exactly, until none is left.  The
+// final map, checks and scale are then those the exact statistics of every tile give.  The
+// intervals are widened by 1e-12 relative, far above the exact pass's own error, so that they
+// hold the exact pass's values and not only the true ones.
+struct Iv {
+  double lo, hi;
+};
+
+Iv bound(double c, double e) {
+  if (e == 0.0) return {c, c};
+  if (!(e < 0.5) || !(c >= 0.0)) return {-INFINITY, INFINITY};
+  return {c / (1.0 + e) * (1.0 - 1e-12), c / (1.0 - e) * (1.0 + 1e-12)};
+}
+
+struct Marks {
+  std::vector<char> need;
+  bool all = false;   // a decision turns on ||V||_F's uncertainty alone: refine every FP32 tile
+  void tile(const cr_tilemat V, int t) {
+    if (V->h_stat_exact[t]) all = true;
+    else need[t] = 1;
+  }
+};
+
+// class decisions of the map at accuracy fa that the bounds leave open
+void mark_map(const cr_tilemat V, double fa, Marks& m) {
+  const int nt = V->nt;
+  double g2lo = 0.0, g2hi = 0.0;
+  for (int i = 0; i < nt; ++i)
+    for (int j = 0; j <= i; ++j) {
+      const int t = tidx(i, j);
+      const Iv f = bound(V->h_frob[t], V->h_stat_err[t]);
+      const double w = i == j ? 1.0 : 2.0, lo = std::max(f.lo, 0.0);
+      g2lo += w * lo * lo;
+      g2hi += w * f.hi * f.hi;
+    }
+  const double glo = sqrt(g2lo) * (1.0 - 1e-12), ghi = sqrt(g2hi) * (1.0 + 1e-12);
+  const double eps[2] = {ldexp(1.0, -10), ldexp(1.0, -23)};
+  for (int i = 0; i < nt; ++i)
+    for (int j = 0; j < i; ++j) {
+      const int t = tidx(i, j);
+      const Iv f = bound(V->h_frob[t], V->h_stat_err[t]);
+      const double llo = std::max(f.lo, 0.0) * nt, lhi = f.hi * nt;
+      for (int q = 0; q < 2; ++q) {
+        const double limlo = (fa / eps[q]) * glo, limhi = (fa / eps[q]) * ghi;
+        if (lhi <= limlo) break;      // below this class's limit for every value allowed
+        if (llo > limhi) continue;    // above it for every value allowed
+        m.tile(V, t);
+        break;
+      }
+    }
+}
+
+// the largest (want_max) or smallest value of x over the tiles with sel[t]
+template <class Sel>
+void mark_extreme(const cr_tilemat V, const std::vector<double>& x, bool want_max, Sel sel, Marks& m) {
+  double edge = want_max ? -INFINITY : INFINITY;
+  for (int t = 0; t < V->ntiles; ++t)
+    if (sel(t)) {
+      const Iv b = bound(x[t], V->h_stat_err[t]);
+      edge = want_max ? std::max(edge, b.lo) : std::min(edge, b.hi);
+    }
+  for (int t = 0; t < V->ntiles; ++t)
+    if (sel(t) && !V->h_stat_exact[t]) {
+      const Iv b = bound(x[t], V->h_stat_err[t]);
+      if (want_max ? b.hi >= edge : b.lo <= edge) m.need[t] = 1;
+    }
+}
+
 // per-tile tables have ntiles entries for the life of the tile matrix: allocated once
 template <class T>
 cr_status upload(T** d, const std::vector<T>& h) {
@@ -190,14 +263,45 @@ extern "C" cr_status cr_precision_map(cr_tilemat V, int amp, double fixedacc, in
     c = checks(V, cls);
     pi.s = 1.0; pi.ell = NAN; pi.u_s = NAN; pi.range_ok = 1;
   } else {
-    double fa = auto_mode ? 1e-4 : fixedacc;
+    double fa = 0.0;
     int it = 0;
     for (;;) {
-      make_map(V, fa, cls);
-      c = checks(V, cls);
-      ++it;
-      if (!auto_mode || c.n16 == 0 || (c.c1 && c.c2) || it >= 100000) break;
-      fa = fa * 0.9;
+      std::vector<double> visited;
+      fa = auto_mode ? 1e-4 : fixedacc;
+      it = 0;
+      for (;;) {
+        make_map(V, fa, cls);
+        c = checks(V, cls);
+        visited.push_back(fa);
+        ++it;
+        if (!auto_mode || c.n16 == 0 || (c.c1 && c.c2) || it >= 100000) break;
+        fa = fa * 0.9;
+      }
+      // re-examine every decision taken above over the statistics' bounds
+      Marks m;
+      m.need.assign(V->ntiles, 0);
+      std::vector<int8_t> ci;
+      for (double f : visited) {
+        mark_map(V, f, m);
+        make_map(V, f, ci);
+        auto is16 = [&](int t) { return ci[t] == CR_PREC_FP16; };
+        mark_extreme(V, V->h_vmax, true, is16, m);
+        mark_extreme(V, V->h_vmin, false, is16, m);
+        mark_extreme(V, V->h_frob, true, is16, m);
+      }
+      auto every = [](int) { return true; };
+      mark_extreme(V, V->h_vmax, true, every, m);
+      mark_extreme(V, V->h_frob, true, every, m);
+      for (int8_t q : {(int8_t)CR_PREC_FP32, (int8_t)CR_PREC_FP16}) {
+        auto in_q = [&](int t) { return cls[t] == q; };
+        mark_extreme(V, V->h_vmax, true, in_q, m);
+        mark_extreme(V, V->h_vmin, false, in_q, m);
+      }
+      std::vector<int> list;
+      for (int t = 0; t < V->ntiles; ++t)
+        if (!V->h_stat_exact[t] && (m.all || m.need[t])) list.push_back(t);
+      if (list.empty()) break;
+      CR_TRY(refine_stats(V, list));
     }
     pi.fixedacc = fa;
     pi.iters = it;

@@ -61,6 +61,58 @@ def test_covariance_and_stats(lib, case):
     V.close()
 
 
+@pytest.mark.parametrize("case", ["a_exp", "ragged_nu15", "nu25", "nu07"])
+def test_fast_statistics_records_within_their_bounds(lib, case):
+    """The FP32 statistics pass of the closed-form Matern orders: each off-diagonal record is
+    within its stated relative bound of the oracle's exact statistics, the bound is small
+    enough to decide on, and the diagonal tiles' records (and every record of the other
+    orders) are exact."""
+    c = COV_CASES[case]
+    xy, V, Vo = _build(lib, c)
+    f, mn, mx, err = lib.tile_stats_records(V)
+    fo, mno, mxo = oracle.tile_stats(Vo, c["nb"])
+    nt = V.nt
+    off = np.tril(np.ones((nt, nt), dtype=bool), -1)
+    diag = np.eye(nt, dtype=bool)
+    closed = c["family"] == "matern" and c["nu"] in (0.5, 1.5, 2.5)
+    if closed:
+        assert np.all(err[off] > 0) and np.all(err[off] < 1e-3), err[off].max()
+    else:
+        assert np.all(err[off] == 0)
+    assert np.all(err[diag] == 0)
+    for got, ref in ((f, fo), (mn, mno), (mx, mxo)):
+        fast = off & (err > 0)
+        assert np.all(np.abs(got[fast] - ref[fast]) <= err[fast] * np.abs(ref[fast]))
+        exact = (diag | off) & (err == 0)
+        np.testing.assert_allclose(got[exact], ref[exact], rtol=1e-13, atol=1e-300)
+    # cr_tile_stats recomputes every fast record exactly
+    f2, mn2, mx2 = lib.tile_stats(V)
+    low = diag | off
+    np.testing.assert_allclose(f2[low], fo[low], rtol=1e-13)
+    np.testing.assert_allclose(mn2[low], mno[low], rtol=1e-13, atol=1e-300)
+    np.testing.assert_allclose(mx2[low], mxo[low], rtol=1e-13)
+    assert np.all(lib.tile_stats_records(V)[3][low] == 0)
+    V.close()
+
+
+@pytest.mark.parametrize("fixedacc,auto", [(1e-6, False), (1e-3, False), (1e-4, True), (3e-5, False)])
+def test_precision_map_on_fast_statistics_equals_exact(lib, fixedacc, auto):
+    """The map, checks and scale taken on the fast statistics (with the exact recomputation of
+    the tiles the decisions depend on) equal those taken on exact statistics of every tile."""
+    c = COV_CASES["a_exp"]
+    xy, V1, _ = _build(lib, c)
+    m1, i1 = lib.precision_map(V1, amp=True, fixedacc=fixedacc, auto=auto)
+    xy, V2, _ = _build(lib, c)
+    lib.tile_stats(V2)   # every record exact first
+    m2, i2 = lib.precision_map(V2, amp=True, fixedacc=fixedacc, auto=auto)
+    np.testing.assert_array_equal(m1, m2)
+    for k in i1:
+        a, b = i1[k], i2[k]
+        assert (a == b) or (np.isnan(a) and np.isnan(b)), (k, a, b)
+    V1.close()
+    V2.close()
+
+
 @pytest.mark.parametrize("fixedacc,auto", [(1e-6, False), (1e-3, False), (1e-4, True)])
 def test_precision_map_matches_oracle(lib, fixedacc, auto):
     c = COV_CASES["a_exp"]
@@ -74,6 +126,9 @@ def test_precision_map_matches_oracle(lib, fixedacc, auto):
     assert info["iters"] == ref["iters"] and info["fixedacc"] == ref["fixedacc"]
     assert bool(info["check1"]) == ref["check1"] and bool(info["check2"]) == ref["check2"]
     assert info["n_fp16"] == ref["n_fp16"]
+    for k in ("R_hp", "rho1", "rho2", "ell", "u_s"):
+        if k in ref and not (np.isnan(info[k]) and np.isnan(ref[k])):
+            assert info[k] == pytest.approx(ref[k], rel=1e-12), k
     V.close()
 
 
