@@ -266,6 +266,7 @@ extern "C" cr_status cr_tilemat_destroy(cr_tilemat V) {
   if (V->s_hi) cudaStreamDestroy(V->s_hi);
   if (V->s_lo) cudaStreamDestroy(V->s_lo);
   if (V->s_mid) cudaStreamDestroy(V->s_mid);
+  if (V->s_gen) cudaStreamDestroy(V->s_gen);
   delete V;
   return CR_OK;
 }

@@ -27,17 +27,19 @@
 
 namespace cr {
 
-cr_status convert_tiles(cr_tilemat V, cudaStream_t stream);
+// d_tiles: count tile codes (i << 16 | j), the first ndiag of them diagonal (FP64 class)
+cr_status convert_tiles(cr_tilemat V, const int* d_tiles, int count, int ndiag, cudaStream_t stream);
 
 namespace {
 
 struct Exec {
-  cudaStream_t hi, lo, mid;
+  cudaStream_t hi, lo, mid, gen;
   const DJob* dj;
   const DPair* dp;
   // per column j: OLD(j) done (lo); diagonal factor and inverse split (hi); NEW(j) rows j+1..
   // done (mid); solve of row j+1 done (hi); solves of rows j+2.. done (mid)
   std::vector<cudaEvent_t> ev_old, ev_split, ev_newr, ev_crit, ev_rest;
+  std::vector<cudaEvent_t> ev_gen;   // per column: its tiles generated (one event per column range)
   cudaEvent_t start;
 };
 
@@ -85,14 +87,38 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
   const size_t dwords = 2 * (size_t)diag_flag_words(nb, V->diag_db);
   double* dpub = V->diag_pub;
   const size_t dpub_bytes = diag_pub_doubles(nb, V->diag_db) * sizeof(double);
+  // Tile generation on its own stream, column by column in ranges of doubling width
+  // ([0,1), [1,2), [2,4), [4,8), ...), diagonal tiles first in each range: the factorisation
+  // of column j waits only for its range, so it starts after the first column's tiles
+  // instead of after all of them.
+  if (nt > 32767) return fail(CR_ERR_ARG, "cr_potrf_adaptive: more than 32767 tile rows");
+  std::vector<int> gen_list, gen_off{0}, gen_ndiag, gen_range_of(nt, 0);
+  for (int c0 = 0, w = 1; c0 < nt; c0 += w, w *= 2) {
+    const int c1 = std::min(nt, c0 + w);
+    gen_ndiag.push_back(c1 - c0);
+    for (int c = c0; c < c1; ++c) {
+      gen_list.push_back(c << 16 | c);
+      gen_range_of[c] = (int)gen_off.size() - 1;
+    }
+    for (int c = c0; c < c1; ++c)
+      for (int i = c + 1; i < nt; ++i) gen_list.push_back(i << 16 | c);
+    gen_off.push_back((int)gen_list.size());
+  }
+  const int n_ranges = (int)gen_off.size() - 1;
+  int* d_gen = nullptr;
+  CR_CUDA(cudaMalloc(&d_gen, gen_list.size() * sizeof(int)));
+  CR_CUDA(cudaMemcpy(d_gen, gen_list.data(), gen_list.size() * sizeof(int), cudaMemcpyHostToDevice));
   P.ops.push_back([=](Exec& x) -> cr_status {
     CR_TRY(status_init_launch(status, x.hi));
     // both parities of the executor's flags and abs-max start cleared
     CR_CUDA(cudaMemsetAsync(dflags, 0, dwords * sizeof(int), x.hi));
     CR_CUDA(cudaMemsetAsync(damax, 0, 2 * sizeof(unsigned long long), x.hi));
     CR_CUDA(cudaMemsetAsync(dpub, 0xff, dpub_bytes, x.hi));   // every element unpublished
-    CR_TRY(convert_tiles(V, x.hi));
-    CR_CUDA(cudaEventRecord(x.start, x.hi));   // the first two OLD steps wait for the converted tiles
+    CR_CUDA(cudaEventRecord(x.start, x.hi));   // the first two OLD steps wait for the status and flags
+    for (int r = 0; r < n_ranges; ++r) {
+      CR_TRY(convert_tiles(V, d_gen + gen_off[r], gen_off[r + 1] - gen_off[r], gen_ndiag[r], x.gen));
+      CR_CUDA(cudaEventRecord(x.ev_gen[r], x.gen));
+    }
     return CR_OK;
   });
 
@@ -202,6 +228,7 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
     const int cap_mid = cap_mid_of(j), cap_lo = std::max(1, sms - cap_mid - HI_SMS);
 
     // ---------------- OLD(j) on the low-priority stream: needs columns <= j-2 complete
+    const int grange = gen_range_of[j];
     P.ops.push_back([=](Exec& x) -> cr_status {
       if (j >= 2) {
         CR_CUDA(cudaStreamWaitEvent(x.lo, x.ev_crit[j - 2], 0));
@@ -209,6 +236,8 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
       } else {
         CR_CUDA(cudaStreamWaitEvent(x.lo, x.start, 0));
       }
+      // column j's tiles (every later use of them is ordered after OLD(j))
+      CR_CUDA(cudaStreamWaitEvent(x.lo, x.ev_gen[grange], 0));
       return CR_OK;
     });
     {
@@ -342,14 +371,17 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
     CR_CUDA(cudaDeviceGetStreamPriorityRange(&lo_prio, &hi_prio));
     CR_CUDA(cudaStreamCreateWithPriority(&V->s_hi, cudaStreamNonBlocking, hi_prio));
     CR_CUDA(cudaStreamCreateWithPriority(&V->s_mid, cudaStreamNonBlocking, hi_prio));
-    CR_CUDA(cudaStreamCreateWithPriority(&V->s_lo, cudaStreamNonBlocking, lo_prio));
+    // the bulk updates rank just above the tile generation, which runs ahead of them
+    CR_CUDA(cudaStreamCreateWithPriority(&V->s_lo, cudaStreamNonBlocking, std::max(hi_prio, lo_prio - 1)));
+    CR_CUDA(cudaStreamCreateWithPriority(&V->s_gen, cudaStreamNonBlocking, lo_prio));
   }
   Exec x;
   x.hi = V->s_hi;
   x.lo = V->s_lo;
   x.mid = V->s_mid;
+  x.gen = V->s_gen;
   cr_status st = CR_OK;
-  for (auto* evs : {&x.ev_old, &x.ev_split, &x.ev_newr, &x.ev_crit, &x.ev_rest}) {
+  for (auto* evs : {&x.ev_old, &x.ev_split, &x.ev_newr, &x.ev_crit, &x.ev_rest, &x.ev_gen}) {
     evs->resize(nt);
     for (auto& e : *evs) cudaEventCreateWithFlags(&e, cudaEventDisableTiming);
   }
@@ -373,20 +405,24 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
     cudaStreamWaitEvent(x.hi, x.start, 0);
     cudaStreamWaitEvent(x.lo, x.start, 0);
     cudaStreamWaitEvent(x.mid, x.start, 0);
+    cudaStreamWaitEvent(x.gen, x.start, 0);
   }
   for (size_t q = 0; st == CR_OK && q < P.ops.size(); ++q) st = P.ops[q](x);
   cudaError_t e1 = cudaStreamSynchronize(x.hi);
   cudaError_t e2 = cudaStreamSynchronize(x.lo);
   cudaError_t e3 = cudaStreamSynchronize(x.mid);
+  cudaError_t e4 = cudaStreamSynchronize(x.gen);
+  if (st == CR_OK && e4 != cudaSuccess) st = cuda_fail(e4, "tile generation");
   if (st == CR_OK && e1 != cudaSuccess) st = cuda_fail(e1, "cholesky (critical stream)");
   if (st == CR_OK && e2 != cudaSuccess) st = cuda_fail(e2, "cholesky (bulk stream)");
   if (st == CR_OK && e3 != cudaSuccess) st = cuda_fail(e3, "cholesky (lookahead stream)");
-  for (auto* evs : {&x.ev_old, &x.ev_split, &x.ev_newr, &x.ev_crit, &x.ev_rest})
+  for (auto* evs : {&x.ev_old, &x.ev_split, &x.ev_newr, &x.ev_crit, &x.ev_rest, &x.ev_gen})
     for (auto& e : *evs) cudaEventDestroy(e);
   cudaEventDestroy(x.start);
   if (d_jobs) cudaFree(d_jobs);
   if (d_pairs) cudaFree(d_pairs);
   if (d_rows) cudaFree(d_rows);
+  if (d_gen) cudaFree(d_gen);
   return st;
 }
 

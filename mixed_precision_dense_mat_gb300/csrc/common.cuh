@@ -119,6 +119,7 @@ struct cr_tilemat_s {
   double* ws64 = nullptr;         // 2 * nt * nb * nb: FP64-class solve inputs (double-buffered by column parity)
   float* w32 = nullptr;           // 2 * nt * nb * nb: FP32 intermediate of FP16/FP32-class tiles (same)
   cudaStream_t s_hi = nullptr, s_lo = nullptr, s_mid = nullptr;   // critical chain / bulk updates / lookahead rows
+  cudaStream_t s_gen = nullptr;   // tile generation ahead of the factorisation
   double* minv = nullptr;         // 2 * nb * nb: inverse of the diagonal factor, by column parity
   double* minv_all = nullptr;     // nt * nb * nb: every diagonal factor's inverse (kept on request)
   double* scratch64 = nullptr;    // nb * nb: temporaries of the diagonal factorisation

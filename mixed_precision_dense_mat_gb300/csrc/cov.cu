@@ -342,26 +342,45 @@ __global__ void k_stats_reduce(const double* __restrict__ part, int ntiles, int 
   stats[STAT_W * t] = a; stats[STAT_W * t + 1] = b; stats[STAT_W * t + 2] = c; stats[STAT_W * t + 3] = e;
 }
 
-// Generation of s^2 V in each tile's class (Alg.2 step 12).  One CTA per (tile, 64-row
-// block).  Padding rows/columns are the identity (scaled by s^2).
-__global__ void __launch_bounds__(256) k_generate(const double* __restrict__ xy, int n, int nb, CovK p, double s2,
-                                                  float s2_hi, float s2_lo, TileView v) {
-  // one-dimensional grid: the (diagonal tile, row block) CTAs first, so that the FP64
-  // evaluations of the diagonal tiles start at once and run beside the other tiles' work
-  const int nrb = nb / 64, ndiag = v.nt * nrb;
-  const int b = blockIdx.x;
-  int i, j, rb;
-  if (b < ndiag) {
-    i = j = b / nrb;
-    rb = b % nrb;
-  } else {
-    const int o = (b - ndiag) / nrb;   // off-diagonal tile o in row order: row i holds i of them
-    rb = (b - ndiag) % nrb;
-    i = (int)((1.0f + sqrtf(8.0f * (float)o + 1.0f)) * 0.5f);
-    while (i * (i - 1) / 2 > o) --i;
-    while ((i + 1) * i / 2 <= o) ++i;
-    j = o - i * (i - 1) / 2;
+// Diagonal tile i (FP64 class), 16 of its rows: 8 from the top half and the mirrored 8 from
+// the bottom half (rows 8q .. 8q+7 and nb-8q-8 .. nb-8q-1), so that the nb/16 CTAs of a tile
+// evaluate equal parts of its lower triangle.  The upper part is stored as zeros; padding
+// rows and columns are the identity (scaled by s^2).
+__device__ __forceinline__ void generate_diag64(const double* __restrict__ xy, int n, int nb, const CovK& p, double s2,
+                                                const TileView& v, int i, int q) {
+  double* dst = v.pool64 + (size_t)v.i64[tidx(i, i)] * nb * nb;
+  for (int rr = 0; rr < 16; ++rr) {
+    const int r = rr < 8 ? 8 * q + rr : nb - 8 * (q + 1) + (rr - 8);
+    const int gi = i * nb + r;
+    for (int c = threadIdx.x; c < nb; c += blockDim.x) {
+      const int gj = i * nb + c;
+      double x = 0.0;
+      if (gi >= n || gj >= n) x = gi == gj ? s2 : 0.0;
+      else if (c <= r) x = cov_entry64(p, xy, gi, gj) * s2;
+      dst[(size_t)r * nb + c] = x;
+    }
   }
+}
+
+// Generation of s^2 V in each tile's class (Alg.2 step 12) over a tile list whose first
+// ndiag entries are diagonal tiles: CTAs 0 .. ndiag nb/16 - 1 take the diagonal tiles, nb/16
+// CTAs each (generate_diag64, the FP64 evaluations spread wide so that they finish early);
+// the others take one (tile, 64-row block) each, row block b % (nb/64) of the tile
+// (i, j) = (e >> 16, e & 0xffff), e = tiles[ndiag + b / (nb/64)].  The list fixes the issue
+// order: the factorisation lists column by column, so that each column is complete before
+// it is needed.  Padding rows/columns are the identity (scaled by s^2).
+__global__ void __launch_bounds__(256) k_generate(const double* __restrict__ xy, int n, int nb, CovK p, double s2,
+                                                  float s2_hi, float s2_lo, TileView v, const int* __restrict__ tiles,
+                                                  int ndiag) {
+  const int nrb = nb / 64, nsub = nb / 16;
+  if ((int)blockIdx.x < ndiag * nsub) {
+    generate_diag64(xy, n, nb, p, s2, v, tiles[blockIdx.x / nsub] >> 16, blockIdx.x % nsub);
+    return;
+  }
+  const int b = blockIdx.x - ndiag * nsub;
+  const int rb = b % nrb;
+  const int e = tiles[ndiag + b / nrb];
+  const int i = e >> 16, j = e & 0xffff;
   const int t = tidx(i, j);
   const int r0 = rb * 64;
   const int cls = v.cls[t];
@@ -635,14 +654,15 @@ cr_status refine_stats(cr_tilemat V, const std::vector<int>& list) {
   return fetch_stats(V);
 }
 
-cr_status convert_tiles(cr_tilemat V, cudaStream_t stream) {
-  const unsigned grid = (unsigned)V->ntiles * (V->nb / 64);
+cr_status convert_tiles(cr_tilemat V, const int* d_tiles, int count, int ndiag, cudaStream_t stream) {
+  if (count <= 0) return CR_OK;
+  const unsigned grid = (unsigned)ndiag * (V->nb / 16) + (unsigned)(count - ndiag) * (V->nb / 64);
   const size_t smem = (size_t)(V->nb + 64) * sizeof(float4);
   const double s2 = V->s * V->s;
   const df s2d = df_from_double(s2);
   {
     TimedScope ts("k_generate", stream);
-    k_generate<<<grid, 256, smem, stream>>>(V->xy, V->n, V->nb, V->covk, s2, s2d.hi, s2d.lo, V->view());
+    k_generate<<<grid, 256, smem, stream>>>(V->xy, V->n, V->nb, V->covk, s2, s2d.hi, s2d.lo, V->view(), d_tiles, ndiag);
   }
   CR_CHECK_LAUNCH("k_generate");
   return CR_OK;
