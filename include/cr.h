@@ -129,14 +129,16 @@ cr_status cr_tilemat_info(cr_tilemat V, int* n, int* nb, int* nt);
  * entries, Section V-D) in one pass without storing the matrix: the tiles are generated
  * in their precision classes by cr_potrf_adaptive, and cr_tilemat_to_dense / cr_krige
  * evaluate V in FP64 on demand.  For Matern nu in {1/2, 3/2, 5/2} the diagonal tiles'
- * statistics are evaluated in double-float arithmetic (about 1e-14 relative) and the
+ * statistics are evaluated in double-float arithmetic (as for cr_tile_stats) and the
  * off-diagonal tiles' in FP32 with a rigorous relative error bound (cr_tile_stats_records);
  * cr_precision_map and cr_tile_stats recompute exactly the records they need.  Other
  * covariances: every tile exact.  Asynchronous. */
 cr_status cr_cov_build(cr_tilemat V, const double* d_xy, const cr_cov_params* p, cr_stream stream);
 
 /* Per-tile statistics as NT x NT row-major host arrays (lower part filled), each exact
- * (about 1e-14 relative): tiles that still hold fast-pass records (below) are recomputed
+ * (double-float: about 1e-14 relative, up to ~3e-13 where entries sit at scaled distances
+ * near 80, beyond which FP64 takes over): tiles that still hold fast-pass records (below)
+ * are recomputed
  * first.  Synchronises the stream used by cr_cov_build.  Any output pointer may be NULL. */
 cr_status cr_tile_stats(cr_tilemat V, double* h_frob, double* h_vmin, double* h_vmax);
 

@@ -228,20 +228,25 @@ __global__ void __launch_bounds__(256) k_cov_stats(const double* __restrict__ xy
 }
 
 // Fast statistics of row block rbk of the off-diagonal tile (i, j), closed-form Matern
-// orders: every entry in FP32 (correctly rounded square root, expf within 2 ulp), distances
-// from the double-float coordinates.  Per entry, with u = 2^-24 and scaled distance x:
-//  - the computed x is off by at most 14 u x + (1/range) C 2^-42, C the largest |coordinate|
-//    (coordinate differences, squares, sum, root, scaling; the pairs' low words are rounded
-//    once more);
+// orders: every entry in FP32, distances from the double-float coordinates, the square root
+// as q rsqrtf(q) (rsqrtf within 2 ulp) and the exponential by __expf (within
+// 2 + floor(1.173 |x|) ulp, the documented bounds of both).  Per entry, with u = 2^-24 and
+// scaled distance x:
+//  - the computed x is off by at most 16.5 u x + (1/range) (C 2^-42 + 2^-70), C the largest
+//    |coordinate| (coordinate differences 6 u per component, 8.5 u for the distance; the
+//    squares and their sum 1 u after the root, the root 5 u, the scaling 2 u; the pairs' low
+//    words are rounded once more, and squares below the FP32 range lose at most 2^-70 of
+//    the distance);
 //  - |d log v / dx| <= 1 for these orders, so that error passes to v unchanged;
-//  - the exponential (4 u), the polynomial (4 u) and the products with sigma^2 (3 u) add 11 u.
+//  - the exponential ((4 + 2.35 x) u), the polynomial (4 u) and the products with sigma^2
+//    (3 u) add (11 + 2.35 x) u.
 // The sum of squares runs in FP32 per thread over K = 64 ceil(nb / 256) entries, in two
 // ranges (v^2 and (v 2^60)^2 for v < 2^-60, so that nothing underflows), so it adds K u to
 // the relative error of the sum (K u / 2 to its square root).  The partial's record holds
 // one relative bound E for its sum of squares' square root, min and max:
-//   E = 1.01 ((16 x_max + 16 + K) u + (1/range) C 2^-41) + 2^-40,
-// or infinity where the bound does not hold (x > 80, where expf leaves the normal range;
-// entries below 2^-100 or above 2^60, where products leave it).
+//   E = 1.01 ((20 x_max + 16 + K) u + (1/range) (C 2^-41 + 2^-69)) + 2^-40,
+// or infinity where the bound does not hold (x > 80, where the exponential leaves the
+// normal range; entries below 2^-120 or above 2^60, where products or squares leave it).
 __device__ __forceinline__ void stats_fast(const double* __restrict__ xy, int n, int nb, const CovK& p, int i, int j,
                                            int rbk, double* __restrict__ sp) {
   const int r0 = rbk * 64;
@@ -262,8 +267,9 @@ __device__ __forceinline__ void stats_fast(const double* __restrict__ xy, int n,
     for (int rr = 0; rr < rows; ++rr) {
       const float4 a = s_row[rr];
       const float dx = (a.x - b.x) + (a.y - b.y), dy = (a.z - b.z) + (a.w - b.w);
-      const float x = sqrtf(fmaf(dx, dx, dy * dy)) * invr;
-      const float e = expf(-x);
+      const float q2 = fmaf(dx, dx, dy * dy);
+      const float x = (q2 > 0.0f ? q2 * rsqrtf(q2) : 0.0f) * invr;
+      const float e = __expf(-x);
       const float poly = kind == 0 ? 1.0f : (kind == 1 ? 1.0f + x : fmaf(x * x, 1.0f / 3.0f, 1.0f + x));
       const float v = sig * poly * e;
       if (v >= small_lim) {
@@ -297,9 +303,9 @@ __device__ __forceinline__ void stats_fast(const double* __restrict__ xy, int n,
       cm = fmax(cm, red[4][q]);
     }
     const double u = 0x1.0p-24, K = 64.0 * ((nb + 255) / 256);
-    double E = 1.01 * ((16.0 * xm + 16.0 + K) * u + (double)p.invr_hi * cm * 0x1.0p-41) + 0x1.0p-40;
+    double E = 1.01 * ((20.0 * xm + 16.0 + K) * u + (double)p.invr_hi * (cm * 0x1.0p-41 + 0x1.0p-69)) + 0x1.0p-40;
     const bool empty = !(b <= cc);   // no valid entry in this row block
-    if (!empty && (!(xm <= 80.0) || !(b >= 0x1.0p-100) || !(cc <= 0x1.0p60))) E = INFINITY;
+    if (!empty && (!(xm <= 80.0) || !(b >= 0x1.0p-120) || !(cc <= 0x1.0p60))) E = INFINITY;
     sp[0] = a; sp[1] = b; sp[2] = cc; sp[3] = E;
   }
 }
