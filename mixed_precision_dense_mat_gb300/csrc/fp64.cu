@@ -144,12 +144,34 @@ __global__ void __launch_bounds__(256) k_split_tile(const double* __restrict__ s
   }
 }
 
+// FP64 -> FP32 rounded to nearest (ties to even) from the IEEE 754 fields, in integer
+// arithmetic: GB300 issues the F2F conversion on its slow FP64/conversion pipe.  Results
+// below 2^-126 come out as signed zero (the FP16 pairs made from them are zero either way:
+// FP16 holds nothing below 2^-24); infinities and NaN map to infinity and NaN.
+__device__ __forceinline__ float narrow(double x) {
+  const unsigned long long b = (unsigned long long)__double_as_longlong(x);
+  const unsigned sign = (unsigned)(b >> 32) & 0x80000000u;
+  const int e = (int)((b >> 52) & 0x7ff);
+  const unsigned long long frac = b & 0xfffffffffffffull;
+  if (e == 0x7ff) return __uint_as_float(sign | 0x7f800000u | (frac ? 0x400000u : 0u));
+  const int fe = e - 1023 + 127;
+  if (fe < 1) return __uint_as_float(sign);
+  if (fe > 254) return __uint_as_float(sign | 0x7f800000u);
+  const unsigned m = (unsigned)(frac >> 29);
+  const unsigned rest = (unsigned)(frac & 0x1fffffffull);   // the 29 dropped bits
+  const unsigned up = (rest > 0x10000000u || (rest == 0x10000000u && (m & 1u))) ? 1u : 0u;
+  // a carry out of the fraction raises the exponent, as rounding should
+  return __uint_as_float((sign | ((unsigned)fe << 23) | m) + up);
+}
+
 // Splits the inverse factor and the diagonal factor of one column in one launch:
 //  - eM with max|M| 2^eM < 2^14 (status[2] = eM), from the running maximum the diagonal
 //    executor accumulated (IEEE bits of max |M|), and the FP16 high/low parts of M 2^eM;
 //  - the FP16 high/low parts of the diagonal factor L (lower part; zero above).
 // Elements [0, nb^2) are M, [nb^2, 2 nb^2) are L; both through FP32, whose 24 bits cover
-// everything an FP16 pair can hold.
+// everything an FP16 pair can hold.  Each thread takes pairs of adjacent elements (nb is
+// even, so a pair never straddles a row or the M / L boundary): 16-byte loads, packed
+// FP16 conversions and 4-byte stores.
 __global__ void __launch_bounds__(256) k_split_diag(const double* __restrict__ Minv, const double* __restrict__ L, int nb,
                                                     const unsigned long long* __restrict__ amax, __half* __restrict__ mh,
                                                     __half* __restrict__ ml, __half* __restrict__ lh, __half* __restrict__ ll,
@@ -159,26 +181,31 @@ __global__ void __launch_bounds__(256) k_split_diag(const double* __restrict__ M
   const int e = (bits == 0 || ef == 0 || ef == 0x7ff) ? 0 : 14 - (ef - 1022);
   if (blockIdx.x == 0 && threadIdx.x == 0) status[2] = e;
   const float sc = ldexpf(1.0f, e);
-  const size_t count = (size_t)nb * nb;
-  for (size_t idx = blockIdx.x * 256 + threadIdx.x; idx < 2 * count; idx += (size_t)gridDim.x * 256) {
-    float x;
-    __half *h, *l;
-    size_t o;
-    if (idx < count) {
-      o = idx;
-      x = (float)Minv[o] * sc;
-      h = mh;
-      l = ml;
+  const size_t half_count = (size_t)nb * nb / 2;
+  for (size_t pidx = blockIdx.x * 256 + threadIdx.x; pidx < 2 * half_count; pidx += (size_t)gridDim.x * 256) {
+    float x0, x1;
+    __half2 *h, *l;
+    size_t q;
+    if (pidx < half_count) {
+      q = pidx;
+      const double2 v = reinterpret_cast<const double2*>(Minv)[q];
+      x0 = narrow(v.x) * sc;
+      x1 = narrow(v.y) * sc;
+      h = reinterpret_cast<__half2*>(mh);
+      l = reinterpret_cast<__half2*>(ml);
     } else {
-      o = idx - count;
-      const int r = (int)(o / nb), c = (int)(o % nb);
-      x = c > r ? 0.0f : (float)L[o];
-      h = lh;
-      l = ll;
+      q = pidx - half_count;
+      const int r = (int)(2 * q / nb), c = (int)(2 * q % nb);
+      const double2 v = reinterpret_cast<const double2*>(L)[q];
+      x0 = c > r ? 0.0f : narrow(v.x);
+      x1 = c + 1 > r ? 0.0f : narrow(v.y);
+      h = reinterpret_cast<__half2*>(lh);
+      l = reinterpret_cast<__half2*>(ll);
     }
-    const __half hv = __float2half_rn(x);
-    h[o] = hv;
-    l[o] = __float2half_rn(x - __half2float(hv));
+    const __half2 hv = __floats2half2_rn(x0, x1);
+    const float2 hf = __half22float2(hv);
+    h[q] = hv;
+    l[q] = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
   }
 }
 
