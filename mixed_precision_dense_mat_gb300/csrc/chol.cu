@@ -88,7 +88,7 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
   double* dpub = V->diag_pub;
   const size_t dpub_bytes = diag_pub_doubles(nb, V->diag_db) * sizeof(double);
   // Tile generation on its own stream, column by column in ranges of doubling width
-  // ([0,1), [1,2), [2,4), [4,8), ...), diagonal tiles first in each range: the factorisation
+  // ([0,1), [1,3), [3,7), [7,15), ...), diagonal tiles first in each range: the factorisation
   // of column j waits only for its range, so it starts after the first column's tiles
   // instead of after all of them.
   if (nt > 32767) return fail(CR_ERR_ARG, "cr_potrf_adaptive: more than 32767 tile rows");
