@@ -267,6 +267,9 @@ extern "C" cr_status cr_tilemat_destroy(cr_tilemat V) {
   if (V->s_lo) cudaStreamDestroy(V->s_lo);
   if (V->s_mid) cudaStreamDestroy(V->s_mid);
   if (V->s_gen) cudaStreamDestroy(V->s_gen);
+  for (cudaEvent_t e : V->sched_ev) cudaEventDestroy(e);
+  dfree(V->sched_ints);
+  if (V->sched_jobs) cudaFree(V->sched_jobs);
   delete V;
   return CR_OK;
 }

@@ -105,9 +105,32 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
     gen_off.push_back((int)gen_list.size());
   }
   const int n_ranges = (int)gen_off.size() - 1;
-  int* d_gen = nullptr;
-  CR_CUDA(cudaMalloc(&d_gen, gen_list.size() * sizeof(int)));
-  CR_CUDA(cudaMemcpy(d_gen, gen_list.data(), gen_list.size() * sizeof(int), cudaMemcpyHostToDevice));
+  // rows solved on the tensor cores, per column
+  std::vector<int> rows_flat;
+  std::vector<int> rows_off(nt + 1, 0);
+  for (int j = 0; j < nt; ++j) {
+    rows_off[j] = (int)rows_flat.size();
+    for (int i = j + 1; i < nt; ++i)
+      if (cls[tidx(i, j)] != CR_PREC_FP64) rows_flat.push_back(i);
+  }
+  rows_off[nt] = (int)rows_flat.size();
+  // both lists in one device buffer kept by the tile matrix (the previous call's kernels are
+  // complete: every call ends by synchronising its streams)
+  const size_t n_ints = rows_flat.size() + gen_list.size();
+  if (n_ints > V->sched_ints_cap) {
+    if (V->sched_ints) cudaFree(V->sched_ints);
+    V->sched_ints = nullptr;
+    V->sched_ints_cap = 0;
+    CR_CUDA(cudaMalloc(&V->sched_ints, n_ints * sizeof(int)));
+    V->sched_ints_cap = n_ints;
+  }
+  int* d_rows = V->sched_ints;
+  int* d_gen = V->sched_ints + rows_flat.size();
+  {
+    std::vector<int> both(rows_flat);
+    both.insert(both.end(), gen_list.begin(), gen_list.end());
+    CR_CUDA(cudaMemcpyAsync(V->sched_ints, both.data(), n_ints * sizeof(int), cudaMemcpyHostToDevice, caller));
+  }
   P.ops.push_back([=](Exec& x) -> cr_status {
     CR_TRY(status_init_launch(status, x.hi));
     // both parities of the executor's flags and abs-max start cleared
@@ -122,20 +145,6 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
     return CR_OK;
   });
 
-  // rows solved on the tensor cores, per column
-  std::vector<int> rows_flat;
-  std::vector<int> rows_off(nt + 1, 0);
-  for (int j = 0; j < nt; ++j) {
-    rows_off[j] = (int)rows_flat.size();
-    for (int i = j + 1; i < nt; ++i)
-      if (cls[tidx(i, j)] != CR_PREC_FP64) rows_flat.push_back(i);
-  }
-  rows_off[nt] = (int)rows_flat.size();
-  int* d_rows = nullptr;
-  if (!rows_flat.empty()) {
-    CR_CUDA(cudaMalloc(&d_rows, rows_flat.size() * sizeof(int)));
-    CR_CUDA(cudaMemcpy(d_rows, rows_flat.data(), rows_flat.size() * sizeof(int), cudaMemcpyHostToDevice));
-  }
 
   TcParams base{};
   base.v = V->view();
@@ -381,16 +390,38 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
   x.mid = V->s_mid;
   x.gen = V->s_gen;
   cr_status st = CR_OK;
-  for (auto* evs : {&x.ev_old, &x.ev_split, &x.ev_newr, &x.ev_crit, &x.ev_rest, &x.ev_gen}) {
-    evs->resize(nt);
-    for (auto& e : *evs) cudaEventCreateWithFlags(&e, cudaEventDisableTiming);
+  // events: created once per tile matrix (6 per column and the start event)
+  if (V->sched_ev.size() != 6 * (size_t)nt + 1) {
+    for (cudaEvent_t e : V->sched_ev) cudaEventDestroy(e);
+    V->sched_ev.assign(6 * (size_t)nt + 1, nullptr);
+    for (auto& e : V->sched_ev) CR_CUDA(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
   }
-  cudaEventCreateWithFlags(&x.start, cudaEventDisableTiming);
-  DJob* d_jobs = nullptr;
-  DPair* d_pairs = nullptr;
-  if (!P.jobs.empty() && cudaMalloc(&d_jobs, P.jobs.size() * sizeof(DJob)) != cudaSuccess) st = fail(CR_ERR_NOMEM, "job list");
-  if (st == CR_OK && !P.pairs.empty() && cudaMalloc(&d_pairs, P.pairs.size() * sizeof(DPair)) != cudaSuccess)
-    st = fail(CR_ERR_NOMEM, "pair list");
+  {
+    size_t q = 0;
+    for (auto* evs : {&x.ev_old, &x.ev_split, &x.ev_newr, &x.ev_crit, &x.ev_rest, &x.ev_gen}) {
+      evs->assign(V->sched_ev.begin() + q, V->sched_ev.begin() + q + nt);
+      q += nt;
+    }
+    x.start = V->sched_ev[q];
+  }
+  // job and pair lists in one device buffer kept by the tile matrix
+  const size_t jobs_bytes = (P.jobs.size() * sizeof(DJob) + 255) & ~(size_t)255;
+  const size_t need = jobs_bytes + P.pairs.size() * sizeof(DPair);
+  if (need > V->sched_jobs_cap) {
+    if (V->sched_jobs) cudaFree(V->sched_jobs);
+    V->sched_jobs = nullptr;
+    V->sched_jobs_cap = 0;
+    if (cudaMalloc(&V->sched_jobs, need) != cudaSuccess) {
+      V->sched_jobs = nullptr;
+      st = fail(CR_ERR_NOMEM, "job list");
+    } else {
+      V->sched_jobs_cap = need;
+    }
+  }
+  DJob* d_jobs = P.jobs.empty() || !V->sched_jobs ? nullptr : reinterpret_cast<DJob*>(V->sched_jobs);
+  DPair* d_pairs = P.pairs.empty() || !V->sched_jobs
+                       ? nullptr
+                       : reinterpret_cast<DPair*>(reinterpret_cast<char*>(V->sched_jobs) + jobs_bytes);
   if (st == CR_OK && d_jobs)
     if (cudaMemcpyAsync(d_jobs, P.jobs.data(), P.jobs.size() * sizeof(DJob), cudaMemcpyHostToDevice, caller) != cudaSuccess)
       st = fail(CR_ERR_CUDA, "job upload");
@@ -416,13 +447,6 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
   if (st == CR_OK && e1 != cudaSuccess) st = cuda_fail(e1, "cholesky (critical stream)");
   if (st == CR_OK && e2 != cudaSuccess) st = cuda_fail(e2, "cholesky (bulk stream)");
   if (st == CR_OK && e3 != cudaSuccess) st = cuda_fail(e3, "cholesky (lookahead stream)");
-  for (auto* evs : {&x.ev_old, &x.ev_split, &x.ev_newr, &x.ev_crit, &x.ev_rest, &x.ev_gen})
-    for (auto& e : *evs) cudaEventDestroy(e);
-  cudaEventDestroy(x.start);
-  if (d_jobs) cudaFree(d_jobs);
-  if (d_pairs) cudaFree(d_pairs);
-  if (d_rows) cudaFree(d_rows);
-  if (d_gen) cudaFree(d_gen);
   return st;
 }
 

@@ -120,6 +120,12 @@ struct cr_tilemat_s {
   float* w32 = nullptr;           // 2 * nt * nb * nb: FP32 intermediate of FP16/FP32-class tiles (same)
   cudaStream_t s_hi = nullptr, s_lo = nullptr, s_mid = nullptr;   // critical chain / bulk updates / lookahead rows
   cudaStream_t s_gen = nullptr;   // tile generation ahead of the factorisation
+  // the factorisation schedule's events and device lists, kept across calls (sized by capacity)
+  std::vector<cudaEvent_t> sched_ev;
+  int* sched_ints = nullptr;      // solve rows, then the generation list
+  size_t sched_ints_cap = 0;
+  void* sched_jobs = nullptr;     // job list, then the pair list
+  size_t sched_jobs_cap = 0;
   double* minv = nullptr;         // 2 * nb * nb: inverse of the diagonal factor, by column parity
   double* minv_all = nullptr;     // nt * nb * nb: every diagonal factor's inverse (kept on request)
   double* scratch64 = nullptr;    // nb * nb: temporaries of the diagonal factorisation
