@@ -240,13 +240,15 @@ __global__ void __launch_bounds__(256) k_cov_stats(const double* __restrict__ xy
 //  - |d log v / dx| <= 1 for these orders, so that error passes to v unchanged;
 //  - the exponential ((4 + 2.35 x) u), the polynomial (4 u) and the products with sigma^2
 //    (3 u) add (11 + 2.35 x) u.
-// The sum of squares runs in FP32 per thread over K = 64 ceil(nb / 256) entries, in two
-// ranges (v^2 and (v 2^60)^2 for v < 2^-60, so that nothing underflows), so it adds K u to
-// the relative error of the sum (K u / 2 to its square root).  The partial's record holds
-// one relative bound E for its sum of squares' square root, min and max:
+// The sum of squares runs in FP32 over 64 ceil(nb / 256) entries per thread and then over the
+// CTA (12 more additions deep), in two ranges (v^2 and (v 2^60)^2 for v < 2^-60, so that
+// nothing underflows), so it adds K u to the relative error of the sum (K u / 2 to its
+// square root), K = 64 ceil(nb / 256) + 12.  The partial's record holds one relative bound
+// E for its sum of squares' square root, min and max:
 //   E = 1.01 ((20 x_max + 16 + K) u + (1/range) (C 2^-41 + 2^-69)) + 2^-40,
 // or infinity where the bound does not hold (x > 80, where the exponential leaves the
-// normal range; entries below 2^-120 or above 2^60, where products or squares leave it).
+// normal range; entries below 2^-120 or above 2^56, where products, squares or their sums
+// leave it).
 __device__ __forceinline__ void stats_fast(const double* __restrict__ xy, int n, int nb, const CovK& p, int i, int j,
                                            int rbk, double* __restrict__ sp) {
   const int r0 = rbk * 64;
@@ -283,29 +285,33 @@ __device__ __forceinline__ void stats_fast(const double* __restrict__ xy, int n,
       xmx = fmaxf(xmx, x);
     }
   }
-  double sq = (double)big + (double)small * 0x1.0p-120;
-  double dmn = vmn, dmx = vmx, dxm = xmx, dcm = cmax;
+  // CTA reduction in FP32 (GB300 issues FP64 arithmetic, comparisons and conversions on its
+  // slow FP64 pipe): the extrema are exact, and the two sums gain at most 5 u (warp tree)
+  // and 7 u (over the 8 warps) of relative error, for 12 + K u in all
   for (int o = 16; o > 0; o >>= 1) {
-    sq += __shfl_down_sync(0xffffffffu, sq, o);
-    dmn = fmin(dmn, __shfl_down_sync(0xffffffffu, dmn, o));
-    dmx = fmax(dmx, __shfl_down_sync(0xffffffffu, dmx, o));
-    dxm = fmax(dxm, __shfl_down_sync(0xffffffffu, dxm, o));
-    dcm = fmax(dcm, __shfl_down_sync(0xffffffffu, dcm, o));
+    big += __shfl_down_sync(0xffffffffu, big, o);
+    small += __shfl_down_sync(0xffffffffu, small, o);
+    vmn = fminf(vmn, __shfl_down_sync(0xffffffffu, vmn, o));
+    vmx = fmaxf(vmx, __shfl_down_sync(0xffffffffu, vmx, o));
+    xmx = fmaxf(xmx, __shfl_down_sync(0xffffffffu, xmx, o));
+    cmax = fmaxf(cmax, __shfl_down_sync(0xffffffffu, cmax, o));
   }
-  __shared__ double red[5][8];
+  __shared__ float red[6][8];
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  if (l == 0) { red[0][w] = sq; red[1][w] = dmn; red[2][w] = dmx; red[3][w] = dxm; red[4][w] = dcm; }
+  if (l == 0) { red[0][w] = big; red[1][w] = small; red[2][w] = vmn; red[3][w] = vmx; red[4][w] = xmx; red[5][w] = cmax; }
   __syncthreads();
   if (threadIdx.x == 0) {
-    double a = 0.0, b = INFINITY, cc = -INFINITY, xm = 0.0, cm = 0.0;
+    float fb = 0.0f, fs = 0.0f, fmn = INFINITY, fmx = -INFINITY, fxm = 0.0f, fcm = 0.0f;
     for (int q = 0; q < (int)(blockDim.x >> 5); ++q) {
-      a += red[0][q]; b = fmin(b, red[1][q]); cc = fmax(cc, red[2][q]); xm = fmax(xm, red[3][q]);
-      cm = fmax(cm, red[4][q]);
+      fb += red[0][q]; fs += red[1][q]; fmn = fminf(fmn, red[2][q]); fmx = fmaxf(fmx, red[3][q]);
+      fxm = fmaxf(fxm, red[4][q]); fcm = fmaxf(fcm, red[5][q]);
     }
-    const double u = 0x1.0p-24, K = 64.0 * ((nb + 255) / 256);
+    const double a = (double)fb + (double)fs * 0x1.0p-120, b = fmn, cc = fmx, xm = fxm, cm = fcm;
+    const double u = 0x1.0p-24, K = 64.0 * ((nb + 255) / 256) + 12.0;
     double E = 1.01 * ((20.0 * xm + 16.0 + K) * u + (double)p.invr_hi * (cm * 0x1.0p-41 + 0x1.0p-69)) + 0x1.0p-40;
     const bool empty = !(b <= cc);   // no valid entry in this row block
-    if (!empty && (!(xm <= 80.0) || !(b >= 0x1.0p-120) || !(cc <= 0x1.0p60))) E = INFINITY;
+    // entries up to 2^56 keep every partial sum of squares below 2^127 (no FP32 overflow)
+    if (!empty && (!(xm <= 80.0) || !(b >= 0x1.0p-120) || !(cc <= 0x1.0p56))) E = INFINITY;
     sp[0] = a; sp[1] = b; sp[2] = cc; sp[3] = E;
   }
 }
