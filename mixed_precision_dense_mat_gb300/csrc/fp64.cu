@@ -228,7 +228,9 @@ cr_status split_tile_launch(const double* src, int nb, __half* hi, __half* lo, i
 }
 cr_status split_diag_launch(const double* Minv, const double* L, int nb, const unsigned long long* amax, __half* mh, __half* ml,
                             __half* lh, __half* ll, int* status, cudaStream_t s) {
-  k_split_diag<<<256, 256, 0, s>>>(Minv, L, nb, amax, mh, ml, lh, ll, status);
+  // one element pair per thread: the kernel is latency-bound, so every load is in flight at once
+  const unsigned grid = (unsigned)(((size_t)nb * nb + 255) / 256);   // 2 nb^2 / 2 pairs, 256 per CTA
+  k_split_diag<<<grid, 256, 0, s>>>(Minv, L, nb, amax, mh, ml, lh, ll, status);
   CR_CHECK_LAUNCH("k_split_diag");
   return CR_OK;
 }
