@@ -100,6 +100,42 @@ def test_headline_workload_full_size(lib):
     V.close()
 
 
+def test_headline_fast_statistics_full_size(lib):
+    """At the benchmark size and in the bench's call sequence (no cr_tile_stats before the
+    map): the FP32 statistics records hold their stated bounds against the oracle on sampled
+    off-diagonal tiles, and the map, checks and scale taken on them (with the policy's exact
+    recomputations) equal those taken after making every record exact."""
+    w = inputgen.WORKLOADS["c"]
+    rng = np.random.default_rng(2)
+    xy = inputgen.workload_locations(w)
+    n, nb = w.n, w.nb
+    V = lib.TileMat(n, nb)
+    lib.cov_build(V, dev(xy), w.family, w.sigma2, w.beta, w.nu, nugget=w.nugget)
+    f, mn, mx, err = lib.tile_stats_records(V)
+    nt = f.shape[0]
+    off = np.tril(np.ones((nt, nt), dtype=bool), -1)
+    assert np.all(err[off] > 0) and np.all(err[off] < 1e-3)
+    for _ in range(16):
+        i = int(rng.integers(1, nt))
+        j = int(rng.integers(0, i))
+        T = oracle.covariance_matrix(xy, w.family, w.sigma2, w.beta, w.nu, w.nugget, w.n_pred, w.tau2,
+                                     rows=slice(i * nb, min(n, (i + 1) * nb)), cols=slice(j * nb, min(n, (j + 1) * nb)))
+        for got, ref in ((f[i, j], np.linalg.norm(T)), (mn[i, j], T.min()), (mx[i, j], T.max())):
+            assert abs(got - ref) <= err[i, j] * abs(ref), (i, j, got, ref, err[i, j])
+    pm_fast, info_fast = lib.precision_map(V, amp=True, fixedacc=w.fixedacc)
+    V.close()
+    torch.cuda.empty_cache()
+    V = lib.TileMat(n, nb)
+    lib.cov_build(V, dev(xy), w.family, w.sigma2, w.beta, w.nu, nugget=w.nugget)
+    lib.tile_stats(V)   # every record exact
+    pm_exact, info_exact = lib.precision_map(V, amp=True, fixedacc=w.fixedacc)
+    V.close()
+    np.testing.assert_array_equal(pm_fast, pm_exact)
+    for k in info_fast:
+        a, b = info_fast[k], info_exact[k]
+        assert (a == b) or (np.isnan(a) and np.isnan(b)), (k, a, b)
+
+
 def test_strong_correlation_workload_full_size(lib):
     w = inputgen.WORKLOADS["b"]
     rng = np.random.default_rng(1)
