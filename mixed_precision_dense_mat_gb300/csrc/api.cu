@@ -149,7 +149,8 @@ static void dfree(T*& p) {
 }
 
 cr_status free_class_storage(cr_tilemat V) {
-  dfree(V->d_cls); dfree(V->d_i64); dfree(V->d_i32); dfree(V->d_hi16); dfree(V->d_lo16);
+  dfree(V->d_tables);
+  V->d_cls = nullptr; V->d_i64 = V->d_i32 = V->d_hi16 = V->d_lo16 = nullptr;
   dfree(V->pool64); dfree(V->pool32); dfree(V->pool16); dfree(V->ws64); dfree(V->w32);
   V->cap64 = V->cap32 = V->cap16 = V->cap_ws64 = V->cap_w32 = 0;
   V->mapped = false;
@@ -262,7 +263,7 @@ extern "C" cr_status cr_tilemat_destroy(cr_tilemat V) {
   cudaDeviceSynchronize();
   free_class_storage(V);
   dfree(V->b16); dfree(V->bnorm_part); dfree(V->minv_all); dfree(V->diag_tasks); dfree(V->diag_flags); dfree(V->diag_pub); dfree(V->minv_part);
-  dfree(V->xy); dfree(V->stat_part); dfree(V->d_refine); dfree(V->stats); dfree(V->minv); dfree(V->scratch64); dfree(V->d_status);
+  dfree(V->xy); dfree(V->stat_part); dfree(V->d_refine); dfree(V->refine_part); dfree(V->stats); dfree(V->minv); dfree(V->scratch64); dfree(V->d_status);
   if (V->s_hi) cudaStreamDestroy(V->s_hi);
   if (V->s_lo) cudaStreamDestroy(V->s_lo);
   if (V->s_mid) cudaStreamDestroy(V->s_mid);

@@ -99,6 +99,7 @@ struct cr_tilemat_s {
   std::vector<double> h_stat_err;  // per tile: relative error bound of its statistics (0: exact)
   std::vector<char> h_stat_exact;  // per tile: statistics from the exact (double-float / FP64) pass
   int* d_refine = nullptr;         // tile list of the exact pass (ntiles ints)
+  double* refine_part = nullptr;   // its partials: ntiles x (nb/16) x STAT_W
   bool stats_on_host = false;
   // precision map and class storage
   bool mapped = false;
@@ -111,7 +112,8 @@ struct cr_tilemat_s {
   int n64 = 0, n32 = 0, n16 = 0;  // slots per pool
   size_t cap64 = 0, cap32 = 0, cap16 = 0, cap_ws64 = 0, cap_w32 = 0;   // allocated elements, kept across maps
   int ws_hi0 = 0, ws_lo0 = 0, minv_hi = 0, minv_lo = 0;
-  int8_t* d_cls = nullptr;
+  int* d_tables = nullptr;        // 4 ntiles ints (i64, i32, hi16, lo16) then ntiles class bytes
+  int8_t* d_cls = nullptr;        // views into d_tables
   int *d_i64 = nullptr, *d_i32 = nullptr, *d_hi16 = nullptr, *d_lo16 = nullptr;
   double* pool64 = nullptr;
   float* pool32 = nullptr;

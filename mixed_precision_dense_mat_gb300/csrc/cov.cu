@@ -135,13 +135,13 @@ __device__ __forceinline__ float load_tile_points(const double* __restrict__ xy,
   return cmax;
 }
 
-// Exact statistics of row block rbk of tile (i, j): partial sum of squares, min, max and 0
-// (an exact partial has no error bound) over valid entries, STAT_W doubles at sp.  Nothing
-// is stored.
-template <bool DF>
+// Exact statistics of row block rbk (ROWS rows, ROWS <= 64) of tile (i, j): partial sum of
+// squares, min, max and 0 (an exact partial has no error bound) over valid entries, STAT_W
+// doubles at sp.  Nothing is stored.
+template <bool DF, int ROWS>
 __device__ __forceinline__ void stats_exact(const double* __restrict__ xy, int n, int nb, const CovK& p, int i, int j,
                                             int rbk, double* __restrict__ sp) {
-  const int r0 = rbk * 64;
+  const int r0 = rbk * ROWS;
   extern __shared__ float4 s_pts[];
   float4* s_col = s_pts;
   float4* s_row = s_pts + nb;
@@ -162,7 +162,7 @@ __device__ __forceinline__ void stats_exact(const double* __restrict__ xy, int n
   // a broadcast read): no per-entry index division
   for (int c = threadIdx.x; c < nb; c += blockDim.x)
 #pragma unroll 1
-  for (int rr = 0; rr < 64; ++rr) {
+  for (int rr = 0; rr < ROWS; ++rr) {
     const int r = r0 + rr;
     const int gi = i * nb + r, gj = j * nb + c;
     if (gi >= n || gj >= n) continue;
@@ -217,26 +217,30 @@ __device__ __forceinline__ void stats_exact(const double* __restrict__ xy, int n
 }
 
 // Exact statistics pass over a tile list (every lower tile in order without one): one CTA
-// per (listed tile, 64-row block).
-template <bool DF>
+// per (listed tile, ROWS-row block).  Partials are indexed by tile, or by list position when
+// by_list is set (the policy's recomputations, whose 16-row blocks keep each CTA short).
+template <bool DF, int ROWS>
 __global__ void __launch_bounds__(256) k_cov_stats(const double* __restrict__ xy, int n, int nb, CovK p,
-                                                   double* __restrict__ stat_part, const int* __restrict__ tiles) {
+                                                   double* __restrict__ stat_part, const int* __restrict__ tiles,
+                                                   int by_list) {
   const int tile = tiles ? tiles[blockIdx.x] : blockIdx.x;
   int i, j;
   tile_of(tile, i, j);
-  stats_exact<DF>(xy, n, nb, p, i, j, blockIdx.y, stat_part + ((size_t)tile * gridDim.y + blockIdx.y) * STAT_W);
+  const size_t slot = by_list ? blockIdx.x : tile;
+  stats_exact<DF, ROWS>(xy, n, nb, p, i, j, blockIdx.y, stat_part + (slot * gridDim.y + blockIdx.y) * STAT_W);
 }
 
 // Fast statistics of row block rbk of the off-diagonal tile (i, j), closed-form Matern
-// orders: every entry in FP32, distances from the double-float coordinates, the square root
+// orders: every entry in FP32, distances from the FP32 roundings of the coordinates (the high
+// words of their double-float pairs), the square root
 // as q rsqrtf(q) (rsqrtf within 2 ulp) and the exponential by __expf (within
 // 2 + floor(1.173 |x|) ulp, the documented bounds of both).  Per entry, with u = 2^-24 and
 // scaled distance x:
-//  - the computed x is off by at most 16.5 u x + (1/range) (C 2^-42 + 2^-70), C the largest
-//    |coordinate| (coordinate differences 6 u per component, 8.5 u for the distance; the
-//    squares and their sum 1 u after the root, the root 5 u, the scaling 2 u; the pairs' low
-//    words are rounded once more, and squares below the FP32 range lose at most 2^-70 of
-//    the distance);
+//  - the computed x is off by at most 16.5 u x + (1/range) (C 2^-22 + 2^-70), C the largest
+//    |coordinate| (each FP32 coordinate is within 2^-24 C, so each difference within
+//    2^-23 C, and the distance within 2^-22.5 C; the differences' roundings 1.5 u, the
+//    squares and their sum 1 u after the root, the root 5 u, the scaling 2 u, with margin;
+//    squares below the FP32 range lose at most 2^-70 of the distance);
 //  - |d log v / dx| <= 1 for these orders, so that error passes to v unchanged;
 //  - the exponential ((4 + 2.35 x) u), the polynomial (4 u) and the products with sigma^2
 //    (3 u) add (11 + 2.35 x) u.
@@ -245,7 +249,7 @@ __global__ void __launch_bounds__(256) k_cov_stats(const double* __restrict__ xy
 // nothing underflows), so it adds K u to the relative error of the sum (K u / 2 to its
 // square root), K = 64 ceil(nb / 256) + 12.  The partial's record holds one relative bound
 // E for its sum of squares' square root, min and max:
-//   E = 1.01 ((20 x_max + 16 + K) u + (1/range) (C 2^-41 + 2^-69)) + 2^-40,
+//   E = 1.01 ((20 x_max + 16 + K) u + (1/range) (C 2^-21 + 2^-69)) + 2^-40,
 // or infinity where the bound does not hold (x > 80, where the exponential leaves the
 // normal range; entries below 2^-120 or above 2^56, where products, squares or their sums
 // leave it).
@@ -268,7 +272,7 @@ __device__ __forceinline__ void stats_fast(const double* __restrict__ xy, int n,
 #pragma unroll 4
     for (int rr = 0; rr < rows; ++rr) {
       const float4 a = s_row[rr];
-      const float dx = (a.x - b.x) + (a.y - b.y), dy = (a.z - b.z) + (a.w - b.w);
+      const float dx = a.x - b.x, dy = a.z - b.z;
       const float q2 = fmaf(dx, dx, dy * dy);
       const float x = (q2 > 0.0f ? q2 * rsqrtf(q2) : 0.0f) * invr;
       const float e = __expf(-x);
@@ -308,7 +312,7 @@ __device__ __forceinline__ void stats_fast(const double* __restrict__ xy, int n,
     }
     const double a = (double)fb + (double)fs * 0x1.0p-120, b = fmn, cc = fmx, xm = fxm, cm = fcm;
     const double u = 0x1.0p-24, K = 64.0 * ((nb + 255) / 256) + 12.0;
-    double E = 1.01 * ((20.0 * xm + 16.0 + K) * u + (double)p.invr_hi * (cm * 0x1.0p-41 + 0x1.0p-69)) + 0x1.0p-40;
+    double E = 1.01 * ((20.0 * xm + 16.0 + K) * u + (double)p.invr_hi * (cm * 0x1.0p-21 + 0x1.0p-69)) + 0x1.0p-40;
     const bool empty = !(b <= cc);   // no valid entry in this row block
     // entries up to 2^56 keep every partial sum of squares below 2^127 (no FP32 overflow)
     if (!empty && (!(xm <= 80.0) || !(b >= 0x1.0p-120) || !(cc <= 0x1.0p56))) E = INFINITY;
@@ -336,19 +340,20 @@ __global__ void __launch_bounds__(256) k_cov_stats_split(const double* __restric
     j = o - i * (i - 1) / 2;
   }
   double* sp = stat_part + ((size_t)tidx(i, j) * nrb + rbk) * STAT_W;
-  if (i == j) stats_exact<true>(xy, n, nb, p, i, j, rbk, sp);
+  if (i == j) stats_exact<true, 64>(xy, n, nb, p, i, j, rbk, sp);
   else stats_fast(xy, n, nb, p, i, j, rbk, sp);
 }
 
 // Per-tile reduction of the partials of the tiles in the list (all tiles without one).
 __global__ void k_stats_reduce(const double* __restrict__ part, int ntiles, int nrb, double* __restrict__ stats,
-                               const int* __restrict__ tiles) {
+                               const int* __restrict__ tiles, int by_list) {
   const int q0 = blockIdx.x * blockDim.x + threadIdx.x;
   if (q0 >= ntiles) return;
   const int t = tiles ? tiles[q0] : q0;
+  const size_t slot = by_list ? q0 : t;   // where the partials are
   double a = 0.0, b = INFINITY, c = -INFINITY, e = 0.0;
   for (int q = 0; q < nrb; ++q) {
-    const double* sp = part + ((size_t)t * nrb + q) * STAT_W;
+    const double* sp = part + (slot * nrb + q) * STAT_W;
     a += sp[0]; b = fmin(b, sp[1]); c = fmax(c, sp[2]); e = fmax(e, sp[3]);
   }
   stats[STAT_W * t] = a; stats[STAT_W * t + 1] = b; stats[STAT_W * t + 2] = c; stats[STAT_W * t + 3] = e;
@@ -603,10 +608,10 @@ extern "C" cr_status cr_cov_build(cr_tilemat V, const double* d_xy, const cr_cov
     if (k.use_df)
       k_cov_stats_split<<<(unsigned)V->ntiles * nrb, 256, smem, stream>>>(V->xy, V->n, V->nb, V->nt, k, V->stat_part);
     else
-      k_cov_stats<false><<<grid, 256, smem, stream>>>(V->xy, V->n, V->nb, k, V->stat_part, nullptr);
+      k_cov_stats<false, 64><<<grid, 256, smem, stream>>>(V->xy, V->n, V->nb, k, V->stat_part, nullptr, 0);
   }
   CR_CHECK_LAUNCH("k_cov_stats");
-  k_stats_reduce<<<(V->ntiles + 127) / 128, 128, 0, stream>>>(V->stat_part, V->ntiles, nrb, V->stats, nullptr);
+  k_stats_reduce<<<(V->ntiles + 127) / 128, 128, 0, stream>>>(V->stat_part, V->ntiles, nrb, V->stats, nullptr, 0);
   CR_CHECK_LAUNCH("k_stats_reduce");
   V->params = *p;
   V->covk = k;
@@ -647,20 +652,23 @@ cr_status refine_stats(cr_tilemat V, const std::vector<int>& list) {
   if (list.empty()) return CR_OK;
   CR_CUDA(cudaSetDevice(V->device));
   if (!V->d_refine) CR_CUDA(cudaMalloc(&V->d_refine, (size_t)V->ntiles * sizeof(int)));
+  // 16-row blocks: 4x the CTAs of the statistics pass, each 4x shorter (a few tiles only)
+  constexpr int RR = 16;
+  const int nrr = V->nb / RR;
+  if (!V->refine_part) CR_CUDA(cudaMalloc(&V->refine_part, (size_t)V->ntiles * nrr * STAT_W * sizeof(double)));
   CR_CUDA(cudaMemcpy(V->d_refine, list.data(), list.size() * sizeof(int), cudaMemcpyHostToDevice));
-  const int nrb = V->nb / 64;
   const size_t smem = (size_t)(V->nb + 64) * sizeof(float4);
-  const dim3 grid((unsigned)list.size(), nrb);
+  const dim3 grid((unsigned)list.size(), nrr);
   {
     TimedScope ts("k_cov_stats_refine", 0);
     if (V->covk.use_df)
-      k_cov_stats<true><<<grid, 256, smem, 0>>>(V->xy, V->n, V->nb, V->covk, V->stat_part, V->d_refine);
+      k_cov_stats<true, RR><<<grid, 256, smem, 0>>>(V->xy, V->n, V->nb, V->covk, V->refine_part, V->d_refine, 1);
     else
-      k_cov_stats<false><<<grid, 256, smem, 0>>>(V->xy, V->n, V->nb, V->covk, V->stat_part, V->d_refine);
+      k_cov_stats<false, RR><<<grid, 256, smem, 0>>>(V->xy, V->n, V->nb, V->covk, V->refine_part, V->d_refine, 1);
   }
   CR_CHECK_LAUNCH("k_cov_stats");
-  k_stats_reduce<<<((unsigned)list.size() + 127) / 128, 128, 0, 0>>>(V->stat_part, (int)list.size(), nrb, V->stats,
-                                                                      V->d_refine);
+  k_stats_reduce<<<((unsigned)list.size() + 127) / 128, 128, 0, 0>>>(V->refine_part, (int)list.size(), nrr, V->stats,
+                                                                      V->d_refine, 1);
   CR_CHECK_LAUNCH("k_stats_reduce");
   V->stats_on_host = false;
   return fetch_stats(V);

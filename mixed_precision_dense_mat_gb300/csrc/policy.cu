@@ -13,6 +13,7 @@
 #include <math.h>
 
 #include <algorithm>
+#include <cstring>
 
 #include "common.cuh"
 
@@ -179,14 +180,6 @@ void mark_extreme(const cr_tilemat V, const std::vector<double>& x, bool want_ma
     }
 }
 
-// per-tile tables have ntiles entries for the life of the tile matrix: allocated once
-template <class T>
-cr_status upload(T** d, const std::vector<T>& h) {
-  if (!*d) CR_CUDA(cudaMalloc(d, std::max<size_t>(1, h.size()) * sizeof(T)));
-  CR_CUDA(cudaMemcpy(*d, h.data(), h.size() * sizeof(T), cudaMemcpyHostToDevice));
-  return CR_OK;
-}
-
 // (re)allocates *d only when the new size exceeds its capacity, so that repeated maps of the
 // same matrix neither free nor allocate (cudaFree synchronises the device)
 template <class T>
@@ -226,11 +219,24 @@ cr_status allocate_class_storage(cr_tilemat V) {
     V->minv_hi = V->n16; V->n16 += 2;   // by column parity
     V->minv_lo = V->n16; V->n16 += 2;
   }
-  CR_TRY(upload(&V->d_cls, V->h_cls));
-  CR_TRY(upload(&V->d_i64, V->h_i64));
-  CR_TRY(upload(&V->d_i32, V->h_i32));
-  CR_TRY(upload(&V->d_hi16, V->h_hi16));
-  CR_TRY(upload(&V->d_lo16, V->h_lo16));
+  // the five per-tile tables in one device buffer and one copy: four int tables, then the
+  // class bytes
+  {
+    const size_t ints = 4 * (size_t)T, bytes = ints * sizeof(int) + (size_t)T;
+    if (!V->d_tables) CR_CUDA(cudaMalloc(&V->d_tables, bytes));
+    std::vector<int> h(ints + ((size_t)T + sizeof(int) - 1) / sizeof(int), 0);
+    std::copy(V->h_i64.begin(), V->h_i64.end(), h.begin());
+    std::copy(V->h_i32.begin(), V->h_i32.end(), h.begin() + T);
+    std::copy(V->h_hi16.begin(), V->h_hi16.end(), h.begin() + 2 * (size_t)T);
+    std::copy(V->h_lo16.begin(), V->h_lo16.end(), h.begin() + 3 * (size_t)T);
+    std::memcpy(h.data() + ints, V->h_cls.data(), (size_t)T);
+    CR_CUDA(cudaMemcpy(V->d_tables, h.data(), bytes, cudaMemcpyHostToDevice));
+    V->d_i64 = V->d_tables;
+    V->d_i32 = V->d_tables + T;
+    V->d_hi16 = V->d_tables + 2 * (size_t)T;
+    V->d_lo16 = V->d_tables + 3 * (size_t)T;
+    V->d_cls = reinterpret_cast<int8_t*>(V->d_tables + ints);
+  }
   CR_TRY(ensure(&V->pool64, &V->cap64, std::max<size_t>(1, (size_t)V->n64) * tile));
   if (V->n32) CR_TRY(ensure(&V->pool32, &V->cap32, (size_t)V->n32 * tile));
   if (V->n16) {
