@@ -182,7 +182,10 @@ cr_status cr_rnorm(double* d_Z, int ldz, int n, int M, uint64_t seed, uint64_t o
 /* Flags of cr_trmm_sim. */
 enum {
   CR_TRMM_FP16_DEST = 1,   /* round each output to FP16 before widening (Alg.1 FP16 destination) */
-  CR_TRMM_GENERATE = 2     /* ignore d_Z; draw M_rand from (seed, offset) in FP32 and round */
+  CR_TRMM_GENERATE = 2,    /* ignore d_Z; draw M_rand from (seed, offset) in FP32 and round */
+  CR_TRMM_SPLIT_L = 4      /* FP32- and FP64-class off-diagonal factor tiles enter as their FP16
+                              high/low pair (two MMAs, ~2^-22 relative) instead of the FP16 cast
+                              of Alg.1 step 15 (2^-11); FP16-class tiles are exact either way */
 };
 
 /* Mixed-precision TRMM (Section IV-C Eq.3, Alg.1): Y = L_s B with B = fp16(M_rand / s)

@@ -87,8 +87,8 @@ __device__ __forceinline__ Job decode(const TcParams& p, int t) {
 // Per-k metadata of one output block, gathered by the 32 lanes of warp 0 into shared memory
 // so that the step enumeration below does no global loads: for the update modes entry
 // k - kbeg holds (product class, A hi slot, B hi slot, A lo slot, B lo slot); for the
-// simulation multiply entry k holds the slot of the factor tile (i, k) in field 1 and, for
-// k = i, the low part of the diagonal factor in field 3.
+// simulation multiply entry k holds the slot of the factor tile (i, k) in field 1 and the slot
+// of its low part in field 3 (-1 for FP16-class tiles, which have none).
 __device__ __forceinline__ void fill_ktable(const TcParams& p, const Job& jb, int* kt) {
   const TileView& v = p.v;
   const int lane = threadIdx.x & 31;
@@ -110,7 +110,7 @@ __device__ __forceinline__ void fill_ktable(const TcParams& p, const Job& jb, in
     for (int k = lane; k <= i; k += 32) {
       int* e = kt + TC_KT_INTS * k;
       e[1] = v.hi16[tidx(i, k)];
-      if (k == i) e[3] = v.lo16[tidx(i, i)];
+      e[3] = v.lo16[tidx(i, k)];
     }
   }
 }
@@ -160,9 +160,16 @@ __device__ __forceinline__ int for_each_step(const TcParams& p, const Job& jb, c
     }
   } else {
     const int i = jb.i;
+    const bool split = (p.flags & CR_TRMM_SPLIT_L) != 0;
     for (int k = 0; k < i; ++k) {
-      const int a = kt[TC_KT_INTS * k + 1];
-      for (int q = 0; q < nq; ++q, ++s) f(a, q * TC_BK, -1, k * v.nb + q * TC_BK, brow);
+      const int a = kt[TC_KT_INTS * k + 1], alo = split ? kt[TC_KT_INTS * k + 3] : -1;
+      for (int q = 0; q < nq; ++q, ++s) {
+        f(a, q * TC_BK, -1, k * v.nb + q * TC_BK, brow);
+        if (alo >= 0) {   // the tile's low part (FP32/FP64 class)
+          f(alo, q * TC_BK, -1, k * v.nb + q * TC_BK, brow);
+          ++s;
+        }
+      }
     }
     const int nqd = (jb.rb + 1) * (TC_BM / TC_BK);    // the diagonal factor is lower triangular
     const int dh = kt[TC_KT_INTS * i + 1], dl = kt[TC_KT_INTS * i + 3];

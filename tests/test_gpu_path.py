@@ -188,6 +188,35 @@ def test_adaptive_cholesky_and_simulation(lib, case, fixedacc):
     V.close()
 
 
+@pytest.mark.parametrize("case,fixedacc", [("a_exp", 1e-6), ("ragged_nu15", 1e-5)])
+def test_trmm_split_factor_tiles(lib, case, fixedacc):
+    """CR_TRMM_SPLIT_L: FP32/FP64-class factor tiles enter the simulation multiply as FP16
+    high/low pairs.  Against the exact product of the GPU's own stored factor with the FP16
+    right-hand side B = fp16(Z / s) (so that only the multiply's treatment of L and its FP32
+    accumulation remain), the split multiply is accurate to the FP32 level, and the default
+    one (FP16 casts, Alg.1 step 15) to the FP16 cast level."""
+    c = COV_CASES[case]
+    xy, V, Vo = _build(lib, c)
+    m, info = lib.precision_map(V, amp=True, fixedacc=fixedacc)
+    assert info["n_fp32"] > 0, info
+    assert lib.potrf_adaptive(V) == 0
+    s = info["s"]
+    Ls = lib.tilemat_to_dense(V, 1).cpu().numpy()   # L_s = s L as stored, lower part
+    M = 96
+    Z = inputgen.standard_normals(c["n"], M, 11)
+    B = (Z / s).astype(np.float16).astype(np.float64)
+    Yref = np.tril(Ls) @ B
+    Yc = lib.trmm_sim(V, colmajor(Z), M).cpu().numpy()
+    Ysp = lib.trmm_sim(V, colmajor(Z), M, flags=lib.CR_TRMM_SPLIT_L).cpu().numpy()
+    e_cast, e_split = relf(Yc, Yref), relf(Ysp, Yref)
+    msg = f"tiles {info['n_fp64']}/{info['n_fp32']}/{info['n_fp16']}: cast {e_cast:.2e} split {e_split:.2e}"
+    assert e_split <= 2e-6, msg
+    assert e_cast >= 20 * e_split, msg
+    # the split multiply is still the simulation: against the oracle within the adaptive bound
+    assert relf(Ysp, oracle.simulate(oracle.cholesky_lower(Vo), Z)) <= 1e-2, msg
+    V.close()
+
+
 def test_rnorm_stream_matches_oracle(lib):
     n, M, seed, off = 777, 33, 42, 5
     Z = lib.rnorm(n, M, seed, off).cpu().numpy()
