@@ -183,9 +183,15 @@ cr_status cr_rnorm(double* d_Z, int ldz, int n, int M, uint64_t seed, uint64_t o
 enum {
   CR_TRMM_FP16_DEST = 1,   /* round each output to FP16 before widening (Alg.1 FP16 destination) */
   CR_TRMM_GENERATE = 2,    /* ignore d_Z; draw M_rand from (seed, offset) in FP32 and round */
-  CR_TRMM_SPLIT_L = 4      /* FP32- and FP64-class off-diagonal factor tiles enter as their FP16
+  CR_TRMM_SPLIT_L = 4,     /* FP32- and FP64-class off-diagonal factor tiles enter as their FP16
                               high/low pair (two MMAs, ~2^-22 relative) instead of the FP16 cast
                               of Alg.1 step 15 (2^-11); FP16-class tiles are exact either way */
+  CR_TRMM_FP16_PER_GEMM = 8 /* the FP16 destination of Alg.1 task by task: each block row's
+                              products (the diagonal one, then k = i-1 down to 0) are accumulated
+                              in FP32 one at a time and the running result is rounded to FP16
+                              after each (Y_i = fp16(Y_i + L_ik B_k)); the last rounding is widened
+                              into d_Y.  Implies CR_TRMM_FP16_DEST's rounding; allocates an
+                              n_pad x M FP16 buffer on first use */
 };
 
 /* Mixed-precision TRMM (Section IV-C Eq.3, Alg.1): Y = L_s B with B = fp16(M_rand / s)

@@ -35,7 +35,7 @@ HEADER = os.path.join(os.path.dirname(_PKG), "include", "cr.h")
 
 CR_PREC_FP64, CR_PREC_FP32, CR_PREC_FP16 = 0, 1, 2
 CR_COV_MATERN, CR_COV_POWEXP = 0, 1
-CR_TRMM_FP16_DEST, CR_TRMM_GENERATE, CR_TRMM_SPLIT_L = 1, 2, 4
+CR_TRMM_FP16_DEST, CR_TRMM_GENERATE, CR_TRMM_SPLIT_L, CR_TRMM_FP16_PER_GEMM = 1, 2, 4, 8
 STATUS = {0: "CR_OK", 1: "CR_ERR_ARG", 2: "CR_ERR_CUDA", 3: "CR_ERR_NOMEM", 4: "CR_ERR_NOT_SPD",
           5: "CR_ERR_EMPTY_SAMPLE", 6: "CR_ERR_NONPOS_MSPE", 7: "CR_ERR_TIMEOUT", 8: "CR_ERR_STATE",
           9: "CR_ERR_NOT_IMPLEMENTED", 10: "CR_ERR_RANGE"}

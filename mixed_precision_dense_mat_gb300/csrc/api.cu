@@ -262,7 +262,7 @@ extern "C" cr_status cr_tilemat_destroy(cr_tilemat V) {
   cudaSetDevice(V->device);
   cudaDeviceSynchronize();
   free_class_storage(V);
-  dfree(V->b16); dfree(V->bnorm_part); dfree(V->minv_all); dfree(V->diag_tasks); dfree(V->diag_flags); dfree(V->diag_pub); dfree(V->minv_part);
+  dfree(V->b16); dfree(V->y16); dfree(V->bnorm_part); dfree(V->minv_all); dfree(V->diag_tasks); dfree(V->diag_flags); dfree(V->diag_pub); dfree(V->minv_part);
   dfree(V->xy); dfree(V->stat_part); dfree(V->d_refine); dfree(V->refine_part); dfree(V->stats); dfree(V->minv); dfree(V->scratch64); dfree(V->d_status);
   if (V->s_hi) cudaStreamDestroy(V->s_hi);
   if (V->s_lo) cudaStreamDestroy(V->s_lo);

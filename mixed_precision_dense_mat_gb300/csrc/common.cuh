@@ -136,6 +136,8 @@ struct cr_tilemat_s {
   // simulation right-hand side B = fp16(M_rand / s), npad x M column-major
   __half* b16 = nullptr;
   size_t b16_elems = 0;
+  __half* y16 = nullptr;          // FP16 destination of the per-product rounding mode (npad x M)
+  size_t y16_elems = 0;
   int b16_M = -1;
   CUtensorMap tm_b16;
   double* bnorm_part = nullptr;   // per-block partial sums of ||B||_F^2

@@ -225,6 +225,17 @@ extern "C" cr_status cr_trmm_sim(cr_tilemat L, const double* d_Z, int ldz, int M
   tp.M = M;
   tp.ncb = (M + TC_BN - 1) / TC_BN;
   tp.flags = flags;
+  if (flags & CR_TRMM_FP16_PER_GEMM) {
+    if (need > L->y16_elems) {
+      if (L->y16) cudaFree(L->y16);
+      L->y16 = nullptr;
+      L->y16_elems = 0;
+      CR_CUDA(cudaMalloc(&L->y16, need * sizeof(__half)));
+      L->y16_elems = need;
+    }
+    tp.y16 = L->y16;
+    tp.ldy16 = L->npad;
+  }
   CR_TRY(tc_launch(tp, L->tm_pool16, L->tm_b16, stream));
   if (h_bnorm) {
     std::vector<double> part(COMP_BLOCKS);

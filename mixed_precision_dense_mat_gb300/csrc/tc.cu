@@ -120,8 +120,10 @@ __device__ __forceinline__ void fill_ktable(const TcParams& p, const Job& jb, in
 // tile pool at rows [rb*128, +128); B (256 rows from b_row) from the pool (b_slot >= 0) or
 // from the 2-D right-hand-side map (b_slot < 0, b_k the global row of the simulation
 // matrix).  kt is the table of fill_ktable.  Returns the number of steps.
+// seg (simulation multiply with CR_TRMM_FP16_PER_GEMM): -1 enumerates the whole chain; 0 only
+// the diagonal factor tile's product; s >= 1 only the product of the factor tile k = i - s.
 template <class F>
-__device__ __forceinline__ int for_each_step(const TcParams& p, const Job& jb, const int* kt, F&& f) {
+__device__ __forceinline__ int for_each_step(const TcParams& p, const Job& jb, const int* kt, F&& f, int seg = -1) {
   const TileView& v = p.v;
   const int nq = v.nb / TC_BK;
   const int brow = jb.cb * TC_BN;
@@ -162,6 +164,7 @@ __device__ __forceinline__ int for_each_step(const TcParams& p, const Job& jb, c
     const int i = jb.i;
     const bool split = (p.flags & CR_TRMM_SPLIT_L) != 0;
     for (int k = 0; k < i; ++k) {
+      if (seg >= 0 && k != i - seg) continue;
       const int a = kt[TC_KT_INTS * k + 1], alo = split ? kt[TC_KT_INTS * k + 3] : -1;
       for (int q = 0; q < nq; ++q, ++s) {
         f(a, q * TC_BK, -1, k * v.nb + q * TC_BK, brow);
@@ -173,7 +176,7 @@ __device__ __forceinline__ int for_each_step(const TcParams& p, const Job& jb, c
     }
     const int nqd = (jb.rb + 1) * (TC_BM / TC_BK);    // the diagonal factor is lower triangular
     const int dh = kt[TC_KT_INTS * i + 1], dl = kt[TC_KT_INTS * i + 3];
-    for (int q = 0; q < nqd; ++q) {
+    for (int q = 0; q < (seg > 0 ? 0 : nqd); ++q) {
       f(dh, q * TC_BK, -1, i * v.nb + q * TC_BK, brow);
       f(dl, q * TC_BK, -1, i * v.nb + q * TC_BK, brow);
       s += 2;
@@ -184,6 +187,32 @@ __device__ __forceinline__ int for_each_step(const TcParams& p, const Job& jb, c
 
 struct NoOp {
   __device__ void operator()(int, int, int, int, int) const {}
+};
+
+// The jobs of one CTA: output blocks t = blockIdx.x, + gridDim.x, ...; with
+// CR_TRMM_FP16_PER_GEMM each block of tile row i is i + 1 consecutive jobs (segments: the
+// diagonal product, then k = i-1 down to 0), each with its own accumulator and epilogue, so
+// that the FP16 destination is rounded after every product as in Alg.1's task sequence.
+struct JobIter {
+  int t, seg, nseg, nblocks;
+  bool perk, started;
+  __device__ JobIter(const TcParams& p, int nb_)
+      : t(blockIdx.x), seg(-1), nseg(1), nblocks(nb_),
+        perk(p.mode == TC_TRMM && (p.flags & CR_TRMM_FP16_PER_GEMM) != 0), started(false) {}
+  __device__ bool next(const TcParams& p) {
+    if (!started) {
+      started = true;
+    } else if (perk && seg + 1 < nseg) {
+      ++seg;
+      return true;
+    } else {
+      t += gridDim.x;
+    }
+    if (t >= nblocks) return false;
+    seg = perk ? 0 : -1;
+    nseg = perk ? decode(p, t).i + 1 : 1;
+    return true;
+  }
 };
 
 // FP32 -> FP64 widening from the IEEE 754 fields (exponent rebiased by 1023 - 127, fraction
@@ -211,6 +240,28 @@ __device__ __forceinline__ void trmm_store(const TcParams& p, const Job& jb, int
     if (col < p.M) {
       const float a = f16 ? __half2float(__float2half_rn(acc[q])) : acc[q];
       p.Y[(size_t)col * p.ldy + row] = widen(a);
+    }
+  }
+}
+
+// CR_TRMM_FP16_PER_GEMM: segment seg of nseg of the block's products.  The running result is
+// kept in the FP16 destination y16 (npad x M column-major) and rounded after every product:
+// y = fp16(y + acc) (y = 0 before the first); the last segment widens y into Y.
+__device__ __forceinline__ void trmm_store_per_gemm(const TcParams& p, const Job& jb, int r_local, int c0,
+                                                    const float* acc, int seg, int nseg) {
+  const TileView& v = p.v;
+  const int row = jb.i * v.nb + jb.rb * TC_BM + r_local;
+  if (row >= v.n) return;
+  const bool last = seg + 1 == nseg;
+#pragma unroll
+  for (int q = 0; q < 16; ++q) {
+    const int col = jb.cb * TC_BN + c0 + q;
+    if (col < p.M) {
+      __half* y = p.y16 + (size_t)col * p.ldy16 + row;
+      const float prev = seg == 0 ? 0.0f : __half2float(*y);
+      const __half h = __float2half_rn(prev + acc[q]);
+      if (last) p.Y[(size_t)col * p.ldy + row] = widen(__half2float(h));
+      else *y = h;
     }
   }
 }
@@ -443,7 +494,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
     uint32_t gs = 0;   // global step count of this CTA
     int u = 0;
-    for (int t = blockIdx.x; t < nblocks; t += gridDim.x, ++u) {
+    for (JobIter it(p, nblocks); it.next(p); ++u) {
+      const int t = it.t;
       const int b = u & 1;
       const uint32_t ph = (uint32_t)(u >> 1) & 1u;
       int* kt = ktab + b * kt_ints;
@@ -483,7 +535,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             tma_load_2d(sb, &tmB, &bars->full[st], bk, brow);
             tma_load_2d(sb + 128 * TC_BK * 2, &tmB, &bars->full[st], bk, brow + 128);
           }
-        });
+        }, it.seg);
       }
       __syncwarp();
     }
@@ -492,7 +544,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const uint32_t idesc = idesc_f16_f32(TC_BM, TC_BN);
       uint32_t gs = 0;
       int u = 0;
-      for (int t = blockIdx.x; t < nblocks; t += gridDim.x, ++u) {
+      for (JobIter it(p, nblocks); it.next(p); ++u) {
+        const int t = it.t;
         const int b = u & 1;
         const uint32_t ph = (uint32_t)(u >> 1) & 1u;
         if (*abort_flag) break;
@@ -502,7 +555,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           break;
         }
         const Job jb = decode(p, t / es);
-        const int S = for_each_step(p, jb, ktab + b * kt_ints, NoOp());
+        const int S = for_each_step(p, jb, ktab + b * kt_ints, NoOp(), it.seg);
         mbar_arrive(&bars->kempty[b]);
         tc_fence_after();
         const uint32_t acc = tmem + (uint32_t)(b * TC_BN);
@@ -539,7 +592,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int quad = warp & 3;
     const int r_local = quad * 32 + lane;
     int u = 0;
-    for (int t = blockIdx.x; t < nblocks; t += gridDim.x, ++u) {
+    for (JobIter it(p, nblocks); it.next(p); ++u) {
+      const int t = it.t;
       const int b = u & 1;
       const uint32_t ph = (uint32_t)(u >> 1) & 1u;
       if (*abort_flag) break;
@@ -562,7 +616,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 #pragma unroll
             for (int q = 0; q < 16; ++q) acc[q] = 0.0f;
           }
-          trmm_store(p, jb, r_local, c0, acc);
+          if (it.perk) trmm_store_per_gemm(p, jb, r_local, c0, acc, it.seg, it.nseg);
+          else trmm_store(p, jb, r_local, c0, acc);
         }
       } else {
         // row-major tiles: each 32 x 32 chunk of the warp's quadrant goes through shared

@@ -217,6 +217,41 @@ def test_trmm_split_factor_tiles(lib, case, fixedacc):
     V.close()
 
 
+def test_trmm_fp16_destination_per_product(lib):
+    """CR_TRMM_FP16_PER_GEMM: each block row's products (the diagonal one, then k = i-1 down
+    to 0) are rounded to the FP16 destination one at a time.  Compared with a host emulation
+    of that task sequence on the GPU's own factor (off-diagonal tiles as their FP16 casts, FP64
+    products, FP16 rounding after each), and with the single final rounding of
+    CR_TRMM_FP16_DEST, which it must differ from."""
+    c = COV_CASES["a_exp"]
+    xy, V, Vo = _build(lib, c)
+    m, info = lib.precision_map(V, amp=True, fixedacc=1e-4)
+    assert lib.potrf_adaptive(V) == 0
+    s, n, nb = info["s"], c["n"], c["nb"]
+    Ls = np.tril(lib.tilemat_to_dense(V, 1).cpu().numpy())
+    M = 80
+    Z = inputgen.standard_normals(n, M, 21)
+    B = (Z / s).astype(np.float16).astype(np.float64)
+    Yp = lib.trmm_sim(V, colmajor(Z), M, flags=lib.CR_TRMM_FP16_PER_GEMM).cpu().numpy()
+    Yd = lib.trmm_sim(V, colmajor(Z), M, flags=lib.CR_TRMM_FP16_DEST).cpu().numpy()
+    nt = (n + nb - 1) // nb
+    Ye = np.zeros((n, M))
+    f16 = lambda a: a.astype(np.float16).astype(np.float64)
+    for i in range(nt):
+        r = slice(i * nb, min(n, (i + 1) * nb))
+        y = f16(Ls[r, r] @ B[r])
+        for k in range(i - 1, -1, -1):
+            q = slice(k * nb, (k + 1) * nb)
+            y = f16(y + f16(Ls[r, q]) @ B[q])
+        Ye[r] = y
+    e_emul, e_once = relf(Yp, Ye), relf(Yp, Yd)
+    msg = f"per-product vs emulation {e_emul:.2e}, vs single rounding {e_once:.2e}"
+    assert e_emul <= 2e-4 and e_emul <= 0.25 * e_once, msg
+    # still the simulation: within the adaptive bound of the oracle's FP64 chain
+    assert relf(Yp, oracle.simulate(oracle.cholesky_lower(Vo), Z)) <= 1e-2, msg
+    V.close()
+
+
 def test_rnorm_stream_matches_oracle(lib):
     n, M, seed, off = 777, 33, 42, 5
     Z = lib.rnorm(n, M, seed, off).cpu().numpy()
