@@ -191,7 +191,7 @@ enum {
                               in FP32 one at a time and the running result is rounded to FP16
                               after each (Y_i = fp16(Y_i + L_ik B_k)); the last rounding is widened
                               into d_Y.  Implies CR_TRMM_FP16_DEST's rounding; allocates an
-                              n_pad x M FP16 buffer on first use */
+                              FP16 buffer of n_pad x (M rounded up to 256) on first use */
 };
 
 /* Mixed-precision TRMM (Section IV-C Eq.3, Alg.1): Y = L_s B with B = fp16(M_rand / s)

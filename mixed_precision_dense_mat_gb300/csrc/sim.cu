@@ -226,15 +226,15 @@ extern "C" cr_status cr_trmm_sim(cr_tilemat L, const double* d_Z, int ldz, int M
   tp.ncb = (M + TC_BN - 1) / TC_BN;
   tp.flags = flags;
   if (flags & CR_TRMM_FP16_PER_GEMM) {
-    if (need > L->y16_elems) {
+    const size_t need16 = (size_t)L->npad * tp.ncb * TC_BN;   // one 128 x 256 tile per output block
+    if (need16 > L->y16_elems) {
       if (L->y16) cudaFree(L->y16);
       L->y16 = nullptr;
       L->y16_elems = 0;
-      CR_CUDA(cudaMalloc(&L->y16, need * sizeof(__half)));
-      L->y16_elems = need;
+      CR_CUDA(cudaMalloc(&L->y16, need16 * sizeof(__half)));
+      L->y16_elems = need16;
     }
     tp.y16 = L->y16;
-    tp.ldy16 = L->npad;
   }
   CR_TRY(tc_launch(tp, L->tm_pool16, L->tm_b16, stream));
   if (h_bnorm) {

@@ -244,25 +244,49 @@ __device__ __forceinline__ void trmm_store(const TcParams& p, const Job& jb, int
   }
 }
 
-// CR_TRMM_FP16_PER_GEMM: segment seg of nseg of the block's products.  The running result is
-// kept in the FP16 destination y16 (npad x M column-major) and rounded after every product:
-// y = fp16(y + acc) (y = 0 before the first); the last segment widens y into Y.
-__device__ __forceinline__ void trmm_store_per_gemm(const TcParams& p, const Job& jb, int r_local, int c0,
+// CR_TRMM_FP16_PER_GEMM: segment seg of nseg of output block t's products.  The running
+// result is kept in the FP16 destination y16 and rounded after every product:
+// y = fp16(y + acc) (y = 0 before the first); the last segment widens y into Y.  y16 holds
+// each output block as its own 128 x 256 row-major FP16 tile (block t at t 128 256), so a
+// thread's 16 columns are two 16-byte words.
+__device__ __forceinline__ void trmm_store_per_gemm(const TcParams& p, const Job& jb, int t, int r_local, int c0,
                                                     const float* acc, int seg, int nseg) {
   const TileView& v = p.v;
   const int row = jb.i * v.nb + jb.rb * TC_BM + r_local;
   if (row >= v.n) return;
-  const bool last = seg + 1 == nseg;
+  uint4* y = reinterpret_cast<uint4*>(p.y16 + ((size_t)t * TC_BM + r_local) * TC_BN + c0);
+  unsigned w[8];   // 16 FP16 values as 8 packed pairs
+  if (seg == 0) {
 #pragma unroll
-  for (int q = 0; q < 16; ++q) {
-    const int col = jb.cb * TC_BN + c0 + q;
-    if (col < p.M) {
-      __half* y = p.y16 + (size_t)col * p.ldy16 + row;
-      const float prev = seg == 0 ? 0.0f : __half2float(*y);
-      const __half h = __float2half_rn(prev + acc[q]);
-      if (last) p.Y[(size_t)col * p.ldy + row] = widen(__half2float(h));
-      else *y = h;
+    for (int q = 0; q < 8; ++q) {
+      const __half2 h = __floats2half2_rn(acc[2 * q], acc[2 * q + 1]);
+      memcpy(&w[q], &h, 4);
     }
+  } else {
+    const uint4 a = y[0], b = y[1];
+    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w; w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      __half2 h;
+      memcpy(&h, &w[q], 4);
+      const float2 f = __half22float2(h);
+      h = __floats2half2_rn(f.x + acc[2 * q], f.y + acc[2 * q + 1]);
+      memcpy(&w[q], &h, 4);
+    }
+  }
+  if (seg + 1 < nseg) {
+    y[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    y[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    return;
+  }
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    __half2 h;
+    memcpy(&h, &w[q], 4);
+    const float2 f = __half22float2(h);
+    const int col = jb.cb * TC_BN + c0 + 2 * q;
+    if (col < p.M) p.Y[(size_t)col * p.ldy + row] = widen(f.x);
+    if (col + 1 < p.M) p.Y[(size_t)(col + 1) * p.ldy + row] = widen(f.y);
   }
 }
 
@@ -616,7 +640,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 #pragma unroll
             for (int q = 0; q < 16; ++q) acc[q] = 0.0f;
           }
-          if (it.perk) trmm_store_per_gemm(p, jb, r_local, c0, acc, it.seg, it.nseg);
+          if (it.perk) trmm_store_per_gemm(p, jb, t, r_local, c0, acc, it.seg, it.nseg);
           else trmm_store(p, jb, r_local, c0, acc);
         }
       } else {

@@ -36,8 +36,8 @@ struct TcParams {
   double* ws64;       // FP64-class triangular-solve inputs
   double* Y;          // simulation output (n x M column-major)
   int ldy, M, ncb, flags;
-  __half* y16;        // CR_TRMM_FP16_PER_GEMM: FP16 destination between products (npad x M, ldy16)
-  int ldy16;
+  __half* y16;        // CR_TRMM_FP16_PER_GEMM: FP16 destination between products, one 128 x 256
+                      // row-major tile per output block (npad x ncb 256 halves)
   int max_ctas;       // grid cap (0: one CTA per SM); background launches leave SMs free for
                       // the critical stream, whose CTAs cannot preempt persistent ones
   int esplit;         // update and solve modes: 1, or CTAs per output block (each repeats the
