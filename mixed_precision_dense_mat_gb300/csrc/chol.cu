@@ -39,7 +39,8 @@ struct Exec {
   // per column j: OLD(j) done (lo); diagonal factor and inverse split (hi); NEW(j) rows j+1..
   // done (mid); solve of row j+1 done (hi); solves of rows j+2.. done (mid)
   std::vector<cudaEvent_t> ev_old, ev_split, ev_newr, ev_crit, ev_rest;
-  std::vector<cudaEvent_t> ev_gen;   // per column: its tiles generated (one event per column range)
+  std::vector<cudaEvent_t> ev_gen;   // per column range: its tiles generated
+  std::vector<cudaEvent_t> ev_gdiag; // per column range: its diagonal tiles generated
   cudaEvent_t start;
 };
 
@@ -139,7 +140,11 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
     CR_CUDA(cudaMemsetAsync(dpub, 0xff, dpub_bytes, x.hi));   // every element unpublished
     CR_CUDA(cudaEventRecord(x.start, x.hi));   // the first two OLD steps wait for the status and flags
     for (int r = 0; r < n_ranges; ++r) {
-      CR_TRY(convert_tiles(V, d_gen + gen_off[r], gen_off[r + 1] - gen_off[r], gen_ndiag[r], x.gen));
+      // the diagonal tiles first, in a launch of their own: the first two columns' diagonal
+      // factorisations need nothing else
+      CR_TRY(convert_tiles(V, d_gen + gen_off[r], gen_ndiag[r], gen_ndiag[r], x.gen));
+      CR_CUDA(cudaEventRecord(x.ev_gdiag[r], x.gen));
+      CR_TRY(convert_tiles(V, d_gen + gen_off[r] + gen_ndiag[r], gen_off[r + 1] - gen_off[r] - gen_ndiag[r], 0, x.gen));
       CR_CUDA(cudaEventRecord(x.ev_gen[r], x.gen));
     }
     return CR_OK;
@@ -273,10 +278,12 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
       t.mode = TC_UPD_OLD;
       t.kbeg = 0;
       t.kend = kold_end;
-      t.row0 = j;
-      t.nrows = nt - j;
+      // without old terms the FP64 diagonal tile is already what its factorisation needs: it
+      // is left out (the critical stream then waits only for its generation, below)
+      t.row0 = kold_end == 0 ? j + 1 : j;
+      t.nrows = nt - t.row0;
       t.max_ctas = cap_lo;
-      P.ops.push_back([=](Exec& x) -> cr_status { return tc_launch(t, *tm, *tm, x.lo); });
+      if (t.nrows > 0) P.ops.push_back([=](Exec& x) -> cr_status { return tc_launch(t, *tm, *tm, x.lo); });
     } else {
       for (int i = j + 1; i < nt; ++i) {
         double* dst = ws64(par, i);
@@ -310,7 +317,16 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
     P.ops.push_back([=](Exec& x) -> cr_status { CR_CUDA(cudaEventRecord(x.ev_newr[j], x.mid)); return CR_OK; });
 
     // ---------------- critical stream: NEW(j) for the diagonal tile, its factor and inverse
-    P.ops.push_back([=](Exec& x) -> cr_status { CR_CUDA(cudaStreamWaitEvent(x.hi, x.ev_old[j], 0)); return CR_OK; });
+    if (V->amp && kold_end == 0) {
+      // the diagonal tile has no old terms: its generation is all the critical stream waits for
+      P.ops.push_back([=](Exec& x) -> cr_status {
+        CR_CUDA(cudaStreamWaitEvent(x.hi, x.ev_gdiag[grange], 0));
+        CR_CUDA(cudaStreamWaitEvent(x.hi, x.start, 0));
+        return CR_OK;
+      });
+    } else {
+      P.ops.push_back([=](Exec& x) -> cr_status { CR_CUDA(cudaStreamWaitEvent(x.hi, x.ev_old[j], 0)); return CR_OK; });
+    }
     new_dgemm(j, j, j + 1, false);
     if (V->amp) {
       TcParams t = tp;
@@ -390,15 +406,15 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
   x.mid = V->s_mid;
   x.gen = V->s_gen;
   cr_status st = CR_OK;
-  // events: created once per tile matrix (6 per column and the start event)
-  if (V->sched_ev.size() != 6 * (size_t)nt + 1) {
+  // events: created once per tile matrix (7 per column and the start event)
+  if (V->sched_ev.size() != 7 * (size_t)nt + 1) {
     for (cudaEvent_t e : V->sched_ev) cudaEventDestroy(e);
-    V->sched_ev.assign(6 * (size_t)nt + 1, nullptr);
+    V->sched_ev.assign(7 * (size_t)nt + 1, nullptr);
     for (auto& e : V->sched_ev) CR_CUDA(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
   }
   {
     size_t q = 0;
-    for (auto* evs : {&x.ev_old, &x.ev_split, &x.ev_newr, &x.ev_crit, &x.ev_rest, &x.ev_gen}) {
+    for (auto* evs : {&x.ev_old, &x.ev_split, &x.ev_newr, &x.ev_crit, &x.ev_rest, &x.ev_gen, &x.ev_gdiag}) {
       evs->assign(V->sched_ev.begin() + q, V->sched_ev.begin() + q + nt);
       q += nt;
     }
