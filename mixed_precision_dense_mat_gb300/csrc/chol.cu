@@ -41,7 +41,8 @@ struct Exec {
   std::vector<cudaEvent_t> ev_old, ev_split, ev_newr, ev_crit, ev_rest;
   std::vector<cudaEvent_t> ev_gen;   // per column range: its tiles generated
   std::vector<cudaEvent_t> ev_gdiag; // per column range: its diagonal tiles generated
-  cudaEvent_t start;
+  cudaEvent_t start;                  // critical stream: status and executor flags cleared
+  cudaEvent_t start0, start1;         // caller: before the prologue; after the job uploads
 };
 
 using Op = std::function<cr_status(Exec&)>;
@@ -132,24 +133,57 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
     both.insert(both.end(), gen_list.begin(), gen_list.end());
     CR_CUDA(cudaMemcpyAsync(V->sched_ints, both.data(), n_ints * sizeof(int), cudaMemcpyHostToDevice, caller));
   }
-  P.ops.push_back([=](Exec& x) -> cr_status {
-    CR_TRY(status_init_launch(status, x.hi));
-    // both parities of the executor's flags and abs-max start cleared
-    CR_CUDA(cudaMemsetAsync(dflags, 0, dwords * sizeof(int), x.hi));
-    CR_CUDA(cudaMemsetAsync(damax, 0, 2 * sizeof(unsigned long long), x.hi));
-    CR_CUDA(cudaMemsetAsync(dpub, 0xff, dpub_bytes, x.hi));   // every element unpublished
-    CR_CUDA(cudaEventRecord(x.start, x.hi));   // the first two OLD steps wait for the status and flags
-    for (int r = 0; r < n_ranges; ++r) {
-      // the diagonal tiles first, in a launch of their own: the first two columns' diagonal
-      // factorisations need nothing else
-      CR_TRY(convert_tiles(V, d_gen + gen_off[r], gen_ndiag[r], gen_ndiag[r], x.gen));
-      CR_CUDA(cudaEventRecord(x.ev_gdiag[r], x.gen));
-      CR_TRY(convert_tiles(V, d_gen + gen_off[r] + gen_ndiag[r], gen_off[r + 1] - gen_off[r] - gen_ndiag[r], 0, x.gen));
-      CR_CUDA(cudaEventRecord(x.ev_gen[r], x.gen));
+  if (!V->s_hi) {
+    int lo_prio = 0, hi_prio = 0;
+    CR_CUDA(cudaDeviceGetStreamPriorityRange(&lo_prio, &hi_prio));
+    CR_CUDA(cudaStreamCreateWithPriority(&V->s_hi, cudaStreamNonBlocking, hi_prio));
+    CR_CUDA(cudaStreamCreateWithPriority(&V->s_mid, cudaStreamNonBlocking, hi_prio));
+    // the bulk updates rank just above the tile generation, which runs ahead of them
+    CR_CUDA(cudaStreamCreateWithPriority(&V->s_lo, cudaStreamNonBlocking, std::max(hi_prio, lo_prio - 1)));
+    CR_CUDA(cudaStreamCreateWithPriority(&V->s_gen, cudaStreamNonBlocking, lo_prio));
+  }
+  Exec x;
+  x.hi = V->s_hi;
+  x.lo = V->s_lo;
+  x.mid = V->s_mid;
+  x.gen = V->s_gen;
+  // events: created once per tile matrix (7 per column and three start events)
+  if (V->sched_ev.size() != 7 * (size_t)nt + 3) {
+    for (cudaEvent_t e : V->sched_ev) cudaEventDestroy(e);
+    V->sched_ev.assign(7 * (size_t)nt + 3, nullptr);
+    for (auto& e : V->sched_ev) CR_CUDA(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+  }
+  {
+    size_t q = 0;
+    for (auto* evs : {&x.ev_old, &x.ev_split, &x.ev_newr, &x.ev_crit, &x.ev_rest, &x.ev_gen, &x.ev_gdiag}) {
+      evs->assign(V->sched_ev.begin() + q, V->sched_ev.begin() + q + nt);
+      q += nt;
     }
-    return CR_OK;
-  });
-
+    x.start = V->sched_ev[q];
+    x.start0 = V->sched_ev[q + 1];
+    x.start1 = V->sched_ev[q + 2];
+  }
+  // The prologue runs at once, so that the GPU generates the first tiles while the host
+  // builds the rest of the schedule: after the caller's prior work and the list upload, the
+  // critical stream clears the status and the executor's flags, and the generation stream
+  // starts on the first column range.
+  CR_CUDA(cudaEventRecord(x.start0, caller));
+  CR_CUDA(cudaStreamWaitEvent(x.hi, x.start0, 0));
+  CR_CUDA(cudaStreamWaitEvent(x.gen, x.start0, 0));
+  CR_TRY(status_init_launch(status, x.hi));
+  // both parities of the executor's flags and abs-max start cleared
+  CR_CUDA(cudaMemsetAsync(dflags, 0, dwords * sizeof(int), x.hi));
+  CR_CUDA(cudaMemsetAsync(damax, 0, 2 * sizeof(unsigned long long), x.hi));
+  CR_CUDA(cudaMemsetAsync(dpub, 0xff, dpub_bytes, x.hi));   // every element unpublished
+  CR_CUDA(cudaEventRecord(x.start, x.hi));   // the first two OLD steps wait for the status and flags
+  for (int r = 0; r < n_ranges; ++r) {
+    // the diagonal tiles first, in a launch of their own: the first two columns' diagonal
+    // factorisations need nothing else
+    CR_TRY(convert_tiles(V, d_gen + gen_off[r], gen_ndiag[r], gen_ndiag[r], x.gen));
+    CR_CUDA(cudaEventRecord(x.ev_gdiag[r], x.gen));
+    CR_TRY(convert_tiles(V, d_gen + gen_off[r] + gen_ndiag[r], gen_off[r + 1] - gen_off[r] - gen_ndiag[r], 0, x.gen));
+    CR_CUDA(cudaEventRecord(x.ev_gen[r], x.gen));
+  }
 
   TcParams base{};
   base.v = V->view();
@@ -391,35 +425,7 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
   }
 
   // streams, events, job upload, replay
-  if (!V->s_hi) {
-    int lo_prio = 0, hi_prio = 0;
-    CR_CUDA(cudaDeviceGetStreamPriorityRange(&lo_prio, &hi_prio));
-    CR_CUDA(cudaStreamCreateWithPriority(&V->s_hi, cudaStreamNonBlocking, hi_prio));
-    CR_CUDA(cudaStreamCreateWithPriority(&V->s_mid, cudaStreamNonBlocking, hi_prio));
-    // the bulk updates rank just above the tile generation, which runs ahead of them
-    CR_CUDA(cudaStreamCreateWithPriority(&V->s_lo, cudaStreamNonBlocking, std::max(hi_prio, lo_prio - 1)));
-    CR_CUDA(cudaStreamCreateWithPriority(&V->s_gen, cudaStreamNonBlocking, lo_prio));
-  }
-  Exec x;
-  x.hi = V->s_hi;
-  x.lo = V->s_lo;
-  x.mid = V->s_mid;
-  x.gen = V->s_gen;
   cr_status st = CR_OK;
-  // events: created once per tile matrix (7 per column and the start event)
-  if (V->sched_ev.size() != 7 * (size_t)nt + 1) {
-    for (cudaEvent_t e : V->sched_ev) cudaEventDestroy(e);
-    V->sched_ev.assign(7 * (size_t)nt + 1, nullptr);
-    for (auto& e : V->sched_ev) CR_CUDA(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
-  }
-  {
-    size_t q = 0;
-    for (auto* evs : {&x.ev_old, &x.ev_split, &x.ev_newr, &x.ev_crit, &x.ev_rest, &x.ev_gen, &x.ev_gdiag}) {
-      evs->assign(V->sched_ev.begin() + q, V->sched_ev.begin() + q + nt);
-      q += nt;
-    }
-    x.start = V->sched_ev[q];
-  }
   // job and pair lists in one device buffer kept by the tile matrix
   const size_t jobs_bytes = (P.jobs.size() * sizeof(DJob) + 255) & ~(size_t)255;
   const size_t need = jobs_bytes + P.pairs.size() * sizeof(DPair);
@@ -447,12 +453,11 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
   x.dj = d_jobs;
   x.dp = d_pairs;
   if (st == CR_OK) {
-    // both library streams start after the caller's prior work (and the uploads)
-    cudaEventRecord(x.start, caller);
-    cudaStreamWaitEvent(x.hi, x.start, 0);
-    cudaStreamWaitEvent(x.lo, x.start, 0);
-    cudaStreamWaitEvent(x.mid, x.start, 0);
-    cudaStreamWaitEvent(x.gen, x.start, 0);
+    // the schedule's streams start after the job and pair uploads
+    cudaEventRecord(x.start1, caller);
+    cudaStreamWaitEvent(x.hi, x.start1, 0);
+    cudaStreamWaitEvent(x.lo, x.start1, 0);
+    cudaStreamWaitEvent(x.mid, x.start1, 0);
   }
   for (size_t q = 0; st == CR_OK && q < P.ops.size(); ++q) st = P.ops[q](x);
   cudaError_t e1 = cudaStreamSynchronize(x.hi);
