@@ -177,11 +177,18 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
   CR_CUDA(cudaMemsetAsync(dpub, 0xff, dpub_bytes, x.hi));   // every element unpublished
   CR_CUDA(cudaEventRecord(x.start, x.hi));   // the first two OLD steps wait for the status and flags
   for (int r = 0; r < n_ranges; ++r) {
-    // the diagonal tiles first, in a launch of their own: the first two columns' diagonal
-    // factorisations need nothing else
-    CR_TRY(convert_tiles(V, d_gen + gen_off[r], gen_ndiag[r], gen_ndiag[r], x.gen));
-    CR_CUDA(cudaEventRecord(x.ev_gdiag[r], x.gen));
-    CR_TRY(convert_tiles(V, d_gen + gen_off[r] + gen_ndiag[r], gen_off[r + 1] - gen_off[r] - gen_ndiag[r], 0, x.gen));
+    if (r <= gen_range_of[std::min(1, nt - 1)]) {
+      // the ranges of columns 0 and 1: the diagonal tiles first, in a launch of their own (the
+      // first two diagonal factorisations need nothing else)
+      CR_TRY(convert_tiles(V, d_gen + gen_off[r], gen_ndiag[r], gen_ndiag[r], x.gen));
+      CR_CUDA(cudaEventRecord(x.ev_gdiag[r], x.gen));
+      CR_TRY(convert_tiles(V, d_gen + gen_off[r] + gen_ndiag[r], gen_off[r + 1] - gen_off[r] - gen_ndiag[r], 0, x.gen));
+    } else {
+      // later ranges in one launch, diagonal tiles issued first, so that their FP64 work
+      // overlaps the other tiles' FP32 work
+      CR_TRY(convert_tiles(V, d_gen + gen_off[r], gen_off[r + 1] - gen_off[r], gen_ndiag[r], x.gen));
+      CR_CUDA(cudaEventRecord(x.ev_gdiag[r], x.gen));
+    }
     CR_CUDA(cudaEventRecord(x.ev_gen[r], x.gen));
   }
 
