@@ -157,6 +157,50 @@ def test_strong_correlation_workload_full_size(lib):
     V.close()
 
 
+def test_scale_sweep_workload_full_size(lib):
+    """The largest scale-sweep configuration (n = 65536, range 0.1, tolerance 1e-6, M = 4096)
+    in the bench's call sequence: the map taken on the fast statistics equals the one taken on
+    exact statistics, and the factor and the simulations agree with the oracle on the leading
+    2048 x 2048 block."""
+    w = inputgen.WORKLOADS["e2"]
+    rng = np.random.default_rng(3)
+    xy = inputgen.workload_locations(w)
+    V = lib.TileMat(w.n, w.nb)
+    lib.cov_build(V, dev(xy), w.family, w.sigma2, w.beta, w.nu, nugget=w.nugget)
+    f, mn, mx = lib.tile_stats(V)
+    _sampled_stats_check(w, xy, f, mn, mx, rng, count=12)
+    pm_exact, info_exact = lib.precision_map(V, amp=True, fixedacc=w.fixedacc)
+    _policy_check(f, mn, mx, pm_exact, info_exact, w.fixedacc)
+    V.close()
+    torch.cuda.empty_cache()
+    V = lib.TileMat(w.n, w.nb)
+    lib.cov_build(V, dev(xy), w.family, w.sigma2, w.beta, w.nu, nugget=w.nugget)
+    pmap, info = lib.precision_map(V, amp=True, fixedacc=w.fixedacc)
+    np.testing.assert_array_equal(pmap, pm_exact)
+    assert info["s"] == info_exact["s"]
+    assert lib.potrf_adaptive(V) == 0
+    s = info["s"]
+    Z = inputgen.standard_normals(2048, w.M, 31)
+    # n x M column-major, zero below the leading rows: the leading rows of L Z depend on the
+    # leading rows of Z only
+    Zd = torch.zeros((w.M, w.n), dtype=torch.float64, device="cuda").T
+    Zd[:2048] = torch.from_numpy(Z).cuda()
+    Yt = lib.trmm_sim(V, Zd, w.M)
+    del Zd
+    Y = Yt[:2048].cpu().numpy()
+    del Yt
+    torch.cuda.empty_cache()
+    Vo = oracle.covariance_matrix(xy[:2048], w.family, w.sigma2, w.beta, w.nu, w.nugget)
+    Lo = oracle.cholesky_lower(Vo)
+    Ld = lib.tilemat_to_dense(V, 1)
+    eL = relf(Ld[:2048, :2048].cpu().numpy() / s, Lo)
+    del Ld
+    torch.cuda.empty_cache()
+    eY = relf(Y, oracle.simulate(Lo, Z))
+    assert eL <= 1e-2 and eY <= 1e-2, (eL, eY, info)
+    V.close()
+
+
 def test_kriging_workload_full_size(lib):
     w = inputgen.WORKLOADS["k"]
     xy = inputgen.workload_locations(w)
