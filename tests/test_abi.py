@@ -53,3 +53,17 @@ def test_header_declares_documented_path():
     names = cr.header_functions()
     for n in ("cr_cov_build", "cr_precision_map", "cr_potrf_adaptive", "cr_trmm_sim", "cr_krige", "cr_calibrate"):
         assert n in names
+
+
+def test_binding_constants_match_the_header():
+    """The enum values the binding passes (precision classes, covariance families, simulation
+    flags, status codes) are the ones include/cr.h declares."""
+    import re
+    text = open(cr.HEADER).read()
+    declared = {m.group(1): int(m.group(2)) for m in re.finditer(r"\b(CR_[A-Z0-9_]+)\s*=\s*(\d+)", text)}
+    for name in ("CR_PREC_FP64", "CR_PREC_FP32", "CR_PREC_FP16", "CR_COV_MATERN", "CR_COV_POWEXP",
+                 "CR_TRMM_FP16_DEST", "CR_TRMM_GENERATE", "CR_TRMM_SPLIT_L", "CR_TRMM_FP16_PER_GEMM"):
+        assert name in declared, name
+        assert getattr(cr, name) == declared[name], name
+    for code, name in cr.STATUS.items():
+        assert declared.get(name, code if name == "CR_OK" else None) == code, name
