@@ -19,7 +19,7 @@ from .covariance import matern, powexp, covariance_fn, covariance_matrix, covari
 from .policy import (PREC_FP64, PREC_FP32, PREC_FP16, tile_stats, tile_stats_from_locations,
                      precision_map, fp16_checks, covariance_scale, select_precision)
 from .linalg import NotSPD, cholesky_lower, solve_lower, solve_lower_transpose
-from .simulate import simulate, splitmix64, rnorm
+from .simulate import simulate, simulate_fp16_per_product, splitmix64, rnorm
 from .krige import universal_kriging, conditional_correction
 from .calibrate import (standardized_statistic, extrema_scan, exceedance_counts,
                         empirical_quantile, sample_without_sentinels, confidence_regions,
@@ -31,7 +31,7 @@ __all__ = [
     "PREC_FP64", "PREC_FP32", "PREC_FP16", "tile_stats", "tile_stats_from_locations",
     "precision_map", "fp16_checks", "covariance_scale", "select_precision",
     "NotSPD", "cholesky_lower", "solve_lower", "solve_lower_transpose",
-    "simulate", "splitmix64", "rnorm", "universal_kriging", "conditional_correction",
+    "simulate", "simulate_fp16_per_product", "splitmix64", "rnorm", "universal_kriging", "conditional_correction",
     "standardized_statistic", "extrema_scan", "exceedance_counts", "empirical_quantile",
     "sample_without_sentinels", "confidence_regions", "EmptySample", "calibrate",
     "truth_field", "excursion_set", "coverage_event",

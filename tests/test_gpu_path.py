@@ -219,9 +219,9 @@ def test_trmm_split_factor_tiles(lib, case, fixedacc):
 
 def test_trmm_fp16_destination_per_product(lib):
     """CR_TRMM_FP16_PER_GEMM: each block row's products (the diagonal one, then k = i-1 down
-    to 0) are rounded to the FP16 destination one at a time.  Compared with a host emulation
-    of that task sequence on the GPU's own factor (off-diagonal tiles as their FP16 casts, FP64
-    products, FP16 rounding after each), and with the single final rounding of
+    to 0) are rounded to the FP16 destination one at a time.  Compared with the oracle's
+    statement of that task sequence on the GPU's own factor (off-diagonal tiles as their FP16
+    casts, FP64 products, FP16 rounding after each), and with the single final rounding of
     CR_TRMM_FP16_DEST, which it must differ from."""
     c = COV_CASES["a_exp"]
     xy, V, Vo = _build(lib, c)
@@ -234,16 +234,13 @@ def test_trmm_fp16_destination_per_product(lib):
     B = (Z / s).astype(np.float16).astype(np.float64)
     Yp = lib.trmm_sim(V, colmajor(Z), M, flags=lib.CR_TRMM_FP16_PER_GEMM).cpu().numpy()
     Yd = lib.trmm_sim(V, colmajor(Z), M, flags=lib.CR_TRMM_FP16_DEST).cpu().numpy()
+    # the factor as the multiply uses it: off-diagonal tiles as their FP16 casts (Alg.1 step 15)
     nt = (n + nb - 1) // nb
-    Ye = np.zeros((n, M))
-    f16 = lambda a: a.astype(np.float16).astype(np.float64)
+    Lc = Ls.astype(np.float16).astype(np.float64)
     for i in range(nt):
         r = slice(i * nb, min(n, (i + 1) * nb))
-        y = f16(Ls[r, r] @ B[r])
-        for k in range(i - 1, -1, -1):
-            q = slice(k * nb, (k + 1) * nb)
-            y = f16(y + f16(Ls[r, q]) @ B[q])
-        Ye[r] = y
+        Lc[r, r] = Ls[r, r]
+    Ye = oracle.simulate_fp16_per_product(Lc, B, nb)
     e_emul, e_once = relf(Yp, Ye), relf(Yp, Yd)
     msg = f"per-product vs emulation {e_emul:.2e}, vs single rounding {e_once:.2e}"
     assert e_emul <= 2e-4 and e_emul <= 0.25 * e_once, msg

@@ -385,3 +385,33 @@ def test_truth_field_mean_and_covariance():
     assert np.max(np.abs(C - V)) < 5 * np.sqrt(2.0 * 2.0 / R) * 2
     # one draw as a vector gives the same column
     np.testing.assert_array_equal(oracle.truth_field(L, X, b, eta[:, 0]), Z[:, 0])
+
+
+def test_fp16_per_product_simulation_pins():
+    """The task-by-task FP16 destination (Alg.1 with §V-F's FP16 storage): a hand-computed case
+    where the order of roundings decides the result, the single-tile case (one rounding of the
+    exact product), exactness when every partial sum is an FP16 integer, and FP16-representable
+    outputs."""
+    # n = 3, nb = 1: row 2 is fp16(1.0), then + 0.75 2^-11 twice; each addition is below half
+    # an FP16 ulp of 1.0 (2^-11), so the per-product result stays 1.0, while the exact sum
+    # 1 + 0.75 2^-10 rounds once to 1 + 2^-10
+    t = 0.75 * 2.0 ** -11
+    L = np.array([[1.0, 0.0, 0.0], [0.0, 1.0, 0.0], [t, t, 1.0]])
+    B = np.ones((3, 1))
+    Y = oracle.simulate_fp16_per_product(L, B, 1)
+    assert Y[2, 0] == 1.0
+    assert np.float16(L[2] @ B[:, 0]) == np.float16(1.0 + 2.0 ** -10)
+    rng = np.random.default_rng(0)
+    # one tile row: a single rounding of the exact product
+    L1 = np.tril(rng.standard_normal((6, 6)))
+    B1 = rng.standard_normal((6, 4))
+    np.testing.assert_array_equal(oracle.simulate_fp16_per_product(L1, B1, 8),
+                                  (L1 @ B1).astype(np.float16).astype(np.float64))
+    # small integers: every partial sum is exact in FP16, so the result is the exact product
+    Li = np.tril(rng.integers(-3, 4, (10, 10))).astype(np.float64)
+    Bi = rng.integers(-3, 4, (10, 5)).astype(np.float64)
+    np.testing.assert_array_equal(oracle.simulate_fp16_per_product(Li, Bi, 3), Li @ Bi)
+    # outputs are FP16 values
+    L2 = np.tril(rng.standard_normal((9, 9)))
+    Y2 = oracle.simulate_fp16_per_product(L2, rng.standard_normal((9, 3)), 4)
+    np.testing.assert_array_equal(Y2, Y2.astype(np.float16).astype(np.float64))
