@@ -123,6 +123,20 @@ cr_status cr_tilemat_create(int n, int nb, cr_tilemat* out);
 cr_status cr_tilemat_destroy(cr_tilemat V);
 cr_status cr_tilemat_info(cr_tilemat V, int* n, int* nb, int* nt);
 
+/* Spatial ordering of the sites (host only, no device work): h_perm (n int32, caller-owned)
+ * receives the permutation that puts the n locations h_xy (row-major pairs (x_i, y_i),
+ * FP64, host) in Z-order, so that h_xy[h_perm[0]], h_xy[h_perm[1]], ... are the sorted
+ * sites.  The pages do not state an ordering, but their precision maps (Section VI-D,
+ * Fig. 5) are banded, which needs nearby sites in nearby tiles: without an ordering,
+ * uniformly scattered sites give no FP16-class tile at any tolerance.  Each coordinate is
+ * quantised to q = clamp(floor(65536 x), 0, 65535), the key interleaves the bits of q_x
+ * (even positions) and q_y (odd positions), and equal keys keep their input order (stable
+ * sort).  Callers order the prediction block and the observation block separately, so that
+ * the block structure of Eq.4 (prediction sites first) is kept, and pass the permuted sites
+ * to cr_cov_build.  Returns CR_ERR_ARG for n < 0, a NULL pointer with n > 0, or a NaN
+ * coordinate. */
+cr_status cr_morton_order(const double* h_xy, int n, int32_t* h_perm);
+
 /* Joint covariance (Section V Eq.4) of the n locations d_xy (n x 2, row-major pairs
  * (x_i, y_i), device, FP64; copied, so the caller may free it afterwards), prediction sites
  * first.  Computes the per-tile statistics (Frobenius norm, min and max entry over valid
@@ -233,7 +247,9 @@ cr_status cr_krige_correct(const double* d_W, int ldw, const double* d_yo, const
  * q_in = Q_level(phi) on the samples without empty-set sentinels; regions
  * d_cin[i] = t_i > q_in, d_cout[i] = t_i >= q_out (uint8).  d_count, d_psi, d_phi may
  * be NULL.  Returns CR_ERR_NONPOS_MSPE if some v_i <= 0 and CR_ERR_EMPTY_SAMPLE if a
- * sample is empty.  Synchronises. */
+ * sample is empty.  Its scratch is library-managed and shared by all calls; the call returns
+ * only after its last kernel has finished, so calls made one after another (on any streams)
+ * never see each other's scratch.  Synchronises. */
 cr_status cr_calibrate(const double* d_S, int lds, int n_p, int M, const double* d_zhat,
                        const double* d_v, double u, double level, uint8_t* d_cin,
                        uint8_t* d_cout, int32_t* d_count, double* d_psi, double* d_phi,
@@ -241,8 +257,9 @@ cr_status cr_calibrate(const double* d_S, int lds, int n_p, int M, const double*
 
 /* Calibration without any allocation.  The paper has no counterpart to this entry point:
  * it exists for callers that cannot allocate device memory themselves, for example code
- * running under a memory pool or a graph-capture regime that forbids cudaMalloc/cudaFree,
- * or embedders that must keep the device footprint fixed after start-up.  It computes
+ * running under a memory pool that owns every device allocation of the process (so a
+ * library-side cudaMalloc would bypass or break its accounting), or embedders that must
+ * keep the device footprint fixed after start-up.  It computes
  * exactly what cr_calibrate computes, with the same arguments and outputs, but its device
  * scratch (t, psi, phi and the per-block partials of the scan) lives in a fixed array
  * inside the library (CR_NOALLOC_SCRATCH_BYTES, held by every device that loads the
@@ -252,8 +269,10 @@ cr_status cr_calibrate(const double* d_S, int lds, int n_p, int M, const double*
  * <= CR_NOALLOC_SCRATCH_BYTES; larger problems return CR_ERR_ARG (use cr_calibrate).
  * The first call on a device looks up the array's device address (once per device, with
  * that device current), so make the first call before any stream capture.  All calls
- * share the one array and the one host buffer: calls that overlap (two streams, two host
- * threads, or two devices at once) race and must be serialised by the caller.
+ * share the one array and the one host buffer: calls that overlap (two host threads, or
+ * two devices at once) race and must be serialised by the caller.  A call returns only after
+ * its last kernel (the region flags, which read the array) has finished on the stream, so
+ * calls issued one after another, even on different streams, do not overlap on the GPU.
  * Synchronises the stream. */
 #define CR_NOALLOC_SCRATCH_BYTES (8u << 20)
 #define CR_NOALLOC_MAX_M 65536

@@ -18,6 +18,7 @@ The functions mirror include/cr.h:
   krige(V, Xo, Xp, yo)                   cr_krige
   krige_correct(W, yo, Y, n_p, n_o)      cr_krige_correct
   calibrate(S, zhat, v, u, level)        cr_calibrate
+  morton_order(xy)                       cr_morton_order (host only)
 The library is never replaced by a fallback: if libcr.so is missing or fails to load, every
 call raises.
 """
@@ -95,6 +96,7 @@ _SIGNATURES = {
     "cr_trmm_sim": (_I, [_P, _P, _I, _I, _U64, _U64, _P, _I, _I, ctypes.POINTER(_D), _P]),
     "cr_krige": (_I, [_P, _P, _P, _P, _P, _I, _P, _P, _P, ctypes.POINTER(_I)]),
     "cr_krige_correct": (_I, [_P, _I, _P, _P, _I, _I, _I, _I, _P, _I, _P]),
+    "cr_morton_order": (_I, [_P, _I, _P]),
     "cr_calibrate": (_I, [_P, _I, _I, _I, _P, _P, _D, _D, _P, _P, _P, _P, _P, ctypes.POINTER(CalibInfo), _P]),
     "cr_calibrate_noalloc": (_I, [_P, _I, _I, _I, _P, _P, _D, _D, _P, _P, _P, _P, _P, ctypes.POINTER(CalibInfo),
                                   _P]),
@@ -211,6 +213,17 @@ class TileMat:
             self.close()
         except Exception:
             pass
+
+
+def morton_order(xy) -> np.ndarray:
+    """cr_morton_order: the stable Z-order permutation of the (n, 2) FP64 host array xy."""
+    load()
+    xy = np.ascontiguousarray(xy, dtype=np.float64)
+    assert xy.ndim == 2 and xy.shape[1] == 2
+    n = xy.shape[0]
+    perm = np.empty(n, dtype=np.int32)
+    _check(_lib.cr_morton_order(xy.ctypes.data if n else None, n, perm.ctypes.data if n else None))
+    return perm
 
 
 def cov_build(V: TileMat, xy, family: str = "matern", sigma2: float = 1.0, range: float = 0.1, nu: float = 0.5,

@@ -282,3 +282,44 @@ extern "C" cr_status cr_tilemat_info(cr_tilemat V, int* n, int* nb, int* nt) {
   if (nt) *nt = V->nt;
   return CR_OK;
 }
+
+// ---------------------------------------------------------------------------------------
+// Spatial ordering of the locations (host only).  The pages' precision maps (Section VI-D,
+// Fig. 5) are banded: nearby sites sit in nearby tiles.  The locations are therefore put in
+// Z-order (Morton order) before the covariance is built: each coordinate is quantised to
+// 16 bits, q = clamp(floor(65536 x), 0, 65535), the key interleaves the bits of q_x (even
+// positions) and q_y (odd positions), and the permutation sorts the keys stably (equal keys
+// keep their input order).
+namespace cr {
+namespace {
+uint32_t spread16(uint32_t v) {
+  v &= 0xffffu;
+  v = (v | (v << 8)) & 0x00ff00ffu;
+  v = (v | (v << 4)) & 0x0f0f0f0fu;
+  v = (v | (v << 2)) & 0x33333333u;
+  v = (v | (v << 1)) & 0x55555555u;
+  return v;
+}
+uint32_t quant16(double x) {
+  const double q = floor(x * 65536.0);   // exact: a power-of-two scale, then an integer part
+  return q <= 0.0 ? 0u : (q >= 65535.0 ? 65535u : (uint32_t)q);
+}
+}  // namespace
+}  // namespace cr
+
+#include <algorithm>
+#include <cmath>
+
+extern "C" cr_status cr_morton_order(const double* h_xy, int n, int32_t* h_perm) {
+  using namespace cr;
+  if (n < 0 || (n > 0 && (!h_xy || !h_perm))) return fail(CR_ERR_ARG, "cr_morton_order: argument");
+  std::vector<uint32_t> key((size_t)n);
+  for (int i = 0; i < n; ++i) {
+    const double x = h_xy[2 * (size_t)i], y = h_xy[2 * (size_t)i + 1];
+    if (std::isnan(x) || std::isnan(y)) return fail(CR_ERR_ARG, "cr_morton_order: NaN coordinate at site " + std::to_string(i));
+    key[i] = spread16(quant16(x)) | (spread16(quant16(y)) << 1);
+  }
+  for (int i = 0; i < n; ++i) h_perm[i] = i;
+  std::stable_sort(h_perm, h_perm + n, [&](int32_t a, int32_t b) { return key[a] < key[b]; });
+  return CR_OK;
+}

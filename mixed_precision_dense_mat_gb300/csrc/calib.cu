@@ -277,6 +277,9 @@ cr_status calibrate_core(const double* d_S, int lds, int n_p, int M, const doubl
   if (out) *out = info;
   k_regions<<<std::min(1024, (n_p + 255) / 256), 256, 0, stream>>>(sc.t, n_p, info.q_in, info.q_out, d_cin, d_cout);
   CR_CHECK_LAUNCH("k_regions");
+  // k_regions reads the shared scratch: return only once it is done, so that a later call on
+  // another stream cannot overwrite t while this one still reads it
+  CR_CUDA(cudaStreamSynchronize(stream));
   return CR_OK;
 }
 
@@ -328,8 +331,8 @@ extern "C" cr_status cr_calibrate(const double* d_S, int lds, int n_p, int M, co
 }
 
 // ---------------------------------------------------------------------------------------
-// Allocation-free calibration, for callers that cannot allocate device memory (a memory
-// pool or capture regime that forbids cudaMalloc/cudaFree, or an embedder whose device
+// Allocation-free calibration, for callers that cannot allocate device memory (code that
+// runs under a memory pool which owns every device allocation, or an embedder whose device
 // footprint must stay fixed after start-up).  Same kernels and results as cr_calibrate;
 // the scratch is a fixed array of this file instead of library-managed allocations.
 namespace cr {
@@ -447,6 +450,9 @@ extern "C" cr_status cr_calibrate_noalloc(const double* d_S, int lds, int n_p, i
   k_regions<<<std::min(1024, (n_p + 255) / 256), 256, 0, stream>>>(t, n_p, info.q_in, info.q_out, d_cin, d_cout);
   count_launch();
   NA_CUDA(cudaGetLastError());
+  // k_regions reads t from the shared array: wait for it while still holding the lock, so that
+  // the next call (on any stream) starts only after this one has stopped using the array
+  NA_CUDA(cudaStreamSynchronize(stream));
 #undef NA_CUDA
   return CR_OK;
 }

@@ -67,3 +67,30 @@ def test_binding_constants_match_the_header():
         assert getattr(cr, name) == declared[name], name
     for code, name in cr.STATUS.items():
         assert declared.get(name, code if name == "CR_OK" else None) == code, name
+
+
+def test_morton_order_matches_the_input_generator(lib):
+    """cr_morton_order (host-only entry point) gives the same permutation, element for element,
+    as the input generator's Z-order on uniform, gridded, jittered and ragged site sets,
+    including points on the unit square's edges and duplicated sites (stable order)."""
+    import numpy as np
+    import inputgen
+    cr.load()
+    cases = [
+        inputgen.uniform_locations(4096, 1),
+        inputgen.uniform_locations(1000, 7),              # ragged size
+        inputgen.grid_cell_centres(64),
+        inputgen.jittered_grid(128, 64, 0.4, 2),
+        np.array([[0.0, 0.0], [1.0, 1.0], [1.0, 0.0], [0.0, 1.0], [0.5, 0.5], [0.5, 0.5],
+                  [-0.25, 2.0], [0.999999999, 0.0000001], [0.5, 0.5]]),
+        np.repeat(inputgen.uniform_locations(37, 3), 3, axis=0),   # triples of equal keys
+    ]
+    for xy in cases:
+        perm = cr.morton_order(xy)
+        ref = inputgen.morton_permutation(xy)
+        np.testing.assert_array_equal(perm, ref.astype(np.int32))
+    assert cr.morton_order(np.zeros((0, 2))).shape == (0,)
+    bad = np.array([[0.1, 0.2], [np.nan, 0.3]])
+    with pytest.raises(cr.CrError) as e:
+        cr.morton_order(bad)
+    assert e.value.code == 1
