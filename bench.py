@@ -45,7 +45,8 @@ NCU_TRAFFIC_PER_LAUNCH = {
 # profiles/k_scan_n32768.md: DRAM bytes of one scan launch at n = 32768, M = 2048; the scan reads
 # S once, so its traffic scales with n M
 SCAN_NCU_BYTES_N32768_M2048 = 537289728 + 3527936
-TIMED_KERNELS = ["k_diag_chol", "k_tc_old", "k_tc_new", "k_tc_trsm", "k_tc_trmm", "k_cov_stats", "k_cov_stats_refine", "k_generate", "k_scan"]
+TIMED_KERNELS = ["k_diag_chol", "k_diag_chol_df", "k_split_diag_df", "k_tc_old", "k_tc_new", "k_tc_trsm", "k_tc_trmm",
+                 "k_cov_stats", "k_cov_stats_refine", "k_generate", "k_scan"]
 WORKLOAD = inputgen.WORKLOADS["c"]
 SEED_Z = 12345
 
@@ -310,7 +311,7 @@ def run_ours(args, world, rank, local):
                                  "frac": ach / pk["bf16_sus"], "traffic": None,
                                  "peak_source": f"{meas} bf16 sustained; work: FP16- and FP32-class Cholesky products "
                                                 "(one per product, however many MMAs it takes)"}
-    for k in ("k_tc_new", "k_tc_trsm", "k_cov_stats", "k_cov_stats_refine", "k_generate"):
+    for k in ("k_tc_old", "k_tc_new", "k_tc_trsm", "k_diag_chol_df", "k_split_diag_df", "k_cov_stats", "k_cov_stats_refine", "k_generate"):
         k_ms, cnt = ktime[k]
         if cnt:
             kern[k] = {"kernel": k, "ms_per_step": k_ms / args.steps, "launches_per_step": cnt / args.steps}

@@ -115,6 +115,26 @@ cr_status cr_timing_enable(int on);
 cr_status cr_timing_read(const char* kernel, double* total_ms, uint64_t* launches);
 cr_status cr_timing_reset(void);
 
+/* Process-wide options (the paper has no counterpart: they control how this library runs
+ * the method, not what it computes).  They apply to calls made after the change.
+ *  CR_OPT_WAIT_LIMIT_US  wall-clock limit of every bounded device-side wait of the
+ *                        factorisation's diagonal executor, in microseconds (default 2000000,
+ *                        range [0, 600000000]).  A wait that runs out makes the factorisation
+ *                        return CR_ERR_TIMEOUT; the tile matrix stays usable and the next
+ *                        cr_potrf_adaptive starts from a clean state.
+ *  CR_OPT_DIAG_ARITH     arithmetic of the FP64 diagonal tiles (Section IV-B keeps them FP64):
+ *                        CR_DIAG_FP64 on the FP64 units; CR_DIAG_DF as double-float pairs of
+ *                        FP32 numbers on the FP32 units (an FP64 emulation with about 48
+ *                        significant bits, several times faster on GB300, whose FP64 units
+ *                        issue 1/64 of the FP32 lanes per cycle); CR_DIAG_AUTO (default):
+ *                        double-float for adaptive factorisations (amp != 0), FP64 for
+ *                        all-FP64 ones (amp = 0, including cr_krige's Sigma_y).
+ * cr_set_option returns CR_ERR_ARG for an unknown option or a value out of range. */
+enum { CR_OPT_WAIT_LIMIT_US = 1, CR_OPT_DIAG_ARITH = 2 };
+enum { CR_DIAG_AUTO = 0, CR_DIAG_FP64 = 1, CR_DIAG_DF = 2 };
+cr_status cr_set_option(int option, long long value);
+cr_status cr_get_option(int option, long long* value);
+
 /* A symmetric n x n matrix stored as its lower tiles (i >= j) of nb x nb entries.
  * NT = ceil(n / nb) tile rows; rows and columns past n are padding and behave like the
  * identity.  nb must be a multiple of 128 with 128 <= nb <= 1024.  The handle owns its
@@ -176,8 +196,11 @@ cr_status cr_precision_map(cr_tilemat V, int amp, double fixedacc, int auto_mode
 /* Adaptive mixed-precision Cholesky (Section IV-B, Alg.2 step 12): scales the tiles by
  * s^2, rounds each to its class, and factors in place, V <- L_s = chol(s^2 V).  FP64
  * tiles run on the FP64 units; FP32/FP16 products on the tensor cores with FP32
- * accumulation.  *info = 0 on success, else the 1-based global column of the first
- * non-positive pivot (LAPACK convention) and CR_ERR_NOT_SPD.  Synchronises. */
+ * accumulation.  The diagonal tiles are factored (with their inverses, which turn the
+ * off-diagonal triangular solves into products) by an on-device dataflow executor, in FP64
+ * or in double-float arithmetic (CR_OPT_DIAG_ARITH).  *info = 0 on success, else the 1-based
+ * global column of the first non-positive pivot (LAPACK convention) and CR_ERR_NOT_SPD;
+ * CR_ERR_TIMEOUT if a bounded device wait ran out (CR_OPT_WAIT_LIMIT_US).  Synchronises. */
 cr_status cr_potrf_adaptive(cr_tilemat V, cr_stream stream, int* info);
 
 /* Copies the tile matrix into a dense n x n column-major FP64 matrix (lower triangle;

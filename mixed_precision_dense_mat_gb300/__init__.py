@@ -37,6 +37,8 @@ HEADER = os.path.join(os.path.dirname(_PKG), "include", "cr.h")
 CR_PREC_FP64, CR_PREC_FP32, CR_PREC_FP16 = 0, 1, 2
 CR_COV_MATERN, CR_COV_POWEXP = 0, 1
 CR_TRMM_FP16_DEST, CR_TRMM_GENERATE, CR_TRMM_SPLIT_L, CR_TRMM_FP16_PER_GEMM = 1, 2, 4, 8
+CR_OPT_WAIT_LIMIT_US, CR_OPT_DIAG_ARITH = 1, 2
+CR_DIAG_AUTO, CR_DIAG_FP64, CR_DIAG_DF = 0, 1, 2
 STATUS = {0: "CR_OK", 1: "CR_ERR_ARG", 2: "CR_ERR_CUDA", 3: "CR_ERR_NOMEM", 4: "CR_ERR_NOT_SPD",
           5: "CR_ERR_EMPTY_SAMPLE", 6: "CR_ERR_NONPOS_MSPE", 7: "CR_ERR_TIMEOUT", 8: "CR_ERR_STATE",
           9: "CR_ERR_NOT_IMPLEMENTED", 10: "CR_ERR_RANGE"}
@@ -80,6 +82,8 @@ _SIGNATURES = {
     "cr_last_error_detail": (ctypes.c_char_p, []),
     "cr_version": (_I, [ctypes.POINTER(_I), ctypes.POINTER(_I)]),
     "cr_kernel_launches": (_I, [ctypes.POINTER(_U64)]),
+    "cr_set_option": (_I, [_I, ctypes.c_longlong]),
+    "cr_get_option": (_I, [_I, ctypes.POINTER(ctypes.c_longlong)]),
     "cr_timing_enable": (_I, [_I]),
     "cr_timing_read": (_I, [ctypes.c_char_p, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_U64)]),
     "cr_timing_reset": (_I, []),
@@ -165,6 +169,19 @@ def kernel_launches() -> int:
     c = _U64(0)
     _check(_lib.cr_kernel_launches(ctypes.byref(c)))
     return c.value
+
+
+def set_option(option: int, value: int) -> None:
+    """cr_set_option: CR_OPT_WAIT_LIMIT_US (microseconds) or CR_OPT_DIAG_ARITH (CR_DIAG_*)."""
+    load()
+    _check(_lib.cr_set_option(option, int(value)))
+
+
+def get_option(option: int) -> int:
+    load()
+    v = ctypes.c_longlong(0)
+    _check(_lib.cr_get_option(option, ctypes.byref(v)))
+    return v.value
 
 
 def timing_enable(on: bool) -> None:

@@ -20,6 +20,11 @@ static std::atomic<uint64_t> g_launches{0};
 
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
+static std::atomic<long long> g_opt_wait_us{2000000};
+static std::atomic<int> g_opt_diag{CR_DIAG_AUTO};
+unsigned long long option_wait_ns() { return 1000ull * (unsigned long long)g_opt_wait_us.load(std::memory_order_relaxed); }
+int option_diag_arith() { return g_opt_diag.load(std::memory_order_relaxed); }
+
 namespace {
 struct TimingState {
   std::mutex mu;
@@ -223,6 +228,29 @@ extern "C" cr_status cr_timing_reset(void) {
   return CR_OK;
 }
 
+extern "C" cr_status cr_set_option(int option, long long value) {
+  if (option == CR_OPT_WAIT_LIMIT_US) {
+    if (value < 0 || value > 600000000ll) return fail(CR_ERR_ARG, "cr_set_option: wait limit outside [0, 600 s]");
+    g_opt_wait_us.store(value);
+    return CR_OK;
+  }
+  if (option == CR_OPT_DIAG_ARITH) {
+    if (value != CR_DIAG_AUTO && value != CR_DIAG_FP64 && value != CR_DIAG_DF)
+      return fail(CR_ERR_ARG, "cr_set_option: diagonal arithmetic must be CR_DIAG_AUTO, CR_DIAG_FP64 or CR_DIAG_DF");
+    g_opt_diag.store((int)value);
+    return CR_OK;
+  }
+  return fail(CR_ERR_ARG, "cr_set_option: unknown option");
+}
+
+extern "C" cr_status cr_get_option(int option, long long* value) {
+  if (!value) return fail(CR_ERR_ARG, "cr_get_option: NULL value");
+  if (option == CR_OPT_WAIT_LIMIT_US) *value = g_opt_wait_us.load();
+  else if (option == CR_OPT_DIAG_ARITH) *value = g_opt_diag.load();
+  else return fail(CR_ERR_ARG, "cr_get_option: unknown option");
+  return CR_OK;
+}
+
 extern "C" cr_status cr_kernel_launches(uint64_t* count) {
   if (!count) return fail(CR_ERR_ARG, "cr_kernel_launches: NULL");
   *count = g_launches.load(std::memory_order_relaxed);
@@ -262,7 +290,7 @@ extern "C" cr_status cr_tilemat_destroy(cr_tilemat V) {
   cudaSetDevice(V->device);
   cudaDeviceSynchronize();
   free_class_storage(V);
-  dfree(V->b16); dfree(V->y16); dfree(V->bnorm_part); dfree(V->minv_all); dfree(V->diag_tasks); dfree(V->diag_flags); dfree(V->diag_pub); dfree(V->minv_part);
+  dfree(V->b16); dfree(V->y16); dfree(V->bnorm_part); dfree(V->minv_all); dfree(V->diag_tasks); dfree(V->diag_flags); dfree(V->diag_pub); dfree(V->minv_part); dfree(V->diag_df);
   dfree(V->xy); dfree(V->stat_part); dfree(V->d_refine); dfree(V->refine_part); dfree(V->stats); dfree(V->minv); dfree(V->scratch64); dfree(V->d_status);
   if (V->s_hi) cudaStreamDestroy(V->s_hi);
   if (V->s_lo) cudaStreamDestroy(V->s_lo);

@@ -89,6 +89,12 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
   const size_t dwords = 2 * (size_t)diag_flag_words(nb, V->diag_db);
   double* dpub = V->diag_pub;
   const size_t dpub_bytes = diag_pub_doubles(nb, V->diag_db) * sizeof(double);
+  // arithmetic of the diagonal executor: double-float (FP64 emulated on the FP32 units) for
+  // adaptive factorisations unless the caller asked otherwise
+  const int arith = option_diag_arith();
+  const bool use_df = arith == CR_DIAG_DF || (arith == CR_DIAG_AUTO && V->amp);
+  const unsigned long long wait_ns = option_wait_ns();
+  if (use_df && !V->diag_df) CR_CUDA(cudaMalloc(&V->diag_df, 2 * nb2 * sizeof(float2)));
   // Tile generation on its own stream, column by column in ranges of doubling width
   // ([0,1), [1,3), [3,7), [7,15), ...), diagonal tiles first in each range: the factorisation
   // of column j waits only for its range, so it starts after the first column's tiles
@@ -390,11 +396,33 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
       CR_CUDA(cudaDeviceGetAttribute(&dgrid, cudaDevAttrMultiProcessorCount, V->device));
       int* flags = V->diag_flags;
       const int4* tasks = V->diag_tasks;
-      P.ops.push_back([=](Exec& x) -> cr_status {
-        // the executor zeroes the upper parts of Ajj and Minv and clears the other parity's
-        // flags and abs-max for the next column
-        return diag_chol_launch(db, Ajj, Minv, W, nb, g, status, flags, par, dpub, tasks, ntask, dgrid, amax, x.hi);
-      });
+      if (use_df) {
+        // double-float executor, then one kernel writing the FP64 factor and inverse and their
+        // FP16 high/low parts (amp only)
+        float2* Ldf = V->diag_df;
+        float2* Mdf = V->diag_df + nb2;
+        float2* Wdf = reinterpret_cast<float2*>(W);
+        __half *mh = nullptr, *ml = nullptr, *dh = nullptr, *dl = nullptr;
+        if (V->amp) {
+          mh = V->pool16 + (size_t)(V->minv_hi + par) * nb2;
+          ml = V->pool16 + (size_t)(V->minv_lo + par) * nb2;
+          dh = V->pool16 + (size_t)V->h_hi16[tidx(j, j)] * nb2;
+          dl = V->pool16 + (size_t)V->h_lo16[tidx(j, j)] * nb2;
+        }
+        int* st_par = status + par;
+        P.ops.push_back([=](Exec& x) -> cr_status {
+          CR_TRY(diag_chol_df_launch(db, Ajj, Ldf, Mdf, Wdf, nb, g, status, flags, par, dpub, tasks, ntask, dgrid, amax,
+                                     wait_ns, x.hi));
+          return split_diag_df_launch(Mdf, Ldf, nb, amax + par, Minv, Ajj, mh, ml, dh, dl, st_par, x.hi);
+        });
+      } else {
+        P.ops.push_back([=](Exec& x) -> cr_status {
+          // the executor zeroes the upper parts of Ajj and Minv and clears the other parity's
+          // flags and abs-max for the next column
+          return diag_chol_launch(db, Ajj, Minv, W, nb, g, status, flags, par, dpub, tasks, ntask, dgrid, amax, wait_ns,
+                                  x.hi);
+        });
+      }
       if (V->minv_all) {
         double* keep = V->minv_all + (size_t)j * nb2;
         P.ops.push_back([=](Exec& x) -> cr_status {
@@ -403,7 +431,7 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
         });
       }
     }
-    if (V->amp) {
+    if (V->amp && !use_df) {
       __half* mh = V->pool16 + (size_t)(V->minv_hi + par) * nb2;
       __half* ml = V->pool16 + (size_t)(V->minv_lo + par) * nb2;
       __half* dh = V->pool16 + (size_t)V->h_hi16[tidx(j, j)] * nb2;

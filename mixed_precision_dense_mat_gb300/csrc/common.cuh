@@ -26,6 +26,11 @@ cr_status cuda_fail(cudaError_t e, const char* what);
 
 void count_launch();
 
+// Process-wide options (cr_set_option): the limit of every bounded device-side wait of the
+// factorisation, and the arithmetic of the diagonal-tile executor (CR_DIAG_*).
+unsigned long long option_wait_ns();
+int option_diag_arith();
+
 // Opt-in device timing of named kernels (cr_timing_enable): a scope object records an event
 // on the launch stream before and after the launch it brackets.
 struct TimedScope {
@@ -147,6 +152,7 @@ struct cr_tilemat_s {
   int* diag_flags = nullptr;
   double* diag_pub = nullptr;     // the diagonal executor's publication buffers (diag_pub_doubles)
   double* minv_part = nullptr;    // per-block partial maxima of |L_jj^-1|
+  float2* diag_df = nullptr;      // 2 * nb * nb double-float pairs: factor, then inverse, of the diagonal tile
   bool factored = false;
   int info = 0;
 

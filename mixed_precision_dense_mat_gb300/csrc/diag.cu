@@ -33,6 +33,7 @@
 #include <vector>
 
 #include "common.cuh"
+#include "df.cuh"
 #include "diag.cuh"
 #include "ptx.cuh"
 
@@ -74,6 +75,7 @@ struct Ctx {
   double* pub_m;
   double* pub_l;
   double* clear_pub;
+  unsigned long long wait_ns;   // limit of every wait (wall clock)
 };
 
 // NaN bit pattern marking an unpublished element; a produced value with this pattern is
@@ -104,7 +106,8 @@ __device__ __forceinline__ void fold_amax(const Ctx& c, double x) {
 
 // Lane `lane` of the polling warp gets the flag (p, v) it waits on for task tk (p = nullptr:
 // nothing); lanes 0-2 cover every task type.
-__device__ __forceinline__ void task_flag(const Ctx& c, int4 tk, int lane, const int*& p, int& v) {
+template <class C>
+__device__ __forceinline__ void task_flag(const C& c, int4 tk, int lane, const int*& p, int& v) {
   const int NB = c.NB;
   p = nullptr;
   v = 1;
@@ -132,9 +135,10 @@ __device__ __forceinline__ void task_flag(const Ctx& c, int4 tk, int lane, const
 }
 
 // All 32 lanes of a warp: waits until *p >= v for every lane with p != nullptr (the lanes
-// poll side by side).  False when the kernel's abort flag is set, or after 2 s, which sets
-// the abort flag and the timeout error bit.
-__device__ bool warp_wait_ge(const Ctx& c, const int* p, int v) {
+// poll side by side).  False when the kernel's abort flag is set, or after the context's wait
+// limit (2 s unless the caller set another), which sets the abort flag and the timeout bit.
+template <class C>
+__device__ bool warp_wait_ge(const C& c, const int* p, int v) {
   bool done = p == nullptr || ld_acquire(p) >= v;
   if (__all_sync(0xffffffffu, done)) return true;
   const uint64_t t0 = global_timer_ns();
@@ -144,7 +148,7 @@ __device__ bool warp_wait_ge(const Ctx& c, const int* p, int v) {
     int stop = 0;
     if ((threadIdx.x & 31) == 0) {
       stop = ld_acquire(c.abort_flag);
-      if (!stop && global_timer_ns() - t0 > 2000000000ull) {
+      if (!stop && global_timer_ns() - t0 > c.wait_ns) {
         atomicOr(&c.status[0], DEV_ERR_TIMEOUT);
         atomicExch(c.abort_flag, 1);
         stop = 1;
@@ -173,8 +177,8 @@ __device__ __forceinline__ void load_block_t(Blk* S, const double* src, int ld) 
 }
 
 // All 256 threads: S (or its transpose) receives the published block at pub once none of its
-// elements is PUB_EMPTY.  False when the kernel's abort flag is set, or after 2 s, which sets
-// the abort flag and the timeout error bit.
+// elements is PUB_EMPTY.  False when the kernel's abort flag is set, or after the wait limit,
+// which sets the abort flag and the timeout error bit.
 __device__ bool load_pub(const Ctx& c, Blk* S, const double* pub, bool transpose) {
   const int r = threadIdx.x / DB, q = threadIdx.x % DB;
   uint64_t t0 = 0;
@@ -190,7 +194,7 @@ __device__ bool load_pub(const Ctx& c, Blk* S, const double* pub, bool transpose
     if (threadIdx.x == 0) {
       if (it == 0) t0 = global_timer_ns();
       stop = ld_acquire(c.abort_flag);
-      if (!stop && global_timer_ns() - t0 > 2000000000ull) {
+      if (!stop && global_timer_ns() - t0 > c.wait_ns) {
         atomicOr(&c.status[0], DEV_ERR_TIMEOUT);
         atomicExch(c.abort_flag, 1);
         stop = 1;
@@ -328,12 +332,12 @@ __device__ void ffN(const Ctx& c, int gcol, const double* src, double* Lout, dou
   if (t < 32) {
     // alpha_t = prod_{c < t} 2^-k_c t_cc, inclusive shuffle scan over lanes 0 .. N-1
     double x = 1.0;
+    // every pivot is checked (lane t: the block's column t, reported 1-based)
+    if (t < N && !positive(f.piv[t])) atomicMin(&c.status[1], gcol + t + 1);
     if (t >= 1 && t < N) {
       const double p = f.piv[t - 1];
-      if (!positive(p)) atomicMin(&c.status[1], gcol + t);
       x = scale2(p, -expo_pos(p));
     }
-    if (t == 0 && !positive(f.piv[0])) atomicMin(&c.status[1], gcol + 1);
 #pragma unroll
     for (int o = 1; o < N; o <<= 1) {
       const double y = __shfl_up_sync(0xffffffffu, x, o);
@@ -655,6 +659,547 @@ __global__ void __launch_bounds__(256) k_diag_chol(Ctx c, const int4* __restrict
   }
 }
 
+
+// =======================================================================================
+// Double-float executor: the same dataflow (task list, flags, publication buffers, chain
+// CTA), with every block held as a double-float pair hi + lo of FP32 numbers (about 48
+// significant bits; the error-free two-product and two-sum of df.cuh).  It emulates the
+// FP64 diagonal tile on the FP32 units, which on GB300 issue 64 times as many lanes per
+// cycle as the FP64 units and have a dependent latency of a few cycles instead of ~64.
+// The updated tile is read in FP64 where a block is first touched (the tasks of step 0 and
+// the chain's first two blocks); factor, Schur complements, inverse and the substitution's
+// accumulators live in double-float buffers, which k_split_diag_df turns into the FP64
+// factor and inverse and into the FP16 high/low parts the tensor cores read.
+
+struct CtxD {
+  const double* A;        // the updated diagonal tile, FP64 row-major (ld nb); read only
+  float2* L;              // running Schur complements, then the factor's blocks (ld nb)
+  float2* Minv;           // the inverse's blocks (ld nb)
+  float2* W;              // accumulators W_RC of the substitution (ld nb)
+  int nb, NB;
+  int* ver;
+  int* fac;
+  int* inv;
+  int* iver;
+  int* abort_flag;
+  int* status;
+  int gcol0;
+  unsigned long long* amax;   // FP32 bits of max |M| over the high parts (non-negative floats order as unsigned)
+  int* clear_flags;
+  int clear_words;
+  unsigned long long* clear_amax;
+  unsigned long long* pub_m;  // publication buffers as in Ctx, one 64-bit word (hi, lo) per element
+  unsigned long long* pub_l;
+  unsigned long long* clear_pub;
+  unsigned long long wait_ns;
+};
+
+typedef df BlkD[DB + 1];   // padded shared-memory row (17 pairs: conflict-free column reads)
+
+__device__ __forceinline__ df to_df(float2 v) { return {v.x, v.y}; }
+__device__ __forceinline__ float2 to_f2(df v) { return make_float2(v.hi, v.lo); }
+// An FP64 value as a double-float pair: hi = its nearest FP32 number, lo = the FP32 rounding
+// of the remainder (FP64 conversions; only where an original block is first read).
+__device__ __forceinline__ df df_of(double x) {
+  const float h = __double2float_rn(x);
+  return {h, __double2float_rn(x - (double)h)};
+}
+// unbiased exponent of a positive normal FP32 number, 0 for anything else (integer tests)
+__device__ __forceinline__ int expo_f(float x) {
+  const int b = __float_as_int(x);
+  const int ex = (b >> 23) & 0xff;
+  return (b > 0 && ex != 0 && ex != 0xff) ? ex - 127 : 0;
+}
+// 2^e as an FP32 number, -126 <= e <= 127
+__device__ __forceinline__ float pow2f(int e) { return __int_as_float((e + 127) << 23); }
+
+// Dot-product accumulator: the high parts of the products are summed with two-sum (a 4-cycle
+// dependent chain through s), every lower-order term (the products' errors, cross terms and
+// the two-sum errors) in the plain FP32 compensation c.  For K terms the result is accurate
+// to about K 2^-48 of the largest partial sum.
+struct DAcc {
+  float s, c;
+};
+__device__ __forceinline__ void mac(DAcc& a, df x, df y) {
+  const float p = __fmul_rn(x.hi, y.hi);
+  float e = __fmaf_rn(x.hi, y.hi, -p);
+  e = __fmaf_rn(x.hi, y.lo, e);
+  e = __fmaf_rn(x.lo, y.hi, e);
+  const float s = __fadd_rn(a.s, p);
+  const float bb = __fsub_rn(s, a.s);
+  const float t = __fadd_rn(__fsub_rn(a.s, __fsub_rn(s, bb)), __fsub_rn(p, bb));
+  a.s = s;
+  a.c = __fadd_rn(a.c, __fadd_rn(t, e));
+}
+__device__ __forceinline__ df acc_df(DAcc a) { return df_two_sum(a.s, a.c); }
+// x - y and x + y, closed by a full two-sum: a Schur complement cancels, and the faster
+// closing step of df_add assumes the sum's high part dominates
+__device__ __forceinline__ df df_sub(df x, df y) {
+  const df s = df_two_sum(x.hi, -y.hi);
+  return df_two_sum(s.hi, __fadd_rn(s.lo, __fsub_rn(x.lo, y.lo)));
+}
+__device__ __forceinline__ df df_sum(df x, df y) {
+  const df s = df_two_sum(x.hi, y.hi);
+  return df_two_sum(s.hi, __fadd_rn(s.lo, __fadd_rn(x.lo, y.lo)));
+}
+
+// 1/sqrt(x) of a positive double-float: an FP32 estimate and one FP32 Newton step (about 24
+// bits), then one double-float Newton step whose residual 1 - x r^2 is formed from exact
+// products (about 47 bits).
+__device__ __forceinline__ df df_rsqrt(df x) {
+  float r = rsqrtf(x.hi);
+  r = __fmaf_rn(0.5f * r, __fmaf_rn(-__fmul_rn(x.hi, r), r, 1.0f), r);
+  const df y = df_mul_f(x, r);
+  const df z = df_mul_f(y, r);
+  const float h = __fsub_rn(__fsub_rn(1.0f, z.hi), z.lo);
+  return df_quick_two_sum(r, __fmul_rn(__fmul_rn(0.5f, r), h));
+}
+
+// One fraction-free elimination step 2^e (d v - a b) in double-float: the high products split
+// exactly, their difference by two-sum, the cross terms by FMA; sc = 2^e (exact scaling).
+__device__ __forceinline__ df ff_step(df d, df v, df a, df b, float sc) {
+  const float ph = __fmul_rn(d.hi, v.hi);
+  const float pe = __fmaf_rn(d.hi, v.hi, -ph);
+  const float qh = __fmul_rn(a.hi, b.hi);
+  const float qe = __fmaf_rn(a.hi, b.hi, -qh);
+  const df s = df_two_sum(ph, -qh);
+  float lo = __fsub_rn(pe, qe);
+  lo = __fmaf_rn(d.hi, v.lo, lo);
+  lo = __fmaf_rn(d.lo, v.hi, lo);
+  lo = __fmaf_rn(-a.hi, b.lo, lo);
+  lo = __fmaf_rn(-a.lo, b.hi, lo);
+  const df r = df_two_sum(s.hi, __fadd_rn(s.lo, lo));
+  return {__fmul_rn(r.hi, sc), __fmul_rn(r.lo, sc)};
+}
+
+__device__ __forceinline__ unsigned long long df_bits(df x) {
+  return (unsigned long long)__float_as_uint(x.hi) | ((unsigned long long)__float_as_uint(x.lo) << 32);
+}
+__device__ __forceinline__ void st_pub_d(unsigned long long* p, df x) {
+  unsigned long long b = df_bits(x);
+  if (b == PUB_EMPTY) b = 0x7fc000007fc00000ull;   // both halves the quiet NaN
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(b) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_pub_u(const unsigned long long* p) {
+  unsigned long long b;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(b) : "l"(p) : "memory");
+  return b;
+}
+
+__device__ __forceinline__ void fold_amax_d(const CtxD& c, df x) {
+  const unsigned b = __reduce_max_sync(0xffffffffu, __float_as_uint(x.hi) & 0x7fffffffu);
+  if ((threadIdx.x & 31) == 0) atomicMax(c.amax, (unsigned long long)b);
+}
+
+// an original block (FP64) into shared memory as double-float pairs
+__device__ __forceinline__ void load_b64(BlkD* S, const double* src, int ld) {
+  for (int idx = threadIdx.x; idx < DB * DB; idx += blockDim.x) {
+    const int r = idx / DB, q = idx % DB;
+    S[r][q] = df_of(__ldcg(src + (size_t)r * ld + q));
+  }
+}
+__device__ __forceinline__ void load_bdf(BlkD* S, const float2* src, int ld) {
+  for (int idx = threadIdx.x; idx < DB * DB; idx += blockDim.x) {
+    const int r = idx / DB, q = idx % DB;
+    S[r][q] = to_df(__ldcg(src + (size_t)r * ld + q));
+  }
+}
+// S[col][q] = src[q][col]
+__device__ __forceinline__ void load_bdf_t(BlkD* S, const float2* src, int ld) {
+  for (int idx = threadIdx.x; idx < DB * DB; idx += blockDim.x) {
+    const int r = idx / DB, q = idx % DB;
+    S[q][r] = to_df(__ldcg(src + (size_t)r * ld + q));
+  }
+}
+
+// All 256 threads: S (or its transpose) receives the published block once none of its words
+// is PUB_EMPTY; false on abort or after the wait limit (which sets abort and timeout).
+__device__ bool load_pub_d(const CtxD& c, BlkD* S, const unsigned long long* pub, bool transpose) {
+  const int r = threadIdx.x / DB, q = threadIdx.x % DB;
+  uint64_t t0 = 0;
+  for (int it = 0;; ++it) {
+    const unsigned long long b = ld_pub_u(pub + threadIdx.x);
+    if (!__syncthreads_or(b == PUB_EMPTY)) {
+      const df x = {__uint_as_float((unsigned)b), __uint_as_float((unsigned)(b >> 32))};
+      if (transpose) S[q][r] = x;
+      else S[r][q] = x;
+      return true;
+    }
+    int stop = 0;
+    if (threadIdx.x == 0) {
+      if (it == 0) t0 = global_timer_ns();
+      stop = ld_acquire(c.abort_flag);
+      if (!stop && global_timer_ns() - t0 > c.wait_ns) {
+        atomicOr(&c.status[0], DEV_ERR_TIMEOUT);
+        atomicExch(c.abort_flag, 1);
+        stop = 1;
+      }
+    }
+    if (__syncthreads_or(stop)) return false;
+  }
+}
+
+struct FFSD {
+  df col[2][DB];   // column c of the working matrix, double-buffered by step parity
+  df row[2][DB];   // row c of the transformed identity
+  df piv[DB];
+  df alpha[DB];
+  df r[DB];
+};
+
+// The fraction-free factorisation of ffN (same element map, same steps, same closing scan of
+// the normalised pivots) in double-float arithmetic.  src: the block (lower part), Lout
+// receives L (lower part), Xout L^-1 (upper part zero).
+__device__ void ffD(const CtxD& c, int gcol, const BlkD* src, BlkD* Lout, BlkD* Xout, FFSD& f) {
+  const int t = threadIdx.x;
+  const int code = c_elem_map.code[t];
+  const bool isT = (code >> 8) != 0;
+  const int i = (code >> 4) & 15, j = code & 15;
+  df v = isT ? src[i][j] : df{0.0f, 0.0f};
+  for (int col = 0; col < DB; ++col) {
+    const int par = col & 1;
+    if (isT && j == col) {
+      f.col[par][i] = v;
+      if (i == col) f.piv[col] = v;
+    }
+    if (!isT && i == col) f.row[par][j] = v;
+    __syncthreads();
+    const df d = f.col[par][col];
+    const df a = f.col[par][i];
+    const df b = isT ? f.col[par][j] : (j == col ? df{1.0f, 0.0f} : f.row[par][j]);
+    const bool act = isT ? (j > col) : (i > col && j <= col);
+    const float sc = pow2f(max(-expo_f(d.hi), -126));
+    if (__any_sync(0xffffffffu, act)) {
+      const df nv = ff_step(d, v, a, b, sc);
+      v = act ? nv : v;
+    }
+  }
+  __syncthreads();
+  if (t < 32) {
+    df x = {1.0f, 0.0f};
+    // every pivot is checked (lane t: the block's column t, reported 1-based)
+    if (t < DB && !(f.piv[t].hi > 0.0f)) atomicMin(&c.status[1], gcol + t + 1);
+    if (t >= 1 && t < DB) {
+      const df p = f.piv[t - 1];
+      const float s = pow2f(max(-expo_f(p.hi), -126));
+      x = {__fmul_rn(p.hi, s), __fmul_rn(p.lo, s)};
+    }
+#pragma unroll
+    for (int o = 1; o < DB; o <<= 1) {
+      const df y = {__shfl_up_sync(0xffffffffu, x.hi, o), __shfl_up_sync(0xffffffffu, x.lo, o)};
+      if (t >= o) x = df_mul(x, y);
+    }
+    if (t < DB) {
+      f.alpha[t] = x;
+      f.r[t] = df_rsqrt(df_mul(x, f.piv[t]));
+    }
+  }
+  __syncthreads();
+  if (isT) {
+    Lout[i][j] = df_mul(v, f.r[j]);
+    if (i != j) Xout[j][i] = df{0.0f, 0.0f};
+    else Xout[i][i] = df_mul(f.r[i], f.alpha[i]);
+  } else {
+    Xout[i][j] = df_mul(df_mul(f.r[i], v), f.alpha[j]);
+  }
+  __syncthreads();
+}
+
+struct FFSharedD {
+  union {
+    df part[2][NT_LOWER];   // halves of the fused symmetric update
+    BlkD l16[DB];           // the factor of the diagonal block
+  };
+  FFSD f;
+};
+
+// Lower element t of diagonal block k, 0 for the other threads: from the FP64 tile for the
+// two blocks nothing has updated yet (k <= 1), else from the double-float buffer.
+__device__ __forceinline__ df diag_elem_d(const CtxD& c, int k) {
+  const int t = threadIdx.x;
+  if (t >= NT_LOWER) return {0.0f, 0.0f};
+  const int i = tri_row(t);
+  const int j = t - i * (i + 1) / 2;
+  const size_t o = (size_t)(k * DB + i) * c.nb + k * DB + j;
+  return k <= 1 ? df_of(__ldcg(c.A + o)) : to_df(__ldcg(c.L + o));
+}
+
+// potrf16 in double-float: factor and inverse of diagonal block k after subtracting P P^T.
+__device__ void potrf16_d(const CtxD& c, int k, df v, const BlkD* P, BlkD* A16, BlkD* X, FFSharedD& sh) {
+  const int t = threadIdx.x;
+  if (P) {
+    auto half_sum = [&](int item) {
+      const int e = item >> 1, q0 = (item & 1) * (DB / 2);
+      const int ii = tri_row(e);
+      const int jj = e - ii * (ii + 1) / 2;
+      DAcc a{0.0f, 0.0f};
+#pragma unroll
+      for (int q = 0; q < DB / 2; ++q) mac(a, P[ii][q0 + q], P[jj][q0 + q]);
+      sh.part[item & 1][e] = acc_df(a);
+    };
+    half_sum(t);
+    if (t < 2 * (NT_LOWER - 128)) half_sum(256 + t);
+    __syncthreads();
+  }
+  if (t < NT_LOWER) {
+    const int i = tri_row(t);
+    const int j = t - i * (i + 1) / 2;
+    if (P) v = df_sub(v, df_sum(sh.part[0][t], sh.part[1][t]));
+    A16[i][j] = v;
+  }
+  __syncthreads();
+  ffD(c, c.gcol0 + k * DB, A16, sh.l16, X, sh.f);
+  {
+    const int i = t / DB, j = t % DB;
+    const size_t o = (size_t)(k * DB + i) * c.nb + k * DB + j;
+    c.Minv[o] = to_f2(X[i][j]);
+    st_pub_d(c.pub_m + k * DB * DB + t, X[i][j]);
+    c.L[o] = j <= i ? to_f2(sh.l16[i][j]) : make_float2(0.0f, 0.0f);
+    fold_amax_d(c, X[i][j]);
+  }
+}
+
+// sum over q <= cc of P[r][q] M[cc][q] (M lower)
+__device__ __forceinline__ df trsm_elem_d(const BlkD* P, const BlkD* M, int r, int cc) {
+  DAcc a{0.0f, 0.0f};
+  for (int q = 0; q <= cc; ++q) mac(a, P[r][q], M[cc][q]);
+  return acc_df(a);
+}
+// sum_q P[r][q] Q[col][q] for (r, col) = (tid / 16, tid % 16)
+__device__ __forceinline__ df gemm_elem_d(const BlkD* P, const BlkD* Q) {
+  const int r = threadIdx.x / DB, col = threadIdx.x % DB;
+  DAcc a{0.0f, 0.0f};
+#pragma unroll
+  for (int q = 0; q < DB; ++q) mac(a, P[r][q], Q[col][q]);
+  return acc_df(a);
+}
+
+// The critical chain of run_chain in double-float.
+__device__ void run_chain_d(const CtxD& c, BlkD* S0, BlkD* S1, BlkD* S2, BlkD* S3, FFSharedD& sh, int* s_ok) {
+  const int NB = c.NB;
+  potrf16_d(c, 0, diag_elem_d(c, 0), nullptr, S0, S1, sh);   // S1 = M_00, published
+  __syncthreads();
+  int r, cc;
+  trsm_owner(r, cc);
+  for (int k = 0; k + 1 < NB; ++k) {
+    const int i = k + 1;
+    if (threadIdx.x < 32) {
+      const int lane = threadIdx.x;
+      const bool ok = warp_wait_ge(c, lane < 2 ? &c.ver[i * NB + (lane ? i : k)] : nullptr, k);
+      if (lane == 0) *s_ok = ok ? 1 : 0;
+    }
+    __syncthreads();
+    if (!*s_ok) return;
+    const size_t oik = (size_t)(i * DB) * c.nb + k * DB;
+    const df vii = diag_elem_d(c, i);
+    if (k == 0) load_b64(S2, c.A + oik, c.nb);
+    else load_bdf(S2, c.L + oik, c.nb);
+    __syncthreads();
+    const df l = trsm_elem_d(S2, S1, r, cc);   // L_ik = A_ik M_kk^T
+    S3[r][cc] = l;
+    c.L[oik + (size_t)r * c.nb + cc] = to_f2(l);
+    st_pub_d(c.pub_l + k * DB * DB + r * DB + cc, l);
+    __syncthreads();
+    potrf16_d(c, i, vii, S3, S0, S1, sh);       // UPDATE(i,i,k) fused; S1 = M_ii, published
+    __syncthreads();
+  }
+}
+
+__global__ void __launch_bounds__(256) k_diag_chol_df(CtxD c, const int4* __restrict__ tasks, int ntasks, int* counter,
+                                                      int* role) {
+  __shared__ BlkD S0[DB];
+  __shared__ BlkD S1[DB];
+  __shared__ BlkD S2[DB];
+  __shared__ BlkD S3[DB];
+  __shared__ FFSharedD sh;
+  __shared__ int s_task;
+  __shared__ int s_ok;
+  __shared__ int4 s_tk;
+  const int NB = c.NB;
+  const size_t rowstride = (size_t)DB * c.nb;
+  if (threadIdx.x == 0) s_task = atomicAdd(role, 1);
+  __syncthreads();
+  if (s_task == 0) {
+    run_chain_d(c, S0, S1, S2, S3, sh, &s_ok);
+    return;
+  }
+  {
+    // the next call's flags, abs-max and publication buffers (no zeroing of upper blocks:
+    // nothing reads them, and the FP64 outputs are written by the split kernel)
+    const int q = s_task - 1, nq = gridDim.x - 1;
+    for (int w = q * 256 + threadIdx.x; w < c.clear_words; w += nq * 256) c.clear_flags[w] = 0;
+    if (q == 0 && threadIdx.x == 0) *c.clear_amax = 0ull;
+    for (int w = q * 256 + threadIdx.x; w < 2 * NB * DB * DB; w += nq * 256) c.clear_pub[w] = PUB_EMPTY;
+  }
+  const int lane = threadIdx.x & 31;
+  int claim = 0;
+  if (threadIdx.x == 32) claim = atomicAdd(counter, 1);
+  while (true) {
+    if (threadIdx.x >= 32 && threadIdx.x < 64) {
+      int t = 0;
+      if (lane == 0) {
+        t = claim;
+        if (t < ntasks) claim = atomicAdd(counter, 1);
+      }
+      t = __shfl_sync(0xffffffffu, t, 0);
+      bool ok = true;
+      if (t < ntasks) {
+        const int4 tk = tasks[t];
+        const int* fp = nullptr;
+        int fv = 0;
+        task_flag(c, tk, lane, fp, fv);
+        ok = warp_wait_ge(c, fp, fv);
+        if (lane == 0) s_tk = tk;
+      }
+      if (lane == 0) {
+        s_task = t;
+        s_ok = ok ? 1 : 0;
+      }
+    }
+    __syncthreads();
+    const int t = s_task;
+    if (t >= ntasks || !s_ok) break;
+    const int4 tk = s_tk;
+    const int type = tk.x;
+    if (type == T_TRSM) {
+      const int i = tk.y, k = tk.w;
+      const size_t o = i * rowstride + k * DB;
+      if (k == 0) load_b64(S0, c.A + o, c.nb);
+      else load_bdf(S0, c.L + o, c.nb);
+      if (!load_pub_d(c, S1, c.pub_m + k * DB * DB, false)) break;
+      __syncthreads();
+      int r, cc;
+      trsm_owner(r, cc);
+      c.L[o + (size_t)r * c.nb + cc] = to_f2(trsm_elem_d(S0, S1, r, cc));
+    } else {
+      const int r = threadIdx.x / DB, col = threadIdx.x % DB;
+      if (type == T_UPDATE) {
+        const int i = tk.y, j = tk.z, k = tk.w;
+        const size_t o = i * rowstride + j * DB + (size_t)r * c.nb + col;
+        const bool live = !(i == j && col > r);
+        // the destination is read with the operands: only this task writes it until its flag
+        df d = {0.0f, 0.0f};
+        if (live) d = k == 0 ? df_of(__ldcg(c.A + o)) : to_df(__ldcg(c.L + o));
+        load_bdf(S0, c.L + i * rowstride + k * DB, c.nb);
+        if (j == k + 1) {
+          if (!load_pub_d(c, S1, c.pub_l + k * DB * DB, false)) break;
+        } else {
+          load_bdf(S1, c.L + j * rowstride + k * DB, c.nb);
+        }
+        __syncthreads();
+        const df p = gemm_elem_d(S0, S1);
+        if (live) c.L[o] = to_f2(df_sub(d, p));
+      } else if (type == T_UPDATE2) {
+        const int i = tk.y, j = tk.z, k = tk.w;
+        const size_t o = i * rowstride + j * DB + (size_t)r * c.nb + col;
+        const bool live2 = !(i == j + 1 && col > r);
+        df d1, d2 = {0.0f, 0.0f};
+        if (k == 0) {
+          d1 = df_of(__ldcg(c.A + o));
+          if (live2) d2 = df_of(__ldcg(c.A + o + DB));
+        } else {
+          d1 = to_df(__ldcg(c.L + o));
+          if (live2) d2 = to_df(__ldcg(c.L + o + DB));
+        }
+        load_bdf(S0, c.L + i * rowstride + k * DB, c.nb);
+        if (j == k + 1) {
+          if (!load_pub_d(c, S1, c.pub_l + k * DB * DB, false)) break;
+        } else {
+          load_bdf(S1, c.L + j * rowstride + k * DB, c.nb);
+        }
+        load_bdf(S2, c.L + (j + 1) * rowstride + k * DB, c.nb);
+        __syncthreads();
+        DAcc a{0.0f, 0.0f}, b{0.0f, 0.0f};
+#pragma unroll
+        for (int q = 0; q < DB; ++q) {
+          const df x = S0[r][q];
+          mac(a, x, S1[col][q]);
+          mac(b, x, S2[col][q]);
+        }
+        c.L[o] = to_f2(df_sub(d1, acc_df(a)));
+        if (live2) c.L[o + DB] = to_f2(df_sub(d2, acc_df(b)));
+      } else if (type == T_IUPD) {
+        // W_RC (+)= L_Rm M_mC
+        const int R = tk.y, C = tk.z, m = tk.w;
+        const size_t o = R * rowstride + C * DB + (size_t)r * c.nb + col;
+        const df d = (m == C) ? df{0.0f, 0.0f} : to_df(__ldcg(c.W + o));
+        if (R == m + 1) {
+          if (!load_pub_d(c, S0, c.pub_l + m * DB * DB, false)) break;
+        } else {
+          load_bdf(S0, c.L + R * rowstride + m * DB, c.nb);
+        }
+        if (m == C) {
+          if (!load_pub_d(c, S1, c.pub_m + C * DB * DB, true)) break;
+        } else {
+          load_bdf_t(S1, c.Minv + m * rowstride + C * DB, c.nb);
+        }
+        __syncthreads();
+        const df p = gemm_elem_d(S0, S1);
+        c.W[o] = to_f2((m == C) ? p : df_sum(d, p));
+      } else {
+        // M_RC = -M_RR W_RC
+        const int R = tk.y, C = tk.z;
+        if (!load_pub_d(c, S0, c.pub_m + R * DB * DB, false)) break;
+        load_bdf_t(S1, c.W + R * rowstride + C * DB, c.nb);
+        __syncthreads();
+        const df mv = df_neg(gemm_elem_d(S0, S1));
+        c.Minv[R * rowstride + C * DB + (size_t)r * c.nb + col] = to_f2(mv);
+        fold_amax_d(c, mv);
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      if (type == T_TRSM) st_release(&c.fac[tk.y * NB + tk.w], 1);
+      else if (type == T_UPDATE) st_release(&c.ver[tk.y * NB + tk.z], tk.w + 1);
+      else if (type == T_UPDATE2) {
+        st_release(&c.ver[tk.y * NB + tk.z], tk.w + 1);
+        st_release(&c.ver[tk.y * NB + tk.z + 1], tk.w + 1);
+      }
+      else if (type == T_IUPD) st_release(&c.iver[tk.y * NB + tk.z], tk.w - tk.z + 1);
+      else st_release(&c.inv[tk.y * NB + tk.z], 1);
+    }
+  }
+}
+
+// The double-float factor and inverse of one tile into FP64 (lower parts; zero above) and
+// into the FP16 high/low parts of M 2^eM and of L, as k_split_diag does from FP64: eM with
+// max|M| 2^eM < 2^14 (status[2] = eM) from the executor's maximum (FP32 bits of the high
+// parts).  Elements [0, nb^2) are M, [nb^2, 2 nb^2) are L, two adjacent ones per thread.
+// The FP16 parts of an element x = hi + lo (scaled) are h = fp16(hi) and fp16((hi - h) + lo).
+__global__ void __launch_bounds__(256) k_split_diag_df(const float2* __restrict__ Mdf, const float2* __restrict__ Ldf,
+                                                       int nb, const unsigned long long* __restrict__ amax,
+                                                       double* __restrict__ M64, double* __restrict__ L64,
+                                                       __half* __restrict__ mh, __half* __restrict__ ml,
+                                                       __half* __restrict__ lh, __half* __restrict__ ll, int* status) {
+  const unsigned bits = (unsigned)*amax;
+  const int ef = (int)((bits >> 23) & 0xff);   // max |M| in [2^(ef-127), 2^(ef-126))
+  const int e = (bits == 0 || ef == 0 || ef == 0xff) ? 0 : 14 - (ef - 126);
+  if (blockIdx.x == 0 && threadIdx.x == 0) status[2] = e;
+  const float sc = ldexpf(1.0f, e);
+  const size_t half_count = (size_t)nb * nb / 2;
+  for (size_t pidx = blockIdx.x * 256 + threadIdx.x; pidx < 2 * half_count; pidx += (size_t)gridDim.x * 256) {
+    const bool isM = pidx < half_count;
+    const size_t q = isM ? pidx : pidx - half_count;
+    const int r = (int)(2 * q / nb), c0 = (int)(2 * q % nb);
+    const float4 v = reinterpret_cast<const float4*>(isM ? Mdf : Ldf)[q];
+    const bool z0 = c0 > r, z1 = c0 + 1 > r;
+    const double d0 = z0 ? 0.0 : (double)v.x + (double)v.y;
+    const double d1 = z1 ? 0.0 : (double)v.z + (double)v.w;
+    reinterpret_cast<double2*>(isM ? M64 : L64)[q] = make_double2(d0, d1);
+    __half* h = isM ? mh : lh;
+    __half* l = isM ? ml : ll;
+    if (h) {
+      const float s = isM ? sc : 1.0f;
+      const float x0 = z0 ? 0.0f : v.x * s, x1 = z1 ? 0.0f : v.z * s;
+      const float y0 = z0 ? 0.0f : v.y * s, y1 = z1 ? 0.0f : v.w * s;
+      const __half2 hv = __floats2half2_rn(x0, x1);
+      const float2 hf = __half22float2(hv);
+      reinterpret_cast<__half2*>(h)[q] = hv;
+      reinterpret_cast<__half2*>(l)[q] = __floats2half2_rn((x0 - hf.x) + y0, (x1 - hf.y) + y1);
+    }
+  }
+}
+
 }  // namespace
 
 bool diag_task_list(int NB, std::vector<int4>& tasks) {
@@ -747,7 +1292,7 @@ bool diag_task_list(int NB, std::vector<int4>& tasks) {
 
 cr_status diag_chol_launch(int db, double* A, double* Minv, double* W, int nb, int gcol0, int* status, int* flags,
                            int par, double* pub, const int4* d_tasks, int ntasks, int grid, unsigned long long* amax,
-                           cudaStream_t s) {
+                           unsigned long long wait_ns, cudaStream_t s) {
   if (db != DB || nb % DB != 0 || grid < 2) return fail(CR_ERR_ARG, "diag_chol_launch: block size 16 dividing nb and at least 2 CTAs");
   const int NB = nb / db;
   const int words = diag_flag_words(nb, db);
@@ -767,6 +1312,7 @@ cr_status diag_chol_launch(int db, double* A, double* Minv, double* W, int nb, i
   int* counter = flags + 4 * NB * NB + 1;
   int* role = flags + 4 * NB * NB + 2;
   c.status = status; c.gcol0 = gcol0; c.amax = amax;
+  c.wait_ns = wait_ns;
   static bool configured = false;
   if (!configured) {
     // same shared-memory carveout as the tensor-core kernel, so these small CTAs can share
@@ -779,6 +1325,53 @@ cr_status diag_chol_launch(int db, double* A, double* Minv, double* W, int nb, i
     k_diag_chol<<<grid, 256, 0, s>>>(c, d_tasks, ntasks, counter, role);
   }
   CR_CHECK_LAUNCH("k_diag_chol");
+  return CR_OK;
+}
+
+cr_status diag_chol_df_launch(int db, const double* A, float2* Ldf, float2* Mdf, float2* Wdf, int nb, int gcol0,
+                              int* status, int* flags, int par, double* pub, const int4* d_tasks, int ntasks, int grid,
+                              unsigned long long* amax, unsigned long long wait_ns, cudaStream_t s) {
+  if (db != DB || nb % DB != 0 || grid < 2) return fail(CR_ERR_ARG, "diag_chol_df_launch: block size 16 dividing nb and at least 2 CTAs");
+  const int NB = nb / db;
+  const int words = diag_flag_words(nb, db);
+  CtxD c;
+  c.A = A; c.L = Ldf; c.Minv = Mdf; c.W = Wdf; c.nb = nb; c.NB = NB;
+  int* cur = flags + (size_t)(par & 1) * words;
+  c.clear_flags = flags + (size_t)((par & 1) ^ 1) * words;
+  c.clear_words = words;
+  c.clear_amax = amax + ((par & 1) ^ 1);
+  unsigned long long* pub64 = reinterpret_cast<unsigned long long*>(pub);
+  c.pub_m = pub64 + (size_t)(par & 1) * diag_pub_doubles(nb, db) / 2;
+  c.pub_l = c.pub_m + (size_t)NB * DB * DB;
+  c.clear_pub = pub64 + (size_t)((par & 1) ^ 1) * diag_pub_doubles(nb, db) / 2;
+  c.amax = amax + (par & 1);
+  c.ver = cur; c.fac = cur + NB * NB; c.inv = cur + 2 * NB * NB; c.iver = cur + 3 * NB * NB;
+  c.abort_flag = cur + 4 * NB * NB;
+  int* counter = cur + 4 * NB * NB + 1;
+  int* role = cur + 4 * NB * NB + 2;
+  c.status = status; c.gcol0 = gcol0;
+  c.wait_ns = wait_ns;
+  static bool configured = false;
+  if (!configured) {
+    CR_CUDA(cudaFuncSetAttribute(k_diag_chol_df, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared));
+    configured = true;
+  }
+  {
+    TimedScope ts("k_diag_chol_df", s);
+    k_diag_chol_df<<<grid, 256, 0, s>>>(c, d_tasks, ntasks, counter, role);
+  }
+  CR_CHECK_LAUNCH("k_diag_chol_df");
+  return CR_OK;
+}
+
+cr_status split_diag_df_launch(const float2* Mdf, const float2* Ldf, int nb, const unsigned long long* amax, double* M64,
+                               double* L64, __half* mh, __half* ml, __half* lh, __half* ll, int* status, cudaStream_t s) {
+  const unsigned grid = (unsigned)(((size_t)nb * nb + 255) / 256);   // 2 nb^2 / 2 pairs, 256 per CTA
+  {
+    TimedScope ts("k_split_diag_df", s);
+    k_split_diag_df<<<grid, 256, 0, s>>>(Mdf, Ldf, nb, amax, M64, L64, mh, ml, lh, ll, status);
+  }
+  CR_CHECK_LAUNCH("k_split_diag_df");
   return CR_OK;
 }
 

@@ -31,8 +31,26 @@ bool diag_task_list(int NB, std::vector<int4>& tasks);
 // doubles; parity par must be all-ones bytes on entry and receives the chain's published
 // blocks, parity 1 - par is refilled with all-ones bytes.  Calls alternate par, and every
 // set is in its entry state before the first call.
+// wait_ns: limit of every device-side wait (the executor aborts with the timeout bit).
 cr_status diag_chol_launch(int db, double* A, double* Minv, double* W, int nb, int gcol0, int* status, int* flags,
                            int par, double* pub, const int4* d_tasks, int ntasks, int grid, unsigned long long* amax,
-                           cudaStream_t s);
+                           unsigned long long wait_ns, cudaStream_t s);
+
+// The same factorisation in double-float arithmetic (FP64 emulated on the FP32 units, about
+// 48 significant bits).  A (FP64, nb x nb row-major, lower part) is only read.  Ldf and Mdf
+// (nb x nb float2 pairs hi, lo, row-major) receive L and L^-1 in their lower parts (the
+// strictly upper 16 x 16 blocks are left as they were), Wdf is nb x nb float2 scratch.
+// amax[par] (zero on entry) receives the FP32 bits of max |L^-1| over the high parts; flags,
+// pub and the parity rule as for diag_chol_launch (the same buffers serve both).
+cr_status diag_chol_df_launch(int db, const double* A, float2* Ldf, float2* Mdf, float2* Wdf, int nb, int gcol0,
+                              int* status, int* flags, int par, double* pub, const int4* d_tasks, int ntasks, int grid,
+                              unsigned long long* amax, unsigned long long wait_ns, cudaStream_t s);
+
+// After diag_chol_df_launch: L64 and M64 (FP64 nb x nb row-major) receive the factor and the
+// inverse with zero upper parts; when mh is not NULL, mh/ml receive the FP16 high/low parts of
+// L^-1 2^eM and lh/ll those of L, with eM (status[2]) chosen from *amax so that
+// max |L^-1| 2^eM < 2^14.
+cr_status split_diag_df_launch(const float2* Mdf, const float2* Ldf, int nb, const unsigned long long* amax, double* M64,
+                               double* L64, __half* mh, __half* ml, __half* lh, __half* ll, int* status, cudaStream_t s);
 
 }  // namespace cr

@@ -86,6 +86,32 @@ def test_headline_workload_full_size(lib):
     # sampled rows at full K-chain length against the GPU's own factor
     rows = np.sort(rng.choice(w.n, 12, replace=False))
     Lr = Ld[torch.from_numpy(rows).cuda()].cpu().numpy() / s
+    # far tiles of the factor against the oracle's covariance: (L_s L_s^T)_ij, formed on the
+    # host from the stored factor's block rows, against s^2 V_ij.  Every product of the
+    # factorisation is taken at least at FP16 precision (unit roundoff 2^-11) with FP32 or
+    # FP64 accumulation and every stored tile is rounded at most to FP16, so the backward
+    # error of a tile obeys ||E_ij||_F <= c 2^-10 sum_k ||L_ik||_F ||L_jk||_F
+    # <= c 2^-10 s^2 sqrt(tr V_ii tr V_jj) (Cauchy-Schwarz; ||L_i,:||_F^2 = s^2 tr V_ii); c = 2
+    nb, nt = w.nb, w.n // w.nb
+    pairs = {(nt - 1, nt - 1), (nt - 1, 0), (nt - 1, nt - 2), (nt - 1, nt // 2), (nt // 2, nt // 2 - 1)}
+    while len(pairs) < 16:
+        i = int(rng.integers(1, nt))
+        pairs.add((i, int(rng.integers(0, i + 1))))
+    tr = nb * (w.sigma2 + w.nugget)
+    worst = 0.0
+    for (i, j) in sorted(pairs):
+        Li = Ld[i * nb:(i + 1) * nb, :(j + 1) * nb].cpu().numpy()
+        Lj = Ld[j * nb:(j + 1) * nb, :(j + 1) * nb].cpu().numpy()
+        P = Li @ Lj.T
+        if i == j:
+            P = np.tril(P)
+        T = oracle.covariance_matrix(xy, w.family, w.sigma2, w.beta, w.nu, w.nugget,
+                                     rows=slice(i * nb, (i + 1) * nb), cols=slice(j * nb, (j + 1) * nb))
+        T = s * s * (np.tril(T) if i == j else T)
+        ratio = np.linalg.norm(P - T) / (2.0 * 2.0 ** -10 * s * s * tr)
+        worst = max(worst, ratio)
+        assert ratio <= 1.0, (i, j, ratio)
+    print(f"far tiles: worst backward error {worst:.3e} of the bound")
     del Ld
     torch.cuda.empty_cache()
     assert relf(Y[rows], Lr @ Z) <= 2e-3
@@ -155,6 +181,52 @@ def test_strong_correlation_workload_full_size(lib):
     # on FP16 operands in the adaptive mode (Alg.1)
     _leading_block(lib, V, w, xy, Z, Y, info["s"], 2048, 1e-9 if all64 else 1e-2, 1e-2)
     V.close()
+
+
+_ORACLE_FACTOR = {}
+
+
+def _oracle_factor_b512():
+    """The oracle's V and L for config b's geometry (computed once per session)."""
+    if not _ORACLE_FACTOR:
+        w = inputgen.WORKLOADS["b"]
+        xy = inputgen.workload_locations(w)
+        Vo = oracle.covariance_matrix(xy, w.family, w.sigma2, w.beta, w.nu, w.nugget)
+        Lo = oracle.cholesky_lower(Vo)
+        scale = max(1.0, relf(np.linalg.cholesky(Vo), Lo) / 1e-14)
+        _ORACLE_FACTOR.update(xy=xy, Lo=Lo, scale=scale)
+    return _ORACLE_FACTOR
+
+
+@pytest.mark.parametrize("arith", ["fp64", "df"])
+def test_all_fp64_factor_at_product_tile_size(lib, arith):
+    """The all-FP64 mode at the tile size the product runs (nb = 512: 16 x 16 tiles, 32 x 32
+    blocks in each diagonal executor launch), on config b's geometry (8192 jittered grid sites,
+    Matern nu = 1.5, range 0.3, nugget 1e-4): the whole factor and the whole simulation
+    Y = L Z (M = 512) against the oracle at the FP64 gate, 1e-11 relative Frobenius (scaled by
+    the measured FP64 ordering noise between the oracle and LAPACK), with the diagonal tiles in
+    FP64 and in double-float arithmetic."""
+    w = inputgen.WORKLOADS["b"]
+    ref = _oracle_factor_b512()
+    xy, Lo, scale = ref["xy"], ref["Lo"], ref["scale"]
+    nb = 512
+    V = lib.TileMat(w.n, nb)
+    lib.cov_build(V, dev(xy), w.family, w.sigma2, w.beta, w.nu, nugget=w.nugget)
+    lib.precision_map(V, amp=False)
+    mode = lib.CR_DIAG_FP64 if arith == "fp64" else lib.CR_DIAG_DF
+    old = lib.get_option(lib.CR_OPT_DIAG_ARITH)
+    lib.set_option(lib.CR_OPT_DIAG_ARITH, mode)
+    try:
+        assert lib.potrf_adaptive(V) == 0
+    finally:
+        lib.set_option(lib.CR_OPT_DIAG_ARITH, old)
+    L = lib.tilemat_to_dense(V, 1).cpu().numpy()
+    Z = inputgen.standard_normals(w.n, w.M, 7)
+    Y = lib.trmm_sim(V, colmajor(Z), w.M).cpu().numpy()
+    V.close()
+    eL = relf(L, Lo)
+    eY = relf(Y, oracle.simulate(Lo, Z))
+    assert eL <= 1e-11 * scale and eY <= 1e-11 * scale, (arith, eL, eY, scale)
 
 
 def test_scale_sweep_workload_full_size(lib):

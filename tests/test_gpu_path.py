@@ -2,6 +2,8 @@
 values come from oracle/ only.  Tolerances: FP64 paths 1e-11 relative Frobenius (tighter
 where the arithmetic allows), adaptive simulation 1e-2 relative Frobenius on Y, integer and
 index outputs bit-exact."""
+import contextlib
+
 import numpy as np
 import pytest
 import torch
@@ -34,7 +36,20 @@ COV_CASES = {
     "powexp": dict(n=512, nb=128, family="powexp", beta=0.033, nu=0.5, nugget=1e-6, n_pred=None, tau2=0.0),
     # scaled distances up to ~70: the far end of the fast statistics' error bound
     "exp_short": dict(n=1024, nb=128, family="matern", beta=0.02, nu=0.5, nugget=1e-4, n_pred=None, tau2=0.0),
+    # the product's tile size: 32 x 32 blocks per diagonal tile in the executor
+    "nb512": dict(n=2048, nb=512, family="matern", beta=0.03, nu=0.5, nugget=1e-4, n_pred=None, tau2=0.0),
 }
+
+
+@contextlib.contextmanager
+def diag_arith(lib, mode):
+    """Runs the block with the diagonal executor's arithmetic set to `mode` (CR_DIAG_*)."""
+    old = lib.get_option(lib.CR_OPT_DIAG_ARITH)
+    lib.set_option(lib.CR_OPT_DIAG_ARITH, mode)
+    try:
+        yield
+    finally:
+        lib.set_option(lib.CR_OPT_DIAG_ARITH, old)
 
 
 def _build(lib, c, seed=1):
@@ -161,8 +176,57 @@ def test_fp64_cholesky_and_simulation(lib, case):
     V.close()
 
 
+@pytest.mark.parametrize("case", ["a_exp", "ragged_nu15", "nb512"])
+def test_double_float_executor_in_fp64_mode(lib, case):
+    """The diagonal executor in double-float arithmetic (FP64 emulated on the FP32 units, the
+    default of adaptive factorisations) forced into the all-FP64 mode: the factor and the
+    simulations meet the FP64 gate against the oracle, 1e-11 relative Frobenius (scaled by the
+    FP64 ordering noise as in test_fp64_cholesky_and_simulation), and the factor agrees with
+    the FP64 executor's to within the double-float precision."""
+    c = COV_CASES[case]
+    xy, V, Vo = _build(lib, c)
+    lib.precision_map(V, amp=False)
+    with diag_arith(lib, lib.CR_DIAG_DF):
+        assert lib.potrf_adaptive(V) == 0
+    Ldf = lib.tilemat_to_dense(V, 1).cpu().numpy()
+    M = 64
+    Z = inputgen.standard_normals(c["n"], M, 3)
+    Ydf = lib.trmm_sim(V, colmajor(Z), M).cpu().numpy()
+    V.close()
+    xy, V, _ = _build(lib, c)
+    lib.precision_map(V, amp=False)
+    with diag_arith(lib, lib.CR_DIAG_FP64):
+        assert lib.potrf_adaptive(V) == 0
+    L64 = lib.tilemat_to_dense(V, 1).cpu().numpy()
+    V.close()
+    Lo = oracle.cholesky_lower(Vo)
+    scale = max(1.0, relf(np.linalg.cholesky(Vo), Lo) / 1e-14)
+    eL, eY, e64 = relf(Ldf, Lo), relf(Ydf, oracle.simulate(Lo, Z)), relf(Ldf, L64)
+    msg = f"double-float: L {eL:.2e}, Y {eY:.2e}, against the FP64 executor {e64:.2e} (noise x{scale:.1f})"
+    assert eL <= 1e-11 * scale and eY <= 1e-11 * scale, msg
+    assert e64 <= 1e-11 * scale, msg
+
+
+@pytest.mark.parametrize("mode", ["fp64", "df"])
+def test_not_spd_at_the_last_pivot_of_a_block(lib, mode):
+    """A zero pivot at the 16th column of the first diagonal block (the last column of the
+    executor's first 16 x 16 block) is reported as column 16 in both arithmetics.  Sites 14
+    and 15 coincide and are far from sites 0-13 (their covariances underflow to exactly 0),
+    with no nugget: rows 14 and 15 stay equal, with unit entries, through the first 14 steps,
+    so the 16th pivot is 1 - 1 * 1 = 0 exactly."""
+    rng = np.random.default_rng(5)
+    xy = np.vstack([rng.uniform(0.0, 0.3, (14, 2)), [[0.99, 0.99], [0.99, 0.99]], rng.uniform(0.0, 0.3, (240, 2))])
+    V = lib.TileMat(256, 128)
+    lib.cov_build(V, dev(xy), "matern", 1.0, 0.001, 0.5, nugget=0.0)
+    lib.precision_map(V, amp=False)
+    with diag_arith(lib, lib.CR_DIAG_FP64 if mode == "fp64" else lib.CR_DIAG_DF):
+        info = lib.potrf_adaptive(V)
+    assert info == 16
+    V.close()
+
+
 @pytest.mark.parametrize("case,fixedacc", [("a_exp", 1e-6), ("a_exp", 1e-3), ("ragged_nu15", 1e-6), ("nu07", 1e-2),
-                                           ("powexp", 1e-3)])
+                                           ("powexp", 1e-3), ("nb512", 1e-4)])
 def test_adaptive_cholesky_and_simulation(lib, case, fixedacc):
     c = COV_CASES[case]
     xy, V, Vo = _build(lib, c)
@@ -259,14 +323,20 @@ def test_rnorm_stream_matches_oracle(lib):
 def test_generated_simulation_matches_oracle_stream(lib):
     c = COV_CASES["a_exp"]
     xy, V, Vo = _build(lib, c)
-    lib.precision_map(V, amp=True, fixedacc=1e-6)
+    _, info = lib.precision_map(V, amp=True, fixedacc=1e-6)
     assert lib.potrf_adaptive(V) == 0
+    s = info["s"]
     M, seed = 100, 9
     Y, bn = lib.trmm_sim(V, None, M, seed=seed, flags=lib.CR_TRMM_GENERATE, want_bnorm=True)
     Zo = oracle.rnorm(c["n"], M, seed)
     Yo = oracle.simulate(oracle.cholesky_lower(Vo), Zo)
     assert relf(Y.cpu().numpy(), Yo) <= 1e-2
-    s = lib.precision_map.__self__ if False else None
+    # ||B||_F of B = M_rand / s before rounding (Alg.1 step 6): the fused path draws the same
+    # stream in FP32 (about 1e-7 relative per draw) ...
+    assert bn == pytest.approx(np.linalg.norm(Zo) / s, rel=1e-6)
+    # ... and a given FP64 right-hand side is divided as it stands
+    _, bn2 = lib.trmm_sim(V, colmajor(Zo), M, want_bnorm=True)
+    assert bn2 == pytest.approx(np.linalg.norm(Zo) / s, rel=1e-12)
     V.close()
 
 
