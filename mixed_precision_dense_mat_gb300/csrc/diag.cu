@@ -840,38 +840,49 @@ __device__ bool load_pub_d(const CtxD& c, BlkD* S, const unsigned long long* pub
 }
 
 struct FFSD {
-  df col[2][DB];   // column c of the working matrix, double-buffered by step parity
-  df row[2][DB];   // row c of the transformed identity
-  df piv[DB];
+  df cr[2][2][DB];   // [step parity][0: column c of the working matrix, 1: row c of the transformed identity]
+  df piv[DB];        // t_cc
+  float sc[DB];      // 2^-k_c with 2^-k_c t_cc in [1, 2), published by the pivot's owner
   df alpha[DB];
   df r[DB];
 };
 
 // The fraction-free factorisation of ffN (same element map, same steps, same closing scan of
-// the normalised pivots) in double-float arithmetic.  src: the block (lower part), Lout
-// receives L (lower part), Xout L^-1 (upper part zero).
+// the normalised pivots) in double-float arithmetic, arranged for few instructions per step:
+// each element is published at one step (working (i, j) into the column buffer at step j,
+// identity (i, j) into the row buffer at step i), the pivot's owner also publishes the step's
+// power of two and the identity's unit diagonal entry, so that every active element reads its
+// operands from fixed slots, and each element's active steps are a bit mask.  src: the block
+// (lower part), Lout receives L (lower part), Xout L^-1 (upper part zero).
 __device__ void ffD(const CtxD& c, int gcol, const BlkD* src, BlkD* Lout, BlkD* Xout, FFSD& f) {
   const int t = threadIdx.x;
   const int code = c_elem_map.code[t];
   const bool isT = (code >> 8) != 0;
   const int i = (code >> 4) & 15, j = code & 15;
+  // active steps: working (i, j) at col < j; identity (i, j) at j <= col < i
+  const unsigned act = isT ? ((1u << j) - 1u) : (((1u << i) - 1u) & ~((1u << j) - 1u));
+  const int pub_step = isT ? j : i;
+  const int kind = isT ? 0 : 1, pub_idx = isT ? i : j;
+  const bool piv_owner = isT && i == j;
   df v = isT ? src[i][j] : df{0.0f, 0.0f};
   for (int col = 0; col < DB; ++col) {
     const int par = col & 1;
-    if (isT && j == col) {
-      f.col[par][i] = v;
-      if (i == col) f.piv[col] = v;
+    if (pub_step == col) {
+      f.cr[par][kind][pub_idx] = v;
+      if (piv_owner) {
+        f.piv[col] = v;
+        f.sc[col] = pow2f(max(-expo_f(v.hi), -126));
+        f.cr[par][1][col] = df{1.0f, 0.0f};
+      }
     }
-    if (!isT && i == col) f.row[par][j] = v;
     __syncthreads();
-    const df d = f.col[par][col];
-    const df a = f.col[par][i];
-    const df b = isT ? f.col[par][j] : (j == col ? df{1.0f, 0.0f} : f.row[par][j]);
-    const bool act = isT ? (j > col) : (i > col && j <= col);
-    const float sc = pow2f(max(-expo_f(d.hi), -126));
-    if (__any_sync(0xffffffffu, act)) {
-      const df nv = ff_step(d, v, a, b, sc);
-      v = act ? nv : v;
+    const bool on = (act >> col) & 1u;
+    if (__any_sync(0xffffffffu, on)) {   // warp-uniform: idle warps issue no work
+      const df d = f.cr[par][0][col];
+      const df a = f.cr[par][0][i];
+      const df b = f.cr[par][kind][j];
+      const df nv = ff_step(d, v, a, b, f.sc[col]);
+      if (on) v = nv;
     }
   }
   __syncthreads();
@@ -881,7 +892,7 @@ __device__ void ffD(const CtxD& c, int gcol, const BlkD* src, BlkD* Lout, BlkD* 
     if (t < DB && !(f.piv[t].hi > 0.0f)) atomicMin(&c.status[1], gcol + t + 1);
     if (t >= 1 && t < DB) {
       const df p = f.piv[t - 1];
-      const float s = pow2f(max(-expo_f(p.hi), -126));
+      const float s = f.sc[t - 1];
       x = {__fmul_rn(p.hi, s), __fmul_rn(p.lo, s)};
     }
 #pragma unroll
@@ -906,10 +917,7 @@ __device__ void ffD(const CtxD& c, int gcol, const BlkD* src, BlkD* Lout, BlkD* 
 }
 
 struct FFSharedD {
-  union {
-    df part[2][NT_LOWER];   // halves of the fused symmetric update
-    BlkD l16[DB];           // the factor of the diagonal block
-  };
+  BlkD l16[DB];   // the factor of the diagonal block
   FFSD f;
 };
 
@@ -927,24 +935,19 @@ __device__ __forceinline__ df diag_elem_d(const CtxD& c, int k) {
 // potrf16 in double-float: factor and inverse of diagonal block k after subtracting P P^T.
 __device__ void potrf16_d(const CtxD& c, int k, df v, const BlkD* P, BlkD* A16, BlkD* X, FFSharedD& sh) {
   const int t = threadIdx.x;
-  if (P) {
-    auto half_sum = [&](int item) {
-      const int e = item >> 1, q0 = (item & 1) * (DB / 2);
-      const int ii = tri_row(e);
-      const int jj = e - ii * (ii + 1) / 2;
-      DAcc a{0.0f, 0.0f};
-#pragma unroll
-      for (int q = 0; q < DB / 2; ++q) mac(a, P[ii][q0 + q], P[jj][q0 + q]);
-      sh.part[item & 1][e] = acc_df(a);
-    };
-    half_sum(t);
-    if (t < 2 * (NT_LOWER - 128)) half_sum(256 + t);
-    __syncthreads();
-  }
   if (t < NT_LOWER) {
+    // lower element t: its whole update, in two interleaved accumulators
     const int i = tri_row(t);
     const int j = t - i * (i + 1) / 2;
-    if (P) v = df_sub(v, df_sum(sh.part[0][t], sh.part[1][t]));
+    if (P) {
+      DAcc a{0.0f, 0.0f}, b{0.0f, 0.0f};
+#pragma unroll
+      for (int q = 0; q < DB; q += 2) {
+        mac(a, P[i][q], P[j][q]);
+        mac(b, P[i][q + 1], P[j][q + 1]);
+      }
+      v = df_sub(v, df_sum(acc_df(a), acc_df(b)));
+    }
     A16[i][j] = v;
   }
   __syncthreads();
