@@ -34,17 +34,6 @@ sys.path.insert(0, ROOT)
 
 import inputgen  # noqa: E402
 
-FP64_PEAK_TFLOPS = 1.19       # measured DFMA rate on GB300 (profiles/fp64_peak_microbench.md)
-# DRAM bytes per launch from one ncu capture of the kernel as it stands (profiles/); None once
-# the kernel has changed since the capture
-NCU_TRAFFIC_PER_LAUNCH = {
-    "k_diag_chol": 1324032 + 8704,   # profiles/k_diag_chol_n8192.md (one 512 tile per launch at any n)
-    "k_tc_trmm": None,               # profiles/k_tc_trmm_n8192.md covers n = 8192 only (not proportional in n)
-    "k_scan": None,                  # set per workload below: proportional to the rows scanned
-}
-# profiles/k_scan_n32768.md: DRAM bytes of one scan launch at n = 32768, M = 2048; the scan reads
-# S once, so its traffic scales with n M
-SCAN_NCU_BYTES_N32768_M2048 = 537289728 + 3527936
 TIMED_KERNELS = ["k_diag_chol", "k_diag_chol_df", "k_split_diag_df", "k_tc_old", "k_tc_new", "k_tc_trsm", "k_tc_trmm",
                  "k_cov_stats", "k_cov_stats_refine", "k_generate", "k_scan"]
 WORKLOAD = inputgen.WORKLOADS["c"]
@@ -203,6 +192,20 @@ def run_reference(args, world, rank):
 
 
 # ----------------------------------------------------------------------------- GPU path
+def run_peaks(local):
+    """Measured peaks of the arithmetic units the path runs on (cr_peak_probe), best of 3."""
+    import torch
+    import mixed_precision_dense_mat_gb300 as cr
+    torch.cuda.set_device(local)
+    cr.load()
+    out = {}
+    for name, kind in (("fp64_dfma", cr.CR_PEAK_DFMA), ("fp64_dmma", cr.CR_PEAK_DMMA), ("fp32_ffma", cr.CR_PEAK_FFMA),
+                       ("df_mac", cr.CR_PEAK_DF_MAC)):
+        out[name] = max(cr.peak_probe(kind, 4096) for _ in range(3))
+    print(json.dumps({"peaks_tflops": out, "device": torch.cuda.get_device_name(local)}), flush=True)
+
+
+
 def run_ours(args, world, rank, local):
     import torch
     import mixed_precision_dense_mat_gb300 as cr
@@ -240,13 +243,18 @@ def run_ours(args, world, rank, local):
         step(SEED_Z + q, [ev() for _ in range(6)])
     torch.cuda.synchronize()
 
+    # peaks of the units without a measured figure, measured here on this GPU: the FP64
+    # FMA (the tile precision's own peak) and the double-float accumulate the diagonal
+    # executor runs on (its ALU roofline)
+    unit_peaks = {"fp64_dfma": cr.peak_probe(cr.CR_PEAK_DFMA, 2048), "df_mac": cr.peak_probe(cr.CR_PEAK_DF_MAC, 2048)}
+
     gpu_id = os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local] if "CUDA_VISIBLE_DEVICES" in os.environ else str(local)
     clocks = ClockSampler(gpu_id)
     barrier(world)
     torch.cuda.synchronize()
     l0 = cr.kernel_launches()
-    cr.timing_reset()
-    cr.timing_enable(not args.no_kernel_timing)
+    # the timed steps run without per-kernel timing (no events around the library's launches)
+    cr.timing_enable(False)
     evs = [[ev() for _ in range(6)] for _ in range(args.steps)]
     t_start, t_end = ev(), ev()
     wall0 = time.perf_counter()
@@ -257,70 +265,92 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     barrier(world)
     wall = time.perf_counter() - wall0
-    cr.timing_enable(False)
     launches = cr.kernel_launches() - l0
-    ktime = {k: cr.timing_read(k) for k in TIMED_KERNELS}
     clk = clocks.stop()
     total_ms = t_start.elapsed_time(t_end)
     total_ms = max_over_ranks(total_ms, world)
     stages = ["cov_build", "precision_map", "potrf", "rng_trmm", "calibrate"]
     st = {s: float(np.mean([evs[q][k].elapsed_time(evs[q][k + 1]) for q in range(args.steps)])) for k, s in enumerate(stages)}
+    per_step = [evs[q][0].elapsed_time(evs[q][5]) for q in range(args.steps)]
     ms = total_ms / args.steps
     fc, ft = flops(n, M)
     value = world * (fc + ft) / (ms / 1e3) / 1e12
     ct_ms = st["potrf"] + st["rng_trmm"]
     ct_tflops = (fc + ft) / (ct_ms / 1e3) / 1e12
 
+    # a separate pass with per-kernel timing (CUDA events on each kernel's own stream) for the
+    # kernel table and the roofline; its steps are not part of the timed result
+    n_inst = 0 if args.no_kernel_timing else max(1, min(args.steps, 3))
+    ktime = {k: (0.0, 0) for k in TIMED_KERNELS}
+    inst_ms = None
+    if n_inst:
+        cr.timing_reset()
+        cr.timing_enable(True)
+        a, b = ev(), ev()
+        a.record(stream)
+        for q in range(n_inst):
+            step(SEED_Z + 300 + q, [ev() for _ in range(6)])
+        b.record(stream)
+        torch.cuda.synchronize()
+        cr.timing_enable(False)
+        inst_ms = a.elapsed_time(b) / n_inst
+        ktime = {k: cr.timing_read(k) for k in TIMED_KERNELS}
+
     pk = peaks()
     pmap, info = info_box["map"], info_box["info"]
     fch, ftr = attributed_flops(pmap.copy(), nb, n, M)
     p16 = pk["bf16_sus"] * 1e12
-    peak_of = {"fp64": FP64_PEAK_TFLOPS * 1e12, "fp16": p16, "fp32": p16 / 3.0}
+    peak_of = {"fp64": unit_peaks["fp64_dfma"] * 1e12, "fp16": p16, "fp32": p16 / 3.0}
     t_star = sum(fch[k] / peak_of[k] for k in fch) + sum(ftr[k] / peak_of[k] for k in ftr)
     frac_weighted = t_star / (ct_ms / 1e3)
 
-    # per-kernel device time inside the timed region (library events on each kernel's own
-    # stream) and the roofline of each against its algorithmic work per launch
+    # per-kernel device time per step (instrumented pass) and the roofline of each against its
+    # algorithmic work per launch
     kern = {}
+    meas = "measured" if pk["src"] == "measured" else "fallback"
     def entry(name, bound, work_per_launch, unit, peak, peak_note):
         k_ms, cnt = ktime[name]
         if cnt == 0:
             return None
         per = k_ms / cnt
         ach = work_per_launch / (per / 1e3) / (1e12 if unit == "TFLOP/s" else 1e9)
-        return {"kernel": name, "bound": bound, "launches_per_step": cnt / args.steps, "ms_per_launch": per,
-                "ms_per_step": k_ms / args.steps, "achieved": ach, "peak": peak, "unit": unit, "frac": ach / peak,
-                "traffic": NCU_TRAFFIC_PER_LAUNCH.get(name), "peak_source": peak_note}
-    meas = "measured" if pk["src"] == "measured" else "fallback"
-    kern["k_diag_chol"] = entry("k_diag_chol", "alu", 2.0 * nb ** 3 / 3.0, "TFLOP/s", FP64_PEAK_TFLOPS,
-                                "FP64 DFMA rate, own microbenchmark (profiles/fp64_peak_microbench.md); work: "
-                                "nb^3/3 factor + nb^3/3 triangular inverse per launch")
+        return {"kernel": name, "bound": bound, "launches_per_step": cnt / n_inst, "ms_per_launch": per,
+                "ms_per_step": k_ms / n_inst, "achieved": ach, "peak": peak, "unit": unit, "frac": ach / peak,
+                "traffic": None, "peak_source": peak_note}
+    kern["k_diag_chol_df"] = entry("k_diag_chol_df", "alu", 2.0 * nb ** 3 / 3.0, "TFLOP/s", unit_peaks["df_mac"],
+                                   "double-float accumulate rate measured in this run (cr_peak_probe CR_PEAK_DF_MAC); "
+                                   "work: nb^3/3 factor + nb^3/3 triangular inverse per launch")
+    kern["k_diag_chol"] = entry("k_diag_chol", "alu", 2.0 * nb ** 3 / 3.0, "TFLOP/s", unit_peaks["fp64_dfma"],
+                                "FP64 FMA rate measured in this run (cr_peak_probe CR_PEAK_DFMA); "
+                                "work: nb^3/3 factor + nb^3/3 triangular inverse per launch")
     kern["k_tc_trmm"] = entry("k_tc_trmm", "tensor", float(n) ** 2 * M, "TFLOP/s", pk["bf16"],
                               f"{meas} bf16 burst (FP16 MMA runs at the bf16 rate); work: n^2 M per launch")
     kern["k_scan"] = entry("k_scan", "hbm", 8.0 * n * M + 16.0 * n, "GB/s", pk["hbm"],
                            f"{meas} HBM copy bandwidth; work: 8 n M + 16 n bytes per launch")
-    if kern["k_scan"]:
-        kern["k_scan"]["traffic"] = round(SCAN_NCU_BYTES_N32768_M2048 * (n * M) / (32768.0 * 2048.0))
-        kern["k_scan"]["traffic_note"] = "ncu DRAM bytes at n = 32768, M = 2048 (scaled by n M at other sizes)"
-    # the Cholesky's tensor-core kernels together: algorithmic products / their summed time
-    tc_ms = sum(ktime[k][0] for k in ("k_tc_old", "k_tc_new", "k_tc_trsm")) / args.steps
+    # the Cholesky's tensor-core work, over the Cholesky stage's wall time (its launches run on
+    # three concurrent streams, so their summed device time exceeds the stage)
+    tc_ms = sum(ktime[k][0] for k in ("k_tc_old", "k_tc_new", "k_tc_trsm"))
     if tc_ms > 0:
-        ach = (fch["fp16"] + fch["fp32"]) / (tc_ms / 1e3) / 1e12
-        kern["k_tc_cholesky"] = {"kernel": "k_tc_old + k_tc_new + k_tc_trsm", "bound": "tensor", "ms_per_step": tc_ms,
-                                 "achieved": ach, "peak": pk["bf16_sus"], "unit": "TFLOP/s",
-                                 "frac": ach / pk["bf16_sus"], "traffic": None,
+        ach = (fch["fp16"] + fch["fp32"]) / (st["potrf"] / 1e3) / 1e12
+        kern["k_tc_cholesky"] = {"kernel": "k_tc (update and solve modes)", "bound": "tensor",
+                                 "ms_per_step_device_sum": tc_ms / n_inst, "stage_ms": st["potrf"], "achieved": ach,
+                                 "peak": pk["bf16_sus"], "unit": "TFLOP/s", "frac": ach / pk["bf16_sus"], "traffic": None,
                                  "peak_source": f"{meas} bf16 sustained; work: FP16- and FP32-class Cholesky products "
-                                                "(one per product, however many MMAs it takes)"}
-    for k in ("k_tc_old", "k_tc_new", "k_tc_trsm", "k_diag_chol_df", "k_split_diag_df", "k_cov_stats", "k_cov_stats_refine", "k_generate"):
+                                                "(one per product, however many MMAs it takes) over the Cholesky "
+                                                "stage's wall time"}
+    for k in ("k_tc_old", "k_tc_new", "k_tc_trsm", "k_split_diag_df", "k_cov_stats", "k_cov_stats_refine", "k_generate"):
         k_ms, cnt = ktime[k]
         if cnt:
-            kern[k] = {"kernel": k, "ms_per_step": k_ms / args.steps, "launches_per_step": cnt / args.steps}
-    timed = {k: v for k, v in kern.items() if v and "achieved" in v}
+            kern[k] = {"kernel": k, "ms_per_step": k_ms / n_inst, "launches_per_step": cnt / n_inst}
+    # the roofline line: the kernel with the largest device time per step among single kernels
+    # with a stated work per launch (each is at most the step time)
+    timed = {k: v for k, v in kern.items() if v and "ms_per_launch" in v}
     roof = None
     if timed:
         dominant = max(timed.values(), key=lambda e: e["ms_per_step"])
         roof = {key: dominant[key] for key in ("bound", "achieved", "peak", "unit", "frac", "traffic")}
         roof["kernel"] = dominant["kernel"]
+        roof["ms_per_step"] = dominant["ms_per_step"]
         roof["peak_source"] = dominant["peak_source"]
 
     # end to end through the public API with host buffers: H2D of the locations, D2H of
@@ -361,7 +391,9 @@ def run_ours(args, world, rank, local):
             "config": {"workload": w.name, "n": n, "nb": nb, "M": M, "fixedacc": w.fixedacc, "range": w.beta,
                        "nu": w.nu, "nugget": w.nugget, "l2": "working set (tiles > 1 GB) larger than L2; no flush",
                        "parallelism": f"replicas x{world}"},
-            "chol_trmm": {"tflops": ct_tflops, "ms": ct_ms, "x_fp64_peak": ct_tflops / FP64_PEAK_TFLOPS,
+            "ms_per_step_median": float(np.median(per_step)), "ms_per_step_min": float(np.min(per_step)),
+            "ms_per_step_max": float(np.max(per_step)),
+            "chol_trmm": {"tflops": ct_tflops, "ms": ct_ms, "x_fp64_peak": ct_tflops / unit_peaks["fp64_dfma"],
                           "frac_weighted_peak": frac_weighted, "weighted_peak_ms": t_star * 1e3,
                           "flops_by_precision": {k: fch[k] + ftr.get(k, 0.0) for k in fch}},
             "sims_per_s": world * M / (st["rng_trmm"] / 1e3),
@@ -370,6 +402,8 @@ def run_ours(args, world, rank, local):
                               "s": info["s"], "check1": info["check1"], "check2": info["check2"]},
             "roofline": roof,
             "kernels": kern,
+            "unit_peaks_tflops": unit_peaks,
+            "kernel_timing_pass": {"steps": n_inst, "ms_per_step": inst_ms},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": int(xy_h.nbytes),
                     "d2h_bytes_per_step": int(n * (1 + 1 + 4))},
@@ -390,12 +424,16 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-kernel-timing", action="store_true", help="skip the per-kernel device timing (no roofline)")
     ap.add_argument("--n", type=int, default=0, help="profiling only: smaller n of the same workload family")
+    ap.add_argument("--peaks", action="store_true", help="print the arithmetic units' measured peaks and exit")
     args = ap.parse_args()
     global WORKLOAD
     if args.n:
         import dataclasses
         WORKLOAD = dataclasses.replace(WORKLOAD, n_pred=args.n, name=WORKLOAD.name.replace("n=32768", f"n={args.n}"))
     world, rank, local = dist_setup()
+    if args.peaks:
+        run_peaks(local)
+        return
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("gloo")

@@ -135,6 +135,19 @@ enum { CR_DIAG_AUTO = 0, CR_DIAG_FP64 = 1, CR_DIAG_DF = 2 };
 cr_status cr_set_option(int option, long long value);
 cr_status cr_get_option(int option, long long* value);
 
+/* Throughput probe of one arithmetic unit, for the roofline denominators of measurements (the
+ * paper has no counterpart).  Runs a kernel of iters iterations of independent dependency
+ * chains on every SM (8 CTAs of 256 threads per SM), after one warm-up launch, and returns its
+ * rate in TFLOP/s (an FMA or MMA multiply-add counts 2 flops per product term):
+ *   CR_PEAK_DFMA    FP64 FMA on the FP64 units
+ *   CR_PEAK_FFMA    FP32 FMA
+ *   CR_PEAK_DF_MAC  the double-float multiply-accumulate of the diagonal executor (an emulated
+ *                   FP64 FMA: 2 flops per accumulate, about 12 FP32 instructions)
+ *   CR_PEAK_DMMA    FP64 tensor-core MMA (mma.sync m8n8k4)
+ * iters in [1, 2^24]; a few thousand give a launch of some milliseconds.  Synchronises. */
+enum { CR_PEAK_DFMA = 1, CR_PEAK_FFMA = 2, CR_PEAK_DF_MAC = 3, CR_PEAK_DMMA = 4 };
+cr_status cr_peak_probe(int kind, int iters, double* tflops, cr_stream stream);
+
 /* A symmetric n x n matrix stored as its lower tiles (i >= j) of nb x nb entries.
  * NT = ceil(n / nb) tile rows; rows and columns past n are padding and behave like the
  * identity.  nb must be a multiple of 128 with 128 <= nb <= 1024.  The handle owns its

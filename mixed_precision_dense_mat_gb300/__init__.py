@@ -39,6 +39,7 @@ CR_COV_MATERN, CR_COV_POWEXP = 0, 1
 CR_TRMM_FP16_DEST, CR_TRMM_GENERATE, CR_TRMM_SPLIT_L, CR_TRMM_FP16_PER_GEMM = 1, 2, 4, 8
 CR_OPT_WAIT_LIMIT_US, CR_OPT_DIAG_ARITH = 1, 2
 CR_DIAG_AUTO, CR_DIAG_FP64, CR_DIAG_DF = 0, 1, 2
+CR_PEAK_DFMA, CR_PEAK_FFMA, CR_PEAK_DF_MAC, CR_PEAK_DMMA = 1, 2, 3, 4
 STATUS = {0: "CR_OK", 1: "CR_ERR_ARG", 2: "CR_ERR_CUDA", 3: "CR_ERR_NOMEM", 4: "CR_ERR_NOT_SPD",
           5: "CR_ERR_EMPTY_SAMPLE", 6: "CR_ERR_NONPOS_MSPE", 7: "CR_ERR_TIMEOUT", 8: "CR_ERR_STATE",
           9: "CR_ERR_NOT_IMPLEMENTED", 10: "CR_ERR_RANGE"}
@@ -83,6 +84,7 @@ _SIGNATURES = {
     "cr_version": (_I, [ctypes.POINTER(_I), ctypes.POINTER(_I)]),
     "cr_kernel_launches": (_I, [ctypes.POINTER(_U64)]),
     "cr_set_option": (_I, [_I, ctypes.c_longlong]),
+    "cr_peak_probe": (_I, [_I, _I, ctypes.POINTER(_D), _P]),
     "cr_get_option": (_I, [_I, ctypes.POINTER(ctypes.c_longlong)]),
     "cr_timing_enable": (_I, [_I]),
     "cr_timing_read": (_I, [ctypes.c_char_p, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_U64)]),
@@ -175,6 +177,14 @@ def set_option(option: int, value: int) -> None:
     """cr_set_option: CR_OPT_WAIT_LIMIT_US (microseconds) or CR_OPT_DIAG_ARITH (CR_DIAG_*)."""
     load()
     _check(_lib.cr_set_option(option, int(value)))
+
+
+def peak_probe(kind: int, iters: int = 4096, stream=None) -> float:
+    """cr_peak_probe: measured TFLOP/s of one arithmetic unit (CR_PEAK_*)."""
+    load()
+    v = _D(0.0)
+    _check(_lib.cr_peak_probe(kind, iters, ctypes.byref(v), _stream(stream)))
+    return v.value
 
 
 def get_option(option: int) -> int:

@@ -12,7 +12,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libcr.so")
-SOURCES = ["api.cu", "cov.cu", "policy.cu", "fp64.cu", "diag.cu", "tc.cu", "chol.cu", "sim.cu", "calib.cu", "krige.cu"]
+SOURCES = ["api.cu", "cov.cu", "policy.cu", "fp64.cu", "diag.cu", "tc.cu", "chol.cu", "sim.cu", "calib.cu", "krige.cu", "peaks.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=default",
          "--expt-relaxed-constexpr", "-Xptxas", "-v"]

@@ -17,6 +17,8 @@
 // FP64.
 #include <math.h>
 
+#include <cmath>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -642,6 +644,12 @@ cr_status fetch_stats(cr_tilemat V) {
     V->h_stat_err[t] = st[STAT_W * t + 3];
     V->h_stat_exact[t] = st[STAT_W * t + 3] == 0.0;
   }
+  // A non-finite sum of squares means non-finite entries: a NaN or infinite coordinate (the
+  // covariance of finite sites is finite).  Reported here, before any factorisation.
+  for (int t = 0; t < V->ntiles; ++t)
+    if (!std::isfinite(V->h_frob[t]))
+      return fail(CR_ERR_ARG, "covariance statistics not finite (tile " + std::to_string(t) +
+                                  "): a NaN or infinite site coordinate");
   V->stats_on_host = true;
   return CR_OK;
 }

@@ -62,7 +62,9 @@ def test_binding_constants_match_the_header():
     text = open(cr.HEADER).read()
     declared = {m.group(1): int(m.group(2)) for m in re.finditer(r"\b(CR_[A-Z0-9_]+)\s*=\s*(\d+)", text)}
     for name in ("CR_PREC_FP64", "CR_PREC_FP32", "CR_PREC_FP16", "CR_COV_MATERN", "CR_COV_POWEXP",
-                 "CR_TRMM_FP16_DEST", "CR_TRMM_GENERATE", "CR_TRMM_SPLIT_L", "CR_TRMM_FP16_PER_GEMM"):
+                 "CR_TRMM_FP16_DEST", "CR_TRMM_GENERATE", "CR_TRMM_SPLIT_L", "CR_TRMM_FP16_PER_GEMM",
+                 "CR_OPT_WAIT_LIMIT_US", "CR_OPT_DIAG_ARITH", "CR_DIAG_AUTO", "CR_DIAG_FP64", "CR_DIAG_DF",
+                 "CR_PEAK_DFMA", "CR_PEAK_FFMA", "CR_PEAK_DF_MAC", "CR_PEAK_DMMA"):
         assert name in declared, name
         assert getattr(cr, name) == declared[name], name
     for code, name in cr.STATUS.items():
@@ -94,3 +96,22 @@ def test_morton_order_matches_the_input_generator(lib):
     with pytest.raises(cr.CrError) as e:
         cr.morton_order(bad)
     assert e.value.code == 1
+
+
+def test_options_host_side(lib):
+    """cr_set_option / cr_get_option: round trip, range checks and unknown options (host only);
+    cr_peak_probe rejects bad arguments before any device work."""
+    cr.load()
+    v = ctypes.c_longlong()
+    assert cr._lib.cr_get_option(cr.CR_OPT_WAIT_LIMIT_US, ctypes.byref(v)) == 0 and v.value == 2000000
+    assert cr._lib.cr_get_option(cr.CR_OPT_DIAG_ARITH, ctypes.byref(v)) == 0 and v.value == cr.CR_DIAG_AUTO
+    assert cr._lib.cr_set_option(cr.CR_OPT_WAIT_LIMIT_US, 5000) == 0
+    assert cr._lib.cr_get_option(cr.CR_OPT_WAIT_LIMIT_US, ctypes.byref(v)) == 0 and v.value == 5000
+    assert cr._lib.cr_set_option(cr.CR_OPT_WAIT_LIMIT_US, -1) == 1
+    assert cr._lib.cr_set_option(cr.CR_OPT_WAIT_LIMIT_US, 2000000) == 0
+    assert cr._lib.cr_set_option(cr.CR_OPT_DIAG_ARITH, 7) == 1
+    assert cr._lib.cr_set_option(99, 0) == 1 and cr._lib.cr_get_option(99, ctypes.byref(v)) == 1
+    assert cr._lib.cr_get_option(cr.CR_OPT_DIAG_ARITH, None) == 1
+    d = ctypes.c_double()
+    assert cr._lib.cr_peak_probe(cr.CR_PEAK_DFMA, 100, None, None) == 1
+    assert cr._lib.cr_peak_probe(cr.CR_PEAK_DFMA, 0, ctypes.byref(d), None) == 1

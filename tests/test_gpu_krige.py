@@ -34,7 +34,7 @@ def _case(n_o, m, seed, nu=1.0, beta=0.1, tau2=0.01):
     return xy, n_p, X, y, V
 
 
-@pytest.mark.parametrize("n_o,m,nb", [(1024, 32, 128), (1000, 24, 128)])
+@pytest.mark.parametrize("n_o,m,nb", [(1024, 32, 128), (1000, 24, 128), (4096, 64, 512)])
 def test_kriging_matches_oracle(lib, n_o, m, nb):
     xy, n_p, X, y, V = _case(n_o, m, 5)
     G = lib.TileMat(len(xy), nb)
