@@ -291,6 +291,17 @@ cr_status cr_calibrate(const double* d_S, int lds, int n_p, int M, const double*
                        uint8_t* d_cout, int32_t* d_count, double* d_psi, double* d_phi,
                        cr_calib_info* out, cr_stream stream);
 
+/* Calibration of the negative excursion set {Z <= u} (Section III: the method applied to the
+ * sign-reversed field and threshold, -S and -u, with -zhat).  Same arguments, layouts,
+ * outputs, errors and synchronisation as cr_calibrate; the outputs are those of the reversed
+ * problem: t'_i = ((-zhat_i) - (-u)) / sqrt(v_i) = -t_i, psi'_j = min{t'_i : S_ij <= u},
+ * phi'_j = max{t'_i : S_ij >= u}, count_i = #{j : S_ij <= u}, q_out' = Q_{1-level}(psi'),
+ * q_in' = Q_level(phi'), d_cin[i] = t'_i > q_in', d_cout[i] = t'_i >= q_out'. */
+cr_status cr_calibrate_negative(const double* d_S, int lds, int n_p, int M, const double* d_zhat,
+                                const double* d_v, double u, double level, uint8_t* d_cin,
+                                uint8_t* d_cout, int32_t* d_count, double* d_psi, double* d_phi,
+                                cr_calib_info* out, cr_stream stream);
+
 /* Calibration without any allocation.  The paper has no counterpart to this entry point:
  * it exists for callers that cannot allocate device memory themselves, for example code
  * running under a memory pool that owns every device allocation of the process (so a

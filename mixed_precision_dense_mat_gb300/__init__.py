@@ -17,7 +17,7 @@ The functions mirror include/cr.h:
   trmm_sim(V, Z, M, ...)                 cr_trmm_sim
   krige(V, Xo, Xp, yo)                   cr_krige
   krige_correct(W, yo, Y, n_p, n_o)      cr_krige_correct
-  calibrate(S, zhat, v, u, level)        cr_calibrate
+  calibrate(S, zhat, v, u, level)        cr_calibrate (negative=True: cr_calibrate_negative)
   morton_order(xy)                       cr_morton_order (host only)
 The library is never replaced by a fallback: if libcr.so is missing or fails to load, every
 call raises.
@@ -104,6 +104,8 @@ _SIGNATURES = {
     "cr_krige_correct": (_I, [_P, _I, _P, _P, _I, _I, _I, _I, _P, _I, _P]),
     "cr_morton_order": (_I, [_P, _I, _P]),
     "cr_calibrate": (_I, [_P, _I, _I, _I, _P, _P, _D, _D, _P, _P, _P, _P, _P, ctypes.POINTER(CalibInfo), _P]),
+    "cr_calibrate_negative": (_I, [_P, _I, _I, _I, _P, _P, _D, _D, _P, _P, _P, _P, _P, ctypes.POINTER(CalibInfo),
+                                   _P]),
     "cr_calibrate_noalloc": (_I, [_P, _I, _I, _I, _P, _P, _D, _D, _P, _P, _P, _P, _P, ctypes.POINTER(CalibInfo),
                                   _P]),
 }
@@ -356,9 +358,11 @@ def krige_correct(W, yo, Y, n_p: int, n_o: int, out=None, stream=None):
     return out
 
 
-def calibrate(S, zhat, v, u: float, level: float, counts: bool = True, extrema: bool = False, stream=None):
-    """cr_calibrate; returns a dict with q_in, q_out, n_psi, n_phi, c_in, c_out and optionally
-    count, psi, phi (CUDA tensors)."""
+def calibrate(S, zhat, v, u: float, level: float, counts: bool = True, extrema: bool = False, negative: bool = False,
+              stream=None):
+    """cr_calibrate (cr_calibrate_negative with negative=True: the negative excursion set);
+    returns a dict with q_in, q_out, n_psi, n_phi, c_in, c_out and optionally count, psi, phi
+    (CUDA tensors)."""
     import torch
     S, lds = as_colmajor(S)
     n_p, M = S.shape
@@ -368,7 +372,8 @@ def calibrate(S, zhat, v, u: float, level: float, counts: bool = True, extrema: 
     psi = torch.empty(M, dtype=torch.float64, device="cuda") if extrema else None
     phi = torch.empty(M, dtype=torch.float64, device="cuda") if extrema else None
     info = CalibInfo()
-    _check(_lib.cr_calibrate(_ptr(S), lds, n_p, M, _ptr(zhat.contiguous()), _ptr(v.contiguous()), u, level,
+    fn = _lib.cr_calibrate_negative if negative else _lib.cr_calibrate
+    _check(fn(_ptr(S), lds, n_p, M, _ptr(zhat.contiguous()), _ptr(v.contiguous()), u, level,
                              _ptr(cin), _ptr(cout), _ptr(cnt), _ptr(psi), _ptr(phi), ctypes.byref(info),
                              _stream(stream)))
     out = {"q_in": info.q_in, "q_out": info.q_out, "n_psi": info.n_psi, "n_phi": info.n_phi, "c_in": cin,

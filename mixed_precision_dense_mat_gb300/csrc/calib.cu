@@ -24,12 +24,15 @@
 
 namespace cr {
 
+// t_i = (zhat_i - u) / sqrt(v_i); for a negative excursion set (neg != 0) the statistic of the
+// sign-reversed problem, ((-zhat_i) - (-u)) / sqrt(v_i), which is exactly -t_i in IEEE arithmetic.
 __global__ void k_tstat(const double* __restrict__ zhat, const double* __restrict__ v, double u, int n_p, double* __restrict__ t,
-                        int* __restrict__ bad) {
+                        int* __restrict__ bad, int neg) {
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_p; i += gridDim.x * blockDim.x) {
     const double vi = v[i];
     if (!(vi > 0.0)) atomicOr(bad, 1);
-    t[i] = (zhat[i] - u) / sqrt(vi);
+    const double ti = (zhat[i] - u) / sqrt(vi);
+    t[i] = neg ? -ti : ti;
   }
 }
 
@@ -54,9 +57,11 @@ __device__ __forceinline__ unsigned dkey_hi(double x) {
   return hi ^ ((unsigned)((int)hi >> 31) | 0x80000000u);
 }
 
+// neg != 0: the negative excursion set (Section III's sign reversal): -S_ij >= -u is S_ij <= u and
+// -S_ij <= -u is S_ij >= u, so the two decisions swap roles (t holds the reversed statistic).
 __global__ void __launch_bounds__(SCAN_THREADS) k_scan(const double* __restrict__ S, int lds, int n_p, int M,
                                                        const double* __restrict__ t, double u, double* __restrict__ psi_part,
-                                                       double* __restrict__ phi_part, int32_t* __restrict__ count) {
+                                                       double* __restrict__ phi_part, int32_t* __restrict__ count, int neg) {
   constexpr int RPT = SCAN_ROWS / SCAN_THREADS;   // rows per thread
   constexpr unsigned long long KEY_PINF = 0xfff0000000000000ull, KEY_MINF = 0x000fffffffffffffull;
   constexpr unsigned KH_PINF = 0xfff00000u, KH_MINF = 0x000fffffu;   // high words of +-inf (and of some NaNs)
@@ -126,8 +131,9 @@ __global__ void __launch_bounds__(SCAN_THREADS) k_scan(const double* __restrict_
       const unsigned kh = dkey_hi(val[q]);
       const bool finite = (kh - (KH_MINF + 1u)) < (KH_PINF - KH_MINF - 1u);   // strictly between the infinities' words
       const bool slow = (kh - tie_lo) <= tie_w || !finite;
-      const bool ge = !slow && kh > tie_hi;
-      const bool le = !slow && !ge;
+      const bool above = !slow && kh > tie_hi;
+      const bool below = !slow && !above;
+      const bool ge = neg ? below : above, le = neg ? above : below;
       gmask |= ge ? bit[q] : 0u;
       lmask |= le ? bit[q] : 0u;
       cnt[q] += ge ? 1 : 0;
@@ -139,7 +145,8 @@ __global__ void __launch_bounds__(SCAN_THREADS) k_scan(const double* __restrict_
         if (smask & (1u << q)) {
           const unsigned long long kv = dkey(val[q]);
           const bool ok = kv >= KEY_MINF && kv <= KEY_PINF;
-          const bool ge = ok && kv >= ku, le = ok && kv <= ku;
+          const bool above = ok && kv >= ku, below = ok && kv <= ku;
+          const bool ge = neg ? below : above, le = neg ? above : below;
           gmask |= ge ? bit[q] : 0u;
           lmask |= le ? bit[q] : 0u;
           cnt[q] += ge ? 1 : 0;
@@ -234,17 +241,17 @@ double empirical_quantile(std::vector<double>& a, double p) {
 
 cr_status calibrate_core(const double* d_S, int lds, int n_p, int M, const double* d_zhat, const double* d_v, double u,
                          double level, uint8_t* d_cin, uint8_t* d_cout, int32_t* d_count, double* d_psi, double* d_phi,
-                         cr_calib_info* out, cudaStream_t stream, const CalibScratch& sc) {
+                         cr_calib_info* out, cudaStream_t stream, const CalibScratch& sc, int neg) {
   const int nrb = (n_p + SCAN_ROWS - 1) / SCAN_ROWS;
   CR_CUDA(cudaMemsetAsync(sc.bad, 0, sizeof(int), stream));
-  k_tstat<<<std::min(1024, (n_p + 255) / 256), 256, 0, stream>>>(d_zhat, d_v, u, n_p, sc.t, sc.bad);
+  k_tstat<<<std::min(1024, (n_p + 255) / 256), 256, 0, stream>>>(d_zhat, d_v, u, n_p, sc.t, sc.bad, neg);
   CR_CHECK_LAUNCH("k_tstat");
   if (d_count) CR_CUDA(cudaMemsetAsync(d_count, 0, (size_t)n_p * sizeof(int32_t), stream));
   dim3 grid;
   CR_CUDA(scan_grid(n_p, M, &grid));
   {
     TimedScope ts("k_scan", stream);
-    k_scan<<<grid, SCAN_THREADS, 0, stream>>>(d_S, lds, n_p, M, sc.t, u, sc.psi_part, sc.phi_part, d_count);
+    k_scan<<<grid, SCAN_THREADS, 0, stream>>>(d_S, lds, n_p, M, sc.t, u, sc.psi_part, sc.phi_part, d_count, neg);
   }
   CR_CHECK_LAUNCH("k_scan");
   k_scan_reduce<<<std::min(1024, (M + 255) / 256), 256, 0, stream>>>(sc.psi_part, sc.phi_part, nrb, M, sc.psi, sc.phi);
@@ -327,7 +334,18 @@ extern "C" cr_status cr_calibrate(const double* d_S, int lds, int n_p, int M, co
     return fail(CR_ERR_ARG, "cr_calibrate: argument");
   std::lock_guard<std::mutex> lk(g_mu);
   CR_TRY(ensure_scratch(n_p, M));
-  return calibrate_core(d_S, lds, n_p, M, d_zhat, d_v, u, level, d_cin, d_cout, d_count, d_psi, d_phi, out, stream, g_sc);
+  return calibrate_core(d_S, lds, n_p, M, d_zhat, d_v, u, level, d_cin, d_cout, d_count, d_psi, d_phi, out, stream, g_sc, 0);
+}
+
+extern "C" cr_status cr_calibrate_negative(const double* d_S, int lds, int n_p, int M, const double* d_zhat,
+                                           const double* d_v, double u, double level, uint8_t* d_cin, uint8_t* d_cout,
+                                           int32_t* d_count, double* d_psi, double* d_phi, cr_calib_info* out,
+                                           cr_stream stream) {
+  if (!d_S || !d_zhat || !d_v || !d_cin || !d_cout || n_p <= 0 || M <= 0 || lds < n_p || !(level > 0.0 && level < 1.0))
+    return fail(CR_ERR_ARG, "cr_calibrate_negative: argument");
+  std::lock_guard<std::mutex> lk(g_mu);
+  CR_TRY(ensure_scratch(n_p, M));
+  return calibrate_core(d_S, lds, n_p, M, d_zhat, d_v, u, level, d_cin, d_cout, d_count, d_psi, d_phi, out, stream, g_sc, 1);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -412,12 +430,12 @@ extern "C" cr_status cr_calibrate_noalloc(const double* d_S, int lds, int n_p, i
   } while (0)
   NA_CUDA(cudaMemsetAsync(bad, 0, sizeof(int), stream));
   if (d_count) NA_CUDA(cudaMemsetAsync(d_count, 0, (size_t)n_p * sizeof(int32_t), stream));
-  k_tstat<<<std::min(1024, (n_p + 255) / 256), 256, 0, stream>>>(d_zhat, d_v, u, n_p, t, bad);
+  k_tstat<<<std::min(1024, (n_p + 255) / 256), 256, 0, stream>>>(d_zhat, d_v, u, n_p, t, bad, 0);
   count_launch();
   NA_CUDA(cudaGetLastError());
   dim3 grid;
   NA_CUDA(scan_grid(n_p, M, &grid));
-  k_scan<<<grid, SCAN_THREADS, 0, stream>>>(d_S, lds, n_p, M, t, u, psi_part, phi_part, d_count);
+  k_scan<<<grid, SCAN_THREADS, 0, stream>>>(d_S, lds, n_p, M, t, u, psi_part, phi_part, d_count, 0);
   count_launch();
   NA_CUDA(cudaGetLastError());
   k_scan_reduce<<<std::min(1024, (M + 255) / 256), 256, 0, stream>>>(psi_part, phi_part, (int)nrb, M, psi, phi);

@@ -23,7 +23,7 @@ from .simulate import simulate, simulate_fp16_per_product, splitmix64, rnorm
 from .krige import universal_kriging, conditional_correction
 from .calibrate import (standardized_statistic, extrema_scan, exceedance_counts,
                         empirical_quantile, sample_without_sentinels, confidence_regions,
-                        EmptySample, calibrate)
+                        EmptySample, calibrate, calibrate_negative)
 from .coverage import truth_field, excursion_set, coverage_event
 
 __all__ = [
@@ -33,6 +33,6 @@ __all__ = [
     "NotSPD", "cholesky_lower", "solve_lower", "solve_lower_transpose",
     "simulate", "simulate_fp16_per_product", "splitmix64", "rnorm", "universal_kriging", "conditional_correction",
     "standardized_statistic", "extrema_scan", "exceedance_counts", "empirical_quantile",
-    "sample_without_sentinels", "confidence_regions", "EmptySample", "calibrate",
+    "sample_without_sentinels", "confidence_regions", "EmptySample", "calibrate", "calibrate_negative",
     "truth_field", "excursion_set", "coverage_event",
 ]

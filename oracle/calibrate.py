@@ -12,6 +12,8 @@
   * §V-C and Alg.2 steps 21-22: with c = 1 - alpha, q_out = Q_alpha(psi),
     q_in = Q_{1-alpha}(phi); C_out = {t_i >= q_out} (non-strict), C_in = {t_i > q_in}.
   * Per-location exceedance counts count_i = #{j : S_ij >= u} (the exceedance idea of §I).
+  * §III: negative excursion sets {Z <= u} are handled by reversing the sign of the process
+    and of the threshold: calibrate_negative(S, z_hat, v, u) = calibrate(-S, -z_hat, v, -u).
 """
 from __future__ import annotations
 
@@ -78,3 +80,10 @@ def calibrate(S: np.ndarray, z_hat: np.ndarray, v: np.ndarray, u: float, level: 
     return {"t": t, "psi": psi, "phi": phi, "q_in": q_in, "q_out": q_out, "c_in": c_in,
             "c_out": c_out, "count": exceedance_counts(S, u), "n_psi": len(a_psi),
             "n_phi": len(a_phi)}
+
+
+def calibrate_negative(S: np.ndarray, z_hat: np.ndarray, v: np.ndarray, u: float, level: float) -> dict:
+    """Confidence regions of the negative excursion set {Z <= u} (§III: the method applied to the
+    sign-reversed field -Z and threshold -u).  t, psi, phi, q_in, q_out and the regions are
+    those of the reversed problem; count_i = #{j : -S_ij >= -u} = #{j : S_ij <= u}."""
+    return calibrate(-np.asarray(S, dtype=np.float64), -np.asarray(z_hat, dtype=np.float64), v, -u, level)

@@ -8,6 +8,8 @@
   * §VI-B.2 / Fig. 3: the excursion set of the truth over the prediction sites is
     A = {i in D_p : Z_i >= u}; a replicate succeeds when C_in is inside A and A is inside
     C_out.  The empirical coverage is the fraction of successful replicates.
+  * §III: for a negative excursion set the truth's set is {i : Z_i <= u} (the positive set
+    of the sign-reversed field at -u).
 """
 from __future__ import annotations
 
@@ -22,14 +24,14 @@ def truth_field(L: np.ndarray, X: np.ndarray, b, eta: np.ndarray) -> np.ndarray:
     return (mean[:, None] if eta.ndim == 2 else mean) + np.asarray(L) @ eta
 
 
-def excursion_set(z_p: np.ndarray, u: float) -> np.ndarray:
-    """A = {i : z_i >= u} as a boolean mask (§VI-B.2)."""
-    return np.asarray(z_p) >= u
+def excursion_set(z_p: np.ndarray, u: float, negative: bool = False) -> np.ndarray:
+    """A = {i : z_i >= u} as a boolean mask (§VI-B.2); {i : z_i <= u} for a negative set (§III)."""
+    return np.asarray(z_p) <= u if negative else np.asarray(z_p) >= u
 
 
-def coverage_event(truth_p: np.ndarray, c_in, c_out, u: float) -> bool:
+def coverage_event(truth_p: np.ndarray, c_in, c_out, u: float, negative: bool = False) -> bool:
     """True when C_in is a subset of A and A is a subset of C_out (§VI-B.2)."""
-    A = excursion_set(truth_p, u)
+    A = excursion_set(truth_p, u, negative)
     inner = np.asarray(c_in).astype(bool)
     outer = np.asarray(c_out).astype(bool)
     return bool(np.all(A[inner]) and np.all(outer[A]))

@@ -385,6 +385,27 @@ def test_calibration_bit_exact_edge_values(lib, u):
     np.testing.assert_array_equal(out["c_out"].cpu().numpy(), ref["c_out"])
 
 
+@pytest.mark.parametrize("u", [0.25, 0.0, -1.5])
+def test_negative_excursion_calibration_bit_exact(lib, u):
+    """The negative excursion set (Section III's sign reversal) against the oracle, bit-exact,
+    including elements equal to u, +-0, infinities and NaN."""
+    rng = np.random.default_rng(41)
+    n_p, M = 2300, 90
+    S = rng.standard_normal((n_p, M))
+    mask = rng.random((n_p, M)) < 0.2
+    S[mask] = rng.choice(np.array([u, np.nextafter(u, np.inf), 0.0, -0.0, np.inf, -np.inf, np.nan]), size=int(mask.sum()))
+    z = rng.standard_normal(n_p) * 0.5
+    v = rng.uniform(0.3, 2.0, n_p)
+    out = lib.calibrate(colmajor(S), dev(z), dev(v), u, 0.9, counts=True, extrema=True, negative=True)
+    ref = oracle.calibrate_negative(S, z, v, u, 0.9)
+    np.testing.assert_array_equal(out["psi"].cpu().numpy(), ref["psi"])
+    np.testing.assert_array_equal(out["phi"].cpu().numpy(), ref["phi"])
+    np.testing.assert_array_equal(out["count"].cpu().numpy(), ref["count"])
+    assert out["q_in"] == ref["q_in"] and out["q_out"] == ref["q_out"]
+    np.testing.assert_array_equal(out["c_in"].cpu().numpy(), ref["c_in"])
+    np.testing.assert_array_equal(out["c_out"].cpu().numpy(), ref["c_out"])
+
+
 def test_calibration_errors(lib):
     n_p, M = 100, 10
     S = np.full((n_p, M), 5.0)

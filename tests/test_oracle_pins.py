@@ -220,6 +220,44 @@ def test_calibration_brute_force_small():
         assert out["c_in"][i] == (t[i] > out["q_in"])
 
 
+def test_negative_excursion_hand_case():
+    """Section III's sign reversal, worked by hand on 3 sites x 4 simulations (u = 0, level 0.5):
+    t = (0.2, -0.15, 0.1), so the reversed t' = (-0.2, 0.15, -0.1); psi'_j takes the sites with
+    S_ij <= 0, phi'_j those with S_ij >= 0; Q_0.5 of 4 values is the 2nd smallest."""
+    S = np.array([[1.0, -1.0, 2.0, -2.0], [-1.0, 1.0, -1.0, 1.0], [0.5, 0.5, -0.5, -0.5]])
+    z = np.array([0.2, -0.3, 0.1])
+    v = np.array([1.0, 4.0, 1.0])
+    out = oracle.calibrate_negative(S, z, v, 0.0, 0.5)
+    np.testing.assert_array_equal(out["t"], [-0.2, 0.15, -0.1])
+    np.testing.assert_array_equal(out["psi"], [0.15, -0.2, -0.1, -0.2])
+    np.testing.assert_array_equal(out["phi"], [-0.1, 0.15, -0.2, 0.15])
+    np.testing.assert_array_equal(out["count"], [2, 2, 2])
+    assert out["q_out"] == -0.2 and out["q_in"] == -0.1
+    np.testing.assert_array_equal(out["c_out"], [1, 1, 1])
+    np.testing.assert_array_equal(out["c_in"], [0, 1, 0])
+    # the negative set of a field is the positive set of the reversed field (Section III)
+    assert list(oracle.excursion_set(np.array([-1.0, 0.0, 1.0]), 0.0, negative=True)) == [True, True, False]
+
+
+def test_negative_excursion_brute_force():
+    """Negative regions against a direct brute-force statement: psi'_j = min{-t_i : S_ij <= u},
+    phi'_j = max{-t_i : S_ij >= u}, counts #{j : S_ij <= u}."""
+    rng = np.random.default_rng(19)
+    n_p, M, u = 9, 15, -0.2
+    S = rng.standard_normal((n_p, M))
+    z = rng.standard_normal(n_p)
+    v = rng.uniform(0.5, 2.0, n_p)
+    out = oracle.calibrate_negative(S, z, v, u, 0.8)
+    t = [-(z[i] - u) / math.sqrt(v[i]) for i in range(n_p)]
+    for j in range(M):
+        a = [t[i] for i in range(n_p) if S[i, j] <= u]
+        b = [t[i] for i in range(n_p) if S[i, j] >= u]
+        assert out["psi"][j] == (min(a) if a else math.inf)
+        assert out["phi"][j] == (max(b) if b else -math.inf)
+    for i in range(n_p):
+        assert out["count"][i] == sum(1 for j in range(M) if S[i, j] <= u)
+
+
 def test_quantile_index_eq9():
     a = np.arange(1.0, 21.0)
     assert oracle.empirical_quantile(a, 0.05) == 1.0
