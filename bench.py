@@ -415,6 +415,106 @@ def run_ours(args, world, rank, local):
     V.close()
 
 
+def run_krige(args, world, rank, local):
+    """The universal-kriging workload (16384 noisy observations and a 128 x 128 prediction grid,
+    Matern nu = 1, range 0.1, tau^2 = 0.01, tile 512, M = 1024, fixedacc 1e-6, u = 1.6, level
+    0.90).  Kriging (W, zhat, v), the map and the factorisation are set up once (their times are
+    reported, not in the metric); one step is one batch of M conditional simulations: normal
+    draws fused with the mixed-precision TRMM, then the correction fused with the calibration
+    (S is never written).  Metric: simulations per second, M / (t_rng + t_trmm + t_correct +
+    t_calibrate).  The unfused correction + calibration is timed beside it."""
+    import torch
+    import mixed_precision_dense_mat_gb300 as cr
+    torch.cuda.set_device(local)
+    cr.load()
+    w = inputgen.WORKLOADS["k"]
+    n, n_p, n_o, nb, M = w.n, w.n_pred, w.n_obs, w.nb, w.M
+    dev = torch.device("cuda", local)
+    xy_h = inputgen.workload_locations(w)
+    xy = torch.from_numpy(xy_h).to(dev)
+    X = np.column_stack([np.ones(n), xy_h[:, 0], xy_h[:, 1]])
+    y_h = inputgen.observation_values(xy_h[n_p:], (1.0, 0.5, -0.3), 0.1, 3)
+    yo = torch.from_numpy(y_h).to(dev)
+    stream = torch.cuda.current_stream()
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    V = cr.TileMat(n, nb)
+    e = [ev() for _ in range(4)]
+    e[0].record(stream)
+    cr.cov_build(V, xy, w.family, w.sigma2, w.beta, w.nu, nugget=w.nugget, n_pred=n_p, tau2=w.tau2)
+    W, zhat, v = cr.krige(V, cr.as_colmajor(torch.from_numpy(X[n_p:]).to(dev))[0],
+                          cr.as_colmajor(torch.from_numpy(X[:n_p]).to(dev))[0], yo)
+    e[1].record(stream)
+    pmap, info = cr.precision_map(V, amp=True, fixedacc=w.fixedacc)
+    assert cr.potrf_adaptive(V) == 0
+    e[2].record(stream)
+    torch.cuda.synchronize()
+    t_krige, t_chol = e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2])
+    Y = cr.colmajor_empty(n, M, torch.float64)
+
+    def step(seed, fused=True):
+        cr.trmm_sim(V, None, M, seed=seed, out=Y, flags=cr.CR_TRMM_GENERATE)
+        if fused:
+            return cr.correct_calibrate(W, yo, Y, n_p, n_o, zhat, v, w.u, w.level)
+        S = cr.krige_correct(W, yo, Y, n_p, n_o)
+        return cr.calibrate(S, zhat, v, w.u, w.level)
+
+    for q in range(args.warmup):
+        step(SEED_Z + q)
+    torch.cuda.synchronize()
+    gpu_id = os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local] if "CUDA_VISIBLE_DEVICES" in os.environ else str(local)
+    clocks = ClockSampler(gpu_id)
+    barrier(world)
+    torch.cuda.synchronize()
+    l0 = cr.kernel_launches()
+    a, b = ev(), ev()
+    a.record(stream)
+    for q in range(args.steps):
+        out = step(SEED_Z + 100 + q)
+    b.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    launches = cr.kernel_launches() - l0
+    clk = clocks.stop()
+    ms = max_over_ranks(a.elapsed_time(b) / args.steps, world)
+    # the parts of one step, and the unfused path, in a separate pass
+    parts = {}
+    pe = [ev() for _ in range(3)]
+    pe[0].record(stream)
+    cr.trmm_sim(V, None, M, seed=SEED_Z + 500, out=Y, flags=cr.CR_TRMM_GENERATE)
+    pe[1].record(stream)
+    cr.correct_calibrate(W, yo, Y, n_p, n_o, zhat, v, w.u, w.level)
+    pe[2].record(stream)
+    torch.cuda.synchronize()
+    parts["rng_trmm"] = pe[0].elapsed_time(pe[1])
+    parts["correct_calibrate_fused"] = pe[1].elapsed_time(pe[2])
+    ue = [ev() for _ in range(3)]
+    ue[0].record(stream)
+    S = cr.krige_correct(W, yo, Y, n_p, n_o)
+    ue[1].record(stream)
+    cr.calibrate(S, zhat, v, w.u, w.level)
+    ue[2].record(stream)
+    torch.cuda.synchronize()
+    parts["correct_unfused"] = ue[0].elapsed_time(ue[1])
+    parts["calibrate_unfused"] = ue[1].elapsed_time(ue[2])
+    corr_flops = 2.0 * n_p * n_o * M
+    if rank == 0:
+        line = {"metric": "conditional simulations/s (kriging workload)", "value": world * M / (ms / 1e3),
+                "unit": "simulations/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16/f32/f64 adaptive; df correction",
+                "data": "synthetic",
+                "config": {"workload": w.name, "n_pred": n_p, "n_obs": n_o, "nb": nb, "M": M, "fixedacc": w.fixedacc,
+                           "u": w.u, "level": w.level, "parallelism": f"replicas x{world}"},
+                "setup_ms": {"covariance_and_kriging": t_krige, "map_and_cholesky": t_chol},
+                "parts_ms": parts,
+                "correction_tflops": corr_flops / (parts["correct_calibrate_fused"] / 1e3) / 1e12,
+                "precision_map": {"n_fp64": info["n_fp64"], "n_fp32": info["n_fp32"], "n_fp16": info["n_fp16"], "s": info["s"]},
+                "regions": {"q_in": out["q_in"], "q_out": out["q_out"], "inner": int(out["c_in"].sum().item()),
+                            "outer": int(out["c_out"].sum().item())},
+                "gpu_launches": launches, "clocks": clk}
+        print(json.dumps(line), flush=True)
+    V.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -425,6 +525,9 @@ def main():
     ap.add_argument("--no-kernel-timing", action="store_true", help="skip the per-kernel device timing (no roofline)")
     ap.add_argument("--n", type=int, default=0, help="profiling only: smaller n of the same workload family")
     ap.add_argument("--peaks", action="store_true", help="print the arithmetic units' measured peaks and exit")
+    ap.add_argument("--workload", default="headline", choices=["headline", "krige"],
+                    help="headline: the Cholesky+TRMM step of the n = 32768 workload (default); krige: conditional "
+                         "simulations per second on the kriging workload")
     args = ap.parse_args()
     global WORKLOAD
     if args.n:
@@ -440,6 +543,8 @@ def main():
     try:
         if args.impl == "reference":
             run_reference(args, world, rank)
+        elif args.workload == "krige":
+            run_krige(args, world, rank, local)
         else:
             run_ours(args, world, rank, local)
     finally:

@@ -271,10 +271,27 @@ cr_status cr_krige(cr_tilemat V, const double* d_Xo, const double* d_Xp, const d
 /* Conditioning correction (Section V-B Eq.7): S = M_p + W^T (y_o 1^T - M_o), where the
  * simulations d_Y (n x M column-major, ldy) hold the prediction rows first (M_p = rows
  * [0, n_p), M_o = rows [n_p, n_p + n_o)).  d_S is n_p x M column-major (lds >= n_p).
- * FP64.  Asynchronous. */
+ * The product runs in double-float arithmetic on the FP32 units (an FP64 emulation with
+ * about 48 significant bits; W and R = y_o 1^T - M_o are rounded to double-float pairs, the
+ * sum M_p + W^T R is formed in FP64): |S - S_exact| <= (n_o + 8) 2^-46 (|W|^T |R|)_ij +
+ * 2^-52 |S_ij|.  Stream-ordered allocation of 8 n_o (n_p + M) bytes of scratch
+ * (cudaMallocAsync).  Asynchronous. */
 cr_status cr_krige_correct(const double* d_W, int ldw, const double* d_yo, const double* d_Y,
                            int ldy, int n_p, int n_o, int M, double* d_S, int lds,
                            cr_stream stream);
+
+/* The correction of cr_krige_correct fused with the calibration of cr_calibrate (or, with
+ * negative != 0, of cr_calibrate_negative): each 64 x 64 block of S is computed by the same
+ * double-float product and handed straight to the scan's decisions, so S is never written
+ * (n_p x M doubles of HBM traffic saved).  Arguments as in those two calls; the results are
+ * identical to cr_calibrate(cr_krige_correct(...)) on the same inputs.  Library-managed
+ * scratch, 8 n_o (n_p + M) + 8 n_p + 16 M + 16 ceil(n_p / 64) M bytes, grown on demand and
+ * shared by all calls: the call returns after its last kernel.  Synchronises. */
+cr_status cr_correct_calibrate(const double* d_W, int ldw, const double* d_yo, const double* d_Y,
+                               int ldy, int n_p, int n_o, int M, const double* d_zhat,
+                               const double* d_v, double u, double level, int negative,
+                               uint8_t* d_cin, uint8_t* d_cout, int32_t* d_count, double* d_psi,
+                               double* d_phi, cr_calib_info* out, cr_stream stream);
 
 /* Calibration (Section V-C Eq.8-9, Alg.2 steps 18-22): t = (zhat - u)/sqrt(v);
  * psi_j = min{t_i : S_ij >= u}, phi_j = max{t_i : S_ij <= u} in one pass over d_S

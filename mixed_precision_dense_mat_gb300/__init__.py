@@ -17,6 +17,7 @@ The functions mirror include/cr.h:
   trmm_sim(V, Z, M, ...)                 cr_trmm_sim
   krige(V, Xo, Xp, yo)                   cr_krige
   krige_correct(W, yo, Y, n_p, n_o)      cr_krige_correct
+  correct_calibrate(W, yo, Y, ...)       cr_correct_calibrate (correction fused with calibration)
   calibrate(S, zhat, v, u, level)        cr_calibrate (negative=True: cr_calibrate_negative)
   morton_order(xy)                       cr_morton_order (host only)
 The library is never replaced by a fallback: if libcr.so is missing or fails to load, every
@@ -104,6 +105,8 @@ _SIGNATURES = {
     "cr_krige_correct": (_I, [_P, _I, _P, _P, _I, _I, _I, _I, _P, _I, _P]),
     "cr_morton_order": (_I, [_P, _I, _P]),
     "cr_calibrate": (_I, [_P, _I, _I, _I, _P, _P, _D, _D, _P, _P, _P, _P, _P, ctypes.POINTER(CalibInfo), _P]),
+    "cr_correct_calibrate": (_I, [_P, _I, _P, _P, _I, _I, _I, _I, _P, _P, _D, _D, _I, _P, _P, _P, _P, _P,
+                                  ctypes.POINTER(CalibInfo), _P]),
     "cr_calibrate_negative": (_I, [_P, _I, _I, _I, _P, _P, _D, _D, _P, _P, _P, _P, _P, ctypes.POINTER(CalibInfo),
                                    _P]),
     "cr_calibrate_noalloc": (_I, [_P, _I, _I, _I, _P, _P, _D, _D, _P, _P, _P, _P, _P, ctypes.POINTER(CalibInfo),
@@ -355,6 +358,33 @@ def krige_correct(W, yo, Y, n_p: int, n_o: int, out=None, stream=None):
     out, lds = as_colmajor(out)
     _check(_lib.cr_krige_correct(_ptr(W), ldw, _ptr(yo.contiguous()), _ptr(Y), ldy, n_p, n_o, M, _ptr(out), lds,
                                  _stream(stream)))
+    return out
+
+
+def correct_calibrate(W, yo, Y, n_p: int, n_o: int, zhat, v, u: float, level: float, counts: bool = True,
+                      extrema: bool = False, negative: bool = False, stream=None):
+    """cr_correct_calibrate: the correction S = M_p + W^T (y_o 1^T - M_o) fused with the
+    calibration (S is never formed); returns the dict of calibrate()."""
+    import torch
+    W, ldw = as_colmajor(W)
+    Y, ldy = as_colmajor(Y)
+    M = Y.shape[1]
+    cin = torch.empty(n_p, dtype=torch.uint8, device="cuda")
+    cout = torch.empty(n_p, dtype=torch.uint8, device="cuda")
+    cnt = torch.empty(n_p, dtype=torch.int32, device="cuda") if counts else None
+    psi = torch.empty(M, dtype=torch.float64, device="cuda") if extrema else None
+    phi = torch.empty(M, dtype=torch.float64, device="cuda") if extrema else None
+    info = CalibInfo()
+    _check(_lib.cr_correct_calibrate(_ptr(W), ldw, _ptr(yo.contiguous()), _ptr(Y), ldy, n_p, n_o, M,
+                                     _ptr(zhat.contiguous()), _ptr(v.contiguous()), u, level, 1 if negative else 0,
+                                     _ptr(cin), _ptr(cout), _ptr(cnt), _ptr(psi), _ptr(phi), ctypes.byref(info),
+                                     _stream(stream)))
+    out = {"q_in": info.q_in, "q_out": info.q_out, "n_psi": info.n_psi, "n_phi": info.n_phi, "c_in": cin,
+           "c_out": cout}
+    if counts:
+        out["count"] = cnt
+    if extrema:
+        out["psi"], out["phi"] = psi, phi
     return out
 
 

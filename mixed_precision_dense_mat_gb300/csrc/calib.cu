@@ -21,6 +21,7 @@
 
 #include "calib.cuh"
 #include "common.cuh"
+#include "df.cuh"
 
 namespace cr {
 
@@ -254,7 +255,16 @@ cr_status calibrate_core(const double* d_S, int lds, int n_p, int M, const doubl
     k_scan<<<grid, SCAN_THREADS, 0, stream>>>(d_S, lds, n_p, M, sc.t, u, sc.psi_part, sc.phi_part, d_count, neg);
   }
   CR_CHECK_LAUNCH("k_scan");
-  k_scan_reduce<<<std::min(1024, (M + 255) / 256), 256, 0, stream>>>(sc.psi_part, sc.phi_part, nrb, M, sc.psi, sc.phi);
+  return calibrate_finish(sc.psi_part, sc.phi_part, nrb, n_p, M, level, sc, d_cin, d_cout, d_psi, d_phi, out, stream);
+}
+
+// Combines the per-row-block partials (nrb x M) into psi and phi in a fixed order, takes the
+// quantiles of the samples without sentinels on the host and writes the regions from sc.t;
+// returns only after its last kernel, which reads sc.t, has finished.
+cr_status calibrate_finish(const double* psi_part, const double* phi_part, int nrb, int n_p, int M, double level,
+                           const CalibScratch& sc, uint8_t* d_cin, uint8_t* d_cout, double* d_psi, double* d_phi,
+                           cr_calib_info* out, cudaStream_t stream) {
+  k_scan_reduce<<<std::min(1024, (M + 255) / 256), 256, 0, stream>>>(psi_part, phi_part, nrb, M, sc.psi, sc.phi);
   CR_CHECK_LAUNCH("k_scan_reduce");
   std::vector<double> psi(M), phi(M);
   int bad = 0;
@@ -346,6 +356,295 @@ extern "C" cr_status cr_calibrate_negative(const double* d_S, int lds, int n_p, 
   std::lock_guard<std::mutex> lk(g_mu);
   CR_TRY(ensure_scratch(n_p, M));
   return calibrate_core(d_S, lds, n_p, M, d_zhat, d_v, u, level, d_cin, d_cout, d_count, d_psi, d_phi, out, stream, g_sc, 1);
+}
+
+// ---------------------------------------------------------------------------------------
+// Conditioning correction (Section V-B Eq.7) as a double-float GEMM, S = M_p + W^T R with
+// R = y_o 1^T - M_o, and its fusion with the calibration scan.
+//
+// The page states the correction in FP64.  GB300's FP64 units issue 1/64 of the FP32 lanes,
+// so the product runs in double-float arithmetic on the FP32 units (about 48 significant
+// bits, the error-free products and sums of df.cuh; an FP64 emulation): W and R are converted
+// to double-float pairs once per call, each CTA computes a 64 x 64 block of S over the whole
+// inner dimension n_o, the block's value is M_p + (hi + lo) in FP64, and the epilogue either
+// stores it (cr_krige_correct) or hands it to the scan's decisions (cr_correct_calibrate:
+// psi/phi partials per 64-row block and per-row exceedance counts), so that S is never
+// written.  Both epilogues see the same values, so the fused and unfused paths decide alike.
+namespace cr {
+namespace {
+
+constexpr int CT = 64;    // rows and columns of an output block
+constexpr int CK = 16;    // inner-dimension chunk staged in shared memory
+constexpr int CTH = 256;  // threads: a 16 x 16 grid, 4 x 4 outputs each
+
+// D[q + c rows] = A[q + c lda] as double-float pairs (rows x cols, column-major)
+__global__ void k_to_df(const double* __restrict__ A, int lda, int rows, int cols, float2* __restrict__ D) {
+  const size_t total = (size_t)rows * cols;
+  for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < total; e += (size_t)gridDim.x * blockDim.x) {
+    const size_t q = e % rows, c = e / rows;
+    const double x = A[q + c * lda];
+    const float h = __double2float_rn(x);
+    D[e] = make_float2(h, __double2float_rn(x - (double)h));
+  }
+}
+// R[q + j n_o] = y_o[q] - M_o[q + j ldy] (FP64), as double-float pairs
+__global__ void k_resid_df(const double* __restrict__ yo, const double* __restrict__ Mo, int ldy, int n_o, int M,
+                           float2* __restrict__ R) {
+  const size_t total = (size_t)n_o * M;
+  for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < total; e += (size_t)gridDim.x * blockDim.x) {
+    const size_t q = e % n_o, j = e / n_o;
+    const double x = yo[q] - Mo[q + j * ldy];
+    const float h = __double2float_rn(x);
+    R[e] = make_float2(h, __double2float_rn(x - (double)h));
+  }
+}
+
+struct CAcc {
+  float s, c;
+};
+// s + c += x y, the high products summed by two-sum, the lower-order terms in c
+__device__ __forceinline__ void cmac(CAcc& a, float2 x, float2 y) {
+  const float p = __fmul_rn(x.x, y.x);
+  float e = __fmaf_rn(x.x, y.x, -p);
+  e = __fmaf_rn(x.x, y.y, e);
+  e = __fmaf_rn(x.y, y.x, e);
+  const float s = __fadd_rn(a.s, p);
+  const float bb = __fsub_rn(s, a.s);
+  const float t = __fadd_rn(__fsub_rn(a.s, __fsub_rn(s, bb)), __fsub_rn(p, bb));
+  a.s = s;
+  a.c = __fadd_rn(a.c, __fadd_rn(t, e));
+}
+
+template <bool SCAN>
+__global__ void __launch_bounds__(CTH) k_corr(const float2* __restrict__ Wd, const float2* __restrict__ Rd,
+                                              const double* __restrict__ Mp, int ldy, int n_p, int n_o, int M,
+                                              double* __restrict__ S, int lds, const double* __restrict__ t, double u, int neg,
+                                              double* __restrict__ psi_part, double* __restrict__ phi_part,
+                                              int32_t* __restrict__ count) {
+  __shared__ float2 As[2][CK][CT + 1];   // padded: the staging stores walk k
+  __shared__ float2 Bs[2][CK][CT + 1];
+  const int i0 = blockIdx.x * CT, j0 = blockIdx.y * CT;
+  const int tid = threadIdx.x, ti = tid >> 4, tj = tid & 15;
+  CAcc acc[4][4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[r][c] = CAcc{0.0f, 0.0f};
+  // staging: element e = tid + 256 s of a chunk is (k = e % 16, row or column e / 16); 16
+  // consecutive threads read 16 consecutive inner indices (128 bytes)
+  float2 ra[4], rb[4];
+  auto fetch = [&](int q0) {
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      const int e = tid + CTH * s, k = e & (CK - 1), r = e >> 4, q = q0 + k;
+      ra[s] = (q < n_o && i0 + r < n_p) ? Wd[(size_t)(i0 + r) * n_o + q] : make_float2(0.0f, 0.0f);
+      rb[s] = (q < n_o && j0 + r < M) ? Rd[(size_t)(j0 + r) * n_o + q] : make_float2(0.0f, 0.0f);
+    }
+  };
+  auto stash = [&](int b) {
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      const int e = tid + CTH * s, k = e & (CK - 1), r = e >> 4;
+      As[b][k][r] = ra[s];
+      Bs[b][k][r] = rb[s];
+    }
+  };
+  const int nch = (n_o + CK - 1) / CK;
+  fetch(0);
+  stash(0);
+  __syncthreads();
+  for (int ch = 0; ch < nch; ++ch) {
+    const int b = ch & 1;
+    if (ch + 1 < nch) fetch((ch + 1) * CK);   // the next chunk in flight during this one's products
+#pragma unroll
+    for (int k = 0; k < CK; ++k) {
+      float2 a[4], bv[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) a[r] = As[b][k][ti + 16 * r];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) bv[c] = Bs[b][k][tj + 16 * c];
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) cmac(acc[r][c], a[r], bv[c]);
+    }
+    if (ch + 1 < nch) stash(b ^ 1);   // buffer b ^ 1 was last read before the previous barrier
+    __syncthreads();
+  }
+  // S_ij = M_p,ij + (hi + lo), in FP64
+  double sv[4][4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int i = i0 + ti + 16 * r, j = j0 + tj + 16 * c;
+      sv[r][c] = 0.0;
+      if (i < n_p && j < M) {
+        const df v = df_two_sum(acc[r][c].s, acc[r][c].c);
+        sv[r][c] = Mp[i + (size_t)j * ldy] + ((double)v.hi + (double)v.lo);
+      }
+    }
+  if (!SCAN) {
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int i = i0 + ti + 16 * r, j = j0 + tj + 16 * c;
+        if (i < n_p && j < M) S[i + (size_t)j * lds] = sv[r][c];
+      }
+    return;
+  }
+  // The scan's decisions on the block: S >= u and S <= u (IEEE comparisons: NaN neither, the
+  // two zeros equal), swapped for a negative excursion set; psi / phi partials are the
+  // extreme keys of t over the qualifying rows, counts the qualifying columns of each row.
+  constexpr unsigned long long KEY_PINF = 0xfff0000000000000ull, KEY_MINF = 0x000fffffffffffffull;
+  __shared__ unsigned long long red_mn[CTH / 32][CT], red_mx[CTH / 32][CT];
+  const int lane = tid & 31, warp = tid >> 5;
+  unsigned long long tk[4];
+  int cnt[4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int i = i0 + ti + 16 * r;
+    tk[r] = i < n_p ? dkey(t[i]) : 0ull;
+    cnt[r] = 0;
+  }
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int j = j0 + tj + 16 * c;
+    unsigned long long mn = KEY_PINF, mx = KEY_MINF;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int i = i0 + ti + 16 * r;
+      const bool valid = i < n_p && j < M;
+      const bool above = valid && sv[r][c] >= u, below = valid && sv[r][c] <= u;
+      const bool ge = neg ? below : above, le = neg ? above : below;
+      if (ge) mn = tk[r] < mn ? tk[r] : mn;
+      if (le) mx = tk[r] > mx ? tk[r] : mx;
+      cnt[r] += ge ? 1 : 0;
+    }
+    // lanes tj and tj + 16 of a warp hold the same column (rows of two ti)
+    const unsigned long long mn2 = __shfl_xor_sync(0xffffffffu, mn, 16), mx2 = __shfl_xor_sync(0xffffffffu, mx, 16);
+    mn = mn2 < mn ? mn2 : mn;
+    mx = mx2 > mx ? mx2 : mx;
+    if (lane < 16) {
+      red_mn[warp][tj + 16 * c] = mn;
+      red_mx[warp][tj + 16 * c] = mx;
+    }
+  }
+  // counts: the 16 lanes of a half-warp share a row
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    int v = cnt[r];
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    const int i = i0 + ti + 16 * r;
+    if (count && tj == 0 && v && i < n_p) atomicAdd(&count[i], v);
+  }
+  __syncthreads();
+  if (tid < CT && j0 + tid < M) {
+    unsigned long long m1 = KEY_PINF, m2 = KEY_MINF;
+#pragma unroll
+    for (int w = 0; w < CTH / 32; ++w) {
+      m1 = red_mn[w][tid] < m1 ? red_mn[w][tid] : m1;
+      m2 = red_mx[w][tid] > m2 ? red_mx[w][tid] : m2;
+    }
+    const size_t o = (size_t)blockIdx.x * M + j0 + tid;
+    psi_part[o] = dkey_inv(m1);   // +inf / -inf when no row of the block qualifies
+    phi_part[o] = dkey_inv(m2);
+  }
+}
+
+// Converts W and R and launches the correction GEMM (stream-ordered).
+cr_status correction_launch(const double* d_W, int ldw, const double* d_yo, const double* d_Y, int ldy, int n_p, int n_o,
+                            int M, float2* Wd, float2* Rd, bool scan, double* d_S, int lds, const double* t, double u, int neg,
+                            double* psi_part, double* phi_part, int32_t* d_count, cudaStream_t stream) {
+  k_to_df<<<2048, 256, 0, stream>>>(d_W, ldw, n_o, n_p, Wd);
+  CR_CHECK_LAUNCH("k_to_df");
+  k_resid_df<<<1024, 256, 0, stream>>>(d_yo, d_Y + n_p, ldy, n_o, M, Rd);
+  CR_CHECK_LAUNCH("k_resid_df");
+  const dim3 grid((unsigned)((n_p + CT - 1) / CT), (unsigned)((M + CT - 1) / CT));
+  if (scan) {
+    TimedScope ts("k_corr_scan", stream);
+    k_corr<true><<<grid, CTH, 0, stream>>>(Wd, Rd, d_Y, ldy, n_p, n_o, M, nullptr, 0, t, u, neg, psi_part, phi_part, d_count);
+  } else {
+    TimedScope ts("k_corr", stream);
+    k_corr<false><<<grid, CTH, 0, stream>>>(Wd, Rd, d_Y, ldy, n_p, n_o, M, d_S, lds, nullptr, 0.0, 0, nullptr, nullptr, nullptr);
+  }
+  CR_CHECK_LAUNCH("k_corr");
+  return CR_OK;
+}
+
+// Library-managed scratch of cr_correct_calibrate, grown on demand (one per process): the
+// double-float copies of W and R, t, psi, phi, the 64-row-block partials and the MSPE flag.
+std::mutex g_cc_mu;
+struct CorrScratch {
+  float2* W = nullptr;
+  float2* R = nullptr;
+  double *t = nullptr, *psi = nullptr, *phi = nullptr, *psi_part = nullptr, *phi_part = nullptr;
+  int* bad = nullptr;
+  size_t capW = 0, capR = 0, capT = 0, capPsi = 0, capPhi = 0, capPP = 0, capFP = 0, capBad = 0;
+};
+CorrScratch g_cc;
+
+template <class T>
+cr_status grow(T** p, size_t* cap, size_t need) {
+  if (need <= *cap) return CR_OK;
+  if (*p) cudaFree(*p);
+  *p = nullptr;
+  *cap = 0;
+  CR_CUDA(cudaMalloc(p, need * sizeof(T)));
+  *cap = need;
+  return CR_OK;
+}
+
+}  // namespace
+
+cr_status correction_async(const double* d_W, int ldw, const double* d_yo, const double* d_Y, int ldy, int n_p, int n_o,
+                           int M, double* d_S, int lds, cudaStream_t stream) {
+  float2 *Wd = nullptr, *Rd = nullptr;
+  CR_CUDA(cudaMallocAsync(&Wd, (size_t)n_o * n_p * sizeof(float2), stream));
+  CR_CUDA(cudaMallocAsync(&Rd, (size_t)n_o * M * sizeof(float2), stream));
+  const cr_status st = correction_launch(d_W, ldw, d_yo, d_Y, ldy, n_p, n_o, M, Wd, Rd, false, d_S, lds, nullptr, 0.0, 0,
+                                         nullptr, nullptr, nullptr, stream);
+  cudaFreeAsync(Wd, stream);
+  cudaFreeAsync(Rd, stream);
+  return st;
+}
+
+}  // namespace cr
+
+extern "C" cr_status cr_correct_calibrate(const double* d_W, int ldw, const double* d_yo, const double* d_Y, int ldy,
+                                          int n_p, int n_o, int M, const double* d_zhat, const double* d_v, double u,
+                                          double level, int negative, uint8_t* d_cin, uint8_t* d_cout, int32_t* d_count,
+                                          double* d_psi, double* d_phi, cr_calib_info* out, cr_stream stream) {
+  if (!d_W || !d_yo || !d_Y || !d_zhat || !d_v || !d_cin || !d_cout || n_p <= 0 || n_o <= 0 || M <= 0 || ldw < n_o ||
+      ldy < n_p + n_o || !(level > 0.0 && level < 1.0))
+    return fail(CR_ERR_ARG, "cr_correct_calibrate: argument");
+  std::lock_guard<std::mutex> lk(g_cc_mu);
+  const size_t nrb = ((size_t)n_p + CT - 1) / CT;
+  CR_TRY(grow(&g_cc.W, &g_cc.capW, (size_t)n_o * n_p));
+  CR_TRY(grow(&g_cc.R, &g_cc.capR, (size_t)n_o * M));
+  CR_TRY(grow(&g_cc.t, &g_cc.capT, (size_t)n_p));
+  CR_TRY(grow(&g_cc.psi, &g_cc.capPsi, (size_t)M));
+  CR_TRY(grow(&g_cc.phi, &g_cc.capPhi, (size_t)M));
+  CR_TRY(grow(&g_cc.psi_part, &g_cc.capPP, nrb * M));
+  CR_TRY(grow(&g_cc.phi_part, &g_cc.capFP, nrb * M));
+  CR_TRY(grow(&g_cc.bad, &g_cc.capBad, (size_t)1));
+  CalibScratch sc;
+  sc.t = g_cc.t;
+  sc.psi = g_cc.psi;
+  sc.phi = g_cc.phi;
+  sc.psi_part = g_cc.psi_part;
+  sc.phi_part = g_cc.phi_part;
+  sc.bad = g_cc.bad;
+  const int neg = negative ? 1 : 0;
+  CR_CUDA(cudaMemsetAsync(sc.bad, 0, sizeof(int), stream));
+  k_tstat<<<std::min(1024, (n_p + 255) / 256), 256, 0, stream>>>(d_zhat, d_v, u, n_p, sc.t, sc.bad, neg);
+  CR_CHECK_LAUNCH("k_tstat");
+  if (d_count) CR_CUDA(cudaMemsetAsync(d_count, 0, (size_t)n_p * sizeof(int32_t), stream));
+  CR_TRY(correction_launch(d_W, ldw, d_yo, d_Y, ldy, n_p, n_o, M, g_cc.W, g_cc.R, true, nullptr, 0, sc.t, u, neg,
+                           sc.psi_part, sc.phi_part, d_count, stream));
+  return calibrate_finish(sc.psi_part, sc.phi_part, (int)nrb, n_p, M, level, sc, d_cin, d_cout, d_psi, d_phi, out, stream);
 }
 
 // ---------------------------------------------------------------------------------------

@@ -21,6 +21,16 @@ struct CalibScratch {
 
 cr_status calibrate_core(const double* d_S, int lds, int n_p, int M, const double* d_zhat, const double* d_v, double u,
                          double level, uint8_t* d_cin, uint8_t* d_cout, int32_t* d_count, double* d_psi, double* d_phi,
-                         cr_calib_info* out, cudaStream_t stream, const CalibScratch& sc);
+                         cr_calib_info* out, cudaStream_t stream, const CalibScratch& sc, int neg);
+
+// Tail of a calibration: partials (nrb x M) -> psi, phi -> host quantiles -> regions from sc.t.
+cr_status calibrate_finish(const double* psi_part, const double* phi_part, int nrb, int n_p, int M, double level,
+                           const CalibScratch& sc, uint8_t* d_cin, uint8_t* d_cout, double* d_psi, double* d_phi,
+                           cr_calib_info* out, cudaStream_t stream);
+
+// Conditioning correction S = M_p + W^T (y_o 1^T - M_o) in double-float arithmetic, into d_S
+// (stream-ordered; allocates its double-float copies of W and R with cudaMallocAsync).
+cr_status correction_async(const double* d_W, int ldw, const double* d_yo, const double* d_Y, int ldy, int n_p, int n_o,
+                           int M, double* d_S, int lds, cudaStream_t stream);
 
 }  // namespace cr

@@ -7,26 +7,19 @@
 //  - Section V-A Eq.6: v = theta0 1 + colsum(W .* U) - 2 colsum(V_op .* W) with U = Sigma_y W
 //    and theta0 = sigma^2.  Since Sigma_y W = L_o Y, colsum(W .* U) = colsum(Y .* Y): the
 //    same quantity without the symmetric product (exact in exact arithmetic).
-//  - Section V-B Eq.7: S = M_p + W^T (y_o 1^T - M_o), residual then one GEMM.
+//  - Section V-B Eq.7: S = M_p + W^T (y_o 1^T - M_o): one double-float GEMM with the residual
+//    formed in its operand conversion (calib.cu, shared with the fused correction + scan).
 // Sigma_y is factored as its own all-FP64 tile matrix by the library's Cholesky (which keeps
 // each diagonal tile's inverse here); the many-right-hand-side triangular solves are blocked
 // substitutions over tile rows whose products run on the FP64 tile GEMM.
 #include <functional>
 
+#include "calib.cuh"
 #include "common.cuh"
 #include "cov.cuh"
 #include "fp64.cuh"
 
 namespace cr {
-
-__global__ void k_residual(const double* __restrict__ yo, const double* __restrict__ Mo, int ldy, int n_o, int M,
-                           double* __restrict__ R) {
-  const size_t total = (size_t)n_o * M;
-  for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < total; e += (size_t)gridDim.x * blockDim.x) {
-    const int j = (int)(e / n_o), q = (int)(e % n_o);
-    R[e] = yo[q] - Mo[(size_t)j * ldy + q];
-  }
-}
 
 // out[i] = sum_q A[q + i lda] B[q + i ldb] (ldb = 0: B is one vector)
 __global__ void __launch_bounds__(256) k_coldot(const double* __restrict__ A, int lda, const double* __restrict__ B, int ldb,
@@ -274,27 +267,5 @@ extern "C" cr_status cr_krige_correct(const double* d_W, int ldw, const double* 
                                       int n_o, int M, double* d_S, int lds, cr_stream stream) {
   if (!d_W || !d_yo || !d_Y || !d_S || n_p <= 0 || n_o <= 0 || M <= 0 || ldw < n_o || ldy < n_p + n_o || lds < n_p)
     return fail(CR_ERR_ARG, "cr_krige_correct: argument");
-  double* R = nullptr;
-  CR_CUDA(cudaMallocAsync(&R, (size_t)n_o * M * sizeof(double), stream));
-  k_residual<<<1216, 256, 0, stream>>>(d_yo, d_Y + n_p, ldy, n_o, M, R);
-  CR_CHECK_LAUNCH("k_residual");
-  CR_CUDA(cudaMemcpy2DAsync(d_S, (size_t)lds * sizeof(double), d_Y, (size_t)ldy * sizeof(double), (size_t)n_p * sizeof(double), M,
-                            cudaMemcpyDeviceToDevice, stream));
-  // S += W^T R : A(m = site i, k = obs q) = W[i ldw + q], B(n = sim j, k = obs q) = R[j n_o + q]
-  std::vector<DJob> jobs;
-  add_jobs(jobs, d_S, lds, n_p, M, 0, 1, 1.0, 1.0, n_o);
-  DPair pr{d_W, R, ldw, 1, n_o, 1, n_o};
-  DJob* dj = nullptr;
-  DPair* dp = nullptr;
-  CR_CUDA(cudaMallocAsync(&dj, jobs.size() * sizeof(DJob), stream));
-  CR_CUDA(cudaMallocAsync(&dp, sizeof(DPair), stream));
-  CR_CUDA(cudaMemcpyAsync(dj, jobs.data(), jobs.size() * sizeof(DJob), cudaMemcpyHostToDevice, stream));
-  CR_CUDA(cudaMemcpyAsync(dp, &pr, sizeof(DPair), cudaMemcpyHostToDevice, stream));
-  CR_TRY(dgemm_launch(64, dj, dp, (int)jobs.size(), stream));
-  CR_CUDA(cudaFreeAsync(dj, stream));
-  CR_CUDA(cudaFreeAsync(dp, stream));
-  CR_CUDA(cudaFreeAsync(R, stream));
-  // pageable host-to-device copies are staged before cudaMemcpyAsync returns, so the host
-  // job vector may go out of scope here
-  return CR_OK;
+  return correction_async(d_W, ldw, d_yo, d_Y, ldy, n_p, n_o, M, d_S, lds, stream);
 }

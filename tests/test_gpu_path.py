@@ -420,14 +420,48 @@ def test_calibration_errors(lib):
 
 
 def test_krige_correct_matches_oracle(lib):
+    """Eq.7 in double-float arithmetic (48 significant bits) against the oracle's FP64, element
+    by element within the product's error bound (n_o + 8) 2^-46 (|W|^T |R|) + 2^-52 |S|, which
+    also covers the oracle's own FP64 rounding (n_o 2^-53 (|W|^T |R|))."""
     rng = np.random.default_rng(2)
-    n_p, n_o, M = 300, 200, 70
-    W = rng.standard_normal((n_o, n_p))
+    for n_p, n_o, M in ((300, 200, 70), (129, 1000, 65)):
+        W = rng.standard_normal((n_o, n_p))
+        y = rng.standard_normal(n_o)
+        Y = rng.standard_normal((n_p + n_o, M))
+        S = lib.krige_correct(colmajor(W), dev(y), colmajor(Y), n_p, n_o).cpu().numpy()
+        So = oracle.conditional_correction(W, y, Y[:n_p], Y[n_p:])
+        R = y[:, None] - Y[n_p:]
+        bound = (n_o + 8) * 2.0 ** -46 * (np.abs(W).T @ np.abs(R)) + 2.0 ** -52 * np.abs(So)
+        assert np.all(np.abs(S - So) <= bound), np.max(np.abs(S - So) / bound)
+        assert np.linalg.norm(S - So) <= np.linalg.norm(bound)
+
+
+@pytest.mark.parametrize("negative", [False, True])
+def test_fused_correction_calibration_matches_unfused(lib, negative):
+    """cr_correct_calibrate (S never written) against cr_krige_correct followed by cr_calibrate
+    on the same inputs, bit-exact, on ragged sizes (not multiples of the 64 x 64 blocks or of the
+    16-wide inner chunks); and against the oracle's calibration of the GPU's own S."""
+    rng = np.random.default_rng(31)
+    n_p, n_o, M, u, level = 1000, 777, 300, 0.4, 0.9
+    W = rng.standard_normal((n_o, n_p)) * 0.05
     y = rng.standard_normal(n_o)
     Y = rng.standard_normal((n_p + n_o, M))
-    S = lib.krige_correct(colmajor(W), dev(y), colmajor(Y), n_p, n_o).cpu().numpy()
-    So = oracle.conditional_correction(W, y, Y[:n_p], Y[n_p:])
-    assert relf(S, So) <= 1e-14
+    z = rng.standard_normal(n_p) * 0.5
+    v = rng.uniform(0.3, 2.0, n_p)
+    Wd, yd, Yd, zd, vd = colmajor(W), dev(y), colmajor(Y), dev(z), dev(v)
+    S = lib.krige_correct(Wd, yd, Yd, n_p, n_o)
+    a = lib.calibrate(S, zd, vd, u, level, counts=True, extrema=True, negative=negative)
+    b = lib.correct_calibrate(Wd, yd, Yd, n_p, n_o, zd, vd, u, level, counts=True, extrema=True, negative=negative)
+    for k in ("psi", "phi", "count", "c_in", "c_out"):
+        np.testing.assert_array_equal(a[k].cpu().numpy(), b[k].cpu().numpy(), err_msg=k)
+    for k in ("q_in", "q_out", "n_psi", "n_phi"):
+        assert a[k] == b[k], k
+    Sg = S.cpu().numpy()
+    ref = (oracle.calibrate_negative if negative else oracle.calibrate)(Sg, z, v, u, level)
+    assert b["q_in"] == ref["q_in"] and b["q_out"] == ref["q_out"]
+    np.testing.assert_array_equal(b["c_in"].cpu().numpy(), ref["c_in"])
+    np.testing.assert_array_equal(b["c_out"].cpu().numpy(), ref["c_out"])
+    np.testing.assert_array_equal(b["count"].cpu().numpy(), ref["count"])
 
 
 def test_not_spd_reports_column(lib):
