@@ -423,7 +423,9 @@ __global__ void __launch_bounds__(CTH) k_corr(const float2* __restrict__ Wd, con
                                               int32_t* __restrict__ count) {
   __shared__ float2 As[2][CK][CT + 1];   // padded: the staging stores walk k
   __shared__ float2 Bs[2][CK][CT + 1];
-  const int i0 = blockIdx.x * CT, j0 = blockIdx.y * CT;
+  // column blocks vary fastest over the grid, so the CTAs that share a block of rows of W run
+  // together and read it from L2 (W is read from HBM about once, R stays in L2)
+  const int i0 = blockIdx.y * CT, j0 = blockIdx.x * CT;
   const int tid = threadIdx.x, ti = tid >> 4, tj = tid & 15;
   CAcc acc[4][4];
 #pragma unroll
@@ -548,7 +550,7 @@ __global__ void __launch_bounds__(CTH) k_corr(const float2* __restrict__ Wd, con
       m1 = red_mn[w][tid] < m1 ? red_mn[w][tid] : m1;
       m2 = red_mx[w][tid] > m2 ? red_mx[w][tid] : m2;
     }
-    const size_t o = (size_t)blockIdx.x * M + j0 + tid;
+    const size_t o = (size_t)blockIdx.y * M + j0 + tid;
     psi_part[o] = dkey_inv(m1);   // +inf / -inf when no row of the block qualifies
     phi_part[o] = dkey_inv(m2);
   }
@@ -562,7 +564,7 @@ cr_status correction_launch(const double* d_W, int ldw, const double* d_yo, cons
   CR_CHECK_LAUNCH("k_to_df");
   k_resid_df<<<1024, 256, 0, stream>>>(d_yo, d_Y + n_p, ldy, n_o, M, Rd);
   CR_CHECK_LAUNCH("k_resid_df");
-  const dim3 grid((unsigned)((n_p + CT - 1) / CT), (unsigned)((M + CT - 1) / CT));
+  const dim3 grid((unsigned)((M + CT - 1) / CT), (unsigned)((n_p + CT - 1) / CT));
   if (scan) {
     TimedScope ts("k_corr_scan", stream);
     k_corr<true><<<grid, CTH, 0, stream>>>(Wd, Rd, d_Y, ldy, n_p, n_o, M, nullptr, 0, t, u, neg, psi_part, phi_part, d_count);

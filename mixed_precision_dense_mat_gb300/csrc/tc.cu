@@ -478,6 +478,9 @@ static_assert(sizeof(TcBars) <= 256, "barrier area");
 
 }  // namespace
 
+// One kernel for every mode; MODE only names the instantiation (equal to p.mode), so that a
+// profiler can tell the modes apart.
+template <int MODE>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     k_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const TcParams p, int nblocks) {
   extern __shared__ uint8_t smem_raw[];
@@ -684,8 +687,10 @@ cr_status tc_launch(const TcParams& p, const CUtensorMap& tmA, const CUtensorMap
   constexpr int kMaxSmem = 227 * 1024;
   static bool configured = false;
   if (!configured) {
-    CR_CUDA(cudaFuncSetAttribute(k_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem));
-    CR_CUDA(cudaFuncSetAttribute(k_tc, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared));
+    for (auto* fn : {k_tc<TC_UPD_OLD>, k_tc<TC_TRSM>, k_tc<TC_TRMM>, k_tc<TC_UPD_NEW>}) {
+      CR_CUDA(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem));
+      CR_CUDA(cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared));
+    }
     configured = true;
   }
   const int es = p.mode == TC_TRMM ? 1 : std::max(1, p.esplit);
@@ -701,7 +706,13 @@ cr_status tc_launch(const TcParams& p, const CUtensorMap& tmA, const CUtensorMap
   {
     static const char* names[4] = {"k_tc_old", "k_tc_trsm", "k_tc_trmm", "k_tc_new"};
     TimedScope ts(names[p.mode & 3], stream);
-    k_tc<<<grid, TC_THREADS, smem, stream>>>(tmA, tmB, p, nblocks);
+    switch (p.mode) {
+      case TC_UPD_OLD: k_tc<TC_UPD_OLD><<<grid, TC_THREADS, smem, stream>>>(tmA, tmB, p, nblocks); break;
+      case TC_TRSM: k_tc<TC_TRSM><<<grid, TC_THREADS, smem, stream>>>(tmA, tmB, p, nblocks); break;
+      case TC_TRMM: k_tc<TC_TRMM><<<grid, TC_THREADS, smem, stream>>>(tmA, tmB, p, nblocks); break;
+      case TC_UPD_NEW: k_tc<TC_UPD_NEW><<<grid, TC_THREADS, smem, stream>>>(tmA, tmB, p, nblocks); break;
+      default: return fail(CR_ERR_ARG, "tensor-core kernel: mode");
+    }
   }
   CR_CHECK_LAUNCH("k_tc");
   return CR_OK;

@@ -18,7 +18,7 @@ import oracle
 
 pytestmark = pytest.mark.gpu
 
-R_REPLICATES = 300
+R_REPLICATES = 1000
 
 
 def dev(a):
@@ -29,8 +29,20 @@ def colmajor(a):
     return torch.from_numpy(np.asfortranarray(a).T.copy()).cuda().T
 
 
-def test_coverage_matches_oracle(lib):
-    m, n_o, nb, M = 32, 1024, 128, 512
+def _binomial_interval(hits, R):
+    p = hits / R
+    h = 1.96 * np.sqrt(p * (1.0 - p) / R)
+    return p, p - h, p + h
+
+
+@pytest.mark.parametrize("M,with_oracle", [(512, True), (4096, False)])
+def test_coverage_study(lib, M, with_oracle):
+    """1000 replicates (the pages' count, Section VI-B.2).  With M = 512 simulations both chains
+    run on the same truths and draws and the GPU's coverage is within +-0.02 of the oracle's;
+    with M = 4096 the GPU chain alone (draws from cr_rnorm) shows how the coverage moves with
+    the number of simulations (the pages use 80,000).  Both print the coverage with a 95 %
+    binomial interval."""
+    m, n_o, nb = 32, 1024, 128
     nu, beta, tau2, u, level, fixedacc = 1.0, 0.1, 0.01, 1.6, 0.90, 1e-4
     b = (1.0, 0.5, -0.3)
     pred = inputgen.morton_sorted(inputgen.grid_cell_centres(m))
@@ -50,7 +62,8 @@ def test_coverage_matches_oracle(lib):
     # oracle: the joint covariance, its factor (also the truth generator) and the weights
     V = oracle.covariance_matrix(xy, "matern", 1.0, beta, nu, 0.0, n_p, tau2)
     Lv = oracle.cholesky_lower(V)
-    Wo, _, vo = oracle.universal_kriging(V[n_p:, n_p:], V[n_p:, :n_p], X[n_p:], X[:n_p], np.zeros(n_o), 1.0)
+    if with_oracle:
+        Wo, _, vo = oracle.universal_kriging(V[n_p:, n_p:], V[n_p:, :n_p], X[n_p:], X[:n_p], np.zeros(n_o), 1.0)
     zeros_p, zeros_o = np.zeros((n_p, 1)), np.zeros((n_o, 1))
 
     hits_gpu = hits_oracle = 0
@@ -58,32 +71,38 @@ def test_coverage_matches_oracle(lib):
     for r in range(R_REPLICATES):
         truth = oracle.truth_field(Lv, X, b, inputgen.standard_normals(n, 1, 1000 + r)[:, 0])
         y = truth[n_p:]
-        Z = inputgen.standard_normals(n, M, 5000 + r)
-        # GPU chain: predictor W^T y (the correction of a zero simulation), simulations,
-        # correction, calibration
+        # GPU chain: predictor W^T y (the correction of a zero simulation), simulations, the
+        # correction fused with the calibration
         z = lib.krige_correct(W, dev(y), zero_col, n_p, n_o)[:, 0].contiguous()
-        Y = lib.trmm_sim(G, colmajor(Z), M)
-        S = lib.krige_correct(W, dev(y), Y, n_p, n_o)
-        out = lib.calibrate(S, z, v, u, level)
+        if with_oracle:
+            Z = inputgen.standard_normals(n, M, 5000 + r)
+            Y = lib.trmm_sim(G, colmajor(Z), M)
+        else:
+            Y = lib.trmm_sim(G, None, M, seed=5000 + r, flags=lib.CR_TRMM_GENERATE)
+        out = lib.correct_calibrate(W, dev(y), Y, n_p, n_o, z, v, u, level)
         c_in, c_out = out["c_in"].cpu().numpy(), out["c_out"].cpu().numpy()
         hits_gpu += oracle.coverage_event(truth[:n_p], c_in, c_out, u)
-        # oracle chain on the same truth and draws
-        zo = oracle.conditional_correction(Wo, y, zeros_p, zeros_o)[:, 0]
-        Yo = oracle.simulate(Lv, Z)
-        So = oracle.conditional_correction(Wo, y, Yo[:n_p], Yo[n_p:])
-        ref = oracle.calibrate(So, zo, vo, u, level)
-        hits_oracle += oracle.coverage_event(truth[:n_p], ref["c_in"], ref["c_out"], u)
-        region_diff.append(max(np.mean(c_in != ref["c_in"]), np.mean(c_out != ref["c_out"])))
+        if with_oracle:
+            # oracle chain on the same truth and draws
+            zo = oracle.conditional_correction(Wo, y, zeros_p, zeros_o)[:, 0]
+            Yo = oracle.simulate(Lv, Z)
+            So = oracle.conditional_correction(Wo, y, Yo[:n_p], Yo[n_p:])
+            ref = oracle.calibrate(So, zo, vo, u, level)
+            hits_oracle += oracle.coverage_event(truth[:n_p], ref["c_in"], ref["c_out"], u)
+            region_diff.append(max(np.mean(c_in != ref["c_in"]), np.mean(c_out != ref["c_out"])))
     G.close()
-    cov_gpu, cov_oracle = hits_gpu / R_REPLICATES, hits_oracle / R_REPLICATES
-    msg = (f"coverage gpu {cov_gpu:.3f} oracle {cov_oracle:.3f}; region differences max {max(region_diff):.4f} "
-           f"mean {np.mean(region_diff):.5f}; tiles fp64/32/16 {info['n_fp64']}/{info['n_fp32']}/{info['n_fp16']}")
+    p, lo, hi = _binomial_interval(hits_gpu, R_REPLICATES)
+    msg = (f"M = {M}, {R_REPLICATES} replicates: coverage gpu {p:.3f} [{lo:.3f}, {hi:.3f}]; tiles fp64/32/16 "
+           f"{info['n_fp64']}/{info['n_fp32']}/{info['n_fp16']}")
+    if with_oracle:
+        po, loo, hio = _binomial_interval(hits_oracle, R_REPLICATES)
+        msg += (f"; oracle {po:.3f} [{loo:.3f}, {hio:.3f}]; region differences max {max(region_diff):.4f} "
+                f"mean {np.mean(region_diff):.5f}")
+        assert abs(p - po) <= 0.02, msg
+        assert max(region_diff) <= 0.01, msg
     print(msg)
-    assert abs(cov_gpu - cov_oracle) <= 0.02, msg
-    assert max(region_diff) <= 0.01, msg
-    # sanity range around the nominal 0.90 (the pages report 0.83-0.91 for this method;
-    # 300 replicates carry a binomial standard error of about 0.017)
-    assert 0.75 <= cov_oracle <= 0.99, msg
+    # sanity range around the nominal 0.90 (the pages report 0.83-0.91 for this method)
+    assert 0.70 <= p <= 0.99, msg
 
 
 def test_scale_without_fp16_tiles(lib):
