@@ -271,6 +271,7 @@ extern "C" cr_status cr_tilemat_create(int n, int nb, cr_tilemat* out) {
   const size_t tile = (size_t)nb * nb;
   cudaError_t e;
   if ((e = cudaMalloc(&V->xy, (size_t)n * 2 * sizeof(double))) != cudaSuccess ||
+      (e = cudaMalloc(&V->xy4, (size_t)n * sizeof(float4))) != cudaSuccess ||
       (e = cudaMalloc(&V->stat_part, (size_t)V->ntiles * (nb / 64) * STAT_W * sizeof(double))) != cudaSuccess ||
       (e = cudaMalloc(&V->stats, (size_t)V->ntiles * STAT_W * sizeof(double))) != cudaSuccess ||
       (e = cudaMalloc(&V->minv, 2 * tile * sizeof(double))) != cudaSuccess ||
@@ -291,7 +292,7 @@ extern "C" cr_status cr_tilemat_destroy(cr_tilemat V) {
   cudaDeviceSynchronize();
   free_class_storage(V);
   dfree(V->b16); dfree(V->y16); dfree(V->bnorm_part); dfree(V->minv_all); dfree(V->diag_tasks); dfree(V->diag_flags); dfree(V->diag_pub); dfree(V->minv_part); dfree(V->diag_df);
-  dfree(V->xy); dfree(V->stat_part); dfree(V->d_refine); dfree(V->refine_part); dfree(V->stats); dfree(V->minv); dfree(V->scratch64); dfree(V->d_status);
+  dfree(V->xy); dfree(V->xy4); dfree(V->stat_part); dfree(V->d_refine); dfree(V->refine_part); dfree(V->stats); dfree(V->minv); dfree(V->scratch64); dfree(V->d_status);
   if (V->s_hi) cudaStreamDestroy(V->s_hi);
   if (V->s_lo) cudaStreamDestroy(V->s_lo);
   if (V->s_mid) cudaStreamDestroy(V->s_mid);

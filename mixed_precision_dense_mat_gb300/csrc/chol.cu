@@ -28,7 +28,8 @@
 namespace cr {
 
 // d_tiles: count tile codes (i << 16 | j), the first ndiag of them diagonal (FP64 class)
-cr_status convert_tiles(cr_tilemat V, const int* d_tiles, int count, int ndiag, cudaStream_t stream);
+cr_status convert_tiles(cr_tilemat V, const int* d_tiles, int count, int ndiag, int nheavy, bool diag_df,
+                        cudaStream_t stream);
 
 namespace {
 
@@ -100,7 +101,7 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
   // of column j waits only for its range, so it starts after the first column's tiles
   // instead of after all of them.
   if (nt > 32767) return fail(CR_ERR_ARG, "cr_potrf_adaptive: more than 32767 tile rows");
-  std::vector<int> gen_list, gen_off{0}, gen_ndiag, gen_range_of(nt, 0);
+  std::vector<int> gen_list, gen_off{0}, gen_ndiag, gen_nheavy, gen_range_of(nt, 0);
   for (int c0 = 0, w = 1; c0 < nt; c0 += w, w *= 2) {
     const int c1 = std::min(nt, c0 + w);
     gen_ndiag.push_back(c1 - c0);
@@ -108,8 +109,17 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
       gen_list.push_back(c << 16 | c);
       gen_range_of[c] = (int)gen_off.size() - 1;
     }
-    for (int c = c0; c < c1; ++c)
-      for (int i = c + 1; i < nt; ++i) gen_list.push_back(i << 16 | c);
+    // the other tiles of the range by cost, heaviest first (FP64 evaluations, then
+    // double-float, then single precision), so that a launch does not end on a few long CTAs
+    for (int pass = 0; pass < 3; ++pass) {
+      for (int c = c0; c < c1; ++c)
+        for (int i = c + 1; i < nt; ++i) {
+          const int k = cls[tidx(i, c)];
+          const int rank = k == CR_PREC_FP64 ? 0 : (k == CR_PREC_FP32 ? 1 : 2);
+          if (rank == pass) gen_list.push_back(i << 16 | c);
+        }
+      if (pass == 1) gen_nheavy.push_back((int)gen_list.size() - gen_off.back() - gen_ndiag.back());
+    }
     gen_off.push_back((int)gen_list.size());
   }
   const int n_ranges = (int)gen_off.size() - 1;
@@ -186,13 +196,15 @@ cr_status build_and_run_cholesky(cr_tilemat V, cudaStream_t caller) {
     if (r <= gen_range_of[std::min(1, nt - 1)]) {
       // the ranges of columns 0 and 1: the diagonal tiles first, in a launch of their own (the
       // first two diagonal factorisations need nothing else)
-      CR_TRY(convert_tiles(V, d_gen + gen_off[r], gen_ndiag[r], gen_ndiag[r], x.gen));
+      CR_TRY(convert_tiles(V, d_gen + gen_off[r], gen_ndiag[r], gen_ndiag[r], 0, use_df, x.gen));
       CR_CUDA(cudaEventRecord(x.ev_gdiag[r], x.gen));
-      CR_TRY(convert_tiles(V, d_gen + gen_off[r] + gen_ndiag[r], gen_off[r + 1] - gen_off[r] - gen_ndiag[r], 0, x.gen));
+      CR_TRY(convert_tiles(V, d_gen + gen_off[r] + gen_ndiag[r], gen_off[r + 1] - gen_off[r] - gen_ndiag[r], 0,
+                           gen_nheavy[r], use_df, x.gen));
     } else {
       // later ranges in one launch, diagonal tiles issued first, so that their FP64 work
       // overlaps the other tiles' FP32 work
-      CR_TRY(convert_tiles(V, d_gen + gen_off[r], gen_off[r + 1] - gen_off[r], gen_ndiag[r], x.gen));
+      CR_TRY(convert_tiles(V, d_gen + gen_off[r], gen_off[r + 1] - gen_off[r], gen_ndiag[r], gen_nheavy[r], use_df,
+                           x.gen));
       CR_CUDA(cudaEventRecord(x.ev_gdiag[r], x.gen));
     }
     CR_CUDA(cudaEventRecord(x.ev_gen[r], x.gen));

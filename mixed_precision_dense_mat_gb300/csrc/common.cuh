@@ -95,6 +95,7 @@ struct cr_tilemat_s {
   int device = 0;
   // covariance model, locations and tile statistics (tiles are generated on demand)
   double* xy = nullptr;          // n x 2 locations (copy of the caller's)
+  float4* xy4 = nullptr;         // the locations as double-float pairs (x.hi, x.lo, y.hi, y.lo)
   cr::CovK covk{};
   double* stat_part = nullptr;   // ntiles * (nb/64) * STAT_W partials
   double* stats = nullptr;       // ntiles * STAT_W : sum of squares, min, max, error parameter

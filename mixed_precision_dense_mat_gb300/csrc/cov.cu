@@ -83,8 +83,8 @@ __device__ __noinline__ double cov_entry64_ool(const CovK& p, const double* __re
   return cov_entry64(p, xy, gi, gj);
 }
 
-// Double-float entry for an off-diagonal pair with coordinate differences (dx, dy); sets
-// *fallback when the scaled distance leaves the double-float exponential's range.
+// Double-float entry for an off-diagonal pair with coordinate differences (dx, dy), times
+// sig; sets *fallback when the scaled distance leaves the double-float exponential's range.
 __device__ __forceinline__ df cov_entry_df(const CovK& p, df dx, df dy, df sig, df inv_range, const DfExpTables& T,
                                            bool* fallback) {
   const df d2 = df_add(df_mul(dx, dx), df_mul(dy, dy));
@@ -119,17 +119,25 @@ __device__ __forceinline__ void tile_of(int t, int& i, int& j) {
   j = t - i * (i + 1) / 2;
 }
 
+// The locations as double-float pairs (x.hi, x.lo, y.hi, y.lo), once per covariance, so that
+// the tile kernels load them without FP64 conversions.
+__global__ void k_points_df(const double* __restrict__ xy, int n, float4* __restrict__ xy4) {
+  const int g = blockIdx.x * blockDim.x + threadIdx.x;
+  if (g >= n) return;
+  const Pt pt = load_pt(xy, g);
+  xy4[g] = make_float4(pt.x.hi, pt.x.lo, pt.y.hi, pt.y.lo);
+}
+
 // Column points (nb) then the 64 row points of row block r0 of tile (i, j) into shared
 // memory as (x.hi, x.lo, y.hi, y.lo); returns the thread's largest |coordinate| (high words).
-__device__ __forceinline__ float load_tile_points(const double* __restrict__ xy, int n, int nb, int i, int j, int r0,
+__device__ __forceinline__ float load_tile_points(const float4* __restrict__ xy4, int n, int nb, int i, int j, int r0,
                                                   float4* s_pts) {
   float cmax = 0.0f;
   for (int q = threadIdx.x; q < nb + 64; q += blockDim.x) {
     const int g = q < nb ? j * nb + q : i * nb + r0 + (q - nb);
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
     if (g < n) {
-      const Pt pt = load_pt(xy, g);
-      v = make_float4(pt.x.hi, pt.x.lo, pt.y.hi, pt.y.lo);
+      v = __ldg(xy4 + g);
       cmax = fmaxf(cmax, fmaxf(fabsf(v.x), fabsf(v.z)));
     }
     s_pts[q] = v;
@@ -141,13 +149,14 @@ __device__ __forceinline__ float load_tile_points(const double* __restrict__ xy,
 // squares, min, max and 0 (an exact partial has no error bound) over valid entries, STAT_W
 // doubles at sp.  Nothing is stored.
 template <bool DF, int ROWS>
-__device__ __forceinline__ void stats_exact(const double* __restrict__ xy, int n, int nb, const CovK& p, int i, int j,
+__device__ __forceinline__ void stats_exact(const double* __restrict__ xy, const float4* __restrict__ xy4, int n, int nb,
+                                            const CovK& p, int i, int j,
                                             int rbk, double* __restrict__ sp) {
   const int r0 = rbk * ROWS;
   extern __shared__ float4 s_pts[];
   float4* s_col = s_pts;
   float4* s_row = s_pts + nb;
-  load_tile_points(xy, n, nb, i, j, r0, s_pts);
+  load_tile_points(xy4, n, nb, i, j, r0, s_pts);
   // exponential tables in shared memory: their per-thread indices diverge
   __shared__ DfExpTables s_T;
   for (int q = threadIdx.x; q < 64; q += blockDim.x) {
@@ -222,14 +231,15 @@ __device__ __forceinline__ void stats_exact(const double* __restrict__ xy, int n
 // per (listed tile, ROWS-row block).  Partials are indexed by tile, or by list position when
 // by_list is set (the policy's recomputations, whose 16-row blocks keep each CTA short).
 template <bool DF, int ROWS>
-__global__ void __launch_bounds__(256) k_cov_stats(const double* __restrict__ xy, int n, int nb, CovK p,
+__global__ void __launch_bounds__(256) k_cov_stats(const double* __restrict__ xy, const float4* __restrict__ xy4, int n,
+                                                   int nb, CovK p,
                                                    double* __restrict__ stat_part, const int* __restrict__ tiles,
                                                    int by_list) {
   const int tile = tiles ? tiles[blockIdx.x] : blockIdx.x;
   int i, j;
   tile_of(tile, i, j);
   const size_t slot = by_list ? blockIdx.x : tile;
-  stats_exact<DF, ROWS>(xy, n, nb, p, i, j, blockIdx.y, stat_part + (slot * gridDim.y + blockIdx.y) * STAT_W);
+  stats_exact<DF, ROWS>(xy, xy4, n, nb, p, i, j, blockIdx.y, stat_part + (slot * gridDim.y + blockIdx.y) * STAT_W);
 }
 
 // Fast statistics of row block rbk of the off-diagonal tile (i, j), closed-form Matern
@@ -255,13 +265,13 @@ __global__ void __launch_bounds__(256) k_cov_stats(const double* __restrict__ xy
 // or infinity where the bound does not hold (x > 80, where the exponential leaves the
 // normal range; entries below 2^-120 or above 2^56, where products, squares or their sums
 // leave it).
-__device__ __forceinline__ void stats_fast(const double* __restrict__ xy, int n, int nb, const CovK& p, int i, int j,
+__device__ __forceinline__ void stats_fast(const float4* __restrict__ xy4, int n, int nb, const CovK& p, int i, int j,
                                            int rbk, double* __restrict__ sp) {
   const int r0 = rbk * 64;
   extern __shared__ float4 s_pts[];
   float4* s_col = s_pts;
   float4* s_row = s_pts + nb;
-  float cmax = load_tile_points(xy, n, nb, i, j, r0, s_pts);
+  float cmax = load_tile_points(xy4, n, nb, i, j, r0, s_pts);
   __syncthreads();
   const float sig = p.sig_hi, invr = p.invr_hi;
   const int kind = p.kind;
@@ -325,7 +335,8 @@ __device__ __forceinline__ void stats_fast(const double* __restrict__ xy, int n,
 // Statistics pass of a new covariance for the closed-form Matern orders: CTAs 0 .. nt nrb - 1
 // take the diagonal tiles exactly (double-float, FP64 for the diagonal entries); the others
 // take the off-diagonal tiles, in row order, through the FP32 pass with its error bound.
-__global__ void __launch_bounds__(256) k_cov_stats_split(const double* __restrict__ xy, int n, int nb, int nt, CovK p,
+__global__ void __launch_bounds__(256) k_cov_stats_split(const double* __restrict__ xy, const float4* __restrict__ xy4,
+                                                         int n, int nb, int nt, CovK p,
                                                          double* __restrict__ stat_part) {
   const int nrb = nb / 64, ndiag = nt * nrb;
   const int b = blockIdx.x;
@@ -342,8 +353,8 @@ __global__ void __launch_bounds__(256) k_cov_stats_split(const double* __restric
     j = o - i * (i - 1) / 2;
   }
   double* sp = stat_part + ((size_t)tidx(i, j) * nrb + rbk) * STAT_W;
-  if (i == j) stats_exact<true, 64>(xy, n, nb, p, i, j, rbk, sp);
-  else stats_fast(xy, n, nb, p, i, j, rbk, sp);
+  if (i == j) stats_exact<true, 64>(xy, xy4, n, nb, p, i, j, rbk, sp);
+  else stats_fast(xy4, n, nb, p, i, j, rbk, sp);
 }
 
 // Per-tile reduction of the partials of the tiles in the list (all tiles without one).
@@ -381,47 +392,232 @@ __device__ __forceinline__ void generate_diag64(const double* __restrict__ xy, i
   }
 }
 
-// Generation of s^2 V in each tile's class (Alg.2 step 12) over a tile list whose first
-// ndiag entries are diagonal tiles: CTAs 0 .. ndiag nb/16 - 1 take the diagonal tiles, nb/16
-// CTAs each (generate_diag64, the FP64 evaluations spread wide so that they finish early);
-// the others take one (tile, 64-row block) each, row block b % (nb/64) of the tile
-// (i, j) = (e >> 16, e & 0xffff), e = tiles[ndiag + b / (nb/64)].  The list fixes the issue
-// order: the factorisation lists column by column, so that each column is complete before
-// it is needed.  Padding rows/columns are the identity (scaled by s^2).
-__global__ void __launch_bounds__(256) k_generate(const double* __restrict__ xy, int n, int nb, CovK p, double s2,
+// Square root by the PTX approximation (relative error about 2^-23): enough for a distance
+// whose covariance is rounded to FP16.
+__device__ __forceinline__ float sqrt_approx(float x) {
+  float y;
+  asm("sqrt.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// FP16 tile, one 64-row block (off-diagonal): a single-precision evaluation, accurate to a
+// few 1e-6, is far inside the 2^-11 rounding of the stored value; distances from the
+// double-float coordinates, so that near points do not lose digits to cancellation.  Each
+// work item is four adjacent columns, whose coordinates stay in registers, over a run of rows
+// taken two at a time (eight independent evaluations in flight, no branches: MODE 0-2 the
+// closed-form Matern orders nu = 1/2, 3/2, 5/2, 3 the power-exponential family); the four
+// values are converted to FP16 in two packed conversions and stored as one 8-byte word, so
+// that a warp writes 256 contiguous bytes of a row.
+template <int MODE>
+__device__ __forceinline__ void gen_fp16_tile(const CovK& p, int n, int nb, int i, int j, int r0, double s2,
+                                              const float4* s_col, const float4* s_row, uint2* dst) {
+  const int nq = nb / 4;
+  const int splits = nq >= 256 ? 1 : (nq >= 128 ? 2 : (nq >= 64 ? 4 : 8));
+  const int run = 64 / splits;
+  const float sig_s2 = p.sig_hi * (float)s2, invr = p.invr_hi, nuf = (float)p.nu;
+  for (int w = threadIdx.x; w < nq * splits; w += blockDim.x) {
+    const int q = w % nq, rs = r0 + (w / nq) * run;
+    const int c0 = 4 * q, gj0 = j * nb + c0;
+    float bxh[4], bxl[4], byh[4], byl[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float4 b4 = s_col[c0 + u];
+      bxh[u] = b4.x; bxl[u] = b4.y; byh[u] = b4.z; byl[u] = b4.w;
+    }
+#pragma unroll 1
+    for (int r = rs; r < rs + run; r += 2) {
+      float val[2][4];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float4 a = s_row[r + h - r0];
+        const bool row_ok = i * nb + r + h < n;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float dx = (a.x - bxh[u]) + (a.y - bxl[u]), dy = (a.z - byh[u]) + (a.w - byl[u]);
+          const float x = sqrt_approx(fmaf(dx, dx, dy * dy)) * invr;
+          float e;
+          if (MODE == 3) {
+            // exp(-x^nu), x^nu = 2^(nu log2 x) (x = 0 gives 0): a few 1e-6 relative
+            const float y = x > 0.0f ? exp2f(nuf * __log2f(x)) : 0.0f;
+            e = __expf(-y);
+          } else {
+            e = __expf(-x);   // ex2-based: ~3e-6 relative at x < 50, against FP16's 4.9e-4
+            if (MODE == 1) e *= 1.0f + x;
+            if (MODE == 2) e *= fmaf(x * x, 1.0f / 3.0f, 1.0f + x);
+          }
+          val[h][u] = (row_ok && gj0 + u < n) ? sig_s2 * e : 0.0f;
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const __half2 lo = __floats2half2_rn(val[h][0], val[h][1]);
+        const __half2 hi = __floats2half2_rn(val[h][2], val[h][3]);
+        dst[((size_t)(r + h) * nb + c0) / 4] =
+            make_uint2(*reinterpret_cast<const unsigned*>(&lo), *reinterpret_cast<const unsigned*>(&hi));
+      }
+    }
+  }
+}
+
+// Double-float covariance of the pair (a, b) (points as (x.hi, x.lo, y.hi, y.lo)) times ss,
+// to about 2^-39 relative, for values rounded to FP32 afterwards, without branches, so that
+// a thread's independent evaluations interleave: the square root from the PTX approximation
+// and one Newton step (as df_sqrt_lite), the exponential of df_exp_lite, the Matern order
+// KIND (nu = 1/2, 3/2, 5/2) as a template argument.  far: the scaled distance is beyond the
+// double-float exponential's range (the value is then to be taken in FP64).
+template <int KIND>
+__device__ __forceinline__ df cov_df_lite(float4 a, float4 b, df ss, df invr, const DfExpTables& T, bool& far) {
+  const df dx = df_add({a.x, a.y}, df_neg({b.x, b.y}));
+  const df dy = df_add({a.z, a.w}, df_neg({b.z, b.w}));
+  const df d2 = df_add(df_mul(dx, dx), df_mul(dy, dy));
+  float s, inv_s;
+  asm("sqrt.approx.ftz.f32 %0, %1;" : "=f"(s) : "f"(d2.hi));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv_s) : "f"(s));
+  const df pp = df_two_prod(s, s);
+  const float res = __fadd_rn(__fsub_rn(__fsub_rn(d2.hi, pp.hi), pp.lo), d2.lo);
+  const float corr = s > 0.0f ? __fmul_rn(res, 0.5f * inv_s) : 0.0f;
+  const df x = df_mul(df_quick_two_sum(s, corr), invr);
+  far = x.hi > 80.0f;
+  df v = df_exp_lite(df_neg(x), T);
+  if (KIND == 1) v = df_mul(df_add_f(x, 1.0f), v);
+  if (KIND == 2) {
+    const df third = {0.3333333432674408f, -9.934107e-09f};   // 1/3 = hi + lo
+    v = df_mul(df_add_f(df_add(x, df_mul(df_mul(x, x), third)), 1.0f), v);
+  }
+  const df out = df_mul(v, ss);
+  const bool zero = d2.hi == 0.0f;   // coincident sites: the covariance is sigma^2
+  return {zero ? ss.hi : out.hi, zero ? ss.lo : out.lo};
+}
+
+// FP32 tile, one block of `rows` rows (off-diagonal, closed-form Matern order KIND): double-
+// float evaluations rounded once to FP32, sigma^2 s^2 folded into one factor ss, four rows
+// at a time (four independent evaluation chains per thread); the rare scaled distances
+// beyond the double-float exponential's range take the FP64 evaluation afterwards.
+template <int KIND>
+__device__ __forceinline__ void gen_fp32_tile(const CovK& p, const double* __restrict__ xy, int n, int nb, int i, int j,
+                                              int r0, int rows, double s2, df ss, df invr, const float4* s_col,
+                                              const float4* s_row, const DfExpTables& T, float* dst) {
+  for (int c = threadIdx.x; c < nb; c += blockDim.x) {
+    const float4 b = s_col[c];
+    const int gj = j * nb + c;
+#pragma unroll 1
+    for (int r = r0; r < r0 + rows; r += 4) {
+      df w[4];
+      bool far[4];
+#pragma unroll
+      for (int h = 0; h < 4; ++h) w[h] = cov_df_lite<KIND>(s_row[r + h - r0], b, ss, invr, T, far[h]);
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const int gi = i * nb + r + h;
+        float f;
+        if (gi >= n || gj >= n) f = 0.0f;
+        else if (__builtin_expect(far[h], 0)) f = (float)(cov_entry64_ool(p, xy, gi, gj) * s2);
+        else f = __fadd_rn(w[h].hi, w[h].lo);
+        dst[(size_t)(r + h) * nb + c] = f;
+      }
+    }
+  }
+}
+
+// Generation of s^2 V in each tile's class (Alg.2 step 12) over a tile list: its first ndiag
+// entries are diagonal tiles, the next nheavy the tiles evaluated in FP64 or double-float
+// (FP64 and FP32 classes), the rest FP16 tiles.  CTAs 0 .. ndiag nb/16 - 1 take the diagonal
+// tiles, nb/16 CTAs each (generate_diag64 in FP64, or the double-float evaluation when the
+// double-float executor factors them; spread wide so that they finish early); then
+// nb/hrows CTAs per heavy tile, hrows rows each (16, 32 or 64: the host picks the largest
+// that still gives the heavy tiles a few waves of CTAs), and nb/64 CTAs per FP16 tile, 64
+// rows each.  The list fixes the issue order within a launch;
+// the factorisation issues one launch per column range, so that each column is complete
+// before it is needed.  Padding rows/columns are the identity (scaled by s^2).
+__global__ void __launch_bounds__(256, 2) k_generate(const double* __restrict__ xy, const float4* __restrict__ xy4, int n,
+                                                     int nb, CovK p, double s2,
                                                   float s2_hi, float s2_lo, TileView v, const int* __restrict__ tiles,
-                                                  int ndiag) {
+                                                  int ndiag, int nheavy, int hrows, int diag_df) {
   const int nrb = nb / 64, nsub = nb / 16;
+  extern __shared__ float4 s_pts[];
+  __shared__ DfExpTables s_T;
   if ((int)blockIdx.x < ndiag * nsub) {
-    generate_diag64(xy, n, nb, p, s2, v, tiles[blockIdx.x / nsub] >> 16, blockIdx.x % nsub);
+    const int i = tiles[blockIdx.x / nsub] >> 16, q = blockIdx.x % nsub;
+    if (!diag_df) {
+      generate_diag64(xy, n, nb, p, s2, v, i, q);
+      return;
+    }
+    // Diagonal tile for the double-float executor, which holds the tile in double-float: the
+    // off-diagonal entries by the double-float evaluation of the FP32-class tiles (the same
+    // ~2^-48 relative accuracy the executor keeps), the diagonal entries in FP64.  Rows as in
+    // generate_diag64: 8 from the top half, the mirrored 8 from the bottom half.
+    float4* s_col = s_pts;
+    float4* s_row = s_pts + nb;
+    auto row_of = [&](int rr) { return rr < 8 ? 8 * q + rr : nb - 8 * (q + 1) + (rr - 8); };
+    for (int k = threadIdx.x; k < nb + 16; k += blockDim.x) {
+      const int g = i * nb + (k < nb ? k : row_of(k - nb));
+      s_pts[k] = g < n ? __ldg(xy4 + g) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (int k = threadIdx.x; k < 64; k += blockDim.x) {
+      s_T.t_hi[k] = c_dfexp.t_hi[k];
+      s_T.t_lo[k] = c_dfexp.t_lo[k];
+    }
+    if (threadIdx.x == 0) { s_T.c1 = c_dfexp.c1; s_T.c2 = c_dfexp.c2; s_T.c3 = c_dfexp.c3; }
+    __syncthreads();
+    double* dst = v.pool64 + (size_t)v.i64[tidx(i, i)] * nb * nb;
+    const df sig = {p.sig_hi, p.sig_lo}, invr = {p.invr_hi, p.invr_lo}, s2d = {s2_hi, s2_lo};
+    for (int rr = 0; rr < 16; ++rr) {
+      const int r = row_of(rr), gi = i * nb + r;
+      const float4 a = s_row[rr];
+      for (int c = threadIdx.x; c < nb; c += blockDim.x) {
+        const int gj = i * nb + c;
+        double x = 0.0;
+        if (gi >= n || gj >= n) {
+          x = gi == gj ? s2 : 0.0;
+        } else if (c == r) {
+          x = cov_entry64(p, xy, gi, gj) * s2;
+        } else if (c < r) {
+          const float4 b = s_col[c];
+          const df dx = df_add({a.x, a.y}, df_neg({b.x, b.y}));
+          const df dy = df_add({a.z, a.w}, df_neg({b.z, b.w}));
+          bool fb = false;
+          const df vd = cov_entry_df(p, dx, dy, sig, invr, s_T, &fb);
+          if (__builtin_expect(fb, 0)) x = cov_entry64_ool(p, xy, gi, gj) * s2;
+          else {
+            const df w = df_mul(vd, s2d);
+            x = (double)w.hi + (double)w.lo;
+          }
+        }
+        dst[(size_t)r * nb + c] = x;
+      }
+    }
     return;
   }
+  // the first nheavy tiles after the diagonal ones (FP64 and FP32 classes) in blocks of hrows
+  // rows, the others in 64-row blocks
   const int b = blockIdx.x - ndiag * nsub;
-  const int rb = b % nrb;
-  const int e = tiles[ndiag + b / nrb];
+  const int hsub = nb / hrows;
+  int e, r0, rows;
+  if (b < nheavy * hsub) {
+    e = tiles[ndiag + b / hsub];
+    r0 = (b % hsub) * hrows;
+    rows = hrows;
+  } else {
+    const int b2 = b - nheavy * hsub;
+    e = tiles[ndiag + nheavy + b2 / nrb];
+    r0 = (b2 % nrb) * 64;
+    rows = 64;
+  }
   const int i = e >> 16, j = e & 0xffff;
   const int t = tidx(i, j);
-  const int r0 = rb * 64;
   const int cls = v.cls[t];
   const bool use_df = p.use_df && cls != CR_PREC_FP64;
   // FP16 tiles take the single-precision evaluation for the closed-form Matern orders and for
   // the power-exponential family
   const bool fast16 = cls == CR_PREC_FP16 && (p.use_df || p.family == CR_COV_POWEXP);
-  extern __shared__ float4 s_pts[];
   float4* s_col = s_pts;
   float4* s_row = s_pts + nb;
   if (use_df || fast16) {
-    for (int q = threadIdx.x; q < nb + 64; q += blockDim.x) {
+    for (int q = threadIdx.x; q < nb + rows; q += blockDim.x) {
       const int g = q < nb ? j * nb + q : i * nb + r0 + (q - nb);
-      float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (g < n) {
-        const Pt pt = load_pt(xy, g);
-        w = make_float4(pt.x.hi, pt.x.lo, pt.y.hi, pt.y.lo);
-      }
-      s_pts[q] = w;
+      s_pts[q] = g < n ? __ldg(xy4 + g) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
-  __shared__ DfExpTables s_T;
   for (int q = threadIdx.x; q < 64; q += blockDim.x) {
     s_T.t_hi[q] = c_dfexp.t_hi[q];
     s_T.t_lo[q] = c_dfexp.t_lo[q];
@@ -430,42 +626,29 @@ __global__ void __launch_bounds__(256) k_generate(const double* __restrict__ xy,
   __syncthreads();
   const size_t count = (size_t)nb * nb;
   if (fast16) {
-    // FP16 tiles (off-diagonal): a single-precision evaluation, accurate to a few 1e-6, is
-    // far inside the 2^-11 rounding of the stored value; distances from the double-float
-    // coordinates, so that near points do not lose digits to cancellation
-    // Two adjacent columns per thread, converted to FP16 together (one packed conversion
-    // instead of two single ones, which issue on GB300's slow conversion pipe) and stored
-    // as one 4-byte pair.
-    __half2* dst = reinterpret_cast<__half2*>(v.pool16 + (size_t)v.hi16[t] * count);
-    const float sig = p.sig_hi, invr = p.invr_hi, s2f = (float)s2, nuf = (float)p.nu;
-    const bool powexp = p.family == CR_COV_POWEXP;
-    const int half_nb = nb / 2;
-    auto entry = [&](int r, int c) {
-      const int gi = i * nb + r, gj = j * nb + c;
-      if (gi >= n || gj >= n) return 0.0f;
-      const float4 a = s_row[r - r0], b = s_col[c];
-      const float dx = (a.x - b.x) + (a.y - b.y), dy = (a.z - b.z) + (a.w - b.w);
-      const float x = sqrtf(fmaf(dx, dx, dy * dy)) * invr;
-      if (powexp) {
-        // exp(-x^nu), x^nu = 2^(nu log2 x) (x = 0 gives 2^-inf = 0): a few 1e-6 relative
-        const float y = x > 0.0f ? exp2f(nuf * __log2f(x)) : 0.0f;
-        return sig * __expf(-y) * s2f;
-      }
-      const float e = __expf(-x);   // ex2-based: ~3e-6 relative at x < 50, against FP16's 4.9e-4
-      const float poly = p.kind == 0 ? 1.0f : (p.kind == 1 ? 1.0f + x : fmaf(x * x, 1.0f / 3.0f, 1.0f + x));
-      return sig * poly * e * s2f;
-    };
-    // each thread keeps its column pair and walks the 64 rows: no per-entry index division
-    for (int cp = threadIdx.x; cp < half_nb; cp += blockDim.x)
-#pragma unroll 1
-      for (int r = r0; r < r0 + 64; ++r)
-        dst[((size_t)r * nb + 2 * cp) / 2] = __floats2half2_rn(entry(r, 2 * cp), entry(r, 2 * cp + 1));
+    uint2* dst = reinterpret_cast<uint2*>(v.pool16 + (size_t)v.hi16[t] * count);
+    switch (p.family == CR_COV_POWEXP ? 3 : p.kind) {
+      case 0: gen_fp16_tile<0>(p, n, nb, i, j, r0, s2, s_col, s_row, dst); break;
+      case 1: gen_fp16_tile<1>(p, n, nb, i, j, r0, s2, s_col, s_row, dst); break;
+      case 2: gen_fp16_tile<2>(p, n, nb, i, j, r0, s2, s_col, s_row, dst); break;
+      default: gen_fp16_tile<3>(p, n, nb, i, j, r0, s2, s_col, s_row, dst); break;
+    }
     return;
   }
   const df sig = {p.sig_hi, p.sig_lo}, invr = {p.invr_hi, p.invr_lo}, s2d = {s2_hi, s2_lo};
+  if (use_df && cls == CR_PREC_FP32 && i != j) {
+    float* dst = v.pool32 + (size_t)v.i32[t] * count;
+    const df ss = df_mul(sig, s2d);
+    switch (p.kind) {
+      case 0: gen_fp32_tile<0>(p, xy, n, nb, i, j, r0, rows, s2, ss, invr, s_col, s_row, s_T, dst); break;
+      case 1: gen_fp32_tile<1>(p, xy, n, nb, i, j, r0, rows, s2, ss, invr, s_col, s_row, s_T, dst); break;
+      default: gen_fp32_tile<2>(p, xy, n, nb, i, j, r0, rows, s2, ss, invr, s_col, s_row, s_T, dst); break;
+    }
+    return;
+  }
   for (int c = threadIdx.x; c < nb; c += blockDim.x)
 #pragma unroll 1
-  for (int r = r0; r < r0 + 64; ++r) {
+  for (int r = r0; r < r0 + rows; ++r) {
     const int gi = i * nb + r, gj = j * nb + c;
     const size_t off = (size_t)r * nb + c;
     double v64 = 0.0;
@@ -599,6 +782,8 @@ extern "C" cr_status cr_cov_build(cr_tilemat V, const double* d_xy, const cr_cov
     k.sig_hi = a.hi; k.sig_lo = a.lo; k.invr_hi = b.hi; k.invr_lo = b.lo;
   }
   CR_CUDA(cudaMemcpyAsync(V->xy, d_xy, (size_t)V->n * 2 * sizeof(double), cudaMemcpyDeviceToDevice, stream));
+  k_points_df<<<(V->n + 255) / 256, 256, 0, stream>>>(V->xy, V->n, V->xy4);
+  CR_CHECK_LAUNCH("k_points_df");
   const int nrb = V->nb / 64;
   dim3 grid(V->ntiles, nrb);
   const size_t smem = (size_t)(V->nb + 64) * sizeof(float4);
@@ -608,9 +793,10 @@ extern "C" cr_status cr_cov_build(cr_tilemat V, const double* d_xy, const cr_cov
     // the other covariances: every tile exact
     TimedScope ts("k_cov_stats", stream);
     if (k.use_df)
-      k_cov_stats_split<<<(unsigned)V->ntiles * nrb, 256, smem, stream>>>(V->xy, V->n, V->nb, V->nt, k, V->stat_part);
+      k_cov_stats_split<<<(unsigned)V->ntiles * nrb, 256, smem, stream>>>(V->xy, V->xy4, V->n, V->nb, V->nt, k,
+                                                                          V->stat_part);
     else
-      k_cov_stats<false, 64><<<grid, 256, smem, stream>>>(V->xy, V->n, V->nb, k, V->stat_part, nullptr, 0);
+      k_cov_stats<false, 64><<<grid, 256, smem, stream>>>(V->xy, V->xy4, V->n, V->nb, k, V->stat_part, nullptr, 0);
   }
   CR_CHECK_LAUNCH("k_cov_stats");
   k_stats_reduce<<<(V->ntiles + 127) / 128, 128, 0, stream>>>(V->stat_part, V->ntiles, nrb, V->stats, nullptr, 0);
@@ -670,9 +856,10 @@ cr_status refine_stats(cr_tilemat V, const std::vector<int>& list) {
   {
     TimedScope ts("k_cov_stats_refine", 0);
     if (V->covk.use_df)
-      k_cov_stats<true, RR><<<grid, 256, smem, 0>>>(V->xy, V->n, V->nb, V->covk, V->refine_part, V->d_refine, 1);
+      k_cov_stats<true, RR><<<grid, 256, smem, 0>>>(V->xy, V->xy4, V->n, V->nb, V->covk, V->refine_part, V->d_refine, 1);
     else
-      k_cov_stats<false, RR><<<grid, 256, smem, 0>>>(V->xy, V->n, V->nb, V->covk, V->refine_part, V->d_refine, 1);
+      k_cov_stats<false, RR><<<grid, 256, smem, 0>>>(V->xy, V->xy4, V->n, V->nb, V->covk, V->refine_part, V->d_refine,
+                                                     1);
   }
   CR_CHECK_LAUNCH("k_cov_stats");
   k_stats_reduce<<<((unsigned)list.size() + 127) / 128, 128, 0, 0>>>(V->refine_part, (int)list.size(), nrr, V->stats,
@@ -682,15 +869,25 @@ cr_status refine_stats(cr_tilemat V, const std::vector<int>& list) {
   return fetch_stats(V);
 }
 
-cr_status convert_tiles(cr_tilemat V, const int* d_tiles, int count, int ndiag, cudaStream_t stream) {
+cr_status convert_tiles(cr_tilemat V, const int* d_tiles, int count, int ndiag, int nheavy, bool diag_df,
+                        cudaStream_t stream) {
   if (count <= 0) return CR_OK;
-  const unsigned grid = (unsigned)ndiag * (V->nb / 16) + (unsigned)(count - ndiag) * (V->nb / 64);
+  // heavy tiles: the largest row block (64, 32 or 16) that still gives them three waves of
+  // CTAs (two CTAs per SM), so that a launch with few heavy tiles does not end on them
+  int sms = 0, dev = 0;
+  CR_CUDA(cudaGetDevice(&dev));
+  CR_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  int hrows = 64;
+  while (hrows > 16 && (long)nheavy * (V->nb / hrows) < 3L * 2 * sms) hrows /= 2;
+  const unsigned grid = (unsigned)ndiag * (V->nb / 16) + (unsigned)nheavy * (V->nb / hrows) +
+                        (unsigned)(count - ndiag - nheavy) * (V->nb / 64);
   const size_t smem = (size_t)(V->nb + 64) * sizeof(float4);
   const double s2 = V->s * V->s;
   const df s2d = df_from_double(s2);
   {
     TimedScope ts("k_generate", stream);
-    k_generate<<<grid, 256, smem, stream>>>(V->xy, V->n, V->nb, V->covk, s2, s2d.hi, s2d.lo, V->view(), d_tiles, ndiag);
+    k_generate<<<grid, 256, smem, stream>>>(V->xy, V->xy4, V->n, V->nb, V->covk, s2, s2d.hi, s2d.lo, V->view(), d_tiles, ndiag,
+                                            nheavy, hrows, diag_df && V->covk.use_df ? 1 : 0);
   }
   CR_CHECK_LAUNCH("k_generate");
   return CR_OK;

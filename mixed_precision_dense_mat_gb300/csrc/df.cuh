@@ -110,4 +110,29 @@ __device__ __forceinline__ df df_exp(df y, const DfExpTables& T) {
   return df_ldexp(df_mul(tj, e), m);
 }
 
+// exp(y) for -80 <= y <= 0 to about 2^-39 relative, for values that are rounded to FP32
+// afterwards: the reduction of df_exp with the last piece of ln2/64 folded into the low
+// part, and exp(r) = 1 + r_hi + (r_lo + r_hi^2/2 + r_hi^3/6 + r_hi^4/24) with the bracket in
+// FP32 (|r| <= ln2/128, so the bracket is below 1.5e-5 and its FP32 rounding below 2^-39; the
+// omitted r^5/120 is below 2^-44).
+__device__ __forceinline__ df df_exp_lite(df y, const DfExpTables& T) {
+  const float big = 12582912.0f;
+  const float kb = __fadd_rn(__fmul_rn(y.hi, 92.33248261689366f), big);   // 64 / ln 2
+  const float kf = __fsub_rn(kb, big);
+  const int k = __float_as_int(kb) - __float_as_int(big);
+  const float t = __fmaf_rn(-kf, T.c1, y.hi);                     // exact
+  const df p = df_two_prod(kf, T.c2);
+  const df s = df_two_sum(t, -p.hi);
+  const float lo = __fmaf_rn(-kf, T.c3, __fsub_rn(__fadd_rn(s.lo, y.lo), p.lo));
+  const df r = df_two_sum(s.hi, lo);   // |lo| may exceed a tiny reduced argument
+  const float x = r.hi;
+  const float q = __fmul_rn(__fmul_rn(x, x), __fmaf_rn(x, __fmaf_rn(x, 1.0f / 24.0f, 1.0f / 6.0f), 0.5f));
+  df e = df_quick_two_sum(1.0f, x);
+  e = df_quick_two_sum(e.hi, __fadd_rn(e.lo, __fadd_rn(r.lo, q)));
+  const int j = k & 63;
+  const int m = (k - j) / 64;
+  const df tj = {T.t_hi[j], T.t_lo[j]};
+  return df_ldexp(df_mul(tj, e), m);
+}
+
 }  // namespace cr
