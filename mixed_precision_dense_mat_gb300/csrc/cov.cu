@@ -491,29 +491,40 @@ __device__ __forceinline__ df cov_df_lite(float4 a, float4 b, df ss, df invr, co
 
 // FP32 tile, one block of `rows` rows (off-diagonal, closed-form Matern order KIND): double-
 // float evaluations rounded once to FP32, sigma^2 s^2 folded into one factor ss, four rows
-// at a time (four independent evaluation chains per thread); the rare scaled distances
-// beyond the double-float exponential's range take the FP64 evaluation afterwards.
-template <int KIND>
+// at a time (four independent evaluation chains per thread).  The rare scaled distances
+// beyond the double-float exponential's range are stored as 0 and redone in FP64 by a second
+// pass of the threads that met one, so that the main loop holds no call.
+template <int KIND, int GR = 4>
 __device__ __forceinline__ void gen_fp32_tile(const CovK& p, const double* __restrict__ xy, int n, int nb, int i, int j,
                                               int r0, int rows, double s2, df ss, df invr, const float4* s_col,
                                               const float4* s_row, const DfExpTables& T, float* dst) {
+  bool any_far = false;
   for (int c = threadIdx.x; c < nb; c += blockDim.x) {
     const float4 b = s_col[c];
     const int gj = j * nb + c;
 #pragma unroll 1
-    for (int r = r0; r < r0 + rows; r += 4) {
-      df w[4];
-      bool far[4];
+    for (int r = r0; r < r0 + rows; r += GR) {
+      df w[GR];
+      bool far[GR];
 #pragma unroll
-      for (int h = 0; h < 4; ++h) w[h] = cov_df_lite<KIND>(s_row[r + h - r0], b, ss, invr, T, far[h]);
+      for (int h = 0; h < GR; ++h) w[h] = cov_df_lite<KIND>(s_row[r + h - r0], b, ss, invr, T, far[h]);
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const int gi = i * nb + r + h;
-        float f;
-        if (gi >= n || gj >= n) f = 0.0f;
-        else if (__builtin_expect(far[h], 0)) f = (float)(cov_entry64_ool(p, xy, gi, gj) * s2);
-        else f = __fadd_rn(w[h].hi, w[h].lo);
-        dst[(size_t)(r + h) * nb + c] = f;
+      for (int h = 0; h < GR; ++h) {
+        const bool valid = i * nb + r + h < n && gj < n;
+        any_far |= valid && far[h];
+        dst[(size_t)(r + h) * nb + c] = (valid && !far[h]) ? __fadd_rn(w[h].hi, w[h].lo) : 0.0f;
+      }
+    }
+  }
+  if (__builtin_expect(any_far, 0)) {
+    for (int c = threadIdx.x; c < nb; c += blockDim.x) {
+      const float4 b = s_col[c];
+      const int gj = j * nb + c;
+      for (int r = r0; r < r0 + rows; ++r) {
+        const int gi = i * nb + r;
+        bool far;
+        (void)cov_df_lite<KIND>(s_row[r - r0], b, ss, invr, T, far);
+        if (far && gi < n && gj < n) dst[(size_t)r * nb + c] = (float)(cov_entry64_ool(p, xy, gi, gj) * s2);
       }
     }
   }
