@@ -420,13 +420,17 @@ def run_krige(args, world, rank, local):
     Matern nu = 1, range 0.1, tau^2 = 0.01, tile 512, M = 1024, fixedacc 1e-6, u = 1.6, level
     0.90).  Kriging (W, zhat, v), the map and the factorisation are set up once (their times are
     reported, not in the metric); one step is one batch of M conditional simulations: normal
-    draws fused with the mixed-precision TRMM, then the correction fused with the calibration
-    (S is never written).  Metric: simulations per second, M / (t_rng + t_trmm + t_correct +
-    t_calibrate).  The unfused correction + calibration is timed beside it."""
+    draws fused with the mixed-precision TRMM, then the correction with the calibration
+    (cr_correct_calibrate: with the double-float product S is never written; with the Ozaki
+    product on the tensor cores, --fp64-gemm ozaki, S goes through scratch).  Metric:
+    simulations per second, M / (t_rng + t_trmm + t_correct + t_calibrate).  The separate
+    correction + calibration calls are timed beside it."""
     import torch
     import mixed_precision_dense_mat_gb300 as cr
     torch.cuda.set_device(local)
     cr.load()
+    ozaki = args.fp64_gemm == "ozaki"
+    cr.set_option(cr.CR_OPT_FP64_GEMM, cr.CR_GEMM_OZAKI if ozaki else cr.CR_GEMM_DF)
     w = inputgen.WORKLOADS["k"]
     n, n_p, n_o, nb, M = w.n, w.n_pred, w.n_obs, w.nb, w.M
     dev = torch.device("cuda", local)
@@ -486,7 +490,7 @@ def run_krige(args, world, rank, local):
     pe[2].record(stream)
     torch.cuda.synchronize()
     parts["rng_trmm"] = pe[0].elapsed_time(pe[1])
-    parts["correct_calibrate_fused"] = pe[1].elapsed_time(pe[2])
+    parts["correct_calibrate"] = pe[1].elapsed_time(pe[2])
     ue = [ev() for _ in range(3)]
     ue[0].record(stream)
     S = cr.krige_correct(W, yo, Y, n_p, n_o)
@@ -494,19 +498,20 @@ def run_krige(args, world, rank, local):
     cr.calibrate(S, zhat, v, w.u, w.level)
     ue[2].record(stream)
     torch.cuda.synchronize()
-    parts["correct_unfused"] = ue[0].elapsed_time(ue[1])
-    parts["calibrate_unfused"] = ue[1].elapsed_time(ue[2])
+    parts["correct"] = ue[0].elapsed_time(ue[1])
+    parts["calibrate"] = ue[1].elapsed_time(ue[2])
     corr_flops = 2.0 * n_p * n_o * M
     if rank == 0:
         line = {"metric": "conditional simulations/s (kriging workload)", "value": world * M / (ms / 1e3),
                 "unit": "simulations/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16/f32/f64 adaptive; df correction",
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16/f32/f64 adaptive; " + ("Ozaki FP16 tensor-core correction" if ozaki else "df correction"),
                 "data": "synthetic",
                 "config": {"workload": w.name, "n_pred": n_p, "n_obs": n_o, "nb": nb, "M": M, "fixedacc": w.fixedacc,
                            "u": w.u, "level": w.level, "parallelism": f"replicas x{world}"},
                 "setup_ms": {"covariance_and_kriging": t_krige, "map_and_cholesky": t_chol},
                 "parts_ms": parts,
-                "correction_tflops": corr_flops / (parts["correct_calibrate_fused"] / 1e3) / 1e12,
+                "correction_tflops": corr_flops / (parts["correct"] / 1e3) / 1e12,
+                "fp64_gemm": args.fp64_gemm,
                 "precision_map": {"n_fp64": info["n_fp64"], "n_fp32": info["n_fp32"], "n_fp16": info["n_fp16"], "s": info["s"]},
                 "regions": {"q_in": out["q_in"], "q_out": out["q_out"], "inner": int(out["c_in"].sum().item()),
                             "outer": int(out["c_out"].sum().item())},
@@ -525,6 +530,9 @@ def main():
     ap.add_argument("--no-kernel-timing", action="store_true", help="skip the per-kernel device timing (no roofline)")
     ap.add_argument("--n", type=int, default=0, help="profiling only: smaller n of the same workload family")
     ap.add_argument("--peaks", action="store_true", help="print the arithmetic units' measured peaks and exit")
+    ap.add_argument("--fp64-gemm", default="ozaki", choices=["df", "ozaki"],
+                    help="kriging workload: the correction's FP64 product in double-float on the FP32 units, or by "
+                         "the Ozaki scheme on the FP16 tensor cores")
     ap.add_argument("--workload", default="headline", choices=["headline", "krige"],
                     help="headline: the Cholesky+TRMM step of the n = 32768 workload (default); krige: conditional "
                          "simulations per second on the kriging workload")

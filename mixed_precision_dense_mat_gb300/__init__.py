@@ -38,8 +38,9 @@ HEADER = os.path.join(os.path.dirname(_PKG), "include", "cr.h")
 CR_PREC_FP64, CR_PREC_FP32, CR_PREC_FP16 = 0, 1, 2
 CR_COV_MATERN, CR_COV_POWEXP = 0, 1
 CR_TRMM_FP16_DEST, CR_TRMM_GENERATE, CR_TRMM_SPLIT_L, CR_TRMM_FP16_PER_GEMM = 1, 2, 4, 8
-CR_OPT_WAIT_LIMIT_US, CR_OPT_DIAG_ARITH = 1, 2
+CR_OPT_WAIT_LIMIT_US, CR_OPT_DIAG_ARITH, CR_OPT_FP64_GEMM = 1, 2, 4
 CR_DIAG_AUTO, CR_DIAG_FP64, CR_DIAG_DF = 0, 1, 2
+CR_GEMM_DF, CR_GEMM_OZAKI = 0, 1
 CR_PEAK_DFMA, CR_PEAK_FFMA, CR_PEAK_DF_MAC, CR_PEAK_DMMA = 1, 2, 3, 4
 STATUS = {0: "CR_OK", 1: "CR_ERR_ARG", 2: "CR_ERR_CUDA", 3: "CR_ERR_NOMEM", 4: "CR_ERR_NOT_SPD",
           5: "CR_ERR_EMPTY_SAMPLE", 6: "CR_ERR_NONPOS_MSPE", 7: "CR_ERR_TIMEOUT", 8: "CR_ERR_STATE",
@@ -179,7 +180,8 @@ def kernel_launches() -> int:
 
 
 def set_option(option: int, value: int) -> None:
-    """cr_set_option: CR_OPT_WAIT_LIMIT_US (microseconds) or CR_OPT_DIAG_ARITH (CR_DIAG_*)."""
+    """cr_set_option: CR_OPT_WAIT_LIMIT_US (microseconds), CR_OPT_DIAG_ARITH (CR_DIAG_*) or
+    CR_OPT_FP64_GEMM (CR_GEMM_*)."""
     load()
     _check(_lib.cr_set_option(option, int(value)))
 

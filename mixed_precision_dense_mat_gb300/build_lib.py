@@ -12,7 +12,8 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libcr.so")
-SOURCES = ["api.cu", "cov.cu", "policy.cu", "fp64.cu", "diag.cu", "tc.cu", "chol.cu", "sim.cu", "calib.cu", "krige.cu", "peaks.cu"]
+SOURCES = ["api.cu", "cov.cu", "policy.cu", "fp64.cu", "diag.cu", "tc.cu", "chol.cu", "sim.cu", "calib.cu", "krige.cu", "peaks.cu",
+           "ozaki.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=default",
          "--expt-relaxed-constexpr", "-Xptxas", "-v"]
@@ -41,7 +42,10 @@ def build(verbose: bool = False) -> str:
     if verbose:
         for src, log in logs:
             sys.stderr.write(f"--- {src}\n{log}")
-    cmd = [nvcc(), *ARCH, "-shared", "-o", LIB, *objs, "-lcudart_static", "-lrt", "-ldl", "-lpthread"]
+    # cuBLAS (the Ozaki product's FP16 slice GEMMs) from the toolkit next to nvcc
+    libdir = os.path.realpath(os.path.join(os.path.dirname(nvcc()), "..", "lib64"))
+    cmd = [nvcc(), *ARCH, "-shared", "-o", LIB, *objs, "-lcudart_static", "-L" + libdir, "-lcublas",
+           "-Xlinker", "-rpath=" + libdir, "-lrt", "-ldl", "-lpthread"]
     p = subprocess.run(cmd, capture_output=True, text=True)
     if p.returncode != 0:
         raise RuntimeError(f"link failed:\n{p.stdout}\n{p.stderr}")

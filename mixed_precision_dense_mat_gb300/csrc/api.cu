@@ -22,8 +22,10 @@ void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 static std::atomic<long long> g_opt_wait_us{2000000};
 static std::atomic<int> g_opt_diag{CR_DIAG_AUTO};
+static std::atomic<int> g_opt_gemm{CR_GEMM_DF};
 unsigned long long option_wait_ns() { return 1000ull * (unsigned long long)g_opt_wait_us.load(std::memory_order_relaxed); }
 int option_diag_arith() { return g_opt_diag.load(std::memory_order_relaxed); }
+int option_fp64_gemm() { return g_opt_gemm.load(std::memory_order_relaxed); }
 
 namespace {
 struct TimingState {
@@ -240,6 +242,12 @@ extern "C" cr_status cr_set_option(int option, long long value) {
     g_opt_diag.store((int)value);
     return CR_OK;
   }
+  if (option == CR_OPT_FP64_GEMM) {
+    if (value != CR_GEMM_DF && value != CR_GEMM_OZAKI)
+      return fail(CR_ERR_ARG, "cr_set_option: FP64 product arithmetic must be CR_GEMM_DF or CR_GEMM_OZAKI");
+    g_opt_gemm.store((int)value);
+    return CR_OK;
+  }
   return fail(CR_ERR_ARG, "cr_set_option: unknown option");
 }
 
@@ -247,6 +255,7 @@ extern "C" cr_status cr_get_option(int option, long long* value) {
   if (!value) return fail(CR_ERR_ARG, "cr_get_option: NULL value");
   if (option == CR_OPT_WAIT_LIMIT_US) *value = g_opt_wait_us.load();
   else if (option == CR_OPT_DIAG_ARITH) *value = g_opt_diag.load();
+  else if (option == CR_OPT_FP64_GEMM) *value = g_opt_gemm.load();
   else return fail(CR_ERR_ARG, "cr_get_option: unknown option");
   return CR_OK;
 }

@@ -622,6 +622,21 @@ extern "C" cr_status cr_correct_calibrate(const double* d_W, int ldw, const doub
   if (!d_W || !d_yo || !d_Y || !d_zhat || !d_v || !d_cin || !d_cout || n_p <= 0 || n_o <= 0 || M <= 0 || ldw < n_o ||
       ldy < n_p + n_o || !(level > 0.0 && level < 1.0))
     return fail(CR_ERR_ARG, "cr_correct_calibrate: argument");
+  if (option_fp64_gemm() == CR_GEMM_OZAKI) {
+    // the Ozaki product writes S (stream-ordered scratch), then the calibration scan reads it
+    double* S = nullptr;
+    CR_CUDA(cudaMallocAsync(&S, (size_t)n_p * M * sizeof(double), stream));
+    cr_status st = ozaki_correction(d_W, ldw, d_yo, d_Y, ldy, n_p, n_o, M, S, n_p, stream);
+    if (st == CR_OK) {
+      std::lock_guard<std::mutex> lk(g_mu);
+      st = ensure_scratch(n_p, M);
+      if (st == CR_OK)
+        st = calibrate_core(S, n_p, n_p, M, d_zhat, d_v, u, level, d_cin, d_cout, d_count, d_psi, d_phi, out, stream, g_sc,
+                            negative ? 1 : 0);
+    }
+    cudaFreeAsync(S, stream);
+    return st;
+  }
   std::lock_guard<std::mutex> lk(g_cc_mu);
   const size_t nrb = ((size_t)n_p + CT - 1) / CT;
   CR_TRY(grow(&g_cc.W, &g_cc.capW, (size_t)n_o * n_p));

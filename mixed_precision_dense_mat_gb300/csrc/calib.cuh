@@ -33,4 +33,9 @@ cr_status calibrate_finish(const double* psi_part, const double* phi_part, int n
 cr_status correction_async(const double* d_W, int ldw, const double* d_yo, const double* d_Y, int ldy, int n_p, int n_o,
                            int M, double* d_S, int lds, cudaStream_t stream);
 
+// The conditioning correction S = M_p + W^T (y_o 1^T - M_o) by the Ozaki product on the FP16
+// tensor cores (ozaki.cu); stream-ordered scratch, asynchronous.
+cr_status ozaki_correction(const double* d_W, int ldw, const double* d_yo, const double* d_Y, int ldy, int n_p, int n_o,
+                           int M, double* d_S, int lds, cudaStream_t stream);
+
 }  // namespace cr

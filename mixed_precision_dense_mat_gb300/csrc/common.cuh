@@ -30,6 +30,7 @@ void count_launch();
 // factorisation, and the arithmetic of the diagonal-tile executor (CR_DIAG_*).
 unsigned long long option_wait_ns();
 int option_diag_arith();
+int option_fp64_gemm();
 
 // Opt-in device timing of named kernels (cr_timing_enable): a scope object records an event
 // on the launch stream before and after the launch it brackets.

@@ -267,5 +267,6 @@ extern "C" cr_status cr_krige_correct(const double* d_W, int ldw, const double* 
                                       int n_o, int M, double* d_S, int lds, cr_stream stream) {
   if (!d_W || !d_yo || !d_Y || !d_S || n_p <= 0 || n_o <= 0 || M <= 0 || ldw < n_o || ldy < n_p + n_o || lds < n_p)
     return fail(CR_ERR_ARG, "cr_krige_correct: argument");
+  if (option_fp64_gemm() == CR_GEMM_OZAKI) return ozaki_correction(d_W, ldw, d_yo, d_Y, ldy, n_p, n_o, M, d_S, lds, stream);
   return correction_async(d_W, ldw, d_yo, d_Y, ldy, n_p, n_o, M, d_S, lds, stream);
 }

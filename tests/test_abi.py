@@ -63,7 +63,8 @@ def test_binding_constants_match_the_header():
     declared = {m.group(1): int(m.group(2)) for m in re.finditer(r"\b(CR_[A-Z0-9_]+)\s*=\s*(\d+)", text)}
     for name in ("CR_PREC_FP64", "CR_PREC_FP32", "CR_PREC_FP16", "CR_COV_MATERN", "CR_COV_POWEXP",
                  "CR_TRMM_FP16_DEST", "CR_TRMM_GENERATE", "CR_TRMM_SPLIT_L", "CR_TRMM_FP16_PER_GEMM",
-                 "CR_OPT_WAIT_LIMIT_US", "CR_OPT_DIAG_ARITH", "CR_DIAG_AUTO", "CR_DIAG_FP64", "CR_DIAG_DF",
+                 "CR_OPT_WAIT_LIMIT_US", "CR_OPT_DIAG_ARITH", "CR_OPT_FP64_GEMM", "CR_DIAG_AUTO", "CR_DIAG_FP64",
+                 "CR_DIAG_DF", "CR_GEMM_DF", "CR_GEMM_OZAKI",
                  "CR_PEAK_DFMA", "CR_PEAK_FFMA", "CR_PEAK_DF_MAC", "CR_PEAK_DMMA"):
         assert name in declared, name
         assert getattr(cr, name) == declared[name], name
@@ -110,6 +111,11 @@ def test_options_host_side(lib):
     assert cr._lib.cr_set_option(cr.CR_OPT_WAIT_LIMIT_US, -1) == 1
     assert cr._lib.cr_set_option(cr.CR_OPT_WAIT_LIMIT_US, 2000000) == 0
     assert cr._lib.cr_set_option(cr.CR_OPT_DIAG_ARITH, 7) == 1
+    assert cr._lib.cr_get_option(cr.CR_OPT_FP64_GEMM, ctypes.byref(v)) == 0 and v.value == cr.CR_GEMM_DF
+    assert cr._lib.cr_set_option(cr.CR_OPT_FP64_GEMM, 2) == 1
+    assert cr._lib.cr_set_option(cr.CR_OPT_FP64_GEMM, cr.CR_GEMM_OZAKI) == 0
+    assert cr._lib.cr_get_option(cr.CR_OPT_FP64_GEMM, ctypes.byref(v)) == 0 and v.value == cr.CR_GEMM_OZAKI
+    assert cr._lib.cr_set_option(cr.CR_OPT_FP64_GEMM, cr.CR_GEMM_DF) == 0
     assert cr._lib.cr_set_option(99, 0) == 1 and cr._lib.cr_get_option(99, ctypes.byref(v)) == 1
     assert cr._lib.cr_get_option(cr.CR_OPT_DIAG_ARITH, None) == 1
     d = ctypes.c_double()

@@ -1,0 +1,125 @@
+"""The conditioning correction (Eq.7 of "Mixed-Precision GPU Acceleration for Confidence Regions
+of Spatial Excursion Sets", Section V-B) with its FP64 product emulated on the FP16 tensor cores
+by the Ozaki scheme (CR_OPT_FP64_GEMM = CR_GEMM_OZAKI), against the oracle's FP64.
+
+Error bound of the emulated product C = W^T R, entry (i, j), with Ea_i the exponent of column i
+of W (max_k |W_ki| < 2^Ea_i) and Eb_j that of column j of R:
+  - slicing: each entry is cut into 7 slices of 7 bits below 2^Ea (truncation), so
+    W_ki = sum_s a_s 2^(Ea - 7 s) + d with |d| < 2^(Ea - 49), |a_s| <= 127 (same for R);
+  - per term k, the truncations and the dropped slice products (s + t >= 9) are below
+    (1 + 1 + 2^-49 + 6 (127/128)^2) 2^(Ea + Eb - 49) < 8.01 2^(Ea + Eb - 49);
+  - the kept products are exact integers (FP16 x FP16 summed over at most 1024 terms, below
+    2^24, in FP32); their 28 power-of-two-scaled sums are added in double-float pairs: at most
+    28 2^-47 (|W|^T |R|)_ij;
+  - S = M_p + C rounds once in FP64, and the oracle's own FP64 product errs by up to
+    n_o 2^-53 (|W|^T |R|)_ij.
+So |S - S_oracle| <= n_o 8.02 2^-49 2^(Ea_i + Eb_j) + (28 2^-47 + n_o 2^-53) (|W|^T |R|)_ij
++ 2^-52 |S_ij|."""
+import contextlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def colmajor(a):
+    return torch.from_numpy(np.asfortranarray(a).T.copy()).cuda().T
+
+
+@contextlib.contextmanager
+def gemm_mode(lib, mode):
+    old = lib.get_option(lib.CR_OPT_FP64_GEMM)
+    lib.set_option(lib.CR_OPT_FP64_GEMM, mode)
+    try:
+        yield
+    finally:
+        lib.set_option(lib.CR_OPT_FP64_GEMM, old)
+
+
+def _exp_above(X):
+    """E per column with max |X| < 2^E (0 for a zero column)."""
+    m = np.max(np.abs(X), axis=0)
+    e = np.zeros(X.shape[1], dtype=np.int64)
+    nz = m > 0
+    e[nz] = np.floor(np.log2(m[nz])).astype(np.int64) + 1
+    return e
+
+
+def _bound(W, R, S, n_o):
+    Ea, Eb = _exp_above(W), _exp_above(R)
+    WR = np.abs(W).T @ np.abs(R)
+    return (n_o * 8.02 * 2.0 ** -49 * np.exp2((Ea[:, None] + Eb[None, :]).astype(float))
+            + (28 * 2.0 ** -47 + n_o * 2.0 ** -53) * WR + 2.0 ** -52 * np.abs(S))
+
+
+@pytest.mark.parametrize("n_p,n_o,M,scale", [(300, 200, 70, 1.0), (129, 1000, 65, 1.0), (257, 2100, 130, 1e-3)])
+def test_ozaki_correction_matches_oracle(lib, n_p, n_o, M, scale):
+    """Element by element within the bound above, on ragged sizes (n_o not a multiple of the
+    1024-row chunks: the padding slices are zero) and with columns of W spanning several orders
+    of magnitude (as kriging weights do)."""
+    rng = np.random.default_rng(n_p + n_o)
+    W = rng.standard_normal((n_o, n_p)) * scale * np.exp(rng.uniform(-8, 2, n_p))[None, :]
+    W[rng.random((n_o, n_p)) < 0.2] *= 1e-6
+    y = rng.standard_normal(n_o)
+    Y = rng.standard_normal((n_p + n_o, M))
+    with gemm_mode(lib, lib.CR_GEMM_OZAKI):
+        S = lib.krige_correct(colmajor(W), dev(y), colmajor(Y), n_p, n_o).cpu().numpy()
+    So = oracle.conditional_correction(W, y, Y[:n_p], Y[n_p:])
+    R = y[:, None] - Y[n_p:]
+    b = _bound(W, R, So, n_o)
+    err = np.abs(S - So)
+    assert np.all(err <= b), float(np.max(err / b))
+    assert np.linalg.norm(err) <= np.linalg.norm(b)
+
+
+def test_ozaki_slices_exact_on_integers(lib):
+    """Entries that are small integers times powers of two are represented exactly by their
+    slices and every slice product is exact, so the product equals the exact integer result."""
+    rng = np.random.default_rng(5)
+    n_p, n_o, M = 200, 3000, 40
+    W = rng.integers(-1000, 1000, (n_o, n_p)).astype(np.float64) * 2.0 ** -20
+    y = rng.integers(-50, 50, n_o).astype(np.float64)
+    Y = np.zeros((n_p + n_o, M))
+    Y[n_p:] = rng.integers(-50, 50, (n_o, M)).astype(np.float64)
+    with gemm_mode(lib, lib.CR_GEMM_OZAKI):
+        S = lib.krige_correct(colmajor(W), dev(y), colmajor(Y), n_p, n_o).cpu().numpy()
+    Wi = (W * 2.0 ** 20).astype(np.int64)
+    Ri = (y[:, None] - Y[n_p:]).astype(np.int64)
+    exact = (Wi.T @ Ri).astype(np.float64) * 2.0 ** -20
+    np.testing.assert_array_equal(S, exact)
+
+
+@pytest.mark.parametrize("negative", [False, True])
+def test_ozaki_correct_calibrate_matches_unfused(lib, negative):
+    """cr_correct_calibrate with the Ozaki product against cr_krige_correct (Ozaki) followed by
+    cr_calibrate: bit-exact (the same S), and the oracle's calibration of that S."""
+    rng = np.random.default_rng(41)
+    n_p, n_o, M, u, level = 1000, 1500, 300, 0.4, 0.9
+    W = rng.standard_normal((n_o, n_p)) * 0.05
+    y = rng.standard_normal(n_o)
+    Y = rng.standard_normal((n_p + n_o, M))
+    z = rng.standard_normal(n_p) * 0.5
+    v = rng.uniform(0.3, 2.0, n_p)
+    Wd, yd, Yd, zd, vd = colmajor(W), dev(y), colmajor(Y), dev(z), dev(v)
+    with gemm_mode(lib, lib.CR_GEMM_OZAKI):
+        S = lib.krige_correct(Wd, yd, Yd, n_p, n_o)
+        a = lib.calibrate(S, zd, vd, u, level, counts=True, extrema=True, negative=negative)
+        b = lib.correct_calibrate(Wd, yd, Yd, n_p, n_o, zd, vd, u, level, counts=True, extrema=True,
+                                  negative=negative)
+    for k in ("psi", "phi", "count", "c_in", "c_out"):
+        np.testing.assert_array_equal(a[k].cpu().numpy(), b[k].cpu().numpy(), err_msg=k)
+    for k in ("q_in", "q_out", "n_psi", "n_phi"):
+        assert a[k] == b[k], k
+    Sg = S.cpu().numpy()
+    ref = (oracle.calibrate_negative if negative else oracle.calibrate)(Sg, z, v, u, level)
+    assert b["q_in"] == ref["q_in"] and b["q_out"] == ref["q_out"]
+    np.testing.assert_array_equal(b["c_in"].cpu().numpy(), ref["c_in"])
+    np.testing.assert_array_equal(b["c_out"].cpu().numpy(), ref["c_out"])
