@@ -99,6 +99,17 @@ cr_status cr_version(int* major, int* minor);
  * *count receives the running total.  Host-side counter, no device work. */
 cr_status cr_kernel_launches(uint64_t* count);
 
+/* Hands back to the driver the device memory that the library keeps in its stream-ordered
+ * scratch pools (one per device).  The conditioning correction takes its scratch from these
+ * pools and frees it at the end of each call; the pools keep the freed memory for the next
+ * call rather than return it at every synchronisation.  The largest user is the Ozaki
+ * product (CR_GEMM_OZAKI): 16 n_o' (n_p + M) bytes of slices (n_o' = n_o rounded up to
+ * 1024), up to 128 n_p M bytes of chunk products (at most 2 GiB), 8 n_o M + 8 n_p M more,
+ * and S (8 n_p M) in cr_correct_calibrate; cr_krige_correct with CR_GEMM_DF takes
+ * 8 n_o (n_p + M) bytes.  Memory still used by work in flight stays in the pool.  No device
+ * work; does not synchronise. */
+cr_status cr_workspace_trim(void);
+
 /* Device timing of the library's main kernels, for measurement (the paper has no counterpart).
  * While enabled, every launch of a timed kernel is bracketed by two CUDA events recorded on
  * the stream the kernel is launched on, and the durations are accumulated per kernel name:
@@ -133,10 +144,11 @@ cr_status cr_timing_reset(void);
  *                        (cr_krige_correct, cr_correct_calibrate): CR_GEMM_DF (default)
  *                        double-float on the FP32 units; CR_GEMM_OZAKI the Ozaki scheme on the
  *                        FP16 tensor cores (Ozaki, Ogita, Oishi, Rump, Numer. Algorithms 59,
- *                        2012): each operand column cut into 7 slices of 7 bits below a power of
- *                        two, the 28 leading slice products computed exactly (FP16 inputs,
- *                        FP32 accumulation over chunks of 1024) and summed in double-float.
- *                        With it cr_correct_calibrate writes S to stream-ordered scratch.
+ *                        2012): each operand column cut into 8 slices of 6 bits below a power of
+ *                        two, the 36 leading slice products computed exactly (FP16 inputs,
+ *                        FP32 accumulation over chunks of at most 4096 rows), one GEMM per
+ *                        level of significance, and summed in double-float.  With it
+ *                        cr_correct_calibrate writes S to stream-ordered scratch.
  * cr_set_option returns CR_ERR_ARG for an unknown option or a value out of range. */
 enum { CR_OPT_WAIT_LIMIT_US = 1, CR_OPT_DIAG_ARITH = 2, CR_OPT_FP64_GEMM = 4 };
 enum { CR_DIAG_AUTO = 0, CR_DIAG_FP64 = 1, CR_DIAG_DF = 2 };

@@ -85,6 +85,7 @@ _SIGNATURES = {
     "cr_last_error_detail": (ctypes.c_char_p, []),
     "cr_version": (_I, [ctypes.POINTER(_I), ctypes.POINTER(_I)]),
     "cr_kernel_launches": (_I, [ctypes.POINTER(_U64)]),
+    "cr_workspace_trim": (_I, []),
     "cr_set_option": (_I, [_I, ctypes.c_longlong]),
     "cr_peak_probe": (_I, [_I, _I, ctypes.POINTER(_D), _P]),
     "cr_get_option": (_I, [_I, ctypes.POINTER(ctypes.c_longlong)]),
@@ -177,6 +178,12 @@ def kernel_launches() -> int:
     c = _U64(0)
     _check(_lib.cr_kernel_launches(ctypes.byref(c)))
     return c.value
+
+
+def workspace_trim() -> None:
+    """cr_workspace_trim: return the library's pooled scratch memory to the driver."""
+    load()
+    _check(_lib.cr_workspace_trim())
 
 
 def set_option(option: int, value: int) -> None:

@@ -260,6 +260,49 @@ extern "C" cr_status cr_get_option(int option, long long* value) {
   return CR_OK;
 }
 
+namespace cr {
+namespace {
+std::mutex g_pool_mu;
+cudaMemPool_t g_pool[64] = {};
+}  // namespace
+
+cudaError_t scratch_alloc(void** p, size_t bytes, cudaStream_t stream) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  cudaMemPool_t pool = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_pool_mu);
+    if (!g_pool[dev]) {
+      cudaMemPoolProps props = {};
+      props.allocType = cudaMemAllocationTypePinned;
+      props.location.type = cudaMemLocationTypeDevice;
+      props.location.id = dev;
+      if ((e = cudaMemPoolCreate(&g_pool[dev], &props)) != cudaSuccess) {
+        g_pool[dev] = nullptr;
+        return e;
+      }
+      uint64_t keep = ~0ull;
+      if ((e = cudaMemPoolSetAttribute(g_pool[dev], cudaMemPoolAttrReleaseThreshold, &keep)) != cudaSuccess) return e;
+    }
+    pool = g_pool[dev];
+  }
+  return cudaMallocFromPoolAsync(p, bytes, pool, stream);
+}
+
+void scratch_free(void* p, cudaStream_t stream) {
+  if (p) cudaFreeAsync(p, stream);
+}
+}  // namespace cr
+
+extern "C" cr_status cr_workspace_trim(void) {
+  std::lock_guard<std::mutex> lk(g_pool_mu);
+  for (cudaMemPool_t pool : g_pool)
+    if (pool) CR_CUDA(cudaMemPoolTrimTo(pool, 0));
+  return CR_OK;
+}
+
 extern "C" cr_status cr_kernel_launches(uint64_t* count) {
   if (!count) return fail(CR_ERR_ARG, "cr_kernel_launches: NULL");
   *count = g_launches.load(std::memory_order_relaxed);

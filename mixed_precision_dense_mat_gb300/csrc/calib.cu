@@ -604,12 +604,15 @@ cr_status grow(T** p, size_t* cap, size_t need) {
 cr_status correction_async(const double* d_W, int ldw, const double* d_yo, const double* d_Y, int ldy, int n_p, int n_o,
                            int M, double* d_S, int lds, cudaStream_t stream) {
   float2 *Wd = nullptr, *Rd = nullptr;
-  CR_CUDA(cudaMallocAsync(&Wd, (size_t)n_o * n_p * sizeof(float2), stream));
-  CR_CUDA(cudaMallocAsync(&Rd, (size_t)n_o * M * sizeof(float2), stream));
+  CR_CUDA(scratch_alloc((void**)&Wd, (size_t)n_o * n_p * sizeof(float2), stream));
+  if (cudaError_t e = scratch_alloc((void**)&Rd, (size_t)n_o * M * sizeof(float2), stream)) {
+    scratch_free(Wd, stream);
+    return cuda_fail(e, "scratch_alloc");
+  }
   const cr_status st = correction_launch(d_W, ldw, d_yo, d_Y, ldy, n_p, n_o, M, Wd, Rd, false, d_S, lds, nullptr, 0.0, 0,
                                          nullptr, nullptr, nullptr, stream);
-  cudaFreeAsync(Wd, stream);
-  cudaFreeAsync(Rd, stream);
+  scratch_free(Wd, stream);
+  scratch_free(Rd, stream);
   return st;
 }
 
@@ -623,9 +626,9 @@ extern "C" cr_status cr_correct_calibrate(const double* d_W, int ldw, const doub
       ldy < n_p + n_o || !(level > 0.0 && level < 1.0))
     return fail(CR_ERR_ARG, "cr_correct_calibrate: argument");
   if (option_fp64_gemm() == CR_GEMM_OZAKI) {
-    // the Ozaki product writes S (stream-ordered scratch), then the calibration scan reads it
+    // the Ozaki product writes S (scratch from the library pool), then the calibration scan reads it
     double* S = nullptr;
-    CR_CUDA(cudaMallocAsync(&S, (size_t)n_p * M * sizeof(double), stream));
+    CR_CUDA(scratch_alloc((void**)&S, (size_t)n_p * M * sizeof(double), stream));
     cr_status st = ozaki_correction(d_W, ldw, d_yo, d_Y, ldy, n_p, n_o, M, S, n_p, stream);
     if (st == CR_OK) {
       std::lock_guard<std::mutex> lk(g_mu);
@@ -634,7 +637,7 @@ extern "C" cr_status cr_correct_calibrate(const double* d_W, int ldw, const doub
         st = calibrate_core(S, n_p, n_p, M, d_zhat, d_v, u, level, d_cin, d_cout, d_count, d_psi, d_phi, out, stream, g_sc,
                             negative ? 1 : 0);
     }
-    cudaFreeAsync(S, stream);
+    scratch_free(S, stream);
     return st;
   }
   std::lock_guard<std::mutex> lk(g_cc_mu);

@@ -26,6 +26,12 @@ cr_status cuda_fail(cudaError_t e, const char* what);
 
 void count_launch();
 
+// Stream-ordered scratch from the library's memory pool of the current device, which keeps
+// freed memory for the next call (unlimited release threshold) instead of returning it to
+// the driver at every synchronisation; cr_workspace_trim returns it.
+cudaError_t scratch_alloc(void** p, size_t bytes, cudaStream_t stream);
+void scratch_free(void* p, cudaStream_t stream);
+
 // Process-wide options (cr_set_option): the limit of every bounded device-side wait of the
 // factorisation, and the arithmetic of the diagonal-tile executor (CR_DIAG_*).
 unsigned long long option_wait_ns();

@@ -6,16 +6,21 @@
 //
 // C = A^T B with A (k x m) and B (k x n) column-major FP64:
 //  - each column c of A gets a power of two 2^Ea_c above its largest |entry| (B likewise), and
-//    |A_rc| 2^(7 S - Ea_c), truncated to an integer below 2^(7 S), is cut into S = 7 slices of
-//    7 bits: A_rc = sum_s a_s,rc 2^(Ea_c - 7 s) + d with |a_s,rc| <= 127 and
-//    |d| < 2^(Ea_c - 49);
-//  - a slice product A_s^T B_t over K <= 1024 rows is a sum of at most 1024 integers of
-//    magnitude <= 127^2 < 2^14, an integer below 2^24, so an FP16 tensor-core GEMM with FP32
-//    accumulation computes it exactly (whatever its summation order);
-//  - the products with s + t <= S + 1 (28 of the 49) are kept: the rest, and the truncations,
-//    are below (k (2 + 8 2^-7) 2^-49) 2^(Ea_i + Eb_j) per output (derived in the tests);
-//  - each kept product, summed over the K chunks in 64-bit integers (exact), is scaled by
-//    2^(Ea_i + Eb_j - 7 (s + t)) (exact) and added to a double-float accumulator.
+//    |A_rc| 2^(6 S - Ea_c), truncated to an integer below 2^(6 S), is cut into S = 8 slices of
+//    6 bits: A_rc = sum_s a_s,rc 2^(Ea_c - 6 s) + d with |a_s,rc| <= 63 and
+//    |d| < 2^(Ea_c - 48);
+//  - the slice products with s + t = L share the scale 2^(Ea_i + Eb_j - 6 L), so for each
+//    level L = 2 .. S + 1 the L - 1 products are one product over the concatenated rows
+//    [A_1; ...; A_(L-1)]^T [B_(L-1); ...; B_1] (the slices of A stored in order, those of B in
+//    reverse, so that both ranges are contiguous);
+//  - that product over a chunk of at most 4096 rows is a sum of at most 4096 integers of
+//    magnitude <= 63^2, below 2^24, so an FP16 tensor-core GEMM with FP32 accumulation computes
+//    it exactly (whatever its summation order);
+//  - the products with s + t <= S + 1 (36 of the 64) are kept: the rest, and the truncations,
+//    are below k 8.95 2^-48 2^(Ea_i + Eb_j) per output (derived in the tests);
+//  - each level's chunk sums, added in 32-bit integers (exact), are scaled by
+//    2^(Ea_i + Eb_j - 6 L) (exact) and added to a double-float accumulator, the least
+//    significant level first; the last addition writes S = M_p + C in FP64.
 // The slice GEMMs are plain FP16 x FP16 -> FP32 library GEMMs (cuBLAS, strided-batched over the
 // K chunks); slicing, exact accumulation and the final sum are this file's kernels.
 #include <cublas_v2.h>
@@ -32,7 +37,9 @@ namespace cr {
 
 namespace {
 
-constexpr int OZ_BITS = 7, OZ_SLICES = 7, OZ_KC = 1024;
+// slice width and count; chunk rows with 4096 * 63^2 < 2^24; chunks per GEMM call at most
+constexpr int OZ_BITS = 6, OZ_SLICES = 8, OZ_KC_MAX = 4096, OZ_GROUP = 32;
+constexpr unsigned long long OZ_MASK = (1ull << OZ_BITS) - 1ull;
 
 // E_c with max_r |X_rc| < 2^E_c (positive doubles order as their bit patterns); 0 for a zero
 // column (its slices are all zero).  One CTA per column.
@@ -58,31 +65,35 @@ __global__ void __launch_bounds__(256) k_oz_colexp(const double* __restrict__ X,
   }
 }
 
-// Slices of X (rows x cols, column-major, ld): out + s * rows_pad * cols holds slice s + 1
-// (the most significant first) as a rows_pad x cols column-major FP16 matrix of integers in
-// [-127, 127], rows beyond `rows` zero.  Integer arithmetic on the FP64 bit pattern only.
+// Slices of X (rows x cols, column-major, ld): column c of out holds, at
+// out + c * S * rows_pad + slot * rows_pad, slice s + 1 (s = 0 the most significant) in slot s,
+// or in slot S - 1 - s when `reversed`, as rows_pad FP16 integers in [-63, 63], rows beyond
+// `rows` zero.  Integer arithmetic on the FP64 bit pattern only.
 __global__ void __launch_bounds__(256) k_oz_slice(const double* __restrict__ X, int ld, int rows, int rows_pad, int cols,
-                                                  const int* __restrict__ E, __half* __restrict__ out) {
-  const size_t total = (size_t)rows_pad * cols, plane = total;
-  for (size_t e = blockIdx.x * (size_t)256 + threadIdx.x; e < total; e += (size_t)gridDim.x * 256) {
-    const int r = (int)(e % rows_pad), c = (int)(e / rows_pad);
-    unsigned long long q = 0ull;
-    bool neg = false;
-    if (r < rows) {
-      const unsigned long long b = (unsigned long long)__double_as_longlong(X[(size_t)c * ld + r]);
-      neg = (b >> 63) != 0;
-      const int eb = (int)((b >> 52) & 0x7ff);
-      const unsigned long long mant = (b & 0x000fffffffffffffull) | (eb ? 0x0010000000000000ull : 0ull);
-      // |x| = mant 2^(e2);  q = floor(|x| 2^(7 S - E_c)) < 2^(7 S)
-      const int e2 = (eb ? eb : 1) - 1075;
-      const int shift = e2 + OZ_BITS * OZ_SLICES - E[c];
-      if (shift >= 0) q = shift < 64 ? mant << shift : 0ull;
-      else q = -shift < 64 ? mant >> (-shift) : 0ull;
-    }
+                                                  const int* __restrict__ E, int reversed, __half* __restrict__ out) {
+  for (int c = blockIdx.y; c < cols; c += gridDim.y) {
+    const int Ec = E[c];
+    __half* oc = out + (size_t)c * OZ_SLICES * rows_pad;
+    for (int r = blockIdx.x * 256 + threadIdx.x; r < rows_pad; r += gridDim.x * 256) {
+      unsigned long long q = 0ull;
+      bool neg = false;
+      if (r < rows) {
+        const unsigned long long b = (unsigned long long)__double_as_longlong(X[(size_t)c * ld + r]);
+        neg = (b >> 63) != 0;
+        const int eb = (int)((b >> 52) & 0x7ff);
+        const unsigned long long mant = (b & 0x000fffffffffffffull) | (eb ? 0x0010000000000000ull : 0ull);
+        // |x| = mant 2^(e2);  q = floor(|x| 2^(6 S - E_c)) < 2^(6 S)
+        const int e2 = (eb ? eb : 1) - 1075;
+        const int shift = e2 + OZ_BITS * OZ_SLICES - Ec;
+        if (shift >= 0) q = shift < 64 ? mant << shift : 0ull;
+        else q = -shift < 64 ? mant >> (-shift) : 0ull;
+      }
 #pragma unroll
-    for (int s = 0; s < OZ_SLICES; ++s) {
-      const int a = (int)((q >> (OZ_BITS * (OZ_SLICES - 1 - s))) & 127ull);
-      out[(size_t)s * plane + e] = __int2half_rn(neg ? -a : a);
+      for (int s = 0; s < OZ_SLICES; ++s) {
+        const int a = (int)((q >> (OZ_BITS * (OZ_SLICES - 1 - s))) & OZ_MASK);
+        const int slot = reversed ? OZ_SLICES - 1 - s : s;
+        oc[(size_t)slot * rows_pad + r] = __int2half_rn(neg ? -a : a);
+      }
     }
   }
 }
@@ -97,39 +108,40 @@ __global__ void __launch_bounds__(256) k_oz_resid(const double* __restrict__ yo,
   }
 }
 
-// C += 2^(Ea_i + Eb_j - 7 lev) sum_b P_b(i, j) for one slice pair (C = that term when first):
-// the chunk products are exact integers below 2^24, their sum (below 2^28) is exact in 64-bit
-// integers and as a double-float pair, and the power-of-two scaling is exact.
-__global__ void __launch_bounds__(256) k_oz_accum(const float* __restrict__ P, int nchunk, int m, int n,
-                                                  const int* __restrict__ Ea, const int* __restrict__ Eb, int lev,
-                                                  float2* __restrict__ C, int first) {
-  const size_t total = (size_t)m * n;
-  for (size_t e = blockIdx.x * (size_t)256 + threadIdx.x; e < total; e += (size_t)gridDim.x * 256) {
-    long long v = 0;
-    for (int b = 0; b < nchunk; ++b) v += (long long)__float2ll_rn(P[(size_t)b * total + e]);
-    const int i = (int)(e % m), j = (int)(e / m);
-    const int ex = Ea[i] + Eb[j] - OZ_BITS * lev;
-    const float h = (float)v;                          // nearest FP32 of v (|v| < 2^28)
-    const float l = (float)(v - (long long)h);         // the rest, below 2^5: exact
-    const df term = {ldexpf(h, ex), ldexpf(l, ex)};
-    if (first) {
-      C[e] = make_float2(term.hi, term.lo);
-    } else {
-      const float2 c = C[e];
-      const df s = df_add({c.x, c.y}, term);
-      C[e] = make_float2(s.hi, s.lo);
-    }
-  }
+// 2^ex as an FP32 factor when it is a normal number (the multiplication is then exact unless
+// the product underflows); outside that range ldexpf.
+__device__ __forceinline__ float oz_scale(float x, int ex) {
+  return (ex >= -126 && ex <= 127) ? x * __int_as_float((ex + 127) << 23) : ldexpf(x, ex);
 }
 
-// S = M_p + C (FP64), C the double-float product.
-__global__ void __launch_bounds__(256) k_oz_final(const float2* __restrict__ C, int m, int n, const double* __restrict__ Y,
-                                                  int ldy, double* __restrict__ S, int lds) {
-  const size_t total = (size_t)m * n;
-  for (size_t e = blockIdx.x * (size_t)256 + threadIdx.x; e < total; e += (size_t)gridDim.x * 256) {
-    const int i = (int)(e % m), j = (int)(e / m);
-    const float2 c = C[e];
-    S[(size_t)j * lds + i] = Y[(size_t)j * ldy + i] + ((double)c.x + (double)c.y);
+// One level's contribution for `nb` chunk products P_b (m x n FP32 exact integers below 2^24):
+// v = sum_b P_b(i, j), exact in 32-bit integers (nb <= 32), split exactly into two floats,
+// scaled by 2^(Ea_i + Eb_j - shift) and added to the double-float C (C = the term when
+// `first`).  With `last`, S = M_p + C in FP64 is written instead of C.
+__global__ void __launch_bounds__(256) k_oz_accum(const float* __restrict__ P, int nb, int m, int n,
+                                                  const int* __restrict__ Ea, const int* __restrict__ Eb, int shift,
+                                                  float2* __restrict__ C, int first, int last,
+                                                  const double* __restrict__ Y, int ldy, double* __restrict__ S, int lds) {
+  const size_t mn = (size_t)m * n;
+  for (int j = blockIdx.y; j < n; j += gridDim.y) {
+    const int ej = Eb[j] - shift;
+    for (int i = blockIdx.x * 256 + threadIdx.x; i < m; i += gridDim.x * 256) {
+      const size_t e = (size_t)j * m + i;
+      const float* p = P + e;
+      int v = 0;
+#pragma unroll 8
+      for (int b = 0; b < nb; ++b) v += __float2int_rn(p[(size_t)b * mn]);
+      const float h = (float)v;                   // nearest FP32 of v (|v| < 2^29)
+      const float l = (float)(v - (int)h);        // the rest, below 2^5: exact
+      const int ex = Ea[i] + ej;
+      df acc = {oz_scale(h, ex), oz_scale(l, ex)};
+      if (!first) {
+        const float2 c = C[e];
+        acc = df_add({c.x, c.y}, acc);
+      }
+      if (last) S[(size_t)j * lds + i] = Y[(size_t)j * ldy + i] + ((double)acc.hi + (double)acc.lo);
+      else C[e] = make_float2(acc.hi, acc.lo);
+    }
   }
 }
 
@@ -148,6 +160,17 @@ cr_status cublas_for(cudaStream_t stream, cublasHandle_t* h) {
   return CR_OK;
 }
 
+// 2-D grid for the column-wise kernels: blocks of 256 rows times columns, about 16 CTAs per SM
+dim3 grid2d(int rows, int cols) {
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int gx = std::max(1, (rows + 255) / 256);
+  const long long want_y = std::max(1LL, (long long)sms * 16 / gx);
+  const int gy = (int)std::min<long long>({(long long)std::max(cols, 1), want_y * 4, 65535LL});
+  return dim3((unsigned)gx, (unsigned)gy);
+}
+
 unsigned grid_for(size_t total) {
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
@@ -159,31 +182,35 @@ unsigned grid_for(size_t total) {
 }  // namespace
 
 // The correction S = M_p + W^T (y_o 1^T - M_o) by the Ozaki product (W: n_o x n_p, ld ldw;
-// Y: (n_p + n_o) x M, ld ldy; S: n_p x M, ld lds).  Stream-ordered scratch: the slices
-// (7 (n_o' n_p + n_o' M) FP16, n_o' = n_o rounded up to 1024), the chunk products
-// (n_o' / 1024 n_p M FP32), R (n_o M FP64) and the accumulator (n_p M double-float pairs).
+// Y: (n_p + n_o) x M, ld ldy; S: n_p x M, ld lds).  Scratch from the library pool: the slices
+// (8 (n_o' n_p + n_o' M) FP16, n_o' = n_o rounded up to 1024), the chunk products (at most
+// 32 n_p M FP32, fewer when that exceeds 2 GiB), R (n_o M FP64) and the accumulator (n_p M
+// double-float pairs).
 cr_status ozaki_correction(const double* d_W, int ldw, const double* d_yo, const double* d_Y, int ldy, int n_p, int n_o,
                            int M, double* d_S, int lds, cudaStream_t stream) {
   std::lock_guard<std::mutex> lk(g_cublas_mu);
   cublasHandle_t h = nullptr;
   CR_TRY(cublas_for(stream, &h));
-  const int kpad = (n_o + OZ_KC - 1) / OZ_KC * OZ_KC, nchunk = kpad / OZ_KC;
-  const size_t m = (size_t)n_p, n = (size_t)M;
+  const int kpad = (n_o + 1023) / 1024 * 1024;
+  // chunk rows: a divisor of kpad, so that no chunk spans two slices
+  const int kc = kpad % OZ_KC_MAX == 0 ? OZ_KC_MAX : (kpad % 2048 == 0 ? 2048 : 1024);
+  const size_t m = (size_t)n_p, n = (size_t)M, ldk = (size_t)OZ_SLICES * kpad;
+  const int group = (int)std::max<size_t>(1, std::min<size_t>(OZ_GROUP, ((size_t)1 << 31) / (m * n * sizeof(float))));
   double* R = nullptr;
   int *Ea = nullptr, *Eb = nullptr;
   __half *As = nullptr, *Bs = nullptr;
   float* P = nullptr;
   float2* C = nullptr;
-  auto alloc = [&](void** p, size_t bytes) { return cudaMallocAsync(p, bytes, stream); };
+  auto alloc = [&](void** p, size_t bytes) { return scratch_alloc(p, bytes, stream); };
   cudaError_t e = cudaSuccess;
   if ((e = alloc((void**)&R, (size_t)n_o * n * sizeof(double))) != cudaSuccess ||
       (e = alloc((void**)&Ea, m * sizeof(int))) != cudaSuccess || (e = alloc((void**)&Eb, n * sizeof(int))) != cudaSuccess ||
-      (e = alloc((void**)&As, (size_t)OZ_SLICES * kpad * m * sizeof(__half))) != cudaSuccess ||
-      (e = alloc((void**)&Bs, (size_t)OZ_SLICES * kpad * n * sizeof(__half))) != cudaSuccess ||
-      (e = alloc((void**)&P, (size_t)nchunk * m * n * sizeof(float))) != cudaSuccess ||
+      (e = alloc((void**)&As, ldk * m * sizeof(__half))) != cudaSuccess ||
+      (e = alloc((void**)&Bs, ldk * n * sizeof(__half))) != cudaSuccess ||
+      (e = alloc((void**)&P, (size_t)group * m * n * sizeof(float))) != cudaSuccess ||
       (e = alloc((void**)&C, m * n * sizeof(float2))) != cudaSuccess) {
     for (void* p : {(void*)R, (void*)Ea, (void*)Eb, (void*)As, (void*)Bs, (void*)P, (void*)C})
-      if (p) cudaFreeAsync(p, stream);
+      scratch_free(p, stream);
     return fail(CR_ERR_NOMEM, std::string("Ozaki product: scratch: ") + cudaGetErrorName(e));
   }
   cr_status st = CR_OK;
@@ -194,39 +221,43 @@ cr_status ozaki_correction(const double* d_W, int ldw, const double* d_yo, const
     count_launch();
     k_oz_colexp<<<(unsigned)n, 256, 0, stream>>>(R, n_o, n_o, Eb);
     count_launch();
-    k_oz_slice<<<grid_for((size_t)kpad * m), 256, 0, stream>>>(d_W, ldw, n_o, kpad, (int)m, Ea, As);
+    k_oz_slice<<<grid2d(kpad, (int)m), 256, 0, stream>>>(d_W, ldw, n_o, kpad, (int)m, Ea, 0, As);
     count_launch();
-    k_oz_slice<<<grid_for((size_t)kpad * n), 256, 0, stream>>>(R, n_o, n_o, kpad, (int)n, Eb, Bs);
+    k_oz_slice<<<grid2d(kpad, (int)n), 256, 0, stream>>>(R, n_o, n_o, kpad, (int)n, Eb, 1, Bs);
     count_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) { st = fail(CR_ERR_CUDA, cudaGetErrorName(e)); break; }
     const float one = 1.0f, zero = 0.0f;
+    const dim3 ga = grid2d((int)m, (int)n);
     bool first = true;
-    for (int lev = 2; lev <= OZ_SLICES + 1 && st == CR_OK; ++lev) {
-      for (int s = 1; s <= OZ_SLICES; ++s) {
-        const int t = lev - s;
-        if (t < 1 || t > OZ_SLICES) continue;
-        const __half* a = As + (size_t)(s - 1) * kpad * m;
-        const __half* b = Bs + (size_t)(t - 1) * kpad * n;
-        // P_c = A_s[chunk c]^T B_t[chunk c], c = 0 .. nchunk-1 (m x n each, exact)
+    // least significant level first
+    for (int lev = OZ_SLICES + 1; lev >= 2 && st == CR_OK; --lev) {
+      // rows of the concatenated product: A slots 0 .. lev-2, B slots S-lev+1 .. S-1
+      const int nchunk = (lev - 1) * kpad / kc;
+      const __half* a0 = As;
+      const __half* b0 = Bs + (size_t)(OZ_SLICES - lev + 1) * kpad;
+      for (int g0 = 0; g0 < nchunk; g0 += group) {
+        const int cnt = std::min(group, nchunk - g0);
+        // P_c = A_lev[chunk g0 + c]^T B_lev[chunk g0 + c], c < cnt (m x n each, exact)
         const cublasStatus_t cs = cublasGemmStridedBatchedEx(
-            h, CUBLAS_OP_T, CUBLAS_OP_N, (int)m, (int)n, OZ_KC, &one, a, CUDA_R_16F, kpad, OZ_KC, b, CUDA_R_16F, kpad,
-            OZ_KC, &zero, P, CUDA_R_32F, (int)m, (long long)(m * n), nchunk, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
+            h, CUBLAS_OP_T, CUBLAS_OP_N, (int)m, (int)n, kc, &one, a0 + (size_t)g0 * kc, CUDA_R_16F, (int)ldk, kc,
+            b0 + (size_t)g0 * kc, CUDA_R_16F, (int)ldk, kc, &zero, P, CUDA_R_32F, (int)m, (long long)(m * n), cnt,
+            CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
         if (cs != CUBLAS_STATUS_SUCCESS) {
           st = fail(CR_ERR_CUDA, "Ozaki product: cublasGemmStridedBatchedEx failed (" + std::to_string((int)cs) + ")");
           break;
         }
+        const bool last = lev == 2 && g0 + cnt >= nchunk;
         TimedScope ts("k_oz_accum", stream);
-        k_oz_accum<<<grid_for(m * n), 256, 0, stream>>>(P, nchunk, (int)m, (int)n, Ea, Eb, lev, C, first ? 1 : 0);
+        k_oz_accum<<<ga, 256, 0, stream>>>(P, cnt, (int)m, (int)n, Ea, Eb, OZ_BITS * lev, C, first ? 1 : 0,
+                                           last ? 1 : 0, d_Y, ldy, d_S, lds);
         count_launch();
         first = false;
       }
     }
     if (st != CR_OK) break;
-    k_oz_final<<<grid_for(m * n), 256, 0, stream>>>(C, (int)m, (int)n, d_Y, ldy, d_S, lds);
-    count_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) st = fail(CR_ERR_CUDA, cudaGetErrorName(e));
   } while (false);
-  for (void* p : {(void*)R, (void*)Ea, (void*)Eb, (void*)As, (void*)Bs, (void*)P, (void*)C}) cudaFreeAsync(p, stream);
+  for (void* p : {(void*)R, (void*)Ea, (void*)Eb, (void*)As, (void*)Bs, (void*)P, (void*)C}) scratch_free(p, stream);
   return st;
 }
 

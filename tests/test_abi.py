@@ -118,6 +118,7 @@ def test_options_host_side(lib):
     assert cr._lib.cr_set_option(cr.CR_OPT_FP64_GEMM, cr.CR_GEMM_DF) == 0
     assert cr._lib.cr_set_option(99, 0) == 1 and cr._lib.cr_get_option(99, ctypes.byref(v)) == 1
     assert cr._lib.cr_get_option(cr.CR_OPT_DIAG_ARITH, None) == 1
+    assert cr._lib.cr_workspace_trim() == 0   # no pool yet: nothing to return, no device call
     d = ctypes.c_double()
     assert cr._lib.cr_peak_probe(cr.CR_PEAK_DFMA, 100, None, None) == 1
     assert cr._lib.cr_peak_probe(cr.CR_PEAK_DFMA, 0, ctypes.byref(d), None) == 1

@@ -4,16 +4,18 @@ by the Ozaki scheme (CR_OPT_FP64_GEMM = CR_GEMM_OZAKI), against the oracle's FP6
 
 Error bound of the emulated product C = W^T R, entry (i, j), with Ea_i the exponent of column i
 of W (max_k |W_ki| < 2^Ea_i) and Eb_j that of column j of R:
-  - slicing: each entry is cut into 7 slices of 7 bits below 2^Ea (truncation), so
-    W_ki = sum_s a_s 2^(Ea - 7 s) + d with |d| < 2^(Ea - 49), |a_s| <= 127 (same for R);
-  - per term k, the truncations and the dropped slice products (s + t >= 9) are below
-    (1 + 1 + 2^-49 + 6 (127/128)^2) 2^(Ea + Eb - 49) < 8.01 2^(Ea + Eb - 49);
-  - the kept products are exact integers (FP16 x FP16 summed over at most 1024 terms, below
-    2^24, in FP32); their 28 power-of-two-scaled sums are added in double-float pairs: at most
-    28 2^-47 (|W|^T |R|)_ij;
+  - slicing: each entry is cut into 8 slices of 6 bits below 2^Ea (truncation), so
+    W_ki = sum_s a_s 2^(Ea - 6 s) + d with |d| < 2^(Ea - 48), |a_s| <= 63 (same for R);
+  - per term k, the two truncations are below 2 2^(Ea + Eb - 48), and the dropped slice
+    products (s + t >= 10: 17 - L of them at level L) below
+    sum_L (17 - L) 63^2 2^(Ea + Eb - 6 L) < 6.9 2^(Ea + Eb - 48), together < 8.95 2^(Ea + Eb - 48);
+  - the kept products are exact integers (FP16 x FP16 summed over at most 4096 terms, below
+    2^24, in FP32; a level's chunk sums exact in 32-bit integers); the 8 levels' power-of-two-
+    scaled sums are added in double-float pairs, each addition within 2^-47 of the running
+    magnitude, itself below (|W|^T |R|)_ij: at most 16 2^-47 (|W|^T |R|)_ij with margin;
   - S = M_p + C rounds once in FP64, and the oracle's own FP64 product errs by up to
     n_o 2^-53 (|W|^T |R|)_ij.
-So |S - S_oracle| <= n_o 8.02 2^-49 2^(Ea_i + Eb_j) + (28 2^-47 + n_o 2^-53) (|W|^T |R|)_ij
+So |S - S_oracle| <= n_o 9 2^-48 2^(Ea_i + Eb_j) + (16 2^-47 + n_o 2^-53) (|W|^T |R|)_ij
 + 2^-52 |S_ij|."""
 import contextlib
 
@@ -56,14 +58,17 @@ def _exp_above(X):
 def _bound(W, R, S, n_o):
     Ea, Eb = _exp_above(W), _exp_above(R)
     WR = np.abs(W).T @ np.abs(R)
-    return (n_o * 8.02 * 2.0 ** -49 * np.exp2((Ea[:, None] + Eb[None, :]).astype(float))
-            + (28 * 2.0 ** -47 + n_o * 2.0 ** -53) * WR + 2.0 ** -52 * np.abs(S))
+    return (n_o * 9.0 * 2.0 ** -48 * np.exp2((Ea[:, None] + Eb[None, :]).astype(float))
+            + (16 * 2.0 ** -47 + n_o * 2.0 ** -53) * WR + 2.0 ** -52 * np.abs(S))
 
 
-@pytest.mark.parametrize("n_p,n_o,M,scale", [(300, 200, 70, 1.0), (129, 1000, 65, 1.0), (257, 2100, 130, 1e-3)])
+@pytest.mark.parametrize("n_p,n_o,M,scale", [(300, 200, 70, 1.0), (129, 1000, 65, 1.0), (257, 2100, 130, 1e-3),
+                                             (64, 4000, 33, 1.0), (100, 6000, 40, 1.0)])
 def test_ozaki_correction_matches_oracle(lib, n_p, n_o, M, scale):
     """Element by element within the bound above, on ragged sizes (n_o not a multiple of the
-    1024-row chunks: the padding slices are zero) and with columns of W spanning several orders
+    1024-row padding: the padding slices are zero; n_o = 2100 pads to 3072 rows in chunks of
+    1024, 4000 to one 4096-row chunk per slice, 6000 to 6144 rows in chunks of 2048, so each
+    level's product spans several chunks and slices) and with columns of W spanning several orders
     of magnitude (as kriging weights do)."""
     rng = np.random.default_rng(n_p + n_o)
     W = rng.standard_normal((n_o, n_p)) * scale * np.exp(rng.uniform(-8, 2, n_p))[None, :]
@@ -78,6 +83,7 @@ def test_ozaki_correction_matches_oracle(lib, n_p, n_o, M, scale):
     err = np.abs(S - So)
     assert np.all(err <= b), float(np.max(err / b))
     assert np.linalg.norm(err) <= np.linalg.norm(b)
+    assert np.linalg.norm(S - So) <= 1e-11 * np.linalg.norm(So)
 
 
 def test_ozaki_slices_exact_on_integers(lib):
@@ -123,3 +129,44 @@ def test_ozaki_correct_calibrate_matches_unfused(lib, negative):
     assert b["q_in"] == ref["q_in"] and b["q_out"] == ref["q_out"]
     np.testing.assert_array_equal(b["c_in"].cpu().numpy(), ref["c_in"])
     np.testing.assert_array_equal(b["c_out"].cpu().numpy(), ref["c_out"])
+
+
+def test_pooled_scratch_reused_and_trimmed(lib):
+    """The correction's scratch comes from the library pool: repeated calls, and a call after
+    cr_workspace_trim has returned the pool's memory, give the same bits."""
+    rng = np.random.default_rng(9)
+    n_p, n_o, M = 500, 2500, 96
+    W = colmajor(rng.standard_normal((n_o, n_p)) * 0.1)
+    y = dev(rng.standard_normal(n_o))
+    Y = colmajor(rng.standard_normal((n_p + n_o, M)))
+    with gemm_mode(lib, lib.CR_GEMM_OZAKI):
+        a = lib.krige_correct(W, y, Y, n_p, n_o).cpu().numpy()
+        b = lib.krige_correct(W, y, Y, n_p, n_o).cpu().numpy()
+        torch.cuda.synchronize()
+        lib.workspace_trim()
+        c = lib.krige_correct(W, y, Y, n_p, n_o).cpu().numpy()
+    np.testing.assert_array_equal(a, b)
+    np.testing.assert_array_equal(a, c)
+
+
+def test_ozaki_full_size_sampled_rows(lib):
+    """The kriging workload's shape (16384 observations, 16384 prediction sites) with 1100
+    simulations: 4096-row chunks, and the chunk products of the least significant levels no
+    longer fit one 2 GiB batch, so those levels take two GEMM calls each.  Sampled rows of S
+    against the oracle within the bound."""
+    rng = np.random.default_rng(77)
+    n_p, n_o, M = 16384, 16384, 1100
+    W = rng.standard_normal((n_o, n_p)) * np.exp(rng.uniform(-6, 1, n_p))[None, :]
+    y = rng.standard_normal(n_o)
+    Y = rng.standard_normal((n_p + n_o, M))
+    with gemm_mode(lib, lib.CR_GEMM_OZAKI):
+        S = lib.krige_correct(colmajor(W), dev(y), colmajor(Y), n_p, n_o)
+    rows = np.sort(rng.choice(n_p, 48, replace=False))
+    rows[0], rows[-1] = 0, n_p - 1
+    Sg = S[torch.from_numpy(rows).cuda()].cpu().numpy()
+    del S
+    So = oracle.conditional_correction(W[:, rows], y, Y[rows], Y[n_p:])
+    R = y[:, None] - Y[n_p:]
+    b = _bound(W[:, rows], R, So, n_o)
+    err = np.abs(Sg - So)
+    assert np.all(err <= b), float(np.max(err / b))
