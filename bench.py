@@ -501,6 +501,25 @@ def run_krige(args, world, rank, local):
     parts["correct"] = ue[0].elapsed_time(ue[1])
     parts["calibrate"] = ue[1].elapsed_time(ue[2])
     corr_flops = 2.0 * n_p * n_o * M
+    oz = None
+    if ozaki:
+        # one more Ozaki correction with per-part device timing: slicing, the slice GEMMs
+        # (FP16 tensor-core flops: sum over levels L = 2..9 of (L - 1) 2 n_p M n_o', n_o' = n_o
+        # rounded up to 1024) and the exact accumulation (its algorithmic bytes: the chunk
+        # products read once, the double-float accumulator written, read and rewritten per
+        # level, Y_p read and S written by the last level)
+        cr.timing_reset()
+        cr.timing_enable(True)
+        cr.krige_correct(W, yo, Y, n_p, n_o, out=S)
+        t = {k: cr.timing_read(k)[0] for k in ("k_oz_slice", "oz_gemm", "k_oz_accum")}
+        cr.timing_enable(False)
+        kpad = -(-n_o // 1024) * 1024
+        kc = 4096 if kpad % 4096 == 0 else (2048 if kpad % 2048 == 0 else 1024)
+        gemm_flops = 36 * 2.0 * n_p * M * kpad
+        accum_bytes = (36 * (kpad // kc) * 4 + 128) * n_p * M
+        oz = {"slice_ms": t["k_oz_slice"], "gemm_ms": t["oz_gemm"], "accum_ms": t["k_oz_accum"],
+              "gemm_fp16_tflops": gemm_flops / (t["oz_gemm"] / 1e3) / 1e12,
+              "accum_gbs": accum_bytes / (t["k_oz_accum"] / 1e3) / 1e9}
     if rank == 0:
         line = {"metric": "conditional simulations/s (kriging workload)", "value": world * M / (ms / 1e3),
                 "unit": "simulations/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -512,6 +531,7 @@ def run_krige(args, world, rank, local):
                 "parts_ms": parts,
                 "correction_tflops": corr_flops / (parts["correct"] / 1e3) / 1e12,
                 "fp64_gemm": args.fp64_gemm,
+                "ozaki_parts": oz,
                 "precision_map": {"n_fp64": info["n_fp64"], "n_fp32": info["n_fp32"], "n_fp16": info["n_fp16"], "s": info["s"]},
                 "regions": {"q_in": out["q_in"], "q_out": out["q_out"], "inner": int(out["c_in"].sum().item()),
                             "outer": int(out["c_out"].sum().item())},

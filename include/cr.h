@@ -113,9 +113,13 @@ cr_status cr_workspace_trim(void);
 /* Device timing of the library's main kernels, for measurement (the paper has no counterpart).
  * While enabled, every launch of a timed kernel is bracketed by two CUDA events recorded on
  * the stream the kernel is launched on, and the durations are accumulated per kernel name:
- *   "k_diag_chol"   FP64 factor and inverse of one diagonal tile
+ *   "k_diag_chol", "k_diag_chol_df"   factor and inverse of one diagonal tile (FP64 / double-float)
+ *   "k_split_diag_df"   the double-float executor's results to their storage formats
  *   "k_tc_old", "k_tc_new", "k_tc_trsm", "k_tc_trmm"   tensor-core kernel by mode
- *   "k_cov_stats", "k_generate"   covariance statistics and tile generation
+ *   "k_cov_stats", "k_cov_stats_refine", "k_generate"   covariance statistics, tile generation
+ *   "k_corr", "k_corr_scan"   double-float correction product (plain / fused with the scan)
+ *   "k_oz_slice", "oz_gemm", "k_oz_accum"   Ozaki product: operand slicing, the slice GEMMs of
+ *                   one level (cuBLAS), the exact accumulation of one level
  *   "k_scan"        calibration scan
  * cr_timing_enable(on) switches recording on (1) or off (0); it does not clear the totals.
  * cr_timing_read(name, &ms, &n) synchronises the device, folds every recorded launch into the

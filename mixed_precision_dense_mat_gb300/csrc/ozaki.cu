@@ -215,16 +215,19 @@ cr_status ozaki_correction(const double* d_W, int ldw, const double* d_yo, const
   }
   cr_status st = CR_OK;
   do {
-    k_oz_resid<<<grid_for((size_t)n_o * n), 256, 0, stream>>>(d_yo, d_Y, ldy, n_p, n_o, M, R);
-    count_launch();
-    k_oz_colexp<<<(unsigned)m, 256, 0, stream>>>(d_W, ldw, n_o, Ea);
-    count_launch();
-    k_oz_colexp<<<(unsigned)n, 256, 0, stream>>>(R, n_o, n_o, Eb);
-    count_launch();
-    k_oz_slice<<<grid2d(kpad, (int)m), 256, 0, stream>>>(d_W, ldw, n_o, kpad, (int)m, Ea, 0, As);
-    count_launch();
-    k_oz_slice<<<grid2d(kpad, (int)n), 256, 0, stream>>>(R, n_o, n_o, kpad, (int)n, Eb, 1, Bs);
-    count_launch();
+    {
+      TimedScope ts("k_oz_slice", stream);   // residual, exponents and slices of both operands
+      k_oz_resid<<<grid_for((size_t)n_o * n), 256, 0, stream>>>(d_yo, d_Y, ldy, n_p, n_o, M, R);
+      count_launch();
+      k_oz_colexp<<<(unsigned)m, 256, 0, stream>>>(d_W, ldw, n_o, Ea);
+      count_launch();
+      k_oz_colexp<<<(unsigned)n, 256, 0, stream>>>(R, n_o, n_o, Eb);
+      count_launch();
+      k_oz_slice<<<grid2d(kpad, (int)m), 256, 0, stream>>>(d_W, ldw, n_o, kpad, (int)m, Ea, 0, As);
+      count_launch();
+      k_oz_slice<<<grid2d(kpad, (int)n), 256, 0, stream>>>(R, n_o, n_o, kpad, (int)n, Eb, 1, Bs);
+      count_launch();
+    }
     if ((e = cudaGetLastError()) != cudaSuccess) { st = fail(CR_ERR_CUDA, cudaGetErrorName(e)); break; }
     const float one = 1.0f, zero = 0.0f;
     const dim3 ga = grid2d((int)m, (int)n);
@@ -238,10 +241,14 @@ cr_status ozaki_correction(const double* d_W, int ldw, const double* d_yo, const
       for (int g0 = 0; g0 < nchunk; g0 += group) {
         const int cnt = std::min(group, nchunk - g0);
         // P_c = A_lev[chunk g0 + c]^T B_lev[chunk g0 + c], c < cnt (m x n each, exact)
-        const cublasStatus_t cs = cublasGemmStridedBatchedEx(
-            h, CUBLAS_OP_T, CUBLAS_OP_N, (int)m, (int)n, kc, &one, a0 + (size_t)g0 * kc, CUDA_R_16F, (int)ldk, kc,
-            b0 + (size_t)g0 * kc, CUDA_R_16F, (int)ldk, kc, &zero, P, CUDA_R_32F, (int)m, (long long)(m * n), cnt,
-            CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
+        cublasStatus_t cs;
+        {
+          TimedScope tg("oz_gemm", stream);
+          cs = cublasGemmStridedBatchedEx(h, CUBLAS_OP_T, CUBLAS_OP_N, (int)m, (int)n, kc, &one, a0 + (size_t)g0 * kc,
+                                          CUDA_R_16F, (int)ldk, kc, b0 + (size_t)g0 * kc, CUDA_R_16F, (int)ldk, kc, &zero,
+                                          P, CUDA_R_32F, (int)m, (long long)(m * n), cnt, CUBLAS_COMPUTE_32F,
+                                          CUBLAS_GEMM_DEFAULT);
+        }
         if (cs != CUBLAS_STATUS_SUCCESS) {
           st = fail(CR_ERR_CUDA, "Ozaki product: cublasGemmStridedBatchedEx failed (" + std::to_string((int)cs) + ")");
           break;
