@@ -33,6 +33,12 @@ cr_status calibrate_finish(const double* psi_part, const double* phi_part, int n
 cr_status correction_async(const double* d_W, int ldw, const double* d_yo, const double* d_Y, int ldy, int n_p, int n_o,
                            int M, double* d_S, int lds, cudaStream_t stream);
 
+// Cout = Cin + alpha A^T B (A: K x m, B: K x n, column-major FP64; Cin NULL for zero; Cout may
+// be Cin) by the Ozaki scheme with S slices of 6 bits (2 <= S <= 10) on the FP16 tensor cores
+// (ozaki.cu); pool scratch, asynchronous.
+cr_status ozaki_gemm_tn(const double* A, int lda, const double* B, int ldb, int K, int m, int n, double alpha,
+                        const double* Cin, int ldci, double* Cout, int ldco, int S, cudaStream_t stream);
+
 // The conditioning correction S = M_p + W^T (y_o 1^T - M_o) by the Ozaki product on the FP16
 // tensor cores (ozaki.cu); stream-ordered scratch, asynchronous.
 cr_status ozaki_correction(const double* d_W, int ldw, const double* d_yo, const double* d_Y, int ldy, int n_p, int n_o,

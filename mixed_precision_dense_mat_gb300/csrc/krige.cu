@@ -11,7 +11,9 @@
 //    formed in its operand conversion (calib.cu, shared with the fused correction + scan).
 // Sigma_y is factored as its own all-FP64 tile matrix by the library's Cholesky (which keeps
 // each diagonal tile's inverse here); the many-right-hand-side triangular solves are blocked
-// substitutions over tile rows whose products run on the FP64 tile GEMM.
+// substitutions over tile rows whose products run on the FP64 tile GEMM, or, with
+// CR_OPT_FP64_GEMM = CR_GEMM_OZAKI, as Ozaki products on the FP16 tensor cores (ozaki.cu) over
+// dense copies of the factor.
 #include <functional>
 
 #include "calib.cuh"
@@ -69,7 +71,88 @@ __global__ void k_mspe(const double* __restrict__ c1, const double* __restrict__
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_p; i += gridDim.x * blockDim.x) v[i] = theta0 + c1[i] - 2.0 * c2[i];
 }
 
+// Dense copies of the strictly lower tiles of an all-FP64 tile factor (row-major tiles in
+// pool64): Lr row-major (Lr[r n + c] = L(r, c)) and Lc column-major (Lc[c n + r] = L(r, c)).
+// The diagonal blocks and the upper part are not written (the solves never read them).  One
+// CTA of 32 x 8 threads per 32 x 32 piece of a tile; the transposed copy goes through shared
+// memory so that both stores are coalesced.  blockIdx.z enumerates the tiles (I, J), I > J.
+__global__ void __launch_bounds__(256) k_dense_lower(const double* __restrict__ pool64, const int* __restrict__ i64, int n,
+                                                     int nb, double* __restrict__ Lr, double* __restrict__ Lc) {
+  const int t = blockIdx.z;
+  int I = (int)((1.0 + sqrt(1.0 + 8.0 * (double)t)) * 0.5);
+  while (I * (I - 1) / 2 > t) --I;
+  while ((I + 1) * I / 2 <= t) ++I;
+  const int J = t - I * (I - 1) / 2;
+  const double* tile = pool64 + (size_t)i64[tidx(I, J)] * nb * nb;
+  const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
+  __shared__ double sm[32][33];
+  for (int q = threadIdx.y; q < 32; q += 8) {
+    const int r = r0 + q, c = c0 + threadIdx.x;
+    const int gr = I * nb + r, gc = J * nb + c;
+    if (r < nb && c < nb && gr < n && gc < n) {
+      const double x = tile[(size_t)r * nb + c];
+      Lr[(size_t)gr * n + gc] = x;
+      sm[q][threadIdx.x] = x;
+    }
+  }
+  __syncthreads();
+  for (int q = threadIdx.y; q < 32; q += 8) {
+    const int c = c0 + q, r = r0 + threadIdx.x;
+    const int gr = I * nb + r, gc = J * nb + c;
+    if (r < nb && c < nb && gr < n && gc < n) Lc[(size_t)gc * n + gr] = sm[threadIdx.x][q];
+  }
+}
+
+// Mt_i = M_i^T for every row-major nb x nb tile M_i of `src` (Mt_i[c nb + r] = M_i[r nb + c]).
+__global__ void __launch_bounds__(256) k_transpose_tiles(const double* __restrict__ src, int nb, double* __restrict__ dst) {
+  const double* a = src + (size_t)blockIdx.z * nb * nb;
+  double* b = dst + (size_t)blockIdx.z * nb * nb;
+  const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
+  __shared__ double sm[32][33];
+  for (int q = threadIdx.y; q < 32; q += 8) {
+    const int r = r0 + q, c = c0 + threadIdx.x;
+    if (r < nb && c < nb) sm[q][threadIdx.x] = a[(size_t)r * nb + c];
+  }
+  __syncthreads();
+  for (int q = threadIdx.y; q < 32; q += 8) {
+    const int c = c0 + q, r = r0 + threadIdx.x;
+    if (r < nb && c < nb) b[(size_t)c * nb + r] = sm[threadIdx.x][q];
+  }
+}
+
 namespace {
+
+// Slices per operand in the solves' Ozaki products: 9 x 6 = 54 bits below each column's power
+// of two, about FP64's 53 (the solution columns span several orders of magnitude, and the
+// scheme's error is relative to each column's largest entry).
+constexpr int KRIGE_OZ_SLICES = 9;
+
+// Blocked solve of the factor's triangular systems with the Ozaki product: forward L X = B or
+// backward L^T X = B, in place on B (n x r, column-major, ld ldb).  Per tile row i:
+// B_i -= L_(i, <i) B_(<i) (forward) or L_(>i, i)^T B_(>i) (backward), then B_i = M_i B_i or
+// M_i^T B_i with M_i the inverse of the diagonal factor.  Lr, Lc are the dense copies of
+// k_dense_lower; Mt holds the transposed inverse tiles.
+cr_status ozaki_trsm(cr_tilemat L, const double* Lr, const double* Lc, const double* Mt, double* B, int ldb, int r,
+                     bool backward, cudaStream_t s) {
+  const int nt = L->nt, nb = L->nb, n = L->n;
+  const size_t nb2 = (size_t)nb * nb;
+  for (int step = 0; step < nt; ++step) {
+    const int i = backward ? nt - 1 - step : step;
+    const int ri = std::min(nb, n - i * nb);
+    double* Bi = B + (size_t)i * nb;
+    if (!backward && i > 0)   // A(k, c) = L(i nb + c, k) = Lr[(i nb + c) n + k]
+      CR_TRY(ozaki_gemm_tn(Lr + (size_t)i * nb * n, n, B, ldb, i * nb, ri, r, -1.0, Bi, ldb, Bi, ldb, KRIGE_OZ_SLICES, s));
+    if (backward && i < nt - 1) {   // A(k, c) = L(k0 + k, i nb + c) = Lc[(i nb + c) n + k0 + k]
+      const int k0 = (i + 1) * nb;
+      CR_TRY(ozaki_gemm_tn(Lc + (size_t)i * nb * n + k0, n, B + k0, ldb, n - k0, ri, r, -1.0, Bi, ldb, Bi, ldb,
+                                KRIGE_OZ_SLICES, s));
+    }
+    // forward: A(k, c) = M_i(c, k) = M_i[c nb + k]; backward: A(k, c) = M_i(k, c) = Mt_i[c nb + k]
+    const double* Md = (backward ? Mt : L->minv_all) + (size_t)i * nb2;
+    CR_TRY(ozaki_gemm_tn(Md, nb, Bi, ldb, ri, ri, r, 1.0, nullptr, 0, Bi, ldb, KRIGE_OZ_SLICES, s));
+  }
+  return CR_OK;
+}
 
 // FP64 GEMM jobs over an m x r column-major output, 64 x 64 blocks.
 void add_jobs(std::vector<DJob>& js, double* C, int ldc, int m, int r, int pbeg, int pcnt, double alpha, double beta, int kmax) {
@@ -233,18 +316,38 @@ extern "C" cr_status cr_krige(cr_tilemat V, const double* d_Xo, const double* d_
   // step 4: W = V_op - X_o H; forward solve (Y), colsum(Y .* Y); backward solve (W)
   CR_CUDA(cudaMemcpy2DAsync(d_W, (size_t)ldw * sizeof(double), Vop, (size_t)n_o * sizeof(double), (size_t)n_o * sizeof(double), n_p,
                             cudaMemcpyDeviceToDevice, s));
+  const bool oz = option_fp64_gemm() == CR_GEMM_OZAKI;
+  double *Lr = nullptr, *Lc = nullptr, *Mt = nullptr;
+  if (oz) {
+    const size_t nn = (size_t)n_o * n_o;
+    Lr = alloc(nn * sizeof(double));
+    Lc = alloc(nn * sizeof(double));
+    Mt = alloc((size_t)So->nt * nb * nb * sizeof(double));
+    if (!Lr || !Lc || !Mt) return fail(CR_ERR_NOMEM, "cr_krige: dense factor copies");
+    const int nstrict = So->nt * (So->nt - 1) / 2;
+    const dim3 blk(32, 8), gt((nb + 31) / 32, (nb + 31) / 32, 1);
+    if (nstrict > 0) {
+      k_dense_lower<<<dim3(gt.x, gt.y, nstrict), blk, 0, s>>>(So->pool64, So->d_i64, n_o, nb, Lr, Lc);
+      CR_CHECK_LAUNCH("k_dense_lower");
+    }
+    k_transpose_tiles<<<dim3(gt.x, gt.y, So->nt), blk, 0, s>>>(So->minv_all, nb, Mt);
+    CR_CHECK_LAUNCH("k_transpose_tiles");
+  }
   {
     Seq S;
     S.pairs.push_back(DPair{d_Xo, H, 1, n_o, 3, 1, 3});       // (X_o H)(q, i) = sum_m Xo[q, m] H[m, i]
     std::vector<DJob> js;
     add_jobs(js, d_W, ldw, n_o, n_p, 0, 1, -1.0, 1.0, 3);
     S.gemm(js);
-    plan_trsm(S, So, d_W, ldw, n_p, false, T);
+    if (!oz) plan_trsm(S, So, d_W, ldw, n_p, false, T);
     CR_TRY(S.run(s));
   }
+  if (oz) CR_TRY(ozaki_trsm(So, Lr, Lc, Mt, d_W, ldw, n_p, false, s));
   k_coldot<<<n_p, 256, 0, s>>>(d_W, ldw, d_W, ldw, n_o, c1);
   CR_CHECK_LAUNCH("k_coldot");
-  {
+  if (oz) {
+    CR_TRY(ozaki_trsm(So, Lr, Lc, Mt, d_W, ldw, n_p, true, s));
+  } else {
     Seq S;
     plan_trsm(S, So, d_W, ldw, n_p, true, T);
     CR_TRY(S.run(s));

@@ -37,8 +37,10 @@ namespace cr {
 
 namespace {
 
-// slice width and count; chunk rows with 4096 * 63^2 < 2^24; chunks per GEMM call at most
-constexpr int OZ_BITS = 6, OZ_SLICES = 8, OZ_KC_MAX = 4096, OZ_GROUP = 32;
+// slice width; slice counts supported (S slices keep 6 S bits below each column's power of
+// two: 48 for the correction, 54 for the kriging solves); chunk rows with 4096 * 63^2 < 2^24;
+// chunks per GEMM call at most
+constexpr int OZ_BITS = 6, OZ_MIN_SLICES = 2, OZ_MAX_SLICES = 10, OZ_KC_MAX = 4096, OZ_GROUP = 32;
 constexpr unsigned long long OZ_MASK = (1ull << OZ_BITS) - 1ull;
 
 // E_c with max_r |X_rc| < 2^E_c (positive doubles order as their bit patterns); 0 for a zero
@@ -65,10 +67,11 @@ __global__ void __launch_bounds__(256) k_oz_colexp(const double* __restrict__ X,
   }
 }
 
-// Slices of X (rows x cols, column-major, ld): column c of out holds, at
+// Slices of X (rows x cols, column-major, ld), OZ_SLICES of them: column c of out holds, at
 // out + c * S * rows_pad + slot * rows_pad, slice s + 1 (s = 0 the most significant) in slot s,
 // or in slot S - 1 - s when `reversed`, as rows_pad FP16 integers in [-63, 63], rows beyond
 // `rows` zero.  Integer arithmetic on the FP64 bit pattern only.
+template <int OZ_SLICES>
 __global__ void __launch_bounds__(256) k_oz_slice(const double* __restrict__ X, int ld, int rows, int rows_pad, int cols,
                                                   const int* __restrict__ E, int reversed, __half* __restrict__ out) {
   for (int c = blockIdx.y; c < cols; c += gridDim.y) {
@@ -82,7 +85,7 @@ __global__ void __launch_bounds__(256) k_oz_slice(const double* __restrict__ X, 
         neg = (b >> 63) != 0;
         const int eb = (int)((b >> 52) & 0x7ff);
         const unsigned long long mant = (b & 0x000fffffffffffffull) | (eb ? 0x0010000000000000ull : 0ull);
-        // |x| = mant 2^(e2);  q = floor(|x| 2^(6 S - E_c)) < 2^(6 S)
+        // |x| = mant 2^(e2);  q = floor(|x| 2^(6 S - E_c)) < 2^(6 S) <= 2^60
         const int e2 = (eb ? eb : 1) - 1075;
         const int shift = e2 + OZ_BITS * OZ_SLICES - Ec;
         if (shift >= 0) q = shift < 64 ? mant << shift : 0ull;
@@ -117,11 +120,12 @@ __device__ __forceinline__ float oz_scale(float x, int ex) {
 // One level's contribution for `nb` chunk products P_b (m x n FP32 exact integers below 2^24):
 // v = sum_b P_b(i, j), exact in 32-bit integers (nb <= 32), split exactly into two floats,
 // scaled by 2^(Ea_i + Eb_j - shift) and added to the double-float C (C = the term when
-// `first`).  With `last`, S = M_p + C in FP64 is written instead of C.
+// `first`).  With `last`, Cout = Cin + alpha C in FP64 is written instead of C (Cin = NULL:
+// zero); Cout may be Cin (each entry is read, then written, by one thread).
 __global__ void __launch_bounds__(256) k_oz_accum(const float* __restrict__ P, int nb, int m, int n,
                                                   const int* __restrict__ Ea, const int* __restrict__ Eb, int shift,
-                                                  float2* __restrict__ C, int first, int last,
-                                                  const double* __restrict__ Y, int ldy, double* __restrict__ S, int lds) {
+                                                  float2* __restrict__ C, int first, int last, double alpha,
+                                                  const double* Cin, int ldci, double* Cout, int ldco) {
   const size_t mn = (size_t)m * n;
   for (int j = blockIdx.y; j < n; j += gridDim.y) {
     const int ej = Eb[j] - shift;
@@ -139,10 +143,21 @@ __global__ void __launch_bounds__(256) k_oz_accum(const float* __restrict__ P, i
         const float2 c = C[e];
         acc = df_add({c.x, c.y}, acc);
       }
-      if (last) S[(size_t)j * lds + i] = Y[(size_t)j * ldy + i] + ((double)acc.hi + (double)acc.lo);
-      else C[e] = make_float2(acc.hi, acc.lo);
+      if (last) {
+        const double base = Cin ? Cin[(size_t)j * ldci + i] : 0.0;
+        Cout[(size_t)j * ldco + i] = base + alpha * ((double)acc.hi + (double)acc.lo);
+      } else {
+        C[e] = make_float2(acc.hi, acc.lo);
+      }
     }
   }
+}
+
+// Cout = Cin (or 0) when the inner dimension is empty.
+__global__ void __launch_bounds__(256) k_oz_copy(const double* Cin, int ldci, int m, int n, double* Cout, int ldco) {
+  for (int j = blockIdx.y; j < n; j += gridDim.y)
+    for (int i = blockIdx.x * 256 + threadIdx.x; i < m; i += gridDim.x * 256)
+      Cout[(size_t)j * ldco + i] = Cin ? Cin[(size_t)j * ldci + i] : 0.0;
 }
 
 std::mutex g_cublas_mu;
@@ -181,73 +196,90 @@ unsigned grid_for(size_t total) {
 
 }  // namespace
 
-// The correction S = M_p + W^T (y_o 1^T - M_o) by the Ozaki product (W: n_o x n_p, ld ldw;
-// Y: (n_p + n_o) x M, ld ldy; S: n_p x M, ld lds).  Scratch from the library pool: the slices
-// (8 (n_o' n_p + n_o' M) FP16, n_o' = n_o rounded up to 1024), the chunk products (at most
-// 32 n_p M FP32, fewer when that exceeds 2 GiB), R (n_o M FP64) and the accumulator (n_p M
+// Cout = Cin + alpha A^T B by the Ozaki product with S slices of 6 bits per operand column
+// (A: K x m, ld lda; B: K x n, ld ldb; Cin, Cout: m x n, ld ldci / ldco; Cin NULL for zero;
+// Cout may equal Cin with the same ld, and may overlap A or B, which are sliced before Cout is
+// written).  The kept products are those with s + t <= S + 1, one GEMM per level.  Scratch
+// from the library pool: the slices (S K' (m + n) FP16, K' = K rounded up to 1024), the chunk
+// products (at most 32 m n FP32, fewer when that exceeds 2 GiB) and the accumulator (m n
 // double-float pairs).
-cr_status ozaki_correction(const double* d_W, int ldw, const double* d_yo, const double* d_Y, int ldy, int n_p, int n_o,
-                           int M, double* d_S, int lds, cudaStream_t stream) {
+cr_status ozaki_gemm_tn(const double* A, int lda, const double* B, int ldb, int K, int m_, int n_, double alpha,
+                        const double* Cin, int ldci, double* Cout, int ldco, int S, cudaStream_t stream) {
+  if (S < OZ_MIN_SLICES || S > OZ_MAX_SLICES) return fail(CR_ERR_ARG, "Ozaki product: slice count");
+  if (m_ <= 0 || n_ <= 0) return CR_OK;
+  const size_t m = (size_t)m_, n = (size_t)n_;
+  if (K <= 0) {
+    k_oz_copy<<<grid2d(m_, n_), 256, 0, stream>>>(Cin, ldci, m_, n_, Cout, ldco);
+    CR_CHECK_LAUNCH("k_oz_copy");
+    return CR_OK;
+  }
   std::lock_guard<std::mutex> lk(g_cublas_mu);
   cublasHandle_t h = nullptr;
   CR_TRY(cublas_for(stream, &h));
-  const int kpad = (n_o + 1023) / 1024 * 1024;
+  const int kpad = (K + 1023) / 1024 * 1024;
   // chunk rows: a divisor of kpad, so that no chunk spans two slices
   const int kc = kpad % OZ_KC_MAX == 0 ? OZ_KC_MAX : (kpad % 2048 == 0 ? 2048 : 1024);
-  const size_t m = (size_t)n_p, n = (size_t)M, ldk = (size_t)OZ_SLICES * kpad;
+  const size_t ldk = (size_t)S * kpad;
   const int group = (int)std::max<size_t>(1, std::min<size_t>(OZ_GROUP, ((size_t)1 << 31) / (m * n * sizeof(float))));
-  double* R = nullptr;
   int *Ea = nullptr, *Eb = nullptr;
   __half *As = nullptr, *Bs = nullptr;
   float* P = nullptr;
   float2* C = nullptr;
   auto alloc = [&](void** p, size_t bytes) { return scratch_alloc(p, bytes, stream); };
   cudaError_t e = cudaSuccess;
-  if ((e = alloc((void**)&R, (size_t)n_o * n * sizeof(double))) != cudaSuccess ||
-      (e = alloc((void**)&Ea, m * sizeof(int))) != cudaSuccess || (e = alloc((void**)&Eb, n * sizeof(int))) != cudaSuccess ||
+  if ((e = alloc((void**)&Ea, m * sizeof(int))) != cudaSuccess || (e = alloc((void**)&Eb, n * sizeof(int))) != cudaSuccess ||
       (e = alloc((void**)&As, ldk * m * sizeof(__half))) != cudaSuccess ||
       (e = alloc((void**)&Bs, ldk * n * sizeof(__half))) != cudaSuccess ||
       (e = alloc((void**)&P, (size_t)group * m * n * sizeof(float))) != cudaSuccess ||
       (e = alloc((void**)&C, m * n * sizeof(float2))) != cudaSuccess) {
-    for (void* p : {(void*)R, (void*)Ea, (void*)Eb, (void*)As, (void*)Bs, (void*)P, (void*)C})
-      scratch_free(p, stream);
+    for (void* p : {(void*)Ea, (void*)Eb, (void*)As, (void*)Bs, (void*)P, (void*)C}) scratch_free(p, stream);
     return fail(CR_ERR_NOMEM, std::string("Ozaki product: scratch: ") + cudaGetErrorName(e));
   }
   cr_status st = CR_OK;
   do {
     {
-      TimedScope ts("k_oz_slice", stream);   // residual, exponents and slices of both operands
-      k_oz_resid<<<grid_for((size_t)n_o * n), 256, 0, stream>>>(d_yo, d_Y, ldy, n_p, n_o, M, R);
+      TimedScope ts("k_oz_slice", stream);   // exponents and slices of both operands
+      k_oz_colexp<<<(unsigned)m, 256, 0, stream>>>(A, lda, K, Ea);
       count_launch();
-      k_oz_colexp<<<(unsigned)m, 256, 0, stream>>>(d_W, ldw, n_o, Ea);
+      k_oz_colexp<<<(unsigned)n, 256, 0, stream>>>(B, ldb, K, Eb);
       count_launch();
-      k_oz_colexp<<<(unsigned)n, 256, 0, stream>>>(R, n_o, n_o, Eb);
-      count_launch();
-      k_oz_slice<<<grid2d(kpad, (int)m), 256, 0, stream>>>(d_W, ldw, n_o, kpad, (int)m, Ea, 0, As);
-      count_launch();
-      k_oz_slice<<<grid2d(kpad, (int)n), 256, 0, stream>>>(R, n_o, n_o, kpad, (int)n, Eb, 1, Bs);
-      count_launch();
+      auto slice = [&](const double* X, int ld, int cols, const int* E, int rev, __half* out) {
+        const dim3 g = grid2d(kpad, cols);
+        switch (S) {
+          case 2: k_oz_slice<2><<<g, 256, 0, stream>>>(X, ld, K, kpad, cols, E, rev, out); break;
+          case 3: k_oz_slice<3><<<g, 256, 0, stream>>>(X, ld, K, kpad, cols, E, rev, out); break;
+          case 4: k_oz_slice<4><<<g, 256, 0, stream>>>(X, ld, K, kpad, cols, E, rev, out); break;
+          case 5: k_oz_slice<5><<<g, 256, 0, stream>>>(X, ld, K, kpad, cols, E, rev, out); break;
+          case 6: k_oz_slice<6><<<g, 256, 0, stream>>>(X, ld, K, kpad, cols, E, rev, out); break;
+          case 7: k_oz_slice<7><<<g, 256, 0, stream>>>(X, ld, K, kpad, cols, E, rev, out); break;
+          case 8: k_oz_slice<8><<<g, 256, 0, stream>>>(X, ld, K, kpad, cols, E, rev, out); break;
+          case 9: k_oz_slice<9><<<g, 256, 0, stream>>>(X, ld, K, kpad, cols, E, rev, out); break;
+          default: k_oz_slice<10><<<g, 256, 0, stream>>>(X, ld, K, kpad, cols, E, rev, out); break;
+        }
+        count_launch();
+      };
+      slice(A, lda, m_, Ea, 0, As);
+      slice(B, ldb, n_, Eb, 1, Bs);
     }
     if ((e = cudaGetLastError()) != cudaSuccess) { st = fail(CR_ERR_CUDA, cudaGetErrorName(e)); break; }
     const float one = 1.0f, zero = 0.0f;
-    const dim3 ga = grid2d((int)m, (int)n);
+    const dim3 ga = grid2d(m_, n_);
     bool first = true;
     // least significant level first
-    for (int lev = OZ_SLICES + 1; lev >= 2 && st == CR_OK; --lev) {
+    for (int lev = S + 1; lev >= 2 && st == CR_OK; --lev) {
       // rows of the concatenated product: A slots 0 .. lev-2, B slots S-lev+1 .. S-1
       const int nchunk = (lev - 1) * kpad / kc;
       const __half* a0 = As;
-      const __half* b0 = Bs + (size_t)(OZ_SLICES - lev + 1) * kpad;
+      const __half* b0 = Bs + (size_t)(S - lev + 1) * kpad;
       for (int g0 = 0; g0 < nchunk; g0 += group) {
         const int cnt = std::min(group, nchunk - g0);
         // P_c = A_lev[chunk g0 + c]^T B_lev[chunk g0 + c], c < cnt (m x n each, exact)
         cublasStatus_t cs;
         {
           TimedScope tg("oz_gemm", stream);
-          cs = cublasGemmStridedBatchedEx(h, CUBLAS_OP_T, CUBLAS_OP_N, (int)m, (int)n, kc, &one, a0 + (size_t)g0 * kc,
-                                          CUDA_R_16F, (int)ldk, kc, b0 + (size_t)g0 * kc, CUDA_R_16F, (int)ldk, kc, &zero,
-                                          P, CUDA_R_32F, (int)m, (long long)(m * n), cnt, CUBLAS_COMPUTE_32F,
-                                          CUBLAS_GEMM_DEFAULT);
+          cs = cublasGemmStridedBatchedEx(h, CUBLAS_OP_T, CUBLAS_OP_N, m_, n_, kc, &one, a0 + (size_t)g0 * kc, CUDA_R_16F,
+                                          (int)ldk, kc, b0 + (size_t)g0 * kc, CUDA_R_16F, (int)ldk, kc, &zero, P, CUDA_R_32F,
+                                          m_, (long long)(m * n), cnt, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
         }
         if (cs != CUBLAS_STATUS_SUCCESS) {
           st = fail(CR_ERR_CUDA, "Ozaki product: cublasGemmStridedBatchedEx failed (" + std::to_string((int)cs) + ")");
@@ -255,8 +287,8 @@ cr_status ozaki_correction(const double* d_W, int ldw, const double* d_yo, const
         }
         const bool last = lev == 2 && g0 + cnt >= nchunk;
         TimedScope ts("k_oz_accum", stream);
-        k_oz_accum<<<ga, 256, 0, stream>>>(P, cnt, (int)m, (int)n, Ea, Eb, OZ_BITS * lev, C, first ? 1 : 0,
-                                           last ? 1 : 0, d_Y, ldy, d_S, lds);
+        k_oz_accum<<<ga, 256, 0, stream>>>(P, cnt, m_, n_, Ea, Eb, OZ_BITS * lev, C, first ? 1 : 0, last ? 1 : 0, alpha,
+                                           Cin, ldci, Cout, ldco);
         count_launch();
         first = false;
       }
@@ -264,7 +296,26 @@ cr_status ozaki_correction(const double* d_W, int ldw, const double* d_yo, const
     if (st != CR_OK) break;
     if ((e = cudaGetLastError()) != cudaSuccess) st = fail(CR_ERR_CUDA, cudaGetErrorName(e));
   } while (false);
-  for (void* p : {(void*)R, (void*)Ea, (void*)Eb, (void*)As, (void*)Bs, (void*)P, (void*)C}) scratch_free(p, stream);
+  for (void* p : {(void*)Ea, (void*)Eb, (void*)As, (void*)Bs, (void*)P, (void*)C}) scratch_free(p, stream);
+  return st;
+}
+
+// The correction S = M_p + W^T (y_o 1^T - M_o) (W: n_o x n_p, ld ldw; Y: (n_p + n_o) x M, ld
+// ldy; S: n_p x M, ld lds): R = y_o 1^T - M_o (n_o M FP64, pool scratch), then the Ozaki
+// product with Cin = M_p.
+cr_status ozaki_correction(const double* d_W, int ldw, const double* d_yo, const double* d_Y, int ldy, int n_p, int n_o,
+                           int M, double* d_S, int lds, cudaStream_t stream) {
+  double* R = nullptr;
+  CR_CUDA(scratch_alloc((void**)&R, (size_t)n_o * M * sizeof(double), stream));
+  {
+    TimedScope ts("k_oz_slice", stream);
+    k_oz_resid<<<grid_for((size_t)n_o * M), 256, 0, stream>>>(d_yo, d_Y, ldy, n_p, n_o, M, R);
+    count_launch();
+  }
+  cr_status st = CR_OK;
+  if (cudaError_t e = cudaGetLastError()) st = fail(CR_ERR_CUDA, cudaGetErrorName(e));
+  if (st == CR_OK) st = ozaki_gemm_tn(d_W, ldw, R, n_o, n_o, n_p, M, 1.0, d_Y, ldy, d_S, lds, 8, stream);
+  scratch_free(R, stream);
   return st;
 }
 

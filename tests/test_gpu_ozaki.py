@@ -23,6 +23,7 @@ import numpy as np
 import pytest
 import torch
 
+import inputgen
 import oracle
 
 pytestmark = pytest.mark.gpu
@@ -170,3 +171,67 @@ def test_ozaki_full_size_sampled_rows(lib):
     b = _bound(W[:, rows], R, So, n_o)
     err = np.abs(Sg - So)
     assert np.all(err <= b), float(np.max(err / b))
+
+
+def relf(a, b):
+    return np.linalg.norm(a - b) / np.linalg.norm(b)
+
+
+def _krige_case(n_o, m, seed, nu=1.0, beta=0.1, tau2=0.01):
+    pred = inputgen.morton_sorted(inputgen.grid_cell_centres(m))
+    obs = inputgen.morton_sorted(inputgen.uniform_locations(n_o, seed))
+    xy = np.ascontiguousarray(np.concatenate([pred, obs]))
+    n_p = len(pred)
+    X = np.column_stack([np.ones(len(xy)), xy[:, 0], xy[:, 1]])
+    y = inputgen.observation_values(obs, (1.0, 0.5, -0.3), 0.3, seed + 1)
+    V = oracle.covariance_matrix(xy, "matern", 1.0, beta, nu, 0.0, n_p, tau2)
+    return xy, n_p, X, y, V
+
+
+@pytest.mark.parametrize("n_o,m,nb", [(1024, 32, 128), (1000, 24, 128), (4096, 64, 512), (2600, 40, 512)])
+def test_ozaki_kriging_matches_oracle(lib, n_o, m, nb):
+    """cr_krige with its many-right-hand-side triangular solves as Ozaki products (Section V-A
+    Eq.5-6; Alg.2 steps 2-6) against the oracle, with the FP64 path's tolerance: W and z_hat
+    within max(1e-10, 20 x the distance between two FP64 orderings of the same solves) in
+    relative Frobenius norm, v within 1e-9, and X_o^T W = X_p^T.  Ragged cases: n_o = 1000 and
+    2600 leave a partial last tile row."""
+    xy, n_p, X, y, V = _krige_case(n_o, m, 5)
+    G = lib.TileMat(len(xy), nb)
+    lib.cov_build(G, dev(xy), "matern", 1.0, 0.1, 1.0, nugget=0.0, n_pred=n_p, tau2=0.01)
+    with gemm_mode(lib, lib.CR_GEMM_OZAKI):
+        W, z, v = lib.krige(G, colmajor(X[n_p:]), colmajor(X[:n_p]), dev(y))
+    Wo, zo, vo = oracle.universal_kriging(V[n_p:, n_p:], V[n_p:, :n_p], X[n_p:], X[:n_p], y, 1.0)
+    K = np.block([[V[n_p:, n_p:], X[n_p:]], [X[n_p:].T, np.zeros((3, 3))]])
+    Wl = np.linalg.solve(K, np.vstack([V[n_p:, :n_p], X[:n_p].T]))[:n_o]
+    tol = max(1e-10, 20 * relf(Wl, Wo))
+    Wg = W.cpu().numpy()
+    assert relf(Wg, Wo) <= tol, (relf(Wg, Wo), tol)
+    assert relf(z.cpu().numpy(), zo) <= tol
+    assert np.max(np.abs(v.cpu().numpy() - vo)) <= 1e-9
+    np.testing.assert_allclose(X[n_p:].T @ Wg, X[:n_p].T, atol=1e-8)
+    G.close()
+
+
+def test_ozaki_kriging_full_size_against_fp64_solves(lib):
+    """The kriging workload (16384 observations, 128 x 128 grid, tile 512): W, z_hat and v from
+    the Ozaki solves against those of the FP64 solves on the same factor, within the oracle
+    tests' 1e-10 floor (relative Frobenius; v within 1e-9), and X_o^T W = X_p^T."""
+    w = inputgen.WORKLOADS["k"]
+    xy = inputgen.workload_locations(w)
+    n_p, n_o = w.n_pred, w.n_obs
+    X = np.column_stack([np.ones(w.n), xy[:, 0], xy[:, 1]])
+    y = inputgen.observation_values(xy[n_p:], (1.0, 0.5, -0.3), 0.1, 3)
+    V = lib.TileMat(w.n, w.nb)
+    lib.cov_build(V, dev(xy), w.family, w.sigma2, w.beta, w.nu, nugget=w.nugget, n_pred=n_p, tau2=w.tau2)
+    Xo, Xp, yd = colmajor(X[n_p:]), colmajor(X[:n_p]), dev(y)
+    with gemm_mode(lib, lib.CR_GEMM_DF):
+        W64, z64, v64 = lib.krige(V, Xo, Xp, yd)
+    with gemm_mode(lib, lib.CR_GEMM_OZAKI):
+        W, z, v = lib.krige(V, Xo, Xp, yd)
+    e = (torch.linalg.norm(W - W64) / torch.linalg.norm(W64)).item()
+    assert e <= 1e-10, e
+    assert (torch.linalg.norm(z - z64) / torch.linalg.norm(z64)).item() <= 1e-10
+    assert torch.max(torch.abs(v - v64)).item() <= 1e-9
+    XoT_W = (torch.from_numpy(X[n_p:]).cuda().T @ W).cpu().numpy()
+    assert np.max(np.abs(XoT_W - X[:n_p].T)) <= 1e-6 * np.max(np.abs(X[:n_p]))
+    V.close()
