@@ -144,15 +144,18 @@ cr_status cr_timing_reset(void);
  *                        issue 1/64 of the FP32 lanes per cycle); CR_DIAG_AUTO (default):
  *                        double-float for adaptive factorisations (amp != 0), FP64 for
  *                        all-FP64 ones (amp = 0, including cr_krige's Sigma_y).
- *  CR_OPT_FP64_GEMM      arithmetic of the conditioning correction's FP64 product W^T R
- *                        (cr_krige_correct, cr_correct_calibrate): CR_GEMM_DF (default)
- *                        double-float on the FP32 units; CR_GEMM_OZAKI the Ozaki scheme on the
- *                        FP16 tensor cores (Ozaki, Ogita, Oishi, Rump, Numer. Algorithms 59,
- *                        2012): each operand column cut into 8 slices of 6 bits below a power of
- *                        two, the 36 leading slice products computed exactly (FP16 inputs,
- *                        FP32 accumulation over chunks of at most 4096 rows), one GEMM per
- *                        level of significance, and summed in double-float.  With it
- *                        cr_correct_calibrate writes S to stream-ordered scratch.
+ *  CR_OPT_FP64_GEMM      arithmetic of the FP64-class products of the conditioning correction
+ *                        (cr_krige_correct, cr_correct_calibrate) and of cr_krige's triangular
+ *                        solves with many right-hand sides: CR_GEMM_DF (default) double-float
+ *                        on the FP32 units for the correction and FP64 for the solves;
+ *                        CR_GEMM_OZAKI the Ozaki scheme on the FP16 tensor cores (Ozaki, Ogita,
+ *                        Oishi, Rump, Numer. Algorithms 59, 2012): each operand column cut into
+ *                        S slices of 6 bits below a power of two (S = 8 for the correction,
+ *                        9 for the solves), the slice products with s + t <= S + 1 computed
+ *                        exactly (FP16 inputs, FP32 accumulation over chunks of at most 4096
+ *                        rows), one GEMM per level of significance, and summed in double-float.
+ *                        With it cr_correct_calibrate writes S to pooled scratch, and cr_krige
+ *                        holds two dense n_o x n_o copies of the factor during its solves.
  * cr_set_option returns CR_ERR_ARG for an unknown option or a value out of range. */
 enum { CR_OPT_WAIT_LIMIT_US = 1, CR_OPT_DIAG_ARITH = 2, CR_OPT_FP64_GEMM = 4 };
 enum { CR_DIAG_AUTO = 0, CR_DIAG_FP64 = 1, CR_DIAG_DF = 2 };
