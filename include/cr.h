@@ -360,12 +360,12 @@ cr_status cr_calibrate_negative(const double* d_S, int lds, int n_p, int M, cons
  * Limits: M <= CR_NOALLOC_MAX_M and 8 n_p + 16 M + 16 ceil(n_p / 2048) M + 1536 bytes
  * <= CR_NOALLOC_SCRATCH_BYTES; larger problems return CR_ERR_ARG (use cr_calibrate).
  * The first call on a device looks up the array's device address (once per device, with
- * that device current), so make the first call before any stream capture.  All calls
- * share the one array and the one host buffer: calls that overlap (two host threads, or
- * two devices at once) race and must be serialised by the caller.  A call returns only after
- * its last kernel (the region flags, which read the array) has finished on the stream, so
- * calls issued one after another, even on different streams, do not overlap on the GPU.
- * Synchronises the stream. */
+ * that device current).  All calls share the one array and the one host buffer; the library
+ * serialises them with a process-wide lock, and a call returns only after its last kernel
+ * (the region flags, which read the array) has finished on the stream, so calls from
+ * several host threads or streams never overlap on the array.  Synchronises the stream and
+ * reads the quantile samples on the host: it cannot be called on a stream that is being
+ * captured into a CUDA graph. */
 #define CR_NOALLOC_SCRATCH_BYTES (8u << 20)
 #define CR_NOALLOC_MAX_M 65536
 cr_status cr_calibrate_noalloc(const double* d_S, int lds, int n_p, int M, const double* d_zhat,
