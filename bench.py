@@ -504,17 +504,19 @@ def run_krige(args, world, rank, local):
     oz = None
     if ozaki:
         # one more Ozaki correction with per-part device timing: slicing, the slice GEMMs
-        # (FP16 tensor-core flops: sum over levels L = 2..9 of (L - 1) 2 n_p M n_o', n_o' = n_o
-        # rounded up to 1024) and the exact accumulation (its algorithmic bytes: the chunk
-        # products read once, the double-float accumulator written, read and rewritten per
-        # level, Y_p read and S written by the last level)
+        # (FP16 tensor-core flops: sum over levels L = 2..9 of (L - 1) 2 n_p M n_o', n_o' = c kc
+        # with c = ceil(n_o / 4096) chunks of kc = ceil(n_o / c) rounded up to 128 rows) and the
+        # exact accumulation (its algorithmic bytes: the chunk products read once, the
+        # double-float accumulator written, read and rewritten per level, Y_p read and S written
+        # by the last level)
         cr.timing_reset()
         cr.timing_enable(True)
         cr.krige_correct(W, yo, Y, n_p, n_o, out=S)
         t = {k: cr.timing_read(k)[0] for k in ("k_oz_slice", "oz_gemm", "k_oz_accum")}
         cr.timing_enable(False)
-        kpad = -(-n_o // 1024) * 1024
-        kc = 4096 if kpad % 4096 == 0 else (2048 if kpad % 2048 == 0 else 1024)
+        cpk = -(-n_o // 4096)
+        kc = -(-(-(-n_o // cpk)) // 128) * 128
+        kpad = cpk * kc
         gemm_flops = 36 * 2.0 * n_p * M * kpad
         accum_bytes = (36 * (kpad // kc) * 4 + 128) * n_p * M
         oz = {"slice_ms": t["k_oz_slice"], "gemm_ms": t["oz_gemm"], "accum_ms": t["k_oz_accum"],

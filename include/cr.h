@@ -103,10 +103,12 @@ cr_status cr_kernel_launches(uint64_t* count);
  * scratch pools (one per device).  The conditioning correction takes its scratch from these
  * pools and frees it at the end of each call; the pools keep the freed memory for the next
  * call rather than return it at every synchronisation.  The largest user is the Ozaki
- * product (CR_GEMM_OZAKI): 16 n_o' (n_p + M) bytes of slices (n_o' = n_o rounded up to
- * 1024), up to 128 n_p M bytes of chunk products (at most 2 GiB), 8 n_o M + 8 n_p M more,
- * and S (8 n_p M) in cr_correct_calibrate; cr_krige_correct with CR_GEMM_DF takes
- * 8 n_o (n_p + M) bytes.  Memory still used by work in flight stays in the pool.  No device
+ * product (CR_GEMM_OZAKI): 16 n_o' (n_p + M_b) bytes of slices (n_o' = n_o rounded up to
+ * whole chunks of at most 4096 rows, by less than 128 rows per chunk; M_b the columns of one
+ * block, all M unless a level's chunk products for all M would exceed 2 GiB), 2 GiB of chunk
+ * products at most (one chunk's 4 n_p M_b bytes when that is more), 8 n_p M_b bytes of
+ * accumulator, 8 n_o M bytes for R, and S (8 n_p M) in cr_correct_calibrate;
+ * cr_krige_correct with CR_GEMM_DF takes 8 n_o (n_p + M) bytes.  Memory still used by work in flight stays in the pool.  No device
  * work; does not synchronise. */
 cr_status cr_workspace_trim(void);
 

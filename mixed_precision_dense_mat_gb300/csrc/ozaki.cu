@@ -199,15 +199,17 @@ unsigned grid_for(size_t total) {
 // Cout = Cin + alpha A^T B by the Ozaki product with S slices of 6 bits per operand column
 // (A: K x m, ld lda; B: K x n, ld ldb; Cin, Cout: m x n, ld ldci / ldco; Cin NULL for zero;
 // Cout may equal Cin with the same ld, and may overlap A or B, which are sliced before Cout is
-// written).  The kept products are those with s + t <= S + 1, one GEMM per level.  Scratch
-// from the library pool: the slices (S K' (m + n) FP16, K' = K rounded up to 1024), the chunk
-// products (at most 32 m n FP32, fewer when that exceeds 2 GiB) and the accumulator (m n
-// double-float pairs).
+// written).  The kept products are those with s + t <= S + 1, one GEMM per level.  The inner
+// dimension is cut into c = ceil(K / 4096) chunks of kc rows (K / c rounded up to 128, so at
+// most 4096), K' = c kc; A's slices are made once, B's per block of output columns, the blocks
+// as wide as keeps the chunk products of one level within 2 GiB.  Scratch from the library
+// pool: the slices (S K' (m + nbc) FP16), the chunk products (at most 32 m nbc FP32) and the
+// accumulator (m nbc double-float pairs), nbc the block width.
 cr_status ozaki_gemm_tn(const double* A, int lda, const double* B, int ldb, int K, int m_, int n_, double alpha,
                         const double* Cin, int ldci, double* Cout, int ldco, int S, cudaStream_t stream) {
   if (S < OZ_MIN_SLICES || S > OZ_MAX_SLICES) return fail(CR_ERR_ARG, "Ozaki product: slice count");
   if (m_ <= 0 || n_ <= 0) return CR_OK;
-  const size_t m = (size_t)m_, n = (size_t)n_;
+  const size_t m = (size_t)m_;
   if (K <= 0) {
     k_oz_copy<<<grid2d(m_, n_), 256, 0, stream>>>(Cin, ldci, m_, n_, Cout, ldco);
     CR_CHECK_LAUNCH("k_oz_copy");
@@ -216,81 +218,91 @@ cr_status ozaki_gemm_tn(const double* A, int lda, const double* B, int ldb, int 
   std::lock_guard<std::mutex> lk(g_cublas_mu);
   cublasHandle_t h = nullptr;
   CR_TRY(cublas_for(stream, &h));
-  const int kpad = (K + 1023) / 1024 * 1024;
-  // chunk rows: a divisor of kpad, so that no chunk spans two slices
-  const int kc = kpad % OZ_KC_MAX == 0 ? OZ_KC_MAX : (kpad % 2048 == 0 ? 2048 : 1024);
+  const int cpk = (K + OZ_KC_MAX - 1) / OZ_KC_MAX;                   // chunks per slice
+  const int kc = ((K + cpk - 1) / cpk + 127) / 128 * 128, kpad = cpk * kc;
   const size_t ldk = (size_t)S * kpad;
-  const int group = (int)std::max<size_t>(1, std::min<size_t>(OZ_GROUP, ((size_t)1 << 31) / (m * n * sizeof(float))));
+  const int group = std::min(OZ_GROUP, S * cpk);                     // chunks per GEMM call
+  const size_t budget = (size_t)1 << 31;
+  const int nbc = (int)std::max<size_t>(1, std::min<size_t>((size_t)n_, budget / (m * group * sizeof(float))));
   int *Ea = nullptr, *Eb = nullptr;
   __half *As = nullptr, *Bs = nullptr;
   float* P = nullptr;
   float2* C = nullptr;
   auto alloc = [&](void** p, size_t bytes) { return scratch_alloc(p, bytes, stream); };
   cudaError_t e = cudaSuccess;
-  if ((e = alloc((void**)&Ea, m * sizeof(int))) != cudaSuccess || (e = alloc((void**)&Eb, n * sizeof(int))) != cudaSuccess ||
+  if ((e = alloc((void**)&Ea, m * sizeof(int))) != cudaSuccess || (e = alloc((void**)&Eb, nbc * sizeof(int))) != cudaSuccess ||
       (e = alloc((void**)&As, ldk * m * sizeof(__half))) != cudaSuccess ||
-      (e = alloc((void**)&Bs, ldk * n * sizeof(__half))) != cudaSuccess ||
-      (e = alloc((void**)&P, (size_t)group * m * n * sizeof(float))) != cudaSuccess ||
-      (e = alloc((void**)&C, m * n * sizeof(float2))) != cudaSuccess) {
+      (e = alloc((void**)&Bs, ldk * nbc * sizeof(__half))) != cudaSuccess ||
+      (e = alloc((void**)&P, (size_t)group * m * nbc * sizeof(float))) != cudaSuccess ||
+      (e = alloc((void**)&C, m * nbc * sizeof(float2))) != cudaSuccess) {
     for (void* p : {(void*)Ea, (void*)Eb, (void*)As, (void*)Bs, (void*)P, (void*)C}) scratch_free(p, stream);
     return fail(CR_ERR_NOMEM, std::string("Ozaki product: scratch: ") + cudaGetErrorName(e));
   }
+  auto slice = [&](const double* X, int ld, int cols, const int* E, int rev, __half* out) {
+    const dim3 g = grid2d(kpad, cols);
+    switch (S) {
+      case 2: k_oz_slice<2><<<g, 256, 0, stream>>>(X, ld, K, kpad, cols, E, rev, out); break;
+      case 3: k_oz_slice<3><<<g, 256, 0, stream>>>(X, ld, K, kpad, cols, E, rev, out); break;
+      case 4: k_oz_slice<4><<<g, 256, 0, stream>>>(X, ld, K, kpad, cols, E, rev, out); break;
+      case 5: k_oz_slice<5><<<g, 256, 0, stream>>>(X, ld, K, kpad, cols, E, rev, out); break;
+      case 6: k_oz_slice<6><<<g, 256, 0, stream>>>(X, ld, K, kpad, cols, E, rev, out); break;
+      case 7: k_oz_slice<7><<<g, 256, 0, stream>>>(X, ld, K, kpad, cols, E, rev, out); break;
+      case 8: k_oz_slice<8><<<g, 256, 0, stream>>>(X, ld, K, kpad, cols, E, rev, out); break;
+      case 9: k_oz_slice<9><<<g, 256, 0, stream>>>(X, ld, K, kpad, cols, E, rev, out); break;
+      default: k_oz_slice<10><<<g, 256, 0, stream>>>(X, ld, K, kpad, cols, E, rev, out); break;
+    }
+    count_launch();
+  };
   cr_status st = CR_OK;
   do {
     {
-      TimedScope ts("k_oz_slice", stream);   // exponents and slices of both operands
+      TimedScope ts("k_oz_slice", stream);   // exponents and slices of A
       k_oz_colexp<<<(unsigned)m, 256, 0, stream>>>(A, lda, K, Ea);
       count_launch();
-      k_oz_colexp<<<(unsigned)n, 256, 0, stream>>>(B, ldb, K, Eb);
-      count_launch();
-      auto slice = [&](const double* X, int ld, int cols, const int* E, int rev, __half* out) {
-        const dim3 g = grid2d(kpad, cols);
-        switch (S) {
-          case 2: k_oz_slice<2><<<g, 256, 0, stream>>>(X, ld, K, kpad, cols, E, rev, out); break;
-          case 3: k_oz_slice<3><<<g, 256, 0, stream>>>(X, ld, K, kpad, cols, E, rev, out); break;
-          case 4: k_oz_slice<4><<<g, 256, 0, stream>>>(X, ld, K, kpad, cols, E, rev, out); break;
-          case 5: k_oz_slice<5><<<g, 256, 0, stream>>>(X, ld, K, kpad, cols, E, rev, out); break;
-          case 6: k_oz_slice<6><<<g, 256, 0, stream>>>(X, ld, K, kpad, cols, E, rev, out); break;
-          case 7: k_oz_slice<7><<<g, 256, 0, stream>>>(X, ld, K, kpad, cols, E, rev, out); break;
-          case 8: k_oz_slice<8><<<g, 256, 0, stream>>>(X, ld, K, kpad, cols, E, rev, out); break;
-          case 9: k_oz_slice<9><<<g, 256, 0, stream>>>(X, ld, K, kpad, cols, E, rev, out); break;
-          default: k_oz_slice<10><<<g, 256, 0, stream>>>(X, ld, K, kpad, cols, E, rev, out); break;
-        }
-        count_launch();
-      };
       slice(A, lda, m_, Ea, 0, As);
-      slice(B, ldb, n_, Eb, 1, Bs);
     }
-    if ((e = cudaGetLastError()) != cudaSuccess) { st = fail(CR_ERR_CUDA, cudaGetErrorName(e)); break; }
     const float one = 1.0f, zero = 0.0f;
-    const dim3 ga = grid2d(m_, n_);
-    bool first = true;
-    // least significant level first
-    for (int lev = S + 1; lev >= 2 && st == CR_OK; --lev) {
-      // rows of the concatenated product: A slots 0 .. lev-2, B slots S-lev+1 .. S-1
-      const int nchunk = (lev - 1) * kpad / kc;
-      const __half* a0 = As;
-      const __half* b0 = Bs + (size_t)(S - lev + 1) * kpad;
-      for (int g0 = 0; g0 < nchunk; g0 += group) {
-        const int cnt = std::min(group, nchunk - g0);
-        // P_c = A_lev[chunk g0 + c]^T B_lev[chunk g0 + c], c < cnt (m x n each, exact)
-        cublasStatus_t cs;
-        {
-          TimedScope tg("oz_gemm", stream);
-          cs = cublasGemmStridedBatchedEx(h, CUBLAS_OP_T, CUBLAS_OP_N, m_, n_, kc, &one, a0 + (size_t)g0 * kc, CUDA_R_16F,
-                                          (int)ldk, kc, b0 + (size_t)g0 * kc, CUDA_R_16F, (int)ldk, kc, &zero, P, CUDA_R_32F,
-                                          m_, (long long)(m * n), cnt, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
-        }
-        if (cs != CUBLAS_STATUS_SUCCESS) {
-          st = fail(CR_ERR_CUDA, "Ozaki product: cublasGemmStridedBatchedEx failed (" + std::to_string((int)cs) + ")");
-          break;
-        }
-        const bool last = lev == 2 && g0 + cnt >= nchunk;
-        TimedScope ts("k_oz_accum", stream);
-        k_oz_accum<<<ga, 256, 0, stream>>>(P, cnt, m_, n_, Ea, Eb, OZ_BITS * lev, C, first ? 1 : 0, last ? 1 : 0, alpha,
-                                           Cin, ldci, Cout, ldco);
+    for (int j0 = 0; j0 < n_ && st == CR_OK; j0 += nbc) {
+      const int w = std::min(nbc, n_ - j0);
+      const double* Bj = B + (size_t)j0 * ldb;
+      {
+        TimedScope ts("k_oz_slice", stream);   // exponents and slices of this block of B
+        k_oz_colexp<<<(unsigned)w, 256, 0, stream>>>(Bj, ldb, K, Eb);
         count_launch();
-        first = false;
+        slice(Bj, ldb, w, Eb, 1, Bs);
+      }
+      if ((e = cudaGetLastError()) != cudaSuccess) { st = fail(CR_ERR_CUDA, cudaGetErrorName(e)); break; }
+      const dim3 ga = grid2d(m_, w);
+      const double* Cin_j = Cin ? Cin + (size_t)j0 * ldci : nullptr;
+      double* Cout_j = Cout + (size_t)j0 * ldco;
+      bool first = true;
+      // least significant level first
+      for (int lev = S + 1; lev >= 2 && st == CR_OK; --lev) {
+        // rows of the concatenated product: A slots 0 .. lev-2, B slots S-lev+1 .. S-1
+        const int nchunk = (lev - 1) * cpk;
+        const __half* a0 = As;
+        const __half* b0 = Bs + (size_t)(S - lev + 1) * kpad;
+        for (int g0 = 0; g0 < nchunk; g0 += group) {
+          const int cnt = std::min(group, nchunk - g0);
+          // P_c = A_lev[chunk g0 + c]^T B_lev[chunk g0 + c], c < cnt (m x w each, exact)
+          cublasStatus_t cs;
+          {
+            TimedScope tg("oz_gemm", stream);
+            cs = cublasGemmStridedBatchedEx(h, CUBLAS_OP_T, CUBLAS_OP_N, m_, w, kc, &one, a0 + (size_t)g0 * kc, CUDA_R_16F,
+                                            (int)ldk, kc, b0 + (size_t)g0 * kc, CUDA_R_16F, (int)ldk, kc, &zero, P,
+                                            CUDA_R_32F, m_, (long long)(m * w), cnt, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
+          }
+          if (cs != CUBLAS_STATUS_SUCCESS) {
+            st = fail(CR_ERR_CUDA, "Ozaki product: cublasGemmStridedBatchedEx failed (" + std::to_string((int)cs) + ")");
+            break;
+          }
+          const bool last = lev == 2 && g0 + cnt >= nchunk;
+          TimedScope ts("k_oz_accum", stream);
+          k_oz_accum<<<ga, 256, 0, stream>>>(P, cnt, m_, w, Ea, Eb, OZ_BITS * lev, C, first ? 1 : 0, last ? 1 : 0, alpha,
+                                             Cin_j, ldci, Cout_j, ldco);
+          count_launch();
+          first = false;
+        }
       }
     }
     if (st != CR_OK) break;

@@ -67,9 +67,9 @@ def _bound(W, R, S, n_o):
                                              (64, 4000, 33, 1.0), (100, 6000, 40, 1.0)])
 def test_ozaki_correction_matches_oracle(lib, n_p, n_o, M, scale):
     """Element by element within the bound above, on ragged sizes (n_o not a multiple of the
-    1024-row padding: the padding slices are zero; n_o = 2100 pads to 3072 rows in chunks of
-    1024, 4000 to one 4096-row chunk per slice, 6000 to 6144 rows in chunks of 2048, so each
-    level's product spans several chunks and slices) and with columns of W spanning several orders
+    128-row padding of the chunks: the padding slices are zero; n_o = 2100 is one chunk of 2176
+    rows per slice, 4000 one of 4096, 6000 two of 3072, so each level's product spans several
+    chunks and slices) and with columns of W spanning several orders
     of magnitude (as kriging weights do)."""
     rng = np.random.default_rng(n_p + n_o)
     W = rng.standard_normal((n_o, n_p)) * scale * np.exp(rng.uniform(-8, 2, n_p))[None, :]
@@ -152,9 +152,9 @@ def test_pooled_scratch_reused_and_trimmed(lib):
 
 def test_ozaki_full_size_sampled_rows(lib):
     """The kriging workload's shape (16384 observations, 16384 prediction sites) with 1100
-    simulations: 4096-row chunks, and the chunk products of the least significant levels no
-    longer fit one 2 GiB batch, so those levels take two GEMM calls each.  Sampled rows of S
-    against the oracle within the bound."""
+    simulations: 4096-row chunks, and the chunk products of a level for all 1100 columns no
+    longer fit the 2 GiB budget, so the product runs in two blocks of columns (1024 and 76).
+    Sampled rows of S against the oracle within the bound."""
     rng = np.random.default_rng(77)
     n_p, n_o, M = 16384, 16384, 1100
     W = rng.standard_normal((n_o, n_p)) * np.exp(rng.uniform(-6, 1, n_p))[None, :]
