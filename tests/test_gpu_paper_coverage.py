@@ -1,7 +1,8 @@
 """The pages' coverage study at their own size ("Mixed-Precision GPU Acceleration for Confidence
 Regions of Spatial Excursion Sets", Section VI-B.2 and Fig. 3): 1000 replicates per correlation
-level, nsim = 80,000 conditional simulations each, adaptive mixed precision with the automatic tolerance (A7: the
-map refined until the FP16 checks pass), or at a fixed tolerance (CR_PAPER_COVERAGE_FIXEDACC).
+level, nsim = 80,000 conditional simulations each, adaptive mixed precision with the automatic
+tolerance (A7: the map refined until the FP16 checks pass), or at a fixed tolerance
+(CR_PAPER_COVERAGE_FIXEDACC).
 
 Geometry of Section VI-B.1: 3200 uniform observations (one fixed seed) and a 120 x 120 grid of
 prediction cells (n = 17,600), power-exponential covariance (sigma^2 = 1, nu = 0.5, range 0.033,
@@ -96,9 +97,10 @@ def test_paper_coverage_study(lib, beta):
     G16.close()
     p = hits / R_REPLICATES
     h = 1.96 * np.sqrt(p * (1.0 - p) / R_REPLICATES)
+    mode = "fixed" if FIXEDACC else "automatic"
     msg = (f"range {beta}: coverage {p:.3f} [{p - h:.3f}, {p + h:.3f}] over {R_REPLICATES} replicates of {NSIM} "
-           f"simulations, {'fixed' if FIXEDACC else 'automatic'} tolerance {info['fixedacc']:g}, tiles fp64/32/16 {info['n_fp64']}/{info['n_fp32']}/{info['n_fp16']}, "
-           f"{secs / R_REPLICATES:.3f} s per replicate")
+           f"simulations, {mode} tolerance {info['fixedacc']:g}, tiles fp64/32/16 "
+           f"{info['n_fp64']}/{info['n_fp32']}/{info['n_fp16']}, {secs / R_REPLICATES:.3f} s per replicate")
     print(msg)
     # the pages report coverages of about 0.83-0.91 for this study (Fig. 3); 0.80-0.95 leaves
     # three binomial standard errors on either side at 1000 replicates
