@@ -249,7 +249,11 @@ cr_status cr_potrf_adaptive(cr_tilemat V, cr_stream stream, int* info);
 /* Copies the tile matrix into a dense n x n column-major FP64 matrix (lower triangle;
  * the strict upper triangle is set to zero).  what = 0: the covariance V built by
  * cr_cov_build; what = 1: the current working tiles as stored in their precision
- * (after cr_potrf_adaptive: the factor L_s).  Asynchronous. */
+ * (after cr_potrf_adaptive: the factor L_s); what = 2: first runs the generation step of
+ * cr_potrf_adaptive alone (Alg.2 step 12: the tiles of s^2 V written in their precision
+ * classes, diagonal tiles as cr_potrf_adaptive would generate them), then copies as for
+ * what = 1; it replaces any factor (factor again before cr_trmm_sim) and synchronises.
+ * what = 1 and 2 need cr_precision_map first.  Asynchronous for what = 0 and 1. */
 cr_status cr_tilemat_to_dense(cr_tilemat V, int what, double* d_out, int ld, cr_stream stream);
 
 /* n x M standard normals (column-major, ldz >= n) from the library's counter-based

@@ -944,12 +944,42 @@ extern "C" cr_status cr_tile_stats_records(cr_tilemat V, double* h_frob, double*
 }
 
 extern "C" cr_status cr_tilemat_to_dense(cr_tilemat V, int what, double* d_out, int ld, cr_stream stream) {
-  if (!V || !d_out || ld < V->n || (what != 0 && what != 1)) return fail(CR_ERR_ARG, "cr_tilemat_to_dense: argument");
+  if (!V || !d_out || ld < V->n || what < 0 || what > 2) return fail(CR_ERR_ARG, "cr_tilemat_to_dense: argument");
   if (what == 0 && !V->built) return fail(CR_ERR_STATE, "cr_tilemat_to_dense: covariance not built");
-  if (what == 1 && !V->mapped) return fail(CR_ERR_STATE, "cr_tilemat_to_dense: no working tiles yet");
+  if (what >= 1 && !V->mapped) return fail(CR_ERR_STATE, "cr_tilemat_to_dense: no working tiles yet");
   CR_CUDA(cudaSetDevice(V->device));
+  if (what == 2) {
+    // the generation step of cr_potrf_adaptive alone, over every tile: diagonal tiles first,
+    // then the FP64/FP32-class tiles, then the FP16-class ones (the launch's expected order),
+    // the diagonal ones in double-float when the double-float executor would factor them
+    const int nt = V->nt;
+    std::vector<int> list;
+    for (int i = 0; i < nt; ++i) list.push_back(i << 16 | i);
+    int nheavy = 0;
+    for (int pass = 0; pass < 2; ++pass)
+      for (int i = 0; i < nt; ++i)
+        for (int j = 0; j < i; ++j) {
+          const bool heavy = V->h_cls[tidx(i, j)] != CR_PREC_FP16;
+          if (heavy == (pass == 0)) {
+            list.push_back(i << 16 | j);
+            nheavy += heavy ? 1 : 0;
+          }
+        }
+    const int arith = option_diag_arith();
+    const bool use_df = arith == CR_DIAG_DF || (arith == CR_DIAG_AUTO && V->amp);
+    int* d_list = nullptr;
+    CR_CUDA(cudaMallocAsync(&d_list, list.size() * sizeof(int), stream));
+    const cudaError_t ce = cudaMemcpyAsync(d_list, list.data(), list.size() * sizeof(int), cudaMemcpyHostToDevice, stream);
+    cr_status st = ce == cudaSuccess ? convert_tiles(V, d_list, (int)list.size(), nt, nheavy, use_df, stream)
+                                     : cuda_fail(ce, "cr_tilemat_to_dense: tile list");
+    cudaFreeAsync(d_list, stream);
+    // the list is copied from host memory that goes out of scope here
+    CR_CUDA(cudaStreamSynchronize(stream));
+    CR_TRY(st);
+    V->factored = false;   // the storage now holds s^2 V, not the factor
+  }
   dim3 grid((V->n + 31) / 32, 64);
-  k_to_dense<<<grid, 256, 0, stream>>>(V->xy, V->covk, V->view(), what, d_out, ld);
+  k_to_dense<<<grid, 256, 0, stream>>>(V->xy, V->covk, V->view(), what == 0 ? 0 : 1, d_out, ld);
   CR_CHECK_LAUNCH("k_to_dense");
   return CR_OK;
 }

@@ -43,8 +43,13 @@ namespace {
 constexpr int OZ_BITS = 6, OZ_MIN_SLICES = 2, OZ_MAX_SLICES = 10, OZ_KC_MAX = 4096, OZ_GROUP = 32;
 constexpr unsigned long long OZ_MASK = (1ull << OZ_BITS) - 1ull;
 
+// Exponent marking a column with an infinite or NaN entry: its slices are zero and every output
+// it touches is NaN (as in an FP64 product, where the entry reaches all of them).
+constexpr int OZ_NONFINITE = 0x7fffffff;
+
 // E_c with max_r |X_rc| < 2^E_c (positive doubles order as their bit patterns); 0 for a zero
-// column (its slices are all zero).  One CTA per column.
+// column (its slices are all zero); OZ_NONFINITE for a column holding an infinity or a NaN.
+// One CTA per column.
 __global__ void __launch_bounds__(256) k_oz_colexp(const double* __restrict__ X, int ld, int rows, int* __restrict__ E) {
   const int c = blockIdx.x;
   unsigned long long m = 0ull;
@@ -63,7 +68,7 @@ __global__ void __launch_bounds__(256) k_oz_colexp(const double* __restrict__ X,
     for (int w = 1; w < 8; ++w) m = red[w] > m ? red[w] : m;
     const int eb = (int)(m >> 52);   // biased exponent of the largest |entry|
     // a normal value lies in [2^(eb-1023), 2^(eb-1022)); a subnormal one below 2^-1022
-    E[c] = m == 0ull ? 0 : (eb == 0 ? -1022 : eb - 1022);
+    E[c] = m == 0ull ? 0 : (eb == 0x7ff ? OZ_NONFINITE : (eb == 0 ? -1022 : eb - 1022));
   }
 }
 
@@ -80,7 +85,7 @@ __global__ void __launch_bounds__(256) k_oz_slice(const double* __restrict__ X, 
     for (int r = blockIdx.x * 256 + threadIdx.x; r < rows_pad; r += gridDim.x * 256) {
       unsigned long long q = 0ull;
       bool neg = false;
-      if (r < rows) {
+      if (r < rows && Ec != OZ_NONFINITE) {
         const unsigned long long b = (unsigned long long)__double_as_longlong(X[(size_t)c * ld + r]);
         neg = (b >> 63) != 0;
         const int eb = (int)((b >> 52) & 0x7ff);
@@ -128,7 +133,7 @@ __global__ void __launch_bounds__(256) k_oz_accum(const float* __restrict__ P, i
                                                   const double* Cin, int ldci, double* Cout, int ldco) {
   const size_t mn = (size_t)m * n;
   for (int j = blockIdx.y; j < n; j += gridDim.y) {
-    const int ej = Eb[j] - shift;
+    const int ej = Eb[j] == OZ_NONFINITE ? 0 : Eb[j] - shift;
     for (int i = blockIdx.x * 256 + threadIdx.x; i < m; i += gridDim.x * 256) {
       const size_t e = (size_t)j * m + i;
       const float* p = P + e;
@@ -137,8 +142,11 @@ __global__ void __launch_bounds__(256) k_oz_accum(const float* __restrict__ P, i
       for (int b = 0; b < nb; ++b) v += __float2int_rn(p[(size_t)b * mn]);
       const float h = (float)v;                   // nearest FP32 of v (|v| < 2^29)
       const float l = (float)(v - (int)h);        // the rest, below 2^5: exact
-      const int ex = Ea[i] + ej;
+      const int ea = Ea[i];
+      const bool nonfinite = ea == OZ_NONFINITE || Eb[j] == OZ_NONFINITE;
+      const int ex = nonfinite ? 0 : ea + ej;
       df acc = {oz_scale(h, ex), oz_scale(l, ex)};
+      if (nonfinite) acc = {__int_as_float(0x7fc00000), 0.0f};   // NaN
       if (!first) {
         const float2 c = C[e];
         acc = df_add({c.x, c.y}, acc);

@@ -24,7 +24,7 @@ from .krige import universal_kriging, conditional_correction
 from .calibrate import (standardized_statistic, extrema_scan, exceedance_counts,
                         empirical_quantile, sample_without_sentinels, confidence_regions,
                         EmptySample, calibrate, calibrate_negative)
-from .coverage import truth_field, excursion_set, coverage_event
+from .coverage import truth_field, excursion_set, coverage_event, inner_event, outer_event
 
 __all__ = [
     "matern", "powexp", "covariance_fn", "covariance_matrix", "covariance_entries",
@@ -34,5 +34,5 @@ __all__ = [
     "simulate", "simulate_fp16_per_product", "splitmix64", "rnorm", "universal_kriging", "conditional_correction",
     "standardized_statistic", "extrema_scan", "exceedance_counts", "empirical_quantile",
     "sample_without_sentinels", "confidence_regions", "EmptySample", "calibrate", "calibrate_negative",
-    "truth_field", "excursion_set", "coverage_event",
+    "truth_field", "excursion_set", "coverage_event", "inner_event", "outer_event",
 ]

@@ -7,7 +7,9 @@
     the tau^2 already on V's observation block (the reading taken for the noise).
   * §VI-B.2 / Fig. 3: the excursion set of the truth over the prediction sites is
     A = {i in D_p : Z_i >= u}; a replicate succeeds when C_in is inside A and A is inside
-    C_out.  The empirical coverage is the fraction of successful replicates.
+    C_out.  The empirical coverage is the fraction of successful replicates.  Fig. 3 plots
+    an inner coverage rate (panel a) and an outer one (panel b): the fractions of replicates
+    with C_in inside A, and with A inside C_out, each on its own.
   * §III: for a negative excursion set the truth's set is {i : Z_i <= u} (the positive set
     of the sign-reversed field at -u).
 """
@@ -35,3 +37,15 @@ def coverage_event(truth_p: np.ndarray, c_in, c_out, u: float, negative: bool = 
     inner = np.asarray(c_in).astype(bool)
     outer = np.asarray(c_out).astype(bool)
     return bool(np.all(A[inner]) and np.all(outer[A]))
+
+
+def inner_event(truth_p: np.ndarray, c_in, u: float, negative: bool = False) -> bool:
+    """True when C_in is a subset of A (the inner region's event of Fig. 3a)."""
+    A = excursion_set(truth_p, u, negative)
+    return bool(np.all(A[np.asarray(c_in).astype(bool)]))
+
+
+def outer_event(truth_p: np.ndarray, c_out, u: float, negative: bool = False) -> bool:
+    """True when A is a subset of C_out (the outer region's event of Fig. 3b)."""
+    A = excursion_set(truth_p, u, negative)
+    return bool(np.all(np.asarray(c_out).astype(bool)[A]))

@@ -66,7 +66,7 @@ def test_coverage_study(lib, M, with_oracle):
         Wo, _, vo = oracle.universal_kriging(V[n_p:, n_p:], V[n_p:, :n_p], X[n_p:], X[:n_p], np.zeros(n_o), 1.0)
     zeros_p, zeros_o = np.zeros((n_p, 1)), np.zeros((n_o, 1))
 
-    hits_gpu = hits_oracle = 0
+    hits_gpu = hits_oracle = inner_gpu = outer_gpu = 0
     region_diff = []
     for r in range(R_REPLICATES):
         truth = oracle.truth_field(Lv, X, b, inputgen.standard_normals(n, 1, 1000 + r)[:, 0])
@@ -82,6 +82,8 @@ def test_coverage_study(lib, M, with_oracle):
         out = lib.correct_calibrate(W, dev(y), Y, n_p, n_o, z, v, u, level)
         c_in, c_out = out["c_in"].cpu().numpy(), out["c_out"].cpu().numpy()
         hits_gpu += oracle.coverage_event(truth[:n_p], c_in, c_out, u)
+        inner_gpu += oracle.inner_event(truth[:n_p], c_in, u)
+        outer_gpu += oracle.outer_event(truth[:n_p], c_out, u)
         if with_oracle:
             # oracle chain on the same truth and draws
             zo = oracle.conditional_correction(Wo, y, zeros_p, zeros_o)[:, 0]
@@ -92,7 +94,8 @@ def test_coverage_study(lib, M, with_oracle):
             region_diff.append(max(np.mean(c_in != ref["c_in"]), np.mean(c_out != ref["c_out"])))
     G.close()
     p, lo, hi = _binomial_interval(hits_gpu, R_REPLICATES)
-    msg = (f"M = {M}, {R_REPLICATES} replicates: coverage gpu {p:.3f} [{lo:.3f}, {hi:.3f}]; tiles fp64/32/16 "
+    msg = (f"M = {M}, {R_REPLICATES} replicates: coverage gpu {p:.3f} [{lo:.3f}, {hi:.3f}] (inner "
+           f"{inner_gpu / R_REPLICATES:.3f}, outer {outer_gpu / R_REPLICATES:.3f}); tiles fp64/32/16 "
            f"{info['n_fp64']}/{info['n_fp32']}/{info['n_fp16']}")
     if with_oracle:
         po, loo, hio = _binomial_interval(hits_oracle, R_REPLICATES)

@@ -132,6 +132,33 @@ def test_ozaki_correct_calibrate_matches_unfused(lib, negative):
     np.testing.assert_array_equal(b["c_out"].cpu().numpy(), ref["c_out"])
 
 
+def test_ozaki_nonfinite_operands_give_nan(lib):
+    """A NaN or an infinity in W (or in R = y_o 1^T - M_o) reaches, in an FP64 product, every
+    output of its column of W (row of S) or of R (column of S): the Ozaki product makes exactly
+    those outputs NaN and leaves the others as they are without the bad entry's column."""
+    rng = np.random.default_rng(13)
+    n_p, n_o, M = 150, 700, 40
+    W = rng.standard_normal((n_o, n_p)) * 0.1
+    y = rng.standard_normal(n_o)
+    Y = rng.standard_normal((n_p + n_o, M))
+    W[17, 5] = np.nan
+    W[300, 80] = np.inf
+    Y[n_p + 9, 33] = -np.inf
+    with gemm_mode(lib, lib.CR_GEMM_OZAKI):
+        S = lib.krige_correct(colmajor(W), dev(y), colmajor(Y), n_p, n_o).cpu().numpy()
+    bad = np.zeros((n_p, M), dtype=bool)
+    bad[[5, 80], :] = True
+    bad[:, 33] = True
+    assert np.all(np.isnan(S[bad]))
+    Wc, Yc = W.copy(), Y.copy()
+    Wc[:, [5, 80]] = 0.0
+    Yc[:, 33] = 0.0
+    So = oracle.conditional_correction(Wc, y, Yc[:n_p], Yc[n_p:])
+    R = y[:, None] - Yc[n_p:]
+    b = _bound(Wc, R, So, n_o)
+    assert np.all(np.abs(S[~bad] - So[~bad]) <= b[~bad])
+
+
 def test_pooled_scratch_reused_and_trimmed(lib):
     """The correction's scratch comes from the library pool: repeated calls, and a call after
     cr_workspace_trim has returned the pool's memory, give the same bits."""

@@ -407,6 +407,13 @@ def test_coverage_event_hand_cases_and_set_semantics():
         A = {i for i in range(9) if t[i] >= 0.3}
         want = {i for i in range(9) if ci[i]} <= A <= {i for i in range(9) if co[i]}
         assert oracle.coverage_event(t, ci, co, 0.3) == want
+        # the separate inner and outer events of Fig. 3a/3b, and their conjunction
+        inner = {i for i in range(9) if ci[i]} <= A
+        outer = A <= {i for i in range(9) if co[i]}
+        assert oracle.inner_event(t, ci, 0.3) == inner and oracle.outer_event(t, co, 0.3) == outer
+        assert (inner and outer) == want
+    assert oracle.inner_event(truth, [1, 0, 1, 0], 1.6) and not oracle.inner_event(truth, [0, 1, 0, 0], 1.6)
+    assert oracle.outer_event(truth, [1, 0, 1, 0], 1.6) and not oracle.outer_event(truth, [1, 1, 0, 1], 1.6)
 
 
 def test_truth_field_mean_and_covariance():
