@@ -87,6 +87,22 @@ def test_ozaki_correction_matches_oracle(lib, n_p, n_o, M, scale):
     assert np.linalg.norm(S - So) <= 1e-11 * np.linalg.norm(So)
 
 
+@pytest.mark.parametrize("n_p,n_o,M", [(1, 1, 1), (3, 1, 5), (1, 4097, 1), (7, 129, 2), (2, 8193, 3)])
+def test_ozaki_correction_degenerate_sizes(lib, n_p, n_o, M):
+    """One output, an inner dimension of 1, and inner dimensions just past a 128-row padding step
+    (129) and past one and two 4096-row chunks (4097: two chunks of 2176 rows; 8193: three of
+    2816), within the bound above."""
+    rng = np.random.default_rng(n_p * 100000 + n_o * 10 + M)
+    W = rng.standard_normal((n_o, n_p))
+    y = rng.standard_normal(n_o)
+    Y = rng.standard_normal((n_p + n_o, M))
+    with gemm_mode(lib, lib.CR_GEMM_OZAKI):
+        S = lib.krige_correct(colmajor(W), dev(y), colmajor(Y), n_p, n_o).cpu().numpy()
+    So = oracle.conditional_correction(W, y, Y[:n_p], Y[n_p:])
+    R = y[:, None] - Y[n_p:]
+    assert np.all(np.abs(S - So) <= _bound(W, R, So, n_o))
+
+
 def test_ozaki_slices_exact_on_integers(lib):
     """Entries that are small integers times powers of two are represented exactly by their
     slices and every slice product is exact, so the product equals the exact integer result."""
