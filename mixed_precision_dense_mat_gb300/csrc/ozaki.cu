@@ -1,14 +1,14 @@
 // FP64-class matrix product on the FP16 tensor cores by the Ozaki scheme (Ozaki, Ogita, Oishi
 // and Rump, "Error-free transformations of matrix multiplication by using fast routines of
-// matrix multiplication and its applications", Numerical Algorithms 59 (2012)), for the
-// conditioning correction of "Mixed-Precision GPU Acceleration for Confidence Regions of
-// Spatial Excursion Sets" (Section V-B Eq.7: S = M_p + W^T (y_o 1^T - M_o)).
+// matrix multiplication and its applications", Numerical Algorithms 59 (2012)), for two steps of
+// "Mixed-Precision GPU Acceleration for Confidence Regions of Spatial Excursion Sets": the
+// conditioning correction (Section V-B Eq.7: S = M_p + W^T (y_o 1^T - M_o)) and the triangular
+// solves of the kriging weights with many right-hand sides (Section V-A, Alg.2 steps 2-4).
 //
-// C = A^T B with A (k x m) and B (k x n) column-major FP64:
+// C = A^T B with A (k x m) and B (k x n) column-major FP64, S slices per operand column:
 //  - each column c of A gets a power of two 2^Ea_c above its largest |entry| (B likewise), and
-//    |A_rc| 2^(6 S - Ea_c), truncated to an integer below 2^(6 S), is cut into S = 8 slices of
-//    6 bits: A_rc = sum_s a_s,rc 2^(Ea_c - 6 s) + d with |a_s,rc| <= 63 and
-//    |d| < 2^(Ea_c - 48);
+//    |A_rc| 2^(6 S - Ea_c), truncated to an integer below 2^(6 S), is cut into S slices of 6
+//    bits: A_rc = sum_s a_s,rc 2^(Ea_c - 6 s) + d with |a_s,rc| <= 63 and |d| < 2^(Ea_c - 6 S);
 //  - the slice products with s + t = L share the scale 2^(Ea_i + Eb_j - 6 L), so for each
 //    level L = 2 .. S + 1 the L - 1 products are one product over the concatenated rows
 //    [A_1; ...; A_(L-1)]^T [B_(L-1); ...; B_1] (the slices of A stored in order, those of B in
@@ -16,11 +16,13 @@
 //  - that product over a chunk of at most 4096 rows is a sum of at most 4096 integers of
 //    magnitude <= 63^2, below 2^24, so an FP16 tensor-core GEMM with FP32 accumulation computes
 //    it exactly (whatever its summation order);
-//  - the products with s + t <= S + 1 (36 of the 64) are kept: the rest, and the truncations,
-//    are below k 8.95 2^-48 2^(Ea_i + Eb_j) per output (derived in the tests);
+//  - the products with s + t <= S + 1 are kept (36 of 64 for S = 8): the rest, and the
+//    truncations, are below k 8.95 2^-48 2^(Ea_i + Eb_j) per output for S = 8 (derived in the
+//    tests);
 //  - each level's chunk sums, added in 32-bit integers (exact), are scaled by
 //    2^(Ea_i + Eb_j - 6 L) (exact) and added to a double-float accumulator, the least
-//    significant level first; the last addition writes S = M_p + C in FP64.
+//    significant level first; the last addition writes Cout = Cin + alpha C in FP64;
+//  - a column holding an infinity or a NaN makes every output it touches NaN.
 // The slice GEMMs are plain FP16 x FP16 -> FP32 library GEMMs (cuBLAS, strided-batched over the
 // K chunks); slicing, exact accumulation and the final sum are this file's kernels.
 #include <cublas_v2.h>
