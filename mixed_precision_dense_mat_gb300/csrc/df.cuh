@@ -80,7 +80,9 @@ struct DfExpTables {
   float c1, c2, c3;
 };
 
-// exp(y) for -80 <= y <= 0 (callers route larger distances elsewhere).
+// exp(y) for -80 <= y <= 0 (callers route larger distances elsewhere), by Tang's
+// table-driven method (P. T. P. Tang, "Table-driven implementation of the exponential function
+// in IEEE floating-point arithmetic", ACM TOMS 15(2), 1989) carried out in double-float:
 // y = k ln2/64 + r with |r| <= ln2/128, k = 64 m + j; exp(y) = 2^m 2^(j/64) exp(r), and
 // exp(r) = 1 + r + r^2/2 + (r^3/6 + r^4/24 + r^5/120) with the bracket in FP32 (its
 // magnitude is below 3e-8, so its FP32 rounding stays near 1e-15 of the result).
