@@ -422,7 +422,8 @@ def run_krige(args, world, rank, local):
     reported, not in the metric); one step is one batch of M conditional simulations: normal
     draws fused with the mixed-precision TRMM, then the correction with the calibration
     (cr_correct_calibrate: with the double-float product S is never written; with the Ozaki
-    product on the tensor cores, --fp64-gemm ozaki, S goes through scratch).  Metric:
+    product on the tensor cores, --fp64-gemm ozaki, S goes through scratch and W's slices are
+    cut once at setup, cr_weights_prepare, as W itself is computed once).  Metric:
     simulations per second, M / (t_rng + t_trmm + t_correct + t_calibrate).  The separate
     correction + calibration calls are timed beside it."""
     import torch
@@ -455,10 +456,25 @@ def run_krige(args, world, rank, local):
     t_krige, t_chol = e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2])
     Y = cr.colmajor_empty(n, M, torch.float64)
 
+    # the Ozaki product cuts the fixed kriging weights into slices once (cr_weights_prepare),
+    # part of the setup like W itself
+    Wp, t_prep = None, 0.0
+    if ozaki:
+        e[2].record(stream)
+        Wp = cr.Weights(W)
+        e[3].record(stream)
+        torch.cuda.synchronize()
+        t_prep = e[2].elapsed_time(e[3])
+
+    def correct_calibrate():
+        if Wp is not None:
+            return cr.correct_calibrate_prepared(Wp, yo, Y, zhat, v, w.u, w.level)
+        return cr.correct_calibrate(W, yo, Y, n_p, n_o, zhat, v, w.u, w.level)
+
     def step(seed, fused=True):
         cr.trmm_sim(V, None, M, seed=seed, out=Y, flags=cr.CR_TRMM_GENERATE)
         if fused:
-            return cr.correct_calibrate(W, yo, Y, n_p, n_o, zhat, v, w.u, w.level)
+            return correct_calibrate()
         S = cr.krige_correct(W, yo, Y, n_p, n_o)
         return cr.calibrate(S, zhat, v, w.u, w.level)
 
@@ -486,24 +502,31 @@ def run_krige(args, world, rank, local):
     pe[0].record(stream)
     cr.trmm_sim(V, None, M, seed=SEED_Z + 500, out=Y, flags=cr.CR_TRMM_GENERATE)
     pe[1].record(stream)
-    cr.correct_calibrate(W, yo, Y, n_p, n_o, zhat, v, w.u, w.level)
+    correct_calibrate()
     pe[2].record(stream)
     torch.cuda.synchronize()
     parts["rng_trmm"] = pe[0].elapsed_time(pe[1])
     parts["correct_calibrate"] = pe[1].elapsed_time(pe[2])
-    ue = [ev() for _ in range(3)]
+    ue = [ev() for _ in range(5)]
     ue[0].record(stream)
-    S = cr.krige_correct(W, yo, Y, n_p, n_o)
+    S = cr.krige_correct_prepared(Wp, yo, Y) if Wp is not None else cr.krige_correct(W, yo, Y, n_p, n_o)
     ue[1].record(stream)
     cr.calibrate(S, zhat, v, w.u, w.level)
     ue[2].record(stream)
+    if Wp is not None:
+        # the same correction cutting W again (cr_krige_correct), for comparison
+        cr.krige_correct(W, yo, Y, n_p, n_o, out=S)
+    ue[3].record(stream)
     torch.cuda.synchronize()
     parts["correct"] = ue[0].elapsed_time(ue[1])
     parts["calibrate"] = ue[1].elapsed_time(ue[2])
+    if Wp is not None:
+        parts["correct_without_prepared_weights"] = ue[2].elapsed_time(ue[3])
     corr_flops = 2.0 * n_p * n_o * M
     oz = None
     if ozaki:
-        # one more Ozaki correction with per-part device timing: slicing, the slice GEMMs
+        # one more Ozaki correction with per-part device timing: slicing (of R: W's slices are
+        # prepared), the slice GEMMs
         # (FP16 tensor-core flops: sum over levels L = 2..9 of (L - 1) 2 n_p M n_o', n_o' = c kc
         # with c = ceil(n_o / 4096) chunks of kc = ceil(n_o / c) rounded up to 128 rows) and the
         # exact accumulation (its algorithmic bytes: the chunk products read once, the
@@ -511,7 +534,7 @@ def run_krige(args, world, rank, local):
         # by the last level)
         cr.timing_reset()
         cr.timing_enable(True)
-        cr.krige_correct(W, yo, Y, n_p, n_o, out=S)
+        cr.krige_correct_prepared(Wp, yo, Y, out=S)
         t = {k: cr.timing_read(k)[0] for k in ("k_oz_slice", "oz_gemm", "k_oz_accum")}
         cr.timing_enable(False)
         cpk = -(-n_o // 4096)
@@ -529,7 +552,8 @@ def run_krige(args, world, rank, local):
                 "data": "synthetic",
                 "config": {"workload": w.name, "n_pred": n_p, "n_obs": n_o, "nb": nb, "M": M, "fixedacc": w.fixedacc,
                            "u": w.u, "level": w.level, "parallelism": f"replicas x{world}"},
-                "setup_ms": {"covariance_and_kriging": t_krige, "map_and_cholesky": t_chol},
+                "setup_ms": {"covariance_and_kriging": t_krige, "map_and_cholesky": t_chol,
+                             "weights_prepare": t_prep},
                 "parts_ms": parts,
                 "correction_tflops": corr_flops / (parts["correct"] / 1e3) / 1e12,
                 "fp64_gemm": args.fp64_gemm,

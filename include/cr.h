@@ -305,11 +305,15 @@ cr_status cr_krige(cr_tilemat V, const double* d_Xo, const double* d_Xp, const d
 /* Conditioning correction (Section V-B Eq.7): S = M_p + W^T (y_o 1^T - M_o), where the
  * simulations d_Y (n x M column-major, ldy) hold the prediction rows first (M_p = rows
  * [0, n_p), M_o = rows [n_p, n_p + n_o)).  d_S is n_p x M column-major (lds >= n_p).
- * The product runs in double-float arithmetic on the FP32 units (an FP64 emulation with
- * about 48 significant bits; W and R = y_o 1^T - M_o are rounded to double-float pairs, the
- * sum M_p + W^T R is formed in FP64): |S - S_exact| <= (n_o + 8) 2^-46 (|W|^T |R|)_ij +
- * 2^-52 |S_ij|.  Stream-ordered allocation of 8 n_o (n_p + M) bytes of scratch
- * (cudaMallocAsync).  Asynchronous. */
+ * With CR_GEMM_DF (the default, CR_OPT_FP64_GEMM) the product runs in double-float
+ * arithmetic on the FP32 units (an FP64 emulation with about 48 significant bits; W and
+ * R = y_o 1^T - M_o are rounded to double-float pairs, the sum M_p + W^T R is formed in
+ * FP64): |S - S_exact| <= (n_o + 8) 2^-46 (|W|^T |R|)_ij + 2^-52 |S_ij|, with 8 n_o (n_p + M)
+ * bytes of pooled scratch (cr_workspace_trim).  With CR_GEMM_OZAKI it is the Ozaki product on
+ * the FP16 tensor cores: |S - S_exact| <= n_o 9 2^-48 2^(Ea_i + Eb_j) + 16 2^-47 (|W|^T |R|)_ij
+ * + 2^-52 |S_ij| (2^Ea_i, 2^Eb_j the powers of two above the largest magnitudes of column i of
+ * W and column j of R); an infinite or NaN entry of W or R makes its row or column of S NaN.
+ * Asynchronous. */
 cr_status cr_krige_correct(const double* d_W, int ldw, const double* d_yo, const double* d_Y,
                            int ldy, int n_p, int n_o, int M, double* d_S, int lds,
                            cr_stream stream);
@@ -320,12 +324,41 @@ cr_status cr_krige_correct(const double* d_W, int ldw, const double* d_yo, const
  * (n_p x M doubles of HBM traffic saved).  Arguments as in those two calls; the results are
  * identical to cr_calibrate(cr_krige_correct(...)) on the same inputs.  Library-managed
  * scratch, 8 n_o (n_p + M) + 8 n_p + 16 M + 16 ceil(n_p / 64) M bytes, grown on demand and
- * shared by all calls: the call returns after its last kernel.  Synchronises. */
+ * shared by all calls: the call returns after its last kernel.  With CR_GEMM_OZAKI the
+ * correction is the Ozaki product of cr_krige_correct, which writes S to pooled scratch, and
+ * the scan of cr_calibrate reads it.  Synchronises. */
 cr_status cr_correct_calibrate(const double* d_W, int ldw, const double* d_yo, const double* d_Y,
                                int ldy, int n_p, int n_o, int M, const double* d_zhat,
                                const double* d_v, double u, double level, int negative,
                                uint8_t* d_cin, uint8_t* d_cout, int32_t* d_count, double* d_psi,
                                double* d_phi, cr_calib_info* out, cr_stream stream);
+
+/* Kriging weights prepared for repeated conditioning corrections by the Ozaki product (the
+ * paper has no counterpart; Alg.2 computes W once, steps 2-4, and applies it to the simulations
+ * in step 17): the column exponents and the 8 slices of 6 bits of W (n_o x n_p column-major,
+ * ldw >= n_o), made once so that the corrections of successive simulation batches with the
+ * same weights do not cut W again.  cr_weights_prepare allocates 2 n_o' n_p + 4 n_p bytes
+ * with cudaMalloc (n_o' = n_o rounded up to whole chunks, see CR_OPT_FP64_GEMM) and cuts the
+ * slices on `stream` (asynchronous: W may change once the stream has passed this call); the
+ * handle does not read W again.  cr_weights_release frees it (cudaFree, which waits for the
+ * device); NULL is accepted.  The handle belongs to the device that was current at
+ * cr_weights_prepare. */
+typedef struct cr_weights_s* cr_weights;
+cr_status cr_weights_prepare(const double* d_W, int ldw, int n_o, int n_p, cr_stream stream,
+                             cr_weights* out);
+cr_status cr_weights_release(cr_weights w);
+
+/* cr_krige_correct and cr_correct_calibrate with prepared weights: always the Ozaki product
+ * (whatever CR_OPT_FP64_GEMM says), with the same results, bit for bit, as those calls with
+ * CR_GEMM_OZAKI on the W the handle was made from; n_o and n_p are the handle's.  Scratch,
+ * synchronisation and errors as in those calls. */
+cr_status cr_krige_correct_prepared(cr_weights w, const double* d_yo, const double* d_Y, int ldy,
+                                    int M, double* d_S, int lds, cr_stream stream);
+cr_status cr_correct_calibrate_prepared(cr_weights w, const double* d_yo, const double* d_Y,
+                                        int ldy, int M, const double* d_zhat, const double* d_v,
+                                        double u, double level, int negative, uint8_t* d_cin,
+                                        uint8_t* d_cout, int32_t* d_count, double* d_psi,
+                                        double* d_phi, cr_calib_info* out, cr_stream stream);
 
 /* Calibration (Section V-C Eq.8-9, Alg.2 steps 18-22): t = (zhat - u)/sqrt(v);
  * psi_j = min{t_i : S_ij >= u}, phi_j = max{t_i : S_ij <= u} in one pass over d_S

@@ -18,6 +18,9 @@ The functions mirror include/cr.h:
   krige(V, Xo, Xp, yo)                   cr_krige
   krige_correct(W, yo, Y, n_p, n_o)      cr_krige_correct
   correct_calibrate(W, yo, Y, ...)       cr_correct_calibrate (correction fused with calibration)
+  Weights(W)                             cr_weights_prepare / cr_weights_release
+  krige_correct_prepared(Wp, yo, Y)      cr_krige_correct_prepared
+  correct_calibrate_prepared(Wp, ...)    cr_correct_calibrate_prepared
   calibrate(S, zhat, v, u, level)        cr_calibrate (negative=True: cr_calibrate_negative)
   morton_order(xy)                       cr_morton_order (host only)
 The library is never replaced by a fallback: if libcr.so is missing or fails to load, every
@@ -113,6 +116,11 @@ _SIGNATURES = {
                                    _P]),
     "cr_calibrate_noalloc": (_I, [_P, _I, _I, _I, _P, _P, _D, _D, _P, _P, _P, _P, _P, ctypes.POINTER(CalibInfo),
                                   _P]),
+    "cr_weights_prepare": (_I, [_P, _I, _I, _I, _P, ctypes.POINTER(_P)]),
+    "cr_weights_release": (_I, [_P]),
+    "cr_krige_correct_prepared": (_I, [_P, _P, _P, _I, _I, _P, _I, _P]),
+    "cr_correct_calibrate_prepared": (_I, [_P, _P, _P, _I, _I, _P, _P, _D, _D, _I, _P, _P, _P, _P, _P,
+                                           ctypes.POINTER(CalibInfo), _P]),
 }
 
 
@@ -370,24 +378,17 @@ def krige_correct(W, yo, Y, n_p: int, n_o: int, out=None, stream=None):
     return out
 
 
-def correct_calibrate(W, yo, Y, n_p: int, n_o: int, zhat, v, u: float, level: float, counts: bool = True,
-                      extrema: bool = False, negative: bool = False, stream=None):
-    """cr_correct_calibrate: the correction S = M_p + W^T (y_o 1^T - M_o) fused with the
-    calibration (S is never formed); returns the dict of calibrate()."""
+def _calib_outputs(n_p: int, M: int, counts: bool, extrema: bool):
     import torch
-    W, ldw = as_colmajor(W)
-    Y, ldy = as_colmajor(Y)
-    M = Y.shape[1]
     cin = torch.empty(n_p, dtype=torch.uint8, device="cuda")
     cout = torch.empty(n_p, dtype=torch.uint8, device="cuda")
     cnt = torch.empty(n_p, dtype=torch.int32, device="cuda") if counts else None
     psi = torch.empty(M, dtype=torch.float64, device="cuda") if extrema else None
     phi = torch.empty(M, dtype=torch.float64, device="cuda") if extrema else None
-    info = CalibInfo()
-    _check(_lib.cr_correct_calibrate(_ptr(W), ldw, _ptr(yo.contiguous()), _ptr(Y), ldy, n_p, n_o, M,
-                                     _ptr(zhat.contiguous()), _ptr(v.contiguous()), u, level, 1 if negative else 0,
-                                     _ptr(cin), _ptr(cout), _ptr(cnt), _ptr(psi), _ptr(phi), ctypes.byref(info),
-                                     _stream(stream)))
+    return cin, cout, cnt, psi, phi, CalibInfo()
+
+
+def _calib_dict(cin, cout, cnt, psi, phi, info, counts: bool, extrema: bool):
     out = {"q_in": info.q_in, "q_out": info.q_out, "n_psi": info.n_psi, "n_phi": info.n_phi, "c_in": cin,
            "c_out": cout}
     if counts:
@@ -395,6 +396,71 @@ def correct_calibrate(W, yo, Y, n_p: int, n_o: int, zhat, v, u: float, level: fl
     if extrema:
         out["psi"], out["phi"] = psi, phi
     return out
+
+
+def correct_calibrate(W, yo, Y, n_p: int, n_o: int, zhat, v, u: float, level: float, counts: bool = True,
+                      extrema: bool = False, negative: bool = False, stream=None):
+    """cr_correct_calibrate: the correction S = M_p + W^T (y_o 1^T - M_o) fused with the
+    calibration (S is never formed); returns the dict of calibrate()."""
+    W, ldw = as_colmajor(W)
+    Y, ldy = as_colmajor(Y)
+    M = Y.shape[1]
+    cin, cout, cnt, psi, phi, info = _calib_outputs(n_p, M, counts, extrema)
+    _check(_lib.cr_correct_calibrate(_ptr(W), ldw, _ptr(yo.contiguous()), _ptr(Y), ldy, n_p, n_o, M,
+                                     _ptr(zhat.contiguous()), _ptr(v.contiguous()), u, level, 1 if negative else 0,
+                                     _ptr(cin), _ptr(cout), _ptr(cnt), _ptr(psi), _ptr(phi), ctypes.byref(info),
+                                     _stream(stream)))
+    return _calib_dict(cin, cout, cnt, psi, phi, info, counts, extrema)
+
+
+class Weights:
+    """cr_weights: kriging weights W (n_o x n_p) prepared for repeated Ozaki corrections."""
+
+    def __init__(self, W, stream=None):
+        load()
+        W, ldw = as_colmajor(W)
+        self.n_o, self.n_p = W.shape
+        h = _P()
+        _check(_lib.cr_weights_prepare(_ptr(W), ldw, self.n_o, self.n_p, _stream(stream), ctypes.byref(h)))
+        self.handle = h
+
+    def close(self):
+        if self.handle:
+            _check(_lib.cr_weights_release(self.handle))
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def krige_correct_prepared(Wp: Weights, yo, Y, out=None, stream=None):
+    """cr_krige_correct_prepared: the Ozaki correction with prepared weights; returns S."""
+    import torch
+    Y, ldy = as_colmajor(Y)
+    M = Y.shape[1]
+    if out is None:
+        out = colmajor_empty(Wp.n_p, M, torch.float64)
+    out, lds = as_colmajor(out)
+    _check(_lib.cr_krige_correct_prepared(Wp.handle, _ptr(yo.contiguous()), _ptr(Y), ldy, M, _ptr(out), lds,
+                                          _stream(stream)))
+    return out
+
+
+def correct_calibrate_prepared(Wp: Weights, yo, Y, zhat, v, u: float, level: float, counts: bool = True,
+                               extrema: bool = False, negative: bool = False, stream=None):
+    """cr_correct_calibrate_prepared: the Ozaki correction with prepared weights, then the
+    calibration; returns the dict of calibrate()."""
+    Y, ldy = as_colmajor(Y)
+    M = Y.shape[1]
+    cin, cout, cnt, psi, phi, info = _calib_outputs(Wp.n_p, M, counts, extrema)
+    _check(_lib.cr_correct_calibrate_prepared(Wp.handle, _ptr(yo.contiguous()), _ptr(Y), ldy, M,
+                                              _ptr(zhat.contiguous()), _ptr(v.contiguous()), u, level,
+                                              1 if negative else 0, _ptr(cin), _ptr(cout), _ptr(cnt), _ptr(psi),
+                                              _ptr(phi), ctypes.byref(info), _stream(stream)))
+    return _calib_dict(cin, cout, cnt, psi, phi, info, counts, extrema)
 
 
 def calibrate(S, zhat, v, u: float, level: float, counts: bool = True, extrema: bool = False, negative: bool = False,

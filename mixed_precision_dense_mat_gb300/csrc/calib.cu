@@ -17,6 +17,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <functional>
 #include <mutex>
 
 #include "calib.cuh"
@@ -618,6 +619,38 @@ cr_status correction_async(const double* d_W, int ldw, const double* d_yo, const
 
 }  // namespace cr
 
+// The Ozaki correction writes S (scratch from the library pool) through `correct`, then the
+// scan of cr_calibrate reads it.
+static cr_status correct_then_calibrate(const std::function<cr_status(double*)>& correct, int n_p, int M,
+                                        const double* d_zhat, const double* d_v, double u, double level, int negative,
+                                        uint8_t* d_cin, uint8_t* d_cout, int32_t* d_count, double* d_psi, double* d_phi,
+                                        cr_calib_info* out, cudaStream_t stream) {
+  double* S = nullptr;
+  CR_CUDA(scratch_alloc((void**)&S, (size_t)n_p * M * sizeof(double), stream));
+  cr_status st = correct(S);
+  if (st == CR_OK) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    st = ensure_scratch(n_p, M);
+    if (st == CR_OK)
+      st = calibrate_core(S, n_p, n_p, M, d_zhat, d_v, u, level, d_cin, d_cout, d_count, d_psi, d_phi, out, stream, g_sc,
+                          negative ? 1 : 0);
+  }
+  scratch_free(S, stream);
+  return st;
+}
+
+extern "C" cr_status cr_correct_calibrate_prepared(cr_weights w, const double* d_yo, const double* d_Y, int ldy, int M,
+                                                   const double* d_zhat, const double* d_v, double u, double level,
+                                                   int negative, uint8_t* d_cin, uint8_t* d_cout, int32_t* d_count,
+                                                   double* d_psi, double* d_phi, cr_calib_info* out, cr_stream stream) {
+  if (!w || !d_yo || !d_Y || !d_zhat || !d_v || !d_cin || !d_cout || M <= 0 || ldy < w->n_p + w->n_o ||
+      !(level > 0.0 && level < 1.0))
+    return fail(CR_ERR_ARG, "cr_correct_calibrate_prepared: argument");
+  return correct_then_calibrate(
+      [&](double* S) { return ozaki_correction_prepared(w, d_yo, d_Y, ldy, M, S, w->n_p, stream); }, w->n_p, M, d_zhat,
+      d_v, u, level, negative, d_cin, d_cout, d_count, d_psi, d_phi, out, stream);
+}
+
 extern "C" cr_status cr_correct_calibrate(const double* d_W, int ldw, const double* d_yo, const double* d_Y, int ldy,
                                           int n_p, int n_o, int M, const double* d_zhat, const double* d_v, double u,
                                           double level, int negative, uint8_t* d_cin, uint8_t* d_cout, int32_t* d_count,
@@ -625,21 +658,10 @@ extern "C" cr_status cr_correct_calibrate(const double* d_W, int ldw, const doub
   if (!d_W || !d_yo || !d_Y || !d_zhat || !d_v || !d_cin || !d_cout || n_p <= 0 || n_o <= 0 || M <= 0 || ldw < n_o ||
       ldy < n_p + n_o || !(level > 0.0 && level < 1.0))
     return fail(CR_ERR_ARG, "cr_correct_calibrate: argument");
-  if (option_fp64_gemm() == CR_GEMM_OZAKI) {
-    // the Ozaki product writes S (scratch from the library pool), then the calibration scan reads it
-    double* S = nullptr;
-    CR_CUDA(scratch_alloc((void**)&S, (size_t)n_p * M * sizeof(double), stream));
-    cr_status st = ozaki_correction(d_W, ldw, d_yo, d_Y, ldy, n_p, n_o, M, S, n_p, stream);
-    if (st == CR_OK) {
-      std::lock_guard<std::mutex> lk(g_mu);
-      st = ensure_scratch(n_p, M);
-      if (st == CR_OK)
-        st = calibrate_core(S, n_p, n_p, M, d_zhat, d_v, u, level, d_cin, d_cout, d_count, d_psi, d_phi, out, stream, g_sc,
-                            negative ? 1 : 0);
-    }
-    scratch_free(S, stream);
-    return st;
-  }
+  if (option_fp64_gemm() == CR_GEMM_OZAKI)
+    return correct_then_calibrate(
+        [&](double* S) { return ozaki_correction(d_W, ldw, d_yo, d_Y, ldy, n_p, n_o, M, S, n_p, stream); }, n_p, M, d_zhat,
+        d_v, u, level, negative, d_cin, d_cout, d_count, d_psi, d_phi, out, stream);
   std::lock_guard<std::mutex> lk(g_cc_mu);
   const size_t nrb = ((size_t)n_p + CT - 1) / CT;
   CR_TRY(grow(&g_cc.W, &g_cc.capW, (size_t)n_o * n_p));

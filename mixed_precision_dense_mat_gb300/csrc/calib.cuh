@@ -40,8 +40,19 @@ cr_status ozaki_gemm_tn(const double* A, int lda, const double* B, int ldb, int 
                         const double* Cin, int ldci, double* Cout, int ldco, int S, cudaStream_t stream);
 
 // The conditioning correction S = M_p + W^T (y_o 1^T - M_o) by the Ozaki product on the FP16
-// tensor cores (ozaki.cu); stream-ordered scratch, asynchronous.
+// tensor cores (ozaki.cu); stream-ordered scratch, asynchronous.  The _prepared form takes W's
+// slices from a cr_weights handle.
 cr_status ozaki_correction(const double* d_W, int ldw, const double* d_yo, const double* d_Y, int ldy, int n_p, int n_o,
                            int M, double* d_S, int lds, cudaStream_t stream);
+cr_status ozaki_correction_prepared(cr_weights w, const double* d_yo, const double* d_Y, int ldy, int M, double* d_S, int lds,
+                                    cudaStream_t stream);
 
 }  // namespace cr
+
+// Kriging weights prepared for the Ozaki correction (cr_weights_prepare): W's column exponents
+// and slices, with the geometry they were cut for.
+struct cr_weights_s {
+  int device = 0, n_o = 0, n_p = 0, slices = 0;
+  int* Ea = nullptr;
+  __half* As = nullptr;
+};

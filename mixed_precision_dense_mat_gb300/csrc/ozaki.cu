@@ -44,6 +44,7 @@ namespace {
 // chunks per GEMM call at most
 constexpr int OZ_BITS = 6, OZ_MIN_SLICES = 2, OZ_MAX_SLICES = 10, OZ_KC_MAX = 4096, OZ_GROUP = 32;
 constexpr unsigned long long OZ_MASK = (1ull << OZ_BITS) - 1ull;
+constexpr int OZ_CORR_SLICES = 8;   // the conditioning correction's slices (48 bits)
 
 // Exponent marking a column with an infinite or NaN entry: its slices are zero and every output
 // it touches is NaN (as in an FP64 product, where the entry reaches all of them).
@@ -206,119 +207,177 @@ unsigned grid_for(size_t total) {
 
 }  // namespace
 
+namespace {
+
+// Geometry of one Ozaki product's inner dimension: c = ceil(K / 4096) chunks of kc rows
+// (K / c rounded up to 128, so at most 4096) per slice, K' = c kc padded rows, S slices.
+struct OzGeom {
+  int K, S, cpk, kc, kpad;
+  size_t ldk;   // S K': the halves of one column's slices
+};
+
+OzGeom oz_geom(int K, int S) {
+  OzGeom g;
+  g.K = K;
+  g.S = S;
+  g.cpk = (K + OZ_KC_MAX - 1) / OZ_KC_MAX;
+  g.kc = ((K + g.cpk - 1) / g.cpk + 127) / 128 * 128;
+  g.kpad = g.cpk * g.kc;
+  g.ldk = (size_t)S * g.kpad;
+  return g;
+}
+
+void oz_slice_launch(const OzGeom& g, const double* X, int ld, int cols, const int* E, int rev, __half* out,
+                     cudaStream_t stream) {
+  const dim3 grid = grid2d(g.kpad, cols);
+  const int K = g.K, kpad = g.kpad;
+  switch (g.S) {
+    case 2: k_oz_slice<2><<<grid, 256, 0, stream>>>(X, ld, K, kpad, cols, E, rev, out); break;
+    case 3: k_oz_slice<3><<<grid, 256, 0, stream>>>(X, ld, K, kpad, cols, E, rev, out); break;
+    case 4: k_oz_slice<4><<<grid, 256, 0, stream>>>(X, ld, K, kpad, cols, E, rev, out); break;
+    case 5: k_oz_slice<5><<<grid, 256, 0, stream>>>(X, ld, K, kpad, cols, E, rev, out); break;
+    case 6: k_oz_slice<6><<<grid, 256, 0, stream>>>(X, ld, K, kpad, cols, E, rev, out); break;
+    case 7: k_oz_slice<7><<<grid, 256, 0, stream>>>(X, ld, K, kpad, cols, E, rev, out); break;
+    case 8: k_oz_slice<8><<<grid, 256, 0, stream>>>(X, ld, K, kpad, cols, E, rev, out); break;
+    case 9: k_oz_slice<9><<<grid, 256, 0, stream>>>(X, ld, K, kpad, cols, E, rev, out); break;
+    default: k_oz_slice<10><<<grid, 256, 0, stream>>>(X, ld, K, kpad, cols, E, rev, out); break;
+  }
+  count_launch();
+}
+
+// The left operand's column exponents (Ea, m) and slices (As, ldk x m halves, in order).
+cr_status oz_slice_left(const OzGeom& g, const double* A, int lda, int m, int* Ea, __half* As, cudaStream_t stream) {
+  TimedScope ts("k_oz_slice", stream);
+  k_oz_colexp<<<(unsigned)m, 256, 0, stream>>>(A, lda, g.K, Ea);
+  count_launch();
+  oz_slice_launch(g, A, lda, m, Ea, 0, As, stream);
+  if (cudaError_t e = cudaGetLastError()) return fail(CR_ERR_CUDA, cudaGetErrorName(e));
+  return CR_OK;
+}
+
+// Cout = Cin + alpha A^T B with A already sliced (Ea, As for m columns, geometry g): B is sliced
+// per block of output columns, the blocks as wide as keeps one level's chunk products within
+// 2 GiB; scratch from the library pool (the slices of a block, its chunk products, at most 32
+// m nbc FP32, and the accumulator, m nbc double-float pairs).
+cr_status oz_product(const OzGeom& g, const int* Ea, const __half* As, int m_, const double* B, int ldb, int n_,
+                     double alpha, const double* Cin, int ldci, double* Cout, int ldco, cudaStream_t stream) {
+  const size_t m = (size_t)m_;
+  std::lock_guard<std::mutex> lk(g_cublas_mu);
+  cublasHandle_t h = nullptr;
+  CR_TRY(cublas_for(stream, &h));
+  const int S = g.S, cpk = g.cpk, kc = g.kc, kpad = g.kpad;
+  const size_t ldk = g.ldk;
+  const int group = std::min(OZ_GROUP, S * cpk);                     // chunks per GEMM call
+  const size_t budget = (size_t)1 << 31;
+  const int nbc = (int)std::max<size_t>(1, std::min<size_t>((size_t)n_, budget / (m * group * sizeof(float))));
+  int* Eb = nullptr;
+  __half* Bs = nullptr;
+  float* P = nullptr;
+  float2* C = nullptr;
+  auto alloc = [&](void** p, size_t bytes) { return scratch_alloc(p, bytes, stream); };
+  cudaError_t e = cudaSuccess;
+  if ((e = alloc((void**)&Eb, nbc * sizeof(int))) != cudaSuccess ||
+      (e = alloc((void**)&Bs, ldk * nbc * sizeof(__half))) != cudaSuccess ||
+      (e = alloc((void**)&P, (size_t)group * m * nbc * sizeof(float))) != cudaSuccess ||
+      (e = alloc((void**)&C, m * nbc * sizeof(float2))) != cudaSuccess) {
+    for (void* p : {(void*)Eb, (void*)Bs, (void*)P, (void*)C}) scratch_free(p, stream);
+    return fail(CR_ERR_NOMEM, std::string("Ozaki product: scratch: ") + cudaGetErrorName(e));
+  }
+  cr_status st = CR_OK;
+  const float one = 1.0f, zero = 0.0f;
+  for (int j0 = 0; j0 < n_ && st == CR_OK; j0 += nbc) {
+    const int w = std::min(nbc, n_ - j0);
+    const double* Bj = B + (size_t)j0 * ldb;
+    {
+      TimedScope ts("k_oz_slice", stream);   // exponents and slices of this block of B
+      k_oz_colexp<<<(unsigned)w, 256, 0, stream>>>(Bj, ldb, g.K, Eb);
+      count_launch();
+      oz_slice_launch(g, Bj, ldb, w, Eb, 1, Bs, stream);
+    }
+    if ((e = cudaGetLastError()) != cudaSuccess) { st = fail(CR_ERR_CUDA, cudaGetErrorName(e)); break; }
+    const dim3 ga = grid2d(m_, w);
+    const double* Cin_j = Cin ? Cin + (size_t)j0 * ldci : nullptr;
+    double* Cout_j = Cout + (size_t)j0 * ldco;
+    bool first = true;
+    // least significant level first
+    for (int lev = S + 1; lev >= 2 && st == CR_OK; --lev) {
+      // rows of the concatenated product: A slots 0 .. lev-2, B slots S-lev+1 .. S-1
+      const int nchunk = (lev - 1) * cpk;
+      const __half* a0 = As;
+      const __half* b0 = Bs + (size_t)(S - lev + 1) * kpad;
+      for (int g0 = 0; g0 < nchunk; g0 += group) {
+        const int cnt = std::min(group, nchunk - g0);
+        // P_c = A_lev[chunk g0 + c]^T B_lev[chunk g0 + c], c < cnt (m x w each, exact)
+        cublasStatus_t cs;
+        {
+          TimedScope tg("oz_gemm", stream);
+          cs = cublasGemmStridedBatchedEx(h, CUBLAS_OP_T, CUBLAS_OP_N, m_, w, kc, &one, a0 + (size_t)g0 * kc, CUDA_R_16F,
+                                          (int)ldk, kc, b0 + (size_t)g0 * kc, CUDA_R_16F, (int)ldk, kc, &zero, P,
+                                          CUDA_R_32F, m_, (long long)(m * w), cnt, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
+        }
+        if (cs != CUBLAS_STATUS_SUCCESS) {
+          st = fail(CR_ERR_CUDA, "Ozaki product: cublasGemmStridedBatchedEx failed (" + std::to_string((int)cs) + ")");
+          break;
+        }
+        const bool last = lev == 2 && g0 + cnt >= nchunk;
+        TimedScope ts("k_oz_accum", stream);
+        k_oz_accum<<<ga, 256, 0, stream>>>(P, cnt, m_, w, Ea, Eb, OZ_BITS * lev, C, first ? 1 : 0, last ? 1 : 0, alpha,
+                                           Cin_j, ldci, Cout_j, ldco);
+        count_launch();
+        first = false;
+      }
+    }
+  }
+  if (st == CR_OK && (e = cudaGetLastError()) != cudaSuccess) st = fail(CR_ERR_CUDA, cudaGetErrorName(e));
+  for (void* p : {(void*)Eb, (void*)Bs, (void*)P, (void*)C}) scratch_free(p, stream);
+  return st;
+}
+
+// R = y_o 1^T - M_o into pool scratch (n_o x M, ld n_o); *R_out NULL on failure.
+cr_status oz_residual(const double* d_yo, const double* d_Y, int ldy, int n_p, int n_o, int M, double** R_out,
+                      cudaStream_t stream) {
+  *R_out = nullptr;
+  double* R = nullptr;
+  CR_CUDA(scratch_alloc((void**)&R, (size_t)n_o * M * sizeof(double), stream));
+  {
+    TimedScope ts("k_oz_slice", stream);
+    k_oz_resid<<<grid_for((size_t)n_o * M), 256, 0, stream>>>(d_yo, d_Y, ldy, n_p, n_o, M, R);
+    count_launch();
+  }
+  if (cudaError_t e = cudaGetLastError()) {
+    scratch_free(R, stream);
+    return fail(CR_ERR_CUDA, cudaGetErrorName(e));
+  }
+  *R_out = R;
+  return CR_OK;
+}
+
+}  // namespace
+
 // Cout = Cin + alpha A^T B by the Ozaki product with S slices of 6 bits per operand column
 // (A: K x m, ld lda; B: K x n, ld ldb; Cin, Cout: m x n, ld ldci / ldco; Cin NULL for zero;
 // Cout may equal Cin with the same ld, and may overlap A or B, which are sliced before Cout is
-// written).  The kept products are those with s + t <= S + 1, one GEMM per level.  The inner
-// dimension is cut into c = ceil(K / 4096) chunks of kc rows (K / c rounded up to 128, so at
-// most 4096), K' = c kc; A's slices are made once, B's per block of output columns, the blocks
-// as wide as keeps the chunk products of one level within 2 GiB.  Scratch from the library
-// pool: the slices (S K' (m + nbc) FP16), the chunk products (at most 32 m nbc FP32) and the
-// accumulator (m nbc double-float pairs), nbc the block width.
+// written).  The kept products are those with s + t <= S + 1, one GEMM per level.  A's slices
+// (S K' m FP16, pool scratch) are made once, B's per block of output columns (oz_product).
 cr_status ozaki_gemm_tn(const double* A, int lda, const double* B, int ldb, int K, int m_, int n_, double alpha,
                         const double* Cin, int ldci, double* Cout, int ldco, int S, cudaStream_t stream) {
   if (S < OZ_MIN_SLICES || S > OZ_MAX_SLICES) return fail(CR_ERR_ARG, "Ozaki product: slice count");
   if (m_ <= 0 || n_ <= 0) return CR_OK;
-  const size_t m = (size_t)m_;
   if (K <= 0) {
     k_oz_copy<<<grid2d(m_, n_), 256, 0, stream>>>(Cin, ldci, m_, n_, Cout, ldco);
     CR_CHECK_LAUNCH("k_oz_copy");
     return CR_OK;
   }
-  std::lock_guard<std::mutex> lk(g_cublas_mu);
-  cublasHandle_t h = nullptr;
-  CR_TRY(cublas_for(stream, &h));
-  const int cpk = (K + OZ_KC_MAX - 1) / OZ_KC_MAX;                   // chunks per slice
-  const int kc = ((K + cpk - 1) / cpk + 127) / 128 * 128, kpad = cpk * kc;
-  const size_t ldk = (size_t)S * kpad;
-  const int group = std::min(OZ_GROUP, S * cpk);                     // chunks per GEMM call
-  const size_t budget = (size_t)1 << 31;
-  const int nbc = (int)std::max<size_t>(1, std::min<size_t>((size_t)n_, budget / (m * group * sizeof(float))));
-  int *Ea = nullptr, *Eb = nullptr;
-  __half *As = nullptr, *Bs = nullptr;
-  float* P = nullptr;
-  float2* C = nullptr;
-  auto alloc = [&](void** p, size_t bytes) { return scratch_alloc(p, bytes, stream); };
-  cudaError_t e = cudaSuccess;
-  if ((e = alloc((void**)&Ea, m * sizeof(int))) != cudaSuccess || (e = alloc((void**)&Eb, nbc * sizeof(int))) != cudaSuccess ||
-      (e = alloc((void**)&As, ldk * m * sizeof(__half))) != cudaSuccess ||
-      (e = alloc((void**)&Bs, ldk * nbc * sizeof(__half))) != cudaSuccess ||
-      (e = alloc((void**)&P, (size_t)group * m * nbc * sizeof(float))) != cudaSuccess ||
-      (e = alloc((void**)&C, m * nbc * sizeof(float2))) != cudaSuccess) {
-    for (void* p : {(void*)Ea, (void*)Eb, (void*)As, (void*)Bs, (void*)P, (void*)C}) scratch_free(p, stream);
-    return fail(CR_ERR_NOMEM, std::string("Ozaki product: scratch: ") + cudaGetErrorName(e));
-  }
-  auto slice = [&](const double* X, int ld, int cols, const int* E, int rev, __half* out) {
-    const dim3 g = grid2d(kpad, cols);
-    switch (S) {
-      case 2: k_oz_slice<2><<<g, 256, 0, stream>>>(X, ld, K, kpad, cols, E, rev, out); break;
-      case 3: k_oz_slice<3><<<g, 256, 0, stream>>>(X, ld, K, kpad, cols, E, rev, out); break;
-      case 4: k_oz_slice<4><<<g, 256, 0, stream>>>(X, ld, K, kpad, cols, E, rev, out); break;
-      case 5: k_oz_slice<5><<<g, 256, 0, stream>>>(X, ld, K, kpad, cols, E, rev, out); break;
-      case 6: k_oz_slice<6><<<g, 256, 0, stream>>>(X, ld, K, kpad, cols, E, rev, out); break;
-      case 7: k_oz_slice<7><<<g, 256, 0, stream>>>(X, ld, K, kpad, cols, E, rev, out); break;
-      case 8: k_oz_slice<8><<<g, 256, 0, stream>>>(X, ld, K, kpad, cols, E, rev, out); break;
-      case 9: k_oz_slice<9><<<g, 256, 0, stream>>>(X, ld, K, kpad, cols, E, rev, out); break;
-      default: k_oz_slice<10><<<g, 256, 0, stream>>>(X, ld, K, kpad, cols, E, rev, out); break;
-    }
-    count_launch();
-  };
-  cr_status st = CR_OK;
-  do {
-    {
-      TimedScope ts("k_oz_slice", stream);   // exponents and slices of A
-      k_oz_colexp<<<(unsigned)m, 256, 0, stream>>>(A, lda, K, Ea);
-      count_launch();
-      slice(A, lda, m_, Ea, 0, As);
-    }
-    const float one = 1.0f, zero = 0.0f;
-    for (int j0 = 0; j0 < n_ && st == CR_OK; j0 += nbc) {
-      const int w = std::min(nbc, n_ - j0);
-      const double* Bj = B + (size_t)j0 * ldb;
-      {
-        TimedScope ts("k_oz_slice", stream);   // exponents and slices of this block of B
-        k_oz_colexp<<<(unsigned)w, 256, 0, stream>>>(Bj, ldb, K, Eb);
-        count_launch();
-        slice(Bj, ldb, w, Eb, 1, Bs);
-      }
-      if ((e = cudaGetLastError()) != cudaSuccess) { st = fail(CR_ERR_CUDA, cudaGetErrorName(e)); break; }
-      const dim3 ga = grid2d(m_, w);
-      const double* Cin_j = Cin ? Cin + (size_t)j0 * ldci : nullptr;
-      double* Cout_j = Cout + (size_t)j0 * ldco;
-      bool first = true;
-      // least significant level first
-      for (int lev = S + 1; lev >= 2 && st == CR_OK; --lev) {
-        // rows of the concatenated product: A slots 0 .. lev-2, B slots S-lev+1 .. S-1
-        const int nchunk = (lev - 1) * cpk;
-        const __half* a0 = As;
-        const __half* b0 = Bs + (size_t)(S - lev + 1) * kpad;
-        for (int g0 = 0; g0 < nchunk; g0 += group) {
-          const int cnt = std::min(group, nchunk - g0);
-          // P_c = A_lev[chunk g0 + c]^T B_lev[chunk g0 + c], c < cnt (m x w each, exact)
-          cublasStatus_t cs;
-          {
-            TimedScope tg("oz_gemm", stream);
-            cs = cublasGemmStridedBatchedEx(h, CUBLAS_OP_T, CUBLAS_OP_N, m_, w, kc, &one, a0 + (size_t)g0 * kc, CUDA_R_16F,
-                                            (int)ldk, kc, b0 + (size_t)g0 * kc, CUDA_R_16F, (int)ldk, kc, &zero, P,
-                                            CUDA_R_32F, m_, (long long)(m * w), cnt, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
-          }
-          if (cs != CUBLAS_STATUS_SUCCESS) {
-            st = fail(CR_ERR_CUDA, "Ozaki product: cublasGemmStridedBatchedEx failed (" + std::to_string((int)cs) + ")");
-            break;
-          }
-          const bool last = lev == 2 && g0 + cnt >= nchunk;
-          TimedScope ts("k_oz_accum", stream);
-          k_oz_accum<<<ga, 256, 0, stream>>>(P, cnt, m_, w, Ea, Eb, OZ_BITS * lev, C, first ? 1 : 0, last ? 1 : 0, alpha,
-                                             Cin_j, ldci, Cout_j, ldco);
-          count_launch();
-          first = false;
-        }
-      }
-    }
-    if (st != CR_OK) break;
-    if ((e = cudaGetLastError()) != cudaSuccess) st = fail(CR_ERR_CUDA, cudaGetErrorName(e));
-  } while (false);
-  for (void* p : {(void*)Ea, (void*)Eb, (void*)As, (void*)Bs, (void*)P, (void*)C}) scratch_free(p, stream);
+  const OzGeom g = oz_geom(K, S);
+  int* Ea = nullptr;
+  __half* As = nullptr;
+  cudaError_t e = scratch_alloc((void**)&Ea, (size_t)m_ * sizeof(int), stream);
+  if (e == cudaSuccess) e = scratch_alloc((void**)&As, g.ldk * m_ * sizeof(__half), stream);
+  cr_status st = e == cudaSuccess ? CR_OK : fail(CR_ERR_NOMEM, std::string("Ozaki product: scratch: ") + cudaGetErrorName(e));
+  if (st == CR_OK) st = oz_slice_left(g, A, lda, m_, Ea, As, stream);
+  if (st == CR_OK) st = oz_product(g, Ea, As, m_, B, ldb, n_, alpha, Cin, ldci, Cout, ldco, stream);
+  scratch_free(Ea, stream);
+  scratch_free(As, stream);
   return st;
 }
 
@@ -328,17 +387,65 @@ cr_status ozaki_gemm_tn(const double* A, int lda, const double* B, int ldb, int 
 cr_status ozaki_correction(const double* d_W, int ldw, const double* d_yo, const double* d_Y, int ldy, int n_p, int n_o,
                            int M, double* d_S, int lds, cudaStream_t stream) {
   double* R = nullptr;
-  CR_CUDA(scratch_alloc((void**)&R, (size_t)n_o * M * sizeof(double), stream));
-  {
-    TimedScope ts("k_oz_slice", stream);
-    k_oz_resid<<<grid_for((size_t)n_o * M), 256, 0, stream>>>(d_yo, d_Y, ldy, n_p, n_o, M, R);
-    count_launch();
-  }
-  cr_status st = CR_OK;
-  if (cudaError_t e = cudaGetLastError()) st = fail(CR_ERR_CUDA, cudaGetErrorName(e));
-  if (st == CR_OK) st = ozaki_gemm_tn(d_W, ldw, R, n_o, n_o, n_p, M, 1.0, d_Y, ldy, d_S, lds, 8, stream);
+  CR_TRY(oz_residual(d_yo, d_Y, ldy, n_p, n_o, M, &R, stream));
+  const cr_status st = ozaki_gemm_tn(d_W, ldw, R, n_o, n_o, n_p, M, 1.0, d_Y, ldy, d_S, lds, OZ_CORR_SLICES, stream);
+  scratch_free(R, stream);
+  return st;
+}
+
+// The correction with W's slices prepared by cr_weights_prepare (same arithmetic as
+// ozaki_correction on the W the handle was made from).
+cr_status ozaki_correction_prepared(cr_weights w, const double* d_yo, const double* d_Y, int ldy, int M, double* d_S, int lds,
+                                    cudaStream_t stream) {
+  CR_CUDA(cudaSetDevice(w->device));
+  double* R = nullptr;
+  CR_TRY(oz_residual(d_yo, d_Y, ldy, w->n_p, w->n_o, M, &R, stream));
+  const OzGeom g = oz_geom(w->n_o, w->slices);
+  const cr_status st = oz_product(g, w->Ea, w->As, w->n_p, R, w->n_o, M, 1.0, d_Y, ldy, d_S, lds, stream);
   scratch_free(R, stream);
   return st;
 }
 
 }  // namespace cr
+
+using namespace cr;
+
+extern "C" cr_status cr_weights_prepare(const double* d_W, int ldw, int n_o, int n_p, cr_stream stream, cr_weights* out) {
+  if (!out) return fail(CR_ERR_ARG, "cr_weights_prepare: NULL output");
+  *out = nullptr;
+  if (!d_W || n_o <= 0 || n_p <= 0 || ldw < n_o) return fail(CR_ERR_ARG, "cr_weights_prepare: argument");
+  int dev = 0;
+  CR_CUDA(cudaGetDevice(&dev));
+  cr_weights w = new cr_weights_s();
+  w->device = dev;
+  w->n_o = n_o;
+  w->n_p = n_p;
+  w->slices = OZ_CORR_SLICES;
+  const OzGeom g = oz_geom(n_o, w->slices);
+  cudaError_t e = cudaMalloc(&w->Ea, (size_t)n_p * sizeof(int));
+  if (e == cudaSuccess) e = cudaMalloc(&w->As, g.ldk * n_p * sizeof(__half));
+  cr_status st = e == cudaSuccess ? CR_OK : cuda_fail(e, "cr_weights_prepare: slices");
+  if (st == CR_OK) st = oz_slice_left(g, d_W, ldw, n_p, w->Ea, w->As, stream);
+  if (st != CR_OK) {
+    cr_weights_release(w);
+    return st;
+  }
+  *out = w;
+  return CR_OK;
+}
+
+extern "C" cr_status cr_weights_release(cr_weights w) {
+  if (!w) return CR_OK;
+  cudaSetDevice(w->device);
+  if (w->Ea) cudaFree(w->Ea);
+  if (w->As) cudaFree(w->As);
+  delete w;
+  return CR_OK;
+}
+
+extern "C" cr_status cr_krige_correct_prepared(cr_weights w, const double* d_yo, const double* d_Y, int ldy, int M,
+                                               double* d_S, int lds, cr_stream stream) {
+  if (!w || !d_yo || !d_Y || !d_S || M <= 0 || ldy < w->n_p + w->n_o || lds < w->n_p)
+    return fail(CR_ERR_ARG, "cr_krige_correct_prepared: argument");
+  return ozaki_correction_prepared(w, d_yo, d_Y, ldy, M, d_S, lds, stream);
+}

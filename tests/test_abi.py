@@ -47,6 +47,13 @@ def test_argument_errors_without_gpu(lib):
     assert cr._lib.cr_calibrate(None, 1, 1, 1, None, None, 0.0, 0.9, None, None, None, None, None, None, None) == 1
     assert cr._lib.cr_krige_correct(None, 1, None, None, 1, 1, 1, 1, None, 1, None) == 1
     assert cr._lib.cr_tilemat_destroy(None) == 0
+    w = ctypes.c_void_p(1)
+    assert cr._lib.cr_weights_prepare(None, 10, 10, 10, None, ctypes.byref(w)) == 1 and w.value is None
+    assert cr._lib.cr_weights_prepare(None, 10, 10, 10, None, None) == 1
+    assert cr._lib.cr_weights_release(None) == 0
+    assert cr._lib.cr_krige_correct_prepared(None, None, None, 1, 1, None, 1, None) == 1
+    assert cr._lib.cr_correct_calibrate_prepared(None, None, None, 1, 1, None, None, 0.0, 0.9, 0, None, None, None,
+                                                 None, None, None, None) == 1
 
 
 def test_header_declares_documented_path():

@@ -175,6 +175,38 @@ def test_ozaki_nonfinite_operands_give_nan(lib):
     assert np.all(np.abs(S[~bad] - So[~bad]) <= b[~bad])
 
 
+@pytest.mark.parametrize("negative", [False, True])
+def test_prepared_weights_bit_exact(lib, negative):
+    """cr_weights_prepare then cr_krige_correct_prepared / cr_correct_calibrate_prepared give
+    the bits of cr_krige_correct / cr_correct_calibrate with CR_GEMM_OZAKI on the same W, over
+    several simulation batches, with W overwritten after the handle was made (the handle does
+    not read W again) and whatever CR_OPT_FP64_GEMM says."""
+    rng = np.random.default_rng(23)
+    n_p, n_o, u, level = 700, 2300, 0.3, 0.9
+    W = rng.standard_normal((n_o, n_p)) * 0.05
+    y = rng.standard_normal(n_o)
+    z = rng.standard_normal(n_p) * 0.5
+    v = rng.uniform(0.3, 2.0, n_p)
+    Wd, yd, zd, vd = colmajor(W), dev(y), dev(z), dev(v)
+    Wp = lib.Weights(Wd)
+    torch.cuda.synchronize()
+    Wkeep = Wd.clone()
+    Wd.fill_(7.0)
+    for batch, M in enumerate((64, 129)):
+        Y = colmajor(np.random.default_rng(100 + batch).standard_normal((n_p + n_o, M)))
+        with gemm_mode(lib, lib.CR_GEMM_OZAKI):
+            S = lib.krige_correct(Wkeep, yd, Y, n_p, n_o).cpu().numpy()
+            a = lib.correct_calibrate(Wkeep, yd, Y, n_p, n_o, zd, vd, u, level, extrema=True, negative=negative)
+        with gemm_mode(lib, lib.CR_GEMM_DF):
+            Sp = lib.krige_correct_prepared(Wp, yd, Y).cpu().numpy()
+            b = lib.correct_calibrate_prepared(Wp, yd, Y, zd, vd, u, level, extrema=True, negative=negative)
+        np.testing.assert_array_equal(S, Sp)
+        for k in ("psi", "phi", "count", "c_in", "c_out"):
+            np.testing.assert_array_equal(a[k].cpu().numpy(), b[k].cpu().numpy(), err_msg=k)
+        assert (a["q_in"], a["q_out"]) == (b["q_in"], b["q_out"])
+    Wp.close()
+
+
 def test_pooled_scratch_reused_and_trimmed(lib):
     """The correction's scratch comes from the library pool: repeated calls, and a call after
     cr_workspace_trim has returned the pool's memory, give the same bits."""
