@@ -263,13 +263,15 @@ def _krige_case(n_o, m, seed, nu=1.0, beta=0.1, tau2=0.01):
     return xy, n_p, X, y, V
 
 
-@pytest.mark.parametrize("n_o,m,nb", [(1024, 32, 128), (1000, 24, 128), (4096, 64, 512), (2600, 40, 512)])
+@pytest.mark.parametrize("n_o,m,nb", [(1024, 32, 128), (1000, 24, 128), (4096, 64, 512), (2600, 40, 512),
+                                      (100, 8, 128)])
 def test_ozaki_kriging_matches_oracle(lib, n_o, m, nb):
     """cr_krige with its many-right-hand-side triangular solves as Ozaki products (Section V-A
     Eq.5-6; Alg.2 steps 2-6) against the oracle, with the FP64 path's tolerance: W and z_hat
     within max(1e-10, 20 x the distance between two FP64 orderings of the same solves) in
     relative Frobenius norm, v within 1e-9, and X_o^T W = X_p^T.  Ragged cases: n_o = 1000 and
-    2600 leave a partial last tile row."""
+    2600 leave a partial last tile row; n_o = 100 is a single partial tile (no off-diagonal
+    update, only the diagonal steps)."""
     xy, n_p, X, y, V = _krige_case(n_o, m, 5)
     G = lib.TileMat(len(xy), nb)
     lib.cov_build(G, dev(xy), "matern", 1.0, 0.1, 1.0, nugget=0.0, n_pred=n_p, tau2=0.01)
