@@ -19,9 +19,10 @@
 //  - the products with s + t <= S + 1 are kept (36 of 64 for S = 8): the rest, and the
 //    truncations, are below k 8.95 2^-48 2^(Ea_i + Eb_j) per output for S = 8 (derived in the
 //    tests);
-//  - each level's chunk sums, added in 32-bit integers (exact), are scaled by
-//    2^(Ea_i + Eb_j - 6 L) (exact) and added to a double-float accumulator, the least
-//    significant level first; the last addition writes Cout = Cin + alpha C in FP64;
+//  - each level's chunk sums, added in 32-bit integers (exact), are scaled by 2^-6L (exact)
+//    and added to a double-float accumulator held in units of 2^(Ea_i + Eb_j), the least
+//    significant level first; the last addition writes Cout = Cin + alpha 2^(Ea_i + Eb_j) C in
+//    FP64 (so the product's range is FP64's);
 //  - a column holding an infinity or a NaN makes every output it touches NaN.
 // The slice GEMMs are plain FP16 x FP16 -> FP32 library GEMMs (cuBLAS, strided-batched over the
 // K chunks); slicing, exact accumulation and the final sum are this file's kernels.
@@ -119,24 +120,22 @@ __global__ void __launch_bounds__(256) k_oz_resid(const double* __restrict__ yo,
   }
 }
 
-// 2^ex as an FP32 factor when it is a normal number (the multiplication is then exact unless
-// the product underflows); outside that range ldexpf.
-__device__ __forceinline__ float oz_scale(float x, int ex) {
-  return (ex >= -126 && ex <= 127) ? x * __int_as_float((ex + 127) << 23) : ldexpf(x, ex);
-}
-
 // One level's contribution for `nb` chunk products P_b (m x n FP32 exact integers below 2^24):
 // v = sum_b P_b(i, j), exact in 32-bit integers (nb <= 32), split exactly into two floats,
-// scaled by 2^(Ea_i + Eb_j - shift) and added to the double-float C (C = the term when
-// `first`).  With `last`, Cout = Cin + alpha C in FP64 is written instead of C (Cin = NULL:
-// zero); Cout may be Cin (each entry is read, then written, by one thread).
+// scaled by 2^-shift (shift = 6 L <= 66: an exact normal FP32 factor) and added to the
+// double-float C (C = the term when `first`).  C holds the product in units of
+// 2^(Ea_i + Eb_j), so its range is FP64's, not FP32's.  With `last`, Cout = Cin +
+// alpha 2^(Ea_i + Eb_j) C in FP64 is written instead of C (Cin = NULL: zero; hi + lo of a
+// double-float value is exact in FP64, the power of two exact unless the result is subnormal);
+// Cout may be Cin (each entry is read, then written, by one thread).
 __global__ void __launch_bounds__(256) k_oz_accum(const float* __restrict__ P, int nb, int m, int n,
                                                   const int* __restrict__ Ea, const int* __restrict__ Eb, int shift,
                                                   float2* __restrict__ C, int first, int last, double alpha,
                                                   const double* Cin, int ldci, double* Cout, int ldco) {
   const size_t mn = (size_t)m * n;
+  const float lev_scale = __int_as_float((127 - shift) << 23);   // 2^-shift
   for (int j = blockIdx.y; j < n; j += gridDim.y) {
-    const int ej = Eb[j] == OZ_NONFINITE ? 0 : Eb[j] - shift;
+    const int eb = Eb[j];
     for (int i = blockIdx.x * 256 + threadIdx.x; i < m; i += gridDim.x * 256) {
       const size_t e = (size_t)j * m + i;
       const float* p = P + e;
@@ -146,9 +145,8 @@ __global__ void __launch_bounds__(256) k_oz_accum(const float* __restrict__ P, i
       const float h = (float)v;                   // nearest FP32 of v (|v| < 2^29)
       const float l = (float)(v - (int)h);        // the rest, below 2^5: exact
       const int ea = Ea[i];
-      const bool nonfinite = ea == OZ_NONFINITE || Eb[j] == OZ_NONFINITE;
-      const int ex = nonfinite ? 0 : ea + ej;
-      df acc = {oz_scale(h, ex), oz_scale(l, ex)};
+      const bool nonfinite = ea == OZ_NONFINITE || eb == OZ_NONFINITE;
+      df acc = {h * lev_scale, l * lev_scale};
       if (nonfinite) acc = {__int_as_float(0x7fc00000), 0.0f};   // NaN
       if (!first) {
         const float2 c = C[e];
@@ -156,7 +154,8 @@ __global__ void __launch_bounds__(256) k_oz_accum(const float* __restrict__ P, i
       }
       if (last) {
         const double base = Cin ? Cin[(size_t)j * ldci + i] : 0.0;
-        Cout[(size_t)j * ldco + i] = base + alpha * ((double)acc.hi + (double)acc.lo);
+        const double prod = nonfinite ? (double)acc.hi : ldexp((double)acc.hi + (double)acc.lo, ea + eb);
+        Cout[(size_t)j * ldco + i] = base + alpha * prod;
       } else {
         C[e] = make_float2(acc.hi, acc.lo);
       }

@@ -103,6 +103,24 @@ def test_ozaki_correction_degenerate_sizes(lib, n_p, n_o, M):
     assert np.all(np.abs(S - So) <= _bound(W, R, So, n_o))
 
 
+@pytest.mark.parametrize("sw,sy", [(1e30, 1e20), (1e-30, 1e-20), (1e150, 1e-160)])
+def test_ozaki_correction_beyond_fp32_range(lib, sw, sy):
+    """Operands whose products lie far outside FP32's range (about 1e50, 1e-50, 1e-10 from
+    1e150 x 1e-160): the accumulation runs in units of each output's column exponents, so the
+    result keeps FP64's range and the bound above."""
+    rng = np.random.default_rng(3)
+    n_p, n_o, M = 90, 1300, 33
+    W = rng.standard_normal((n_o, n_p)) * sw
+    y = rng.standard_normal(n_o) * sy
+    Y = rng.standard_normal((n_p + n_o, M)) * sy
+    with gemm_mode(lib, lib.CR_GEMM_OZAKI):
+        S = lib.krige_correct(colmajor(W), dev(y), colmajor(Y), n_p, n_o).cpu().numpy()
+    So = oracle.conditional_correction(W, y, Y[:n_p], Y[n_p:])
+    R = y[:, None] - Y[n_p:]
+    assert np.all(np.isfinite(S))
+    assert np.all(np.abs(S - So) <= _bound(W, R, So, n_o))
+
+
 def test_ozaki_slices_exact_on_integers(lib):
     """Entries that are small integers times powers of two are represented exactly by their
     slices and every slice product is exact, so the product equals the exact integer result."""
